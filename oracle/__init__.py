@@ -1,0 +1,215 @@
+"""CPU oracle for the Float8 linear layer with dynamic per-tensor scaling.
+
+TEST INFRASTRUCTURE ONLY.  The oracle is a plain, slow, obviously correct CPU
+statement of what the hot path computes.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import it;
+the product package never does, and it never imports the product package.
+
+Every function states the passage it follows.  Page titles used below:
+
+* [TT]  "TorchTitan: a one-stop PyTorch-native solution for production LLM
+  pre-training" (zenmind.me paper analysis), section 3.3 "Memory and compute
+  optimisations", bullet "Mixed precision and Float8" -- Float8 is a derived
+  dtype for linear layers with dynamic/delayed/static per-tensor scaling,
+  composable with autograd.
+* [L9]  "Lecture 9 exercises" (juanwang-buaa tutorials), the answer on fp16
+  loss scaling versus FP8 scaling -- one scale factor per tensor (or per block).
+
+Where the pages are silent the reading taken is stated on the function.  The
+arithmetic lives in ``fp8_oracle.c`` (plain C, built with gcc by ``build()``);
+this module only marshals numpy arrays.
+
+Parity pins: every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_*.py`` against something other than itself (brute force,
+exact integer arithmetic, closed forms, library routines, hand-worked cases in
+``tests/golden/``).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3 = 0
+E5M2 = 1
+FMT_MAX = 448.0          # numerator of the scale for all three tensors
+AMAX_FLOOR = 1e-12       # amax floor before the division
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_OUT_DIR, "libfp8oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile fp8_oracle.c into a shared library with gcc; return its path."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, f32, u8p, f32p = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p
+        lib.orc_fp8_decode.restype = ctypes.c_double
+        lib.orc_fp8_decode.argtypes = [ctypes.c_int, ctypes.c_uint8]
+        lib.orc_fp8_encode.restype = ctypes.c_uint8
+        lib.orc_fp8_encode.argtypes = [ctypes.c_int, f32]
+        lib.orc_encode_f32.restype = None
+        lib.orc_encode_f32.argtypes = [ctypes.c_void_p, i64, ctypes.c_int, u8p]
+        lib.orc_amax_bf16.restype = f32
+        lib.orc_amax_bf16.argtypes = [ctypes.c_void_p, i64]
+        lib.orc_scale.restype = None
+        lib.orc_scale.argtypes = [f32, f32, f32p, f32p]
+        lib.orc_cast_bf16.restype = None
+        lib.orc_cast_bf16.argtypes = [ctypes.c_void_p, i64, ctypes.c_int, f32, u8p]
+        lib.orc_transpose_u8.restype = None
+        lib.orc_transpose_u8.argtypes = [u8p, i64, i64, u8p]
+        lib.orc_gemm_rows.restype = None
+        lib.orc_gemm_rows.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64,
+                                      f32, f32, ctypes.c_void_p, i64, ctypes.c_void_p]
+        lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_num_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle takes C-contiguous arrays"
+    return a.ctypes.data
+
+
+def num_threads() -> int:
+    """Host threads the oracle's parallel loops use (OpenMP)."""
+    return int(_load().orc_num_threads())
+
+
+# ---------------------------------------------------------------- formats
+
+def decode_table(fmt: int) -> np.ndarray:
+    """Value of each of the 256 FP8 codes (float64) from the sign/exponent/
+    mantissa definition of e4m3 (fn variant) or e5m2.  The pages name only
+    the "derived dtype" [TT]; the two formats are the reading stated in the
+    design notes."""
+    lib = _load()
+    return np.array([lib.orc_fp8_decode(fmt, c) for c in range(256)], dtype=np.float64)
+
+
+def encode(fmt: int, v) -> np.ndarray:
+    """Saturating round-to-nearest-even of fp32 values into FP8 codes."""
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    q = np.empty(v.shape, dtype=np.uint8)
+    _load().orc_encode_f32(_ptr(v), v.size, fmt, _ptr(q))
+    return q
+
+
+# ---------------------------------------------------------- scaling steps
+
+def amax(x_bits: np.ndarray) -> np.float32:
+    """amax = max |x| over the whole bf16 tensor: dynamic per-tensor scaling
+    takes one statistic per tensor per step [TT], [L9]."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    return np.float32(_load().orc_amax_bf16(_ptr(x_bits), x_bits.size))
+
+
+def scale(amax_value: float, fmt_max: float = FMT_MAX):
+    """(scale, inv_scale) = (fmt_max / max(amax, 1e-12), 1 / scale) in fp32.
+
+    The pages give one factor per tensor [L9]; fmt_max = 448 for all three
+    tensors and the 1e-12 floor are the readings stated in the design notes."""
+    s = ctypes.c_float()
+    inv = ctypes.c_float()
+    _load().orc_scale(float(np.float32(amax_value)), float(np.float32(fmt_max)),
+                      ctypes.addressof(s), ctypes.addressof(inv))
+    return np.float32(s.value), np.float32(inv.value)
+
+
+def cast(x_bits: np.ndarray, fmt: int, scale_value: float) -> np.ndarray:
+    """q = sat_RNE_fp8(fp32(x) * scale), element by element (derived dtype
+    [TT]); the fp32 product is rounded once, then once more into FP8."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    q = np.empty(x_bits.shape, dtype=np.uint8)
+    _load().orc_cast_bf16(_ptr(x_bits), x_bits.size, fmt, float(np.float32(scale_value)), _ptr(q))
+    return q
+
+
+def transpose(q: np.ndarray) -> np.ndarray:
+    """qT[c][r] = q[r][c]: the copy whose contiguous index is the other one."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    rows, cols = q.shape
+    qT = np.empty((cols, rows), dtype=np.uint8)
+    _load().orc_transpose_u8(_ptr(q), rows, cols, _ptr(qT))
+    return qT
+
+
+def quantize(x_bits: np.ndarray, fmt: int, fmt_max: float = FMT_MAX) -> dict:
+    """The whole per-tensor scaling of one bf16 matrix: amax, scale, the FP8
+    copy and its transpose."""
+    a = amax(x_bits)
+    s, inv = scale(a, fmt_max)
+    q = cast(x_bits, fmt, s)
+    return {"amax": a, "scale": s, "inv_scale": inv, "q": q, "qT": transpose(q)}
+
+
+# ------------------------------------------------------------------ GEMMs
+
+def gemm_rows(A: np.ndarray, fa: int, B: np.ndarray, fb: int,
+              inv_a: float, inv_b: float, rows=None) -> np.ndarray:
+    """C = (dec(A) . dec(B)^T) * inv_a * inv_b in float64 for the listed rows
+    of C (all rows when ``rows`` is None).  A is [P x R] codes and B is
+    [Q x R] codes, both with the contraction index contiguous."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    P, R = A.shape
+    Q, R2 = B.shape
+    assert R == R2, "contraction lengths differ"
+    if rows is None:
+        rows = np.arange(P, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < P)
+    out = np.empty((rows.size, Q), dtype=np.float64)
+    _load().orc_gemm_rows(_ptr(A), fa, _ptr(B), fb, P, Q, R,
+                          float(np.float32(inv_a)), float(np.float32(inv_b)),
+                          _ptr(rows), rows.size, _ptr(out))
+    return out
+
+
+def fwd_ref(xq, inv_x, wq, inv_w, rows=None):
+    """Y = X . W^T of the Float8 linear (forward), e4m3 x e4m3 [TT]."""
+    return gemm_rows(xq, E4M3, wq, E4M3, inv_x, inv_w, rows)
+
+
+def dgrad_ref(dyq, inv_dy, wqT, inv_w, rows=None):
+    """dX = dY . W (input gradient through autograd [TT]), e5m2 x e4m3."""
+    return gemm_rows(dyq, E5M2, wqT, E4M3, inv_dy, inv_w, rows)
+
+
+def wgrad_ref(dyqT, inv_dy, xqT, inv_x, rows=None):
+    """dW = dY^T . X (weight gradient through autograd [TT]), e5m2 x e4m3."""
+    return gemm_rows(dyqT, E5M2, xqT, E4M3, inv_dy, inv_x, rows)
+
+
+def within_tolerance(y: np.ndarray, ref: np.ndarray, rms_ref: float):
+    """Elementwise GEMM bar: |y - ref| <= 2^-7 |ref| + 1e-3 rms(ref).
+    Returns (ok, worst ratio of error to the allowed bound)."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = 2.0 ** -7 * np.abs(ref) + 1e-3 * rms_ref
+    err = np.abs(y - ref)
+    ratio = float(np.max(err / np.maximum(bound, np.finfo(np.float64).tiny))) if err.size else 0.0
+    return bool(np.all(err <= bound)), ratio

@@ -1,0 +1,269 @@
+/*
+ * fp8_oracle.c -- plain, slow CPU definition of the Float8 linear layer's hot
+ * path with dynamic per-tensor scaling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or constant
+ * generator with the CUDA library; it includes no CUDA header.
+ *
+ * Sources (page titles; sections):
+ *  - "TorchTitan: a one-stop PyTorch-native solution for production LLM
+ *    pre-training" (zenmind.me paper analysis), section 3.3 "Memory and compute
+ *    optimisations", bullet "Mixed precision and Float8": Float8 is a derived
+ *    dtype applied to linear layers, with dynamic / delayed / static per-tensor
+ *    scaling, composable with autograd.
+ *  - "Lecture 9 exercises" (juanwang-buaa tutorials), answer on fp16 loss
+ *    scaling versus FP8 scaling: FP8 scaling is one factor per tensor (or per
+ *    block); what FP8 saves is only what is stored in FP8.
+ * The pages do not fix the formats or the arithmetic.  The readings used here
+ * (e4m3 for X and W, e5m2 for dY; scale = fmt_max / amax with fmt_max = 448;
+ * fp32 product then one saturating round-to-nearest-even into the format;
+ * amax floored at 1e-12; the three GEMMs of a linear's forward and backward
+ * with the inverse scales applied after the fp32 sum) are listed with their
+ * reasons in the design notes.
+ *
+ * FP8 formats follow their published bit-level definitions (OCP 8-bit
+ * floating point, "FP8 formats for deep learning"):
+ *   e4m3 ("fn" variant): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
+ *        no infinities, S.1111.111 is NaN, largest finite 448 (0x7E).
+ *   e5m2: 1 sign, 5 exponent bits (bias 15), 2 mantissa bits, IEEE-like:
+ *        exponent 31 holds Inf (mantissa 0) and NaN, largest finite 57344 (0x7B).
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fno-fast-math -shared.
+ * fp-contract is off so that no product is fused into an add on any host.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_E4M3 0
+#define ORC_E5M2 1
+
+/* ------------------------------------------------------------------ bits */
+
+static float f32_from_bits(uint32_t b) {
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+static uint32_t bits_from_f32(float f) {
+    uint32_t b;
+    memcpy(&b, &f, sizeof b);
+    return b;
+}
+
+/* bf16 is the upper half of an IEEE binary32: widening is exact. */
+float orc_bf16_to_f32(uint16_t h) { return f32_from_bits((uint32_t)h << 16); }
+
+/* ------------------------------------------------------- format params */
+
+typedef struct {
+    int ebits;      /* exponent field width          */
+    int mbits;      /* mantissa field width          */
+    int bias;       /* exponent bias                 */
+    int max_code;   /* largest finite magnitude code */
+    int ieee_inf;   /* 1: all-ones exponent is Inf/NaN (e5m2); 0: only S.1111.111 is NaN (e4m3fn) */
+} fp8_fmt;
+
+static fp8_fmt fmt_params(int fmt) {
+    fp8_fmt f;
+    if (fmt == ORC_E4M3) {
+        f.ebits = 4; f.mbits = 3; f.bias = 7; f.max_code = 0x7E; f.ieee_inf = 0;
+    } else {
+        f.ebits = 5; f.mbits = 2; f.bias = 15; f.max_code = 0x7B; f.ieee_inf = 1;
+    }
+    return f;
+}
+
+/* --------------------------------------------------------------- decode */
+
+/* Value of one FP8 code, straight from the sign/exponent/mantissa definition.
+ * Returns NaN for NaN codes and +-Inf for e5m2's infinities. */
+double orc_fp8_decode(int fmt, uint8_t code) {
+    fp8_fmt f = fmt_params(fmt);
+    int sign = code >> 7;
+    int e = (code >> f.mbits) & ((1 << f.ebits) - 1);
+    int m = code & ((1 << f.mbits) - 1);
+    int emax_field = (1 << f.ebits) - 1;
+    double v;
+    if (f.ieee_inf && e == emax_field) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else if (!f.ieee_inf && e == emax_field && m == (1 << f.mbits) - 1) {
+        v = NAN;
+    } else if (e == 0) {
+        /* subnormal: 0.m x 2^(1-bias) */
+        v = ldexp((double)m, 1 - f.bias - f.mbits);
+    } else {
+        /* normal: 1.m x 2^(e-bias) */
+        v = ldexp((double)((1 << f.mbits) + m), e - f.bias - f.mbits);
+    }
+    return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------- encode */
+
+/* x / 2^s rounded to the nearest integer, ties to the even integer. */
+static uint64_t shift_rne(uint64_t x, int s) {
+    if (s <= 0) return x;
+    if (s >= 64) return 0;
+    uint64_t q = x >> s;
+    uint64_t r = x & ((1ull << s) - 1);
+    uint64_t half = 1ull << (s - 1);
+    if (r > half || (r == half && (q & 1))) q += 1;
+    return q;
+}
+
+/* Saturating round-to-nearest-even of one fp32 value into an FP8 code,
+ * by integer manipulation of the binary32 fields:
+ *  - NaN stays NaN (sign kept, mantissa all ones);
+ *  - |v| at or above the largest finite value (Inf included) gives the
+ *    largest finite code with v's sign (saturation);
+ *  - otherwise the significand is rounded to the format's mantissa width at
+ *    v's exponent, or at the format's subnormal spacing when v lies below the
+ *    smallest normal; ties go to the even code; the sign of zero is kept. */
+uint8_t orc_fp8_encode(int fmt, float v) {
+    fp8_fmt f = fmt_params(fmt);
+    uint32_t u = bits_from_f32(v);
+    uint8_t sign = (uint8_t)((u >> 31) << 7);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) /* NaN */
+        return (uint8_t)(sign | 0x7F);
+    double max_val = orc_fp8_decode(fmt, (uint8_t)f.max_code);
+    if ((double)f32_from_bits(a) >= max_val) /* saturate, Inf included */
+        return (uint8_t)(sign | f.max_code);
+
+    int exp32 = (int)(a >> 23);             /* biased binary32 exponent */
+    uint64_t sig = a & 0x7FFFFFu;           /* 23-bit fraction           */
+    if (exp32 == 0) {
+        /* binary32 subnormal: below 2^-126, far under half the smallest
+         * FP8 subnormal (2^-10 for e4m3, 2^-17 for e5m2): rounds to zero. */
+        return sign;
+    }
+    sig |= 1u << 23;                        /* implicit leading one      */
+    int e = exp32 - 127;                    /* unbiased exponent         */
+    int emin = 1 - f.bias;                  /* smallest normal exponent  */
+    uint32_t mag;
+    if (e >= emin) {
+        uint64_t r = shift_rne(sig, 23 - f.mbits);   /* 1.m with mbits bits */
+        if (r == (1ull << (f.mbits + 1))) {          /* carried into next binade */
+            r >>= 1;
+            e += 1;
+        }
+        mag = (uint32_t)(((e + f.bias) << f.mbits) | (int)(r & ((1u << f.mbits) - 1)));
+    } else {
+        /* subnormal target: count units of 2^(emin - mbits).  A carry to
+         * 2^mbits units is exactly the smallest normal code. */
+        int s = (23 - f.mbits) + (emin - e);
+        mag = (uint32_t)shift_rne(sig, s);
+    }
+    return (uint8_t)(sign | mag);
+}
+
+/* encode() applied to an array of binary32 values. */
+void orc_encode_f32(const float *v, int64_t n, int fmt, uint8_t *q) {
+    for (int64_t i = 0; i < n; ++i) q[i] = orc_fp8_encode(fmt, v[i]);
+}
+
+/* ---------------------------------------------------------------- amax */
+
+/* amax = max_i |x_i| over a bf16 tensor (fp32 result, exact: the maximum of
+ * bf16 magnitudes is itself a bf16 value).  Magnitudes are ordered by the
+ * IEEE 754 totalOrder predicate: for finite values that is the ordinary
+ * order, +Inf lies above every finite value and NaNs lie above +Inf, ordered
+ * by payload.  An empty tensor gives 0. */
+float orc_amax_bf16(const uint16_t *x, int64_t n) {
+    float best = 0.0f;
+    uint16_t nan_mag = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        uint16_t mag = (uint16_t)(x[i] & 0x7FFF);
+        if (mag > 0x7F80) {                 /* NaN */
+            if (mag > nan_mag) nan_mag = mag;
+            continue;
+        }
+        float v = fabsf(orc_bf16_to_f32(x[i]));
+        if (v > best) best = v;
+    }
+    if (nan_mag) return orc_bf16_to_f32(nan_mag);
+    return best;
+}
+
+/* --------------------------------------------------------------- scale */
+
+/* scale = fmt_max / max(amax, 1e-12) and inv_scale = 1 / scale, both as
+ * binary32 round-to-nearest operations.  A NaN amax propagates. */
+void orc_scale(float amax, float fmt_max, float *scale, float *inv_scale) {
+    volatile float a = (amax < 1e-12f) ? 1e-12f : amax;
+    volatile float s = fmt_max / a;
+    volatile float inv = 1.0f / s;
+    *scale = s;
+    *inv_scale = inv;
+}
+
+/* ---------------------------------------------------------------- cast */
+
+/* q_i = encode(fp32(x_i) * scale): the product is one binary32 multiply
+ * (round to nearest even), then one saturating RNE into the FP8 format. */
+void orc_cast_bf16(const uint16_t *x, int64_t n, int fmt, float scale, uint8_t *q) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        volatile float v = orc_bf16_to_f32(x[i]) * scale;
+        q[i] = orc_fp8_encode(fmt, v);
+    }
+}
+
+/* qT[c][r] = q[r][c] for a row-major [rows x cols] byte matrix. */
+void orc_transpose_u8(const uint8_t *q, int64_t rows, int64_t cols, uint8_t *qT) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < cols; ++c)
+        for (int64_t r = 0; r < rows; ++r)
+            qT[c * rows + r] = q[r * cols + c];
+}
+
+/* ---------------------------------------------------------------- GEMM */
+
+/* Reference for one scaled FP8 GEMM written as C = A . B^T, with both
+ * operands stored with the contraction index contiguous:
+ *     A is [P x R] codes (format fa), B is [Q x R] codes (format fb),
+ *     C[p][q] = ( sum_k dec(A[p][k]) * dec(B[q][k]) ) * inv_a * inv_b,
+ * the sum taken in binary64 in increasing k, the inverse scales applied
+ * after it in binary64.  Only the rows listed in `rows` (nrows of them) are
+ * computed; out is [nrows x Q].  The forward pass, input gradient and weight
+ * gradient of the linear layer are the three instances
+ *     Y  = Xq . Wq^T        (A = Xq,   B = Wq)
+ *     dX = dYq . (WqT)^T    (A = dYq,  B = WqT,  i.e. dY . W)
+ *     dW = dYqT . (XqT)^T   (A = dYqT, B = XqT,  i.e. dY^T . X). */
+void orc_gemm_rows(const uint8_t *A, int fa, const uint8_t *B, int fb,
+                   int64_t P, int64_t Q, int64_t R, float inv_a, float inv_b,
+                   const int64_t *rows, int64_t nrows, double *out) {
+    double da[256], db[256];
+    for (int c = 0; c < 256; ++c) {
+        da[c] = orc_fp8_decode(fa, (uint8_t)c);
+        db[c] = orc_fp8_decode(fb, (uint8_t)c);
+    }
+    (void)P;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const uint8_t *a = A + rows[i] * R;
+        for (int64_t q = 0; q < Q; ++q) {
+            const uint8_t *b = B + q * R;
+            double s = 0.0;
+            for (int64_t k = 0; k < R; ++k)
+                s += da[a[k]] * db[b[k]];
+            out[i * Q + q] = s * (double)inv_a * (double)inv_b;
+        }
+    }
+}
+
+/* Number of threads the parallel loops above use. */
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
