@@ -1,0 +1,431 @@
+"""Benchmark: Float8 linear fwd+bwd TFLOPS (amax and cast included) on the
+Llama-3.1-8B SwiGLU FFN.
+
+One step is the whole hot path for the FFN's three linears on one batch of
+8192 tokens: for each of w1 and w3 (X [8192 x 4096], W [14336 x 4096],
+dY [8192 x 14336]) and w2 (H [8192 x 14336], W [4096 x 14336],
+dY [8192 x 4096]): amax of X, W, dY; scale + cast + transpose of each; the
+forward, input-gradient and weight-gradient FP8 GEMMs.  Nothing is cached
+across steps (dynamic scaling recomputes every statistic every step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  N > 1 runs under torchrun: each rank runs
+its own replica on its own batch (the path has no exchange step), timing is
+bracketed by a barrier + synchronize and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "FP8 linear fwd+bwd TFLOPS incl. amax/cast, % of GB300 dense FP8 peak"
+WORKLOAD = "llama3.1-8b-swiglu-ffn"
+FP8_PER_BF16 = 2.0            # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- inputs
+
+def ffn_layers():
+    """(name, workload, x tensor id, w tensor id, dy tensor id) for w1, w3, w2."""
+    w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
+    w2 = wl.WORKLOADS["llama3_8b_ffn_w2"]
+    return [("w1", w13, wl.X, wl.W, wl.DY), ("w3", w13, wl.X, wl.W3, wl.DY3), ("w2", w2, wl.X, wl.W, wl.DY)]
+
+
+def step_flops() -> int:
+    return sum(w.flops for _, w, *_ in ffn_layers())
+
+
+def host_inputs(rank: int):
+    """bf16 bit patterns for one step; activations and gradients per rank."""
+    out = {}
+    for name, w, xid, wid, did in ffn_layers():
+        xkey = (w.name, xid, rank)
+        if xkey not in out:
+            out[xkey] = wl.generate((w.M, w.K), *w.x, seed=w.seed + 1000 * rank, tensor_id=xid)
+        out[(name, "w")] = wl.generate((w.N, w.K), *w.w, seed=w.seed, tensor_id=wid)
+        out[(name, "dy")] = wl.generate((w.M, w.N), *w.dy, seed=w.seed + 1000 * rank, tensor_id=did)
+        out[(name, "x")] = out[xkey]
+    return {k: v for k, v in out.items() if isinstance(k[1], str)}
+
+
+# ------------------------------------------------------------------ peaks
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        load = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- oracle (CPU)
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of one FFN step: the per-tensor
+    scaling (amax, scale, cast, transpose) of the first `frac` of every
+    tensor's rows and the three GEMMs on `frac` of their output rows (full
+    FP8 operands prepared once, untimed).  Work scales linearly with rows,
+    so the full-step time is the sample time / frac."""
+
+    def __init__(self, frac: float):
+        import oracle
+        self.o = oracle
+        self.frac = frac
+        self.layers = []
+        for name, w, xid, wid, did in ffn_layers():
+            X = wl.generate((w.M, w.K), *w.x, seed=w.seed, tensor_id=xid)
+            W = wl.generate((w.N, w.K), *w.w, seed=w.seed, tensor_id=wid)
+            D = wl.generate((w.M, w.N), *w.dy, seed=w.seed, tensor_id=did)
+            qx, qw, qd = (oracle.quantize(X, oracle.E4M3), oracle.quantize(W, oracle.E4M3),
+                          oracle.quantize(D, oracle.E5M2))
+            self.layers.append((w, X, W, D, qx, qw, qd))
+
+    def run(self) -> float:
+        o, f = self.o, self.frac
+        t0 = time.perf_counter()
+        for w, X, W, D, qx, qw, qd in self.layers:
+            for T, fmt in ((X, o.E4M3), (W, o.E4M3), (D, o.E5M2)):
+                rows = max(16, int(round(T.shape[0] * f)))
+                o.quantize(T[:rows], fmt)
+            rm = np.arange(max(1, int(round(w.M * f))))
+            rn = np.arange(max(1, int(round(w.N * f))))
+            o.fwd_ref(qx["q"], qx["inv_scale"], qw["q"], qw["inv_scale"], rm)
+            o.dgrad_ref(qd["q"], qd["inv_scale"], qw["qT"], qw["inv_scale"], rm)
+            o.wgrad_ref(qd["qT"], qd["inv_scale"], qx["qT"], qx["inv_scale"], rn)
+        return time.perf_counter() - t0
+
+    def describe(self) -> str:
+        return (f"one Llama-3.1-8B FFN step (w1, w3, w2) sampled at {self.frac:.5g} of its rows: "
+                f"amax/scale/cast/transpose of that share of every X, W, dY and that share of "
+                f"the output rows of every fwd/dgrad/wgrad GEMM; full-step time = sample time / share")
+
+
+def cpu_baseline_value(sample_s: float, frac: float) -> float:
+    return step_flops() / (sample_s / frac) / 1e12
+
+
+# ------------------------------------------------------------ reference
+
+def run_reference(args, rank: int) -> None:
+    if rank != 0:
+        return
+    import oracle
+    frac = args.ref_frac
+    s = OracleSample(frac)
+    for _ in range(args.warmup):
+        s.run()
+    times = [s.run() for _ in range(args.steps)]
+    total = sum(times)
+    step_s = total / len(times) / frac
+    value = step_flops() / step_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": s.describe()},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- ours
+
+def run_ours(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+    import float8_linear_layers_gb300 as fl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    host = host_inputs(rank)
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    dev_in = {k: up(v) for k, v in host.items()}
+    # X is shared by w1 and w3: one device copy
+    dev_in[("w3", "x")] = dev_in[("w1", "x")]
+    layers = []
+    for name, w, *_ in ffn_layers():
+        layers.append((name, w, fl.Float8Linear(w.M, w.K, w.N, device=dev)))
+    stream = torch.cuda.current_stream(dev)
+
+    # Per-kernel events inside the timed region: events bracket each launch
+    # on the stream the kernels run on.
+    def step(events=None):
+        for name, w, lin in layers:
+            x, wt, dy = dev_in[(name, "x")], dev_in[(name, "w")], dev_in[(name, "dy")]
+            if events is None:
+                lin.step(x, wt, dy)
+                continue
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+            ev[0].record(stream)
+            fl.fp8lin_amax(x, lin.x8.amax)
+            ev[1].record(stream)
+            fl.fp8lin_cast_transpose(x, fl.E4M3, lin.x8.amax, lin.x8.scale, lin.x8.inv_scale, lin.x8.q, lin.x8.qT)
+            ev[2].record(stream)
+            lin.w8.quantize(wt)
+            ev[3].record(stream)
+            fl.fp8lin_fwd(lin.x8.q, lin.x8.inv_scale, lin.w8.q, lin.w8.inv_scale, lin.y)
+            ev[4].record(stream)
+            fl.fp8lin_amax(dy, lin.dy8.amax)
+            ev[5].record(stream)
+            fl.fp8lin_cast_transpose(dy, fl.E5M2, lin.dy8.amax, lin.dy8.scale, lin.dy8.inv_scale, lin.dy8.q, lin.dy8.qT)
+            ev[6].record(stream)
+            fl.fp8lin_dgrad(lin.dy8.q, lin.dy8.inv_scale, lin.w8.qT, lin.w8.inv_scale, lin.dx)
+            ev[7].record(stream)
+            fl.fp8lin_wgrad(lin.dy8.qT, lin.dy8.inv_scale, lin.x8.qT, lin.x8.inv_scale, lin.dw)
+            ev[8].record(stream)
+            events.append((name, w, ev))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+
+    # ---- timed region (device-resident inputs)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    events = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(events)
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    assert fl.fp8lin_device_error() == 0, "a GEMM kernel reported a timed-out wait"
+
+    # per-kernel times from the events
+    gemm_ms = amax_ms = cast_ms = 0.0
+    gemm_flops = amax_bytes = cast_bytes = 0
+    per_layer = {}
+    for name, w, ev in events:
+        amax_x = ev[0].elapsed_time(ev[1])
+        cast_x = ev[1].elapsed_time(ev[2])
+        wq = ev[2].elapsed_time(ev[3])
+        fwd = ev[3].elapsed_time(ev[4])
+        amax_d = ev[4].elapsed_time(ev[5])
+        cast_d = ev[5].elapsed_time(ev[6])
+        dgrad = ev[6].elapsed_time(ev[7])
+        wgrad = ev[7].elapsed_time(ev[8])
+        gemm_ms += fwd + dgrad + wgrad
+        gemm_flops += 3 * 2 * w.M * w.N * w.K
+        amax_ms += amax_x + amax_d
+        amax_bytes += 2 * (w.M * w.K + w.M * w.N)
+        cast_ms += cast_x + cast_d
+        cast_bytes += 4 * (w.M * w.K + w.M * w.N)
+        pl = per_layer.setdefault(name, {"ms": 0.0, "gemm_ms": 0.0, "n": 0, "flops": w.flops})
+        pl["ms"] += ev[0].elapsed_time(ev[8])
+        pl["gemm_ms"] += fwd + dgrad + wgrad
+        pl["n"] += 1
+
+    peaks, peak_src = load_peaks()
+    fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    fp8_peak_burst = peaks["bf16_tflops"] * FP8_PER_BF16
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_flops() / (ms_per_step * 1e-3) / 1e12
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    n_gemm = 9 * args.steps
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for k, v in host.items()}
+        outs = {name: [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (lin.y, lin.dx, lin.dw)]
+                for name, _, lin in layers}
+        h2d = sum(t.numel() * 2 for k, t in pinned.items() if not (k[0] == "w3" and k[1] == "x"))
+        d2h = sum(t.numel() * 2 for ts in outs.values() for t in ts)
+
+        def e2e_step():
+            for k, t in pinned.items():
+                if k[0] == "w3" and k[1] == "x":
+                    continue
+                dev_in[k].copy_(t, non_blocking=True)
+            for name, w, lin in layers:
+                y, dx, dw = lin.step(dev_in[(name, "x")], dev_in[(name, "w")], dev_in[(name, "dy")])
+                for o, d in zip(outs[name], (y, dx, dw)):
+                    o.copy_(d, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * step_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        s = OracleSample(args.cpu_frac)
+        secs = s.run()
+        cpu = {"value": cpu_baseline_value(secs, args.cpu_frac), "unit": "TFLOPS",
+               "cores": oracle.num_threads(), "kind": "oracle", "sample": s.describe(),
+               "sample_seconds": secs}
+
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD,
+                   "linears": {"w1": "M8192 K4096 N14336", "w3": "M8192 K4096 N14336",
+                               "w2": "M8192 K14336 N4096"},
+                   "l2": "inputs larger than L2: one step streams ~2.9 GB of distinct operands through a 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak_sustained,
+        "fp8_peak_tflops": {"sustained": fp8_peak_sustained, "burst": fp8_peak_burst,
+                            "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
+        "roofline": {"bound": "tensor", "kernel": "fp8_gemm_tn_kernel", "achieved": gemm_tflops,
+                     "peak": fp8_peak_sustained, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
+                     "traffic": None, "peak_source": f"{peak_src} sustained bf16 x {FP8_PER_BF16:g}",
+                     "launches_timed": n_gemm},
+        "kernels": {
+            "gemm": {"ms_per_step": gemm_ms / args.steps, "tflops": gemm_tflops},
+            "amax": {"ms_per_step": amax_ms / args.steps,
+                     "gbs": amax_bytes / (amax_ms * 1e-3) / 1e9 if amax_ms else None},
+            "cast_transpose": {"ms_per_step": cast_ms / args.steps,
+                               "gbs": cast_bytes / (cast_ms * 1e-3) / 1e9 if cast_ms else None},
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+        },
+        "per_linear": {k: {"tflops": v["flops"] * v["n"] / (v["ms"] * 1e-3) / 1e12,
+                           "gemm_tflops": v["flops"] * v["n"] / (v["gemm_ms"] * 1e-3) / 1e12}
+                       for k, v in per_layer.items()},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 27 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
+    ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # timing rule: at least three warm-up steps
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,245 @@
+"""Python binding of libfp8lin: the Float8 linear layer hot path on one GB300.
+
+Argument marshalling only.  Every step of the path (amax, scale, cast,
+transpose, the three GEMMs) runs in the library's own CUDA kernels; PyTorch
+provides device memory and streams.  There is no fallback: importing this
+module fails when the library has not been built.
+
+The names mirror the C ABI in include/fp8lin.h:
+
+    fp8lin_amax(x, amax)
+    fp8lin_cast_transpose(x, fmt, amax, scale, inv_scale, q, qT, fmt_max=448.0)
+    fp8lin_fwd(xq, inv_x, wq, inv_w, y)
+    fp8lin_dgrad(dyq, inv_dy, wqT, inv_w, dx)
+    fp8lin_wgrad(dyqT, inv_dy, xqT, inv_x, dw)
+
+Each takes an optional ``stream`` (a torch.cuda.Stream; default: the current
+stream) and raises Fp8LinError on a non-OK status.  ``Float8Linear`` below
+sequences the nine calls of one linear's forward and backward pass.
+
+Source of the method: "TorchTitan: a one-stop PyTorch-native solution for
+production LLM pre-training" (zenmind.me analysis), section 3.3, bullet
+"Mixed precision and Float8" (Float8 linear layers with dynamic per-tensor
+scaling, composable with autograd); "Lecture 9 exercises", the answer on FP8
+scaling (one factor per tensor; only what is stored in FP8 is saved).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+E4M3 = 0
+E5M2 = 1
+FMT_MAX = 448.0
+
+_STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNED",
+           3: "FP8LIN_ERR_UNSUPPORTED_SHAPE", 4: "FP8LIN_ERR_CUDA", 5: "FP8LIN_ERR_TIMEOUT",
+           6: "FP8LIN_ERR_UNSUPPORTED_DEVICE"}
+
+# Every entry point declared in include/fp8lin.h.
+ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_fwd", "fp8lin_dgrad",
+                "fp8lin_wgrad", "fp8lin_status_str", "fp8lin_device_error")
+
+
+class Fp8LinError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call}: {_STATUS.get(status, status)}: {status_str(status)}")
+
+
+def _load_library() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libfp8lin is not built ({path} missing): run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    sigs = {
+        "fp8lin_amax": [vp, i64, vp, vp],
+        "fp8lin_cast_transpose": [vp, i64, i64, ci, f32, vp, vp, vp, vp, vp, vp],
+        "fp8lin_fwd": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8lin_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8lin_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8lin_device_error": [vp, vp],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.fp8lin_status_str.argtypes = [ctypes.c_int]
+    lib.fp8lin_status_str.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load_library()
+LIBRARY_PATH = _build.LIB
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return _lib.fp8lin_status_str(int(status)).decode()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _check(call: str, status: int) -> None:
+    if status != 0:
+        raise Fp8LinError(call, status)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> None:
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------ entry points
+
+def fp8lin_amax(x: torch.Tensor, amax: torch.Tensor, stream=None) -> None:
+    """amax[0] = max |x| over the whole bf16 tensor x."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(amax, "amax", torch.float32)
+    _check("fp8lin_amax", _lib.fp8lin_amax(_ptr(x), x.numel(), _ptr(amax), _stream(stream)))
+
+
+def fp8lin_cast_transpose(x: torch.Tensor, fmt: int, amax: torch.Tensor, scale: torch.Tensor,
+                          inv_scale: torch.Tensor, q: torch.Tensor | None, qT: torch.Tensor | None,
+                          fmt_max: float = FMT_MAX, stream=None) -> None:
+    """scale = fmt_max / amax; q = sat_RNE(x * scale) [rows x cols]; qT = q^T."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [rows x cols] matrix")
+    for t, n in ((amax, "amax"), (scale, "scale"), (inv_scale, "inv_scale")):
+        _dev(t, n, torch.float32)
+    _dev(q, "q")
+    _dev(qT, "qT")
+    rows, cols = x.shape
+    _check("fp8lin_cast_transpose",
+           _lib.fp8lin_cast_transpose(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(amax),
+                                      _ptr(scale), _ptr(inv_scale), _ptr(q), _ptr(qT),
+                                      _stream(stream)))
+
+
+def fp8lin_fwd(xq, inv_x, wq, inv_w, y, stream=None) -> None:
+    """Y [M x N] = bf16((Xq . Wq^T) * inv_x * inv_w); Xq [M x K], Wq [N x K]."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    for t, n in ((xq, "xq"), (wq, "wq"), (inv_x, "inv_x"), (inv_w, "inv_w"), (y, "y")):
+        _dev(t, n)
+    if wq.shape[1] != K or tuple(y.shape) != (M, N) or y.dtype != torch.bfloat16:
+        raise ValueError("shape/dtype mismatch: xq [M,K], wq [N,K], y bf16 [M,N]")
+    _check("fp8lin_fwd", _lib.fp8lin_fwd(_ptr(xq), _ptr(inv_x), _ptr(wq), _ptr(inv_w), _ptr(y),
+                                         M, N, K, _stream(stream)))
+
+
+def fp8lin_dgrad(dyq, inv_dy, wqT, inv_w, dx, stream=None) -> None:
+    """dX [M x K] = bf16((dYq . WqT^T) * inv_dy * inv_w); dYq [M x N], WqT [K x N]."""
+    M, N = dyq.shape
+    K = wqT.shape[0]
+    for t, n in ((dyq, "dyq"), (wqT, "wqT"), (inv_dy, "inv_dy"), (inv_w, "inv_w"), (dx, "dx")):
+        _dev(t, n)
+    if wqT.shape[1] != N or tuple(dx.shape) != (M, K) or dx.dtype != torch.bfloat16:
+        raise ValueError("shape/dtype mismatch: dyq [M,N], wqT [K,N], dx bf16 [M,K]")
+    _check("fp8lin_dgrad", _lib.fp8lin_dgrad(_ptr(dyq), _ptr(inv_dy), _ptr(wqT), _ptr(inv_w),
+                                             _ptr(dx), M, N, K, _stream(stream)))
+
+
+def fp8lin_wgrad(dyqT, inv_dy, xqT, inv_x, dw, stream=None) -> None:
+    """dW [N x K] = bf16((dYqT . XqT^T) * inv_dy * inv_x); dYqT [N x M], XqT [K x M]."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    for t, n in ((dyqT, "dyqT"), (xqT, "xqT"), (inv_dy, "inv_dy"), (inv_x, "inv_x"), (dw, "dw")):
+        _dev(t, n)
+    if xqT.shape[1] != M or tuple(dw.shape) != (N, K) or dw.dtype != torch.bfloat16:
+        raise ValueError("shape/dtype mismatch: dyqT [N,M], xqT [K,M], dw bf16 [N,K]")
+    _check("fp8lin_wgrad", _lib.fp8lin_wgrad(_ptr(dyqT), _ptr(inv_dy), _ptr(xqT), _ptr(inv_x),
+                                             _ptr(dw), M, N, K, _stream(stream)))
+
+
+def fp8lin_device_error(stream=None) -> int:
+    """Raw device error word since the last call (0 = none); synchronises."""
+    word = ctypes.c_uint32(0)
+    st = _lib.fp8lin_device_error(_stream(stream), ctypes.addressof(word))
+    if st not in (0, 5):
+        _check("fp8lin_device_error", st)
+    return int(word.value)
+
+
+# ----------------------------------------------------------- one linear
+
+class Float8Tensor:
+    """Per-tensor FP8 state of one bf16 matrix: amax, scale, inverse scale and
+    the FP8 copies in both majornesses (device buffers, caller-visible)."""
+
+    def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX):
+        self.rows, self.cols, self.fmt, self.fmt_max = rows, cols, fmt, fmt_max
+        scalars = torch.zeros(3, dtype=torch.float32, device=device)
+        self.amax, self.scale, self.inv_scale = scalars[0:1], scalars[1:2], scalars[2:3]
+        self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+        self.qT = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+
+    def quantize(self, x: torch.Tensor, stream=None) -> "Float8Tensor":
+        """Dynamic scaling of x: amax, then scale + cast + transpose."""
+        fp8lin_amax(x, self.amax, stream)
+        fp8lin_cast_transpose(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT,
+                              self.fmt_max, stream)
+        return self
+
+
+class Float8Linear:
+    """The nine calls of one Float8 linear's forward and backward pass, on
+    caller-owned bf16 X [M x K], W [N x K], dY [M x N].  Buffers for the FP8
+    copies and the outputs are allocated once and reused every step; the
+    transposed copies of X and W made in forward are what backward reads."""
+
+    def __init__(self, M: int, K: int, N: int, device="cuda", fmt_max: float = FMT_MAX):
+        self.M, self.K, self.N = M, K, N
+        self.x8 = Float8Tensor(M, K, E4M3, device, fmt_max)
+        self.w8 = Float8Tensor(N, K, E4M3, device, fmt_max)
+        self.dy8 = Float8Tensor(M, N, E5M2, device, fmt_max)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=device)
+
+    @property
+    def flops(self) -> int:
+        return 6 * self.M * self.N * self.K
+
+    def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
+        self.x8.quantize(x, stream)
+        self.w8.quantize(w, stream)
+        fp8lin_fwd(self.x8.q, self.x8.inv_scale, self.w8.q, self.w8.inv_scale, self.y, stream)
+        return self.y
+
+    def backward(self, dy: torch.Tensor, stream=None):
+        self.dy8.quantize(dy, stream)
+        fp8lin_dgrad(self.dy8.q, self.dy8.inv_scale, self.w8.qT, self.w8.inv_scale, self.dx, stream)
+        fp8lin_wgrad(self.dy8.qT, self.dy8.inv_scale, self.x8.qT, self.x8.inv_scale, self.dw, stream)
+        return self.dx, self.dw
+
+    def step(self, x, w, dy, stream=None):
+        self.forward(x, w, stream)
+        self.backward(dy, stream)
+        return self.y, self.dx, self.dw
+
+    # kernels one step launches (amax x3, cast x3, three GEMMs)
+    KERNELS_PER_STEP = 9

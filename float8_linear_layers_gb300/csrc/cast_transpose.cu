@@ -1,0 +1,177 @@
+// cast_transpose.cu -- scale one bf16 matrix and cast it to FP8 (the Float8
+// derived dtype; TorchTitan analysis page, section 3.3, "Mixed precision and
+// Float8"), writing the row-major copy and the transposed copy in one pass.
+//
+// HBM-bound: per element 2 bytes read, 1 + 1 bytes written.  One CTA owns a
+// 128 x 128 tile:
+//  * phase 1: coalesced 16-byte loads (16 threads per 256-byte tile row, all
+//    eight loads of a thread issued before any use), fp32 product with the
+//    scale, cvt.rn.satfinite into packed FP8 pairs; the row-major copy is
+//    stored straight from registers (8 bytes per thread, 128-byte rows);
+//    the bytes also go to a 16 KB shared tile whose 4-byte words are XOR
+//    swizzled by row group so that phase 2 reads are bank-conflict free;
+//  * phase 2: each thread gathers a 16-row x 4-column block as 16 words,
+//    transposes 4 x 4 byte blocks with byte permutes and stores four 16-byte
+//    chunks of the transposed copy; eight lanes cover one 128-byte row of
+//    the transposed copy, so every warp store writes four full 128-byte rows.
+// The scale is derived in every CTA from the device amax (IEEE division), so
+// no separate launch and no host round trip is needed; CTA 0 publishes it.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kThreads = 256;
+
+// Word index of (row, word) in the swizzled shared tile: bits 2..4 of the
+// word index are XORed with the row's 16-row group.
+__device__ __forceinline__ int swz(int row, int word) { return word ^ (((row >> 4) & 7) << 2); }
+
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d) {
+    // cvt packs its first source operand into the upper byte of each pair.
+    uint16_t lo, hi;
+    if (FMT == FP8LIN_E4M3) {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    } else {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    }
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int FMT>
+__device__ __forceinline__ uint2 cast8(uint4 v, float s) {
+    uint2 r;
+    r.x = cvt4<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s),
+                    __fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s));
+    r.y = cvt4<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s),
+                    __fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s));
+    return r;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c, int num_tiles,
+                      float fmt_max, const float *__restrict__ amax, float *__restrict__ scale_out,
+                      float *__restrict__ inv_out, uint8_t *__restrict__ q, uint8_t *__restrict__ qT) {
+    __shared__ __align__(16) uint32_t tile[kTile][kTile / 4];
+
+    // scale = fmt_max / max(amax, 1e-12): binary32, round to nearest even.
+    float a = __ldg(amax);
+    a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
+    const float s = __fdiv_rn(fmt_max, a);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *scale_out = s;
+        *inv_out = __frcp_rn(s);
+    }
+    if ((int)blockIdx.x >= num_tiles) return;
+
+    const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+    const int r0 = tr * kTile, c0 = tc * kTile;
+    const int t = threadIdx.x;
+
+    // ---- phase 1: 128 rows x 16 chunks of 8 elements = 2048 chunks, 8 per thread
+    const int ch = t % 16;          // chunk within the row (8 columns)
+    const int row_base = t / 16;    // rows row_base + 16 i
+    const bool col_in = (c0 + ch * 8) < cols;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + row_base + 16 * i;
+        if (col_in && r < rows)
+            v[i] = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)r * cols + c0 + ch * 8));
+        else
+            v[i] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int lr = row_base + 16 * i;
+        const int r = r0 + lr;
+        const uint2 p = cast8<FMT>(v[i], s);
+        if (q != nullptr && col_in && r < rows)
+            *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + c0 + ch * 8) = p;
+        if (qT != nullptr)
+            *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = p;
+    }
+    if (qT == nullptr) return;
+    __syncthreads();
+
+    // ---- phase 2: warp w owns columns 16w..16w+15; lane (rc, cq) owns rows
+    // 16 rc .. 16 rc + 15 of columns 16 w + 4 cq .. + 3.
+    const int w = t / 32, lane = t % 32;
+    const int rc = lane % 8, cq = lane / 8;
+    const int word = 4 * w + cq;
+    uint32_t rw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int lr = 16 * rc + i;
+        rw[i] = tile[lr][swz(lr, word)];
+    }
+    // out[j][k]: column j, rows 4k .. 4k+3 (byte b = row 4k+b)
+    uint32_t out[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t a0 = rw[4 * k], a1 = rw[4 * k + 1], a2 = rw[4 * k + 2], a3 = rw[4 * k + 3];
+        const uint32_t t0 = __byte_perm(a0, a1, 0x5140);  // a0.b0 a1.b0 a0.b1 a1.b1
+        const uint32_t t1 = __byte_perm(a2, a3, 0x5140);  // a2.b0 a3.b0 a2.b1 a3.b1
+        const uint32_t t2 = __byte_perm(a0, a1, 0x7362);  // a0.b2 a1.b2 a0.b3 a1.b3
+        const uint32_t t3 = __byte_perm(a2, a3, 0x7362);  // a2.b2 a3.b2 a2.b3 a3.b3
+        out[0][k] = __byte_perm(t0, t1, 0x5410);
+        out[1][k] = __byte_perm(t0, t1, 0x7632);
+        out[2][k] = __byte_perm(t2, t3, 0x5410);
+        out[3][k] = __byte_perm(t2, t3, 0x7632);
+    }
+    const int rr = r0 + 16 * rc;
+    if (rr < rows) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + 16 * w + 4 * cq + j;
+            if (c < cols)
+                *reinterpret_cast<uint4 *>(qT + (int64_t)c * rows + rr) =
+                    make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                               float fmt_max, const float *amax, float *scale,
+                                               float *inv_scale, uint8_t *q, uint8_t *qT,
+                                               cudaStream_t stream) {
+    using namespace fp8lin;
+    if (amax == nullptr || scale == nullptr || inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return FP8LIN_ERR_INVALID_ARG;
+    if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
+    if (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f)) return FP8LIN_ERR_INVALID_ARG;
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(amax, 4) || !aligned(scale, 4) || !aligned(inv_scale, 4)) return FP8LIN_ERR_MISALIGNED;
+    if (!empty && (!aligned(x, 16) || !aligned(q, 16) || !aligned(qT, 16))) return FP8LIN_ERR_MISALIGNED;
+    if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    const int64_t num_tiles = empty ? 0 : tiles_r * tiles_c;
+    if (num_tiles > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    const int grid = num_tiles > 0 ? (int)num_tiles : 1;  // one CTA publishes the scale
+    const int tc = tiles_c > 0 ? (int)tiles_c : 1;
+    const uint16_t *xs = static_cast<const uint16_t *>(x);
+    if (fmt == FP8LIN_E4M3)
+        cast_transpose_kernel<FP8LIN_E4M3><<<grid, kThreads, 0, stream>>>(
+            xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max, amax, scale, inv_scale, q, qT);
+    else
+        cast_transpose_kernel<FP8LIN_E5M2><<<grid, kThreads, 0, stream>>>(
+            xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max, amax, scale, inv_scale, q, qT);
+    return check_launch();
+}

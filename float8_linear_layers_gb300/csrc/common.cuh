@@ -1,0 +1,31 @@
+// common.cuh -- host-side argument checks and per-device facts shared by the
+// translation units of libfp8lin.  Device code lives with its kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fp8lin.h"
+
+namespace fp8lin {
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline bool dim_ok(int64_t d) { return d >= 0 && d <= FP8LIN_MAX_DIM; }
+
+// Map the last CUDA error (launch configuration, invalid handle, ...) to a status.
+inline fp8lin_status check_launch() {
+    return cudaGetLastError() == cudaSuccess ? FP8LIN_OK : FP8LIN_ERR_CUDA;
+}
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+};
+
+// Facts about the current device, cached per device ordinal.
+fp8lin_status current_device(DeviceInfo *info);
+
+}  // namespace fp8lin

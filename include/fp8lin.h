@@ -1,0 +1,179 @@
+/*
+ * fp8lin.h -- C ABI of the Float8 linear layer hot path for one GB300 GPU
+ * (sm_103a): dynamic per-tensor scaling and the three scaled FP8 GEMMs of a
+ * linear layer's forward and backward pass.
+ *
+ * Source of the method: "TorchTitan: a one-stop PyTorch-native solution for
+ * production LLM pre-training" (zenmind.me paper analysis), section 3.3
+ * "Memory and compute optimisations", bullet "Mixed precision and Float8":
+ * Float8 is a derived dtype applied selectively to linear layers, with
+ * dynamic / delayed / static per-tensor scaling, composable with autograd.
+ * "Lecture 9 exercises" (juanwang-buaa tutorials), the answer on fp16 loss
+ * scaling versus FP8 scaling: FP8 scaling is one factor per tensor, and FP8
+ * saves only what is stored in FP8 (the FP8 copies are what the backward
+ * pass keeps).  The pages fix neither the formats nor the arithmetic; this
+ * library takes e4m3 for activations and weights, e5m2 for output
+ * gradients, scale = fmt_max / amax (fmt_max = 448), a saturating
+ * round-to-nearest-even cast, fp32 accumulation and the inverse scales
+ * applied to the fp32 accumulator before the bf16 store.
+ *
+ * Conventions (nn.Linear):  X is [M x K] (tokens x in-features), W is
+ * [N x K] (out-features x in-features), dY is [M x N]; every matrix is
+ * row-major.  One linear's step is
+ *     forward : fp8lin_amax(X), fp8lin_amax(W),
+ *               fp8lin_cast_transpose(X -> Xq, XqT), (W -> Wq, WqT),
+ *               fp8lin_fwd(Xq, Wq) -> Y
+ *     backward: fp8lin_amax(dY), fp8lin_cast_transpose(dY -> dYq, dYqT),
+ *               fp8lin_dgrad(dYq, WqT) -> dX, fp8lin_wgrad(dYqT, XqT) -> dW
+ *
+ * Ownership: the caller allocates and owns every buffer (device memory),
+ * including the one-float amax / scale / inverse-scale slots.  No entry
+ * point allocates device memory; the GEMM kernels allocate and free tensor
+ * memory (TMEM) on chip inside the kernel.
+ *
+ * Synchronisation: every call is asynchronous on `stream` (a CUDA stream of
+ * the current device; 0 = legacy default stream).  Scales never leave the
+ * device, so no call synchronises with the host.  Calls on one stream run in
+ * order; the caller orders calls across streams.
+ *
+ * Errors: argument checks run on the host before anything is launched.  A
+ * failed check returns its status and launches nothing.  A launch failure
+ * returns FP8LIN_ERR_CUDA.  Faults inside a kernel surface, as usual with
+ * CUDA, at the caller's next synchronisation.  Every wait inside the GEMM
+ * kernels is bounded in time: a wait that runs out makes the kernel stop
+ * cleanly and record FP8LIN_ERR_TIMEOUT in a device word that
+ * fp8lin_device_error() reads back.
+ */
+#ifndef FP8LIN_H
+#define FP8LIN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8lin_status {
+    FP8LIN_OK = 0,
+    FP8LIN_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, bad format or fmt_max */
+    FP8LIN_ERR_MISALIGNED = 2,         /* a pointer breaks the alignment stated on the call  */
+    FP8LIN_ERR_UNSUPPORTED_SHAPE = 3,  /* a dimension is not a multiple of 16 or too large   */
+    FP8LIN_ERR_CUDA = 4,               /* the CUDA runtime reported an error                 */
+    FP8LIN_ERR_TIMEOUT = 5,            /* a bounded wait inside a kernel ran out             */
+    FP8LIN_ERR_UNSUPPORTED_DEVICE = 6  /* the current device is not compute capability 10.3  */
+} fp8lin_status;
+
+typedef enum fp8lin_fmt {
+    FP8LIN_E4M3 = 0,  /* 1-4-3, bias 7, no Inf, largest finite 448 (activations, weights) */
+    FP8LIN_E5M2 = 1   /* 1-5-2, bias 15, largest finite 57344 (output gradients)          */
+} fp8lin_fmt;
+
+/* Largest dimension accepted by any call (rows, columns, M, N or K). */
+#define FP8LIN_MAX_DIM ((int64_t)1 << 30)
+
+/*
+ * amax of one bf16 tensor: *amax = max_i |x_i| (fp32, exact).
+ * Dynamic per-tensor scaling takes this statistic of the tensor itself each
+ * step (TorchTitan analysis page, section 3.3, "Mixed precision and Float8";
+ * Lecture 9 exercises, FP8 scaling is one factor per tensor).
+ *
+ *   x      device, n bf16 values, contiguous, 16-byte aligned.
+ *   n      element count, >= 0 (n == 0 gives amax = 0).
+ *   amax   device, one float, 4-byte aligned.  Overwritten: the call clears
+ *          it on `stream` before the reduction.
+ * Magnitudes are ordered like the IEEE 754 totalOrder predicate: a NaN in x
+ * gives a NaN amax, an infinity gives +Inf.
+ */
+fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cudaStream_t stream);
+
+/*
+ * Scale and cast one bf16 matrix to FP8, writing the row-major copy and/or
+ * its transpose (the copy whose contiguous index is the row index), so that
+ * each GEMM reads both operands with the contraction index contiguous.
+ * Source: the Float8 derived dtype (TorchTitan analysis page, section 3.3).
+ *
+ *   x          device, bf16 [rows x cols] row-major, 16-byte aligned.
+ *   rows, cols >= 0, multiples of 16, <= FP8LIN_MAX_DIM.
+ *   fmt        FP8LIN_E4M3 (X, W) or FP8LIN_E5M2 (dY).
+ *   fmt_max    finite, > 0: the scale's numerator (448 for all three tensors).
+ *   amax       device, one float written by fp8lin_amax (read only).
+ *   scale      device, one float: receives fmt_max / max(amax, 1e-12) (fp32,
+ *              round to nearest even).
+ *   inv_scale  device, one float: receives 1 / scale (fp32 RN), the factor
+ *              the GEMM epilogues apply.
+ *   q          device, u8 [rows x cols] or NULL; 16-byte aligned.
+ *   qT         device, u8 [cols x rows] or NULL; 16-byte aligned.
+ * Every code is sat_RNE(fp32(x) * scale): the binary32 product rounded to
+ * nearest even, then rounded to nearest even into the format, saturating at
+ * the format's largest finite value (Inf included); NaN stays NaN; the sign
+ * of zero is kept.  A NaN amax gives a NaN scale.
+ */
+fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols,
+                                    fp8lin_fmt fmt, float fmt_max, const float *amax,
+                                    float *scale, float *inv_scale,
+                                    uint8_t *q, uint8_t *qT, cudaStream_t stream);
+
+/*
+ * Forward GEMM of the Float8 linear: Y = bf16_RN( (Xq . Wq^T)_fp32 * (inv_x * inv_w) ).
+ * Source: Float8 applied to the linear layer's matmul (TorchTitan analysis
+ * page, section 3.3).
+ *
+ *   xq     device, e4m3 [M x K] row-major (K contiguous), 16-byte aligned.
+ *   inv_x  device, one float (inverse scale of X).
+ *   wq     device, e4m3 [N x K] row-major, 16-byte aligned.
+ *   inv_w  device, one float (inverse scale of W).
+ *   y      device, bf16 [M x N] row-major, 16-byte aligned; fully overwritten.
+ *   M, N, K  >= 0, multiples of 16, <= FP8LIN_MAX_DIM.  K == 0 writes zeros.
+ */
+fp8lin_status fp8lin_fwd(const uint8_t *xq, const float *inv_x, const uint8_t *wq,
+                         const float *inv_w, void *y, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream);
+
+/*
+ * Input-gradient GEMM: dX = bf16_RN( (dYq . WqT^T)_fp32 * (inv_dy * inv_w) ),
+ * i.e. dY . W.  Source: the backward pass of the Float8 linear through
+ * autograd (TorchTitan analysis page, section 3.3).
+ *
+ *   dyq     device, e5m2 [M x N] row-major (N contiguous), 16-byte aligned.
+ *   inv_dy  device, one float.
+ *   wqT     device, e4m3 [K x N] (the transposed copy of Wq), 16-byte aligned.
+ *   inv_w   device, one float.
+ *   dx      device, bf16 [M x K] row-major, 16-byte aligned; fully overwritten.
+ *   M, N, K  as for fp8lin_fwd.  N == 0 writes zeros.
+ */
+fp8lin_status fp8lin_dgrad(const uint8_t *dyq, const float *inv_dy, const uint8_t *wqT,
+                           const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t stream);
+
+/*
+ * Weight-gradient GEMM: dW = bf16_RN( (dYqT . XqT^T)_fp32 * (inv_dy * inv_x) ),
+ * i.e. dY^T . X.  Source: as for fp8lin_dgrad.
+ *
+ *   dyqT    device, e5m2 [N x M] (the transposed copy of dYq), 16-byte aligned.
+ *   inv_dy  device, one float.
+ *   xqT     device, e4m3 [K x M] (the transposed copy of Xq), 16-byte aligned.
+ *   inv_x   device, one float.
+ *   dw      device, bf16 [N x K] row-major, 16-byte aligned; fully overwritten.
+ *   M, N, K  as for fp8lin_fwd.  M == 0 writes zeros.
+ */
+fp8lin_status fp8lin_wgrad(const uint8_t *dyqT, const float *inv_dy, const uint8_t *xqT,
+                           const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
+                           cudaStream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char *fp8lin_status_str(fp8lin_status status);
+
+/*
+ * Read and clear the device word in which a GEMM kernel records a bounded
+ * wait that ran out.  Synchronises `stream` first.  Returns FP8LIN_OK when
+ * no kernel timed out since the last call, FP8LIN_ERR_TIMEOUT when one did
+ * (and writes the raw word to *word when word is not NULL).
+ */
+fp8lin_status fp8lin_device_error(cudaStream_t stream, uint32_t *word);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8LIN_H */

@@ -1,0 +1,90 @@
+"""The C ABI on the host: the library loads without a GPU, exports every
+entry point include/fp8lin.h declares, and rejects bad arguments before
+touching CUDA (no GPU needed: argument checks run first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "fp8lin.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
+    return ctypes.CDLL(path)
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8lin_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_entry_points()
+    for n in ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), f"{name} declared in fp8lin.h but not exported"
+
+
+def test_binding_lists_every_declared_symbol(lib):
+    import float8_linear_layers_gb300 as fl
+    assert sorted(fl.ENTRY_POINTS) == declared_entry_points()
+
+
+def test_status_strings(lib):
+    lib.fp8lin_status_str.restype = ctypes.c_char_p
+    for s in range(7):
+        assert lib.fp8lin_status_str(s)
+    assert b"unknown" in lib.fp8lin_status_str(99)
+
+
+def _c(lib, name, *args):
+    fn = getattr(lib, name)
+    fn.restype = ctypes.c_int
+    return fn(*args)
+
+
+V = ctypes.c_void_p
+I = ctypes.c_int64
+F = ctypes.c_float
+
+
+def test_argument_checks_without_gpu(lib):
+    a16 = V(4096)      # 16-byte-aligned fake addresses: never dereferenced on these paths
+    a4 = V(4100)
+    # amax: null out / negative n / misaligned input
+    assert _c(lib, "fp8lin_amax", a16, I(16), V(0), V(0)) == 1
+    assert _c(lib, "fp8lin_amax", a16, I(-1), a16, V(0)) == 1
+    assert _c(lib, "fp8lin_amax", V(4098), I(16), a16, V(0)) == 2
+    assert _c(lib, "fp8lin_amax", a16, I(16), V(4098), V(0)) == 2
+    # cast: bad format, bad fmt_max, shape not a multiple of 16, misaligned
+    ct = lib.fp8lin_cast_transpose
+    ct.restype = ctypes.c_int
+    ct.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V, V]
+    assert ct(a16, 32, 32, 2, 448.0, a16, a16, a16, a16, a16, None) == 1
+    assert ct(a16, 32, 32, 0, 0.0, a16, a16, a16, a16, a16, None) == 1
+    assert ct(a16, 32, 32, 0, float("nan"), a16, a16, a16, a16, a16, None) == 1
+    assert ct(a16, 32, 24, 0, 448.0, a16, a16, a16, a16, a16, None) == 3
+    assert ct(a16, 1 << 31, 32, 0, 448.0, a16, a16, a16, a16, a16, None) == 3
+    assert ct(a16, 32, 32, 0, 448.0, a16, a16, a16, a4, a16, None) == 2
+    assert ct(a16, 32, 32, 0, 448.0, None, a16, a16, a16, a16, None) == 1
+    # GEMMs: null scales, misaligned operand, ragged dims
+    for name in ("fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [V, V, V, V, V, I, I, I, V]
+        assert fn(a16, None, a16, a16, a16, 128, 128, 128, None) == 1
+        assert fn(a16, a16, a16, a16, a16, -16, 128, 128, None) == 1
+        assert fn(a4, a16, a16, a16, a16, 128, 128, 128, None) == 2
+        assert fn(a16, a16, a16, a16, a16, 128, 120, 128, None) == 3
+        assert fn(a16, a16, a16, a16, a16, 128, 128, 8, None) == 3

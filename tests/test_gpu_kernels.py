@@ -1,0 +1,256 @@
+"""Parity of each CUDA kernel with the CPU oracle, through the C ABI, on
+seeded inputs that span several tiles and ragged tails, plus edge cases.
+
+Bar: amax, scale, inverse scale and every FP8 byte bit-exact; GEMM outputs
+within |y - ref| <= 2^-7 |ref| + 1e-3 rms(ref) elementwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import (Guarded, assert_gemm_close, bf16_to_f64, f32_bits, scalar_bits,
+                         to_dev_bf16, to_dev_u8)
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+
+
+# ------------------------------------------------------------------ amax
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, 4096 * 3 + 5, 1 << 20, (1 << 22) + 24])
+def test_amax_bit_exact(fp8lin, n):
+    x = wl.generate((n,), "normal", 1.0, 17, n % 1000)
+    amax = torch.full((1,), -1.0, device="cuda")
+    fp8lin.fp8lin_amax(to_dev_bf16(x), amax)
+    assert scalar_bits(amax) == f32_bits(oracle.amax(x))
+
+
+def test_amax_empty_and_special_values(fp8lin):
+    amax = torch.full((1,), 7.0, device="cuda")
+    fp8lin.fp8lin_amax(torch.empty(0, dtype=torch.bfloat16, device="cuda"), amax)
+    assert amax.item() == 0.0
+    cases = [
+        np.array([0x0000, 0x8000] * 20, np.uint16),                       # +-0
+        np.array([0x0001, 0x8003, 0x0002] * 11, np.uint16),               # bf16 subnormals
+        np.array([0x3F80] * 100 + [0xC2C8] + [0x3F80] * 37, np.uint16),   # single negative extreme
+        np.array([0x3F80, 0x7F80, 0xC000] * 9, np.uint16),                # +Inf
+        np.array([0x3F80, 0x7F80, 0xFFC1, 0x7FC0] * 9, np.uint16),        # NaNs above Inf
+    ]
+    for x in cases:
+        fp8lin.fp8lin_amax(to_dev_bf16(x), amax)
+        assert scalar_bits(amax) == f32_bits(oracle.amax(x))
+
+
+def test_amax_every_bf16_pattern(fp8lin):
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = x[(x & 0x7FFF) < 0x7F80]
+    amax = torch.zeros(1, device="cuda")
+    for arr in (finite, x):
+        fp8lin.fp8lin_amax(to_dev_bf16(arr), amax)
+        assert scalar_bits(amax) == f32_bits(oracle.amax(arr))
+
+
+# ------------------------------------------------------------------ cast
+
+CAST_SHAPES = [(16, 16), (128, 128), (144, 272), (256, 512), (384, 1040), (1040, 384), (2048, 4096)]
+
+
+def _run_cast(fp8lin, x_bits, fmt, fmt_max=448.0, want_q=True, want_qT=True):
+    rows, cols = x_bits.shape
+    x = to_dev_bf16(x_bits)
+    amax = torch.zeros(1, device="cuda")
+    scale = torch.full((1,), -1.0, device="cuda")
+    inv = torch.full((1,), -1.0, device="cuda")
+    q = Guarded((rows, cols), torch.uint8) if want_q else None
+    qT = Guarded((cols, rows), torch.uint8) if want_qT else None
+    fp8lin.fp8lin_amax(x, amax)
+    fp8lin.fp8lin_cast_transpose(x, fmt, amax, scale, inv, q.t if q else None, qT.t if qT else None,
+                                 fmt_max)
+    torch.cuda.synchronize()
+    return amax, scale, inv, q, qT
+
+
+@pytest.mark.parametrize("shape", CAST_SHAPES)
+@pytest.mark.parametrize("fmt,dist", [(E4M3, ("normal", 1.0)), (E4M3, ("normal", 0.02)),
+                                      (E5M2, ("normal", 1e-3)), (E5M2, ("laplace", 1e-3))])
+def test_cast_transpose_bit_exact(fp8lin, shape, fmt, dist):
+    x = wl.generate(shape, *dist, seed=shape[0] + shape[1], tensor_id=fmt)
+    amax, scale, inv, q, qT = _run_cast(fp8lin, x, fmt)
+    ref = oracle.quantize(x, fmt)
+    assert scalar_bits(amax) == f32_bits(ref["amax"])
+    assert scalar_bits(scale) == f32_bits(ref["scale"])
+    assert scalar_bits(inv) == f32_bits(ref["inv_scale"])
+    assert np.array_equal(q.t.cpu().numpy(), ref["q"])
+    assert np.array_equal(qT.t.cpu().numpy(), ref["qT"])
+    assert q.intact() and qT.intact()
+
+
+@pytest.mark.parametrize("fmt,fmt_max", [(E4M3, 448.0), (E5M2, 448.0), (E5M2, 57344.0)])
+def test_cast_every_bf16_pattern(fp8lin, fmt, fmt_max):
+    """All 65,536 bf16 patterns as one 256 x 256 tensor, cast with the scale
+    from a fixed amax (so the scale is not dominated by NaN/Inf)."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+    xd = to_dev_bf16(x)
+    for amax_value in (448.0, 3.0, 1e-3, 5.0e4):
+        amax = torch.tensor([amax_value], dtype=torch.float32, device="cuda")
+        scale = torch.zeros(1, device="cuda")
+        inv = torch.zeros(1, device="cuda")
+        q = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+        qT = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+        fp8lin.fp8lin_cast_transpose(xd, fmt, amax, scale, inv, q, qT, fmt_max)
+        s, i = oracle.scale(np.float32(amax_value), fmt_max)
+        assert scalar_bits(scale) == f32_bits(s) and scalar_bits(inv) == f32_bits(i)
+        ref = oracle.cast(x, fmt, s)
+        got = q.cpu().numpy()
+        xf = wl.bf16_bits_to_f32(x)
+        nan_in = np.isnan(xf)
+        table = oracle.decode_table(fmt)
+        assert np.isnan(table[got[nan_in]]).all()          # NaN stays NaN (any NaN code)
+        assert np.array_equal(got[~nan_in], ref[~nan_in])
+        assert np.array_equal(qT.cpu().numpy(), got.T)
+
+
+def test_cast_zero_tensor_and_one_sided_outputs(fp8lin):
+    x = np.zeros((64, 96), np.uint16)
+    x[3, 5] = 0x8000  # -0
+    amax, scale, inv, q, qT = _run_cast(fp8lin, x, E4M3)
+    ref = oracle.quantize(x, E4M3)
+    assert amax.item() == 0.0 and scalar_bits(scale) == f32_bits(ref["scale"])
+    assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and q.t.cpu().numpy()[3, 5] == 0x80
+    y = wl.generate((160, 208), "normal", 1.0, 5, 0)
+    ref = oracle.quantize(y, E5M2)
+    _, _, _, q, qT = _run_cast(fp8lin, y, E5M2, want_qT=False)
+    assert qT is None and np.array_equal(q.t.cpu().numpy(), ref["q"]) and q.intact()
+    _, _, _, q, qT = _run_cast(fp8lin, y, E5M2, want_q=False)
+    assert q is None and np.array_equal(qT.t.cpu().numpy(), ref["qT"]) and qT.intact()
+
+
+def test_cast_empty_matrix_still_publishes_scale(fp8lin):
+    x = torch.empty((0, 32), dtype=torch.bfloat16, device="cuda")
+    amax = torch.tensor([2.0], device="cuda")
+    scale = torch.zeros(1, device="cuda")
+    inv = torch.zeros(1, device="cuda")
+    fp8lin.fp8lin_cast_transpose(x, E4M3, amax, scale, inv, None, None)
+    assert scale.item() == 224.0 and scalar_bits(inv) == f32_bits(oracle.scale(2.0)[1])
+
+
+def test_cast_amax_invariant(fp8lin):
+    x = wl.generate((512, 384), "normal", 1.0, 8, 0, outlier_frac=1e-3)
+    _, _, _, q, _ = _run_cast(fp8lin, x, E4M3)
+    xf = wl.bf16_bits_to_f32(x)
+    at = np.abs(xf) == np.abs(xf).max()
+    qq = q.t.cpu().numpy()
+    assert np.all((qq[at] & 0x7F) == 0x7E)
+
+
+# ------------------------------------------------------------------ GEMMs
+
+def _codes(shape, fmt, seed):
+    """FP8 operands as the oracle's cast makes them from seeded bf16 input."""
+    dist = ("normal", 1.0) if fmt == E4M3 else ("laplace", 1e-3)
+    x = wl.generate(shape, *dist, seed=seed, tensor_id=7)
+    r = oracle.quantize(x, fmt)
+    return r["q"], r["inv_scale"]
+
+
+GEMM_SHAPES = [(16, 16, 16), (128, 256, 128), (256, 1024, 512), (144, 272, 208),
+               (384, 1040, 4112), (1040, 400, 96), (2048, 2048, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("which", ["fwd", "dgrad", "wgrad"])
+def test_gemm_matches_oracle(fp8lin, M, N, K, which):
+    seed = M * 7 + N * 3 + K
+    if which == "fwd":      # Y[M,N] = Xq[M,K] . Wq[N,K]^T
+        P, Q, R, fa = M, N, K, E4M3
+    elif which == "dgrad":  # dX[M,K] = dYq[M,N] . WqT[K,N]^T
+        P, Q, R, fa = M, K, N, E5M2
+    else:                   # dW[N,K] = dYqT[N,M] . XqT[K,M]^T
+        P, Q, R, fa = N, K, M, E5M2
+    A, ia = _codes((P, R), fa, seed)
+    B, ib = _codes((Q, R), E4M3, seed + 1)
+    out = Guarded((P, Q), torch.bfloat16)
+    out.t.fill_(float("nan"))
+    a, b = to_dev_u8(A), to_dev_u8(B)
+    sa = torch.tensor([ia], dtype=torch.float32, device="cuda")
+    sb = torch.tensor([ib], dtype=torch.float32, device="cuda")
+    getattr(fp8lin, "fp8lin_" + which)(a, sa, b, sb, out.t)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    ref = oracle.gemm_rows(A, fa, B, E4M3, ia, ib)
+    assert_gemm_close(bf16_to_f64(out.t), ref, f"{which} {M}x{N}x{K}")
+    assert out.intact()
+
+
+def test_gemm_empty_dimensions(fp8lin):
+    z = torch.zeros(1, device="cuda")
+    y = torch.full((32, 48), 3.0, dtype=torch.bfloat16, device="cuda")
+    e = torch.empty((32, 0), dtype=torch.uint8, device="cuda")
+    f = torch.empty((48, 0), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_fwd(e, z, f, z, y)          # K = 0: Y = 0
+    assert (y == 0).all()
+    y0 = torch.empty((0, 48), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_fwd(torch.empty((0, 32), dtype=torch.uint8, device="cuda"), z,
+                      torch.empty((48, 32), dtype=torch.uint8, device="cuda"), z, y0)
+    torch.cuda.synchronize()
+
+
+def test_gemm_closed_forms(fp8lin):
+    # one-hot rows of A pick columns of B; all-ones gives K
+    K, N = 256, 272
+    A = np.zeros((K, K), np.uint8)
+    A[np.arange(K), np.arange(K)] = 0x38  # e4m3 1.0
+    B, _ = _codes((N, K), E4M3, 99)
+    one = torch.ones(1, device="cuda")
+    y = torch.empty((K, N), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_fwd(to_dev_u8(A), one, to_dev_u8(B), one, y)
+    exp = oracle.decode_table(E4M3)[B].T
+    assert np.array_equal(bf16_to_f64(y), exp)
+    ones_a = torch.full((128, 4096), 0x3C, dtype=torch.uint8, device="cuda")  # e5m2 1.0
+    ones_b = torch.full((256, 4096), 0x38, dtype=torch.uint8, device="cuda")  # e4m3 1.0
+    y = torch.empty((128, 256), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_dgrad(ones_a, one, ones_b, one, y)
+    assert (y.float() == 4096.0).all()
+
+
+# -------------------------------------------------------------- sequence
+
+@pytest.mark.parametrize("M,K,N", [(256, 512, 1024), (144, 208, 272), (640, 384, 1296)])
+def test_float8_linear_step_matches_oracle(fp8lin, M, K, N):
+    X = wl.generate((M, K), "normal", 1.0, 3, wl.X)
+    W = wl.generate((N, K), "normal", 0.02, 3, wl.W)
+    dY = wl.generate((M, N), "normal", 1e-3, 3, wl.DY)
+    lin = fp8lin.Float8Linear(M, K, N)
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    ox, ow, od = oracle.quantize(X, E4M3), oracle.quantize(W, E4M3), oracle.quantize(dY, E5M2)
+    for t8, r in ((lin.x8, ox), (lin.w8, ow), (lin.dy8, od)):
+        assert scalar_bits(t8.amax) == f32_bits(r["amax"])
+        assert scalar_bits(t8.scale) == f32_bits(r["scale"])
+        assert scalar_bits(t8.inv_scale) == f32_bits(r["inv_scale"])
+        assert np.array_equal(t8.q.cpu().numpy(), r["q"])
+        assert np.array_equal(t8.qT.cpu().numpy(), r["qT"])
+    assert_gemm_close(bf16_to_f64(y), oracle.fwd_ref(ox["q"], ox["inv_scale"], ow["q"], ow["inv_scale"]), "Y")
+    assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_ref(od["q"], od["inv_scale"], ow["qT"], ow["inv_scale"]), "dX")
+    assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_ref(od["qT"], od["inv_scale"], ox["qT"], ox["inv_scale"]), "dW")
+
+
+def test_repeated_calls_and_streams(fp8lin):
+    """Same inputs on a side stream, twice: identical results."""
+    M, K, N = 256, 512, 1024
+    X = to_dev_bf16(wl.generate((M, K), "normal", 1.0, 4, 0))
+    W = to_dev_bf16(wl.generate((N, K), "normal", 0.02, 4, 1))
+    dY = to_dev_bf16(wl.generate((M, N), "normal", 1e-3, 4, 2))
+    a = fp8lin.Float8Linear(M, K, N)
+    ra = [t.clone() for t in a.step(X, W, dY)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    b = fp8lin.Float8Linear(M, K, N)
+    with torch.cuda.stream(s):
+        b.step(X, W, dY, stream=s)
+        rb = [t.clone() for t in b.step(X, W, dY, stream=s)]
+    torch.cuda.synchronize()
+    for u, v in zip(ra, rb):
+        assert torch.equal(u, v)
