@@ -3,22 +3,26 @@
 // analysis page, section 3.3, "Mixed precision and Float8").
 //
 // HBM-bound: 2 bytes read per element, nothing else.  Design:
-//  * grid sized to the SM count x resident blocks, grid-stride over 16-byte
-//    vectors (8 bf16) with four independent loads in flight per thread;
+//  * one block per 32 KB chunk (256 threads x eight 16-byte vectors), all
+//    eight loads of a thread issued before any is used, so up to eight
+//    resident blocks keep ~256 KB of reads in flight per SM;
 //  * |x| is the bf16 pattern with the sign bit cleared; non-negative IEEE
 //    patterns order like unsigned integers (NaN above Inf above finite, the
 //    totalOrder of magnitudes), so the reduction runs on packed 16-bit
 //    unsigned maxima (vmaxu2) and never converts to float;
-//  * warp reduction with redux.sync, block reduction through shared memory,
-//    one atomicMax per block on the fp32 bit pattern (bf16 << 16).
+//  * warp reduction with redux.sync, block reduction through shared memory;
+//    a block issues its atomicMax on the fp32 bit pattern (bf16 << 16) only
+//    when its maximum exceeds the value already there, so the thousands of
+//    blocks of a large tensor do not serialise on one address.
 #include <cstdint>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kUnroll = 4;
+constexpr int kThreads = 256;
+constexpr int kVec = 8;                       // 16-byte vectors per thread
+constexpr int kChunk = kThreads * kVec;       // vectors per block (32 KB)
 
 __device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
     uint4 v;
@@ -40,19 +44,22 @@ __device__ __forceinline__ uint32_t absmax4(uint32_t m, uint4 v) {
 __global__ void __launch_bounds__(kThreads)
 amax_bf16_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restrict__ tail,
                  int ntail, unsigned int *__restrict__ amax_bits) {
+    const int64_t base = (int64_t)blockIdx.x * kChunk + threadIdx.x;
     uint32_t m = 0;  // two packed 16-bit magnitudes
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
-        uint4 v[kUnroll];
+    if (base + (int64_t)(kVec - 1) * kThreads < nvec) {
+        uint4 v[kVec];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream16(x + i + u * stride);
+        for (int u = 0; u < kVec; ++u) v[u] = ld_stream16(x + base + (int64_t)u * kThreads);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) m = absmax4(m, v[u]);
+        for (int u = 0; u < kVec; ++u) m = absmax4(m, v[u]);
+    } else {
+        for (int u = 0; u < kVec; ++u) {
+            const int64_t i = base + (int64_t)u * kThreads;
+            if (i < nvec) m = absmax4(m, ld_stream16(x + i));
+        }
     }
-    for (; i < nvec; i += stride) m = absmax4(m, ld_stream16(x + i));
     uint32_t r = max(m & 0xFFFFu, m >> 16);
-    if (blockIdx.x == 0 && threadIdx.x < ntail) r = max(r, (uint32_t)(tail[threadIdx.x] & 0x7FFFu));
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x < ntail) r = max(r, (uint32_t)(tail[threadIdx.x] & 0x7FFFu));
 
     r = __reduce_max_sync(0xFFFFFFFFu, r);
     __shared__ uint32_t warp_max[kThreads / 32];
@@ -62,7 +69,11 @@ amax_bf16_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__re
     if (warp == 0) {
         r = lane < kThreads / 32 ? warp_max[lane] : 0u;
         r = __reduce_max_sync(0xFFFFFFFFu, r);
-        if (lane == 0 && r != 0) atomicMax(amax_bits, r << 16);
+        if (lane == 0 && r != 0) {
+            const uint32_t bits = r << 16;
+            // a relaxed read first: most blocks find a larger value already there
+            if (bits > *reinterpret_cast<volatile unsigned int *>(amax_bits)) atomicMax(amax_bits, bits);
+        }
     }
 }
 
@@ -81,9 +92,9 @@ extern "C" fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cuda
     const int64_t nvec = n / 8;
     const int ntail = (int)(n % 8);
     const uint16_t *tail = static_cast<const uint16_t *>(x) + nvec * 8;
-    int64_t want = (nvec + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
-    int64_t cap = (int64_t)dev.sm_count * (2048 / kThreads);  // one full wave of resident blocks
-    int grid = (int)(want < 1 ? 1 : (want < cap ? want : cap));
+    const int64_t blocks = (nvec + kChunk - 1) / kChunk;
+    if (blocks > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    const int grid = blocks < 1 ? 1 : (int)blocks;
     amax_bf16_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint4 *>(x), nvec, tail, ntail,
                                                     reinterpret_cast<unsigned int *>(amax));
     return check_launch();
