@@ -11,26 +11,34 @@
 //     wgrad : dW [N x K] = dYqT [N x M] . XqT [K x M]^T    e5m2 x e4m3
 // and the epilogue computes C = bf16_RN(acc_fp32 * (inv_a * inv_b)).
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0      TMA producer: 2-D tiled bulk-tensor loads of 128 x 128-byte
-//               A and 256 x 128-byte B boxes, 128-byte swizzle, into a
-//               4-stage shared-memory ring guarded by full/empty mbarriers;
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
-//               accumulators); one thread issues tcgen05.mma kind::f8f6f4
-//               (M = 128, N = 256, K = 32 per instruction, 4 per stage) and
-//               tcgen05.commit frees each stage and publishes each finished
-//               accumulator;
+// Kernel structure: clusters of two CTAs (one per SM of a pair), persistent,
+// 192 threads per CTA.  A CTA pair owns a 256 x 256 output tile and computes
+// it with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 32 per
+// instruction): CTA r of the pair holds rows [128 r, 128 r + 128) of the A
+// slab and rows [128 r, 128 r + 128) of the B slab in its own shared memory,
+// and each SM's tensor core writes its 128 accumulator rows into its own
+// TMEM.  Per CTA:
+//   warp 0      TMA producer: 2-D tiled bulk-tensor loads of 128 x 128-byte A
+//               and B boxes (128-byte swizzle) into a 6-stage ring; both
+//               CTAs' loads complete on the leader CTA's full barrier;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//               collectively with the peer CTA; in the leader CTA one thread
+//               issues the MMAs (four per 128-byte slab) and multicasts each
+//               tcgen05.commit to both CTAs' empty / accumulator barriers;
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, scale,
-//               round to bf16, 16-byte stores; the accumulator is handed back
-//               as soon as it is read, so the epilogue of tile i overlaps the
-//               main loop of tile i + 1.
-// Tiles are visited in groups of kGroupM row-blocks so that concurrently
-// running CTAs share A and B panels in L2.
+//               round to bf16, 16-byte stores; each warp then arrives on the
+//               leader's accumulator-empty barrier, so the epilogue of tile i
+//               overlaps the main loop of tile i + 1.
+// Halving the B bytes per CTA (32 KB per slab instead of 48 KB for a
+// 128 x 256 single-CTA tile) cuts the L2 -> SM traffic per flop by a third
+// and leaves room for six stages.  Pair tiles are visited in groups of
+// kGroupM row-blocks so that concurrently running pairs share panels in L2.
 //
 // Every mbarrier wait is bounded by wall-clock time (globaltimer).  A wait
-// that runs out records FP8LIN_ERR_TIMEOUT in a device word, raises a
-// shared abort flag that ends every role's loop, drains the copies and MMAs
-// still in flight (again with bounded waits) and frees TMEM before exiting.
+// that runs out records FP8LIN_ERR_TIMEOUT in a device word, raises the
+// CTA's abort flag, which ends every role's loop, drains the copies and MMAs
+// still in flight (again with bounded waits), and the pair frees TMEM after
+// a cluster barrier.
 #include <atomic>
 #include <cstdint>
 #include <cuda.h>
@@ -41,16 +49,18 @@
 
 namespace {
 
-constexpr int kBM = 128;              // rows of A per tile (UMMA M)
-constexpr int kBN = 256;              // rows of B per tile (UMMA N)
+constexpr int kPairM = 256;           // output rows per CTA pair (UMMA M, cta_group::2)
+constexpr int kPairN = 256;           // output columns per CTA pair (UMMA N)
+constexpr int kBM = kPairM / 2;       // A rows held by each CTA
+constexpr int kBN = kPairN / 2;       // B rows held by each CTA
 constexpr int kBK = 128;              // contraction bytes per stage (one 128-byte swizzle row)
 constexpr int kUmmaK = 32;            // contraction elements per tcgen05.mma for 8-bit types
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kAStage = kBM * kBK;    // 16 KB
-constexpr int kBStage = kBN * kBK;    // 32 KB
+constexpr int kBStage = kBN * kBK;    // 16 KB
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 2 * kBN;    // two fp32 accumulators
-constexpr int kGroupM = 16;
+constexpr int kTmemCols = 2 * kPairN; // two fp32 accumulators of 256 columns
+constexpr int kGroupM = 8;            // pair-tile rows per raster group
 constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 1024 /*barriers*/ + 1024 /*alignment*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
@@ -73,10 +83,6 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -113,15 +119,6 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0,
-                                            int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -148,19 +145,58 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
-__device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address, in the shared::cluster window, of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Arrive on an mbarrier of either CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier of either CTA of the pair (the leader's, for the pair's MMA).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t cluster_bar,
+                                                 int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+// Arrive (once) on the mbarrier at this shared offset in every CTA of `mask`
+// when all MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -210,15 +246,19 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kAStage;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sB + kStages * kBStage);
-    uint64_t *full = bars;                    // [kStages] TMA bytes landed
-    uint64_t *empty = bars + kStages;         // [kStages] MMAs done reading the stage
-    uint64_t *acc_full = bars + 2 * kStages;  // [2] accumulator finished
-    uint64_t *acc_empty = acc_full + 2;       // [2] epilogue done reading the accumulator
-    uint64_t *mma_done = acc_empty + 2;       // [1] drain of outstanding MMAs
+    uint64_t *full = bars;                    // [kStages] both CTAs' slabs landed (leader's copy used)
+    uint64_t *empty = bars + kStages;         // [kStages] the pair's MMAs are done with the slab
+    uint64_t *acc_full = bars + 2 * kStages;  // [2] accumulator finished (arrived in both CTAs)
+    uint64_t *acc_empty = acc_full + 2;       // [2] both CTAs' epilogues drained it (leader's copy used)
+    uint64_t *mma_done = acc_empty + 2;       // [1] drain of outstanding MMAs (leader)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -226,7 +266,7 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
-            mbar_init(smem_u32(&acc_empty[b]), 4);  // one arrive per epilogue warp
+            mbar_init(smem_u32(&acc_empty[b]), 8);  // four epilogue warps in each CTA of the pair
         }
         mbar_init(smem_u32(mma_done), 1);
         *abort_flag = 0;
@@ -238,14 +278,16 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         prefetch_tensormap(&map_b);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        // one warp of each CTA of the pair allocates collectively
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -253,21 +295,23 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const int num_kb = (R + kBK - 1) / kBK;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t armed = 0;  // bit s: stage s has been armed at least once
-            uint32_t armed_parity = 0;
-            for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+            uint32_t armed = 0, armed_parity = 0;
+            for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
+                const int a_row = tm * kPairM + (int)rank * kBM;
+                const int b_row = tn * kPairN + (int)rank * kBN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
-                    const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_arrive_expect_tx(fb, kAStage + kBStage);
-                    tma_load_2d(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, tm * kBM);
-                    tma_load_2d(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, tn * kBN);
+                    const uint32_t fb_local = smem_u32(&full[stage]);
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
+                    const uint32_t fb = mapa_shared(fb_local, 0);
+                    tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
+                    tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -276,24 +320,24 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     }
                 }
             }
-            if (*abort_flag) {
-                // Let every copy this thread started land before the CTA exits.
+            if (*abort_flag && leader) {
+                // Let every copy of the pair land before either CTA exits.
                 for (int s = 0; s < kStages; ++s)
                     if (armed & (1u << s))
                         mbar_wait(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+            for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kPairN);
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
@@ -307,48 +351,48 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
                         // advance the start address by k * 32 bytes inside the swizzle row
                         const uint64_t off = (uint64_t)((k * kUmmaK) >> 4);
-                        umma_f8f6f4(d_tmem, a_desc + off, b_desc + off, idesc, (kb | k) != 0 ? 1u : 0u);
+                        umma_f8f6f4_pair(d_tmem, a_desc + off, b_desc + off, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    umma_commit(smem_u32(&empty[stage]));
+                    umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(&acc_full[acc]));
+                umma_commit_multicast(smem_u32(&acc_full[acc]), 0x3);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             // Every MMA issued above has completed once this arrives.
-            umma_commit(smem_u32(mma_done));
+            umma_commit_multicast(smem_u32(mma_done), 0x1);
             volatile int no_abort = 0;
             mbar_wait(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
         const int sub = warp % 4;  // TMEM sub-partition this warp may read: lanes 32 sub .. 32 sub + 31
         const float sc = __fmul_rn(__ldg(inv_a), __ldg(inv_b));
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int t = pair; t < num_tiles; t += npairs) {
             const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, kWaitLimitNs);
             // reconverge: tcgen05.ld is warp-collective (.sync.aligned)
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             int tm, tn;
             tiles.coords(t, tm, tn);
-            const int row = tm * kBM + sub * 32 + lane;
+            const int row = tm * kPairM + (int)rank * kBM + sub * 32 + lane;
             __nv_bfloat16 *crow = C + (int64_t)row * Q;
-            const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
+            const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kPairN);
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int c = 0; c < kPairN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
                 tmem_ld_wait();
-                const int col0 = tn * kBN + c * 32;
+                const int col0 = tn * kPairN + c * 32;
                 if (row < P) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
@@ -369,7 +413,7 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -379,10 +423,11 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // neither CTA frees TMEM or exits while the pair still uses its shared memory
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -424,18 +469,34 @@ bool make_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: fp32 accumulator
 // (bits 4..5 = 1), A / B formats (bits 7..9 / 10..12: 0 = e4m3, 1 = e5m2),
 // both operands K-major (bits 15, 16 = 0), N >> 3 at bits 17..22, M >> 4 at
-// bits 24..28.
+// bits 24..28; M and N are the pair's (256 x 256).
 uint32_t make_idesc(fp8lin_fmt fa, fp8lin_fmt fb) {
     uint32_t d = 0;
     d |= 1u << 4;
     d |= (uint32_t)fa << 7;
     d |= (uint32_t)fb << 10;
-    d |= (uint32_t)(kBN >> 3) << 17;
-    d |= (uint32_t)(kBM >> 4) << 24;
+    d |= (uint32_t)(kPairN >> 3) << 17;
+    d |= (uint32_t)(kPairM >> 4) << 24;
     return d;
 }
 
 std::atomic<bool> g_smem_attr_set[64];
+std::atomic<int> g_max_clusters[64];
+
+cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    attr->id = cudaLaunchAttributeClusterDimension;
+    attr->val.clusterDim.x = 2;
+    attr->val.clusterDim.y = 1;
+    attr->val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
 
 fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const uint8_t *B, fp8lin_fmt fb,
                       const float *inv_b, void *C, int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
@@ -457,7 +518,7 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         return cudaMemsetAsync(C, 0, (size_t)P * (size_t)Q * 2, stream) == cudaSuccess ? FP8LIN_OK
                                                                                        : FP8LIN_ERR_CUDA;
     }
-    const int64_t tiles_m = (P + kBM - 1) / kBM, tiles_n = (Q + kBN - 1) / kBN;
+    const int64_t tiles_m = (P + kPairM - 1) / kPairM, tiles_n = (Q + kPairN - 1) / kPairN;
     if (tiles_m * tiles_n > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
 
     CUtensorMap map_a, map_b;
@@ -469,15 +530,28 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         if (cudaFuncSetAttribute(fp8_gemm_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess)
             return FP8LIN_ERR_CUDA;
+        // pairs that can be resident at once (a GPC with an odd number of free SMs leaves one idle)
+        int clusters = 0;
+        cudaLaunchAttribute attr;
+        cudaLaunchConfig_t cfg = launch_config(2 * (dev.sm_count / 2), nullptr, &attr);
+        if (cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_tn_kernel, &cfg) != cudaSuccess || clusters < 1)
+            clusters = dev.sm_count / 2;
+        g_max_clusters[dev.device].store(clusters, std::memory_order_relaxed);
         g_smem_attr_set[dev.device].store(true, std::memory_order_release);
     }
 
     TileMap tm{(int)tiles_m, (int)tiles_n};
     const int num_tiles = (int)(tiles_m * tiles_n);
-    const int grid = num_tiles < dev.sm_count ? num_tiles : dev.sm_count;
-    fp8_gemm_tn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, static_cast<__nv_bfloat16 *>(C),
-                                                               (int)P, (int)Q, (int)R, inv_a, inv_b,
-                                                               make_idesc(fa, fb), tm);
+    const int max_pairs = g_max_clusters[dev.device].load(std::memory_order_relaxed);
+    const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = launch_config(2 * pairs, stream, &attr);
+    __nv_bfloat16 *c = static_cast<__nv_bfloat16 *>(C);
+    const int p = (int)P, q = (int)Q, r = (int)R;
+    const uint32_t idesc = make_idesc(fa, fb);
+    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel, map_a, map_b, c, p, q, r, inv_a, inv_b, idesc, tm) !=
+        cudaSuccess)
+        return FP8LIN_ERR_CUDA;
     return check_launch();
 }
 
