@@ -169,13 +169,15 @@ class OracleSample:
             D = wl.generate((w.M, w.N), *w.dy, seed=w.seed, tensor_id=did)
             qx, qw, qd = (oracle.quantize(X, oracle.E4M3), oracle.quantize(W, oracle.E4M3),
                           oracle.quantize(D, oracle.E5M2))
-            self.layers.append((w, X, W, D, qx, qw, qd))
+            self.layers.append((name, w, X, W, D, qx, qw, qd))
 
     def run(self) -> float:
         o, f = self.o, self.frac
         t0 = time.perf_counter()
-        for w, X, W, D, qx, qw, qd in self.layers:
-            for T, fmt in ((X, o.E4M3), (W, o.E4M3), (D, o.E5M2)):
+        for name, w, X, W, D, qx, qw, qd in self.layers:
+            # w3 reads the X already cast for w1
+            todo = ((W, o.E4M3), (D, o.E5M2)) if name == "w3" else ((X, o.E4M3), (W, o.E4M3), (D, o.E5M2))
+            for T, fmt in todo:
                 rows = max(16, int(round(T.shape[0] * f)))
                 o.quantize(T[:rows], fmt)
             rm = np.arange(max(1, int(round(w.M * f))))
@@ -187,7 +189,7 @@ class OracleSample:
 
     def describe(self) -> str:
         return (f"one Llama-3.1-8B FFN step (w1, w3, w2) sampled at {self.frac:.5g} of its rows: "
-                f"amax/scale/cast/transpose of that share of every X, W, dY and that share of "
+                f"amax/scale/cast/transpose of that share of X (once for w1 and w3), H, every W and dY, and that share of "
                 f"the output rows of every fwd/dgrad/wgrad GEMM; full-step time = sample time / share")
 
 
@@ -224,6 +226,138 @@ def run_reference(args, rank: int) -> None:
 
 # ------------------------------------------------------------------- ours
 
+class FFNStep:
+    """The Llama-3.1-8B SwiGLU FFN's three Float8 linears as one training
+    step, issued through the public entry points.
+
+    Data dependencies follow the FFN: w1 and w3 read the same X (cast once);
+    w2 reads H = silu(Y1) * Y3, so H's cast waits for both forward GEMMs;
+    dY2 comes from upstream; dY1 and dY3 come from w2's input gradient dH
+    through the SwiGLU backward, so their casts wait for w2's dgrad.  (H, dY1,
+    dY3 and dY2 are seeded synthetic tensors of those shapes; the SwiGLU
+    itself is not part of the linear layer's path.)
+
+    With overlap, every amax / cast runs on a low-priority side stream and
+    the GEMMs on a high-priority main stream, so the HBM-bound scaling work
+    hides behind tensor-bound GEMMs wherever the dependencies allow -- the
+    overlap window the pages describe for FP8 scaling work.  Each step starts
+    after the previous one has finished (the FP8 buffers are reused)."""
+
+    def __init__(self, fl, dev, dev_in, overlap=True):
+        import torch
+        self.fl, self.t = fl, torch
+        self.overlap = overlap
+        w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
+        w2 = wl.WORKLOADS["llama3_8b_ffn_w2"]
+        self.shapes = {"w1": w13, "w3": w13, "w2": w2}
+        F = fl.Float8Tensor
+        self.x8 = F(w13.M, w13.K, fl.E4M3, dev)                     # X, shared by w1 and w3
+        self.h8 = F(w2.M, w2.K, fl.E4M3, dev)                       # H, input of w2
+        self.w8 = {n: F(w.N, w.K, fl.E4M3, dev) for n, w in self.shapes.items()}
+        self.d8 = {n: F(w.M, w.N, fl.E5M2, dev) for n, w in self.shapes.items()}
+        bf = torch.bfloat16
+        self.y = {n: torch.empty((w.M, w.N), dtype=bf, device=dev) for n, w in self.shapes.items()}
+        self.dx = {n: torch.empty((w.M, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
+        self.dw = {n: torch.empty((w.N, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
+        self.inp = dev_in
+        if overlap:
+            self.main = torch.cuda.Stream(device=dev, priority=-1)
+            self.side = torch.cuda.Stream(device=dev, priority=0)
+        else:
+            self.main = self.side = torch.cuda.current_stream(dev)
+        # amax + cast per quantised tensor (X, H, three W, three dY), three GEMMs per linear
+        self.kernels_per_step = 2 * 8 + 9
+
+    def describe(self):
+        if not self.overlap:
+            return "serial: one stream, X cast once for w1 and w3"
+        return ("two streams: amax/cast on a low-priority side stream overlapping the GEMMs on a "
+                "high-priority main stream, FFN data dependencies kept; X cast once for w1 and w3")
+
+    def outputs(self):
+        return [t for n in ("w1", "w3", "w2") for t in (self.y[n], self.dx[n], self.dw[n])]
+
+    def _ev(self):
+        return self.t.cuda.Event(enable_timing=True)
+
+    def _mark(self, stream, rec, kind, label, work, fn):
+        if rec is None:
+            fn()
+            return
+        e0, e1 = self._ev(), self._ev()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        rec.append((kind, label, e0, e1, work))
+
+    def _quantize(self, rec, label, x, t8):
+        fl, s = self.fl, self.side
+        n = x.numel()
+        self._mark(s, rec, "amax", label, 2 * n, lambda: fl.fp8lin_amax(x, t8.amax, s))
+        self._mark(s, rec, "cast", label, 4 * n, lambda: fl.fp8lin_cast_transpose(
+            x, t8.fmt, t8.amax, t8.scale, t8.inv_scale, t8.q, t8.qT, t8.fmt_max, s))
+
+    def _signal(self, stream):
+        if not self.overlap:
+            return None
+        e = self.t.cuda.Event()
+        e.record(stream)
+        return e
+
+    def _wait(self, stream, ev):
+        if ev is not None:
+            stream.wait_event(ev)
+
+    def _gemm(self, rec, name, which):
+        fl, m = self.fl, self.main
+        w = self.shapes[name]
+        work = 2 * w.M * w.N * w.K
+        x8 = self.x8 if name != "w2" else self.h8
+        w8, d8 = self.w8[name], self.d8[name]
+        if which == "fwd":
+            fn = lambda: fl.fp8lin_fwd(x8.q, x8.inv_scale, w8.q, w8.inv_scale, self.y[name], m)
+        elif which == "dgrad":
+            fn = lambda: fl.fp8lin_dgrad(d8.q, d8.inv_scale, w8.qT, w8.inv_scale, self.dx[name], m)
+        else:
+            fn = lambda: fl.fp8lin_wgrad(d8.qT, d8.inv_scale, x8.qT, x8.inv_scale, self.dw[name], m)
+        self._mark(m, rec, "gemm", f"{name}.{which}", work, fn)
+
+    def run(self, rec=None):
+        inp, m, s = self.inp, self.main, self.side
+        self._wait(s, self._signal(m))                    # previous step done with the buffers
+        self._quantize(rec, "x", inp[("w1", "x")], self.x8)
+        self._quantize(rec, "w1", inp[("w1", "w")], self.w8["w1"])
+        e_w1 = self._signal(s)
+        self._quantize(rec, "w3", inp[("w3", "w")], self.w8["w3"])
+        e_w3 = self._signal(s)
+        self._quantize(rec, "w2", inp[("w2", "w")], self.w8["w2"])
+        self._quantize(rec, "dy2", inp[("w2", "dy")], self.d8["w2"])
+        e_w2 = self._signal(s)
+        self._wait(m, e_w1)
+        self._gemm(rec, "w1", "fwd")
+        self._wait(m, e_w3)
+        self._gemm(rec, "w3", "fwd")
+        self._wait(s, self._signal(m))                    # H = silu(Y1) * Y3 needs both outputs
+        self._quantize(rec, "h", inp[("w2", "x")], self.h8)
+        e_h = self._signal(s)
+        self._wait(m, e_h)
+        self._wait(m, e_w2)
+        self._gemm(rec, "w2", "fwd")
+        self._gemm(rec, "w2", "dgrad")
+        self._wait(s, self._signal(m))                    # dY1, dY3 derive from dH
+        self._quantize(rec, "dy1", inp[("w1", "dy")], self.d8["w1"])
+        e_d1 = self._signal(s)
+        self._quantize(rec, "dy3", inp[("w3", "dy")], self.d8["w3"])
+        e_d3 = self._signal(s)
+        self._gemm(rec, "w2", "wgrad")
+        self._wait(m, e_d1)
+        self._gemm(rec, "w1", "dgrad")
+        self._gemm(rec, "w1", "wgrad")
+        self._wait(m, e_d3)
+        self._gemm(rec, "w3", "dgrad")
+        self._gemm(rec, "w3", "wgrad")
+
+
 def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     import torch
     import float8_linear_layers_gb300 as fl
@@ -239,40 +373,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     def up(bits):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
     dev_in = {k: up(v) for k, v in host.items()}
-    # X is shared by w1 and w3: one device copy
-    dev_in[("w3", "x")] = dev_in[("w1", "x")]
-    layers = []
-    for name, w, *_ in ffn_layers():
-        layers.append((name, w, fl.Float8Linear(w.M, w.K, w.N, device=dev)))
-    stream = torch.cuda.current_stream(dev)
+    dev_in[("w3", "x")] = dev_in[("w1", "x")]   # w1 and w3 read the same X
+    ffn = FFNStep(fl, dev, dev_in, overlap=not args.serial)
+    stream = ffn.main
+    torch.cuda.set_stream(stream)
 
-    # Per-kernel events inside the timed region: events bracket each launch
-    # on the stream the kernels run on.
     def step(events=None):
-        for name, w, lin in layers:
-            x, wt, dy = dev_in[(name, "x")], dev_in[(name, "w")], dev_in[(name, "dy")]
-            if events is None:
-                lin.step(x, wt, dy)
-                continue
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
-            ev[0].record(stream)
-            fl.fp8lin_amax(x, lin.x8.amax)
-            ev[1].record(stream)
-            fl.fp8lin_cast_transpose(x, fl.E4M3, lin.x8.amax, lin.x8.scale, lin.x8.inv_scale, lin.x8.q, lin.x8.qT)
-            ev[2].record(stream)
-            lin.w8.quantize(wt)
-            ev[3].record(stream)
-            fl.fp8lin_fwd(lin.x8.q, lin.x8.inv_scale, lin.w8.q, lin.w8.inv_scale, lin.y)
-            ev[4].record(stream)
-            fl.fp8lin_amax(dy, lin.dy8.amax)
-            ev[5].record(stream)
-            fl.fp8lin_cast_transpose(dy, fl.E5M2, lin.dy8.amax, lin.dy8.scale, lin.dy8.inv_scale, lin.dy8.q, lin.dy8.qT)
-            ev[6].record(stream)
-            fl.fp8lin_dgrad(lin.dy8.q, lin.dy8.inv_scale, lin.w8.qT, lin.w8.inv_scale, lin.dx)
-            ev[7].record(stream)
-            fl.fp8lin_wgrad(lin.dy8.qT, lin.dy8.inv_scale, lin.x8.qT, lin.x8.inv_scale, lin.dw)
-            ev[8].record(stream)
-            events.append((name, w, ev))
+        ffn.run(events)
 
     def barrier():
         if dist is not None:
@@ -304,34 +411,27 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         elapsed_ms = float(t.item())
     assert fl.fp8lin_device_error() == 0, "a GEMM kernel reported a timed-out wait"
 
-    # per-kernel times from the events
-    gemm_ms = amax_ms = cast_ms = 0.0
-    gemm_flops = amax_bytes = cast_bytes = 0
+    # per-kernel times from the events (each pair brackets one launch on its stream)
+    kern = {"gemm": [0.0, 0], "amax": [0.0, 0], "cast": [0.0, 0]}
+    w1_fwd_ms, w1_fwd_n = 0.0, 0
     per_layer = {}
-    w1_fwd_ms, w1_fwd_n, w1_fwd_flops = 0.0, 0, 0
-    for name, w, ev in events:
-        amax_x = ev[0].elapsed_time(ev[1])
-        cast_x = ev[1].elapsed_time(ev[2])
-        wq = ev[2].elapsed_time(ev[3])
-        fwd = ev[3].elapsed_time(ev[4])
-        amax_d = ev[4].elapsed_time(ev[5])
-        cast_d = ev[5].elapsed_time(ev[6])
-        dgrad = ev[6].elapsed_time(ev[7])
-        wgrad = ev[7].elapsed_time(ev[8])
-        if name == "w1":
-            w1_fwd_ms += fwd
-            w1_fwd_n += 1
-            w1_fwd_flops = 2 * w.M * w.N * w.K
-        gemm_ms += fwd + dgrad + wgrad
-        gemm_flops += 3 * 2 * w.M * w.N * w.K
-        amax_ms += amax_x + amax_d
-        amax_bytes += 2 * (w.M * w.K + w.M * w.N)
-        cast_ms += cast_x + cast_d
-        cast_bytes += 4 * (w.M * w.K + w.M * w.N)
-        pl = per_layer.setdefault(name, {"ms": 0.0, "gemm_ms": 0.0, "n": 0, "flops": w.flops})
-        pl["ms"] += ev[0].elapsed_time(ev[8])
-        pl["gemm_ms"] += fwd + dgrad + wgrad
-        pl["n"] += 1
+    for kind, label, e0, e1, work in events:
+        ms = e0.elapsed_time(e1)
+        kern[kind][0] += ms
+        kern[kind][1] += work
+        if kind == "gemm":
+            lay = label.split(".")[0]
+            pl = per_layer.setdefault(lay, [0.0, 0])
+            pl[0] += ms
+            pl[1] += work
+            if label == "w1.fwd":
+                w1_fwd_ms += ms
+                w1_fwd_n += 1
+    gemm_ms, gemm_flops = kern["gemm"]
+    amax_ms, amax_bytes = kern["amax"]
+    cast_ms, cast_bytes = kern["cast"]
+    w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
+    w1_fwd_flops = 2 * w13.M * w13.N * w13.K
 
     peaks, peak_src = load_peaks()
     fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
@@ -340,27 +440,22 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     value = world * step_flops() / (ms_per_step * 1e-3) / 1e12
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     w1_fwd_tflops = w1_fwd_flops / (w1_fwd_ms / w1_fwd_n * 1e-3) / 1e12
-    n_gemm = 9 * args.steps
 
     # ---- end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
         pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-                  for k, v in host.items()}
-        outs = {name: [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (lin.y, lin.dx, lin.dw)]
-                for name, _, lin in layers}
-        h2d = sum(t.numel() * 2 for k, t in pinned.items() if not (k[0] == "w3" and k[1] == "x"))
-        d2h = sum(t.numel() * 2 for ts in outs.values() for t in ts)
+                  for k, v in host.items() if not (k[0] == "w3" and k[1] == "x")}
+        outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in ffn.outputs()]
+        h2d = sum(t.numel() * 2 for t in pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs)
 
         def e2e_step():
             for k, t in pinned.items():
-                if k[0] == "w3" and k[1] == "x":
-                    continue
                 dev_in[k].copy_(t, non_blocking=True)
-            for name, w, lin in layers:
-                y, dx, dw = lin.step(dev_in[(name, "x")], dev_in[(name, "w")], dev_in[(name, "dy")])
-                for o, d in zip(outs[name], (y, dx, dw)):
-                    o.copy_(d, non_blocking=True)
+            ffn.run()
+            for o, d in zip(outs, ffn.outputs()):
+                o.copy_(d, non_blocking=True)
 
         e2e_step()
         barrier()
@@ -416,18 +511,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                      "launches_timed": w1_fwd_n},
         "kernels": {
             "gemm": {"ms_per_step": gemm_ms / args.steps, "tflops": gemm_tflops},
-            "amax": {"ms_per_step": amax_ms / args.steps,
+            "amax": {"ms_per_step": amax_ms / args.steps, "note": "event time per launch, may overlap GEMMs",
                      "gbs": amax_bytes / (amax_ms * 1e-3) / 1e9 if amax_ms else None},
             "cast_transpose": {"ms_per_step": cast_ms / args.steps,
                                "gbs": cast_bytes / (cast_ms * 1e-3) / 1e9 if cast_ms else None},
             "hbm_peak_gbs": peaks["hbm_gbs"],
         },
-        "per_linear": {k: {"tflops": v["flops"] * v["n"] / (v["ms"] * 1e-3) / 1e12,
-                           "gemm_tflops": v["flops"] * v["n"] / (v["gemm_ms"] * 1e-3) / 1e12}
-                       for k, v in per_layer.items()},
+        "per_linear_gemm_tflops": {k: v[1] / (v[0] * 1e-3) / 1e12 for k, v in per_layer.items()},
+        "schedule": ffn.describe(),
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 27 * args.steps,
+        "gpu_launches": ffn.kernels_per_step * args.steps,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -504,6 +598,7 @@ def main():
     ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
     ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "amax", "cast"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()
