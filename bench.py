@@ -290,8 +290,8 @@ class FFNStep:
         e1.record(stream)
         rec.append((kind, label, e0, e1, work))
 
-    def _quantize(self, rec, label, x, t8):
-        fl, s = self.fl, self.side
+    def _quantize(self, rec, label, x, t8, stream=None):
+        fl, s = self.fl, (self.side if stream is None else stream)
         n = x.numel()
         self._mark(s, rec, "amax", label, 2 * n, lambda: fl.fp8lin_amax(x, t8.amax, s))
         self._mark(s, rec, "cast", label, 4 * n, lambda: fl.fp8lin_cast_transpose(
@@ -323,33 +323,44 @@ class FFNStep:
         self._mark(m, rec, "gemm", f"{name}.{which}", work, fn)
 
     def run(self, rec=None):
+        """One step.  Side-stream work that should run under a GEMM waits for
+        a marker recorded on the main stream just before that GEMM's launch,
+        so the GEMM's persistent CTAs are resident first and the HBM-bound
+        kernels fill the SM resources the GEMM leaves free."""
         inp, m, s = self.inp, self.main, self.side
-        self._wait(s, self._signal(m))                    # previous step done with the buffers
-        self._quantize(rec, "x", inp[("w1", "x")], self.x8)
-        self._quantize(rec, "w1", inp[("w1", "w")], self.w8["w1"])
-        e_w1 = self._signal(s)
+        # X and W1 gate the first GEMM: nothing to hide them behind, so they
+        # run on the main stream (no cross-stream hop).
+        self._quantize(rec, "x", inp[("w1", "x")], self.x8, m)
+        self._quantize(rec, "w1", inp[("w1", "w")], self.w8["w1"], m)
+        g = self._signal(m)                               # w1 fwd about to launch
+        self._gemm(rec, "w1", "fwd")
+        self._wait(s, g)
         self._quantize(rec, "w3", inp[("w3", "w")], self.w8["w3"])
         e_w3 = self._signal(s)
         self._quantize(rec, "w2", inp[("w2", "w")], self.w8["w2"])
-        self._quantize(rec, "dy2", inp[("w2", "dy")], self.d8["w2"])
         e_w2 = self._signal(s)
-        self._wait(m, e_w1)
-        self._gemm(rec, "w1", "fwd")
         self._wait(m, e_w3)
         self._gemm(rec, "w3", "fwd")
-        self._wait(s, self._signal(m))                    # H = silu(Y1) * Y3 needs both outputs
-        self._quantize(rec, "h", inp[("w2", "x")], self.h8)
-        e_h = self._signal(s)
-        self._wait(m, e_h)
+        # H = silu(Y1) * Y3 needs both forward outputs; it gates w2's forward
+        # GEMM, so it too runs on the main stream.
+        self._quantize(rec, "h", inp[("w2", "x")], self.h8, m)
         self._wait(m, e_w2)
+        g = self._signal(m)                               # w2 fwd about to launch
+        self._wait(s, g)
+        self._quantize(rec, "dy2", inp[("w2", "dy")], self.d8["w2"])
+        e_d2 = self._signal(s)
         self._gemm(rec, "w2", "fwd")
+        self._wait(m, e_d2)
         self._gemm(rec, "w2", "dgrad")
-        self._wait(s, self._signal(m))                    # dY1, dY3 derive from dH
+        e_dh = self._signal(m)                            # dY1, dY3 derive from dH
+        g = self._signal(m)
+        self._gemm(rec, "w2", "wgrad")
+        self._wait(s, e_dh)
+        self._wait(s, g)
         self._quantize(rec, "dy1", inp[("w1", "dy")], self.d8["w1"])
         e_d1 = self._signal(s)
         self._quantize(rec, "dy3", inp[("w3", "dy")], self.d8["w3"])
         e_d3 = self._signal(s)
-        self._gemm(rec, "w2", "wgrad")
         self._wait(m, e_d1)
         self._gemm(rec, "w1", "dgrad")
         self._gemm(rec, "w1", "wgrad")
@@ -427,6 +438,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             if label == "w1.fwd":
                 w1_fwd_ms += ms
                 w1_fwd_n += 1
+    gemm_evs = [(label, e0, e1) for kind, label, e0, e1, _ in events if kind == "gemm"]
+    per_step = len(gemm_evs) // args.steps
+    gaps = {}
+    for k in range(args.steps):
+        seq = gemm_evs[k * per_step:(k + 1) * per_step]
+        prev = t_start if k == 0 else gemm_evs[k * per_step - 1][2]
+        for label, e0, e1 in seq:
+            gaps[label] = gaps.get(label, 0.0) + prev.elapsed_time(e0) / args.steps
+            prev = e1
     gemm_ms, gemm_flops = kern["gemm"]
     amax_ms, amax_bytes = kern["amax"]
     cast_ms, cast_bytes = kern["cast"]
@@ -519,6 +539,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         },
         "per_linear_gemm_tflops": {k: v[1] / (v[0] * 1e-3) / 1e12 for k, v in per_layer.items()},
         "schedule": ffn.describe(),
+        "main_stream_idle_before_gemm_ms": {k: round(v, 4) for k, v in gaps.items()},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": ffn.kernels_per_step * args.steps,

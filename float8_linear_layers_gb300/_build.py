@@ -21,6 +21,8 @@ LIB = os.path.join(OUT, "libfp8lin.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + INCLUDE, "-I" + CSRC]
+# extra nvcc flags (e.g. -DFP8LIN_GEMM_STAGES=5 to size the GEMM's shared-memory ring)
+EXTRA = os.environ.get("FP8LIN_NVCC_FLAGS", "").split()
 
 
 def nvcc() -> str:
@@ -39,7 +41,7 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or EXTRA:
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
@@ -56,7 +58,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for src in _sources():
         obj = os.path.join(OUT, "obj", os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *EXTRA, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd))
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

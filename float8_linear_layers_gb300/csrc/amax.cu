@@ -26,7 +26,7 @@ constexpr int kChunk = kThreads * kVec;       // vectors per block (32 KB)
 
 __device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -86,6 +86,8 @@ extern "C" fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cuda
     if (n > FP8LIN_MAX_DIM * FP8LIN_MAX_DIM) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
     DeviceInfo dev;
     fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    st = prefer_max_shared_carveout(reinterpret_cast<const void *>(&amax_bf16_kernel), dev.device, 0);
     if (st != FP8LIN_OK) return st;
     if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
     if (n == 0) return FP8LIN_OK;

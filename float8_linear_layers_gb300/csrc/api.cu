@@ -35,6 +35,21 @@ fp8lin_status current_device(DeviceInfo *info) {
     return FP8LIN_OK;
 }
 
+namespace {
+constexpr int kMaxCarveoutSlots = 8;
+std::atomic<bool> g_carveout_set[kMaxDevices][kMaxCarveoutSlots];
+}  // namespace
+
+fp8lin_status prefer_max_shared_carveout(const void *kernel, int device, int slot) {
+    if (device < 0 || device >= kMaxDevices || slot < 0 || slot >= kMaxCarveoutSlots) return FP8LIN_ERR_CUDA;
+    if (g_carveout_set[device][slot].load(std::memory_order_acquire)) return FP8LIN_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
+    g_carveout_set[device][slot].store(true, std::memory_order_release);
+    return FP8LIN_OK;
+}
+
 }  // namespace fp8lin
 
 extern "C" const char *fp8lin_status_str(fp8lin_status s) {

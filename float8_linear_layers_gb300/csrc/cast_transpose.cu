@@ -16,6 +16,8 @@
 //    the transposed copy, so every warp store writes four full 128-byte rows.
 // The scale is derived in every CTA from the device amax (IEEE division), so
 // no separate launch and no host round trip is needed; CTA 0 publishes it.
+// Tiles are visited from the last row block to the first, so that the part of
+// the tensor the preceding amax pass read last is re-read from L2.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -42,6 +44,16 @@ __device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d) {
         asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
     }
     return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (the data is used once;
+// at the shared-memory-heavy carveout L1 is small).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -74,7 +86,10 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
     }
     if ((int)blockIdx.x >= num_tiles) return;
 
-    const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+    // Tiles run last-row-block first: the amax pass that precedes this kernel
+    // read the tensor front to back, so its tail is what L2 still holds.
+    const int tile_id = num_tiles - 1 - (int)blockIdx.x;
+    const int tr = tile_id / tiles_c, tc = tile_id % tiles_c;
     const int r0 = tr * kTile, c0 = tc * kTile;
     const int t = threadIdx.x;
 
@@ -87,7 +102,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
     for (int i = 0; i < 8; ++i) {
         const int r = r0 + row_base + 16 * i;
         if (col_in && r < rows)
-            v[i] = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)r * cols + c0 + ch * 8));
+            v[i] = ld_stream16(x + (int64_t)r * cols + c0 + ch * 8);
         else
             v[i] = make_uint4(0, 0, 0, 0);
     }
@@ -167,6 +182,12 @@ extern "C" fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int6
     const int grid = num_tiles > 0 ? (int)num_tiles : 1;  // one CTA publishes the scale
     const int tc = tiles_c > 0 ? (int)tiles_c : 1;
     const uint16_t *xs = static_cast<const uint16_t *>(x);
+    st = prefer_max_shared_carveout(reinterpret_cast<const void *>(&cast_transpose_kernel<FP8LIN_E4M3>),
+                                    dev.device, 1);
+    if (st == FP8LIN_OK)
+        st = prefer_max_shared_carveout(reinterpret_cast<const void *>(&cast_transpose_kernel<FP8LIN_E5M2>),
+                                        dev.device, 2);
+    if (st != FP8LIN_OK) return st;
     if (fmt == FP8LIN_E4M3)
         cast_transpose_kernel<FP8LIN_E4M3><<<grid, kThreads, 0, stream>>>(
             xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max, amax, scale, inv_scale, q, qT);

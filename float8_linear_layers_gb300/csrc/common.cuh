@@ -28,4 +28,10 @@ struct DeviceInfo {
 // Facts about the current device, cached per device ordinal.
 fp8lin_status current_device(DeviceInfo *info);
 
+// Ask for the largest shared-memory carveout for `kernel` (once per device).
+// The GEMM runs every SM at that carveout; an SM hosts CTAs of concurrently
+// running kernels only when their carveouts agree, so the HBM-bound amax and
+// cast kernels use the same setting to run beside a GEMM on another stream.
+fp8lin_status prefer_max_shared_carveout(const void *kernel, int device, int slot);
+
 }  // namespace fp8lin

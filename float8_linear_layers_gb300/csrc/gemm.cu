@@ -55,7 +55,10 @@ constexpr int kBM = kPairM / 2;       // A rows held by each CTA
 constexpr int kBN = kPairN / 2;       // B rows held by each CTA
 constexpr int kBK = 128;              // contraction bytes per stage (one 128-byte swizzle row)
 constexpr int kUmmaK = 32;            // contraction elements per tcgen05.mma for 8-bit types
-constexpr int kStages = 6;
+#ifndef FP8LIN_GEMM_STAGES
+#define FP8LIN_GEMM_STAGES 6
+#endif
+constexpr int kStages = FP8LIN_GEMM_STAGES;
 constexpr int kAStage = kBM * kBK;    // 16 KB
 constexpr int kBStage = kBN * kBK;    // 16 KB
 constexpr int kThreads = 192;
@@ -528,7 +531,9 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     if (dev.device >= 64) return FP8LIN_ERR_CUDA;
     if (!g_smem_attr_set[dev.device].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(fp8_gemm_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_tn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return FP8LIN_ERR_CUDA;
         // pairs that can be resident at once (a GPC with an odd number of free SMs leaves one idle)
         int clusters = 0;
