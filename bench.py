@@ -243,18 +243,19 @@ class FFNStep:
     overlap window the pages describe for FP8 scaling work.  Each step starts
     after the previous one has finished (the FP8 buffers are reused)."""
 
-    def __init__(self, fl, dev, dev_in, overlap=True):
+    def __init__(self, fl, dev, dev_in, overlap=True, scaling="dynamic"):
         import torch
         self.fl, self.t = fl, torch
         self.overlap = overlap
+        self.scaling = scaling
         w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
         w2 = wl.WORKLOADS["llama3_8b_ffn_w2"]
         self.shapes = {"w1": w13, "w3": w13, "w2": w2}
-        F = fl.Float8Tensor
-        self.x8 = F(w13.M, w13.K, fl.E4M3, dev)                     # X, shared by w1 and w3
-        self.h8 = F(w2.M, w2.K, fl.E4M3, dev)                       # H, input of w2
-        self.w8 = {n: F(w.N, w.K, fl.E4M3, dev) for n, w in self.shapes.items()}
-        self.d8 = {n: F(w.M, w.N, fl.E5M2, dev) for n, w in self.shapes.items()}
+        F = lambda r, c, f: fl.Float8Tensor(r, c, f, dev, scaling=scaling)
+        self.x8 = F(w13.M, w13.K, fl.E4M3)                          # X, shared by w1 and w3
+        self.h8 = F(w2.M, w2.K, fl.E4M3)                            # H, input of w2
+        self.w8 = {n: F(w.N, w.K, fl.E4M3) for n, w in self.shapes.items()}
+        self.d8 = {n: F(w.M, w.N, fl.E5M2) for n, w in self.shapes.items()}
         bf = torch.bfloat16
         self.y = {n: torch.empty((w.M, w.N), dtype=bf, device=dev) for n, w in self.shapes.items()}
         self.dx = {n: torch.empty((w.M, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
@@ -265,14 +266,17 @@ class FFNStep:
             self.side = torch.cuda.Stream(device=dev, priority=0)
         else:
             self.main = self.side = torch.cuda.current_stream(dev)
-        # amax + cast per quantised tensor (X, H, three W, three dY), three GEMMs per linear
-        self.kernels_per_step = 2 * 8 + 9
+        # per quantised tensor (X, H, three W, three dY): amax + cast (dynamic)
+        # or the cast alone (delayed: it records the amax itself); 9 GEMMs
+        self.kernels_per_step = (2 if scaling == "dynamic" else 1) * 8 + 9
 
     def describe(self):
+        how = f"{self.scaling} per-tensor scaling; "
         if not self.overlap:
-            return "serial: one stream, X cast once for w1 and w3"
-        return ("two streams: amax/cast on a low-priority side stream overlapping the GEMMs on a "
-                "high-priority main stream, FFN data dependencies kept; X cast once for w1 and w3")
+            return how + "serial: one stream, X cast once for w1 and w3"
+        return how + ("two streams: casts that the FFN dependencies leave hidable run on a "
+                      "low-priority side stream under the GEMMs of a high-priority main stream; "
+                      "X, W1 and H gate a GEMM and run on the main stream; X cast once for w1 and w3")
 
     def outputs(self):
         return [t for n in ("w1", "w3", "w2") for t in (self.y[n], self.dx[n], self.dw[n])]
@@ -293,6 +297,9 @@ class FFNStep:
     def _quantize(self, rec, label, x, t8, stream=None):
         fl, s = self.fl, (self.side if stream is None else stream)
         n = x.numel()
+        if t8.scaling != "dynamic":
+            self._mark(s, rec, "cast", label, 4 * n, lambda: t8.quantize(x, s))
+            return
         self._mark(s, rec, "amax", label, 2 * n, lambda: fl.fp8lin_amax(x, t8.amax, s))
         self._mark(s, rec, "cast", label, 4 * n, lambda: fl.fp8lin_cast_transpose(
             x, t8.fmt, t8.amax, t8.scale, t8.inv_scale, t8.q, t8.qT, t8.fmt_max, s))
@@ -385,7 +392,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
     dev_in = {k: up(v) for k, v in host.items()}
     dev_in[("w3", "x")] = dev_in[("w1", "x")]   # w1 and w3 read the same X
-    ffn = FFNStep(fl, dev, dev_in, overlap=not args.serial)
+    ffn = FFNStep(fl, dev, dev_in, overlap=not args.serial, scaling=args.scaling)
     stream = ffn.main
     torch.cuda.set_stream(stream)
 
@@ -514,7 +521,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD,
+        "config": {"workload": WORKLOAD, "scaling": args.scaling,
                    "linears": {"w1": "M8192 K4096 N14336", "w3": "M8192 K4096 N14336",
                                "w2": "M8192 K14336 N4096"},
                    "l2": "inputs larger than L2: one step streams ~2.9 GB of distinct operands through a 129 MB L2",
@@ -620,6 +627,8 @@ def main():
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
+    ap.add_argument("--scaling", choices=["dynamic", "delayed"], default="dynamic",
+                    help="per-tensor scaling recipe (the headline metric is dynamic)")
     ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "amax", "cast"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()

@@ -41,8 +41,9 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
            6: "FP8LIN_ERR_UNSUPPORTED_DEVICE"}
 
 # Every entry point declared in include/fp8lin.h.
-ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_fwd", "fp8lin_dgrad",
-                "fp8lin_wgrad", "fp8lin_status_str", "fp8lin_device_error")
+ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_static",
+                "fp8lin_cast_transpose_delayed", "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad",
+                "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
 
 class Fp8LinError(RuntimeError):
@@ -61,10 +62,13 @@ def _load_library() -> ctypes.CDLL:
     sigs = {
         "fp8lin_amax": [vp, i64, vp, vp],
         "fp8lin_cast_transpose": [vp, i64, i64, ci, f32, vp, vp, vp, vp, vp, vp],
+        "fp8lin_cast_transpose_static": [vp, i64, i64, ci, vp, vp, vp, vp, vp, vp],
+        "fp8lin_cast_transpose_delayed": [vp, i64, i64, ci, f32, vp, i64, i64, vp, vp, vp, vp, vp],
         "fp8lin_fwd": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8lin_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8lin_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8lin_device_error": [vp, vp],
+        "fp8lin_selftest_bounded_wait": [ctypes.c_uint64, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -139,6 +143,43 @@ def fp8lin_cast_transpose(x: torch.Tensor, fmt: int, amax: torch.Tensor, scale: 
                                       _stream(stream)))
 
 
+def fp8lin_cast_transpose_static(x: torch.Tensor, fmt: int, scale: torch.Tensor, inv_scale: torch.Tensor,
+                                 q: torch.Tensor | None, qT: torch.Tensor | None,
+                                 amax: torch.Tensor | None = None, stream=None) -> None:
+    """Static scaling: q = sat_RNE(x * scale) with a caller-fixed scale;
+    inv_scale = 1/scale; amax (optional) receives max |x|."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [rows x cols] matrix")
+    for t, n in ((scale, "scale"), (inv_scale, "inv_scale"), (amax, "amax")):
+        _dev(t, n, torch.float32)
+    _dev(q, "q")
+    _dev(qT, "qT")
+    rows, cols = x.shape
+    _check("fp8lin_cast_transpose_static",
+           _lib.fp8lin_cast_transpose_static(_ptr(x), rows, cols, int(fmt), _ptr(scale), _ptr(inv_scale),
+                                             _ptr(q), _ptr(qT), _ptr(amax), _stream(stream)))
+
+
+def fp8lin_cast_transpose_delayed(x: torch.Tensor, fmt: int, amax_history: torch.Tensor, slot: int,
+                                  scale: torch.Tensor, inv_scale: torch.Tensor, q: torch.Tensor | None,
+                                  qT: torch.Tensor | None, fmt_max: float = FMT_MAX, stream=None) -> None:
+    """Delayed scaling: scale from the amax history (all slots but `slot`);
+    the cast records max |x| into amax_history[slot]."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [rows x cols] matrix")
+    for t, n in ((amax_history, "amax_history"), (scale, "scale"), (inv_scale, "inv_scale")):
+        _dev(t, n, torch.float32)
+    _dev(q, "q")
+    _dev(qT, "qT")
+    rows, cols = x.shape
+    _check("fp8lin_cast_transpose_delayed",
+           _lib.fp8lin_cast_transpose_delayed(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(amax_history),
+                                              amax_history.numel(), int(slot), _ptr(scale), _ptr(inv_scale),
+                                              _ptr(q), _ptr(qT), _stream(stream)))
+
+
 def fp8lin_fwd(xq, inv_x, wq, inv_w, y, stream=None) -> None:
     """Y [M x N] = bf16((Xq . Wq^T) * inv_x * inv_w); Xq [M x K], Wq [N x K]."""
     M, K = xq.shape
@@ -184,24 +225,60 @@ def fp8lin_device_error(stream=None) -> int:
     return int(word.value)
 
 
+def fp8lin_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch a wait that runs out after limit_ns (see include/fp8lin.h)."""
+    _check("fp8lin_selftest_bounded_wait", _lib.fp8lin_selftest_bounded_wait(int(limit_ns), _stream(stream)))
+
+
 # ----------------------------------------------------------- one linear
 
 class Float8Tensor:
-    """Per-tensor FP8 state of one bf16 matrix: amax, scale, inverse scale and
-    the FP8 copies in both majornesses (device buffers, caller-visible)."""
+    """Per-tensor FP8 state of one bf16 matrix: the scale, its inverse and
+    the FP8 copies in both majornesses (device buffers, caller-visible).
 
-    def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX):
+    scaling = "dynamic": amax of this tensor, then scale + cast (default);
+              "delayed": scale from an amax history ring (``history_len``
+                         slots), this tensor's amax recorded by the cast; the
+                         first call seeds the ring with one amax pass;
+              "static":  a fixed scale set with ``set_scale``."""
+
+    def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX,
+                 scaling: str = "dynamic", history_len: int = 16):
+        if scaling not in ("dynamic", "delayed", "static"):
+            raise ValueError(f"unknown scaling {scaling!r}")
         self.rows, self.cols, self.fmt, self.fmt_max = rows, cols, fmt, fmt_max
+        self.scaling = scaling
         scalars = torch.zeros(3, dtype=torch.float32, device=device)
         self.amax, self.scale, self.inv_scale = scalars[0:1], scalars[1:2], scalars[2:3]
         self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
         self.qT = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+        if scaling == "delayed":
+            self.history = torch.zeros(history_len, dtype=torch.float32, device=device)
+            self.slot = 0
+            self.seeded = False
+
+    def set_scale(self, value: float) -> "Float8Tensor":
+        """The fixed scale of static scaling."""
+        self.scale.fill_(float(value))
+        return self
 
     def quantize(self, x: torch.Tensor, stream=None) -> "Float8Tensor":
-        """Dynamic scaling of x: amax, then scale + cast + transpose."""
-        fp8lin_amax(x, self.amax, stream)
-        fp8lin_cast_transpose(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT,
-                              self.fmt_max, stream)
+        """Scale, cast and transpose x according to this tensor's scaling."""
+        if self.scaling == "dynamic":
+            fp8lin_amax(x, self.amax, stream)
+            fp8lin_cast_transpose(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT,
+                                  self.fmt_max, stream)
+        elif self.scaling == "static":
+            fp8lin_cast_transpose_static(x, self.fmt, self.scale, self.inv_scale, self.q, self.qT,
+                                         self.amax, stream)
+        else:
+            n = self.history.numel()
+            if not self.seeded:
+                fp8lin_amax(x, self.history[(self.slot - 1) % n:(self.slot - 1) % n + 1], stream)
+                self.seeded = True
+            fp8lin_cast_transpose_delayed(x, self.fmt, self.history, self.slot, self.scale, self.inv_scale,
+                                          self.q, self.qT, self.fmt_max, stream)
+            self.slot = (self.slot + 1) % n
         return self
 
 
@@ -211,11 +288,12 @@ class Float8Linear:
     copies and the outputs are allocated once and reused every step; the
     transposed copies of X and W made in forward are what backward reads."""
 
-    def __init__(self, M: int, K: int, N: int, device="cuda", fmt_max: float = FMT_MAX):
+    def __init__(self, M: int, K: int, N: int, device="cuda", fmt_max: float = FMT_MAX,
+                 scaling: str = "dynamic", history_len: int = 16):
         self.M, self.K, self.N = M, K, N
-        self.x8 = Float8Tensor(M, K, E4M3, device, fmt_max)
-        self.w8 = Float8Tensor(N, K, E4M3, device, fmt_max)
-        self.dy8 = Float8Tensor(M, N, E5M2, device, fmt_max)
+        self.x8 = Float8Tensor(M, K, E4M3, device, fmt_max, scaling, history_len)
+        self.w8 = Float8Tensor(N, K, E4M3, device, fmt_max, scaling, history_len)
+        self.dy8 = Float8Tensor(M, N, E5M2, device, fmt_max, scaling, history_len)
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=device)

@@ -69,19 +69,54 @@ __device__ __forceinline__ uint2 cast8(uint4 v, float s) {
     return r;
 }
 
-template <int FMT>
+// Where the scale comes from.
+enum ScaleMode : int {
+    kDynamic = 0,  // scale = fmt_max / max(amax, 1e-12), amax of this tensor (computed beforehand)
+    kStatic = 1,   // scale given by the caller
+    kDelayed = 2,  // scale = fmt_max / max(max of the amax history except `slot`, 1e-12)
+};
+
+// Largest of n non-negative fp32 values (their bit patterns order the same
+// way; a NaN ranks above everything), skipping index `skip`.  Warp-parallel.
+__device__ __forceinline__ float history_max(const float *__restrict__ h, int n, int skip) {
+    const int lane = threadIdx.x % 32;
+    uint32_t m = 0;
+    for (int i = lane; i < n; i += 32)
+        if (i != skip) m = max(m, __float_as_uint(__ldg(h + i)) & 0x7FFFFFFFu);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    return __uint_as_float(m);
+}
+
+// Packed 16-bit magnitude maximum of eight bf16 values.
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, uint4 v) {
+    const uint32_t k = 0x7FFF7FFFu;
+    m = __vmaxu2(m, v.x & k);
+    m = __vmaxu2(m, v.y & k);
+    m = __vmaxu2(m, v.z & k);
+    m = __vmaxu2(m, v.w & k);
+    return m;
+}
+
+template <int FMT, int MODE, bool RECORD>
 __global__ void __launch_bounds__(kThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c, int num_tiles,
-                      float fmt_max, const float *__restrict__ amax, float *__restrict__ scale_out,
-                      float *__restrict__ inv_out, uint8_t *__restrict__ q, uint8_t *__restrict__ qT) {
+                      float fmt_max, const float *__restrict__ scale_src, int hist_len, int slot,
+                      float *__restrict__ scale_out, float *__restrict__ inv_out, uint8_t *__restrict__ q,
+                      uint8_t *__restrict__ qT, unsigned int *__restrict__ amax_record) {
     __shared__ __align__(16) uint32_t tile[kTile][kTile / 4];
+    __shared__ uint32_t warp_max[kThreads / 32];
 
-    // scale = fmt_max / max(amax, 1e-12): binary32, round to nearest even.
-    float a = __ldg(amax);
-    a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
-    const float s = __fdiv_rn(fmt_max, a);
+    float s;
+    if (MODE == kStatic) {
+        s = __ldg(scale_src);
+    } else {
+        // scale = fmt_max / max(amax, 1e-12): binary32, round to nearest even.
+        float a = (MODE == kDynamic) ? __ldg(scale_src) : history_max(scale_src, hist_len, slot);
+        a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
+        s = __fdiv_rn(fmt_max, a);
+    }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        *scale_out = s;
+        if (scale_out != nullptr) *scale_out = s;
         *inv_out = __frcp_rn(s);
     }
     if ((int)blockIdx.x >= num_tiles) return;
@@ -105,6 +140,23 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
             v[i] = ld_stream16(x + (int64_t)r * cols + c0 + ch * 8);
         else
             v[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (RECORD) {
+        // this tile's max |x| (zero padding never raises it), one conditional
+        // atomicMax per CTA on the fp32 bit pattern (bf16 << 16)
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = absmax8(m, v[i]);
+        uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+        if (t % 32 == 0) warp_max[t / 32] = r;
+        __syncthreads();
+        if (t < 32) {
+            r = __reduce_max_sync(0xFFFFFFFFu, t < kThreads / 32 ? warp_max[t] : 0u);
+            if (t == 0 && r != 0) {
+                const uint32_t bits = r << 16;
+                if (bits > *reinterpret_cast<volatile unsigned int *>(amax_record)) atomicMax(amax_record, bits);
+            }
+        }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -156,20 +208,57 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
     }
 }
 
-}  // namespace
+template <int FMT>
+void launch_mode(int mode, bool record, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
+                 int tiles_c, int num_tiles, float fmt_max, const float *src, int hist_len, int slot,
+                 float *scale, float *inv, uint8_t *q, uint8_t *qT, unsigned int *rec) {
+#define FP8LIN_CAST_LAUNCH(MODE, REC)                                                                        \
+    cast_transpose_kernel<FMT, MODE, REC><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_c, num_tiles,  \
+                                                                          fmt_max, src, hist_len, slot,      \
+                                                                          scale, inv, q, qT, rec)
+    if (mode == kDynamic)
+        FP8LIN_CAST_LAUNCH(kDynamic, false);
+    else if (mode == kStatic && !record)
+        FP8LIN_CAST_LAUNCH(kStatic, false);
+    else if (mode == kStatic)
+        FP8LIN_CAST_LAUNCH(kStatic, true);
+    else
+        FP8LIN_CAST_LAUNCH(kDelayed, true);
+#undef FP8LIN_CAST_LAUNCH
+}
 
-extern "C" fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
-                                               float fmt_max, const float *amax, float *scale,
-                                               float *inv_scale, uint8_t *q, uint8_t *qT,
-                                               cudaStream_t stream) {
+template <int FMT>
+fp8lin_status set_carveouts(int device) {
     using namespace fp8lin;
-    if (amax == nullptr || scale == nullptr || inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    const int base = FMT == FP8LIN_E4M3 ? 1 : 5;
+    fp8lin_status st = prefer_max_shared_carveout(
+        reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kDynamic, false>), device, base);
+    if (st == FP8LIN_OK)
+        st = prefer_max_shared_carveout(
+            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kStatic, false>), device, base + 1);
+    if (st == FP8LIN_OK)
+        st = prefer_max_shared_carveout(
+            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kStatic, true>), device, base + 2);
+    if (st == FP8LIN_OK)
+        st = prefer_max_shared_carveout(
+            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kDelayed, true>), device, base + 3);
+    return st;
+}
+
+// Checks shared by the three scalings, then the launch.
+fp8lin_status cast_common(int mode, const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
+                          const float *src, int hist_len, int slot, float *scale, float *inv_scale, uint8_t *q,
+                          uint8_t *qT, float *amax_record, cudaStream_t stream) {
+    using namespace fp8lin;
+    if (src == nullptr || inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (mode != kStatic && scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0) return FP8LIN_ERR_INVALID_ARG;
     if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
-    if (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f)) return FP8LIN_ERR_INVALID_ARG;
+    if (mode != kStatic && (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f))) return FP8LIN_ERR_INVALID_ARG;
     const bool empty = rows == 0 || cols == 0;
     if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
-    if (!aligned(amax, 4) || !aligned(scale, 4) || !aligned(inv_scale, 4)) return FP8LIN_ERR_MISALIGNED;
+    if (!aligned(src, 4) || !aligned(scale, 4) || !aligned(inv_scale, 4) || !aligned(amax_record, 4))
+        return FP8LIN_ERR_MISALIGNED;
     if (!empty && (!aligned(x, 16) || !aligned(q, 16) || !aligned(qT, 16))) return FP8LIN_ERR_MISALIGNED;
     if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
     DeviceInfo dev;
@@ -181,18 +270,46 @@ extern "C" fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int6
     if (num_tiles > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
     const int grid = num_tiles > 0 ? (int)num_tiles : 1;  // one CTA publishes the scale
     const int tc = tiles_c > 0 ? (int)tiles_c : 1;
-    const uint16_t *xs = static_cast<const uint16_t *>(x);
-    st = prefer_max_shared_carveout(reinterpret_cast<const void *>(&cast_transpose_kernel<FP8LIN_E4M3>),
-                                    dev.device, 1);
-    if (st == FP8LIN_OK)
-        st = prefer_max_shared_carveout(reinterpret_cast<const void *>(&cast_transpose_kernel<FP8LIN_E5M2>),
-                                        dev.device, 2);
+    st = fmt == FP8LIN_E4M3 ? set_carveouts<FP8LIN_E4M3>(dev.device) : set_carveouts<FP8LIN_E5M2>(dev.device);
     if (st != FP8LIN_OK) return st;
+    const bool record = amax_record != nullptr;
+    if (record && cudaMemsetAsync(amax_record, 0, sizeof(float), stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
+    const uint16_t *xs = static_cast<const uint16_t *>(x);
+    unsigned int *rec = reinterpret_cast<unsigned int *>(amax_record);
     if (fmt == FP8LIN_E4M3)
-        cast_transpose_kernel<FP8LIN_E4M3><<<grid, kThreads, 0, stream>>>(
-            xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max, amax, scale, inv_scale, q, qT);
+        launch_mode<FP8LIN_E4M3>(mode, record, grid, stream, xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max,
+                                 src, hist_len, slot, scale, inv_scale, q, qT, rec);
     else
-        cast_transpose_kernel<FP8LIN_E5M2><<<grid, kThreads, 0, stream>>>(
-            xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max, amax, scale, inv_scale, q, qT);
+        launch_mode<FP8LIN_E5M2>(mode, record, grid, stream, xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max,
+                                 src, hist_len, slot, scale, inv_scale, q, qT, rec);
     return check_launch();
+}
+
+}  // namespace
+
+extern "C" fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                               float fmt_max, const float *amax, float *scale,
+                                               float *inv_scale, uint8_t *q, uint8_t *qT,
+                                               cudaStream_t stream) {
+    return cast_common(kDynamic, x, rows, cols, fmt, fmt_max, amax, 0, 0, scale, inv_scale, q, qT, nullptr,
+                       stream);
+}
+
+extern "C" fp8lin_status fp8lin_cast_transpose_static(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                                      const float *scale, float *inv_scale, uint8_t *q,
+                                                      uint8_t *qT, float *amax, cudaStream_t stream) {
+    return cast_common(kStatic, x, rows, cols, fmt, 0.0f, scale, 0, 0, nullptr, inv_scale, q, qT, amax,
+                       stream);
+}
+
+extern "C" fp8lin_status fp8lin_cast_transpose_delayed(const void *x, int64_t rows, int64_t cols,
+                                                       fp8lin_fmt fmt, float fmt_max, float *amax_history,
+                                                       int64_t history_len, int64_t slot, float *scale,
+                                                       float *inv_scale, uint8_t *q, uint8_t *qT,
+                                                       cudaStream_t stream) {
+    if (amax_history == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (history_len < 2 || history_len > FP8LIN_MAX_HISTORY || slot < 0 || slot >= history_len)
+        return FP8LIN_ERR_INVALID_ARG;
+    return cast_common(kDelayed, x, rows, cols, fmt, fmt_max, amax_history, (int)history_len, (int)slot, scale,
+                       inv_scale, q, qT, amax_history + slot, stream);
 }

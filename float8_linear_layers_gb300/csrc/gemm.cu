@@ -579,6 +579,34 @@ extern "C" fp8lin_status fp8lin_wgrad(const uint8_t *dyqT, const float *inv_dy, 
     return gemm_tn(dyqT, FP8LIN_E5M2, inv_dy, xqT, FP8LIN_E4M3, inv_x, dw, N, K, M, stream);
 }
 
+namespace {
+
+// One bounded wait on an mbarrier that nothing arrives on: the same wait the
+// GEMM kernels use, made to run out so that its timeout path can be checked.
+__global__ void bounded_wait_probe_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns);
+}
+
+}  // namespace
+
+extern "C" fp8lin_status fp8lin_selftest_bounded_wait(uint64_t limit_ns, cudaStream_t stream) {
+    using namespace fp8lin;
+    if (limit_ns < 1000ull || limit_ns > 1000000000ull) return FP8LIN_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    bounded_wait_probe_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_ns);
+    return check_launch();
+}
+
 extern "C" fp8lin_status fp8lin_device_error(cudaStream_t stream, uint32_t *word) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
     unsigned int v = 0, zero = 0;

@@ -72,6 +72,9 @@ typedef enum fp8lin_fmt {
 /* Largest dimension accepted by any call (rows, columns, M, N or K). */
 #define FP8LIN_MAX_DIM ((int64_t)1 << 30)
 
+/* Longest amax history accepted by fp8lin_cast_transpose_delayed. */
+#define FP8LIN_MAX_HISTORY 1024
+
 /*
  * amax of one bf16 tensor: *amax = max_i |x_i| (fp32, exact).
  * Dynamic per-tensor scaling takes this statistic of the tensor itself each
@@ -113,6 +116,52 @@ fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols,
                                     fp8lin_fmt fmt, float fmt_max, const float *amax,
                                     float *scale, float *inv_scale,
                                     uint8_t *q, uint8_t *qT, cudaStream_t stream);
+
+/*
+ * Static scaling: cast with a scale the caller fixes (TorchTitan analysis
+ * page, section 3.3: torchao offers dynamic, delayed and static per-tensor
+ * scaling).  Same layouts, rounding and saturation as fp8lin_cast_transpose.
+ *
+ *   scale      device, one float, read only: the scale to apply.
+ *   inv_scale  device, one float: receives 1 / scale (fp32 RN).
+ *   amax       device, one float, or NULL: when given, receives max |x| of
+ *              this tensor (cleared by the call first), e.g. to calibrate or
+ *              to monitor the fixed scale.
+ *   x, rows, cols, fmt, q, qT as for fp8lin_cast_transpose.
+ */
+fp8lin_status fp8lin_cast_transpose_static(const void *x, int64_t rows, int64_t cols,
+                                           fp8lin_fmt fmt, const float *scale, float *inv_scale,
+                                           uint8_t *q, uint8_t *qT, float *amax,
+                                           cudaStream_t stream);
+
+/*
+ * Delayed scaling: the scale comes from the statistics of previous steps, so
+ * no amax pass has to run before the cast (TorchTitan analysis page, section
+ * 3.3, "delayed" per-tensor scaling; Lecture 9 exercises: delayed scaling
+ * uses the previous step's statistics so the scaling work can hide in an
+ * overlap window).  The pages give no history rule; this library keeps a
+ * caller-owned ring of amax values:
+ *
+ *   scale          = fmt_max / max(max_{i != slot} amax_history[i], 1e-12)
+ *   amax_history[slot] = max |x| of this tensor (cleared by the call first,
+ *                        then recorded by the cast kernel itself)
+ *
+ * and the caller advances slot = (slot + 1) % history_len every step.  A
+ * history whose other slots are all zero (the first step) gives the floor
+ * scale, which saturates everything: seed slot (slot + 1) % history_len with
+ * one fp8lin_amax of the tensor first.
+ *
+ *   amax_history  device, history_len floats (4-byte aligned), read and written.
+ *   history_len   2 .. FP8LIN_MAX_HISTORY.
+ *   slot          0 .. history_len - 1: the entry this step writes.
+ *   fmt_max, scale, inv_scale, x, rows, cols, fmt, q, qT as for
+ *   fp8lin_cast_transpose.  Values beyond the scaled range saturate.
+ */
+fp8lin_status fp8lin_cast_transpose_delayed(const void *x, int64_t rows, int64_t cols,
+                                            fp8lin_fmt fmt, float fmt_max, float *amax_history,
+                                            int64_t history_len, int64_t slot, float *scale,
+                                            float *inv_scale, uint8_t *q, uint8_t *qT,
+                                            cudaStream_t stream);
 
 /*
  * Forward GEMM of the Float8 linear: Y = bf16_RN( (Xq . Wq^T)_fp32 * (inv_x * inv_w) ).
@@ -171,6 +220,18 @@ const char *fp8lin_status_str(fp8lin_status status);
  * (and writes the raw word to *word when word is not NULL).
  */
 fp8lin_status fp8lin_device_error(cudaStream_t stream, uint32_t *word);
+
+/*
+ * Self-test of the bounded waits: launches one CTA that waits on an mbarrier
+ * nothing arrives on, for at most limit_ns nanoseconds (1 us .. 1 s), using
+ * the same wait as the GEMM kernels.  The wait runs out and records
+ * FP8LIN_ERR_TIMEOUT in the device word that fp8lin_device_error() reads;
+ * the context stays usable.  Failure detection on this path is tested
+ * without any GPU fault (bounded waits of the GEMM pipeline: the pipeline
+ * has no counterpart on the pages; it follows from making every wait of an
+ * asynchronous producer/consumer ring finite).
+ */
+fp8lin_status fp8lin_selftest_bounded_wait(uint64_t limit_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -83,6 +83,10 @@ def _load():
         lib.orc_gemm_rows.restype = None
         lib.orc_gemm_rows.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64,
                                       f32, f32, ctypes.c_void_p, i64, ctypes.c_void_p]
+        lib.orc_reciprocal.restype = f32
+        lib.orc_reciprocal.argtypes = [f32]
+        lib.orc_history_max.restype = f32
+        lib.orc_history_max.argtypes = [ctypes.c_void_p, i64, i64]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -164,6 +168,35 @@ def quantize(x_bits: np.ndarray, fmt: int, fmt_max: float = FMT_MAX) -> dict:
     s, inv = scale(a, fmt_max)
     q = cast(x_bits, fmt, s)
     return {"amax": a, "scale": s, "inv_scale": inv, "q": q, "qT": transpose(q)}
+
+
+def quantize_static(x_bits: np.ndarray, fmt: int, scale_value: float) -> dict:
+    """Static scaling [TT]: the caller fixes the scale; the inverse scale is
+    1/scale in fp32; the tensor's amax is reported alongside."""
+    s = np.float32(scale_value)
+    inv = np.float32(_load().orc_reciprocal(float(s)))
+    q = cast(x_bits, fmt, s)
+    return {"amax": amax(x_bits), "scale": s, "inv_scale": inv, "q": q, "qT": transpose(q)}
+
+
+def history_max(history: np.ndarray, skip: int) -> np.float32:
+    """Largest amax in the history, leaving out the slot being written."""
+    h = np.ascontiguousarray(history, dtype=np.float32)
+    return np.float32(_load().orc_history_max(_ptr(h), h.size, int(skip)))
+
+
+def quantize_delayed(x_bits: np.ndarray, fmt: int, history: np.ndarray, slot: int,
+                     fmt_max: float = FMT_MAX) -> dict:
+    """Delayed scaling: the scale comes from the previous steps' statistics
+    ([TT] "delayed"; [L9]: delayed scaling uses the previous step's
+    statistics).  Reading taken (the pages give no history rule): a ring of
+    amax values; scale = fmt_max / max(max over the ring except `slot`,
+    1e-12); this tensor's amax is then stored at `slot`."""
+    s, inv = scale(history_max(history, slot), fmt_max)
+    q = cast(x_bits, fmt, s)
+    new_hist = np.array(history, dtype=np.float32, copy=True)
+    new_hist[slot] = amax(x_bits)
+    return {"scale": s, "inv_scale": inv, "q": q, "qT": transpose(q), "history": new_hist}
 
 
 # ------------------------------------------------------------------ GEMMs

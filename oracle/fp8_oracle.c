@@ -204,6 +204,34 @@ void orc_scale(float amax, float fmt_max, float *scale, float *inv_scale) {
     *inv_scale = inv;
 }
 
+/* 1 / s as one binary32 round-to-nearest division (static scaling's
+ * inverse scale). */
+float orc_reciprocal(float s) {
+    volatile float r = 1.0f / s;
+    return r;
+}
+
+/* Largest entry of an amax history h[0..n), leaving out index `skip` (the
+ * slot the current step writes): delayed scaling takes its statistic from
+ * earlier steps.  Entries are non-negative; ordered like orc_amax_bf16
+ * (totalOrder: a NaN ranks above every number).  No entry gives 0. */
+float orc_history_max(const float *h, int64_t n, int64_t skip) {
+    float best = 0.0f;
+    uint32_t nan_bits = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (i == skip) continue;
+        uint32_t b = bits_from_f32(h[i]) & 0x7FFFFFFFu;
+        if (b > 0x7F800000u) {
+            if (b > nan_bits) nan_bits = b;
+            continue;
+        }
+        float v = f32_from_bits(b);
+        if (v > best) best = v;
+    }
+    if (nan_bits) return f32_from_bits(nan_bits);
+    return best;
+}
+
 /* ---------------------------------------------------------------- cast */
 
 /* q_i = encode(fp32(x_i) * scale): the product is one binary32 multiply
