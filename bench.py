@@ -243,7 +243,7 @@ class FFNStep:
     overlap window the pages describe for FP8 scaling work.  Each step starts
     after the previous one has finished (the FP8 buffers are reused)."""
 
-    def __init__(self, fl, dev, dev_in, overlap=True, scaling="dynamic"):
+    def __init__(self, fl, dev, dev_in, overlap=True, scaling="dynamic", streams=None):
         import torch
         self.fl, self.t = fl, torch
         self.overlap = overlap
@@ -261,7 +261,9 @@ class FFNStep:
         self.dx = {n: torch.empty((w.M, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
         self.dw = {n: torch.empty((w.N, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
         self.inp = dev_in
-        if overlap:
+        if streams is not None:
+            self.main, self.side = streams
+        elif overlap:
             self.main = torch.cuda.Stream(device=dev, priority=-1)
             self.side = torch.cuda.Stream(device=dev, priority=0)
         else:
@@ -376,6 +378,84 @@ class FFNStep:
         self._gemm(rec, "w3", "wgrad")
 
 
+def run_e2e(args, fl, dev, host, ffn, world, dist, barrier):
+    """The same FFN step measured end to end from pinned host memory: every
+    step uploads its bf16 inputs (X, H, three W, three dY) and reads back all
+    nine outputs (Y, dX, dW of w1, w3, w2).  Inputs and outputs are double
+    buffered so that step i+1's upload and step i's readback run on their own
+    copy streams while step i computes."""
+    import torch
+    pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+              for k, v in host.items() if not (k[0] == "w3" and k[1] == "x")}
+    h2d_bytes = sum(t.numel() * 2 for t in pinned.values())
+    sets = []
+    for k in range(2):
+        din = {key: torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for key, t in pinned.items()}
+        din[("w3", "x")] = din[("w1", "x")]
+        f = ffn if k == 0 else FFNStep(fl, dev, din, overlap=ffn.overlap, scaling=ffn.scaling,
+                                       streams=(ffn.main, ffn.side))
+        if k == 0:
+            f.inp = din
+        outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in f.outputs()]
+        sets.append((f, din, outs))
+    d2h_bytes = sum(t.numel() * t.element_size() for t in sets[0][2])
+    copy_in = torch.cuda.Stream(device=dev)
+    copy_out = torch.cuda.Stream(device=dev)
+    main = ffn.main
+
+    def run(n, timed):
+        ev = lambda: torch.cuda.Event(enable_timing=timed)
+        ev_in, ev_done, ev_out = [None, None], [None, None], [None, None]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def upload(k):
+            with torch.cuda.stream(copy_in):
+                for key, t in pinned.items():
+                    sets[k][1][key].copy_(t, non_blocking=True)
+            e = ev()
+            e.record(copy_in)
+            ev_in[k] = e
+
+        t0.record(copy_in)
+        upload(0)
+        for i in range(n):
+            k, j = i % 2, (i + 1) % 2
+            if i + 1 < n:
+                if ev_done[j] is not None:
+                    copy_in.wait_event(ev_done[j])       # step i-1 is done reading set j
+                upload(j)
+            main.wait_event(ev_in[k])
+            if ev_out[k] is not None:
+                main.wait_event(ev_out[k])               # step i-2's outputs have left set k
+            f, _, outs = sets[k]
+            f.run()
+            e = ev()
+            e.record(main)
+            ev_done[k] = e
+            copy_out.wait_event(e)
+            with torch.cuda.stream(copy_out):
+                for o, d in zip(outs, f.outputs()):
+                    o.copy_(d, non_blocking=True)
+            e = ev()
+            e.record(copy_out)
+            ev_out[k] = e
+        t1.record(copy_out)
+        return t0, t1
+
+    run(2, False)
+    barrier()
+    t0, t1 = run(args.e2e_steps, True)
+    barrier()
+    e_ms = t0.elapsed_time(t1) / args.e2e_steps
+    if dist is not None:
+        t = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    return {"value": world * step_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": e_ms,
+            "pipeline": "double-buffered: upload of step i+1 and readback of step i overlap step i's compute"}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     import torch
     import float8_linear_layers_gb300 as fl
@@ -471,35 +551,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # ---- end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
-        pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-                  for k, v in host.items() if not (k[0] == "w3" and k[1] == "x")}
-        outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in ffn.outputs()]
-        h2d = sum(t.numel() * 2 for t in pinned.values())
-        d2h = sum(t.numel() * t.element_size() for t in outs)
-
-        def e2e_step():
-            for k, t in pinned.items():
-                dev_in[k].copy_(t, non_blocking=True)
-            ffn.run()
-            for o, d in zip(outs, ffn.outputs()):
-                o.copy_(d, non_blocking=True)
-
-        e2e_step()
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * step_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+        e2e = run_e2e(args, fl, dev, host, ffn, world, dist, barrier)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -622,7 +674,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
