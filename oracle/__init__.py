@@ -87,6 +87,15 @@ def _load():
         lib.orc_reciprocal.argtypes = [f32]
         lib.orc_history_max.restype = f32
         lib.orc_history_max.argtypes = [ctypes.c_void_p, i64, i64]
+        lib.orc_amax_rows_bf16.restype = None
+        lib.orc_amax_rows_bf16.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p]
+        lib.orc_amax_cols_bf16.restype = None
+        lib.orc_amax_cols_bf16.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p]
+        lib.orc_cast_rows_bf16.restype = None
+        lib.orc_cast_rows_bf16.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_int, ctypes.c_void_p, u8p]
+        lib.orc_gemm_rows_vec.restype = None
+        lib.orc_gemm_rows_vec.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_void_p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -197,6 +206,78 @@ def quantize_delayed(x_bits: np.ndarray, fmt: int, history: np.ndarray, slot: in
     new_hist = np.array(history, dtype=np.float32, copy=True)
     new_hist[slot] = amax(x_bits)
     return {"scale": s, "inv_scale": inv, "q": q, "qT": transpose(q), "history": new_hist}
+
+
+def amax_rows(x_bits: np.ndarray) -> np.ndarray:
+    """amax of every row of a bf16 matrix (row-wise scaling's statistic)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out = np.empty(x.shape[0], dtype=np.float32)
+    _load().orc_amax_rows_bf16(_ptr(x), x.shape[0], x.shape[1], _ptr(out))
+    return out
+
+
+def amax_cols(x_bits: np.ndarray) -> np.ndarray:
+    """amax of every column of a bf16 matrix."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out = np.empty(x.shape[1], dtype=np.float32)
+    _load().orc_amax_cols_bf16(_ptr(x), x.shape[0], x.shape[1], _ptr(out))
+    return out
+
+
+def scales(amax_values: np.ndarray, fmt_max: float = FMT_MAX):
+    """scale() applied to every entry of an amax vector."""
+    pairs = [scale(a, fmt_max) for a in np.asarray(amax_values, dtype=np.float32)]
+    s = np.array([p[0] for p in pairs], dtype=np.float32)
+    inv = np.array([p[1] for p in pairs], dtype=np.float32)
+    return s, inv
+
+
+def cast_rows(x_bits: np.ndarray, fmt: int, row_scales: np.ndarray) -> np.ndarray:
+    """q[r][c] = sat_RNE(fp32(x[r][c]) * scale[r])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    sc = np.ascontiguousarray(row_scales, dtype=np.float32)
+    assert sc.size == x.shape[0]
+    q = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_cast_rows_bf16(_ptr(x), x.shape[0], x.shape[1], fmt, _ptr(sc), _ptr(q))
+    return q
+
+
+def quantize_rowwise(x_bits: np.ndarray, fmt: int, fmt_max: float = FMT_MAX) -> dict:
+    """Per-block scaling with one block per row of each GEMM operand ([L9]:
+    one factor per tensor, or even per block).  Reading taken: a block must
+    not vary along the GEMM's contraction (the scale then factors out of the
+    sum and is applied after it), so the row-major copy q takes one scale per
+    row of x and the transposed copy qT one scale per row of x^T, i.e. per
+    column of x; each copy is cast from the bf16 source with its own scales."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    ar, ac = amax_rows(x), amax_cols(x)
+    sr, ir = scales(ar, fmt_max)
+    sc, ic = scales(ac, fmt_max)
+    q = cast_rows(x, fmt, sr)
+    qT = cast_rows(np.ascontiguousarray(x.T), fmt, sc)
+    return {"row_amax": ar, "col_amax": ac, "row_scale": sr, "row_inv": ir, "col_scale": sc, "col_inv": ic,
+            "q": q, "qT": qT}
+
+
+def gemm_rows_vec(A: np.ndarray, fa: int, B: np.ndarray, fb: int, inv_a: np.ndarray, inv_b: np.ndarray,
+                  rows=None) -> np.ndarray:
+    """C = (dec(A) . dec(B)^T)[p][q] * inv_a[p] * inv_b[q] in float64, for the
+    listed rows of C: the GEMM with row-wise (per-block) scales."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    P, R = A.shape
+    Q, R2 = B.shape
+    assert R == R2
+    ia = np.ascontiguousarray(inv_a, dtype=np.float32)
+    ib = np.ascontiguousarray(inv_b, dtype=np.float32)
+    assert ia.size == P and ib.size == Q
+    if rows is None:
+        rows = np.arange(P, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, Q), dtype=np.float64)
+    _load().orc_gemm_rows_vec(_ptr(A), fa, _ptr(B), fb, P, Q, R, _ptr(ia), _ptr(ib), _ptr(rows), rows.size,
+                              _ptr(out))
+    return out
 
 
 # ------------------------------------------------------------------ GEMMs

@@ -244,6 +244,45 @@ void orc_cast_bf16(const uint16_t *x, int64_t n, int fmt, float scale, uint8_t *
     }
 }
 
+/* Row-wise scaling ("per block", one block = one row of the operand, the
+ * finest block that stays constant along the GEMM's contraction):
+ * amax of every row of a row-major bf16 [rows x cols] matrix. */
+void orc_amax_rows_bf16(const uint16_t *x, int64_t rows, int64_t cols, float *out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) out[r] = orc_amax_bf16(x + r * cols, cols);
+}
+
+/* amax of every column (column c's elements are x[r][c], r = 0..rows-1). */
+void orc_amax_cols_bf16(const uint16_t *x, int64_t rows, int64_t cols, float *out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < cols; ++c) {
+        float best = 0.0f;
+        uint16_t nan_mag = 0;
+        for (int64_t r = 0; r < rows; ++r) {
+            uint16_t h = x[r * cols + c];
+            uint16_t mag = (uint16_t)(h & 0x7FFF);
+            if (mag > 0x7F80) {
+                if (mag > nan_mag) nan_mag = mag;
+                continue;
+            }
+            float v = fabsf(orc_bf16_to_f32(h));
+            if (v > best) best = v;
+        }
+        out[c] = nan_mag ? orc_bf16_to_f32(nan_mag) : best;
+    }
+}
+
+/* q[r][c] = encode(fp32(x[r][c]) * scale[r]): the cast with one scale per row. */
+void orc_cast_rows_bf16(const uint16_t *x, int64_t rows, int64_t cols, int fmt, const float *scale,
+                        uint8_t *q) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            volatile float v = orc_bf16_to_f32(x[r * cols + c]) * scale[r];
+            q[r * cols + c] = orc_fp8_encode(fmt, v);
+        }
+}
+
 /* qT[c][r] = q[r][c] for a row-major [rows x cols] byte matrix. */
 void orc_transpose_u8(const uint8_t *q, int64_t rows, int64_t cols, uint8_t *qT) {
 #pragma omp parallel for schedule(static)
@@ -283,6 +322,29 @@ void orc_gemm_rows(const uint8_t *A, int fa, const uint8_t *B, int fb,
             for (int64_t k = 0; k < R; ++k)
                 s += da[a[k]] * db[b[k]];
             out[i * Q + q] = s * (double)inv_a * (double)inv_b;
+        }
+    }
+}
+
+/* orc_gemm_rows with one inverse scale per row of A and per row of B:
+ * C[p][q] = ( sum_k dec(A[p][k]) * dec(B[q][k]) ) * inv_a[p] * inv_b[q]. */
+void orc_gemm_rows_vec(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t P, int64_t Q, int64_t R,
+                       const float *inv_a, const float *inv_b, const int64_t *rows, int64_t nrows, double *out) {
+    double da[256], db[256];
+    for (int c = 0; c < 256; ++c) {
+        da[c] = orc_fp8_decode(fa, (uint8_t)c);
+        db[c] = orc_fp8_decode(fb, (uint8_t)c);
+    }
+    (void)P;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const uint8_t *a = A + rows[i] * R;
+        for (int64_t q = 0; q < Q; ++q) {
+            const uint8_t *b = B + q * R;
+            double s = 0.0;
+            for (int64_t k = 0; k < R; ++k)
+                s += da[a[k]] * db[b[k]];
+            out[i * Q + q] = s * (double)inv_a[rows[i]] * (double)inv_b[q];
         }
     }
 }
