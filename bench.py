@@ -270,7 +270,7 @@ class FFNStep:
             self.main = self.side = torch.cuda.current_stream(dev)
         # per quantised tensor (X, H, three W, three dY): amax + cast (dynamic)
         # or the cast alone (delayed: it records the amax itself); 9 GEMMs
-        self.kernels_per_step = (2 if scaling == "dynamic" else 1) * 8 + 9
+        self.kernels_per_step = (2 if scaling in ("dynamic", "rowwise") else 1) * 8 + 9
 
     def describe(self):
         how = f"{self.scaling} per-tensor scaling; "
@@ -299,6 +299,12 @@ class FFNStep:
     def _quantize(self, rec, label, x, t8, stream=None):
         fl, s = self.fl, (self.side if stream is None else stream)
         n = x.numel()
+        if t8.scaling == "rowwise":
+            self._mark(s, rec, "amax", label, 2 * n,
+                       lambda: fl.fp8lin_amax_rowcol(x, t8.row_amax, t8.col_amax, s))
+            self._mark(s, rec, "cast", label, 4 * n, lambda: fl.fp8lin_cast_transpose_rowwise(
+                x, t8.fmt, t8.row_amax, t8.col_amax, t8.row_inv, t8.col_inv, t8.q, t8.qT, t8.fmt_max, s))
+            return
         if t8.scaling != "dynamic":
             self._mark(s, rec, "cast", label, 4 * n, lambda: t8.quantize(x, s))
             return
@@ -323,6 +329,15 @@ class FFNStep:
         work = 2 * w.M * w.N * w.K
         x8 = self.x8 if name != "w2" else self.h8
         w8, d8 = self.w8[name], self.d8[name]
+        if self.scaling == "rowwise":
+            if which == "fwd":
+                fn = lambda: fl.fp8lin_fwd_rowwise(x8.q, x8.row_inv, w8.q, w8.row_inv, self.y[name], m)
+            elif which == "dgrad":
+                fn = lambda: fl.fp8lin_dgrad_rowwise(d8.q, d8.row_inv, w8.qT, w8.col_inv, self.dx[name], m)
+            else:
+                fn = lambda: fl.fp8lin_wgrad_rowwise(d8.qT, d8.col_inv, x8.qT, x8.col_inv, self.dw[name], m)
+            self._mark(m, rec, "gemm", f"{name}.{which}", work, fn)
+            return
         if which == "fwd":
             fn = lambda: fl.fp8lin_fwd(x8.q, x8.inv_scale, w8.q, w8.inv_scale, self.y[name], m)
         elif which == "dgrad":
@@ -623,7 +638,7 @@ def run_profile_case(args) -> None:
     case = args.profile_case
     need_x = case in ("gemm_fwd", "gemm_wgrad")
     need_w = case in ("gemm_fwd", "gemm_dgrad")
-    need_dy = case in ("gemm_dgrad", "gemm_wgrad", "amax", "cast")   # dY: 235 MB > L2
+    need_dy = case in ("gemm_dgrad", "gemm_wgrad", "amax", "cast", "amax_rowcol", "cast_rowwise")  # dY: 235 MB > L2
     x8 = w8 = d8 = None
     if need_x:
         x = up(w.make_x())
@@ -650,6 +665,17 @@ def run_profile_case(args) -> None:
     elif case == "amax":
         launch = lambda: fl.fp8lin_amax(dy, d8.amax)
         work, unit = 2 * w.M * w.N, "byte"
+    elif case == "amax_rowcol":
+        ra = torch.zeros(w.M, device=dev)
+        ca = torch.zeros(w.N, device=dev)
+        launch = lambda: fl.fp8lin_amax_rowcol(dy, ra, ca)
+        work, unit = 2 * w.M * w.N, "byte"
+    elif case == "cast_rowwise":
+        ra, ca = torch.zeros(w.M, device=dev), torch.zeros(w.N, device=dev)
+        ri, ci = torch.zeros(w.M, device=dev), torch.zeros(w.N, device=dev)
+        fl.fp8lin_amax_rowcol(dy, ra, ca)
+        launch = lambda: fl.fp8lin_cast_transpose_rowwise(dy, fl.E5M2, ra, ca, ri, ci, d8.q, d8.qT)
+        work, unit = 4 * w.M * w.N, "byte"
     else:
         launch = lambda: fl.fp8lin_cast_transpose(dy, fl.E5M2, d8.amax, d8.scale, d8.inv_scale, d8.q, d8.qT)
         work, unit = 4 * w.M * w.N, "byte"
@@ -679,9 +705,10 @@ def main():
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
-    ap.add_argument("--scaling", choices=["dynamic", "delayed"], default="dynamic",
+    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise"], default="dynamic",
                     help="per-tensor scaling recipe (the headline metric is dynamic)")
-    ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "amax", "cast"],
+    ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "amax", "cast",
+                                               "amax_rowcol", "cast_rowwise"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least three warm-up steps

@@ -42,7 +42,9 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
 
 # Every entry point declared in include/fp8lin.h.
 ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_static",
-                "fp8lin_cast_transpose_delayed", "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad",
+                "fp8lin_cast_transpose_delayed", "fp8lin_amax_rowcol", "fp8lin_cast_transpose_rowwise",
+                "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad",
+                "fp8lin_fwd_rowwise", "fp8lin_dgrad_rowwise", "fp8lin_wgrad_rowwise",
                 "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
 
@@ -64,6 +66,11 @@ def _load_library() -> ctypes.CDLL:
         "fp8lin_cast_transpose": [vp, i64, i64, ci, f32, vp, vp, vp, vp, vp, vp],
         "fp8lin_cast_transpose_static": [vp, i64, i64, ci, vp, vp, vp, vp, vp, vp],
         "fp8lin_cast_transpose_delayed": [vp, i64, i64, ci, f32, vp, i64, i64, vp, vp, vp, vp, vp],
+        "fp8lin_amax_rowcol": [vp, i64, i64, vp, vp, vp],
+        "fp8lin_cast_transpose_rowwise": [vp, i64, i64, ci, f32, vp, vp, vp, vp, vp, vp, vp],
+        "fp8lin_fwd_rowwise": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8lin_dgrad_rowwise": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8lin_wgrad_rowwise": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8lin_fwd": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8lin_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8lin_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
@@ -180,6 +187,57 @@ def fp8lin_cast_transpose_delayed(x: torch.Tensor, fmt: int, amax_history: torch
                                               _ptr(q), _ptr(qT), _stream(stream)))
 
 
+def fp8lin_amax_rowcol(x: torch.Tensor, row_amax: torch.Tensor | None, col_amax: torch.Tensor | None,
+                       stream=None) -> None:
+    """row_amax[r] = max |x[r, :]|, col_amax[c] = max |x[:, c]| (either may be None)."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(row_amax, "row_amax", torch.float32)
+    _dev(col_amax, "col_amax", torch.float32)
+    rows, cols = x.shape
+    _check("fp8lin_amax_rowcol", _lib.fp8lin_amax_rowcol(_ptr(x), rows, cols, _ptr(row_amax), _ptr(col_amax),
+                                                         _stream(stream)))
+
+
+def fp8lin_cast_transpose_rowwise(x: torch.Tensor, fmt: int, row_amax, col_amax, row_inv_scale, col_inv_scale,
+                                  q, qT, fmt_max: float = FMT_MAX, stream=None) -> None:
+    """q with one scale per row, qT with one scale per column of x."""
+    _dev(x, "x", torch.bfloat16)
+    for t, n in ((row_amax, "row_amax"), (col_amax, "col_amax"), (row_inv_scale, "row_inv_scale"),
+                 (col_inv_scale, "col_inv_scale")):
+        _dev(t, n, torch.float32)
+    _dev(q, "q")
+    _dev(qT, "qT")
+    rows, cols = x.shape
+    _check("fp8lin_cast_transpose_rowwise",
+           _lib.fp8lin_cast_transpose_rowwise(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(row_amax),
+                                              _ptr(col_amax), _ptr(row_inv_scale), _ptr(col_inv_scale),
+                                              _ptr(q), _ptr(qT), _stream(stream)))
+
+
+def _gemm_call(name, a, sa, b, sb, c, M, N, K, stream):
+    for t, n in ((a, "a"), (b, "b"), (sa, "inv_a"), (sb, "inv_b"), (c, "out")):
+        _dev(t, n)
+    _check(name, getattr(_lib, name)(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(c), M, N, K, _stream(stream)))
+
+
+def fp8lin_fwd_rowwise(xq, inv_x_rows, wq, inv_w_rows, y, stream=None) -> None:
+    """Y = bf16((Xq . Wq^T)[m, n] * inv_x_rows[m] * inv_w_rows[n])."""
+    M, K = xq.shape
+    _gemm_call("fp8lin_fwd_rowwise", xq, inv_x_rows, wq, inv_w_rows, y, M, wq.shape[0], K, stream)
+
+
+def fp8lin_dgrad_rowwise(dyq, inv_dy_rows, wqT, inv_w_cols, dx, stream=None) -> None:
+    """dX = bf16((dYq . WqT^T)[m, k] * inv_dy_rows[m] * inv_w_cols[k])."""
+    M, N = dyq.shape
+    _gemm_call("fp8lin_dgrad_rowwise", dyq, inv_dy_rows, wqT, inv_w_cols, dx, M, N, wqT.shape[0], stream)
+
+
+def fp8lin_wgrad_rowwise(dyqT, inv_dy_cols, xqT, inv_x_cols, dw, stream=None) -> None:
+    """dW = bf16((dYqT . XqT^T)[n, k] * inv_dy_cols[n] * inv_x_cols[k])."""
+    N, M = dyqT.shape
+    _gemm_call("fp8lin_wgrad_rowwise", dyqT, inv_dy_cols, xqT, inv_x_cols, dw, M, N, xqT.shape[0], stream)
+
+
 def fp8lin_fwd(xq, inv_x, wq, inv_w, y, stream=None) -> None:
     """Y [M x N] = bf16((Xq . Wq^T) * inv_x * inv_w); Xq [M x K], Wq [N x K]."""
     M, K = xq.shape
@@ -240,11 +298,14 @@ class Float8Tensor:
               "delayed": scale from an amax history ring (``history_len``
                          slots), this tensor's amax recorded by the cast; the
                          first call seeds the ring with one amax pass;
-              "static":  a fixed scale set with ``set_scale``."""
+              "static":  a fixed scale set with ``set_scale``;
+              "rowwise": one scale per row of q and per row of qT (per
+                         column of the source): per-block scaling with
+                         blocks that do not cross the GEMM contraction."""
 
     def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX,
                  scaling: str = "dynamic", history_len: int = 16):
-        if scaling not in ("dynamic", "delayed", "static"):
+        if scaling not in ("dynamic", "delayed", "static", "rowwise"):
             raise ValueError(f"unknown scaling {scaling!r}")
         self.rows, self.cols, self.fmt, self.fmt_max = rows, cols, fmt, fmt_max
         self.scaling = scaling
@@ -252,6 +313,11 @@ class Float8Tensor:
         self.amax, self.scale, self.inv_scale = scalars[0:1], scalars[1:2], scalars[2:3]
         self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
         self.qT = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+        if scaling == "rowwise":
+            self.row_amax = torch.zeros(rows, dtype=torch.float32, device=device)
+            self.col_amax = torch.zeros(cols, dtype=torch.float32, device=device)
+            self.row_inv = torch.zeros(rows, dtype=torch.float32, device=device)
+            self.col_inv = torch.zeros(cols, dtype=torch.float32, device=device)
         if scaling == "delayed":
             self.history = torch.zeros(history_len, dtype=torch.float32, device=device)
             self.slot = 0
@@ -268,6 +334,10 @@ class Float8Tensor:
             fp8lin_amax(x, self.amax, stream)
             fp8lin_cast_transpose(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT,
                                   self.fmt_max, stream)
+        elif self.scaling == "rowwise":
+            fp8lin_amax_rowcol(x, self.row_amax, self.col_amax, stream)
+            fp8lin_cast_transpose_rowwise(x, self.fmt, self.row_amax, self.col_amax, self.row_inv, self.col_inv,
+                                          self.q, self.qT, self.fmt_max, stream)
         elif self.scaling == "static":
             fp8lin_cast_transpose_static(x, self.fmt, self.scale, self.inv_scale, self.q, self.qT,
                                          self.amax, stream)
@@ -305,13 +375,20 @@ class Float8Linear:
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
         self.x8.quantize(x, stream)
         self.w8.quantize(w, stream)
-        fp8lin_fwd(self.x8.q, self.x8.inv_scale, self.w8.q, self.w8.inv_scale, self.y, stream)
+        if self.x8.scaling == "rowwise":
+            fp8lin_fwd_rowwise(self.x8.q, self.x8.row_inv, self.w8.q, self.w8.row_inv, self.y, stream)
+        else:
+            fp8lin_fwd(self.x8.q, self.x8.inv_scale, self.w8.q, self.w8.inv_scale, self.y, stream)
         return self.y
 
     def backward(self, dy: torch.Tensor, stream=None):
         self.dy8.quantize(dy, stream)
-        fp8lin_dgrad(self.dy8.q, self.dy8.inv_scale, self.w8.qT, self.w8.inv_scale, self.dx, stream)
-        fp8lin_wgrad(self.dy8.qT, self.dy8.inv_scale, self.x8.qT, self.x8.inv_scale, self.dw, stream)
+        if self.dy8.scaling == "rowwise":
+            fp8lin_dgrad_rowwise(self.dy8.q, self.dy8.row_inv, self.w8.qT, self.w8.col_inv, self.dx, stream)
+            fp8lin_wgrad_rowwise(self.dy8.qT, self.dy8.col_inv, self.x8.qT, self.x8.col_inv, self.dw, stream)
+        else:
+            fp8lin_dgrad(self.dy8.q, self.dy8.inv_scale, self.w8.qT, self.w8.inv_scale, self.dx, stream)
+            fp8lin_wgrad(self.dy8.qT, self.dy8.inv_scale, self.x8.qT, self.x8.inv_scale, self.dw, stream)
         return self.dx, self.dw
 
     def step(self, x, w, dy, stream=None):

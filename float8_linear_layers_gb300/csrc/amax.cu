@@ -77,7 +77,105 @@ amax_bf16_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__re
     }
 }
 
+// Row and column amax of a row-major bf16 [rows x cols] matrix (row-wise
+// scaling's statistics).  One CTA per 128 x 128 tile, the same coalesced
+// 16-byte loads as the cast kernel; per-row maxima reduce across the 16
+// threads that share a row (shuffles), per-column maxima across the 16 row
+// groups (shuffle + shared memory); one atomicMax per row and per column of
+// the tile, issued as fire-and-forget reductions (the addresses are spread
+// over all rows and columns, so they do not serialise).
+constexpr int kTile = 128;
+
+__global__ void __launch_bounds__(256)
+amax_rowcol_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c,
+                   unsigned int *__restrict__ row_bits, unsigned int *__restrict__ col_bits) {
+    __shared__ uint32_t col_part[8][kTile / 2];  // [warp][packed column pair]
+    const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+    const int r0 = tr * kTile, c0 = tc * kTile;
+    const int t = threadIdx.x, ch = t % 16, row_base = t / 16;
+    const bool col_in = (c0 + ch * 8) < cols;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + row_base + 16 * i;
+        v[i] = (col_in && r < rows) ? ld_stream16(reinterpret_cast<const uint4 *>(x + (int64_t)r * cols + c0 + ch * 8))
+                                    : make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t k = 0x7FFF7FFFu;
+    // columns: packed maxima of this thread's 8 columns over its 8 rows
+    uint4 cm = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        cm.x = __vmaxu2(cm.x, v[i].x & k);
+        cm.y = __vmaxu2(cm.y, v[i].y & k);
+        cm.z = __vmaxu2(cm.z, v[i].z & k);
+        cm.w = __vmaxu2(cm.w, v[i].w & k);
+        // rows: the 16 lanes sharing this row combine their 8-column maxima
+        uint32_t m = absmax4(0u, v[i]);
+        m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const int r = r0 + row_base + 16 * i;
+        if (row_bits != nullptr && ch == 0 && r < rows && m != 0)
+            atomicMax(row_bits + r, m << 16);  // result unused: a non-blocking reduction
+    }
+    if (col_bits == nullptr) return;
+    // lanes t and t ^ 16 hold the same columns for two row groups
+    cm.x = __vmaxu2(cm.x, __shfl_xor_sync(0xFFFFFFFFu, cm.x, 16));
+    cm.y = __vmaxu2(cm.y, __shfl_xor_sync(0xFFFFFFFFu, cm.y, 16));
+    cm.z = __vmaxu2(cm.z, __shfl_xor_sync(0xFFFFFFFFu, cm.z, 16));
+    cm.w = __vmaxu2(cm.w, __shfl_xor_sync(0xFFFFFFFFu, cm.w, 16));
+    const int warp = t / 32, lane = t % 32;
+    if (lane < 16) {
+        col_part[warp][4 * ch + 0] = cm.x;
+        col_part[warp][4 * ch + 1] = cm.y;
+        col_part[warp][4 * ch + 2] = cm.z;
+        col_part[warp][4 * ch + 3] = cm.w;
+    }
+    __syncthreads();
+    if (t < kTile / 2) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m = __vmaxu2(m, col_part[w][t]);
+        const int c = c0 + 2 * t;
+        if (c < cols) {
+            const uint32_t lo = (m & 0xFFFFu) << 16, hi = m & 0xFFFF0000u;
+            if (lo != 0) atomicMax(col_bits + c, lo);
+            if (hi != 0) atomicMax(col_bits + c + 1, hi);
+        }
+    }
+}
+
 }  // namespace
+
+extern "C" fp8lin_status fp8lin_amax_rowcol(const void *x, int64_t rows, int64_t cols, float *row_amax,
+                                            float *col_amax, cudaStream_t stream) {
+    using namespace fp8lin;
+    if (rows < 0 || cols < 0) return FP8LIN_ERR_INVALID_ARG;
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if ((row_amax == nullptr && rows > 0 && col_amax == nullptr)) return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(row_amax, 4) || !aligned(col_amax, 4) || (!empty && !aligned(x, 16))) return FP8LIN_ERR_MISALIGNED;
+    if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    st = prefer_max_shared_carveout(reinterpret_cast<const void *>(&amax_rowcol_kernel), dev.device, 9);
+    if (st != FP8LIN_OK) return st;
+    if (row_amax != nullptr && rows > 0 &&
+        cudaMemsetAsync(row_amax, 0, (size_t)rows * sizeof(float), stream) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
+    if (col_amax != nullptr && cols > 0 &&
+        cudaMemsetAsync(col_amax, 0, (size_t)cols * sizeof(float), stream) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
+    if (empty) return FP8LIN_OK;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    if (tiles_r * tiles_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    amax_rowcol_kernel<<<(int)(tiles_r * tiles_c), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(x), (int)rows, (int)cols, (int)tiles_c,
+        reinterpret_cast<unsigned int *>(row_amax), reinterpret_cast<unsigned int *>(col_amax));
+    return check_launch();
+}
 
 extern "C" fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cudaStream_t stream) {
     using namespace fp8lin;

@@ -69,12 +69,30 @@ __device__ __forceinline__ uint2 cast8(uint4 v, float s) {
     return r;
 }
 
+// Eight elements with one scale per element (row-wise scaling's qT codes:
+// the scale of each column).
+template <int FMT>
+__device__ __forceinline__ uint2 cast8_each(uint4 v, const float (&sc)[8]) {
+    uint2 r;
+    r.x = cvt4<FMT>(__fmul_rn(bf16_lo(v.x), sc[0]), __fmul_rn(bf16_hi(v.x), sc[1]),
+                    __fmul_rn(bf16_lo(v.y), sc[2]), __fmul_rn(bf16_hi(v.y), sc[3]));
+    r.y = cvt4<FMT>(__fmul_rn(bf16_lo(v.z), sc[4]), __fmul_rn(bf16_hi(v.z), sc[5]),
+                    __fmul_rn(bf16_lo(v.w), sc[6]), __fmul_rn(bf16_hi(v.w), sc[7]));
+    return r;
+}
+
 // Where the scale comes from.
 enum ScaleMode : int {
     kDynamic = 0,  // scale = fmt_max / max(amax, 1e-12), amax of this tensor (computed beforehand)
     kStatic = 1,   // scale given by the caller
     kDelayed = 2,  // scale = fmt_max / max(max of the amax history except `slot`, 1e-12)
+    kRowwise = 3,  // one scale per row of q (from row amax) and per row of qT (from column amax)
 };
+
+__device__ __forceinline__ float scale_from_amax(float a, float fmt_max) {
+    a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
+    return __fdiv_rn(fmt_max, a);
+}
 
 // Largest of n non-negative fp32 values (their bit patterns order the same
 // way; a NaN ranks above everything), skipping index `skip`.  Warp-parallel.
@@ -102,12 +120,16 @@ __global__ void __launch_bounds__(kThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c, int num_tiles,
                       float fmt_max, const float *__restrict__ scale_src, int hist_len, int slot,
                       float *__restrict__ scale_out, float *__restrict__ inv_out, uint8_t *__restrict__ q,
-                      uint8_t *__restrict__ qT, unsigned int *__restrict__ amax_record) {
+                      uint8_t *__restrict__ qT, unsigned int *__restrict__ amax_record,
+                      const float *__restrict__ col_src, float *__restrict__ col_inv_out) {
     __shared__ __align__(16) uint32_t tile[kTile][kTile / 4];
     __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ float srow[MODE == kRowwise ? kTile : 1], scol[MODE == kRowwise ? kTile : 1];
 
-    float s;
-    if (MODE == kStatic) {
+    float s = 0.0f;
+    if (MODE == kRowwise) {
+        // per-row / per-column scales are formed below, per element
+    } else if (MODE == kStatic) {
         s = __ldg(scale_src);
     } else {
         // scale = fmt_max / max(amax, 1e-12): binary32, round to nearest even.
@@ -115,7 +137,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
         a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
         s = __fdiv_rn(fmt_max, a);
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (MODE != kRowwise && blockIdx.x == 0 && threadIdx.x == 0) {
         if (scale_out != nullptr) *scale_out = s;
         *inv_out = __frcp_rn(s);
     }
@@ -158,15 +180,46 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
             }
         }
     }
+    if (MODE == kRowwise) {
+        // q: the scale of each row; qT: the scale of each column (a row of
+        // x^T).  The tile's 128 + 128 scales are formed once, one per thread.
+        if (t < kTile) {
+            const int r = r0 + t;
+            const bool ok = q != nullptr && r < rows;
+            const float rs = ok ? scale_from_amax(__ldg(scale_src + r), fmt_max) : 0.0f;
+            srow[t] = rs;
+            if (ok && tc == 0) inv_out[r] = __frcp_rn(rs);
+        } else {
+            const int c = c0 + t - kTile;
+            const bool ok = qT != nullptr && c < cols;
+            const float cs = ok ? scale_from_amax(__ldg(col_src + c), fmt_max) : 0.0f;
+            scol[t - kTile] = cs;
+            if (ok && tr == 0) col_inv_out[c] = __frcp_rn(cs);
+        }
+        __syncthreads();
+        float csc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int lr = row_base + 16 * i;
-        const int r = r0 + lr;
-        const uint2 p = cast8<FMT>(v[i], s);
-        if (q != nullptr && col_in && r < rows)
-            *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + c0 + ch * 8) = p;
-        if (qT != nullptr)
-            *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = p;
+        for (int j = 0; j < 8; ++j) csc[j] = scol[ch * 8 + j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int lr = row_base + 16 * i;
+            const int r = r0 + lr;
+            if (q != nullptr && col_in && r < rows)
+                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + c0 + ch * 8) = cast8<FMT>(v[i], srow[lr]);
+            if (qT != nullptr)
+                *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = cast8_each<FMT>(v[i], csc);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int lr = row_base + 16 * i;
+            const int r = r0 + lr;
+            const uint2 p = cast8<FMT>(v[i], s);
+            if (q != nullptr && col_in && r < rows)
+                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + c0 + ch * 8) = p;
+            if (qT != nullptr)
+                *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = p;
+        }
     }
     if (qT == nullptr) return;
     __syncthreads();
@@ -211,12 +264,16 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
 template <int FMT>
 void launch_mode(int mode, bool record, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
                  int tiles_c, int num_tiles, float fmt_max, const float *src, int hist_len, int slot,
-                 float *scale, float *inv, uint8_t *q, uint8_t *qT, unsigned int *rec) {
+                 float *scale, float *inv, uint8_t *q, uint8_t *qT, unsigned int *rec, const float *col_src,
+                 float *col_inv) {
 #define FP8LIN_CAST_LAUNCH(MODE, REC)                                                                        \
     cast_transpose_kernel<FMT, MODE, REC><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_c, num_tiles,  \
                                                                           fmt_max, src, hist_len, slot,      \
-                                                                          scale, inv, q, qT, rec)
-    if (mode == kDynamic)
+                                                                          scale, inv, q, qT, rec, col_src,   \
+                                                                          col_inv)
+    if (mode == kRowwise)
+        FP8LIN_CAST_LAUNCH(kRowwise, false);
+    else if (mode == kDynamic)
         FP8LIN_CAST_LAUNCH(kDynamic, false);
     else if (mode == kStatic && !record)
         FP8LIN_CAST_LAUNCH(kStatic, false);
@@ -242,19 +299,31 @@ fp8lin_status set_carveouts(int device) {
     if (st == FP8LIN_OK)
         st = prefer_max_shared_carveout(
             reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kDelayed, true>), device, base + 3);
+    if (st == FP8LIN_OK)
+        st = prefer_max_shared_carveout(
+            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kRowwise, false>), device, base + 20);
     return st;
 }
 
 // Checks shared by the three scalings, then the launch.
 fp8lin_status cast_common(int mode, const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
                           const float *src, int hist_len, int slot, float *scale, float *inv_scale, uint8_t *q,
-                          uint8_t *qT, float *amax_record, cudaStream_t stream) {
+                          uint8_t *qT, float *amax_record, cudaStream_t stream, const float *col_src = nullptr,
+                          float *col_inv = nullptr) {
     using namespace fp8lin;
-    if (src == nullptr || inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
-    if (mode != kStatic && scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (mode == kRowwise) {
+        // q needs the row statistics and receives row inverse scales; qT the column ones
+        if (q != nullptr && (src == nullptr || inv_scale == nullptr)) return FP8LIN_ERR_INVALID_ARG;
+        if (qT != nullptr && (col_src == nullptr || col_inv == nullptr)) return FP8LIN_ERR_INVALID_ARG;
+        if (!aligned(col_src, 4) || !aligned(col_inv, 4)) return FP8LIN_ERR_MISALIGNED;
+    } else {
+        if (src == nullptr || inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+        if (mode != kStatic && scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    }
     if (rows < 0 || cols < 0) return FP8LIN_ERR_INVALID_ARG;
     if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
     if (mode != kStatic && (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f))) return FP8LIN_ERR_INVALID_ARG;
+    if (mode == kRowwise && rows * cols == 0) return FP8LIN_OK;  // no rows or columns: nothing to scale
     const bool empty = rows == 0 || cols == 0;
     if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
     if (!aligned(src, 4) || !aligned(scale, 4) || !aligned(inv_scale, 4) || !aligned(amax_record, 4))
@@ -278,10 +347,10 @@ fp8lin_status cast_common(int mode, const void *x, int64_t rows, int64_t cols, f
     unsigned int *rec = reinterpret_cast<unsigned int *>(amax_record);
     if (fmt == FP8LIN_E4M3)
         launch_mode<FP8LIN_E4M3>(mode, record, grid, stream, xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max,
-                                 src, hist_len, slot, scale, inv_scale, q, qT, rec);
+                                 src, hist_len, slot, scale, inv_scale, q, qT, rec, col_src, col_inv);
     else
         launch_mode<FP8LIN_E5M2>(mode, record, grid, stream, xs, (int)rows, (int)cols, tc, (int)num_tiles, fmt_max,
-                                 src, hist_len, slot, scale, inv_scale, q, qT, rec);
+                                 src, hist_len, slot, scale, inv_scale, q, qT, rec, col_src, col_inv);
     return check_launch();
 }
 
@@ -312,4 +381,13 @@ extern "C" fp8lin_status fp8lin_cast_transpose_delayed(const void *x, int64_t ro
         return FP8LIN_ERR_INVALID_ARG;
     return cast_common(kDelayed, x, rows, cols, fmt, fmt_max, amax_history, (int)history_len, (int)slot, scale,
                        inv_scale, q, qT, amax_history + slot, stream);
+}
+
+extern "C" fp8lin_status fp8lin_cast_transpose_rowwise(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                                       float fmt_max, const float *row_amax, const float *col_amax,
+                                                       float *row_inv_scale, float *col_inv_scale, uint8_t *q,
+                                                       uint8_t *qT, cudaStream_t stream) {
+    if (q == nullptr && qT == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    return cast_common(kRowwise, x, rows, cols, fmt, fmt_max, row_amax, 0, 0, nullptr, row_inv_scale, q, qT, nullptr,
+                       stream, col_amax, col_inv_scale);
 }

@@ -239,6 +239,10 @@ struct TileMap {
 
 // --------------------------------------------------------------- kernel
 
+// VEC = false: inv_a, inv_b point to one float each (per-tensor scaling).
+// VEC = true:  inv_a[P] and inv_b[Q] hold one inverse scale per row of A and
+//              per row of B (row-wise scaling): C[p][q] = acc * (inv_a[p] * inv_b[q]).
+template <bool VEC>
 __global__ void __launch_bounds__(kThreads, 1)
 fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    __nv_bfloat16 *__restrict__ C, int P, int Q, int R, const float *__restrict__ inv_a,
@@ -377,7 +381,7 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     } else {
         // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
         const int sub = warp % 4;  // TMEM sub-partition this warp may read: lanes 32 sub .. 32 sub + 31
-        const float sc = __fmul_rn(__ldg(inv_a), __ldg(inv_b));
+        const float sc = VEC ? 0.0f : __fmul_rn(__ldg(inv_a), __ldg(inv_b));
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < num_tiles; t += npairs) {
@@ -390,25 +394,42 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             const int row = tm * kPairM + (int)rank * kBM + sub * 32 + lane;
             __nv_bfloat16 *crow = C + (int64_t)row * Q;
             const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kPairN);
+            const float sa = (VEC && row < P) ? __ldg(inv_a + row) : 0.0f;
 #pragma unroll 1
             for (int c = 0; c < kPairN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
-                tmem_ld_wait();
                 const int col0 = tn * kPairN + c * 32;
+                float f[32];
+                if (VEC) {
+                    // one inverse scale per output column: the same 32 floats for every lane
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const float4 b4 = (col0 + 4 * g < Q) ? __ldg(reinterpret_cast<const float4 *>(inv_b + col0) + g)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                        f[4 * g + 0] = __fmul_rn(sa, b4.x);
+                        f[4 * g + 1] = __fmul_rn(sa, b4.y);
+                        f[4 * g + 2] = __fmul_rn(sa, b4.z);
+                        f[4 * g + 3] = __fmul_rn(sa, b4.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) f[j] = sc;
+                }
+                tmem_ld_wait();
                 if (row < P) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         if (col0 + 8 * g < Q) {
                             uint4 o;
-                            o.x = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 0]), sc),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 1]), sc));
-                            o.y = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 2]), sc),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 3]), sc));
-                            o.z = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 4]), sc),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 5]), sc));
-                            o.w = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 6]), sc),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 7]), sc));
+                            o.x = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 0]), f[8 * g + 0]),
+                                              __fmul_rn(__uint_as_float(r[8 * g + 1]), f[8 * g + 1]));
+                            o.y = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 2]), f[8 * g + 2]),
+                                              __fmul_rn(__uint_as_float(r[8 * g + 3]), f[8 * g + 3]));
+                            o.z = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 4]), f[8 * g + 4]),
+                                              __fmul_rn(__uint_as_float(r[8 * g + 5]), f[8 * g + 5]));
+                            o.w = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 6]), f[8 * g + 6]),
+                                              __fmul_rn(__uint_as_float(r[8 * g + 7]), f[8 * g + 7]));
                             *reinterpret_cast<uint4 *>(crow + col0 + 8 * g) = o;
                         }
                     }
@@ -483,8 +504,8 @@ uint32_t make_idesc(fp8lin_fmt fa, fp8lin_fmt fb) {
     return d;
 }
 
-std::atomic<bool> g_smem_attr_set[64];
-std::atomic<int> g_max_clusters[64];
+std::atomic<bool> g_smem_attr_set[2][64];
+std::atomic<int> g_max_clusters[2][64];
 
 cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
@@ -501,11 +522,13 @@ cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttrib
     return cfg;
 }
 
+template <bool VEC>
 fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const uint8_t *B, fp8lin_fmt fb,
                       const float *inv_b, void *C, int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
     using namespace fp8lin;
     if (inv_a == nullptr || inv_b == nullptr) return FP8LIN_ERR_INVALID_ARG;
     if (P < 0 || Q < 0 || R < 0) return FP8LIN_ERR_INVALID_ARG;
+    if (VEC && (!aligned(inv_a, 16) || !aligned(inv_b, 16))) return FP8LIN_ERR_MISALIGNED;
     const bool empty_out = P == 0 || Q == 0;
     if (!empty_out && C == nullptr) return FP8LIN_ERR_INVALID_ARG;
     if (!empty_out && R > 0 && (A == nullptr || B == nullptr)) return FP8LIN_ERR_INVALID_ARG;
@@ -529,32 +552,32 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         return FP8LIN_ERR_CUDA;
 
     if (dev.device >= 64) return FP8LIN_ERR_CUDA;
-    if (!g_smem_attr_set[dev.device].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(fp8_gemm_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (!g_smem_attr_set[VEC][dev.device].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(fp8_gemm_tn_kernel<VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(fp8_gemm_tn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+            cudaFuncSetAttribute(fp8_gemm_tn_kernel<VEC>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return FP8LIN_ERR_CUDA;
         // pairs that can be resident at once (a GPC with an odd number of free SMs leaves one idle)
         int clusters = 0;
         cudaLaunchAttribute attr;
         cudaLaunchConfig_t cfg = launch_config(2 * (dev.sm_count / 2), nullptr, &attr);
-        if (cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_tn_kernel, &cfg) != cudaSuccess || clusters < 1)
+        if (cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_tn_kernel<VEC>, &cfg) != cudaSuccess || clusters < 1)
             clusters = dev.sm_count / 2;
-        g_max_clusters[dev.device].store(clusters, std::memory_order_relaxed);
-        g_smem_attr_set[dev.device].store(true, std::memory_order_release);
+        g_max_clusters[VEC][dev.device].store(clusters, std::memory_order_relaxed);
+        g_smem_attr_set[VEC][dev.device].store(true, std::memory_order_release);
     }
 
     TileMap tm{(int)tiles_m, (int)tiles_n};
     const int num_tiles = (int)(tiles_m * tiles_n);
-    const int max_pairs = g_max_clusters[dev.device].load(std::memory_order_relaxed);
+    const int max_pairs = g_max_clusters[VEC][dev.device].load(std::memory_order_relaxed);
     const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(2 * pairs, stream, &attr);
     __nv_bfloat16 *c = static_cast<__nv_bfloat16 *>(C);
     const int p = (int)P, q = (int)Q, r = (int)R;
     const uint32_t idesc = make_idesc(fa, fb);
-    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel, map_a, map_b, c, p, q, r, inv_a, inv_b, idesc, tm) !=
+    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel<VEC>, map_a, map_b, c, p, q, r, inv_a, inv_b, idesc, tm) !=
         cudaSuccess)
         return FP8LIN_ERR_CUDA;
     return check_launch();
@@ -564,19 +587,37 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
 
 extern "C" fp8lin_status fp8lin_fwd(const uint8_t *xq, const float *inv_x, const uint8_t *wq, const float *inv_w,
                                     void *y, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
-    return gemm_tn(xq, FP8LIN_E4M3, inv_x, wq, FP8LIN_E4M3, inv_w, y, M, N, K, stream);
+    return gemm_tn<false>(xq, FP8LIN_E4M3, inv_x, wq, FP8LIN_E4M3, inv_w, y, M, N, K, stream);
 }
 
 extern "C" fp8lin_status fp8lin_dgrad(const uint8_t *dyq, const float *inv_dy, const uint8_t *wqT,
                                       const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
                                       cudaStream_t stream) {
-    return gemm_tn(dyq, FP8LIN_E5M2, inv_dy, wqT, FP8LIN_E4M3, inv_w, dx, M, K, N, stream);
+    return gemm_tn<false>(dyq, FP8LIN_E5M2, inv_dy, wqT, FP8LIN_E4M3, inv_w, dx, M, K, N, stream);
 }
 
 extern "C" fp8lin_status fp8lin_wgrad(const uint8_t *dyqT, const float *inv_dy, const uint8_t *xqT,
                                       const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
                                       cudaStream_t stream) {
-    return gemm_tn(dyqT, FP8LIN_E5M2, inv_dy, xqT, FP8LIN_E4M3, inv_x, dw, N, K, M, stream);
+    return gemm_tn<false>(dyqT, FP8LIN_E5M2, inv_dy, xqT, FP8LIN_E4M3, inv_x, dw, N, K, M, stream);
+}
+
+extern "C" fp8lin_status fp8lin_fwd_rowwise(const uint8_t *xq, const float *inv_x_rows, const uint8_t *wq,
+                                            const float *inv_w_rows, void *y, int64_t M, int64_t N, int64_t K,
+                                            cudaStream_t stream) {
+    return gemm_tn<true>(xq, FP8LIN_E4M3, inv_x_rows, wq, FP8LIN_E4M3, inv_w_rows, y, M, N, K, stream);
+}
+
+extern "C" fp8lin_status fp8lin_dgrad_rowwise(const uint8_t *dyq, const float *inv_dy_rows, const uint8_t *wqT,
+                                              const float *inv_w_cols, void *dx, int64_t M, int64_t N, int64_t K,
+                                              cudaStream_t stream) {
+    return gemm_tn<true>(dyq, FP8LIN_E5M2, inv_dy_rows, wqT, FP8LIN_E4M3, inv_w_cols, dx, M, K, N, stream);
+}
+
+extern "C" fp8lin_status fp8lin_wgrad_rowwise(const uint8_t *dyqT, const float *inv_dy_cols, const uint8_t *xqT,
+                                              const float *inv_x_cols, void *dw, int64_t M, int64_t N, int64_t K,
+                                              cudaStream_t stream) {
+    return gemm_tn<true>(dyqT, FP8LIN_E5M2, inv_dy_cols, xqT, FP8LIN_E4M3, inv_x_cols, dw, N, K, M, stream);
 }
 
 namespace {

@@ -164,6 +164,41 @@ fp8lin_status fp8lin_cast_transpose_delayed(const void *x, int64_t rows, int64_t
                                             cudaStream_t stream);
 
 /*
+ * Row-wise ("per block") scaling, statistics: row_amax[r] = max_c |x[r][c]|
+ * and col_amax[c] = max_r |x[r][c]| of a bf16 [rows x cols] matrix.
+ * "Lecture 9 exercises": FP8 scaling is one factor per tensor, or even per
+ * block.  The block taken here is one row of each GEMM operand: the finest
+ * block that is constant along the GEMM's contraction, so that its scale
+ * factors out of the sum and is applied in the epilogue.
+ *
+ *   x          device, bf16 [rows x cols] row-major, 16-byte aligned.
+ *   rows, cols >= 0, multiples of 16, <= FP8LIN_MAX_DIM.
+ *   row_amax   device, rows floats, or NULL; cleared by the call first.
+ *   col_amax   device, cols floats, or NULL (not both NULL); cleared first.
+ */
+fp8lin_status fp8lin_amax_rowcol(const void *x, int64_t rows, int64_t cols, float *row_amax,
+                                 float *col_amax, cudaStream_t stream);
+
+/*
+ * Row-wise scaling, cast: q[r][c] = sat_RNE(fp32(x[r][c]) * s_row[r]) and
+ * qT[c][r] = sat_RNE(fp32(x[r][c]) * s_col[c]) with
+ * s_row[r] = fmt_max / max(row_amax[r], 1e-12), s_col[c] likewise from
+ * col_amax; each copy is cast from the bf16 source with the scales of its
+ * own rows, so qT is in general not the byte transpose of q.
+ *
+ *   row_amax, row_inv_scale   device, rows floats: read / receives 1 / s_row
+ *                             (needed when q is not NULL).
+ *   col_amax, col_inv_scale   device, cols floats: read / receives 1 / s_col
+ *                             (needed when qT is not NULL).
+ *   q, qT      device, as for fp8lin_cast_transpose (not both NULL).
+ */
+fp8lin_status fp8lin_cast_transpose_rowwise(const void *x, int64_t rows, int64_t cols,
+                                            fp8lin_fmt fmt, float fmt_max, const float *row_amax,
+                                            const float *col_amax, float *row_inv_scale,
+                                            float *col_inv_scale, uint8_t *q, uint8_t *qT,
+                                            cudaStream_t stream);
+
+/*
  * Forward GEMM of the Float8 linear: Y = bf16_RN( (Xq . Wq^T)_fp32 * (inv_x * inv_w) ).
  * Source: Float8 applied to the linear layer's matmul (TorchTitan analysis
  * page, section 3.3).
@@ -209,6 +244,25 @@ fp8lin_status fp8lin_dgrad(const uint8_t *dyq, const float *inv_dy, const uint8_
 fp8lin_status fp8lin_wgrad(const uint8_t *dyqT, const float *inv_dy, const uint8_t *xqT,
                            const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
                            cudaStream_t stream);
+
+/*
+ * The three GEMMs with row-wise scales: C[p][q] = bf16_RN(acc[p][q] *
+ * (inv_a[p] * inv_b[q])), inv_a one float per row of A and inv_b one per row
+ * of B (16-byte aligned device vectors).  Operands, shapes and outputs as for
+ * fp8lin_fwd / fp8lin_dgrad / fp8lin_wgrad:
+ *   fwd   inv_x_rows [M] (X's row scales),   inv_w_rows [N] (W's row scales)
+ *   dgrad inv_dy_rows [M] (dY's row scales), inv_w_cols [K] (W's column scales)
+ *   wgrad inv_dy_cols [N] (dY's column scales), inv_x_cols [K] (X's column scales)
+ */
+fp8lin_status fp8lin_fwd_rowwise(const uint8_t *xq, const float *inv_x_rows, const uint8_t *wq,
+                                 const float *inv_w_rows, void *y, int64_t M, int64_t N, int64_t K,
+                                 cudaStream_t stream);
+fp8lin_status fp8lin_dgrad_rowwise(const uint8_t *dyq, const float *inv_dy_rows, const uint8_t *wqT,
+                                   const float *inv_w_cols, void *dx, int64_t M, int64_t N, int64_t K,
+                                   cudaStream_t stream);
+fp8lin_status fp8lin_wgrad_rowwise(const uint8_t *dyqT, const float *inv_dy_cols, const uint8_t *xqT,
+                                   const float *inv_x_cols, void *dw, int64_t M, int64_t N, int64_t K,
+                                   cudaStream_t stream);
 
 /* Static English description of a status code (never NULL). */
 const char *fp8lin_status_str(fp8lin_status status);
