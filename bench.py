@@ -1,14 +1,18 @@
-"""Benchmark: Float8 linear fwd+bwd TFLOPS (amax and cast included) on the
-Llama-3.1-8B SwiGLU FFN.
+"""Benchmark: Float8 linear fwd+bwd TFLOPS (amax and cast included).
 
-One step is the whole hot path for the FFN's three linears on one batch of
-8192 tokens: for each of w1 and w3 (X [8192 x 4096], W [14336 x 4096],
+Default workload: the Llama-3.1-8B SwiGLU FFN (``--workload ffn8b``).  One
+step is the whole hot path for the FFN's three linears on one batch of 8192
+tokens: for each of w1 and w3 (X [8192 x 4096], W [14336 x 4096],
 dY [8192 x 14336]) and w2 (H [8192 x 14336], W [4096 x 14336],
-dY [8192 x 4096]): amax of X, W, dY; scale + cast + transpose of each; the
-forward, input-gradient and weight-gradient FP8 GEMMs.  Nothing is cached
-across steps (dynamic scaling recomputes every statistic every step).
+dY [8192 x 4096]): the statistics and casts of X, W and dY (X once for w1
+and w3) and the forward, input-gradient and weight-gradient FP8 GEMMs.
+``--workload block8b`` adds the attention block's fused QKV [4096 -> 6144]
+and output [4096 -> 4096] projections: every linear of one Llama-3.1-8B
+transformer block.  Nothing is cached across steps (dynamic scaling
+recomputes every statistic every step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload ffn8b|block8b] [--scaling dynamic|delayed|rowwise]
 
 Prints one JSON line on rank 0.  N > 1 runs under torchrun: each rank runs
 its own replica on its own batch (the path has no exchange step), timing is
@@ -18,13 +22,13 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
 import sys
 import tempfile
 import time
+from dataclasses import dataclass
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -35,35 +39,96 @@ import numpy as np  # noqa: E402
 import workloads as wl  # noqa: E402
 
 METRIC = "FP8 linear fwd+bwd TFLOPS incl. amax/cast, % of GB300 dense FP8 peak"
-WORKLOAD = "llama3.1-8b-swiglu-ffn"
 FP8_PER_BF16 = 2.0            # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+E4M3, E5M2 = 0, 1
 
 
-# ----------------------------------------------------------------- inputs
+# ---------------------------------------------------------- step graphs
 
-def ffn_layers():
-    """(name, workload, x tensor id, w tensor id, dy tensor id) for w1, w3, w2."""
-    w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
-    w2 = wl.WORKLOADS["llama3_8b_ffn_w2"]
-    return [("w1", w13, wl.X, wl.W, wl.DY), ("w3", w13, wl.X, wl.W3, wl.DY3), ("w2", w2, wl.X, wl.W, wl.DY)]
-
-
-def step_flops() -> int:
-    return sum(w.flops for _, w, *_ in ffn_layers())
+@dataclass(frozen=True)
+class Linear:
+    name: str
+    workload: str          # key of workloads.WORKLOADS (shape, distributions, seed)
+    x: str                 # key of the activation it reads (shared keys are cast once)
+    w_id: int              # tensor ids of W and dY inside the workload's streams
+    dy_id: int
 
 
-def host_inputs(rank: int):
-    """bf16 bit patterns for one step; activations and gradients per rank."""
+@dataclass(frozen=True)
+class Spec:
+    """One training step over several Float8 linears.
+
+    gemms: issue order on the main stream, as (linear, "fwd"|"dgrad"|"wgrad").
+    avail: for every cast input, the GEMM after which its bf16 data exists
+           (None = at the start of the step).  A cast that its first consumer
+           needs right after the data appears runs on the main stream; any
+           other runs on the side stream, released just before the GEMM that
+           follows its producer, so it hides under GEMMs."""
+    name: str
+    description: str
+    linears: tuple
+    gemms: tuple
+    avail: dict
+
+
+_FFN_LINEARS = (Linear("w1", "llama3_8b_ffn_w13", "xf", wl.W, wl.DY),
+                Linear("w3", "llama3_8b_ffn_w13", "xf", wl.W3, wl.DY3),
+                Linear("w2", "llama3_8b_ffn_w2", "h", wl.W, wl.DY))
+_FFN_GEMMS = (("w1", "fwd"), ("w3", "fwd"), ("w2", "fwd"), ("w2", "dgrad"), ("w2", "wgrad"),
+              ("w1", "dgrad"), ("w1", "wgrad"), ("w3", "dgrad"), ("w3", "wgrad"))
+_FFN_AVAIL = {
+    "xf": None, "w:w1": None, "w:w3": None, "w:w2": None,
+    "h": ("w3", "fwd"),          # H = silu(Y1) * Y3
+    "dy:w2": ("w3", "fwd"),      # upstream gradient: cast under w2's forward (a deeper layer's wgrad in a full model)
+    "dy:w1": ("w2", "dgrad"),    # dY1, dY3 derive from dH through the SwiGLU backward
+    "dy:w3": ("w2", "dgrad"),
+}
+
+SPECS = {
+    "ffn8b": Spec(
+        "llama3.1-8b-swiglu-ffn",
+        "Llama-3.1-8B SwiGLU FFN: w1, w3 (M8192 K4096 N14336, shared X) and w2 (M8192 K14336 N4096)",
+        _FFN_LINEARS, _FFN_GEMMS, _FFN_AVAIL),
+    "block8b": Spec(
+        "llama3.1-8b-block-linears",
+        "every linear of one Llama-3.1-8B block: fused QKV (M8192 K4096 N6144), O (M8192 K4096 N4096), "
+        "w1, w3 (M8192 K4096 N14336, shared X) and w2 (M8192 K14336 N4096)",
+        (Linear("qkv", "llama3_8b_qkv", "xa", wl.W, wl.DY), Linear("o", "llama3_8b_o", "xo", wl.W, wl.DY))
+        + _FFN_LINEARS,
+        (("qkv", "fwd"), ("o", "fwd")) + _FFN_GEMMS
+        + (("o", "dgrad"), ("o", "wgrad"), ("qkv", "dgrad"), ("qkv", "wgrad")),
+        {**_FFN_AVAIL, "xa": None, "w:qkv": None, "w:o": None,
+         "xo": ("qkv", "fwd"),       # attention output
+         "xf": ("o", "fwd"),         # FFN input: residual + norm after the attention block
+         "dy:o": ("w3", "dgrad"),    # dX of w1 and w3 summed, through the residual
+         "dy:qkv": ("o", "dgrad")}), # through the attention backward
+}
+
+
+def spec_flops(spec: Spec) -> int:
+    return sum(wl.WORKLOADS[l.workload].flops for l in spec.linears)
+
+
+def cast_inputs(spec: Spec):
+    """Every bf16 tensor the step casts: key -> (rows, cols, fmt, workload, dist, seed, tensor id, outliers)."""
     out = {}
-    for name, w, xid, wid, did in ffn_layers():
-        xkey = (w.name, xid, rank)
-        if xkey not in out:
-            out[xkey] = wl.generate((w.M, w.K), *w.x, seed=w.seed + 1000 * rank, tensor_id=xid)
-        out[(name, "w")] = wl.generate((w.N, w.K), *w.w, seed=w.seed, tensor_id=wid)
-        out[(name, "dy")] = wl.generate((w.M, w.N), *w.dy, seed=w.seed + 1000 * rank, tensor_id=did)
-        out[(name, "x")] = out[xkey]
-    return {k: v for k, v in out.items() if isinstance(k[1], str)}
+    for l in spec.linears:
+        w = wl.WORKLOADS[l.workload]
+        out.setdefault(l.x, (w.M, w.K, E4M3, w, w.x, w.seed, wl.X, w.x_outlier_frac))
+        out["w:" + l.name] = (w.N, w.K, E4M3, w, w.w, w.seed, l.w_id, 0.0)
+        out["dy:" + l.name] = (w.M, w.N, E5M2, w, w.dy, w.seed, l.dy_id, 0.0)
+    return out
+
+
+def host_inputs(spec: Spec, rank: int):
+    """bf16 bit patterns of every cast input; activations and gradients per rank."""
+    out = {}
+    for key, (rows, cols, _, w, dist, seed, tid, outl) in cast_inputs(spec).items():
+        per_rank = not key.startswith("w:")
+        out[key] = wl.generate((rows, cols), *dist, seed=seed + (1000 * rank if per_rank else 0),
+                               tensor_id=tid, outlier_frac=outl)
+    return out
 
 
 # ------------------------------------------------------------------ peaks
@@ -152,34 +217,29 @@ class ClockSampler:
 # ---------------------------------------------------------- oracle (CPU)
 
 class OracleSample:
-    """The CPU oracle on a bounded sample of one FFN step: the per-tensor
-    scaling (amax, scale, cast, transpose) of the first `frac` of every
-    tensor's rows and the three GEMMs on `frac` of their output rows (full
-    FP8 operands prepared once, untimed).  Work scales linearly with rows,
-    so the full-step time is the sample time / frac."""
+    """The CPU oracle on a bounded sample of one step: the per-tensor scaling
+    (amax, scale, cast, transpose) of the first `frac` of every cast input's
+    rows and every GEMM on `frac` of its output rows (full FP8 operands
+    prepared once, untimed).  Work scales linearly with rows, so the
+    full-step time is the sample time / frac."""
 
-    def __init__(self, frac: float):
+    def __init__(self, spec: Spec, frac: float):
         import oracle
-        self.o = oracle
-        self.frac = frac
-        self.layers = []
-        for name, w, xid, wid, did in ffn_layers():
-            X = wl.generate((w.M, w.K), *w.x, seed=w.seed, tensor_id=xid)
-            W = wl.generate((w.N, w.K), *w.w, seed=w.seed, tensor_id=wid)
-            D = wl.generate((w.M, w.N), *w.dy, seed=w.seed, tensor_id=did)
-            qx, qw, qd = (oracle.quantize(X, oracle.E4M3), oracle.quantize(W, oracle.E4M3),
-                          oracle.quantize(D, oracle.E5M2))
-            self.layers.append((name, w, X, W, D, qx, qw, qd))
+        self.o, self.spec, self.frac = oracle, spec, frac
+        self.inputs = {}
+        for key, (rows, cols, fmt, w, dist, seed, tid, outl) in cast_inputs(spec).items():
+            bits = wl.generate((rows, cols), *dist, seed=seed, tensor_id=tid, outlier_frac=outl)
+            self.inputs[key] = (bits, fmt, oracle.quantize(bits, fmt))
 
     def run(self) -> float:
         o, f = self.o, self.frac
         t0 = time.perf_counter()
-        for name, w, X, W, D, qx, qw, qd in self.layers:
-            # w3 reads the X already cast for w1
-            todo = ((W, o.E4M3), (D, o.E5M2)) if name == "w3" else ((X, o.E4M3), (W, o.E4M3), (D, o.E5M2))
-            for T, fmt in todo:
-                rows = max(16, int(round(T.shape[0] * f)))
-                o.quantize(T[:rows], fmt)
+        for key, (bits, fmt, _) in self.inputs.items():
+            rows = max(16, int(round(bits.shape[0] * f)))
+            o.quantize(bits[:rows], fmt)
+        for l in self.spec.linears:
+            w = wl.WORKLOADS[l.workload]
+            qx, qw, qd = (self.inputs[k][2] for k in (l.x, "w:" + l.name, "dy:" + l.name))
             rm = np.arange(max(1, int(round(w.M * f))))
             rn = np.arange(max(1, int(round(w.N * f))))
             o.fwd_ref(qx["q"], qx["inv_scale"], qw["q"], qw["inv_scale"], rm)
@@ -188,13 +248,9 @@ class OracleSample:
         return time.perf_counter() - t0
 
     def describe(self) -> str:
-        return (f"one Llama-3.1-8B FFN step (w1, w3, w2) sampled at {self.frac:.5g} of its rows: "
-                f"amax/scale/cast/transpose of that share of X (once for w1 and w3), H, every W and dY, and that share of "
-                f"the output rows of every fwd/dgrad/wgrad GEMM; full-step time = sample time / share")
-
-
-def cpu_baseline_value(sample_s: float, frac: float) -> float:
-    return step_flops() / (sample_s / frac) / 1e12
+        return (f"one step of {self.spec.description}, sampled at {self.frac:.5g} of its rows: "
+                f"amax/scale/cast/transpose of that share of every cast input (shared X once) and that share "
+                f"of the output rows of every fwd/dgrad/wgrad GEMM; full-step time = sample time / share")
 
 
 # ------------------------------------------------------------ reference
@@ -203,19 +259,19 @@ def run_reference(args, rank: int) -> None:
     if rank != 0:
         return
     import oracle
+    spec = SPECS[args.workload]
     frac = args.ref_frac
-    s = OracleSample(frac)
+    s = OracleSample(spec, frac)
     for _ in range(args.warmup):
         s.run()
     times = [s.run() for _ in range(args.steps)]
-    total = sum(times)
-    step_s = total / len(times) / frac
-    value = step_flops() / step_s / 1e12
+    step_s = sum(times) / len(times) / frac
+    value = spec_flops(spec) / step_s / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "data": "synthetic", "config": {"workload": spec.name, "scaling": "dynamic"},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": s.describe()},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -226,41 +282,65 @@ def run_reference(args, rank: int) -> None:
 
 # ------------------------------------------------------------------- ours
 
-class FFNStep:
-    """The Llama-3.1-8B SwiGLU FFN's three Float8 linears as one training
-    step, issued through the public entry points.
+def plan(spec: Spec, overlap: bool = True):
+    """Where each cast runs.  Returns (main_casts, side_casts, needed_by):
+    main_casts[i] are issued on the main stream right before GEMM i;
+    side_casts[i] are released on the side stream just before GEMM i
+    launches; needed_by[key] is the first GEMM that reads the cast."""
+    lin = {l.name: l for l in spec.linears}
+    idx = {g: i for i, g in enumerate(spec.gemms)}
+    first_use = {}
+    for i, (name, which) in enumerate(spec.gemms):
+        l = lin[name]
+        uses = {"fwd": (l.x, "w:" + name), "dgrad": ("dy:" + name, "w:" + name),
+                "wgrad": ("dy:" + name, l.x)}[which]
+        for k in uses:
+            first_use.setdefault(k, i)
+    main_casts = {i: [] for i in range(len(spec.gemms))}
+    side_casts = {i: [] for i in range(len(spec.gemms))}
+    for key in cast_inputs(spec):
+        a = spec.avail[key]
+        release = 0 if a is None else idx[a] + 1
+        n = first_use[key]
+        if release > n:
+            raise ValueError(f"{key} is read by GEMM {n} before it exists")
+        if not overlap or release == n:
+            main_casts[n].append(key)
+        else:
+            side_casts[release].append(key)
+    for i in side_casts:
+        side_casts[i].sort(key=lambda k: first_use[k])
+    return main_casts, side_casts, first_use
 
-    Data dependencies follow the FFN: w1 and w3 read the same X (cast once);
-    w2 reads H = silu(Y1) * Y3, so H's cast waits for both forward GEMMs;
-    dY2 comes from upstream; dY1 and dY3 come from w2's input gradient dH
-    through the SwiGLU backward, so their casts wait for w2's dgrad.  (H, dY1,
-    dY3 and dY2 are seeded synthetic tensors of those shapes; the SwiGLU
-    itself is not part of the linear layer's path.)
 
-    With overlap, every amax / cast runs on a low-priority side stream and
-    the GEMMs on a high-priority main stream, so the HBM-bound scaling work
-    hides behind tensor-bound GEMMs wherever the dependencies allow -- the
-    overlap window the pages describe for FP8 scaling work.  Each step starts
-    after the previous one has finished (the FP8 buffers are reused)."""
+class StepGraph:
+    """A Spec issued through the public entry points on two CUDA streams.
 
-    def __init__(self, fl, dev, dev_in, overlap=True, scaling="dynamic", streams=None):
+    With overlap, casts that have a GEMM to hide under run on a low-priority
+    side stream; the GEMMs, and casts that gate the next GEMM, run on a
+    high-priority main stream.  Side-stream work waits for a marker recorded
+    on the main stream just before the GEMM it should run under is launched,
+    so that GEMM's persistent CTAs are resident first and the HBM-bound
+    kernels fill the SM resources it leaves free -- the overlap window the
+    pages describe for FP8 scaling work.  Each step starts after the previous
+    one has finished (FP8 buffers and outputs are reused)."""
+
+    def __init__(self, fl, spec: Spec, dev, dev_in, overlap=True, scaling="dynamic", streams=None):
         import torch
-        self.fl, self.t = fl, torch
-        self.overlap = overlap
-        self.scaling = scaling
-        w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
-        w2 = wl.WORKLOADS["llama3_8b_ffn_w2"]
-        self.shapes = {"w1": w13, "w3": w13, "w2": w2}
-        F = lambda r, c, f: fl.Float8Tensor(r, c, f, dev, scaling=scaling)
-        self.x8 = F(w13.M, w13.K, fl.E4M3)                          # X, shared by w1 and w3
-        self.h8 = F(w2.M, w2.K, fl.E4M3)                            # H, input of w2
-        self.w8 = {n: F(w.N, w.K, fl.E4M3) for n, w in self.shapes.items()}
-        self.d8 = {n: F(w.M, w.N, fl.E5M2) for n, w in self.shapes.items()}
-        bf = torch.bfloat16
-        self.y = {n: torch.empty((w.M, w.N), dtype=bf, device=dev) for n, w in self.shapes.items()}
-        self.dx = {n: torch.empty((w.M, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
-        self.dw = {n: torch.empty((w.N, w.K), dtype=bf, device=dev) for n, w in self.shapes.items()}
+        self.fl, self.t, self.spec = fl, torch, spec
+        self.overlap, self.scaling = overlap, scaling
         self.inp = dev_in
+        self.lin = {l.name: l for l in spec.linears}
+        self.t8 = {}
+        for key, (rows, cols, fmt, *_) in cast_inputs(spec).items():
+            self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling)
+        bf = torch.bfloat16
+        self.out = {}
+        for l in spec.linears:
+            w = wl.WORKLOADS[l.workload]
+            self.out[l.name] = {"fwd": torch.empty((w.M, w.N), dtype=bf, device=dev),
+                                "dgrad": torch.empty((w.M, w.K), dtype=bf, device=dev),
+                                "wgrad": torch.empty((w.N, w.K), dtype=bf, device=dev)}
         if streams is not None:
             self.main, self.side = streams
         elif overlap:
@@ -268,21 +348,25 @@ class FFNStep:
             self.side = torch.cuda.Stream(device=dev, priority=0)
         else:
             self.main = self.side = torch.cuda.current_stream(dev)
-        # per quantised tensor (X, H, three W, three dY): amax + cast (dynamic)
-        # or the cast alone (delayed: it records the amax itself); 9 GEMMs
-        self.kernels_per_step = (2 if scaling in ("dynamic", "rowwise") else 1) * 8 + 9
+        self._plan()
+        per_cast = 2 if scaling in ("dynamic", "rowwise") else 1
+        self.kernels_per_step = per_cast * len(self.t8) + len(spec.gemms)
+
+    def _plan(self):
+        self.main_casts, self.side_casts, self.needed_by = plan(self.spec, self.overlap)
 
     def describe(self):
-        how = f"{self.scaling} per-tensor scaling; "
+        how = f"{self.scaling} per-tensor scaling" if self.scaling != "rowwise" else "row-wise (per-block) scaling"
         if not self.overlap:
-            return how + "serial: one stream, X cast once for w1 and w3"
-        return how + ("two streams: casts that the FFN dependencies leave hidable run on a "
-                      "low-priority side stream under the GEMMs of a high-priority main stream; "
-                      "X, W1 and H gate a GEMM and run on the main stream; X cast once for w1 and w3")
+            return how + "; serial: one stream, shared X cast once"
+        return how + ("; two streams: casts that the data dependencies leave hidable run on a low-priority side "
+                      "stream under the GEMMs of a high-priority main stream; casts that gate the next GEMM run on "
+                      "the main stream; shared X cast once")
 
     def outputs(self):
-        return [t for n in ("w1", "w3", "w2") for t in (self.y[n], self.dx[n], self.dw[n])]
+        return [self.out[l.name][w] for l in self.spec.linears for w in ("fwd", "dgrad", "wgrad")]
 
+    # -- issue -------------------------------------------------------------
     def _ev(self):
         return self.t.cuda.Event(enable_timing=True)
 
@@ -296,127 +380,80 @@ class FFNStep:
         e1.record(stream)
         rec.append((kind, label, e0, e1, work))
 
-    def _quantize(self, rec, label, x, t8, stream=None):
-        fl, s = self.fl, (self.side if stream is None else stream)
+    def _cast(self, rec, key, stream):
+        fl, x, t8 = self.fl, self.inp[key], self.t8[key]
         n = x.numel()
         if t8.scaling == "rowwise":
-            self._mark(s, rec, "amax", label, 2 * n,
-                       lambda: fl.fp8lin_amax_rowcol(x, t8.row_amax, t8.col_amax, s))
-            self._mark(s, rec, "cast", label, 4 * n, lambda: fl.fp8lin_cast_transpose_rowwise(
-                x, t8.fmt, t8.row_amax, t8.col_amax, t8.row_inv, t8.col_inv, t8.q, t8.qT, t8.fmt_max, s))
-            return
-        if t8.scaling != "dynamic":
-            self._mark(s, rec, "cast", label, 4 * n, lambda: t8.quantize(x, s))
-            return
-        self._mark(s, rec, "amax", label, 2 * n, lambda: fl.fp8lin_amax(x, t8.amax, s))
-        self._mark(s, rec, "cast", label, 4 * n, lambda: fl.fp8lin_cast_transpose(
-            x, t8.fmt, t8.amax, t8.scale, t8.inv_scale, t8.q, t8.qT, t8.fmt_max, s))
-
-    def _signal(self, stream):
-        if not self.overlap:
-            return None
-        e = self.t.cuda.Event()
-        e.record(stream)
-        return e
-
-    def _wait(self, stream, ev):
-        if ev is not None:
-            stream.wait_event(ev)
+            self._mark(stream, rec, "amax", key, 2 * n,
+                       lambda: fl.fp8lin_amax_rowcol(x, t8.row_amax, t8.col_amax, stream))
+            self._mark(stream, rec, "cast", key, 4 * n, lambda: fl.fp8lin_cast_transpose_rowwise(
+                x, t8.fmt, t8.row_amax, t8.col_amax, t8.row_inv, t8.col_inv, t8.q, t8.qT, t8.fmt_max, stream))
+        elif t8.scaling == "dynamic":
+            self._mark(stream, rec, "amax", key, 2 * n, lambda: fl.fp8lin_amax(x, t8.amax, stream))
+            self._mark(stream, rec, "cast", key, 4 * n, lambda: fl.fp8lin_cast_transpose(
+                x, t8.fmt, t8.amax, t8.scale, t8.inv_scale, t8.q, t8.qT, t8.fmt_max, stream))
+        else:
+            self._mark(stream, rec, "cast", key, 4 * n, lambda: t8.quantize(x, stream))
 
     def _gemm(self, rec, name, which):
         fl, m = self.fl, self.main
-        w = self.shapes[name]
-        work = 2 * w.M * w.N * w.K
-        x8 = self.x8 if name != "w2" else self.h8
-        w8, d8 = self.w8[name], self.d8[name]
+        l = self.lin[name]
+        w = wl.WORKLOADS[l.workload]
+        x8, w8, d8 = self.t8[l.x], self.t8["w:" + name], self.t8["dy:" + name]
+        out = self.out[name][which]
         if self.scaling == "rowwise":
-            if which == "fwd":
-                fn = lambda: fl.fp8lin_fwd_rowwise(x8.q, x8.row_inv, w8.q, w8.row_inv, self.y[name], m)
-            elif which == "dgrad":
-                fn = lambda: fl.fp8lin_dgrad_rowwise(d8.q, d8.row_inv, w8.qT, w8.col_inv, self.dx[name], m)
-            else:
-                fn = lambda: fl.fp8lin_wgrad_rowwise(d8.qT, d8.col_inv, x8.qT, x8.col_inv, self.dw[name], m)
-            self._mark(m, rec, "gemm", f"{name}.{which}", work, fn)
-            return
-        if which == "fwd":
-            fn = lambda: fl.fp8lin_fwd(x8.q, x8.inv_scale, w8.q, w8.inv_scale, self.y[name], m)
-        elif which == "dgrad":
-            fn = lambda: fl.fp8lin_dgrad(d8.q, d8.inv_scale, w8.qT, w8.inv_scale, self.dx[name], m)
+            fn = {"fwd": lambda: fl.fp8lin_fwd_rowwise(x8.q, x8.row_inv, w8.q, w8.row_inv, out, m),
+                  "dgrad": lambda: fl.fp8lin_dgrad_rowwise(d8.q, d8.row_inv, w8.qT, w8.col_inv, out, m),
+                  "wgrad": lambda: fl.fp8lin_wgrad_rowwise(d8.qT, d8.col_inv, x8.qT, x8.col_inv, out, m)}[which]
         else:
-            fn = lambda: fl.fp8lin_wgrad(d8.qT, d8.inv_scale, x8.qT, x8.inv_scale, self.dw[name], m)
-        self._mark(m, rec, "gemm", f"{name}.{which}", work, fn)
+            fn = {"fwd": lambda: fl.fp8lin_fwd(x8.q, x8.inv_scale, w8.q, w8.inv_scale, out, m),
+                  "dgrad": lambda: fl.fp8lin_dgrad(d8.q, d8.inv_scale, w8.qT, w8.inv_scale, out, m),
+                  "wgrad": lambda: fl.fp8lin_wgrad(d8.qT, d8.inv_scale, x8.qT, x8.inv_scale, out, m)}[which]
+        self._mark(m, rec, "gemm", f"{name}.{which}", 2 * w.M * w.N * w.K, fn)
 
     def run(self, rec=None):
-        """One step.  Side-stream work that should run under a GEMM waits for
-        a marker recorded on the main stream just before that GEMM's launch,
-        so the GEMM's persistent CTAs are resident first and the HBM-bound
-        kernels fill the SM resources the GEMM leaves free."""
-        inp, m, s = self.inp, self.main, self.side
-        # X and W1 gate the first GEMM: nothing to hide them behind, so they
-        # run on the main stream (no cross-stream hop).
-        self._quantize(rec, "x", inp[("w1", "x")], self.x8, m)
-        self._quantize(rec, "w1", inp[("w1", "w")], self.w8["w1"], m)
-        g = self._signal(m)                               # w1 fwd about to launch
-        self._gemm(rec, "w1", "fwd")
-        self._wait(s, g)
-        self._quantize(rec, "w3", inp[("w3", "w")], self.w8["w3"])
-        e_w3 = self._signal(s)
-        self._quantize(rec, "w2", inp[("w2", "w")], self.w8["w2"])
-        e_w2 = self._signal(s)
-        self._wait(m, e_w3)
-        self._gemm(rec, "w3", "fwd")
-        # H = silu(Y1) * Y3 needs both forward outputs; it gates w2's forward
-        # GEMM, so it too runs on the main stream.
-        self._quantize(rec, "h", inp[("w2", "x")], self.h8, m)
-        self._wait(m, e_w2)
-        g = self._signal(m)                               # w2 fwd about to launch
-        self._wait(s, g)
-        self._quantize(rec, "dy2", inp[("w2", "dy")], self.d8["w2"])
-        e_d2 = self._signal(s)
-        self._gemm(rec, "w2", "fwd")
-        self._wait(m, e_d2)
-        self._gemm(rec, "w2", "dgrad")
-        e_dh = self._signal(m)                            # dY1, dY3 derive from dH
-        g = self._signal(m)
-        self._gemm(rec, "w2", "wgrad")
-        self._wait(s, e_dh)
-        self._wait(s, g)
-        self._quantize(rec, "dy1", inp[("w1", "dy")], self.d8["w1"])
-        e_d1 = self._signal(s)
-        self._quantize(rec, "dy3", inp[("w3", "dy")], self.d8["w3"])
-        e_d3 = self._signal(s)
-        self._wait(m, e_d1)
-        self._gemm(rec, "w1", "dgrad")
-        self._gemm(rec, "w1", "wgrad")
-        self._wait(m, e_d3)
-        self._gemm(rec, "w3", "dgrad")
-        self._gemm(rec, "w3", "wgrad")
+        m, s = self.main, self.side
+        ready = {}
+        for i, (name, which) in enumerate(self.spec.gemms):
+            for key in self.main_casts[i]:
+                self._cast(rec, key, m)
+            if self.side_casts[i]:
+                marker = self.t.cuda.Event()
+                marker.record(m)                      # this GEMM is about to launch
+                s.wait_event(marker)
+                for key in self.side_casts[i]:
+                    self._cast(rec, key, s)
+                    e = self.t.cuda.Event()
+                    e.record(s)
+                    ready[key] = e
+            for key, e in list(ready.items()):
+                if self.needed_by[key] == i:
+                    m.wait_event(e)
+                    del ready[key]
+            self._gemm(rec, name, which)
 
 
-def run_e2e(args, fl, dev, host, ffn, world, dist, barrier):
-    """The same FFN step measured end to end from pinned host memory: every
-    step uploads its bf16 inputs (X, H, three W, three dY) and reads back all
-    nine outputs (Y, dX, dW of w1, w3, w2).  Inputs and outputs are double
-    buffered so that step i+1's upload and step i's readback run on their own
-    copy streams while step i computes."""
+def run_e2e(args, fl, spec, dev, host, step, world, dist, barrier):
+    """The same step measured end to end from pinned host memory: every step
+    uploads every bf16 input and reads back every output (Y, dX, dW of each
+    linear).  Inputs and outputs are double buffered so that step i+1's
+    upload and step i's readback run on their own copy streams while step i
+    computes."""
     import torch
-    pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-              for k, v in host.items() if not (k[0] == "w3" and k[1] == "x")}
+    pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in host.items()}
     h2d_bytes = sum(t.numel() * 2 for t in pinned.values())
     sets = []
     for k in range(2):
         din = {key: torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for key, t in pinned.items()}
-        din[("w3", "x")] = din[("w1", "x")]
-        f = ffn if k == 0 else FFNStep(fl, dev, din, overlap=ffn.overlap, scaling=ffn.scaling,
-                                       streams=(ffn.main, ffn.side))
-        if k == 0:
-            f.inp = din
-        outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in f.outputs()]
-        sets.append((f, din, outs))
+        g = step if k == 0 else StepGraph(fl, spec, dev, din, overlap=step.overlap, scaling=step.scaling,
+                                          streams=(step.main, step.side))
+        g.inp = din
+        outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in g.outputs()]
+        sets.append((g, din, outs))
     d2h_bytes = sum(t.numel() * t.element_size() for t in sets[0][2])
     copy_in = torch.cuda.Stream(device=dev)
     copy_out = torch.cuda.Stream(device=dev)
-    main = ffn.main
+    main = step.main
 
     def run(n, timed):
         ev = lambda: torch.cuda.Event(enable_timing=timed)
@@ -442,14 +479,14 @@ def run_e2e(args, fl, dev, host, ffn, world, dist, barrier):
             main.wait_event(ev_in[k])
             if ev_out[k] is not None:
                 main.wait_event(ev_out[k])               # step i-2's outputs have left set k
-            f, _, outs = sets[k]
-            f.run()
+            g, _, outs = sets[k]
+            g.run()
             e = ev()
             e.record(main)
             ev_done[k] = e
             copy_out.wait_event(e)
             with torch.cuda.stream(copy_out):
-                for o, d in zip(outs, f.outputs()):
+                for o, d in zip(outs, g.outputs()):
                     o.copy_(d, non_blocking=True)
             e = ev()
             e.record(copy_out)
@@ -466,7 +503,7 @@ def run_e2e(args, fl, dev, host, ffn, world, dist, barrier):
         t = torch.tensor([e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e_ms = float(t.item())
-    return {"value": world * step_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+    return {"value": world * spec_flops(spec) / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
             "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": e_ms,
             "pipeline": "double-buffered: upload of step i+1 and readback of step i overlap step i's compute"}
 
@@ -475,6 +512,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     import torch
     import float8_linear_layers_gb300 as fl
 
+    spec = SPECS[args.workload]
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     dist = None
@@ -482,17 +520,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    host = host_inputs(rank)
-    def up(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-    dev_in = {k: up(v) for k, v in host.items()}
-    dev_in[("w3", "x")] = dev_in[("w1", "x")]   # w1 and w3 read the same X
-    ffn = FFNStep(fl, dev, dev_in, overlap=not args.serial, scaling=args.scaling)
-    stream = ffn.main
+    host = host_inputs(spec, rank)
+    dev_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in host.items()}
+    step = StepGraph(fl, spec, dev, dev_in, overlap=not args.serial, scaling=args.scaling)
+    stream = step.main
     torch.cuda.set_stream(stream)
-
-    def step(events=None):
-        ffn.run(events)
 
     def barrier():
         if dist is not None:
@@ -500,7 +532,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step()
+        step.run()
     barrier()
 
     # ---- timed region (device-resident inputs)
@@ -513,7 +545,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     barrier()
     t_start.record(stream)
     for _ in range(args.steps):
-        step(events)
+        step.run(events)
     t_end.record(stream)
     barrier()
     clocks = sampler.stop()
@@ -526,15 +558,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     # per-kernel times from the events (each pair brackets one launch on its stream)
     kern = {"gemm": [0.0, 0], "amax": [0.0, 0], "cast": [0.0, 0]}
-    w1_fwd_ms, w1_fwd_n = 0.0, 0
     per_layer = {}
+    w1_fwd_ms, w1_fwd_n = 0.0, 0
     for kind, label, e0, e1, work in events:
         ms = e0.elapsed_time(e1)
         kern[kind][0] += ms
         kern[kind][1] += work
         if kind == "gemm":
-            lay = label.split(".")[0]
-            pl = per_layer.setdefault(lay, [0.0, 0])
+            pl = per_layer.setdefault(label.split(".")[0], [0.0, 0])
             pl[0] += ms
             pl[1] += work
             if label == "w1.fwd":
@@ -559,23 +590,21 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
     fp8_peak_burst = peaks["bf16_tflops"] * FP8_PER_BF16
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_flops() / (ms_per_step * 1e-3) / 1e12
+    value = world * spec_flops(spec) / (ms_per_step * 1e-3) / 1e12
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     w1_fwd_tflops = w1_fwd_flops / (w1_fwd_ms / w1_fwd_n * 1e-3) / 1e12
 
-    # ---- end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
-        e2e = run_e2e(args, fl, dev, host, ffn, world, dist, barrier)
+        e2e = run_e2e(args, fl, spec, dev, host, step, world, dist, barrier)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        s = OracleSample(args.cpu_frac)
+        s = OracleSample(spec, args.cpu_frac)
         secs = s.run()
-        cpu = {"value": cpu_baseline_value(secs, args.cpu_frac), "unit": "TFLOPS",
-               "cores": oracle.num_threads(), "kind": "oracle", "sample": s.describe(),
-               "sample_seconds": secs}
+        cpu = {"value": spec_flops(spec) / (secs / args.cpu_frac) / 1e12, "unit": "TFLOPS",
+               "cores": oracle.num_threads(), "kind": "oracle", "sample": s.describe(), "sample_seconds": secs}
 
     if dist is not None:
         dist.barrier()
@@ -588,10 +617,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "scaling": args.scaling,
-                   "linears": {"w1": "M8192 K4096 N14336", "w3": "M8192 K4096 N14336",
-                               "w2": "M8192 K14336 N4096"},
-                   "l2": "inputs larger than L2: one step streams ~2.9 GB of distinct operands through a 129 MB L2",
+        "config": {"workload": spec.name, "scaling": args.scaling, "linears": spec.description,
+                   "l2": "inputs larger than L2: one step streams several GB of distinct operands through a 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": 100.0 * value / world / fp8_peak_sustained,
         "fp8_peak_tflops": {"sustained": fp8_peak_sustained, "burst": fp8_peak_burst,
@@ -612,11 +639,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "hbm_peak_gbs": peaks["hbm_gbs"],
         },
         "per_linear_gemm_tflops": {k: v[1] / (v[0] * 1e-3) / 1e12 for k, v in per_layer.items()},
-        "schedule": ffn.describe(),
+        "schedule": step.describe(),
         "main_stream_idle_before_gemm_ms": {k: round(v, 4) for k, v in gaps.items()},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": ffn.kernels_per_step * args.steps,
+        "gpu_launches": step.kernels_per_step * args.steps,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -700,13 +727,14 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(SPECS), default="ffn8b")
+    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise"], default="dynamic",
+                    help="scaling recipe (the headline metric is dynamic per-tensor)")
+    ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
-    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise"], default="dynamic",
-                    help="per-tensor scaling recipe (the headline metric is dynamic)")
     ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "amax", "cast",
                                                "amax_rowcol", "cast_rowwise"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")

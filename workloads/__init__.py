@@ -189,6 +189,9 @@ WORKLOADS = {
     "llama3_8b_qkv": Workload("llama3_8b_qkv", 8192, 4096, 6144, ("normal", 1.0),
                               ("normal", 0.02), ("normal", 1e-3), seed=1,
                               note="Llama-3.1-8B fused QKV projection, 1 x 8192 tokens"),
+    "llama3_8b_o": Workload("llama3_8b_o", 8192, 4096, 4096, ("normal", 1.0), ("normal", 0.02),
+                            ("normal", 1e-3), seed=6,
+                            note="Llama-3.1-8B attention output projection (used by the whole-block step)"),
     "llama3_8b_ffn_w13": Workload("llama3_8b_ffn_w13", 8192, 4096, 14336, ("normal", 1.0),
                                   ("normal", 0.02), ("normal", 1e-3), seed=2,
                                   note="Llama-3.1-8B SwiGLU FFN w1 (= w3 shape)"),
