@@ -498,14 +498,20 @@ def run_e2e(args, fl, spec, dev, host, step, world, dist, barrier):
     barrier()
     t0, t1 = run(args.e2e_steps, True)
     barrier()
-    e_ms = t0.elapsed_time(t1) / args.e2e_steps
-    if dist is not None:
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(t0.elapsed_time(t1) / args.e2e_steps, dist, dev)
     return {"value": world * spec_flops(spec) / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
             "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": e_ms,
             "pipeline": "double-buffered: upload of step i+1 and readback of step i overlap step i's compute"}
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_ours(args, rank: int, world: int, local_rank: int) -> None:
@@ -549,11 +555,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     t_end.record(stream)
     barrier()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     assert fl.fp8lin_device_error() == 0, "a GEMM kernel reported a timed-out wait"
 
     # per-kernel times from the events (each pair brackets one launch on its stream)
