@@ -32,7 +32,8 @@
 // Halving the B bytes per CTA (32 KB per slab instead of 48 KB for a
 // 128 x 256 single-CTA tile) cuts the L2 -> SM traffic per flop by a third
 // and leaves room for six stages.  Pair tiles are visited in groups of
-// kGroupM row-blocks so that concurrently running pairs share panels in L2.
+// raster groups chosen from the operand sizes (see TileMap), so that the
+// smaller operand is read from DRAM once when it fits in L2.
 //
 // Every mbarrier wait is bounded by wall-clock time (globaltimer).  A wait
 // that runs out records FP8LIN_ERR_TIMEOUT in a device word, raises the
@@ -63,7 +64,8 @@ constexpr int kAStage = kBM * kBK;    // 16 KB
 constexpr int kBStage = kBN * kBK;    // 16 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * kPairN; // two fp32 accumulators of 256 columns
-constexpr int kGroupM = 8;            // pair-tile rows per raster group
+constexpr int64_t kL2Resident = 40ll << 20;  // an operand up to this size is kept resident in L2
+constexpr int64_t kL2GroupBytes = 24ll << 20; // otherwise: panels of one raster group
 constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 1024 /*barriers*/ + 1024 /*alignment*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
@@ -224,16 +226,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ------------------------------------------------------------- schedule
 
+// Pair tiles are visited in groups of `group` tiles along the "inner" axis
+// (rows of A, or columns when `swap`), the inner index running fastest, so
+// that the group's panels of that operand stay in L2 while the other
+// operand's panels stream past them once per group.
 struct TileMap {
-    int tiles_m, tiles_n;
+    int tiles_m, tiles_n, group, swap;
     __device__ __forceinline__ void coords(int t, int &tm, int &tn) const {
-        const int per_group = kGroupM * tiles_n;
+        const int ti = swap ? tiles_n : tiles_m;   // inner axis
+        const int to = swap ? tiles_m : tiles_n;   // outer axis
+        const int per_group = group * to;
         const int g = t / per_group;
-        const int first_m = g * kGroupM;
-        const int gm = min(tiles_m - first_m, kGroupM);
+        const int first = g * group;
+        const int gi = min(ti - first, group);
         const int r = t - g * per_group;
-        tm = first_m + r % gm;
-        tn = r / gm;
+        const int i = first + r % gi, o = r / gi;
+        tm = swap ? o : i;
+        tn = swap ? i : o;
     }
 };
 
@@ -568,7 +577,31 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         g_smem_attr_set[VEC][dev.device].store(true, std::memory_order_release);
     }
 
-    TileMap tm{(int)tiles_m, (int)tiles_n};
+    // Raster: keep the smaller operand resident in L2 and stream the larger
+    // one once; if neither fits, hold groups of ~kL2GroupBytes of panels of
+    // one operand while the other streams past once per group, choosing the
+    // orientation with the fewest modelled DRAM bytes.
+    const int64_t bytes_a = P * R, bytes_b = Q * R;
+    TileMap tm{(int)tiles_m, (int)tiles_n, 1, 0};
+    if (bytes_a <= kL2Resident && bytes_a <= bytes_b) {
+        tm.group = (int)tiles_m;                      // all of A per column of tiles
+    } else if (bytes_b <= kL2Resident) {
+        tm.group = (int)tiles_n;                      // all of B per row of tiles
+        tm.swap = 1;
+    } else {
+        const int64_t panel = (int64_t)kPairM * R;   // bytes of one pair-row (or pair-column) panel
+        int64_t g = kL2GroupBytes / panel;
+        if (g < 1) g = 1;
+        const int64_t gm = g < tiles_m ? g : tiles_m, gn = g < tiles_n ? g : tiles_n;
+        const int64_t traffic_m = bytes_a + bytes_b * ((tiles_m + gm - 1) / gm);   // A panels held
+        const int64_t traffic_n = bytes_b + bytes_a * ((tiles_n + gn - 1) / gn);   // B panels held
+        if (traffic_n < traffic_m) {
+            tm.group = (int)gn;
+            tm.swap = 1;
+        } else {
+            tm.group = (int)gm;
+        }
+    }
     const int num_tiles = (int)(tiles_m * tiles_n);
     const int max_pairs = g_max_clusters[VEC][dev.device].load(std::memory_order_relaxed);
     const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
