@@ -24,11 +24,15 @@ constexpr int kThreads = 256;
 constexpr int kVec = 8;                       // 16-byte vectors per thread
 constexpr int kChunk = kThreads * kVec;       // vectors per block (32 KB)
 
+// Streaming 16-byte load: no L1 allocation, and first in line for L2
+// eviction, so a GEMM running beside this kernel keeps its resident operand.
 __device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+                 : "l"(p), "l"(policy));
     return v;
 }
 

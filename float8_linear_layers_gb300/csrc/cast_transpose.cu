@@ -48,12 +48,32 @@ __device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d) {
 
 // Streaming 16-byte load that does not allocate in L1 (the data is used once;
 // at the shared-memory-heavy carveout L1 is small).
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+__device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+                 : "l"(p), "l"(policy));
     return v;
+}
+
+// L2 policy for data touched once: first in line for eviction, so a GEMM
+// running beside this kernel keeps its resident operand in L2.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void st_stream8(void *p, uint2 v, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream16(void *p, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -154,12 +174,13 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
     const int ch = t % 16;          // chunk within the row (8 columns)
     const int row_base = t / 16;    // rows row_base + 16 i
     const bool col_in = (c0 + ch * 8) < cols;
+    const uint64_t pol = evict_first_policy();
     uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = r0 + row_base + 16 * i;
         if (col_in && r < rows)
-            v[i] = ld_stream16(x + (int64_t)r * cols + c0 + ch * 8);
+            v[i] = ld_stream16(x + (int64_t)r * cols + c0 + ch * 8, pol);
         else
             v[i] = make_uint4(0, 0, 0, 0);
     }
@@ -205,7 +226,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
             const int lr = row_base + 16 * i;
             const int r = r0 + lr;
             if (q != nullptr && col_in && r < rows)
-                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + c0 + ch * 8) = cast8<FMT>(v[i], srow[lr]);
+                st_stream8(q + (int64_t)r * cols + c0 + ch * 8, cast8<FMT>(v[i], srow[lr]), pol);
             if (qT != nullptr)
                 *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = cast8_each<FMT>(v[i], csc);
         }
@@ -216,7 +237,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
             const int r = r0 + lr;
             const uint2 p = cast8<FMT>(v[i], s);
             if (q != nullptr && col_in && r < rows)
-                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + c0 + ch * 8) = p;
+                st_stream8(q + (int64_t)r * cols + c0 + ch * 8, p, pol);
             if (qT != nullptr)
                 *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = p;
         }
@@ -255,8 +276,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
         for (int j = 0; j < 4; ++j) {
             const int c = c0 + 16 * w + 4 * cq + j;
             if (c < cols)
-                *reinterpret_cast<uint4 *>(qT + (int64_t)c * rows + rr) =
-                    make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
+                st_stream16(qT + (int64_t)c * rows + rr, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]), pol);
         }
     }
 }
