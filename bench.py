@@ -106,6 +106,25 @@ SPECS = {
 }
 
 
+def _single(key: str, wname: str, desc: str) -> Spec:
+    """One linear's step: forward, then the gradient dY arrives (upstream)."""
+    return Spec(key, desc, (Linear("l", wname, "x", wl.W, wl.DY),),
+                (("l", "fwd"), ("l", "dgrad"), ("l", "wgrad")),
+                {"x": None, "w:l": None, "dy:l": ("l", "fwd")})
+
+
+SPECS.update({
+    "tiny": _single("tiny", "tiny", "one linear M256 K512 N1024"),
+    "qkv8b": _single("llama3.1-8b-qkv", "llama3_8b_qkv", "Llama-3.1-8B fused QKV, M8192 K4096 N6144"),
+    "w13_8b": _single("llama3.1-8b-ffn-w1", "llama3_8b_ffn_w13", "Llama-3.1-8B FFN w1 (= w3), M8192 K4096 N14336"),
+    "w2_8b": _single("llama3.1-8b-ffn-w2", "llama3_8b_ffn_w2", "Llama-3.1-8B FFN w2, M8192 K14336 N4096"),
+    "w1_70b": _single("llama3.1-70b-ffn-w1", "llama3_70b_ffn_w1",
+                      "Llama-3.1-70B FFN w1 with 0.1% x100 outliers in X, M16384 K8192 N28672"),
+    "w1_405b": _single("llama3.1-405b-ffn-w1", "llama3_405b_ffn_w1",
+                       "Llama-3.1-405B FFN w1 (Laplace dY), M8192 K16384 N53248"),
+})
+
+
 def spec_flops(spec: Spec) -> int:
     return sum(wl.WORKLOADS[l.workload].flops for l in spec.linears)
 
@@ -562,6 +581,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     kern = {"gemm": [0.0, 0], "amax": [0.0, 0], "cast": [0.0, 0]}
     per_layer = {}
     w1_fwd_ms, w1_fwd_n = 0.0, 0
+    # the roofline's launch: w1's forward GEMM where the step has one, else the linear's forward
+    roof_name = "w1" if "w1" in {l.name for l in spec.linears} else spec.linears[0].name
+    roof_label = roof_name + ".fwd"
     for kind, label, e0, e1, work in events:
         ms = e0.elapsed_time(e1)
         kern[kind][0] += ms
@@ -570,7 +592,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             pl = per_layer.setdefault(label.split(".")[0], [0.0, 0])
             pl[0] += ms
             pl[1] += work
-            if label == "w1.fwd":
+            if label == roof_label:
                 w1_fwd_ms += ms
                 w1_fwd_n += 1
     gemm_evs = [(label, e0, e1) for kind, label, e0, e1, _ in events if kind == "gemm"]
@@ -585,8 +607,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     gemm_ms, gemm_flops = kern["gemm"]
     amax_ms, amax_bytes = kern["amax"]
     cast_ms, cast_bytes = kern["cast"]
-    w13 = wl.WORKLOADS["llama3_8b_ffn_w13"]
-    w1_fwd_flops = 2 * w13.M * w13.N * w13.K
+    rw = wl.WORKLOADS[next(l.workload for l in spec.linears if l.name == roof_name)]
+    w1_fwd_flops = 2 * rw.M * rw.N * rw.K
 
     peaks, peak_src = load_peaks()
     fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
@@ -627,8 +649,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                             "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
         "roofline": {"bound": "tensor", "achieved": w1_fwd_tflops, "peak": fp8_peak_sustained,
                      "unit": "TFLOP/s", "frac": w1_fwd_tflops / fp8_peak_sustained,
-                     "traffic": gemm_traffic(),
-                     "kernel": "fp8_gemm_tn_kernel, w1 forward launch (Y 8192x14336, K 4096): "
+                     "traffic": gemm_traffic() if rw.name == "llama3_8b_ffn_w13" else None,
+                     "kernel": f"fp8_gemm_tn_kernel, {roof_label} launch (Y {rw.M}x{rw.N}, K {rw.K}): "
                                "2*M*N*K flop per launch / mean event-timed launch duration",
                      "peak_source": f"{peak_src} sustained bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)",
                      "launches_timed": w1_fwd_n},

@@ -65,7 +65,7 @@ constexpr int kBStage = kBN * kBK;    // 16 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * kPairN; // two fp32 accumulators of 256 columns
 constexpr int64_t kL2Resident = 40ll << 20;  // an operand up to this size is kept resident in L2
-constexpr int64_t kL2GroupBytes = 24ll << 20; // otherwise: panels of one raster group
+constexpr int kWaveGroup = 8;                 // otherwise: pair tiles per raster group
 constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 1024 /*barriers*/ + 1024 /*alignment*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
@@ -578,9 +578,11 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     }
 
     // Raster: keep the smaller operand resident in L2 and stream the larger
-    // one once; if neither fits, hold groups of ~kL2GroupBytes of panels of
-    // one operand while the other streams past once per group, choosing the
-    // orientation with the fewest modelled DRAM bytes.
+    // one once.  If neither fits, the ~76 pairs running at once move through
+    // the contraction together, so L2 only has to hold their current slabs:
+    // group kWaveGroup tiles along one axis (a wave covers a compact block of
+    // tiles, each panel read once per group), choosing the orientation with
+    // the fewest modelled DRAM bytes.
     const int64_t bytes_a = P * R, bytes_b = Q * R;
     TileMap tm{(int)tiles_m, (int)tiles_n, 1, 0};
     if (bytes_a <= kL2Resident && bytes_a <= bytes_b) {
@@ -589,9 +591,7 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         tm.group = (int)tiles_n;                      // all of B per row of tiles
         tm.swap = 1;
     } else {
-        const int64_t panel = (int64_t)kPairM * R;   // bytes of one pair-row (or pair-column) panel
-        int64_t g = kL2GroupBytes / panel;
-        if (g < 1) g = 1;
+        const int64_t g = kWaveGroup;
         const int64_t gm = g < tiles_m ? g : tiles_m, gn = g < tiles_n ? g : tiles_n;
         const int64_t traffic_m = bytes_a + bytes_b * ((tiles_m + gm - 1) / gm);   // A panels held
         const int64_t traffic_n = bytes_b + bytes_a * ((tiles_n + gn - 1) / gn);   // B panels held
