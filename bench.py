@@ -390,7 +390,7 @@ class StepGraph:
         return self.t.cuda.Event(enable_timing=True)
 
     def _mark(self, stream, rec, kind, label, work, fn):
-        if rec is None:
+        if rec is None or (kind != "gemm" and getattr(rec, "gemm_only", False)):
             fn()
             return
         e0, e1 = self._ev(), self._ev()
@@ -564,7 +564,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     time.sleep(0.3)
-    events = []
+    class _GemmEvents(list):
+        gemm_only = True          # the timed region brackets only the GEMMs (the roofline's launches)
+
+    events = _GemmEvents()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -576,6 +579,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     clocks = sampler.stop()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     assert fl.fp8lin_device_error() == 0, "a GEMM kernel reported a timed-out wait"
+    # per-kernel breakdown of amax / cast from separate, fully instrumented steps
+    detail = []
+    for _ in range(3):
+        step.run(detail)
+    barrier()
 
     # per-kernel times from the events (each pair brackets one launch on its stream)
     kern = {"gemm": [0.0, 0], "amax": [0.0, 0], "cast": [0.0, 0]}
@@ -584,10 +592,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # the roofline's launch: w1's forward GEMM where the step has one, else the linear's forward
     roof_name = "w1" if "w1" in {l.name for l in spec.linears} else spec.linears[0].name
     roof_label = roof_name + ".fwd"
-    for kind, label, e0, e1, work in events:
-        ms = e0.elapsed_time(e1)
+    for kind, label, e0, e1, work in list(events) + [d for d in detail if d[0] != "gemm"]:
+        ms = e0.elapsed_time(e1) / (3 if kind != "gemm" else 1) * (args.steps if kind != "gemm" else 1)
         kern[kind][0] += ms
-        kern[kind][1] += work
+        kern[kind][1] += work / 3 * args.steps if kind != "gemm" else work
         if kind == "gemm":
             pl = per_layer.setdefault(label.split(".")[0], [0.0, 0])
             pl[0] += ms
@@ -617,6 +625,26 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     value = world * spec_flops(spec) / (ms_per_step * 1e-3) / 1e12
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     w1_fwd_tflops = w1_fwd_flops / (w1_fwd_ms / w1_fwd_n * 1e-3) / 1e12
+
+    graph = None
+    if args.graph:
+        # the same step captured once in a CUDA graph and replayed: no host
+        # launch cost per kernel (what launch-bound small shapes need)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            step.run()
+        for _ in range(args.warmup):
+            cg.replay()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            cg.replay()
+        g1.record(stream)
+        barrier()
+        g_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, dist, dev)
+        graph = {"ms_per_step": g_ms, "value": world * spec_flops(spec) / (g_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                 "note": "same step replayed from a captured CUDA graph"}
 
     e2e = None
     if args.e2e_steps > 0:
@@ -656,7 +684,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                      "launches_timed": w1_fwd_n},
         "kernels": {
             "gemm": {"ms_per_step": gemm_ms / args.steps, "tflops": gemm_tflops},
-            "amax": {"ms_per_step": amax_ms / args.steps, "note": "event time per launch, may overlap GEMMs",
+            "amax": {"ms_per_step": amax_ms / args.steps,
+                     "note": "amax and cast times from 3 extra fully instrumented steps; may overlap GEMMs",
                      "gbs": amax_bytes / (amax_ms * 1e-3) / 1e9 if amax_ms else None},
             "cast_transpose": {"ms_per_step": cast_ms / args.steps,
                                "gbs": cast_bytes / (cast_ms * 1e-3) / 1e9 if cast_ms else None},
@@ -666,6 +695,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "schedule": step.describe(),
         "main_stream_idle_before_gemm_ms": {k: round(v, 4) for k, v in gaps.items()},
         "clocks": clocks,
+        "graph": graph,
         "e2e": e2e,
         "gpu_launches": step.kernels_per_step * args.steps,
         "cpu_baseline": cpu,
@@ -755,6 +785,7 @@ def main():
     ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise"], default="dynamic",
                     help="scaling recipe (the headline metric is dynamic per-tensor)")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
+    ap.add_argument("--graph", action="store_true", help="also time the step replayed from a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
