@@ -317,6 +317,7 @@ def plan(spec: Spec, overlap: bool = True):
             first_use.setdefault(k, i)
     main_casts = {i: [] for i in range(len(spec.gemms))}
     side_casts = {i: [] for i in range(len(spec.gemms))}
+    beside = {i: [] for i in range(len(spec.gemms))}
     for key in cast_inputs(spec):
         a = spec.avail[key]
         release = 0 if a is None else idx[a] + 1
@@ -327,9 +328,14 @@ def plan(spec: Spec, overlap: bool = True):
             main_casts[n].append(key)
         else:
             side_casts[release].append(key)
+    if overlap:
+        # several casts gating the same GEMM with nothing to hide under: the
+        # first stays on the main stream, the others run beside it
+        for i in main_casts:
+            main_casts[i], beside[i] = main_casts[i][:1], main_casts[i][1:]
     for i in side_casts:
         side_casts[i].sort(key=lambda k: first_use[k])
-    return main_casts, side_casts, first_use
+    return main_casts, side_casts, first_use, beside
 
 
 class StepGraph:
@@ -372,7 +378,7 @@ class StepGraph:
         self.kernels_per_step = per_cast * len(self.t8) + len(spec.gemms)
 
     def _plan(self):
-        self.main_casts, self.side_casts, self.needed_by = plan(self.spec, self.overlap)
+        self.main_casts, self.side_casts, self.needed_by, self.beside = plan(self.spec, self.overlap)
 
     def describe(self):
         how = f"{self.scaling} per-tensor scaling" if self.scaling != "rowwise" else "row-wise (per-block) scaling"
@@ -434,6 +440,15 @@ class StepGraph:
         m, s = self.main, self.side
         ready = {}
         for i, (name, which) in enumerate(self.spec.gemms):
+            if self.beside[i]:
+                marker = self.t.cuda.Event()
+                marker.record(m)                      # the casts gating GEMM i start together
+                s.wait_event(marker)
+                for key in self.beside[i]:
+                    self._cast(rec, key, s)
+                    e = self.t.cuda.Event()
+                    e.record(s)
+                    ready[key] = e
             for key in self.main_casts[i]:
                 self._cast(rec, key, m)
             if self.side_casts[i]:

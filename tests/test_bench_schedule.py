@@ -5,12 +5,16 @@ import bench
 
 
 def _check(spec, overlap):
-    main, side, needed = bench.plan(spec, overlap)
+    main, side, needed, beside = bench.plan(spec, overlap)
     idx = {g: i for i, g in enumerate(spec.gemms)}
     placed = {}
     for i, keys in main.items():
         for k in keys:
             placed[k] = ("main", i)
+    for i, keys in beside.items():
+        for k in keys:
+            assert needed[k] == i and k not in placed
+            placed[k] = ("beside", i)
     for i, keys in side.items():
         for k in keys:
             placed[k] = ("side", i)
@@ -27,7 +31,7 @@ def _check(spec, overlap):
 def test_ffn_schedule():
     spec = bench.SPECS["ffn8b"]
     main, side = _check(spec, True)
-    assert main[0] == ["xf", "w:w1"] and main[2] == ["h"]
+    assert main[0] == ["xf"] and main[2] == ["h"]
     assert side[0] == ["w:w3", "w:w2"] and side[2] == ["dy:w2"] and side[4] == ["dy:w1", "dy:w3"]
     assert bench.spec_flops(spec) == 3 * 6 * 8192 * 4096 * 14336
 
@@ -35,7 +39,7 @@ def test_ffn_schedule():
 def test_block_schedule():
     spec = bench.SPECS["block8b"]
     main, side = _check(spec, True)
-    assert main[0] == ["xa", "w:qkv"] and "xo" in main[1] and "xf" in main[2]
+    assert main[0] == ["xa"] and "xo" in main[1] and "xf" in main[2]
     assert "dy:o" in side[spec.gemms.index(("w3", "wgrad"))]
     assert "dy:qkv" in side[spec.gemms.index(("o", "wgrad"))]
     assert len(spec.gemms) == 15 and len(bench.cast_inputs(spec)) == 14
