@@ -153,12 +153,13 @@ def host_inputs(spec: Spec, rank: int):
 # ------------------------------------------------------------------ peaks
 
 GEMM_SRC = os.path.join(ROOT, "float8_linear_layers_gb300", "csrc", "gemm.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fp8_gemm_tn_kernel__w1_fwd_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fp8_gemm_tn_kernel__ffn8b_step_traffic.json")
 
 
-def gemm_traffic():
-    """DRAM bytes per w1-forward GEMM launch from the committed ncu capture,
-    or None when the GEMM source changed since the counters were taken."""
+def gemm_traffic(workload: str):
+    """Mean DRAM bytes per GEMM launch of one step of `workload`, from the
+    committed ncu capture; None when the GEMM source changed since the
+    counters were taken or no capture covers this workload."""
     import hashlib
     try:
         with open(TRAFFIC_FILE) as f:
@@ -167,9 +168,9 @@ def gemm_traffic():
             sha = hashlib.sha256(f.read()).hexdigest()
     except (OSError, ValueError):
         return None
-    if t.get("gemm_cu_sha256") != sha:
+    if t.get("gemm_cu_sha256") != sha or t.get("workload") != workload:
         return None
-    return int(t["dram_bytes_read"]) + int(t["dram_bytes_write"])
+    return int(t["mean_dram_bytes_per_launch"])
 
 
 def load_peaks():
@@ -690,13 +691,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "pct_of_fp8_peak": 100.0 * value / world / fp8_peak_sustained,
         "fp8_peak_tflops": {"sustained": fp8_peak_sustained, "burst": fp8_peak_burst,
                             "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
-        "roofline": {"bound": "tensor", "achieved": w1_fwd_tflops, "peak": fp8_peak_sustained,
-                     "unit": "TFLOP/s", "frac": w1_fwd_tflops / fp8_peak_sustained,
-                     "traffic": gemm_traffic() if rw.name == "llama3_8b_ffn_w13" else None,
-                     "kernel": f"fp8_gemm_tn_kernel, {roof_label} launch (Y {rw.M}x{rw.N}, K {rw.K}): "
-                               "2*M*N*K flop per launch / mean event-timed launch duration",
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sustained,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
+                     "traffic": gemm_traffic(args.workload),
+                     "kernel": "fp8_gemm_tn_kernel, every launch of the timed region: mean 2*M*N*K flop per "
+                               "launch / mean event-timed launch duration (launches run beside the side-stream "
+                               "casts); traffic = mean DRAM bytes per GEMM launch of one step (ncu)",
                      "peak_source": f"{peak_src} sustained bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)",
-                     "launches_timed": w1_fwd_n},
+                     "launches_timed": len(gemm_evs),
+                     f"{roof_label}_tflops": w1_fwd_tflops},
         "kernels": {
             "gemm": {"ms_per_step": gemm_ms / args.steps, "tflops": gemm_tflops},
             "amax": {"ms_per_step": amax_ms / args.steps,
