@@ -108,9 +108,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase of parity `parity` to complete, for at most `limit` ns.
 // Gives up early once another role has raised the abort flag.  On running
-// out, records the timeout and raises the flag.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned long long limit) {
+// out, records the timeout and raises the flag.  The loop lives out of line;
+// callers inline only the first try (mbar_wait below).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            unsigned long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
@@ -122,6 +123,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned long long limit) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, limit);
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
@@ -345,33 +351,60 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader CTA)
+        // Slabs are consumed two at a time: one pair of barrier waits, then
+        // eight MMAs.  The tensor pipe keeps only a short queue of issued
+        // MMAs, and the waits, fence and commits between groups must fit in
+        // the time the queued ones take; four MMAs per wait leave the pipe
+        // idle for part of every slab, eight do not.
         if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            // descriptors of slab 0; slab s starts s * 16 KB later (start-address field counts 16-byte units)
+            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
             for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kPairN);
                 bool ok = true;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+                for (int kb = 0; kb < num_kb; kb += 2) {
+                    const bool two = kb + 1 < num_kb;
+                    const bool wrap = stage + 1 == kStages;
+                    const int stage2 = wrap ? 0 : stage + 1;
+                    const uint32_t phase2 = wrap ? phase ^ 1u : phase;
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
+                        (two && !mbar_wait(smem_u32(&full[stage2]), phase2, abort_flag, kWaitLimitNs))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = sw128_kmajor_desc(smem_u32(sA + stage * kAStage));
-                    const uint64_t b_desc = sw128_kmajor_desc(smem_u32(sB + stage * kBStage));
+                    {
+                        const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kAStage >> 4));
+                        const uint64_t b_desc = b_desc0 + (uint64_t)(stage * (kBStage >> 4));
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // advance the start address by k * 32 bytes inside the swizzle row
-                        const uint64_t off = (uint64_t)((k * kUmmaK) >> 4);
-                        umma_f8f6f4_pair(d_tmem, a_desc + off, b_desc + off, idesc, (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            // advance the start address by k * 32 bytes inside the swizzle row
+                            const uint64_t off = (uint64_t)((k * kUmmaK) >> 4);
+                            umma_f8f6f4_pair(d_tmem, a_desc + off, b_desc + off, idesc, (kb | k) != 0 ? 1u : 0u);
+                        }
+                        umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
                     }
-                    umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
-                    if (++stage == kStages) {
-                        stage = 0;
+                    if (two) {
+                        const uint64_t a_desc = a_desc0 + (uint64_t)(stage2 * (kAStage >> 4));
+                        const uint64_t b_desc = b_desc0 + (uint64_t)(stage2 * (kBStage >> 4));
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            const uint64_t off = (uint64_t)((k * kUmmaK) >> 4);
+                            umma_f8f6f4_pair(d_tmem, a_desc + off, b_desc + off, idesc, 1u);
+                        }
+                        umma_commit_multicast(smem_u32(&empty[stage2]), 0x3);
+                    }
+                    const int adv = two ? 2 : 1;
+                    stage += adv;
+                    if (stage >= kStages) {
+                        stage -= kStages;
                         phase ^= 1u;
                     }
                 }
