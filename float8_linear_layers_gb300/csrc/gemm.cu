@@ -26,9 +26,11 @@
 //               issues the MMAs (four per 128-byte slab) and multicasts each
 //               tcgen05.commit to both CTAs' empty / accumulator barriers;
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, scale,
-//               round to bf16, 16-byte stores; each warp then arrives on the
-//               leader's accumulator-empty barrier, so the epilogue of tile i
-//               overlaps the main loop of tile i + 1.
+//               round to bf16, stage the 32 x 64-byte block in shared memory
+//               (64-byte swizzle) and TMA-store it; each warp arrives on
+//               the leader's accumulator-empty barrier once the last columns
+//               are in registers, so the epilogue of tile i overlaps the
+//               main loop of tile i + 1.
 // Halving the B bytes per CTA (32 KB per slab instead of 48 KB for a
 // 128 x 256 single-CTA tile) cuts the L2 -> SM traffic per flop by a third
 // and leaves room for six stages.  Pair tiles are visited in groups of
@@ -66,11 +68,19 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * kPairN; // two fp32 accumulators of 256 columns
 constexpr int64_t kL2Resident = 40ll << 20;  // an operand up to this size is kept resident in L2
 constexpr int kWaveGroup = 8;                 // otherwise: pair tiles per raster group
-constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 1024 /*barriers*/ + 1024 /*alignment*/;
+constexpr int kEpiCols = 32;                 // output columns per staged store: 64 bytes of bf16
+constexpr int kEpiBuf = 32 * kEpiCols * 2;   // one epilogue warp's 32 rows x 64 bytes (2 KB)
+constexpr int kEpiBytes = 4 * kEpiBuf;       // four epilogue warps, one buffer each
+// The ring plus staging stays small enough that one cast / amax CTA (about
+// 18 KB of shared memory) still fits beside a GEMM CTA on the same SM.
+constexpr int kSmemBytes = kStages * (kAStage + kBStage) + kEpiBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
 
 static_assert(kBK == 128, "one stage is one 128-byte swizzle row of contraction");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
+static_assert(kPairN % kEpiCols == 0, "the epilogue stores whole 32-column blocks");
+static_assert(kSmemBytes + 1024 + 18 * 1024 + 1024 <= 233472, "a cast CTA must fit beside a GEMM CTA");
 
 __device__ unsigned int g_device_error = 0;
 
@@ -190,6 +200,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// TMA store of one box from this CTA's shared memory, tracked in the
+// issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until none of this thread's committed bulk stores still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until all of this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void umma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -260,14 +284,15 @@ struct TileMap {
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads, 1)
 fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   __nv_bfloat16 *__restrict__ C, int P, int Q, int R, const float *__restrict__ inv_a,
+                   const __grid_constant__ CUtensorMap map_c, int P, int Q, int R, const float *__restrict__ inv_a,
                    const float *__restrict__ inv_b, uint32_t idesc, TileMap tiles) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kAStage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + kStages * kBStage);
+    uint8_t *sC = sB + kStages * kBStage;     // epilogue staging: [4 warps][32 rows x 64 B], 64-byte swizzle
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kEpiBytes);
     uint64_t *full = bars;                    // [kStages] both CTAs' slabs landed (leader's copy used)
     uint64_t *empty = bars + kStages;         // [kStages] the pair's MMAs are done with the slab
     uint64_t *acc_full = bars + 2 * kStages;  // [2] accumulator finished (arrived in both CTAs)
@@ -422,7 +447,15 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
+        // Per 32-column block: tcgen05.ld, scale, round to bf16, write the
+        // warp's 32 x 64-byte block into shared memory in the TMA 64-byte
+        // swizzle (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3):
+        // conflict-free), and one lane issues a TMA store of the block.  The
+        // accumulator is handed back as soon as its last columns are in
+        // registers; the stores drain behind the next tile.
         const int sub = warp % 4;  // TMEM sub-partition this warp may read: lanes 32 sub .. 32 sub + 31
+        uint8_t *stage_c = sC + (warp - 2) * kEpiBuf;
+        uint8_t *dst = stage_c + lane * (kEpiCols * 2);
         const float sc = VEC ? 0.0f : __fmul_rn(__ldg(inv_a), __ldg(inv_b));
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -433,15 +466,15 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             tc_fence_after();
             int tm, tn;
             tiles.coords(t, tm, tn);
-            const int row = tm * kPairM + (int)rank * kBM + sub * 32 + lane;
-            __nv_bfloat16 *crow = C + (int64_t)row * Q;
+            const int row0 = tm * kPairM + (int)rank * kBM + sub * 32;  // first of this warp's rows
+            const int row = row0 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kPairN);
             const float sa = (VEC && row < P) ? __ldg(inv_a + row) : 0.0f;
 #pragma unroll 1
-            for (int c = 0; c < kPairN / 32; ++c) {
+            for (int blk = 0; blk < kPairN / kEpiCols; ++blk) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
-                const int col0 = tn * kPairN + c * 32;
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(blk * kEpiCols), r);
+                const int col0 = tn * kPairN + blk * kEpiCols;
                 float f[32];
                 if (VEC) {
                     // one inverse scale per output column: the same 32 floats for every lane
@@ -459,32 +492,43 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     for (int j = 0; j < 32; ++j) f[j] = sc;
                 }
                 tmem_ld_wait();
-                if (row < P) {
+                if (blk == kPairN / kEpiCols - 1) {
+                    // every column of the accumulator is in registers: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+                }
+                // the previous block's store must have read the staging buffer
+                if (lane == 0) bulk_wait_read_0();
+                __syncwarp();
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (col0 + 8 * g < Q) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 0]), f[8 * g + 0]),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 1]), f[8 * g + 1]));
-                            o.y = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 2]), f[8 * g + 2]),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 3]), f[8 * g + 3]));
-                            o.z = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 4]), f[8 * g + 4]),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 5]), f[8 * g + 5]));
-                            o.w = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * g + 6]), f[8 * g + 6]),
-                                              __fmul_rn(__uint_as_float(r[8 * g + 7]), f[8 * g + 7]));
-                            *reinterpret_cast<uint4 *>(crow + col0 + 8 * g) = o;
-                        }
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    uint4 o;
+                    o.x = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * c + 0]), f[8 * c + 0]),
+                                      __fmul_rn(__uint_as_float(r[8 * c + 1]), f[8 * c + 1]));
+                    o.y = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * c + 2]), f[8 * c + 2]),
+                                      __fmul_rn(__uint_as_float(r[8 * c + 3]), f[8 * c + 3]));
+                    o.z = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * c + 4]), f[8 * c + 4]),
+                                      __fmul_rn(__uint_as_float(r[8 * c + 5]), f[8 * c + 5]));
+                    o.w = pack_bf16x2(__fmul_rn(__uint_as_float(r[8 * c + 6]), f[8 * c + 6]),
+                                      __fmul_rn(__uint_as_float(r[8 * c + 7]), f[8 * c + 7]));
+                    *reinterpret_cast<uint4 *>(dst + ((c ^ ((lane >> 1) & 3)) << 4)) = o;
+                }
+                // make the generic-proxy writes visible to the TMA engine, then store
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0 && row0 < P && col0 < Q) {
+                    tma_store_2d(&map_c, smem_u32(stage_c), col0, row0);
+                    bulk_commit_group();
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -517,6 +561,20 @@ EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
+}
+
+// 2-D map over the row-major bf16 output [rows x cols]; box = 32 rows x 32
+// columns (64 bytes), 64-byte swizzle, as the epilogue stages it.
+bool make_output_map(CUtensorMap *map, void *base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kEpiCols, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D map over a row-major [rows x inner] byte matrix, box = box_rows x 128 bytes.
@@ -589,8 +647,9 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     const int64_t tiles_m = (P + kPairM - 1) / kPairM, tiles_n = (Q + kPairN - 1) / kPairN;
     if (tiles_m * tiles_n > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
 
-    CUtensorMap map_a, map_b;
-    if (!make_operand_map(&map_a, A, P, R, kBM) || !make_operand_map(&map_b, B, Q, R, kBN))
+    CUtensorMap map_a, map_b, map_c;
+    if (!make_operand_map(&map_a, A, P, R, kBM) || !make_operand_map(&map_b, B, Q, R, kBN) ||
+        !make_output_map(&map_c, C, P, Q))
         return FP8LIN_ERR_CUDA;
 
     if (dev.device >= 64) return FP8LIN_ERR_CUDA;
@@ -640,10 +699,9 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(2 * pairs, stream, &attr);
-    __nv_bfloat16 *c = static_cast<__nv_bfloat16 *>(C);
     const int p = (int)P, q = (int)Q, r = (int)R;
     const uint32_t idesc = make_idesc(fa, fb);
-    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel<VEC>, map_a, map_b, c, p, q, r, inv_a, inv_b, idesc, tm) !=
+    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel<VEC>, map_a, map_b, map_c, p, q, r, inv_a, inv_b, idesc, tm) !=
         cudaSuccess)
         return FP8LIN_ERR_CUDA;
     return check_launch();
