@@ -156,10 +156,11 @@ GEMM_SRC = os.path.join(ROOT, "float8_linear_layers_gb300", "csrc", "gemm.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fp8_gemm_tn_kernel__ffn8b_step_traffic.json")
 
 
-def gemm_traffic(workload: str):
+def gemm_traffic(workload: str, scaling: str):
     """Mean DRAM bytes per GEMM launch of one step of `workload`, from the
-    committed ncu capture; None when the GEMM source changed since the
-    counters were taken or no capture covers this workload."""
+    committed ncu capture of the per-tensor-scale GEMM; None when the GEMM
+    source changed since the counters were taken, no capture covers this
+    workload, or the step runs the row-wise-scale GEMM instead."""
     import hashlib
     try:
         with open(TRAFFIC_FILE) as f:
@@ -168,7 +169,7 @@ def gemm_traffic(workload: str):
             sha = hashlib.sha256(f.read()).hexdigest()
     except (OSError, ValueError):
         return None
-    if t.get("gemm_cu_sha256") != sha or t.get("workload") != workload:
+    if t.get("gemm_cu_sha256") != sha or t.get("workload") != workload or scaling == "rowwise":
         return None
     return int(t["mean_dram_bytes_per_launch"])
 
@@ -693,7 +694,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                             "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sustained,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
-                     "traffic": gemm_traffic(args.workload),
+                     "traffic": gemm_traffic(args.workload, args.scaling),
                      "kernel": "fp8_gemm_tn_kernel, every launch of the timed region: mean 2*M*N*K flop per "
                                "launch / mean event-timed launch duration (launches run beside the side-stream "
                                "casts); traffic = mean DRAM bytes per GEMM launch of one step (ncu)",
