@@ -129,21 +129,24 @@ def spec_flops(spec: Spec) -> int:
     return sum(wl.WORKLOADS[l.workload].flops for l in spec.linears)
 
 
-# HBM bytes per cast element for one step: dynamic and row-wise read x twice
-# (amax pass, cast pass) and write two FP8 copies; delayed and static skip the
-# separate amax pass.
-CAST_BYTES_PER_ELEM = {"dynamic": 6, "rowwise": 6, "delayed": 4, "static": 4}
+def cast_elem_bytes(scaling: str, transpose: bool) -> int:
+    """HBM bytes per cast element in one step: the cast reads x (2 B) and
+    writes one FP8 copy, or two with the transposed copy (always for
+    row-wise scaling); dynamic and row-wise scaling read x once more for the
+    amax pass, delayed and static do not."""
+    two_copies = transpose or scaling == "rowwise"
+    return 2 + 1 + (1 if two_copies else 0) + (2 if scaling in ("dynamic", "rowwise") else 0)
 
 
-def cast_bytes(spec: Spec, scaling: str) -> int:
-    return sum(r * c for (r, c, *_) in cast_inputs(spec).values()) * CAST_BYTES_PER_ELEM[scaling]
+def cast_bytes(spec: Spec, scaling: str, transpose: bool = False) -> int:
+    return sum(r * c for (r, c, *_) in cast_inputs(spec).values()) * cast_elem_bytes(scaling, transpose)
 
 
-def attainable(spec: Spec, scaling: str, peak_tflops: float, hbm_gbs: float) -> dict:
+def attainable(spec: Spec, scaling: str, peak_tflops: float, hbm_gbs: float, transpose: bool = False) -> dict:
     """Bound if every GEMM ran at the tensor peak and every amax / cast alone
     at the copy bandwidth, one after another: flop / (flop / P + cast bytes / BW).
     Running the casts beside the GEMMs can beat it."""
-    flop, b = spec_flops(spec), cast_bytes(spec, scaling)
+    flop, b = spec_flops(spec), cast_bytes(spec, scaling, transpose)
     t = flop / (peak_tflops * 1e12) + b / (hbm_gbs * 1e9)
     return {"serial_bound_tflops": flop / t / 1e12, "frac_of_peak": flop / t / 1e12 / peak_tflops,
             "cast_bytes_per_step": b,
@@ -374,15 +377,19 @@ class StepGraph:
     pages describe for FP8 scaling work.  Each step starts after the previous
     one has finished (FP8 buffers and outputs are reused)."""
 
-    def __init__(self, fl, spec: Spec, dev, dev_in, overlap=True, scaling="dynamic", streams=None):
+    def __init__(self, fl, spec: Spec, dev, dev_in, overlap=True, scaling="dynamic", streams=None,
+                 transpose=False):
         import torch
         self.fl, self.t, self.spec = fl, torch, spec
         self.overlap, self.scaling = overlap, scaling
+        # one FP8 copy per tensor (backward GEMMs read it MN-major) unless the
+        # transposed copies are asked for; row-wise scaling always needs them
+        self.transpose = transpose or scaling == "rowwise"
         self.inp = dev_in
         self.lin = {l.name: l for l in spec.linears}
         self.t8 = {}
         for key, (rows, cols, fmt, *_) in cast_inputs(spec).items():
-            self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling)
+            self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=self.transpose)
         bf = torch.bfloat16
         self.out = {}
         for l in spec.linears:
@@ -432,17 +439,18 @@ class StepGraph:
     def _cast(self, rec, key, stream):
         fl, x, t8 = self.fl, self.inp[key], self.t8[key]
         n = x.numel()
+        cast_bytes = (4 if t8.qT is not None else 3) * n   # read bf16, write one or two FP8 copies
         if t8.scaling == "rowwise":
             self._mark(stream, rec, "amax", key, 2 * n,
                        lambda: fl.fp8lin_amax_rowcol(x, t8.row_amax, t8.col_amax, stream))
-            self._mark(stream, rec, "cast", key, 4 * n, lambda: fl.fp8lin_cast_transpose_rowwise(
+            self._mark(stream, rec, "cast", key, cast_bytes, lambda: fl.fp8lin_cast_transpose_rowwise(
                 x, t8.fmt, t8.row_amax, t8.col_amax, t8.row_inv, t8.col_inv, t8.q, t8.qT, t8.fmt_max, stream))
         elif t8.scaling == "dynamic":
             self._mark(stream, rec, "amax", key, 2 * n, lambda: fl.fp8lin_amax(x, t8.amax, stream))
-            self._mark(stream, rec, "cast", key, 4 * n, lambda: fl.fp8lin_cast_transpose(
+            self._mark(stream, rec, "cast", key, cast_bytes, lambda: fl.fp8lin_cast_transpose(
                 x, t8.fmt, t8.amax, t8.scale, t8.inv_scale, t8.q, t8.qT, t8.fmt_max, stream))
         else:
-            self._mark(stream, rec, "cast", key, 4 * n, lambda: t8.quantize(x, stream))
+            self._mark(stream, rec, "cast", key, cast_bytes, lambda: t8.quantize(x, stream))
 
     def _gemm(self, rec, name, which):
         fl, m = self.fl, self.main
@@ -454,10 +462,14 @@ class StepGraph:
             fn = {"fwd": lambda: fl.fp8lin_fwd_rowwise(x8.q, x8.row_inv, w8.q, w8.row_inv, out, m),
                   "dgrad": lambda: fl.fp8lin_dgrad_rowwise(d8.q, d8.row_inv, w8.qT, w8.col_inv, out, m),
                   "wgrad": lambda: fl.fp8lin_wgrad_rowwise(d8.qT, d8.col_inv, x8.qT, x8.col_inv, out, m)}[which]
-        else:
+        elif self.transpose:
             fn = {"fwd": lambda: fl.fp8lin_fwd(x8.q, x8.inv_scale, w8.q, w8.inv_scale, out, m),
                   "dgrad": lambda: fl.fp8lin_dgrad(d8.q, d8.inv_scale, w8.qT, w8.inv_scale, out, m),
                   "wgrad": lambda: fl.fp8lin_wgrad(d8.qT, d8.inv_scale, x8.qT, x8.inv_scale, out, m)}[which]
+        else:
+            fn = {"fwd": lambda: fl.fp8lin_fwd(x8.q, x8.inv_scale, w8.q, w8.inv_scale, out, m),
+                  "dgrad": lambda: fl.fp8lin_dgrad_mn(d8.q, d8.inv_scale, w8.q, w8.inv_scale, out, m),
+                  "wgrad": lambda: fl.fp8lin_wgrad_mn(d8.q, d8.inv_scale, x8.q, x8.inv_scale, out, m)}[which]
         self._mark(m, rec, "gemm", f"{name}.{which}", 2 * w.M * w.N * w.K, fn)
 
     def run(self, rec=None):
@@ -504,7 +516,7 @@ def run_e2e(args, fl, spec, dev, host, step, world, dist, barrier):
     for k in range(2):
         din = {key: torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for key, t in pinned.items()}
         g = step if k == 0 else StepGraph(fl, spec, dev, din, overlap=step.overlap, scaling=step.scaling,
-                                          streams=(step.main, step.side))
+                                          streams=(step.main, step.side), transpose=step.transpose)
         g.inp = din
         outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in g.outputs()]
         sets.append((g, din, outs))
@@ -588,7 +600,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     host = host_inputs(spec, rank)
     dev_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in host.items()}
-    step = StepGraph(fl, spec, dev, dev_in, overlap=not args.serial, scaling=args.scaling)
+    step = StepGraph(fl, spec, dev, dev_in, overlap=not args.serial, scaling=args.scaling,
+                     transpose=args.transpose)
     stream = step.main
     torch.cuda.set_stream(stream)
 
@@ -711,10 +724,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
         "data": "synthetic",
         "config": {"workload": spec.name, "scaling": args.scaling, "linears": spec.description,
+                   "fp8_copies": ("row-major and transposed; backward GEMMs read the transposed copies"
+                                  if step.transpose else
+                                  "one row-major copy per tensor; backward GEMMs read it MN-major"),
                    "l2": "inputs larger than L2: one step streams several GB of distinct operands through a 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": 100.0 * value / world / fp8_peak_sustained,
-        "attainable": attainable(spec, args.scaling, fp8_peak_sustained, peaks["hbm_gbs"]),
+        "attainable": attainable(spec, args.scaling, fp8_peak_sustained, peaks["hbm_gbs"], step.transpose),
         "fp8_peak_tflops": {"sustained": fp8_peak_sustained, "burst": fp8_peak_burst,
                             "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sustained,
@@ -761,9 +777,10 @@ def run_profile_case(args) -> None:
     dev = torch.device("cuda", 0)
     up = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
     case = args.profile_case
-    need_x = case in ("gemm_fwd", "gemm_wgrad")
-    need_w = case in ("gemm_fwd", "gemm_dgrad")
-    need_dy = case in ("gemm_dgrad", "gemm_wgrad", "amax", "cast", "amax_rowcol", "cast_rowwise")  # dY: 235 MB > L2
+    need_x = case in ("gemm_fwd", "gemm_wgrad", "gemm_wgrad_mn")
+    need_w = case in ("gemm_fwd", "gemm_dgrad", "gemm_dgrad_mn")
+    need_dy = case in ("gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn", "gemm_wgrad_mn", "amax", "cast", "cast_q",
+                       "amax_rowcol", "cast_rowwise")  # dY: 235 MB > L2
     x8 = w8 = d8 = None
     if need_x:
         x = up(w.make_x())
@@ -787,6 +804,17 @@ def run_profile_case(args) -> None:
         out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
         launch = lambda: fl.fp8lin_wgrad(d8.qT, d8.inv_scale, x8.qT, x8.inv_scale, out)
         work, unit = 2 * w.M * w.N * w.K, "flop"
+    elif case == "gemm_dgrad_mn":
+        out = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
+        launch = lambda: fl.fp8lin_dgrad_mn(d8.q, d8.inv_scale, w8.q, w8.inv_scale, out)
+        work, unit = 2 * w.M * w.N * w.K, "flop"
+    elif case == "gemm_wgrad_mn":
+        out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+        launch = lambda: fl.fp8lin_wgrad_mn(d8.q, d8.inv_scale, x8.q, x8.inv_scale, out)
+        work, unit = 2 * w.M * w.N * w.K, "flop"
+    elif case == "cast_q":
+        launch = lambda: fl.fp8lin_cast_transpose(dy, fl.E5M2, d8.amax, d8.scale, d8.inv_scale, d8.q, None)
+        work, unit = 3 * w.M * w.N, "byte"
     elif case == "amax":
         launch = lambda: fl.fp8lin_amax(dy, d8.amax)
         work, unit = 2 * w.M * w.N, "byte"
@@ -829,14 +857,18 @@ def main():
     ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise"], default="dynamic",
                     help="scaling recipe (the headline metric is dynamic per-tensor)")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
+    ap.add_argument("--transpose", action="store_true",
+                    help="casts also write the transposed FP8 copies and the backward GEMMs read those "
+                         "(default: one copy per tensor, read MN-major by the backward GEMMs)")
     ap.add_argument("--graph", action="store_true", help="also time the step replayed from a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=32,
                     help="steps of the end-to-end run; the average includes one pipeline fill and drain")
     ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "amax", "cast",
-                                               "amax_rowcol", "cast_rowwise"],
+    ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn",
+                                               "gemm_wgrad_mn", "amax", "cast", "cast_q", "amax_rowcol",
+                                               "cast_rowwise"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least three warm-up steps

@@ -43,7 +43,7 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
 # Every entry point declared in include/fp8lin.h.
 ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_static",
                 "fp8lin_cast_transpose_delayed", "fp8lin_amax_rowcol", "fp8lin_cast_transpose_rowwise",
-                "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad",
+                "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
                 "fp8lin_fwd_rowwise", "fp8lin_dgrad_rowwise", "fp8lin_wgrad_rowwise",
                 "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
@@ -60,30 +60,40 @@ def _load_library() -> ctypes.CDLL:
         raise ImportError(f"libfp8lin is not built ({path} missing): run "
                           "`python -c 'import __graft_entry__ as g; g.build()'` first")
     lib = ctypes.CDLL(path)
-    vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
-    sigs = {
-        "fp8lin_amax": [vp, i64, vp, vp],
-        "fp8lin_cast_transpose": [vp, i64, i64, ci, f32, vp, vp, vp, vp, vp, vp],
-        "fp8lin_cast_transpose_static": [vp, i64, i64, ci, vp, vp, vp, vp, vp, vp],
-        "fp8lin_cast_transpose_delayed": [vp, i64, i64, ci, f32, vp, i64, i64, vp, vp, vp, vp, vp],
-        "fp8lin_amax_rowcol": [vp, i64, i64, vp, vp, vp],
-        "fp8lin_cast_transpose_rowwise": [vp, i64, i64, ci, f32, vp, vp, vp, vp, vp, vp, vp],
-        "fp8lin_fwd_rowwise": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
-        "fp8lin_dgrad_rowwise": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
-        "fp8lin_wgrad_rowwise": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
-        "fp8lin_fwd": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
-        "fp8lin_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
-        "fp8lin_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
-        "fp8lin_device_error": [vp, vp],
-        "fp8lin_selftest_bounded_wait": [ctypes.c_uint64, vp],
-    }
-    for name, args in sigs.items():
+    missing = set(ENTRY_POINTS) - set(SIGNATURES) - {"fp8lin_status_str"}
+    if missing:
+        # ctypes would pass undeclared 64-bit pointers as 32-bit ints
+        raise ImportError(f"no ctypes signature for {sorted(missing)}")
+    for name, args in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
     lib.fp8lin_status_str.argtypes = [ctypes.c_int]
     lib.fp8lin_status_str.restype = ctypes.c_char_p
     return lib
+
+
+# Argument types of every entry point, in the order include/fp8lin.h declares
+# them (pointers and cudaStream_t as c_void_p).
+_vp, _i64, _f32, _ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+SIGNATURES = {
+    "fp8lin_amax": [_vp, _i64, _vp, _vp],
+    "fp8lin_cast_transpose": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_cast_transpose_static": [_vp, _i64, _i64, _ci, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_cast_transpose_delayed": [_vp, _i64, _i64, _ci, _f32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_amax_rowcol": [_vp, _i64, _i64, _vp, _vp, _vp],
+    "fp8lin_cast_transpose_rowwise": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_fwd_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_dgrad_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_wgrad_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_fwd": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_dgrad": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_wgrad": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_dgrad_mn": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_wgrad_mn": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_device_error": [_vp, _vp],
+    "fp8lin_selftest_bounded_wait": [ctypes.c_uint64, _vp],
+}
 
 
 _lib = _load_library()
@@ -262,6 +272,30 @@ def fp8lin_dgrad(dyq, inv_dy, wqT, inv_w, dx, stream=None) -> None:
                                              _ptr(dx), M, N, K, _stream(stream)))
 
 
+def fp8lin_dgrad_mn(dyq, inv_dy, wq, inv_w, dx, stream=None) -> None:
+    """dX [M x K] = bf16((dYq . Wq) * inv_dy * inv_w); dYq [M x N], Wq [N x K] as cast (no transposed copy)."""
+    M, N = dyq.shape
+    K = wq.shape[1]
+    for t, n in ((dyq, "dyq"), (wq, "wq"), (inv_dy, "inv_dy"), (inv_w, "inv_w"), (dx, "dx")):
+        _dev(t, n)
+    if wq.shape[0] != N or tuple(dx.shape) != (M, K) or dx.dtype != torch.bfloat16:
+        raise ValueError("shape/dtype mismatch: dyq [M,N], wq [N,K], dx bf16 [M,K]")
+    _check("fp8lin_dgrad_mn", _lib.fp8lin_dgrad_mn(_ptr(dyq), _ptr(inv_dy), _ptr(wq), _ptr(inv_w),
+                                                   _ptr(dx), M, N, K, _stream(stream)))
+
+
+def fp8lin_wgrad_mn(dyq, inv_dy, xq, inv_x, dw, stream=None) -> None:
+    """dW [N x K] = bf16((dYq^T . Xq) * inv_dy * inv_x); dYq [M x N], Xq [M x K] as cast (no transposed copy)."""
+    M, N = dyq.shape
+    K = xq.shape[1]
+    for t, n in ((dyq, "dyq"), (xq, "xq"), (inv_dy, "inv_dy"), (inv_x, "inv_x"), (dw, "dw")):
+        _dev(t, n)
+    if xq.shape[0] != M or tuple(dw.shape) != (N, K) or dw.dtype != torch.bfloat16:
+        raise ValueError("shape/dtype mismatch: dyq [M,N], xq [M,K], dw bf16 [N,K]")
+    _check("fp8lin_wgrad_mn", _lib.fp8lin_wgrad_mn(_ptr(dyq), _ptr(inv_dy), _ptr(xq), _ptr(inv_x),
+                                                   _ptr(dw), M, N, K, _stream(stream)))
+
+
 def fp8lin_wgrad(dyqT, inv_dy, xqT, inv_x, dw, stream=None) -> None:
     """dW [N x K] = bf16((dYqT . XqT^T) * inv_dy * inv_x); dYqT [N x M], XqT [K x M]."""
     N, M = dyqT.shape
@@ -292,7 +326,8 @@ def fp8lin_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
 
 class Float8Tensor:
     """Per-tensor FP8 state of one bf16 matrix: the scale, its inverse and
-    the FP8 copies in both majornesses (device buffers, caller-visible).
+    the FP8 copies (device buffers, caller-visible): q [rows x cols] and,
+    with ``transpose`` (always for row-wise scaling), qT [cols x rows].
 
     scaling = "dynamic": amax of this tensor, then scale + cast (default);
               "delayed": scale from an amax history ring (``history_len``
@@ -304,15 +339,17 @@ class Float8Tensor:
                          blocks that do not cross the GEMM contraction."""
 
     def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX,
-                 scaling: str = "dynamic", history_len: int = 16):
+                 scaling: str = "dynamic", history_len: int = 16, transpose: bool = True):
         if scaling not in ("dynamic", "delayed", "static", "rowwise"):
             raise ValueError(f"unknown scaling {scaling!r}")
+        if scaling == "rowwise" and not transpose:
+            raise ValueError("row-wise scaling needs the transposed copy (its scales run along columns)")
         self.rows, self.cols, self.fmt, self.fmt_max = rows, cols, fmt, fmt_max
         self.scaling = scaling
         scalars = torch.zeros(3, dtype=torch.float32, device=device)
         self.amax, self.scale, self.inv_scale = scalars[0:1], scalars[1:2], scalars[2:3]
         self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
-        self.qT = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+        self.qT = torch.empty((cols, rows), dtype=torch.uint8, device=device) if transpose else None
         if scaling == "rowwise":
             self.row_amax = torch.zeros(rows, dtype=torch.float32, device=device)
             self.col_amax = torch.zeros(cols, dtype=torch.float32, device=device)
@@ -355,15 +392,23 @@ class Float8Tensor:
 class Float8Linear:
     """The nine calls of one Float8 linear's forward and backward pass, on
     caller-owned bf16 X [M x K], W [N x K], dY [M x N].  Buffers for the FP8
-    copies and the outputs are allocated once and reused every step; the
-    transposed copies of X and W made in forward are what backward reads."""
+    copies and the outputs are allocated once and reused every step; the FP8
+    copies of X and W made in forward are what backward reads.
+
+    transpose = False (default for per-tensor scaling): one FP8 copy per
+    tensor, and the backward GEMMs read Wq, dYq and Xq MN-major
+    (fp8lin_dgrad_mn / fp8lin_wgrad_mn).  transpose = True: the casts also
+    write the transposed copies and the backward GEMMs read those (always so
+    for row-wise scaling)."""
 
     def __init__(self, M: int, K: int, N: int, device="cuda", fmt_max: float = FMT_MAX,
-                 scaling: str = "dynamic", history_len: int = 16):
+                 scaling: str = "dynamic", history_len: int = 16, transpose: bool | None = None):
         self.M, self.K, self.N = M, K, N
-        self.x8 = Float8Tensor(M, K, E4M3, device, fmt_max, scaling, history_len)
-        self.w8 = Float8Tensor(N, K, E4M3, device, fmt_max, scaling, history_len)
-        self.dy8 = Float8Tensor(M, N, E5M2, device, fmt_max, scaling, history_len)
+        self.transpose = (scaling == "rowwise") if transpose is None else bool(transpose)
+        args = (device, fmt_max, scaling, history_len, self.transpose)
+        self.x8 = Float8Tensor(M, K, E4M3, *args)
+        self.w8 = Float8Tensor(N, K, E4M3, *args)
+        self.dy8 = Float8Tensor(M, N, E5M2, *args)
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=device)
@@ -386,9 +431,12 @@ class Float8Linear:
         if self.dy8.scaling == "rowwise":
             fp8lin_dgrad_rowwise(self.dy8.q, self.dy8.row_inv, self.w8.qT, self.w8.col_inv, self.dx, stream)
             fp8lin_wgrad_rowwise(self.dy8.qT, self.dy8.col_inv, self.x8.qT, self.x8.col_inv, self.dw, stream)
-        else:
+        elif self.transpose:
             fp8lin_dgrad(self.dy8.q, self.dy8.inv_scale, self.w8.qT, self.w8.inv_scale, self.dx, stream)
             fp8lin_wgrad(self.dy8.qT, self.dy8.inv_scale, self.x8.qT, self.x8.inv_scale, self.dw, stream)
+        else:
+            fp8lin_dgrad_mn(self.dy8.q, self.dy8.inv_scale, self.w8.q, self.w8.inv_scale, self.dx, stream)
+            fp8lin_wgrad_mn(self.dy8.q, self.dy8.inv_scale, self.x8.q, self.x8.inv_scale, self.dw, stream)
         return self.dx, self.dw
 
     def step(self, x, w, dy, stream=None):

@@ -3,13 +3,19 @@
 // precision and Float8": Float8 applied to linear layers, composable with
 // autograd, so forward, input gradient and weight gradient all run in FP8).
 //
-// Every GEMM is issued as C[P x Q] = A[P x R] . B[Q x R]^T with both operands
-// stored contraction-contiguous ("K-major"); the cast kernel's transposed
-// copies make that true for all three:
-//     fwd   : Y [M x N]  = Xq   [M x K] . Wq  [N x K]^T    e4m3 x e4m3
-//     dgrad : dX [M x K] = dYq  [M x N] . WqT [K x N]^T    e5m2 x e4m3
-//     wgrad : dW [N x K] = dYqT [N x M] . XqT [K x M]^T    e5m2 x e4m3
-// and the epilogue computes C = bf16_RN(acc_fp32 * (inv_a * inv_b)).
+// Every GEMM is issued as C[P x Q] = A[P x R] . B[Q x R]^T.  Each operand is
+// read either K-major (stored [rows x R], contraction contiguous) or MN-major
+// (stored [R x rows], the row index contiguous): tcgen05 takes 8-bit operands
+// in both majornesses, so the row-major FP8 copies the cast writes serve all
+// three GEMMs and the transposed copies are optional:
+//     fwd      : Y [M x N]  = Xq   [M x K] . Wq  [N x K]^T   both K-major
+//     dgrad    : dX [M x K] = dYq  [M x N] . WqT [K x N]^T   both K-major
+//     dgrad_mn : dX [M x K] = dYq  [M x N] . (Wq [N x K], read MN-major)
+//     wgrad    : dW [N x K] = dYqT [N x M] . XqT [K x M]^T   both K-major
+//     wgrad_mn : dW [N x K] = (dYq [M x N], MN-major) . (Xq [M x K], MN-major)
+// (e4m3 x e4m3 forward, e5m2 x e4m3 backward) and the epilogue computes
+// C = bf16_RN(acc_fp32 * (inv_a * inv_b)).  The two readings of the same
+// bytes give bit-identical products.
 //
 // Kernel structure: clusters of two CTAs (one per SM of a pair), persistent,
 // 192 threads per CTA.  A CTA pair owns a 256 x 256 output tile and computes
@@ -166,6 +172,17 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
+// Start-address step, in 16-byte units, of the k-th K = 32 slice of a
+// 128 x 128-byte slab.  K-major slab: rows are operand rows, so the slice
+// starts 32 bytes further along each swizzled row.  MN-major slab: rows are
+// contraction indices, so the slice starts 32 rows (4 KB) further down; the
+// same descriptor (128-byte swizzle, 1024-byte stride between 8-row groups)
+// describes both, with the majorness in the instruction descriptor.
+template <bool MN>
+__device__ __forceinline__ uint64_t kslice(int k) {
+    return MN ? (uint64_t)((k * kUmmaK * 128) >> 4) : (uint64_t)((k * kUmmaK) >> 4);
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -281,7 +298,10 @@ struct TileMap {
 // VEC = false: inv_a, inv_b point to one float each (per-tensor scaling).
 // VEC = true:  inv_a[P] and inv_b[Q] hold one inverse scale per row of A and
 //              per row of B (row-wise scaling): C[p][q] = acc * (inv_a[p] * inv_b[q]).
-template <bool VEC>
+// A_MN / B_MN: the operand is stored MN-major ([R x P] / [R x Q], the row
+//              index contiguous) and loaded as 128 contraction rows x 128
+//              bytes per slab; otherwise K-major ([P x R] / [Q x R]).
+template <bool VEC, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
 fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_c, int P, int Q, int R, const float *__restrict__ inv_a,
@@ -357,8 +377,10 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     const uint32_t fb_local = smem_u32(&full[stage]);
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
                     const uint32_t fb = mapa_shared(fb_local, 0);
-                    tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
-                    tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
+                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
+                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
+                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
+                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -410,9 +432,8 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                         const uint64_t b_desc = b_desc0 + (uint64_t)(stage * (kBStage >> 4));
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            // advance the start address by k * 32 bytes inside the swizzle row
-                            const uint64_t off = (uint64_t)((k * kUmmaK) >> 4);
-                            umma_f8f6f4_pair(d_tmem, a_desc + off, b_desc + off, idesc, (kb | k) != 0 ? 1u : 0u);
+                            umma_f8f6f4_pair(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc,
+                                             (kb | k) != 0 ? 1u : 0u);
                         }
                         umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
                     }
@@ -421,8 +442,7 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                         const uint64_t b_desc = b_desc0 + (uint64_t)(stage2 * (kBStage >> 4));
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            const uint64_t off = (uint64_t)((k * kUmmaK) >> 4);
-                            umma_f8f6f4_pair(d_tmem, a_desc + off, b_desc + off, idesc, 1u);
+                            umma_f8f6f4_pair(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc, 1u);
                         }
                         umma_commit_multicast(smem_u32(&empty[stage2]), 0x3);
                     }
@@ -577,6 +597,21 @@ bool make_output_map(CUtensorMap *map, void *base, int64_t rows, int64_t cols) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over an operand read MN-major: logically [P x R], stored as the
+// row-major [R x P] byte matrix (P contiguous); box = 128 contraction rows x
+// box_cols bytes.
+bool make_operand_map_mn(CUtensorMap *map, const void *base, int64_t P, int64_t R, int box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)P, (cuuint64_t)R};
+    cuuint64_t strides[1] = {(cuuint64_t)P};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kBK};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over a row-major [rows x inner] byte matrix, box = box_rows x 128 bytes.
 bool make_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t inner, int box_rows) {
     EncodeTiledFn fn = encode_fn();
@@ -592,20 +627,29 @@ bool make_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t 
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: fp32 accumulator
 // (bits 4..5 = 1), A / B formats (bits 7..9 / 10..12: 0 = e4m3, 1 = e5m2),
-// both operands K-major (bits 15, 16 = 0), N >> 3 at bits 17..22, M >> 4 at
-// bits 24..28; M and N are the pair's (256 x 256).
-uint32_t make_idesc(fp8lin_fmt fa, fp8lin_fmt fb) {
+// A / B majorness (bits 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 at bits
+// 17..22, M >> 4 at bits 24..28; M and N are the pair's (256 x 256).
+uint32_t make_idesc(fp8lin_fmt fa, fp8lin_fmt fb, bool a_mn, bool b_mn) {
     uint32_t d = 0;
     d |= 1u << 4;
     d |= (uint32_t)fa << 7;
     d |= (uint32_t)fb << 10;
+    d |= (uint32_t)a_mn << 15;
+    d |= (uint32_t)b_mn << 16;
     d |= (uint32_t)(kPairN >> 3) << 17;
     d |= (uint32_t)(kPairM >> 4) << 24;
     return d;
 }
 
-std::atomic<bool> g_smem_attr_set[2][64];
-std::atomic<int> g_max_clusters[2][64];
+// Per kernel instance (scale mode x A majorness x B majorness) and device:
+// attributes set, co-resident clusters.
+std::atomic<bool> g_smem_attr_set[8][64];
+std::atomic<int> g_max_clusters[8][64];
+
+template <bool VEC, bool A_MN, bool B_MN>
+constexpr int instance() {
+    return VEC * 4 + A_MN * 2 + B_MN;
+}
 
 cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
@@ -622,7 +666,7 @@ cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttrib
     return cfg;
 }
 
-template <bool VEC>
+template <bool VEC, bool A_MN, bool B_MN>
 fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const uint8_t *B, fp8lin_fmt fb,
                       const float *inv_b, void *C, int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
     using namespace fp8lin;
@@ -648,25 +692,28 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     if (tiles_m * tiles_n > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
 
     CUtensorMap map_a, map_b, map_c;
-    if (!make_operand_map(&map_a, A, P, R, kBM) || !make_operand_map(&map_b, B, Q, R, kBN) ||
+    const bool ok_a = A_MN ? make_operand_map_mn(&map_a, A, P, R, kBM) : make_operand_map(&map_a, A, P, R, kBM);
+    const bool ok_b = B_MN ? make_operand_map_mn(&map_b, B, Q, R, kBN) : make_operand_map(&map_b, B, Q, R, kBN);
+    if (!ok_a || !ok_b ||
         !make_output_map(&map_c, C, P, Q))
         return FP8LIN_ERR_CUDA;
 
     if (dev.device >= 64) return FP8LIN_ERR_CUDA;
-    if (!g_smem_attr_set[VEC][dev.device].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(fp8_gemm_tn_kernel<VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (!g_smem_attr_set[instance<VEC, A_MN, B_MN>()][dev.device].load(std::memory_order_acquire)) {
+        auto kernel = fp8_gemm_tn_kernel<VEC, A_MN, B_MN>;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(fp8_gemm_tn_kernel<VEC>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return FP8LIN_ERR_CUDA;
         // pairs that can be resident at once (a GPC with an odd number of free SMs leaves one idle)
         int clusters = 0;
         cudaLaunchAttribute attr;
         cudaLaunchConfig_t cfg = launch_config(2 * (dev.sm_count / 2), nullptr, &attr);
-        if (cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_tn_kernel<VEC>, &cfg) != cudaSuccess || clusters < 1)
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1)
             clusters = dev.sm_count / 2;
-        g_max_clusters[VEC][dev.device].store(clusters, std::memory_order_relaxed);
-        g_smem_attr_set[VEC][dev.device].store(true, std::memory_order_release);
+        g_max_clusters[instance<VEC, A_MN, B_MN>()][dev.device].store(clusters, std::memory_order_relaxed);
+        g_smem_attr_set[instance<VEC, A_MN, B_MN>()][dev.device].store(true, std::memory_order_release);
     }
 
     // Raster: keep the smaller operand resident in L2 and stream the larger
@@ -695,13 +742,14 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         }
     }
     const int num_tiles = (int)(tiles_m * tiles_n);
-    const int max_pairs = g_max_clusters[VEC][dev.device].load(std::memory_order_relaxed);
+    const int max_pairs = g_max_clusters[instance<VEC, A_MN, B_MN>()][dev.device].load(std::memory_order_relaxed);
     const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_config(2 * pairs, stream, &attr);
     const int p = (int)P, q = (int)Q, r = (int)R;
-    const uint32_t idesc = make_idesc(fa, fb);
-    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel<VEC>, map_a, map_b, map_c, p, q, r, inv_a, inv_b, idesc, tm) !=
+    const uint32_t idesc = make_idesc(fa, fb, A_MN, B_MN);
+    if (cudaLaunchKernelEx(&cfg, fp8_gemm_tn_kernel<VEC, A_MN, B_MN>, map_a, map_b, map_c, p, q, r, inv_a, inv_b,
+                           idesc, tm) !=
         cudaSuccess)
         return FP8LIN_ERR_CUDA;
     return check_launch();
@@ -711,37 +759,50 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
 
 extern "C" fp8lin_status fp8lin_fwd(const uint8_t *xq, const float *inv_x, const uint8_t *wq, const float *inv_w,
                                     void *y, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
-    return gemm_tn<false>(xq, FP8LIN_E4M3, inv_x, wq, FP8LIN_E4M3, inv_w, y, M, N, K, stream);
+    return gemm_tn<false, false, false>(xq, FP8LIN_E4M3, inv_x, wq, FP8LIN_E4M3, inv_w, y, M, N, K, stream);
 }
 
 extern "C" fp8lin_status fp8lin_dgrad(const uint8_t *dyq, const float *inv_dy, const uint8_t *wqT,
                                       const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
                                       cudaStream_t stream) {
-    return gemm_tn<false>(dyq, FP8LIN_E5M2, inv_dy, wqT, FP8LIN_E4M3, inv_w, dx, M, K, N, stream);
+    return gemm_tn<false, false, false>(dyq, FP8LIN_E5M2, inv_dy, wqT, FP8LIN_E4M3, inv_w, dx, M, K, N, stream);
 }
 
 extern "C" fp8lin_status fp8lin_wgrad(const uint8_t *dyqT, const float *inv_dy, const uint8_t *xqT,
                                       const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
                                       cudaStream_t stream) {
-    return gemm_tn<false>(dyqT, FP8LIN_E5M2, inv_dy, xqT, FP8LIN_E4M3, inv_x, dw, N, K, M, stream);
+    return gemm_tn<false, false, false>(dyqT, FP8LIN_E5M2, inv_dy, xqT, FP8LIN_E4M3, inv_x, dw, N, K, M, stream);
+}
+
+// The backward GEMMs on the row-major FP8 copies the cast writes as q.
+extern "C" fp8lin_status fp8lin_dgrad_mn(const uint8_t *dyq, const float *inv_dy, const uint8_t *wq,
+                                         const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
+                                         cudaStream_t stream) {
+    return gemm_tn<false, false, true>(dyq, FP8LIN_E5M2, inv_dy, wq, FP8LIN_E4M3, inv_w, dx, M, K, N, stream);
+}
+
+extern "C" fp8lin_status fp8lin_wgrad_mn(const uint8_t *dyq, const float *inv_dy, const uint8_t *xq,
+                                         const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
+                                         cudaStream_t stream) {
+    return gemm_tn<false, true, true>(dyq, FP8LIN_E5M2, inv_dy, xq, FP8LIN_E4M3, inv_x, dw, N, K, M, stream);
 }
 
 extern "C" fp8lin_status fp8lin_fwd_rowwise(const uint8_t *xq, const float *inv_x_rows, const uint8_t *wq,
                                             const float *inv_w_rows, void *y, int64_t M, int64_t N, int64_t K,
                                             cudaStream_t stream) {
-    return gemm_tn<true>(xq, FP8LIN_E4M3, inv_x_rows, wq, FP8LIN_E4M3, inv_w_rows, y, M, N, K, stream);
+    return gemm_tn<true, false, false>(xq, FP8LIN_E4M3, inv_x_rows, wq, FP8LIN_E4M3, inv_w_rows, y, M, N, K, stream);
 }
 
 extern "C" fp8lin_status fp8lin_dgrad_rowwise(const uint8_t *dyq, const float *inv_dy_rows, const uint8_t *wqT,
                                               const float *inv_w_cols, void *dx, int64_t M, int64_t N, int64_t K,
                                               cudaStream_t stream) {
-    return gemm_tn<true>(dyq, FP8LIN_E5M2, inv_dy_rows, wqT, FP8LIN_E4M3, inv_w_cols, dx, M, K, N, stream);
+    return gemm_tn<true, false, false>(dyq, FP8LIN_E5M2, inv_dy_rows, wqT, FP8LIN_E4M3, inv_w_cols, dx, M, K, N, stream);
 }
 
 extern "C" fp8lin_status fp8lin_wgrad_rowwise(const uint8_t *dyqT, const float *inv_dy_cols, const uint8_t *xqT,
                                               const float *inv_x_cols, void *dw, int64_t M, int64_t N, int64_t K,
                                               cudaStream_t stream) {
-    return gemm_tn<true>(dyqT, FP8LIN_E5M2, inv_dy_cols, xqT, FP8LIN_E4M3, inv_x_cols, dw, N, K, M, stream);
+    return gemm_tn<true, false, false>(dyqT, FP8LIN_E5M2, inv_dy_cols, xqT, FP8LIN_E4M3, inv_x_cols, dw, N, K, M, stream);
 }
 
 namespace {

@@ -25,6 +25,8 @@
  *               fp8lin_fwd(Xq, Wq) -> Y
  *     backward: fp8lin_amax(dY), fp8lin_cast_transpose(dY -> dYq, dYqT),
  *               fp8lin_dgrad(dYq, WqT) -> dX, fp8lin_wgrad(dYqT, XqT) -> dW
+ * or, with no transposed copies (qT = NULL in every cast):
+ *               fp8lin_dgrad_mn(dYq, Wq) -> dX, fp8lin_wgrad_mn(dYq, Xq) -> dW
  *
  * Ownership: the caller allocates and owns every buffer (device memory),
  * including the one-float amax / scale / inverse-scale slots.  No entry
@@ -244,6 +246,35 @@ fp8lin_status fp8lin_dgrad(const uint8_t *dyq, const float *inv_dy, const uint8_
 fp8lin_status fp8lin_wgrad(const uint8_t *dyqT, const float *inv_dy, const uint8_t *xqT,
                            const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
                            cudaStream_t stream);
+
+/*
+ * The two backward GEMMs on the row-major FP8 copies (q of
+ * fp8lin_cast_transpose), so a per-tensor-scaled linear needs no transposed
+ * copy.  Same products, bit for bit, as fp8lin_dgrad / fp8lin_wgrad on the
+ * transposed copies: the tensor cores read an 8-bit operand either
+ * contraction-contiguous or row-index-contiguous, and these entry points
+ * read Wq, dYq and Xq the second way.  With them each tensor of a
+ * per-tensor-scaled step (TorchTitan analysis page, section 3.3: Float8
+ * forward and backward through autograd) is cast once, to the one FP8 copy
+ * that all three GEMMs read.  Row-wise scaling still needs the transposed
+ * copies, whose scales run along the other axis.
+ *
+ * fp8lin_dgrad_mn: dX = bf16_RN( (dYq . Wq)_fp32 * (inv_dy * inv_w) ) = dY . W
+ *   dyq     device, e5m2 [M x N] row-major, 16-byte aligned.
+ *   wq      device, e4m3 [N x K] row-major (the copy fp8lin_fwd reads).
+ *   dx      device, bf16 [M x K] row-major, 16-byte aligned; fully overwritten.
+ * fp8lin_wgrad_mn: dW = bf16_RN( (dYq^T . Xq)_fp32 * (inv_dy * inv_x) ) = dY^T . X
+ *   dyq     device, e5m2 [M x N] row-major, 16-byte aligned.
+ *   xq      device, e4m3 [M x K] row-major (the copy fp8lin_fwd reads).
+ *   dw      device, bf16 [N x K] row-major, 16-byte aligned; fully overwritten.
+ * inv_*, M, N, K and the errors as for fp8lin_dgrad / fp8lin_wgrad.
+ */
+fp8lin_status fp8lin_dgrad_mn(const uint8_t *dyq, const float *inv_dy, const uint8_t *wq,
+                              const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream);
+fp8lin_status fp8lin_wgrad_mn(const uint8_t *dyq, const float *inv_dy, const uint8_t *xq,
+                              const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream);
 
 /*
  * The three GEMMs with row-wise scales: C[p][q] = bf16_RN(acc[p][q] *

@@ -41,6 +41,37 @@ def test_binding_lists_every_declared_symbol(lib):
     assert sorted(fl.ENTRY_POINTS) == declared_entry_points()
 
 
+def declared_parameter_types():
+    """name -> list of C parameter types, from the header's prototypes."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(fp8lin_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        types = []
+        for p in params.split(","):
+            p = " ".join(p.split())
+            if p in ("", "void"):
+                continue
+            types.append(p.rsplit(" ", 1)[0] if "*" not in p else "pointer")
+        out[name] = types
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every argument type the binding declares is the header's: an
+    undeclared or narrowed pointer would reach the kernels truncated."""
+    import float8_linear_layers_gb300 as fl
+    ctype_of = {"pointer": ctypes.c_void_p, "cudaStream_t": ctypes.c_void_p, "int64_t": ctypes.c_int64,
+                "uint64_t": ctypes.c_uint64, "float": ctypes.c_float, "fp8lin_fmt": ctypes.c_int,
+                "fp8lin_status": ctypes.c_int, "int": ctypes.c_int}
+    decl = declared_parameter_types()
+    assert set(decl) == set(fl.ENTRY_POINTS)
+    for name, types in decl.items():
+        if name == "fp8lin_status_str":
+            continue
+        want = [ctype_of[t.replace("const ", "")] for t in types]
+        assert fl.SIGNATURES[name] == want, f"{name}: binding {fl.SIGNATURES[name]} vs header {types}"
+
+
 def test_status_strings(lib):
     lib.fp8lin_status_str.restype = ctypes.c_char_p
     for s in range(7):

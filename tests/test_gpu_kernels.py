@@ -217,12 +217,44 @@ def test_gemm_closed_forms(fp8lin):
 
 # -------------------------------------------------------------- sequence
 
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_mn_operands_match_transposed_copies(fp8lin, M, N, K):
+    """dgrad / wgrad reading the row-major copies MN-major: the oracle's
+    product, and bit for bit what the K-major GEMMs give on the transposed
+    copies of the same bytes."""
+    seed = M * 5 + N * 11 + K
+    dyq, idy = _codes((M, N), E5M2, seed)
+    wq, iw = _codes((N, K), E4M3, seed + 1)
+    xq, ix = _codes((M, K), E4M3, seed + 2)
+    d_dyq, d_wq, d_xq = to_dev_u8(dyq), to_dev_u8(wq), to_dev_u8(xq)
+    sdy, sw, sx = (torch.tensor([v], dtype=torch.float32, device="cuda") for v in (idy, iw, ix))
+    dx_mn, dw_mn = Guarded((M, K), torch.bfloat16), Guarded((N, K), torch.bfloat16)
+    dx_mn.t.fill_(float("nan"))
+    dw_mn.t.fill_(float("nan"))
+    fp8lin.fp8lin_dgrad_mn(d_dyq, sdy, d_wq, sw, dx_mn.t)
+    fp8lin.fp8lin_wgrad_mn(d_dyq, sdy, d_xq, sx, dw_mn.t)
+    dx_t = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw_t = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_dgrad(d_dyq, sdy, to_dev_u8(np.ascontiguousarray(wq.T)), sw, dx_t)
+    fp8lin.fp8lin_wgrad(to_dev_u8(np.ascontiguousarray(dyq.T)), sdy, to_dev_u8(np.ascontiguousarray(xq.T)), sx, dw_t)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    assert dx_mn.intact() and dw_mn.intact()
+    assert torch.equal(dx_mn.t.view(torch.int16), dx_t.view(torch.int16))
+    assert torch.equal(dw_mn.t.view(torch.int16), dw_t.view(torch.int16))
+    assert_gemm_close(bf16_to_f64(dx_mn.t), oracle.dgrad_ref(dyq, idy, np.ascontiguousarray(wq.T), iw),
+                      f"dgrad_mn {M}x{N}x{K}")
+    assert_gemm_close(bf16_to_f64(dw_mn.t), oracle.wgrad_ref(np.ascontiguousarray(dyq.T), idy,
+                                                             np.ascontiguousarray(xq.T), ix), f"wgrad_mn {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("transpose", [False, True])
 @pytest.mark.parametrize("M,K,N", [(256, 512, 1024), (144, 208, 272), (640, 384, 1296)])
-def test_float8_linear_step_matches_oracle(fp8lin, M, K, N):
+def test_float8_linear_step_matches_oracle(fp8lin, M, K, N, transpose):
     X = wl.generate((M, K), "normal", 1.0, 3, wl.X)
     W = wl.generate((N, K), "normal", 0.02, 3, wl.W)
     dY = wl.generate((M, N), "normal", 1e-3, 3, wl.DY)
-    lin = fp8lin.Float8Linear(M, K, N)
+    lin = fp8lin.Float8Linear(M, K, N, transpose=transpose)
     y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
     torch.cuda.synchronize()
     ox, ow, od = oracle.quantize(X, E4M3), oracle.quantize(W, E4M3), oracle.quantize(dY, E5M2)
@@ -231,7 +263,10 @@ def test_float8_linear_step_matches_oracle(fp8lin, M, K, N):
         assert scalar_bits(t8.scale) == f32_bits(r["scale"])
         assert scalar_bits(t8.inv_scale) == f32_bits(r["inv_scale"])
         assert np.array_equal(t8.q.cpu().numpy(), r["q"])
-        assert np.array_equal(t8.qT.cpu().numpy(), r["qT"])
+        if transpose:
+            assert np.array_equal(t8.qT.cpu().numpy(), r["qT"])
+        else:
+            assert t8.qT is None
     assert_gemm_close(bf16_to_f64(y), oracle.fwd_ref(ox["q"], ox["inv_scale"], ow["q"], ow["inv_scale"]), "Y")
     assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_ref(od["q"], od["inv_scale"], ow["qT"], ow["inv_scale"]), "dX")
     assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_ref(od["qT"], od["inv_scale"], ox["qT"], ox["inv_scale"]), "dW")

@@ -31,12 +31,20 @@ def _rows(n, seed):
 def test_workload_step_matches_oracle(fp8lin, name):
     w = wl.WORKLOADS[name]
     X, W, dY = w.make_x(), w.make_w(), w.make_dy()
-    lin = fp8lin.Float8Linear(w.M, w.K, w.N)
+    lin = fp8lin.Float8Linear(w.M, w.K, w.N, transpose=True)
     xd, wd, dd = to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY)
     y, dx, dw = lin.step(xd, wd, dd)
+    # the default path (one FP8 copy per tensor, backward GEMMs reading it
+    # MN-major) must give the same bytes
+    one = fp8lin.Float8Linear(w.M, w.K, w.N)
+    y1, dx1, dw1 = one.step(xd, wd, dd)
     torch.cuda.synchronize()
     assert fp8lin.fp8lin_device_error() == 0
     del xd, wd, dd
+    assert one.x8.qT is None and torch.equal(one.dy8.q, lin.dy8.q)
+    for a, b, n in ((y1, y, "Y"), (dx1, dx, "dX"), (dw1, dw, "dW")):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name} {n}: MN-major path differs"
+    del one, y1, dx1, dw1
 
     refs = {}
     for key, bits, fmt, t8 in (("x", X, E4M3, lin.x8), ("w", W, E4M3, lin.w8), ("dy", dY, E5M2, lin.dy8)):
