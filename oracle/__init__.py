@@ -96,6 +96,16 @@ def _load():
         lib.orc_gemm_rows_vec.restype = None
         lib.orc_gemm_rows_vec.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_void_p]
+        lib.orc_scales.restype = None
+        lib.orc_scales.argtypes = [ctypes.c_void_p, i64, f32, ctypes.c_void_p, ctypes.c_void_p]
+        lib.orc_amax_blocks_bf16.restype = None
+        lib.orc_amax_blocks_bf16.argtypes = [ctypes.c_void_p, i64, i64, i64, i64, ctypes.c_void_p]
+        lib.orc_cast_blocks_bf16.restype = None
+        lib.orc_cast_blocks_bf16.argtypes = [ctypes.c_void_p, i64, i64, i64, i64, ctypes.c_int, ctypes.c_void_p,
+                                             u8p]
+        lib.orc_gemm_blocks.restype = None
+        lib.orc_gemm_blocks.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64, i64,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_void_p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -278,6 +288,116 @@ def gemm_rows_vec(A: np.ndarray, fa: int, B: np.ndarray, fb: int, inv_a: np.ndar
     _load().orc_gemm_rows_vec(_ptr(A), fa, _ptr(B), fb, P, Q, R, _ptr(ia), _ptr(ib), _ptr(rows), rows.size,
                               _ptr(out))
     return out
+
+
+# ------------------------------------------------------------ block scaling
+
+BLOCK = 128  # contraction block of the block recipe: 1 x 128 and 128 x 128 blocks
+
+
+def scales_array(amax_values: np.ndarray, fmt_max: float = FMT_MAX):
+    """scale() of every entry of an amax array (any shape), in C."""
+    a = np.ascontiguousarray(amax_values, dtype=np.float32)
+    s = np.empty_like(a)
+    inv = np.empty_like(a)
+    _load().orc_scales(_ptr(a), a.size, float(np.float32(fmt_max)), _ptr(s), _ptr(inv))
+    return s, inv
+
+
+def amax_blocks(x_bits: np.ndarray, br: int, bc: int) -> np.ndarray:
+    """amax of every br x bc block of a bf16 matrix ([ceil(rows/br) x ceil(cols/bc)];
+    edge blocks are cut short)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    out = np.empty(((rows + br - 1) // br, (cols + bc - 1) // bc), dtype=np.float32)
+    _load().orc_amax_blocks_bf16(_ptr(x), rows, cols, br, bc, _ptr(out))
+    return out
+
+
+def cast_blocks(x_bits: np.ndarray, fmt: int, br: int, bc: int, block_scales: np.ndarray) -> np.ndarray:
+    """q[r][c] = sat_RNE(fp32(x[r][c]) * scale[r // br][c // bc])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    sc = np.ascontiguousarray(block_scales, dtype=np.float32)
+    rows, cols = x.shape
+    assert sc.shape == ((rows + br - 1) // br, (cols + bc - 1) // bc)
+    q = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_cast_blocks_bf16(_ptr(x), rows, cols, br, bc, fmt, _ptr(sc), _ptr(q))
+    return q
+
+
+def quantize_blocks(x_bits: np.ndarray, fmt: int, br: int, bc: int, fmt_max: float = FMT_MAX) -> dict:
+    """Block scaling ([L9]: one factor per tensor, "or even per block"): the
+    per-tensor recipe applied to every br x bc block of x on its own --
+    amax of the block, scale = fmt_max / max(amax, 1e-12), saturating RNE
+    cast of the block's elements.  Returns amax, scale and inv_scale as
+    [blocks down x blocks across] arrays and q (row-major, like x)."""
+    a = amax_blocks(x_bits, br, bc)
+    s, inv = scales_array(a, fmt_max)
+    return {"amax": a, "scale": s, "inv_scale": inv, "q": cast_blocks(x_bits, fmt, br, bc, s)}
+
+
+def gemm_blocks(A: np.ndarray, fa: int, B: np.ndarray, fb: int, inv_a: np.ndarray, inv_b: np.ndarray,
+                rb: int = BLOCK, rows=None) -> np.ndarray:
+    """C[p][q] = sum_j (sum_{k in block j} dec(A[p][k]) dec(B[q][k])) * inv_a[p][j] * inv_b[q][j]
+    in float64: the GEMM with block scales along the contraction (blocks of
+    rb indices).  A [P x R] and B [Q x R] codes, contraction contiguous;
+    inv_a [P x nb], inv_b [Q x nb] with nb = ceil(R / rb)."""
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    P, R = A.shape
+    Q, R2 = B.shape
+    assert R == R2
+    nb = (R + rb - 1) // rb
+    ia = np.ascontiguousarray(inv_a, dtype=np.float32)
+    ib = np.ascontiguousarray(inv_b, dtype=np.float32)
+    assert ia.shape == (P, nb) and ib.shape == (Q, nb)
+    if rows is None:
+        rows = np.arange(P, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, Q), dtype=np.float64)
+    _load().orc_gemm_blocks(_ptr(A), fa, _ptr(B), fb, P, Q, R, rb, _ptr(ia), _ptr(ib), _ptr(rows), rows.size,
+                            _ptr(out))
+    return out
+
+
+def quantize_block_recipe(x_bits, w_bits, dy_bits, fmt_max: float = FMT_MAX) -> dict:
+    """The FP8 copies of one linear under block scaling, each with its blocks
+    along the contraction of the GEMM that reads it (reading in the design
+    notes): X in 1 x 128 blocks (forward, contraction K) and 128 x 1 blocks
+    (weight gradient, contraction M); W in 128 x 128 blocks (forward and
+    input gradient); dY in 1 x 128 blocks (input gradient, contraction N)
+    and 128 x 1 blocks (weight gradient)."""
+    return {"x_k": quantize_blocks(x_bits, E4M3, 1, BLOCK, fmt_max),
+            "x_m": quantize_blocks(x_bits, E4M3, BLOCK, 1, fmt_max),
+            "w": quantize_blocks(w_bits, E4M3, BLOCK, BLOCK, fmt_max),
+            "dy_n": quantize_blocks(dy_bits, E5M2, 1, BLOCK, fmt_max),
+            "dy_m": quantize_blocks(dy_bits, E5M2, BLOCK, 1, fmt_max)}
+
+
+def _rows_of(block_inv: np.ndarray, n: int) -> np.ndarray:
+    """[nbr x nb] block inverse scales of 128-row blocks -> one row per operand row ([n x nb])."""
+    return np.ascontiguousarray(np.repeat(block_inv, BLOCK, axis=0)[:n])
+
+
+def fwd_block_ref(xq_k, ix_k, wq, iw, rows=None):
+    """Y = X . W^T with X in 1 x 128 and W in 128 x 128 blocks (contraction K)."""
+    return gemm_blocks(xq_k, E4M3, wq, E4M3, ix_k, _rows_of(iw, wq.shape[0]), BLOCK, rows)
+
+
+def dgrad_block_ref(dyq_n, idy_n, wq, iw, rows=None):
+    """dX = dY . W with dY in 1 x 128 and W in 128 x 128 blocks (contraction N):
+    B = W^T, whose row k takes the scales of W's block column k // 128."""
+    wqT = np.ascontiguousarray(np.asarray(wq).T)
+    return gemm_blocks(dyq_n, E5M2, wqT, E4M3, idy_n, _rows_of(np.asarray(iw).T, wqT.shape[0]), BLOCK, rows)
+
+
+def wgrad_block_ref(dyq_m, idy_m, xq_m, ix_m, rows=None):
+    """dW = dY^T . X with dY and X in 128 x 1 blocks (contraction M):
+    A = dY^T with row n scaled by idy_m[:, n], B = X^T with row k by ix_m[:, k]."""
+    dyqT = np.ascontiguousarray(np.asarray(dyq_m).T)
+    xqT = np.ascontiguousarray(np.asarray(xq_m).T)
+    return gemm_blocks(dyqT, E5M2, xqT, E4M3, np.ascontiguousarray(np.asarray(idy_m).T),
+                       np.ascontiguousarray(np.asarray(ix_m).T), BLOCK, rows)
 
 
 # ------------------------------------------------------------------ GEMMs

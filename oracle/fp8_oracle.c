@@ -1,6 +1,7 @@
 /*
  * fp8_oracle.c -- plain, slow CPU definition of the Float8 linear layer's hot
- * path with dynamic per-tensor scaling.
+ * path: per-tensor scaling (dynamic, delayed, static), row-wise scaling and
+ * block scaling.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
  * call this file: only the tests, the smoke check and the benchmark's CPU
@@ -204,6 +205,11 @@ void orc_scale(float amax, float fmt_max, float *scale, float *inv_scale) {
     *inv_scale = inv;
 }
 
+/* orc_scale applied to n amax values. */
+void orc_scales(const float *amax, int64_t n, float fmt_max, float *scale, float *inv_scale) {
+    for (int64_t i = 0; i < n; ++i) orc_scale(amax[i], fmt_max, &scale[i], &inv_scale[i]);
+}
+
 /* 1 / s as one binary32 round-to-nearest division (static scaling's
  * inverse scale). */
 float orc_reciprocal(float s) {
@@ -283,6 +289,45 @@ void orc_cast_rows_bf16(const uint16_t *x, int64_t rows, int64_t cols, int fmt, 
         }
 }
 
+/* Block scaling ("per block", block = br x bc elements of the row-major
+ * [rows x cols] source; blocks at the right and bottom edges are cut short):
+ * amax of block (i, j) = max |x[r][c]| over r in [i br, (i+1) br) and
+ * c in [j bc, (j+1) bc), same ordering as orc_amax_bf16 (a NaN magnitude
+ * above every number).  out is [ceil(rows/br) x ceil(cols/bc)]. */
+void orc_amax_blocks_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t br, int64_t bc, float *out) {
+    const int64_t nbr = (rows + br - 1) / br, nbc = (cols + bc - 1) / bc;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t b = 0; b < nbr * nbc; ++b) {
+        const int64_t bi = b / nbc, bj = b % nbc;
+        float best = 0.0f;
+        uint16_t nan_mag = 0;
+        for (int64_t r = bi * br; r < rows && r < (bi + 1) * br; ++r)
+            for (int64_t c = bj * bc; c < cols && c < (bj + 1) * bc; ++c) {
+                uint16_t mag = (uint16_t)(x[r * cols + c] & 0x7FFF);
+                if (mag > 0x7F80) {
+                    if (mag > nan_mag) nan_mag = mag;
+                    continue;
+                }
+                float v = orc_bf16_to_f32(mag);
+                if (v > best) best = v;
+            }
+        out[b] = nan_mag ? orc_bf16_to_f32(nan_mag) : best;
+    }
+}
+
+/* q[r][c] = encode(fp32(x[r][c]) * scale[r / br][c / bc]): the cast with one
+ * scale per block (scale is [ceil(rows/br) x ceil(cols/bc)]). */
+void orc_cast_blocks_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t br, int64_t bc, int fmt,
+                          const float *scale, uint8_t *q) {
+    const int64_t nbc = (cols + bc - 1) / bc;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            volatile float v = orc_bf16_to_f32(x[r * cols + c]) * scale[(r / br) * nbc + c / bc];
+            q[r * cols + c] = orc_fp8_encode(fmt, v);
+        }
+}
+
 /* qT[c][r] = q[r][c] for a row-major [rows x cols] byte matrix. */
 void orc_transpose_u8(const uint8_t *q, int64_t rows, int64_t cols, uint8_t *qT) {
 #pragma omp parallel for schedule(static)
@@ -345,6 +390,42 @@ void orc_gemm_rows_vec(const uint8_t *A, int fa, const uint8_t *B, int fb, int64
             for (int64_t k = 0; k < R; ++k)
                 s += da[a[k]] * db[b[k]];
             out[i * Q + q] = s * (double)inv_a[rows[i]] * (double)inv_b[q];
+        }
+    }
+}
+
+/* The GEMM with block scales along the contraction: the contraction is cut
+ * into blocks of rb indices (the last one short), and
+ *     C[p][q] = sum over blocks j of
+ *               ( sum_{k in block j} dec(A[p][k]) * dec(B[q][k]) ) * inv_a[p][j] * inv_b[q][j],
+ * each block's sum in binary64 in increasing k, scaled in binary64, the
+ * blocks added in increasing j.  inv_a is [P x nb], inv_b is [Q x nb]
+ * (nb = ceil(R / rb)): one inverse scale per operand row and contraction
+ * block, whatever block shape the operand was quantised with. */
+void orc_gemm_blocks(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t P, int64_t Q, int64_t R,
+                     int64_t rb, const float *inv_a, const float *inv_b, const int64_t *rows, int64_t nrows,
+                     double *out) {
+    double da[256], db[256];
+    for (int c = 0; c < 256; ++c) {
+        da[c] = orc_fp8_decode(fa, (uint8_t)c);
+        db[c] = orc_fp8_decode(fb, (uint8_t)c);
+    }
+    (void)P;
+    const int64_t nb = (R + rb - 1) / rb;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t p = rows[i];
+        const uint8_t *a = A + p * R;
+        for (int64_t q = 0; q < Q; ++q) {
+            const uint8_t *b = B + q * R;
+            double total = 0.0;
+            for (int64_t j = 0; j < nb; ++j) {
+                double s = 0.0;
+                for (int64_t k = j * rb; k < R && k < (j + 1) * rb; ++k)
+                    s += da[a[k]] * db[b[k]];
+                total += s * (double)inv_a[p * nb + j] * (double)inv_b[q * nb + j];
+            }
+            out[i * Q + q] = total;
         }
     }
 }
