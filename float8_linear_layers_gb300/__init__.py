@@ -44,6 +44,7 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
 ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_static",
                 "fp8lin_cast_transpose_delayed", "fp8lin_amax_rowcol", "fp8lin_cast_transpose_rowwise",
                 "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
+                "fp8lin_cast_blockwise",
                 "fp8lin_fwd_rowwise", "fp8lin_dgrad_rowwise", "fp8lin_wgrad_rowwise",
                 "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
@@ -83,6 +84,7 @@ SIGNATURES = {
     "fp8lin_cast_transpose_delayed": [_vp, _i64, _i64, _ci, _f32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_amax_rowcol": [_vp, _i64, _i64, _vp, _vp, _vp],
     "fp8lin_cast_transpose_rowwise": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_cast_blockwise": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_fwd_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_dgrad_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_wgrad_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
@@ -195,6 +197,23 @@ def fp8lin_cast_transpose_delayed(x: torch.Tensor, fmt: int, amax_history: torch
            _lib.fp8lin_cast_transpose_delayed(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(amax_history),
                                               amax_history.numel(), int(slot), _ptr(scale), _ptr(inv_scale),
                                               _ptr(q), _ptr(qT), _stream(stream)))
+
+
+def fp8lin_cast_blockwise(x: torch.Tensor, fmt: int, q_row=None, inv_row=None, q_col=None, inv_col=None,
+                          q_tile=None, inv_tile=None, fmt_max: float = FMT_MAX, stream=None) -> None:
+    """Block scaling in one pass: q_row / inv_row (1 x 128 blocks), q_col / inv_col
+    (128 x 1 blocks), q_tile / inv_tile (128 x 128 blocks); any subset of the pairs."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [rows x cols] matrix")
+    for t, n in ((q_row, "q_row"), (q_col, "q_col"), (q_tile, "q_tile")):
+        _dev(t, n)
+    for t, n in ((inv_row, "inv_row"), (inv_col, "inv_col"), (inv_tile, "inv_tile")):
+        _dev(t, n, torch.float32)
+    rows, cols = x.shape
+    _check("fp8lin_cast_blockwise",
+           _lib.fp8lin_cast_blockwise(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(q_row), _ptr(inv_row),
+                                      _ptr(q_col), _ptr(inv_col), _ptr(q_tile), _ptr(inv_tile), _stream(stream)))
 
 
 def fp8lin_amax_rowcol(x: torch.Tensor, row_amax: torch.Tensor | None, col_amax: torch.Tensor | None,

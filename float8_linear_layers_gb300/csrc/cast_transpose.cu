@@ -325,6 +325,149 @@ fp8lin_status set_carveouts(int device) {
     return st;
 }
 
+// ------------------------------------------------------------ block scaling
+
+// Block scaling: every block is scaled like a tensor of its own (amax of the
+// block, scale = fmt_max / max(amax, 1e-12), saturating RNE cast).  Every
+// 1 x 128, 128 x 1 and 128 x 128 block lies inside one 128 x 128 tile, so one
+// pass over x makes any of
+//   ROW : 1 x 128 blocks (a scale per row of the tile)     q_row, inv_row [rows x tiles_c]
+//   COL : 128 x 1 blocks (a scale per column of the tile)  q_col, inv_col [tiles_r x cols]
+//   TILE: the 128 x 128 block                              q_tile, inv_tile [tiles_r x tiles_c]
+// (each copy row-major like x), with no separate amax pass: 2 bytes read and
+// 1 byte written per element and copy.  Row maxima reduce over the 16 lanes
+// that share a row; column maxima over the thread's 8 rows, the lane pair
+// 16 apart, then the 8 warps through shared memory.
+template <int FMT, bool ROW, bool COL, bool TILE>
+__global__ void __launch_bounds__(kThreads)
+cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c, float fmt_max,
+                  uint8_t *__restrict__ q_row, float *__restrict__ inv_row, uint8_t *__restrict__ q_col,
+                  float *__restrict__ inv_col, uint8_t *__restrict__ q_tile, float *__restrict__ inv_tile) {
+    __shared__ uint32_t col_part[COL ? kThreads / 32 : 1][kTile];  // per-warp column maxima (magnitude bits)
+    __shared__ float col_scale[COL ? kTile : 1];
+    __shared__ uint32_t warp_max[kThreads / 32];
+
+    const int tr = (int)blockIdx.x / tiles_c, tc = (int)blockIdx.x % tiles_c;
+    const int r0 = tr * kTile, c0 = tc * kTile;
+    const int t = threadIdx.x, lane = t % 32, warp = t / 32;
+    const int ch = t % 16;        // 8-column chunk of the tile row
+    const int row_base = t / 16;  // rows row_base + 16 i
+    const bool col_in = (c0 + ch * 8) < cols;
+    const uint64_t pol = evict_first_policy();
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + row_base + 16 * i;
+        v[i] = (col_in && r < rows) ? ld_stream16(x + (int64_t)r * cols + c0 + ch * 8, pol) : make_uint4(0, 0, 0, 0);
+    }
+
+    // magnitudes as bf16 bit patterns without the sign: their unsigned order
+    // is the order of |x| (a NaN above everything); zero padding never wins
+    const uint32_t k = 0x7FFF7FFFu;
+    uint32_t rowm[8];
+    uint32_t colm2[4] = {0, 0, 0, 0};  // packed pairs: columns 2j, 2j + 1 of this thread's chunk
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = v[i].x & k, b = v[i].y & k, c = v[i].z & k, d = v[i].w & k;
+        const uint32_t m = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
+        rowm[i] = max(m & 0xFFFFu, m >> 16);
+        colm2[0] = __vmaxu2(colm2[0], a);
+        colm2[1] = __vmaxu2(colm2[1], b);
+        colm2[2] = __vmaxu2(colm2[2], c);
+        colm2[3] = __vmaxu2(colm2[3], d);
+    }
+    if (ROW) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) rowm[i] = max(rowm[i], __shfl_xor_sync(0xFFFFFFFFu, rowm[i], o));
+    }
+    if (COL) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t m = __vmaxu2(colm2[j], __shfl_xor_sync(0xFFFFFFFFu, colm2[j], 16));
+            if (lane < 16) {
+                col_part[warp][ch * 8 + 2 * j] = m & 0xFFFFu;
+                col_part[warp][ch * 8 + 2 * j + 1] = m >> 16;
+            }
+        }
+    }
+    if (TILE) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = max(m, rowm[i]);
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0) warp_max[warp] = m;
+    }
+    if (COL || TILE) __syncthreads();
+    if (COL) {
+        if (t < kTile) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) m = max(m, col_part[w][t]);
+            const float s = scale_from_amax(__uint_as_float(m << 16), fmt_max);
+            col_scale[t] = s;
+            if (c0 + t < cols) inv_col[(int64_t)tr * cols + c0 + t] = __frcp_rn(s);
+        }
+        __syncthreads();
+    }
+    float s_tile = 0.0f;
+    if (TILE) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) m = max(m, warp_max[w]);
+        s_tile = scale_from_amax(__uint_as_float(m << 16), fmt_max);
+        if (t == 0) inv_tile[(int64_t)tr * tiles_c + tc] = __frcp_rn(s_tile);
+    }
+    float csc[8];
+    if (COL) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) csc[e] = col_scale[ch * 8 + e];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + row_base + 16 * i;
+        const bool ok = col_in && r < rows;
+        const int64_t off = (int64_t)r * cols + c0 + ch * 8;
+        if (ROW) {
+            const float s = scale_from_amax(__uint_as_float(rowm[i] << 16), fmt_max);
+            if (ok) st_stream8(q_row + off, cast8<FMT>(v[i], s), pol);
+            if (ch == 0 && r < rows) inv_row[(int64_t)r * tiles_c + tc] = __frcp_rn(s);
+        }
+        if (COL && ok) st_stream8(q_col + off, cast8_each<FMT>(v[i], csc), pol);
+        if (TILE && ok) st_stream8(q_tile + off, cast8<FMT>(v[i], s_tile), pol);
+    }
+}
+
+template <int FMT, bool ROW, bool COL, bool TILE>
+fp8lin_status launch_block(int device, int slot, int grid, cudaStream_t stream, const uint16_t *x, int rows,
+                           int cols, int tiles_c, float fmt_max, uint8_t *q_row, float *inv_row, uint8_t *q_col,
+                           float *inv_col, uint8_t *q_tile, float *inv_tile) {
+    fp8lin_status st = fp8lin::prefer_max_shared_carveout(
+        reinterpret_cast<const void *>(&cast_block_kernel<FMT, ROW, COL, TILE>), device, slot);
+    if (st != FP8LIN_OK) return st;
+    cast_block_kernel<FMT, ROW, COL, TILE><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_c, fmt_max, q_row,
+                                                                         inv_row, q_col, inv_col, q_tile, inv_tile);
+    return FP8LIN_OK;
+}
+
+template <int FMT>
+fp8lin_status launch_block_any(int device, int which, int grid, cudaStream_t stream, const uint16_t *x, int rows,
+                               int cols, int tiles_c, float fmt_max, uint8_t *qr, float *ir, uint8_t *qc, float *ic,
+                               uint8_t *qt, float *it) {
+    // carveout slots 32.. (e4m3) and 40.. (e5m2), one per combination of copies
+    const int slot = (FMT == FP8LIN_E4M3 ? 32 : 40) + which;
+    switch (which) {
+        case 1: return launch_block<FMT, true, false, false>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        case 2: return launch_block<FMT, false, true, false>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        case 3: return launch_block<FMT, true, true, false>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        case 4: return launch_block<FMT, false, false, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        case 5: return launch_block<FMT, true, false, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        case 6: return launch_block<FMT, false, true, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        default: return launch_block<FMT, true, true, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+    }
+}
+
 // Checks shared by the three scalings, then the launch.
 fp8lin_status cast_common(int mode, const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
                           const float *src, int hist_len, int slot, float *scale, float *inv_scale, uint8_t *q,
@@ -401,6 +544,43 @@ extern "C" fp8lin_status fp8lin_cast_transpose_delayed(const void *x, int64_t ro
         return FP8LIN_ERR_INVALID_ARG;
     return cast_common(kDelayed, x, rows, cols, fmt, fmt_max, amax_history, (int)history_len, (int)slot, scale,
                        inv_scale, q, qT, amax_history + slot, stream);
+}
+
+extern "C" fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                               float fmt_max, uint8_t *q_row, float *inv_row, uint8_t *q_col,
+                                               float *inv_col, uint8_t *q_tile, float *inv_tile,
+                                               cudaStream_t stream) {
+    using namespace fp8lin;
+    // each copy comes with its inverse scales, or neither is asked for
+    if ((q_row == nullptr) != (inv_row == nullptr) || (q_col == nullptr) != (inv_col == nullptr) ||
+        (q_tile == nullptr) != (inv_tile == nullptr))
+        return FP8LIN_ERR_INVALID_ARG;
+    const int which = (q_row ? 1 : 0) | (q_col ? 2 : 0) | (q_tile ? 4 : 0);
+    if (which == 0) return FP8LIN_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return FP8LIN_ERR_INVALID_ARG;
+    if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
+    if (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f)) return FP8LIN_ERR_INVALID_ARG;
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(inv_row, 4) || !aligned(inv_col, 4) || !aligned(inv_tile, 4)) return FP8LIN_ERR_MISALIGNED;
+    if (!empty && (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16) || !aligned(q_tile, 16)))
+        return FP8LIN_ERR_MISALIGNED;
+    if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    if (empty) return FP8LIN_OK;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    if (tiles_r * tiles_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    const int grid = (int)(tiles_r * tiles_c);
+    const uint16_t *xs = static_cast<const uint16_t *>(x);
+    st = fmt == FP8LIN_E4M3
+             ? launch_block_any<FP8LIN_E4M3>(dev.device, which, grid, stream, xs, (int)rows, (int)cols, (int)tiles_c,
+                                             fmt_max, q_row, inv_row, q_col, inv_col, q_tile, inv_tile)
+             : launch_block_any<FP8LIN_E5M2>(dev.device, which, grid, stream, xs, (int)rows, (int)cols, (int)tiles_c,
+                                             fmt_max, q_row, inv_row, q_col, inv_col, q_tile, inv_tile);
+    if (st != FP8LIN_OK) return st;
+    return check_launch();
 }
 
 extern "C" fp8lin_status fp8lin_cast_transpose_rowwise(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,

@@ -277,6 +277,34 @@ fp8lin_status fp8lin_wgrad_mn(const uint8_t *dyq, const float *inv_dy, const uin
                               cudaStream_t stream);
 
 /*
+ * Block scaling: every block of x is scaled like a tensor of its own
+ * ("one factor per tensor, or even per block": Lecture 9 exercises, the
+ * answer on fp16 loss scaling versus FP8 scaling) -- amax of the block,
+ * scale = fmt_max / max(amax, 1e-12) (binary32, round to nearest even), a
+ * saturating round-to-nearest-even cast -- in one pass over x, with no
+ * separate amax call.  Any of three copies, each row-major [rows x cols]
+ * like x, with its inverse scales (1 / scale, binary32):
+ *   q_row,  inv_row  [rows x ceil(cols/128)]            1 x 128 blocks
+ *   q_col,  inv_col  [ceil(rows/128) x cols]            128 x 1 blocks
+ *   q_tile, inv_tile [ceil(rows/128) x ceil(cols/128)]  128 x 128 blocks
+ * Blocks at the right and bottom edges are cut short.  A linear takes X as
+ * q_row (forward) and q_col (weight gradient), W as q_tile, dY as q_row
+ * (input gradient) and q_col (weight gradient); see fp8lin_fwd_block.
+ *
+ *   x        device, bf16 [rows x cols] row-major, 16-byte aligned.
+ *   fmt      FP8LIN_E4M3 or FP8LIN_E5M2; fmt_max > 0 (448 by default).
+ *   q_*      device, u8 [rows x cols], 16-byte aligned, or NULL.
+ *   inv_*    device floats (sizes above), or NULL together with their q_*.
+ *   rows, cols  >= 0, multiples of 16, <= FP8LIN_MAX_DIM.
+ * Errors: a q_* without its inv_* (or the reverse), or no copy at all, is
+ * FP8LIN_ERR_INVALID_ARG; alignment and shape as for fp8lin_cast_transpose.
+ */
+fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                    float fmt_max, uint8_t *q_row, float *inv_row, uint8_t *q_col,
+                                    float *inv_col, uint8_t *q_tile, float *inv_tile,
+                                    cudaStream_t stream);
+
+/*
  * The three GEMMs with row-wise scales: C[p][q] = bf16_RN(acc[p][q] *
  * (inv_a[p] * inv_b[q])), inv_a one float per row of A and inv_b one per row
  * of B (16-byte aligned device vectors).  Operands, shapes and outputs as for

@@ -1,0 +1,57 @@
+"""Block scaling on the GPU against the oracle: the one-pass block cast
+(1 x 128, 128 x 1 and 128 x 128 blocks) with every FP8 byte and every
+inverse scale bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import Guarded, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+KINDS = {"row": (1, 128), "col": (128, 1), "tile": (128, 128)}
+
+
+def _blocks(rows, cols, kind):
+    br, bc = KINDS[kind]
+    return (rows + br - 1) // br, (cols + bc - 1) // bc
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (144, 272), (384, 1040), (1040, 384), (2048, 4096)])
+@pytest.mark.parametrize("fmt,dist", [(E4M3, ("normal", 1.0)), (E5M2, ("laplace", 1e-3))])
+@pytest.mark.parametrize("kinds", [("row", "col"), ("tile",), ("row",), ("col",), ("row", "col", "tile")])
+def test_block_cast_bit_exact(fp8lin, shape, fmt, dist, kinds):
+    rows, cols = shape
+    x = wl.generate(shape, *dist, seed=rows * 3 + cols, tensor_id=5, outlier_frac=1e-3)
+    xd = to_dev_bf16(x)
+    q, inv = {}, {}
+    for k in kinds:
+        q[k] = Guarded((rows, cols), torch.uint8)
+        inv[k] = Guarded(_blocks(rows, cols, k), torch.float32)
+    args = {}
+    for k in ("row", "col", "tile"):
+        args["q_" + k] = q[k].t if k in q else None
+        args["inv_" + k] = inv[k].t if k in inv else None
+    fp8lin.fp8lin_cast_blockwise(xd, fmt, **args)
+    torch.cuda.synchronize()
+    for k in kinds:
+        ref = oracle.quantize_blocks(x, fmt, *KINDS[k])
+        assert np.array_equal(inv[k].t.cpu().numpy().view(np.uint32), ref["inv_scale"].view(np.uint32)), k
+        assert np.array_equal(q[k].t.cpu().numpy(), ref["q"]), k
+        assert q[k].intact() and inv[k].intact(), k
+
+
+def test_block_cast_zero_tensor_and_arguments(fp8lin):
+    x = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
+    q = torch.full((128, 256), 0xFF, dtype=torch.uint8, device="cuda")
+    inv = torch.zeros((128, 2), dtype=torch.float32, device="cuda")
+    fp8lin.fp8lin_cast_blockwise(x, E4M3, q_row=q, inv_row=inv)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_blocks(np.zeros((128, 256), np.uint16), E4M3, 1, 128)
+    assert (q == 0).all() and np.array_equal(inv.cpu().numpy().view(np.uint32), ref["inv_scale"].view(np.uint32))
+    with pytest.raises(fp8lin.Fp8LinError):
+        fp8lin.fp8lin_cast_blockwise(x, E4M3, q_row=q)            # a copy without its scales
+    with pytest.raises(fp8lin.Fp8LinError):
+        fp8lin.fp8lin_cast_blockwise(x, E4M3)                     # nothing asked for
