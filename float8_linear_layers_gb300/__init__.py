@@ -44,7 +44,7 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
 ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_static",
                 "fp8lin_cast_transpose_delayed", "fp8lin_amax_rowcol", "fp8lin_cast_transpose_rowwise",
                 "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
-                "fp8lin_cast_blockwise",
+                "fp8lin_cast_blockwise", "fp8lin_fwd_block", "fp8lin_dgrad_block", "fp8lin_wgrad_block",
                 "fp8lin_fwd_rowwise", "fp8lin_dgrad_rowwise", "fp8lin_wgrad_rowwise",
                 "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
@@ -85,6 +85,9 @@ SIGNATURES = {
     "fp8lin_amax_rowcol": [_vp, _i64, _i64, _vp, _vp, _vp],
     "fp8lin_cast_transpose_rowwise": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_cast_blockwise": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_fwd_block": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_dgrad_block": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_wgrad_block": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_fwd_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_dgrad_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_wgrad_rowwise": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
@@ -247,6 +250,46 @@ def _gemm_call(name, a, sa, b, sb, c, M, N, K, stream):
     for t, n in ((a, "a"), (b, "b"), (sa, "inv_a"), (sb, "inv_b"), (c, "out")):
         _dev(t, n)
     _check(name, getattr(_lib, name)(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(c), M, N, K, _stream(stream)))
+
+
+def _blocks(n: int) -> int:
+    return (n + 127) // 128
+
+
+def _block_gemm(name, a, ia, b, ib, out, M, N, K, ia_shape, ib_shape, out_shape, stream):
+    for t, n in ((a, "a"), (b, "b"), (out, "out")):
+        _dev(t, n)
+    for t, n, shape in ((ia, "inv_a", ia_shape), (ib, "inv_b", ib_shape)):
+        _dev(t, n, torch.float32)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name}: {n} must be {shape}, got {tuple(t.shape)}")
+    if tuple(out.shape) != out_shape or out.dtype != torch.bfloat16:
+        raise ValueError(f"{name}: output must be bf16 {out_shape}")
+    _check(name, getattr(_lib, name)(_ptr(a), _ptr(ia), _ptr(b), _ptr(ib), _ptr(out), M, N, K, _stream(stream)))
+
+
+def fp8lin_fwd_block(xq, inv_x, wq, inv_w, y, stream=None) -> None:
+    """Y = sum_j (Xq . Wq^T)_j * inv_x[m][j] * inv_w[n/128][j]: Xq in 1 x 128 and Wq in 128 x 128 blocks."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _block_gemm("fp8lin_fwd_block", xq, inv_x, wq, inv_w, y, M, N, K, (M, _blocks(K)), (_blocks(N), _blocks(K)),
+                (M, N), stream)
+
+
+def fp8lin_dgrad_block(dyq, inv_dy, wq, inv_w, dx, stream=None) -> None:
+    """dX = sum_j (dYq . Wq)_j * inv_dy[m][j] * inv_w[j][k/128]: dYq in 1 x 128 and Wq in 128 x 128 blocks."""
+    M, N = dyq.shape
+    K = wq.shape[1]
+    _block_gemm("fp8lin_dgrad_block", dyq, inv_dy, wq, inv_w, dx, M, N, K, (M, _blocks(N)),
+                (_blocks(N), _blocks(K)), (M, K), stream)
+
+
+def fp8lin_wgrad_block(dyq, inv_dy, xq, inv_x, dw, stream=None) -> None:
+    """dW = sum_j (dYq^T . Xq)_j * inv_dy[j][n] * inv_x[j][k]: dYq and Xq in 128 x 1 blocks."""
+    M, N = dyq.shape
+    K = xq.shape[1]
+    _block_gemm("fp8lin_wgrad_block", dyq, inv_dy, xq, inv_x, dw, M, N, K, (_blocks(M), N), (_blocks(M), K),
+                (N, K), stream)
 
 
 def fp8lin_fwd_rowwise(xq, inv_x_rows, wq, inv_w_rows, y, stream=None) -> None:

@@ -251,6 +251,34 @@ __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mas
         : "memory");
 }
 
+// Single-CTA forms (the block-scaled kernel): TMA completing on this CTA's
+// barrier, MMA of one SM's tensor core, commit to this CTA's barrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_f8f6f4_single(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_single(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -562,6 +590,270 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     }
 }
 
+// ------------------------------------------------- block-scaled kernel
+
+// Block scaling along the contraction: C[p][q] = sum over 128-long
+// contraction blocks j of (sum_{k in j} A[p][k] B[q][k])_fp32 * ia(p, j) * ib(q, j),
+// with ia(p, j) = inv_a[p * sa_p + j * sa_r] and ib(q, j) = inv_b[(q / 128) *
+// sb_q + j * sb_r], or inv_b[q * sb_q + j * sb_r] when B_COLS (one scale per
+// row of B, i.e. per output column).
+//
+// One CTA per SM, persistent over 128 x 128 output tiles, 192 threads:
+//   warp 0      TMA producer: 128 x 128-byte A and B slabs (one contraction
+//               block each) into a 6-stage ring;
+//   warp 1      allocates 256 TMEM columns (two 128 x 128 fp32 partial
+//               buffers); one thread issues the four tcgen05.mma (M 128,
+//               N 128, K 32) of a contraction block into a fresh partial
+//               buffer and commits it;
+//   warps 2..5  promotion: read the block's partial sums from TMEM (32 rows
+//               x 32 columns at a time), multiply by ia * ib and add them to
+//               fp32 accumulators held in registers (32 rows x 128 columns
+//               per warp), hand the buffer back; after the last block, round
+//               to bf16 and TMA-store as the per-tensor epilogue does.
+// The two partial buffers let the MMAs of block j + 1 run while block j is
+// promoted.
+constexpr int kBlkTile = 128;                         // output rows and columns per tile; contraction block
+constexpr int kBlkStages = 6;
+constexpr int kBlkSlab = kBlkTile * kBK;              // 16 KB per operand and stage
+constexpr int kBlkThreads = 192;
+constexpr int kBlkTmemCols = 2 * kBlkTile;
+constexpr int kBlkEpiBytes = 4 * kEpiBuf;
+constexpr int kBlkSmemBytes = kBlkStages * 2 * kBlkSlab + kBlkEpiBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+static_assert(kBlkSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
+
+template <bool A_MN, bool B_MN, bool B_COLS>
+__global__ void __launch_bounds__(kBlkThreads, 1)
+fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                      const __grid_constant__ CUtensorMap map_c, int P, int Q, int R,
+                      const float *__restrict__ inv_a, long long sa_p, long long sa_r,
+                      const float *__restrict__ inv_b, long long sb_q, long long sb_r, uint32_t idesc,
+                      TileMap tiles) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + kBlkStages * kBlkSlab;
+    uint8_t *sC = sB + kBlkStages * kBlkSlab;           // epilogue staging: [4 warps][32 rows x 64 B]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kBlkEpiBytes);
+    uint64_t *full = bars;                              // [stages] slab landed
+    uint64_t *empty = bars + kBlkStages;                // [stages] MMAs done with the slab
+    uint64_t *pfull = bars + 2 * kBlkStages;            // [2] partial sums of a block ready
+    uint64_t *pempty = pfull + 2;                       // [2] the four promotion warps have read them
+    uint64_t *mma_done = pempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBlkStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&pfull[b]), 1);
+            mbar_init(smem_u32(&pempty[b]), 4);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
+        prefetch_tensormap(&map_c);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kBlkTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = tiles.tiles_m * tiles.tiles_n;
+    const int num_kb = (R + kBK - 1) / kBK;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;
+            for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+                int tm, tn;
+                tiles.coords(t, tm, tn);
+                const int a_row = tm * kBlkTile, b_row = tn * kBlkTile;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, 2 * kBlkSlab);
+                    if (A_MN) tma_load_2d(smem_u32(sA + stage * kBlkSlab), &map_a, fb, a_row, kb * kBK);
+                    else      tma_load_2d(smem_u32(sA + stage * kBlkSlab), &map_a, fb, kb * kBK, a_row);
+                    if (B_MN) tma_load_2d(smem_u32(sB + stage * kBlkSlab), &map_b, fb, b_row, kb * kBK);
+                    else      tma_load_2d(smem_u32(sB + stage * kBlkSlab), &map_b, fb, kb * kBK, b_row);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kBlkStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // let every copy land before the CTA exits
+                for (int s = 0; s < kBlkStages; ++s)
+                    if (armed & (1u << s))
+                        mbar_wait(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int pb = 0;
+            uint32_t pphase = 0;
+            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok && !*abort_flag; t += gridDim.x) {
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&pempty[pb]), pphase ^ 1u, abort_flag, kWaitLimitNs) ||
+                        !mbar_wait(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kBlkSlab >> 4));
+                    const uint64_t b_desc = b_desc0 + (uint64_t)(stage * (kBlkSlab >> 4));
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(pb * kBlkTile);
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k)
+                        umma_f8f6f4_single(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc,
+                                           k != 0 ? 1u : 0u);
+                    umma_commit_single(smem_u32(&empty[stage]));
+                    umma_commit_single(smem_u32(&pfull[pb]));
+                    if (++stage == kBlkStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (++pb == 2) {
+                        pb = 0;
+                        pphase ^= 1u;
+                    }
+                }
+            }
+            umma_commit_single(smem_u32(mma_done));
+            volatile int no_abort = 0;
+            mbar_wait(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
+        }
+    } else {
+        // ------------------------------------------------ promotion + epilogue
+        const int sub = warp % 4;  // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows of the tile
+        uint8_t *stage_c = sC + (warp - 2) * kEpiBuf;
+        uint8_t *dst = stage_c + lane * (kEpiCols * 2);
+        int pb = 0;
+        uint32_t pphase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tiles.coords(t, tm, tn);
+            const int row0 = tm * kBlkTile + sub * 32;
+            const int row = row0 + lane;
+            float acc[kBlkTile];
+#pragma unroll
+            for (int j = 0; j < kBlkTile; ++j) acc[j] = 0.0f;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const float sa = row < P ? __ldg(inv_a + row * sa_p + kb * sa_r) : 0.0f;
+                const float sb_tile = B_COLS ? 0.0f : __ldg(inv_b + (long long)tn * sb_q + kb * sb_r);
+                const bool ready = mbar_wait(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs);
+                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(pb * kBlkTile);
+#pragma unroll
+                for (int c = 0; c < kBlkTile / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
+                    float s[32];
+                    if (B_COLS) {
+                        // one scale per output column: the same 32 floats for every lane
+                        const int col0 = tn * kBlkTile + c * 32;
+                        const float *bp = inv_b + (long long)col0 * sb_q + kb * sb_r;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const float4 b4 = (col0 + 4 * g < Q) ? __ldg(reinterpret_cast<const float4 *>(bp) + g)
+                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                            s[4 * g + 0] = __fmul_rn(sa, b4.x);
+                            s[4 * g + 1] = __fmul_rn(sa, b4.y);
+                            s[4 * g + 2] = __fmul_rn(sa, b4.z);
+                            s[4 * g + 3] = __fmul_rn(sa, b4.w);
+                        }
+                    } else {
+                        const float st = __fmul_rn(sa, sb_tile);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s[j] = st;
+                    }
+                    tmem_ld_wait();
+                    if (c == kBlkTile / 32 - 1) {
+                        // the whole partial buffer is in registers: hand it back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_local(smem_u32(&pempty[pb]));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(__uint_as_float(r[j]), s[j], acc[c * 32 + j]);
+                }
+                if (++pb == 2) {
+                    pb = 0;
+                    pphase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            // epilogue: round to bf16, stage 32 columns at a time, TMA-store
+#pragma unroll
+            for (int c = 0; c < kBlkTile / kEpiCols; ++c) {
+                const int col0 = tn * kBlkTile + c * kEpiCols;
+                if (lane == 0) bulk_wait_read_0();
+                __syncwarp();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int j = c * kEpiCols + 8 * g;
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
+                    o.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+                    o.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+                    o.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+                    *reinterpret_cast<uint4 *>(dst + ((g ^ ((lane >> 1) & 3)) << 4)) = o;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0 && row0 < P && col0 < Q) {
+                    tma_store_2d(&map_c, smem_u32(stage_c), col0, row0);
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kBlkTmemCols)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -628,16 +920,17 @@ bool make_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: fp32 accumulator
 // (bits 4..5 = 1), A / B formats (bits 7..9 / 10..12: 0 = e4m3, 1 = e5m2),
 // A / B majorness (bits 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 at bits
-// 17..22, M >> 4 at bits 24..28; M and N are the pair's (256 x 256).
-uint32_t make_idesc(fp8lin_fmt fa, fp8lin_fmt fb, bool a_mn, bool b_mn) {
+// 17..22, M >> 4 at bits 24..28; M and N are the pair's (256 x 256), or the
+// single CTA's (128 x 128) for the block-scaled kernel.
+uint32_t make_idesc(fp8lin_fmt fa, fp8lin_fmt fb, bool a_mn, bool b_mn, int m = kPairM, int n = kPairN) {
     uint32_t d = 0;
     d |= 1u << 4;
     d |= (uint32_t)fa << 7;
     d |= (uint32_t)fb << 10;
     d |= (uint32_t)a_mn << 15;
     d |= (uint32_t)b_mn << 16;
-    d |= (uint32_t)(kPairN >> 3) << 17;
-    d |= (uint32_t)(kPairM >> 4) << 24;
+    d |= (uint32_t)(n >> 3) << 17;
+    d |= (uint32_t)(m >> 4) << 24;
     return d;
 }
 
@@ -666,13 +959,41 @@ cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttrib
     return cfg;
 }
 
-template <bool VEC, bool A_MN, bool B_MN>
-fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const uint8_t *B, fp8lin_fmt fb,
-                      const float *inv_b, void *C, int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
+// Raster: keep the smaller operand resident in L2 and stream the larger one
+// once.  If neither fits, the tiles running at once move through the
+// contraction together, so L2 only has to hold their current slabs: group
+// kWaveGroup tiles along one axis (a wave covers a compact block of tiles,
+// each panel read once per group), choosing the orientation with the fewest
+// modelled DRAM bytes.
+TileMap raster(int64_t P, int64_t Q, int64_t R, int64_t tiles_m, int64_t tiles_n) {
+    const int64_t bytes_a = P * R, bytes_b = Q * R;
+    TileMap tm{(int)tiles_m, (int)tiles_n, 1, 0};
+    if (bytes_a <= kL2Resident && bytes_a <= bytes_b) {
+        tm.group = (int)tiles_m;                      // all of A per column of tiles
+    } else if (bytes_b <= kL2Resident) {
+        tm.group = (int)tiles_n;                      // all of B per row of tiles
+        tm.swap = 1;
+    } else {
+        const int64_t g = kWaveGroup;
+        const int64_t gm = g < tiles_m ? g : tiles_m, gn = g < tiles_n ? g : tiles_n;
+        const int64_t traffic_m = bytes_a + bytes_b * ((tiles_m + gm - 1) / gm);   // A panels held
+        const int64_t traffic_n = bytes_b + bytes_a * ((tiles_n + gn - 1) / gn);   // B panels held
+        if (traffic_n < traffic_m) {
+            tm.group = (int)gn;
+            tm.swap = 1;
+        } else {
+            tm.group = (int)gm;
+        }
+    }
+    return tm;
+}
+
+// Checks shared by every GEMM entry point.
+fp8lin_status gemm_checks(const uint8_t *A, const float *inv_a, const uint8_t *B, const float *inv_b, void *C,
+                          int64_t P, int64_t Q, int64_t R) {
     using namespace fp8lin;
     if (inv_a == nullptr || inv_b == nullptr) return FP8LIN_ERR_INVALID_ARG;
     if (P < 0 || Q < 0 || R < 0) return FP8LIN_ERR_INVALID_ARG;
-    if (VEC && (!aligned(inv_a, 16) || !aligned(inv_b, 16))) return FP8LIN_ERR_MISALIGNED;
     const bool empty_out = P == 0 || Q == 0;
     if (!empty_out && C == nullptr) return FP8LIN_ERR_INVALID_ARG;
     if (!empty_out && R > 0 && (A == nullptr || B == nullptr)) return FP8LIN_ERR_INVALID_ARG;
@@ -680,8 +1001,19 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return FP8LIN_ERR_MISALIGNED;
     if (!dim_ok(P) || !dim_ok(Q) || !dim_ok(R) || P % 16 || Q % 16 || R % 16)
         return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    return FP8LIN_OK;
+}
+
+template <bool VEC, bool A_MN, bool B_MN>
+fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const uint8_t *B, fp8lin_fmt fb,
+                      const float *inv_b, void *C, int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
+    using namespace fp8lin;
+    fp8lin_status st = gemm_checks(A, inv_a, B, inv_b, C, P, Q, R);
+    if (st != FP8LIN_OK) return st;
+    if (VEC && (!aligned(inv_a, 16) || !aligned(inv_b, 16))) return FP8LIN_ERR_MISALIGNED;
+    const bool empty_out = P == 0 || Q == 0;
     DeviceInfo dev;
-    fp8lin_status st = current_device(&dev);
+    st = current_device(&dev);
     if (st != FP8LIN_OK) return st;
     if (empty_out) return FP8LIN_OK;
     if (R == 0) {  // empty contraction: C = 0
@@ -716,31 +1048,7 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
         g_smem_attr_set[instance<VEC, A_MN, B_MN>()][dev.device].store(true, std::memory_order_release);
     }
 
-    // Raster: keep the smaller operand resident in L2 and stream the larger
-    // one once.  If neither fits, the ~76 pairs running at once move through
-    // the contraction together, so L2 only has to hold their current slabs:
-    // group kWaveGroup tiles along one axis (a wave covers a compact block of
-    // tiles, each panel read once per group), choosing the orientation with
-    // the fewest modelled DRAM bytes.
-    const int64_t bytes_a = P * R, bytes_b = Q * R;
-    TileMap tm{(int)tiles_m, (int)tiles_n, 1, 0};
-    if (bytes_a <= kL2Resident && bytes_a <= bytes_b) {
-        tm.group = (int)tiles_m;                      // all of A per column of tiles
-    } else if (bytes_b <= kL2Resident) {
-        tm.group = (int)tiles_n;                      // all of B per row of tiles
-        tm.swap = 1;
-    } else {
-        const int64_t g = kWaveGroup;
-        const int64_t gm = g < tiles_m ? g : tiles_m, gn = g < tiles_n ? g : tiles_n;
-        const int64_t traffic_m = bytes_a + bytes_b * ((tiles_m + gm - 1) / gm);   // A panels held
-        const int64_t traffic_n = bytes_b + bytes_a * ((tiles_n + gn - 1) / gn);   // B panels held
-        if (traffic_n < traffic_m) {
-            tm.group = (int)gn;
-            tm.swap = 1;
-        } else {
-            tm.group = (int)gm;
-        }
-    }
+    const TileMap tm = raster(P, Q, R, tiles_m, tiles_n);
     const int num_tiles = (int)(tiles_m * tiles_n);
     const int max_pairs = g_max_clusters[instance<VEC, A_MN, B_MN>()][dev.device].load(std::memory_order_relaxed);
     const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
@@ -755,7 +1063,94 @@ fp8lin_status gemm_tn(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, const
     return check_launch();
 }
 
+std::atomic<bool> g_blk_attr_set[8][64];
+std::atomic<int> g_blk_ctas[8][64];
+
+// The block-scaled GEMM (see fp8_gemm_block_kernel): inverse scales of A at
+// inv_a[p * sa_p + j * sa_r], of B at inv_b[(q / 128) * sb_q + j * sb_r] (or
+// [q * sb_q + j * sb_r] when B_COLS); sizes are the caller's to guarantee.
+template <bool A_MN, bool B_MN, bool B_COLS>
+fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, int64_t sa_p, int64_t sa_r,
+                         const uint8_t *B, fp8lin_fmt fb, const float *inv_b, int64_t sb_q, int64_t sb_r, void *C,
+                         int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
+    using namespace fp8lin;
+    fp8lin_status st = gemm_checks(A, inv_a, B, inv_b, C, P, Q, R);
+    if (st != FP8LIN_OK) return st;
+    if (B_COLS && !aligned(inv_b, 16)) return FP8LIN_ERR_MISALIGNED;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    if (P == 0 || Q == 0) return FP8LIN_OK;
+    if (R == 0) {
+        return cudaMemsetAsync(C, 0, (size_t)P * (size_t)Q * 2, stream) == cudaSuccess ? FP8LIN_OK
+                                                                                       : FP8LIN_ERR_CUDA;
+    }
+    const int64_t tiles_m = (P + kBlkTile - 1) / kBlkTile, tiles_n = (Q + kBlkTile - 1) / kBlkTile;
+    if (tiles_m * tiles_n > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    CUtensorMap map_a, map_b, map_c;
+    const bool ok_a = A_MN ? make_operand_map_mn(&map_a, A, P, R, kBlkTile) : make_operand_map(&map_a, A, P, R, kBlkTile);
+    const bool ok_b = B_MN ? make_operand_map_mn(&map_b, B, Q, R, kBlkTile) : make_operand_map(&map_b, B, Q, R, kBlkTile);
+    if (!ok_a || !ok_b || !make_output_map(&map_c, C, P, Q)) return FP8LIN_ERR_CUDA;
+    if (dev.device >= 64) return FP8LIN_ERR_CUDA;
+    constexpr int inst = A_MN * 4 + B_MN * 2 + B_COLS;
+    auto kernel = fp8_gemm_block_kernel<A_MN, B_MN, B_COLS>;
+    if (!g_blk_attr_set[inst][dev.device].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBlkSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return FP8LIN_ERR_CUDA;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlkThreads, kBlkSmemBytes) !=
+                cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        g_blk_ctas[inst][dev.device].store(per_sm * dev.sm_count, std::memory_order_relaxed);
+        g_blk_attr_set[inst][dev.device].store(true, std::memory_order_release);
+    }
+    const TileMap tm = raster(P, Q, R, tiles_m, tiles_n);
+    const int num_tiles = (int)(tiles_m * tiles_n);
+    const int max_ctas = g_blk_ctas[inst][dev.device].load(std::memory_order_relaxed);
+    const int grid = num_tiles < max_ctas ? num_tiles : max_ctas;
+    const uint32_t idesc = make_idesc(fa, fb, A_MN, B_MN, kBlkTile, kBlkTile);
+    kernel<<<grid, kBlkThreads, kBlkSmemBytes, stream>>>(map_a, map_b, map_c, (int)P, (int)Q, (int)R, inv_a,
+                                                         (long long)sa_p, (long long)sa_r, inv_b, (long long)sb_q,
+                                                         (long long)sb_r, idesc, tm);
+    return check_launch();
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 }  // namespace
+
+// Block scaling: X and dY in 1 x 128 / 128 x 1 blocks, W in 128 x 128 blocks
+// (fp8lin_cast_blockwise); the GEMM scales each 128-long contraction block.
+extern "C" fp8lin_status fp8lin_fwd_block(const uint8_t *xq, const float *inv_x, const uint8_t *wq,
+                                          const float *inv_w, void *y, int64_t M, int64_t N, int64_t K,
+                                          cudaStream_t stream) {
+    // A = Xq (row blocks, inv_x [M x KB]), B = Wq (tiles, inv_w [NB x KB]); contraction K
+    const int64_t kb = ceil_div(K, kBlkTile);
+    return gemm_block<false, false, false>(xq, FP8LIN_E4M3, inv_x, kb, 1, wq, FP8LIN_E4M3, inv_w, kb, 1, y, M, N,
+                                           K, stream);
+}
+
+extern "C" fp8lin_status fp8lin_dgrad_block(const uint8_t *dyq, const float *inv_dy, const uint8_t *wq,
+                                            const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
+                                            cudaStream_t stream) {
+    // A = dYq (row blocks, inv_dy [M x NB]), B = Wq read MN-major: row k of B,
+    // contraction block j scaled by inv_w[j][k / 128]; contraction N
+    const int64_t nb = ceil_div(N, kBlkTile), kb = ceil_div(K, kBlkTile);
+    return gemm_block<false, true, false>(dyq, FP8LIN_E5M2, inv_dy, nb, 1, wq, FP8LIN_E4M3, inv_w, 1, kb, dx, M, K,
+                                          N, stream);
+}
+
+extern "C" fp8lin_status fp8lin_wgrad_block(const uint8_t *dyq, const float *inv_dy, const uint8_t *xq,
+                                            const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
+                                            cudaStream_t stream) {
+    // A = dYq read MN-major (column blocks: row n of A, block j at inv_dy[j][n]),
+    // B = Xq read MN-major (column blocks: row k of B, block j at inv_x[j][k]); contraction M
+    return gemm_block<true, true, true>(dyq, FP8LIN_E5M2, inv_dy, 1, N, xq, FP8LIN_E4M3, inv_x, 1, K, dw, N, K, M,
+                                        stream);
+}
 
 extern "C" fp8lin_status fp8lin_fwd(const uint8_t *xq, const float *inv_x, const uint8_t *wq, const float *inv_w,
                                     void *y, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {

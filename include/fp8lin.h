@@ -305,6 +305,38 @@ fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int64_t cols, f
                                     cudaStream_t stream);
 
 /*
+ * The three GEMMs of a block-scaled linear (copies from
+ * fp8lin_cast_blockwise).  The contraction is cut into blocks of 128; the
+ * tensor cores sum each block in fp32, the partial sum is multiplied by the
+ * two operands' inverse scales for that block (fp32) and added to an fp32
+ * total, which is rounded to bf16 (round to nearest even) at the end:
+ *   fwd  : Y [M x N]  = sum_j (Xq Wq^T)_j  * inv_x[m][j]  * inv_w[n/128][j]   contraction K
+ *   dgrad: dX [M x K] = sum_j (dYq Wq)_j   * inv_dy[m][j] * inv_w[j][k/128]   contraction N
+ *   wgrad: dW [N x K] = sum_j (dYq^T Xq)_j * inv_dy[j][n] * inv_x[j][k]       contraction M
+ * (Lecture 9 exercises: FP8 scaling per tensor or per block; TorchTitan
+ * analysis page, section 3.3: the Float8 linear's three GEMMs.)
+ *
+ * fp8lin_fwd_block:   xq = q_row of X [M x K] e4m3, inv_x [M x ceil(K/128)];
+ *                     wq = q_tile of W [N x K] e4m3, inv_w [ceil(N/128) x ceil(K/128)].
+ * fp8lin_dgrad_block: dyq = q_row of dY [M x N] e5m2, inv_dy [M x ceil(N/128)];
+ *                     wq, inv_w as for the forward.
+ * fp8lin_wgrad_block: dyq = q_col of dY [M x N] e5m2, inv_dy [ceil(M/128) x N];
+ *                     xq = q_col of X [M x K] e4m3, inv_x [ceil(M/128) x K]
+ *                     (16-byte aligned).
+ * Outputs bf16 row-major, 16-byte aligned, fully overwritten.  Pointers,
+ * shapes and errors otherwise as for fp8lin_fwd.
+ */
+fp8lin_status fp8lin_fwd_block(const uint8_t *xq, const float *inv_x, const uint8_t *wq,
+                               const float *inv_w, void *y, int64_t M, int64_t N, int64_t K,
+                               cudaStream_t stream);
+fp8lin_status fp8lin_dgrad_block(const uint8_t *dyq, const float *inv_dy, const uint8_t *wq,
+                                 const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
+                                 cudaStream_t stream);
+fp8lin_status fp8lin_wgrad_block(const uint8_t *dyq, const float *inv_dy, const uint8_t *xq,
+                                 const float *inv_x, void *dw, int64_t M, int64_t N, int64_t K,
+                                 cudaStream_t stream);
+
+/*
  * The three GEMMs with row-wise scales: C[p][q] = bf16_RN(acc[p][q] *
  * (inv_a[p] * inv_b[q])), inv_a one float per row of A and inv_b one per row
  * of B (16-byte aligned device vectors).  Operands, shapes and outputs as for

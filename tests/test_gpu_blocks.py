@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_helpers import Guarded, to_dev_bf16
+from gpu_helpers import Guarded, assert_gemm_close, bf16_to_f64, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 E4M3, E5M2 = oracle.E4M3, oracle.E5M2
@@ -55,3 +55,33 @@ def test_block_cast_zero_tensor_and_arguments(fp8lin):
         fp8lin.fp8lin_cast_blockwise(x, E4M3, q_row=q)            # a copy without its scales
     with pytest.raises(fp8lin.Fp8LinError):
         fp8lin.fp8lin_cast_blockwise(x, E4M3)                     # nothing asked for
+
+
+GEMM_SHAPES = [(128, 128, 128), (144, 272, 208), (384, 1040, 4112), (1040, 400, 96), (2048, 2048, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("which", ["fwd", "dgrad", "wgrad"])
+def test_block_gemm_matches_oracle(fp8lin, M, N, K, which):
+    X = wl.generate((M, K), "normal", 1.0, M + 1, wl.X, outlier_frac=1e-3)
+    W = wl.generate((N, K), "normal", 0.02, N + 2, wl.W)
+    dY = wl.generate((M, N), "laplace", 1e-3, K + 3, wl.DY)
+    r = oracle.quantize_block_recipe(X, W, dY)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    if which == "fwd":
+        out, args = Guarded((M, N), torch.bfloat16), (r["x_k"], r["w"])
+        ref = oracle.fwd_block_ref(r["x_k"]["q"], r["x_k"]["inv_scale"], r["w"]["q"], r["w"]["inv_scale"])
+    elif which == "dgrad":
+        out, args = Guarded((M, K), torch.bfloat16), (r["dy_n"], r["w"])
+        ref = oracle.dgrad_block_ref(r["dy_n"]["q"], r["dy_n"]["inv_scale"], r["w"]["q"], r["w"]["inv_scale"])
+    else:
+        out, args = Guarded((N, K), torch.bfloat16), (r["dy_m"], r["x_m"])
+        ref = oracle.wgrad_block_ref(r["dy_m"]["q"], r["dy_m"]["inv_scale"], r["x_m"]["q"], r["x_m"]["inv_scale"])
+    out.t.fill_(float("nan"))
+    a, b = args
+    getattr(fp8lin, f"fp8lin_{which}_block")(dev(a["q"]), dev(a["inv_scale"]), dev(b["q"]), dev(b["inv_scale"]),
+                                             out.t)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    assert_gemm_close(bf16_to_f64(out.t), ref, f"{which} block {M}x{N}x{K}")
+    assert out.intact()
