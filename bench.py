@@ -129,17 +129,22 @@ def spec_flops(spec: Spec) -> int:
     return sum(wl.WORKLOADS[l.workload].flops for l in spec.linears)
 
 
-def cast_elem_bytes(scaling: str, transpose: bool) -> int:
+def cast_elem_bytes(scaling: str, transpose: bool, weight: bool = False) -> int:
     """HBM bytes per cast element in one step: the cast reads x (2 B) and
     writes one FP8 copy, or two with the transposed copy (always for
-    row-wise scaling); dynamic and row-wise scaling read x once more for the
-    amax pass, delayed and static do not."""
+    row-wise scaling; for block scaling, activations and gradients get a
+    row-block and a column-block copy, weights one 128 x 128-block copy);
+    dynamic and row-wise scaling read x once more for the amax pass, delayed,
+    static and block scaling do not."""
+    if scaling == "block":
+        return 2 + (1 if weight else 2)
     two_copies = transpose or scaling == "rowwise"
     return 2 + 1 + (1 if two_copies else 0) + (2 if scaling in ("dynamic", "rowwise") else 0)
 
 
 def cast_bytes(spec: Spec, scaling: str, transpose: bool = False) -> int:
-    return sum(r * c for (r, c, *_) in cast_inputs(spec).values()) * cast_elem_bytes(scaling, transpose)
+    return sum(r * c * cast_elem_bytes(scaling, transpose, key.startswith("w:"))
+               for key, (r, c, *_) in cast_inputs(spec).items())
 
 
 def attainable(spec: Spec, scaling: str, peak_tflops: float, hbm_gbs: float, transpose: bool = False) -> dict:
@@ -185,7 +190,7 @@ def gemm_traffic(workload: str, scaling: str):
     """Mean DRAM bytes per GEMM launch of one step of `workload`, from the
     committed ncu capture of the per-tensor-scale GEMM; None when the GEMM
     source changed since the counters were taken, no capture covers this
-    workload, or the step runs the row-wise-scale GEMM instead."""
+    workload, or the step runs the row-wise- or block-scaled GEMM instead."""
     import hashlib
     try:
         with open(TRAFFIC_FILE) as f:
@@ -194,7 +199,7 @@ def gemm_traffic(workload: str, scaling: str):
             sha = hashlib.sha256(f.read()).hexdigest()
     except (OSError, ValueError):
         return None
-    if t.get("gemm_cu_sha256") != sha or t.get("workload") != workload or scaling == "rowwise":
+    if t.get("gemm_cu_sha256") != sha or t.get("workload") != workload or scaling in ("rowwise", "block"):
         return None
     return int(t["mean_dram_bytes_per_launch"])
 
@@ -383,13 +388,18 @@ class StepGraph:
         self.fl, self.t, self.spec = fl, torch, spec
         self.overlap, self.scaling = overlap, scaling
         # one FP8 copy per tensor (backward GEMMs read it MN-major) unless the
-        # transposed copies are asked for; row-wise scaling always needs them
-        self.transpose = transpose or scaling == "rowwise"
+        # transposed copies are asked for; row-wise scaling always needs them,
+        # block scaling never writes them
+        self.transpose = (transpose or scaling == "rowwise") and scaling != "block"
         self.inp = dev_in
         self.lin = {l.name: l for l in spec.linears}
         self.t8 = {}
         for key, (rows, cols, fmt, *_) in cast_inputs(spec).items():
-            self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=self.transpose)
+            if scaling == "block":   # weights in 128 x 128 blocks, activations and gradients in row / column blocks
+                self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=False,
+                                               blocks="tile" if key.startswith("w:") else "rowcol")
+            else:
+                self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=self.transpose)
         bf = torch.bfloat16
         self.out = {}
         for l in spec.linears:
@@ -405,7 +415,7 @@ class StepGraph:
         else:
             self.main = self.side = torch.cuda.current_stream(dev)
         self._plan()
-        per_cast = 2 if scaling in ("dynamic", "rowwise") else 1
+        per_cast = 2 if scaling in ("dynamic", "rowwise") else 1   # block and delayed: one kernel per cast
         self.kernels_per_step = per_cast * len(self.t8) + len(spec.gemms)
 
     def _plan(self):
@@ -439,8 +449,11 @@ class StepGraph:
     def _cast(self, rec, key, stream):
         fl, x, t8 = self.fl, self.inp[key], self.t8[key]
         n = x.numel()
-        cast_bytes = (4 if t8.qT is not None else 3) * n   # read bf16, write one or two FP8 copies
-        if t8.scaling == "rowwise":
+        two_copies = t8.qT is not None or getattr(t8, "blocks", None) == "rowcol"
+        cast_bytes = (4 if two_copies else 3) * n   # read bf16, write one or two FP8 copies
+        if t8.scaling == "block":
+            self._mark(stream, rec, "cast", key, cast_bytes, lambda: t8.quantize(x, stream))
+        elif t8.scaling == "rowwise":
             self._mark(stream, rec, "amax", key, 2 * n,
                        lambda: fl.fp8lin_amax_rowcol(x, t8.row_amax, t8.col_amax, stream))
             self._mark(stream, rec, "cast", key, cast_bytes, lambda: fl.fp8lin_cast_transpose_rowwise(
@@ -458,7 +471,11 @@ class StepGraph:
         w = wl.WORKLOADS[l.workload]
         x8, w8, d8 = self.t8[l.x], self.t8["w:" + name], self.t8["dy:" + name]
         out = self.out[name][which]
-        if self.scaling == "rowwise":
+        if self.scaling == "block":
+            fn = {"fwd": lambda: fl.fp8lin_fwd_block(x8.q, x8.row_inv, w8.q, w8.tile_inv, out, m),
+                  "dgrad": lambda: fl.fp8lin_dgrad_block(d8.q, d8.row_inv, w8.q, w8.tile_inv, out, m),
+                  "wgrad": lambda: fl.fp8lin_wgrad_block(d8.qc, d8.col_inv, x8.qc, x8.col_inv, out, m)}[which]
+        elif self.scaling == "rowwise":
             fn = {"fwd": lambda: fl.fp8lin_fwd_rowwise(x8.q, x8.row_inv, w8.q, w8.row_inv, out, m),
                   "dgrad": lambda: fl.fp8lin_dgrad_rowwise(d8.q, d8.row_inv, w8.qT, w8.col_inv, out, m),
                   "wgrad": lambda: fl.fp8lin_wgrad_rowwise(d8.qT, d8.col_inv, x8.qT, x8.col_inv, out, m)}[which]
@@ -736,7 +753,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sustained,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
                      "traffic": gemm_traffic(args.workload, args.scaling),
-                     "kernel": "fp8_gemm_tn_kernel, every launch of the timed region: mean 2*M*N*K flop per "
+                     "kernel": ("fp8_gemm_block_kernel" if args.scaling == "block" else "fp8_gemm_tn_kernel") +
+                               ", every launch of the timed region: mean 2*M*N*K flop per "
                                "launch / mean event-timed launch duration (launches run beside the side-stream "
                                "casts); traffic = mean DRAM bytes per GEMM launch of one step (ncu)",
                      "peak_source": f"{peak_src} sustained bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)",
@@ -780,7 +798,8 @@ def run_profile_case(args) -> None:
     need_x = case in ("gemm_fwd", "gemm_wgrad", "gemm_wgrad_mn")
     need_w = case in ("gemm_fwd", "gemm_dgrad", "gemm_dgrad_mn")
     need_dy = case in ("gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn", "gemm_wgrad_mn", "amax", "cast", "cast_q",
-                       "amax_rowcol", "cast_rowwise")  # dY: 235 MB > L2
+                       "amax_rowcol", "cast_rowwise", "gemm_fwd_block", "gemm_dgrad_block", "gemm_wgrad_block",
+                       "cast_block")  # dY: 235 MB > L2
     x8 = w8 = d8 = None
     if need_x:
         x = up(w.make_x())
@@ -804,6 +823,29 @@ def run_profile_case(args) -> None:
         out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
         launch = lambda: fl.fp8lin_wgrad(d8.qT, d8.inv_scale, x8.qT, x8.inv_scale, out)
         work, unit = 2 * w.M * w.N * w.K, "flop"
+    elif case in ("gemm_fwd_block", "gemm_dgrad_block", "gemm_wgrad_block", "cast_block"):
+        xb = fl.Float8Tensor(w.M, w.K, fl.E4M3, dev, scaling="block", blocks="rowcol")
+        wb = fl.Float8Tensor(w.N, w.K, fl.E4M3, dev, scaling="block", blocks="tile")
+        db = fl.Float8Tensor(w.M, w.N, fl.E5M2, dev, scaling="block", blocks="rowcol")
+        if case != "cast_block":
+            xb.quantize(up(w.make_x()))
+            wb.quantize(up(w.make_w()))
+        db.quantize(dy)
+        torch.cuda.synchronize()
+        if case == "gemm_fwd_block":
+            out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+            launch = lambda: fl.fp8lin_fwd_block(xb.q, xb.row_inv, wb.q, wb.tile_inv, out)
+        elif case == "gemm_dgrad_block":
+            out = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
+            launch = lambda: fl.fp8lin_dgrad_block(db.q, db.row_inv, wb.q, wb.tile_inv, out)
+        elif case == "gemm_wgrad_block":
+            out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+            launch = lambda: fl.fp8lin_wgrad_block(db.qc, db.col_inv, xb.qc, xb.col_inv, out)
+        if case == "cast_block":
+            launch = lambda: db.quantize(dy)
+            work, unit = 4 * w.M * w.N, "byte"
+        else:
+            work, unit = 2 * w.M * w.N * w.K, "flop"
     elif case == "gemm_dgrad_mn":
         out = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
         launch = lambda: fl.fp8lin_dgrad_mn(d8.q, d8.inv_scale, w8.q, w8.inv_scale, out)
@@ -854,7 +896,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(SPECS), default="ffn8b")
-    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise"], default="dynamic",
+    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise", "block"], default="dynamic",
                     help="scaling recipe (the headline metric is dynamic per-tensor)")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
     ap.add_argument("--transpose", action="store_true",
@@ -867,8 +909,9 @@ def main():
     ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn",
-                                               "gemm_wgrad_mn", "amax", "cast", "cast_q", "amax_rowcol",
-                                               "cast_rowwise"],
+                                               "gemm_wgrad_mn", "gemm_fwd_block", "gemm_dgrad_block",
+                                               "gemm_wgrad_block", "amax", "cast", "cast_q", "cast_block",
+                                               "amax_rowcol", "cast_rowwise"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least three warm-up steps

@@ -398,12 +398,33 @@ class Float8Tensor:
               "static":  a fixed scale set with ``set_scale``;
               "rowwise": one scale per row of q and per row of qT (per
                          column of the source): per-block scaling with
-                         blocks that do not cross the GEMM contraction."""
+                         blocks that do not cross the GEMM contraction;
+              "block":   blocks of 128 along the contraction, one pass with
+                         no amax call: ``blocks="rowcol"`` (activations,
+                         gradients) gives q in 1 x 128 blocks (row_inv
+                         [rows x ceil(cols/128)]) and qc in 128 x 1 blocks
+                         (col_inv [ceil(rows/128) x cols]); ``blocks="tile"``
+                         (weights) gives q in 128 x 128 blocks (tile_inv)."""
 
     def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX,
-                 scaling: str = "dynamic", history_len: int = 16, transpose: bool = True):
-        if scaling not in ("dynamic", "delayed", "static", "rowwise"):
+                 scaling: str = "dynamic", history_len: int = 16, transpose: bool = True, blocks: str = "rowcol"):
+        if scaling not in ("dynamic", "delayed", "static", "rowwise", "block"):
             raise ValueError(f"unknown scaling {scaling!r}")
+        if scaling == "block":
+            if blocks not in ("rowcol", "tile"):
+                raise ValueError(f"unknown blocks {blocks!r}")
+            self.rows, self.cols, self.fmt, self.fmt_max, self.scaling, self.blocks = (rows, cols, fmt, fmt_max,
+                                                                                      scaling, blocks)
+            nr, nc = (rows + 127) // 128, (cols + 127) // 128
+            self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+            self.qT = None
+            if blocks == "rowcol":
+                self.row_inv = torch.zeros((rows, nc), dtype=torch.float32, device=device)
+                self.qc = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+                self.col_inv = torch.zeros((nr, cols), dtype=torch.float32, device=device)
+            else:
+                self.tile_inv = torch.zeros((nr, nc), dtype=torch.float32, device=device)
+            return
         if scaling == "rowwise" and not transpose:
             raise ValueError("row-wise scaling needs the transposed copy (its scales run along columns)")
         self.rows, self.cols, self.fmt, self.fmt_max = rows, cols, fmt, fmt_max
@@ -429,7 +450,14 @@ class Float8Tensor:
 
     def quantize(self, x: torch.Tensor, stream=None) -> "Float8Tensor":
         """Scale, cast and transpose x according to this tensor's scaling."""
-        if self.scaling == "dynamic":
+        if self.scaling == "block":
+            if self.blocks == "rowcol":
+                fp8lin_cast_blockwise(x, self.fmt, q_row=self.q, inv_row=self.row_inv, q_col=self.qc,
+                                      inv_col=self.col_inv, fmt_max=self.fmt_max, stream=stream)
+            else:
+                fp8lin_cast_blockwise(x, self.fmt, q_tile=self.q, inv_tile=self.tile_inv, fmt_max=self.fmt_max,
+                                      stream=stream)
+        elif self.scaling == "dynamic":
             fp8lin_amax(x, self.amax, stream)
             fp8lin_cast_transpose(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT,
                                   self.fmt_max, stream)
@@ -467,10 +495,12 @@ class Float8Linear:
                  scaling: str = "dynamic", history_len: int = 16, transpose: bool | None = None):
         self.M, self.K, self.N = M, K, N
         self.transpose = (scaling == "rowwise") if transpose is None else bool(transpose)
+        if scaling == "block" and self.transpose:
+            raise ValueError("block scaling writes no transposed copies")
         args = (device, fmt_max, scaling, history_len, self.transpose)
-        self.x8 = Float8Tensor(M, K, E4M3, *args)
-        self.w8 = Float8Tensor(N, K, E4M3, *args)
-        self.dy8 = Float8Tensor(M, N, E5M2, *args)
+        self.x8 = Float8Tensor(M, K, E4M3, *args, blocks="rowcol")
+        self.w8 = Float8Tensor(N, K, E4M3, *args, blocks="tile")
+        self.dy8 = Float8Tensor(M, N, E5M2, *args, blocks="rowcol")
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=device)
@@ -482,7 +512,9 @@ class Float8Linear:
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
         self.x8.quantize(x, stream)
         self.w8.quantize(w, stream)
-        if self.x8.scaling == "rowwise":
+        if self.x8.scaling == "block":
+            fp8lin_fwd_block(self.x8.q, self.x8.row_inv, self.w8.q, self.w8.tile_inv, self.y, stream)
+        elif self.x8.scaling == "rowwise":
             fp8lin_fwd_rowwise(self.x8.q, self.x8.row_inv, self.w8.q, self.w8.row_inv, self.y, stream)
         else:
             fp8lin_fwd(self.x8.q, self.x8.inv_scale, self.w8.q, self.w8.inv_scale, self.y, stream)
@@ -490,7 +522,10 @@ class Float8Linear:
 
     def backward(self, dy: torch.Tensor, stream=None):
         self.dy8.quantize(dy, stream)
-        if self.dy8.scaling == "rowwise":
+        if self.dy8.scaling == "block":
+            fp8lin_dgrad_block(self.dy8.q, self.dy8.row_inv, self.w8.q, self.w8.tile_inv, self.dx, stream)
+            fp8lin_wgrad_block(self.dy8.qc, self.dy8.col_inv, self.x8.qc, self.x8.col_inv, self.dw, stream)
+        elif self.dy8.scaling == "rowwise":
             fp8lin_dgrad_rowwise(self.dy8.q, self.dy8.row_inv, self.w8.qT, self.w8.col_inv, self.dx, stream)
             fp8lin_wgrad_rowwise(self.dy8.qT, self.dy8.col_inv, self.x8.qT, self.x8.col_inv, self.dw, stream)
         elif self.transpose:

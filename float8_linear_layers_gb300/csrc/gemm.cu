@@ -598,28 +598,40 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 // sb_q + j * sb_r], or inv_b[q * sb_q + j * sb_r] when B_COLS (one scale per
 // row of B, i.e. per output column).
 //
-// One CTA per SM, persistent over 128 x 128 output tiles, 192 threads:
-//   warp 0      TMA producer: 128 x 128-byte A and B slabs (one contraction
-//               block each) into a 6-stage ring;
-//   warp 1      allocates 256 TMEM columns (two 128 x 128 fp32 partial
-//               buffers); one thread issues the four tcgen05.mma (M 128,
-//               N 128, K 32) of a contraction block into a fresh partial
-//               buffer and commits it;
-//   warps 2..5  promotion: read the block's partial sums from TMEM (32 rows
-//               x 32 columns at a time), multiply by ia * ib and add them to
-//               fp32 accumulators held in registers (32 rows x 128 columns
-//               per warp), hand the buffer back; after the last block, round
-//               to bf16 and TMA-store as the per-tensor epilogue does.
-// The two partial buffers let the MMAs of block j + 1 run while block j is
-// promoted.
+// One CTA per SM, persistent over 128 x 128 output tiles, 320 threads:
+//   warp 0      TMA producer: per contraction block a 128 x 128-byte A slab
+//               and B slab into a 6-stage ring;
+//   warp 1      allocates all 512 TMEM columns: four 128 x 128 fp32 partial
+//               buffers, used as two pairs; one thread issues the MMAs of two
+//               contraction blocks at a time (M 128, N 128, K 32; four per
+//               block, each block into its own buffer of the pair) and
+//               commits the pair;
+//   warps 2..9  promotion: warp w reads TMEM lanes 32 (w % 4) .. + 31,
+//               columns 64 ((w - 2) / 4) .. + 63 of a buffer (32 rows x 64
+//               columns, two 32-column loads in flight), multiplies by
+//               ia * ib and adds to 64 fp32 accumulators in registers, hands
+//               the pair back after its last block; after the tile's last
+//               block, rounds to bf16 and TMA-stores as the per-tensor
+//               epilogue does.
+// Ten warps leave each thread at most 168 registers (three warps share one
+// sub-partition's 16K); two buffer pairs let the MMAs of blocks j + 2, j + 3
+// run while blocks j, j + 1 are promoted, and eight MMAs per wait keep the
+// issuer's waits and commits covered.
 constexpr int kBlkTile = 128;                         // output rows and columns per tile; contraction block
 constexpr int kBlkStages = 6;
-constexpr int kBlkSlab = kBlkTile * kBK;              // 16 KB per operand and stage
-constexpr int kBlkThreads = 192;
-constexpr int kBlkTmemCols = 2 * kBlkTile;
-constexpr int kBlkEpiBytes = 4 * kEpiBuf;
-constexpr int kBlkSmemBytes = kBlkStages * 2 * kBlkSlab + kBlkEpiBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+constexpr int kBlkSlab = kBlkTile * kBK;              // 16 KB: one operand slab of one contraction block
+constexpr int kBlkStage = 2 * kBlkSlab;               // A + B
+constexpr int kBlkThreads = 320;
+constexpr int kBlkPromoWarps = 8;
+constexpr int kBlkWarpCols = 64;                      // columns each promotion warp owns
+constexpr int kBlkTmemCols = 4 * kBlkTile;
+constexpr int kBlkEpiBytes = kBlkPromoWarps * kEpiBuf;
+constexpr int kBlkColScaleBytes = kBlkPromoWarps * kBlkWarpCols * 4;  // per-column scales of one block, per warp
+constexpr int kBlkSmemBytes =
+    kBlkStages * kBlkStage + kBlkEpiBytes + kBlkColScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 static_assert(kBlkSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
+static_assert(kBlkTmemCols <= 512, "TMEM holds 512 columns");
+static_assert(kBlkStages % 2 == 0, "slabs are consumed two at a time");
 
 template <bool A_MN, bool B_MN, bool B_COLS>
 __global__ void __launch_bounds__(kBlkThreads, 1)
@@ -631,14 +643,14 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + kBlkStages * kBlkSlab;
-    uint8_t *sC = sB + kBlkStages * kBlkSlab;           // epilogue staging: [4 warps][32 rows x 64 B]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sC + kBlkEpiBytes);
-    uint64_t *full = bars;                              // [stages] slab landed
-    uint64_t *empty = bars + kBlkStages;                // [stages] MMAs done with the slab
-    uint64_t *pfull = bars + 2 * kBlkStages;            // [2] partial sums of a block ready
-    uint64_t *pempty = pfull + 2;                       // [2] the four promotion warps have read them
+    uint8_t *ring = smem;                               // [stages][A slab, B slab]
+    uint8_t *sC = ring + kBlkStages * kBlkStage;        // epilogue staging: [8 warps][32 rows x 64 B]
+    float *sCol = reinterpret_cast<float *>(sC + kBlkEpiBytes);  // [8 warps][64] column scales (B_COLS)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sCol + kBlkPromoWarps * kBlkWarpCols);
+    uint64_t *full = bars;                              // [stages] slabs landed
+    uint64_t *empty = bars + kBlkStages;                // [stages] MMAs done with the slabs
+    uint64_t *pfull = bars + 2 * kBlkStages;            // [2] partial sums of a buffer pair ready
+    uint64_t *pempty = pfull + 2;                       // [2] the promotion warps have read them
     uint64_t *mma_done = pempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -651,7 +663,7 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&pfull[b]), 1);
-            mbar_init(smem_u32(&pempty[b]), 4);
+            mbar_init(smem_u32(&pempty[b]), kBlkPromoWarps);
         }
         mbar_init(smem_u32(mma_done), 1);
         *abort_flag = 0;
@@ -690,11 +702,12 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
                     const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_arrive_expect_tx(fb, 2 * kBlkSlab);
-                    if (A_MN) tma_load_2d(smem_u32(sA + stage * kBlkSlab), &map_a, fb, a_row, kb * kBK);
-                    else      tma_load_2d(smem_u32(sA + stage * kBlkSlab), &map_a, fb, kb * kBK, a_row);
-                    if (B_MN) tma_load_2d(smem_u32(sB + stage * kBlkSlab), &map_b, fb, b_row, kb * kBK);
-                    else      tma_load_2d(smem_u32(sB + stage * kBlkSlab), &map_b, fb, kb * kBK, b_row);
+                    mbar_arrive_expect_tx(fb, kBlkStage);
+                    const uint32_t dst = smem_u32(ring + stage * kBlkStage);
+                    if (A_MN) tma_load_2d(dst, &map_a, fb, a_row, kb * kBK);
+                    else      tma_load_2d(dst, &map_a, fb, kb * kBK, a_row);
+                    if (B_MN) tma_load_2d(dst + kBlkSlab, &map_b, fb, b_row, kb * kBK);
+                    else      tma_load_2d(dst + kBlkSlab, &map_b, fb, kb * kBK, b_row);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kBlkStages) {
@@ -715,34 +728,45 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int pb = 0;
+            int pair = 0;
             uint32_t pphase = 0;
-            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
-            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
+            const uint64_t desc0 = sw128_kmajor_desc(smem_u32(ring));
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok && !*abort_flag; t += gridDim.x) {
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(smem_u32(&pempty[pb]), pphase ^ 1u, abort_flag, kWaitLimitNs) ||
-                        !mbar_wait(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+                for (int kb = 0; kb < num_kb; kb += 2) {
+                    const int n = min(2, num_kb - kb);
+                    if (!mbar_wait(smem_u32(&pempty[pair]), pphase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kBlkSlab >> 4));
-                    const uint64_t b_desc = b_desc0 + (uint64_t)(stage * (kBlkSlab >> 4));
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(pb * kBlkTile);
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k)
-                        umma_f8f6f4_single(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc,
-                                           k != 0 ? 1u : 0u);
-                    umma_commit_single(smem_u32(&empty[stage]));
-                    umma_commit_single(smem_u32(&pfull[pb]));
-                    if (++stage == kBlkStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    int st = stage;
+                    uint32_t ph = phase;
+                    for (int i = 0; i < n && ok; ++i) {
+                        if (!mbar_wait(smem_u32(&full[st]), ph, abort_flag, kWaitLimitNs)) ok = false;
+                        if (++st == kBlkStages) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
-                    if (++pb == 2) {
-                        pb = 0;
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int i = 0; i < n; ++i) {
+                        const uint64_t a_desc = desc0 + (uint64_t)(stage * (kBlkStage >> 4));
+                        const uint64_t b_desc = a_desc + (uint64_t)(kBlkSlab >> 4);
+                        const uint32_t d_tmem = tmem_base + (uint32_t)((pair * 2 + i) * kBlkTile);
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k)
+                            umma_f8f6f4_single(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc,
+                                               k != 0 ? 1u : 0u);
+                        umma_commit_single(smem_u32(&empty[stage]));
+                        if (++stage == kBlkStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    umma_commit_single(smem_u32(&pfull[pair]));
+                    if (++pair == 2) {
+                        pair = 0;
                         pphase ^= 1u;
                     }
                 }
@@ -753,10 +777,12 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         }
     } else {
         // ------------------------------------------------ promotion + epilogue
-        const int sub = warp % 4;  // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows of the tile
+        const int sub = warp % 4;          // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows
+        const int cw = (warp - 2) / 4;     // which 64-column half of the tile
         uint8_t *stage_c = sC + (warp - 2) * kEpiBuf;
         uint8_t *dst = stage_c + lane * (kEpiCols * 2);
-        int pb = 0;
+        float *col_scale = sCol + (warp - 2) * kBlkWarpCols;
+        int pair = 0;
         uint32_t pphase = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -764,62 +790,80 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
             tiles.coords(t, tm, tn);
             const int row0 = tm * kBlkTile + sub * 32;
             const int row = row0 + lane;
-            float acc[kBlkTile];
+            const int col_base = tn * kBlkTile + cw * kBlkWarpCols;   // first output column of this warp
+            float acc[kBlkWarpCols];
 #pragma unroll
-            for (int j = 0; j < kBlkTile; ++j) acc[j] = 0.0f;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const float sa = row < P ? __ldg(inv_a + row * sa_p + kb * sa_r) : 0.0f;
-                const float sb_tile = B_COLS ? 0.0f : __ldg(inv_b + (long long)tn * sb_q + kb * sb_r);
-                const bool ready = mbar_wait(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs);
+            for (int j = 0; j < kBlkWarpCols; ++j) acc[j] = 0.0f;
+            for (int kb0 = 0; kb0 < num_kb && ok; kb0 += 2) {
+                const int n = min(2, num_kb - kb0);
+                const bool ready = mbar_wait(smem_u32(&pfull[pair]), pphase, abort_flag, kWaitLimitNs);
                 if (!__all_sync(0xFFFFFFFFu, ready)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(pb * kBlkTile);
-#pragma unroll
-                for (int c = 0; c < kBlkTile / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + (uint32_t)(c * 32), r);
-                    float s[32];
+                for (int i = 0; i < n; ++i) {
+                    const int kb = kb0 + i;
+                    const float sa = row < P ? __ldg(inv_a + row * sa_p + kb * sa_r) : 0.0f;
+                    float sab = sa;
                     if (B_COLS) {
-                        // one scale per output column: the same 32 floats for every lane
-                        const int col0 = tn * kBlkTile + c * 32;
-                        const float *bp = inv_b + (long long)col0 * sb_q + kb * sb_r;
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            const float4 b4 = (col0 + 4 * g < Q) ? __ldg(reinterpret_cast<const float4 *>(bp) + g)
-                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                            s[4 * g + 0] = __fmul_rn(sa, b4.x);
-                            s[4 * g + 1] = __fmul_rn(sa, b4.y);
-                            s[4 * g + 2] = __fmul_rn(sa, b4.z);
-                            s[4 * g + 3] = __fmul_rn(sa, b4.w);
-                        }
+                        // this block's scales of the warp's 64 columns (lanes 0..15 load 4 each),
+                        // kept in shared memory and read back as broadcasts
+                        const int c4 = col_base + 4 * lane;
+                        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (lane < kBlkWarpCols / 4 && c4 < Q)
+                            b4 = __ldg(reinterpret_cast<const float4 *>(inv_b + (long long)c4 * sb_q + kb * sb_r));
+                        __syncwarp();   // the previous block's reads of col_scale are done
+                        if (lane < kBlkWarpCols / 4) reinterpret_cast<float4 *>(col_scale)[lane] = b4;
+                        __syncwarp();
                     } else {
-                        const float st = __fmul_rn(sa, sb_tile);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) s[j] = st;
+                        sab = __fmul_rn(sa, col_base < Q ? __ldg(inv_b + (long long)(col_base / kBlkTile) * sb_q +
+                                                                 kb * sb_r)
+                                                         : 0.0f);
                     }
+                    const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) +
+                                           (uint32_t)((pair * 2 + i) * kBlkTile + cw * kBlkWarpCols);
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(tbase, r0);
+                    tmem_ld_32x32b_x32(tbase + 32u, r1);
                     tmem_ld_wait();
-                    if (c == kBlkTile / 32 - 1) {
-                        // the whole partial buffer is in registers: hand it back
+                    if (i == n - 1) {
+                        // the warp's part of the pair is in registers: hand it back
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_local(smem_u32(&pempty[pb]));
+                        if (lane == 0) mbar_arrive_local(smem_u32(&pempty[pair]));
+                    }
+                    if (B_COLS) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const float4 b0 = reinterpret_cast<const float4 *>(col_scale)[g];
+                            const float4 b1 = reinterpret_cast<const float4 *>(col_scale)[8 + g];
+                            r0[4 * g + 0] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 0]), b0.x));
+                            r0[4 * g + 1] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 1]), b0.y));
+                            r0[4 * g + 2] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 2]), b0.z));
+                            r0[4 * g + 3] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 3]), b0.w));
+                            r1[4 * g + 0] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 0]), b1.x));
+                            r1[4 * g + 1] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 1]), b1.y));
+                            r1[4 * g + 2] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 2]), b1.z));
+                            r1[4 * g + 3] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 3]), b1.w));
+                        }
                     }
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(__uint_as_float(r[j]), s[j], acc[c * 32 + j]);
+                    for (int j = 0; j < 32; ++j) {
+                        acc[j] = __fmaf_rn(__uint_as_float(r0[j]), sab, acc[j]);
+                        acc[32 + j] = __fmaf_rn(__uint_as_float(r1[j]), sab, acc[32 + j]);
+                    }
                 }
-                if (++pb == 2) {
-                    pb = 0;
+                if (++pair == 2) {
+                    pair = 0;
                     pphase ^= 1u;
                 }
             }
             if (!ok) break;
             // epilogue: round to bf16, stage 32 columns at a time, TMA-store
 #pragma unroll
-            for (int c = 0; c < kBlkTile / kEpiCols; ++c) {
-                const int col0 = tn * kBlkTile + c * kEpiCols;
+            for (int c = 0; c < kBlkWarpCols / kEpiCols; ++c) {
+                const int col0 = col_base + c * kEpiCols;
                 if (lane == 0) bulk_wait_read_0();
                 __syncwarp();
 #pragma unroll

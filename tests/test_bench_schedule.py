@@ -74,3 +74,6 @@ def test_attainable_bound():
     assert abs(a["frac_of_peak"] - gemm_ms / (gemm_ms + cast_ms)) < 1e-9
     assert 0.81 < a["frac_of_peak"] < 0.83
     assert bench.attainable(w13, "dynamic", 3423.0, 6775.9)["frac_of_peak"] > a["frac_of_peak"]
+    # block scaling: one pass per tensor, two copies for activations and gradients, one for weights
+    w_elems = 2 * 14336 * 4096 + 4096 * 14336
+    assert bench.cast_bytes(ffn, "block") == 4 * (elems - w_elems) + 3 * w_elems

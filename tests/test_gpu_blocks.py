@@ -85,3 +85,58 @@ def test_block_gemm_matches_oracle(fp8lin, M, N, K, which):
     assert fp8lin.fp8lin_device_error() == 0
     assert_gemm_close(bf16_to_f64(out.t), ref, f"{which} block {M}x{N}x{K}")
     assert out.intact()
+
+
+def _check_block_copies(name, lin, r):
+    got = {"x_k": (lin.x8.q, lin.x8.row_inv), "x_m": (lin.x8.qc, lin.x8.col_inv), "w": (lin.w8.q, lin.w8.tile_inv),
+           "dy_n": (lin.dy8.q, lin.dy8.row_inv), "dy_m": (lin.dy8.qc, lin.dy8.col_inv)}
+    for key, (q, inv) in got.items():
+        assert np.array_equal(inv.cpu().numpy().view(np.uint32), r[key]["inv_scale"].view(np.uint32)), f"{name} {key}"
+        assert np.array_equal(q.cpu().numpy(), r[key]["q"]), f"{name} {key}"
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 512, 1024), (144, 208, 272), (640, 384, 1296)])
+def test_block_linear_step_matches_oracle(fp8lin, M, K, N):
+    X = wl.generate((M, K), "normal", 1.0, 21, wl.X, outlier_frac=1e-3)
+    W = wl.generate((N, K), "normal", 0.02, 21, wl.W)
+    dY = wl.generate((M, N), "normal", 1e-3, 21, wl.DY)
+    lin = fp8lin.Float8Linear(M, K, N, scaling="block")
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    r = oracle.quantize_block_recipe(X, W, dY)
+    _check_block_copies(f"{M}x{K}x{N}", lin, r)
+    assert_gemm_close(bf16_to_f64(y), oracle.fwd_block_ref(r["x_k"]["q"], r["x_k"]["inv_scale"], r["w"]["q"],
+                                                           r["w"]["inv_scale"]), "Y")
+    assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_block_ref(r["dy_n"]["q"], r["dy_n"]["inv_scale"], r["w"]["q"],
+                                                              r["w"]["inv_scale"]), "dX")
+    assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_block_ref(r["dy_m"]["q"], r["dy_m"]["inv_scale"], r["x_m"]["q"],
+                                                              r["x_m"]["inv_scale"]), "dW")
+
+
+def _rows(n, seed, count=40):
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(n, size=min(n, count - 2), replace=False)
+    return np.unique(np.concatenate([[0, n - 1], pick])).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_block_workload_step_matches_oracle(fp8lin, name):
+    """Every configuration at full size: every FP8 byte and inverse scale of
+    the five block-scaled copies bit-exact; Y, dX, dW on sampled rows."""
+    w = wl.WORKLOADS[name]
+    X, W, dY = w.make_x(), w.make_w(), w.make_dy()
+    lin = fp8lin.Float8Linear(w.M, w.K, w.N, scaling="block")
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    r = oracle.quantize_block_recipe(X, W, dY)
+    _check_block_copies(name, lin, r)
+    rm, rn = _rows(w.M, w.seed), _rows(w.N, w.seed + 1)
+    pick = lambda t, rows: bf16_to_f64(t[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(pick(y, rm), oracle.fwd_block_ref(r["x_k"]["q"], r["x_k"]["inv_scale"], r["w"]["q"],
+                                                        r["w"]["inv_scale"], rm), f"{name} Y")
+    assert_gemm_close(pick(dx, rm), oracle.dgrad_block_ref(r["dy_n"]["q"], r["dy_n"]["inv_scale"], r["w"]["q"],
+                                                           r["w"]["inv_scale"], rm), f"{name} dX")
+    assert_gemm_close(pick(dw, rn), oracle.wgrad_block_ref(r["dy_m"]["q"], r["dy_m"]["inv_scale"], r["x_m"]["q"],
+                                                           r["x_m"]["inv_scale"], rn), f"{name} dW")
