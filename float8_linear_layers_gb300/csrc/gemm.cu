@@ -785,12 +785,43 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         int pair = 0;
         uint32_t pphase = 0;
         bool ok = true;
+        // The scales of block j + 1 are loaded while block j is promoted (the
+        // next tile's first block after a tile's last): sa = this row's A
+        // scale, sb = the B block's scale or, with B_COLS, four column scales
+        // per lane 0..15.
+        auto load_scales = [&](int row_, int col_base_, int kb_, float &sa_o, float &sb_o, float4 &cv_o) {
+            sa_o = row_ < P ? __ldg(inv_a + row_ * sa_p + kb_ * sa_r) : 0.0f;
+            if (B_COLS) {
+                const int c4 = col_base_ + 4 * lane;
+                cv_o = (lane < kBlkWarpCols / 4 && c4 < Q)
+                           ? __ldg(reinterpret_cast<const float4 *>(inv_b + (long long)c4 * sb_q + kb_ * sb_r))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                sb_o = col_base_ < Q ? __ldg(inv_b + (long long)(col_base_ / kBlkTile) * sb_q + kb_ * sb_r) : 0.0f;
+            }
+        };
+        auto bases = [&](int t_, int &row_, int &col_base_) {
+            int tm_, tn_;
+            tiles.coords(t_, tm_, tn_);
+            row_ = tm_ * kBlkTile + sub * 32 + lane;
+            col_base_ = tn_ * kBlkTile + cw * kBlkWarpCols;
+        };
+        float sa_c = 0.0f, sb_c = 0.0f;
+        float4 cv_c = make_float4(0.f, 0.f, 0.f, 0.f);
+        if ((int)blockIdx.x < num_tiles) {
+            int r_, c_;
+            bases(blockIdx.x, r_, c_);
+            load_scales(r_, c_, 0, sa_c, sb_c, cv_c);
+        }
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int tm, tn;
             tiles.coords(t, tm, tn);
             const int row0 = tm * kBlkTile + sub * 32;
             const int row = row0 + lane;
             const int col_base = tn * kBlkTile + cw * kBlkWarpCols;   // first output column of this warp
+            const int t_next = t + (int)gridDim.x;
+            int row_next = 0, col_next = 0;
+            if (t_next < num_tiles) bases(t_next, row_next, col_next);
             float acc[kBlkWarpCols];
 #pragma unroll
             for (int j = 0; j < kBlkWarpCols; ++j) acc[j] = 0.0f;
@@ -804,22 +835,19 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                 tc_fence_after();
                 for (int i = 0; i < n; ++i) {
                     const int kb = kb0 + i;
-                    const float sa = row < P ? __ldg(inv_a + row * sa_p + kb * sa_r) : 0.0f;
-                    float sab = sa;
+                    float sa_n = 0.0f, sb_n = 0.0f;
+                    float4 cv_n = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (kb + 1 < num_kb)
+                        load_scales(row, col_base, kb + 1, sa_n, sb_n, cv_n);
+                    else if (t_next < num_tiles)
+                        load_scales(row_next, col_next, 0, sa_n, sb_n, cv_n);
+                    float sab = sa_c;
                     if (B_COLS) {
-                        // this block's scales of the warp's 64 columns (lanes 0..15 load 4 each),
-                        // kept in shared memory and read back as broadcasts
-                        const int c4 = col_base + 4 * lane;
-                        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (lane < kBlkWarpCols / 4 && c4 < Q)
-                            b4 = __ldg(reinterpret_cast<const float4 *>(inv_b + (long long)c4 * sb_q + kb * sb_r));
                         __syncwarp();   // the previous block's reads of col_scale are done
-                        if (lane < kBlkWarpCols / 4) reinterpret_cast<float4 *>(col_scale)[lane] = b4;
+                        if (lane < kBlkWarpCols / 4) reinterpret_cast<float4 *>(col_scale)[lane] = cv_c;
                         __syncwarp();
                     } else {
-                        sab = __fmul_rn(sa, col_base < Q ? __ldg(inv_b + (long long)(col_base / kBlkTile) * sb_q +
-                                                                 kb * sb_r)
-                                                         : 0.0f);
+                        sab = __fmul_rn(sa_c, sb_c);
                     }
                     const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) +
                                            (uint32_t)((pair * 2 + i) * kBlkTile + cw * kBlkWarpCols);
@@ -853,6 +881,9 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                         acc[j] = __fmaf_rn(__uint_as_float(r0[j]), sab, acc[j]);
                         acc[32 + j] = __fmaf_rn(__uint_as_float(r1[j]), sab, acc[32 + j]);
                     }
+                    sa_c = sa_n;
+                    sb_c = sb_n;
+                    cv_c = cv_n;
                 }
                 if (++pair == 2) {
                     pair = 0;
