@@ -12,7 +12,7 @@ transformer block.  Nothing is cached across steps (dynamic scaling
 recomputes every statistic every step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload ffn8b|block8b] [--scaling dynamic|delayed|rowwise]
+                    [--workload ffn8b|block8b] [--scaling dynamic|delayed|rowwise|block]
 
 Prints one JSON line on rank 0.  N > 1 runs under torchrun: each rank runs
 its own replica on its own batch (the path has no exchange step), timing is
