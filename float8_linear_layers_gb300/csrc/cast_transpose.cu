@@ -1,8 +1,12 @@
 // cast_transpose.cu -- scale one bf16 matrix and cast it to FP8 (the Float8
 // derived dtype; TorchTitan analysis page, section 3.3, "Mixed precision and
-// Float8"), writing the row-major copy and the transposed copy in one pass.
+// Float8"), writing the row-major copy and, when asked for, the transposed
+// copy in the same pass (the tensor cores read 8-bit operands either way, so
+// per-tensor scaling needs only the row-major copy).  Per-tensor, delayed,
+// static and row-wise scales here; block scales (cast_block_kernel, below)
+// in one pass with no amax call.
 //
-// HBM-bound: per element 2 bytes read, 1 + 1 bytes written.  One CTA owns a
+// HBM-bound: per element 2 bytes read, 1 (+ 1) bytes written.  One CTA owns a
 // 128 x 128 tile:
 //  * phase 1: coalesced 16-byte loads (16 threads per 256-byte tile row, all
 //    eight loads of a thread issued before any use), fp32 product with the

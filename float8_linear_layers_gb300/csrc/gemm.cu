@@ -43,6 +43,10 @@
 // raster groups chosen from the operand sizes (see TileMap), so that the
 // smaller operand is read from DRAM once when it fits in L2.
 //
+// The block-scaled GEMM (fp8_gemm_block_kernel, further down) runs one CTA
+// per SM on 128 x 128 tiles and scales every 128-long contraction block's
+// partial sums on the CUDA cores.
+//
 // Every mbarrier wait is bounded by wall-clock time (globaltimer).  A wait
 // that runs out records FP8LIN_ERR_TIMEOUT in a device word, raises the
 // CTA's abort flag, which ends every role's loop, drains the copies and MMAs
