@@ -119,3 +119,34 @@ def test_argument_checks_without_gpu(lib):
         assert fn(a4, a16, a16, a16, a16, 128, 128, 128, None) == 2
         assert fn(a16, a16, a16, a16, a16, 128, 120, 128, None) == 3
         assert fn(a16, a16, a16, a16, a16, 128, 128, 8, None) == 3
+
+
+def test_argument_checks_of_mn_and_block_entry_points(lib):
+    a16 = V(4096)      # 16-byte-aligned fake addresses: never dereferenced on these paths
+    a4 = V(4100)
+    # GEMMs on the row-major copies and the block-scaled GEMMs: same checks as fp8lin_fwd
+    for name in ("fp8lin_dgrad_mn", "fp8lin_wgrad_mn", "fp8lin_fwd_block", "fp8lin_dgrad_block",
+                 "fp8lin_wgrad_block"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [V, V, V, V, V, I, I, I, V]
+        assert fn(a16, None, a16, a16, a16, 128, 128, 128, None) == 1, name
+        assert fn(a16, a16, a16, a16, a16, 128, -16, 128, None) == 1, name
+        assert fn(a16, a16, a4, a16, a16, 128, 128, 128, None) == 2, name
+        assert fn(a16, a16, a16, a16, a4, 128, 128, 128, None) == 2, name
+        assert fn(a16, a16, a16, a16, a16, 136, 128, 128, None) == 3, name
+    # the weight-gradient block GEMM reads its column scales as float4s
+    fn = lib.fp8lin_wgrad_block
+    assert fn(a16, a16, a16, V(4100), a16, 128, 128, 128, None) == 2
+    # block cast: each copy with its scales, at least one copy, formats, alignment, shapes
+    cb = lib.fp8lin_cast_blockwise
+    cb.restype = ctypes.c_int
+    cb.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V, V, V]
+    assert cb(a16, 32, 32, 0, 448.0, a16, None, None, None, None, None, None) == 1   # q without scales
+    assert cb(a16, 32, 32, 0, 448.0, None, a16, None, None, None, None, None) == 1   # scales without q
+    assert cb(a16, 32, 32, 0, 448.0, None, None, None, None, None, None, None) == 1  # nothing asked for
+    assert cb(a16, 32, 32, 3, 448.0, a16, a16, None, None, None, None, None) == 1    # format
+    assert cb(a16, 32, 32, 0, -1.0, a16, a16, None, None, None, None, None) == 1     # fmt_max
+    assert cb(a16, 32, 32, 0, 448.0, a4, a16, None, None, None, None, None) == 2     # misaligned copy
+    assert cb(a16, 32, 32, 0, 448.0, a16, V(4098), None, None, None, None, None) == 2  # misaligned scales
+    assert cb(a16, 32, 40, 0, 448.0, a16, a16, None, None, None, None, None) == 3    # ragged shape
