@@ -11,15 +11,16 @@ from gpu_helpers import to_dev_bf16
 pytestmark = pytest.mark.gpu
 
 
-def test_linear_step_in_cuda_graph(fp8lin):
+@pytest.mark.parametrize("scaling", ["dynamic", "block"])
+def test_linear_step_in_cuda_graph(fp8lin, scaling):
     M, K, N = 640, 384, 1296
     X = to_dev_bf16(wl.generate((M, K), "normal", 1.0, 31, 0))
     W = to_dev_bf16(wl.generate((N, K), "normal", 0.02, 31, 1))
     dY = to_dev_bf16(wl.generate((M, N), "normal", 1e-3, 31, 2))
-    eager = fp8lin.Float8Linear(M, K, N)
+    eager = fp8lin.Float8Linear(M, K, N, scaling=scaling)
     ref = [t.clone() for t in eager.step(X, W, dY)]
 
-    lin = fp8lin.Float8Linear(M, K, N)
+    lin = fp8lin.Float8Linear(M, K, N, scaling=scaling)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
