@@ -204,7 +204,7 @@ def fp8lin_cast_transpose_delayed(x: torch.Tensor, fmt: int, amax_history: torch
 
 def fp8lin_cast_blockwise(x: torch.Tensor, fmt: int, q_row=None, inv_row=None, q_col=None, inv_col=None,
                           q_tile=None, inv_tile=None, fmt_max: float = FMT_MAX, stream=None) -> None:
-    """Block scaling in one pass: q_row / inv_row (1 x 128 blocks), q_col / inv_col
+    """Block scaling in one pass: q_row / inv_row (1 x 128 blocks, inv_row [ceil(cols/128) x rows]), q_col / inv_col
     (128 x 1 blocks), q_tile / inv_tile (128 x 128 blocks); any subset of the pairs."""
     _dev(x, "x", torch.bfloat16)
     if x.dim() != 2:
@@ -269,18 +269,18 @@ def _block_gemm(name, a, ia, b, ib, out, M, N, K, ia_shape, ib_shape, out_shape,
 
 
 def fp8lin_fwd_block(xq, inv_x, wq, inv_w, y, stream=None) -> None:
-    """Y = sum_j (Xq . Wq^T)_j * inv_x[m][j] * inv_w[n/128][j]: Xq in 1 x 128 and Wq in 128 x 128 blocks."""
+    """Y = sum_j (Xq . Wq^T)_j * inv_x[j][m] * inv_w[n/128][j]: Xq in 1 x 128 and Wq in 128 x 128 blocks."""
     M, K = xq.shape
     N = wq.shape[0]
-    _block_gemm("fp8lin_fwd_block", xq, inv_x, wq, inv_w, y, M, N, K, (M, _blocks(K)), (_blocks(N), _blocks(K)),
+    _block_gemm("fp8lin_fwd_block", xq, inv_x, wq, inv_w, y, M, N, K, (_blocks(K), M), (_blocks(N), _blocks(K)),
                 (M, N), stream)
 
 
 def fp8lin_dgrad_block(dyq, inv_dy, wq, inv_w, dx, stream=None) -> None:
-    """dX = sum_j (dYq . Wq)_j * inv_dy[m][j] * inv_w[j][k/128]: dYq in 1 x 128 and Wq in 128 x 128 blocks."""
+    """dX = sum_j (dYq . Wq)_j * inv_dy[j][m] * inv_w[j][k/128]: dYq in 1 x 128 and Wq in 128 x 128 blocks."""
     M, N = dyq.shape
     K = wq.shape[1]
-    _block_gemm("fp8lin_dgrad_block", dyq, inv_dy, wq, inv_w, dx, M, N, K, (M, _blocks(N)),
+    _block_gemm("fp8lin_dgrad_block", dyq, inv_dy, wq, inv_w, dx, M, N, K, (_blocks(N), M),
                 (_blocks(N), _blocks(K)), (M, K), stream)
 
 
@@ -402,7 +402,7 @@ class Float8Tensor:
               "block":   blocks of 128 along the contraction, one pass with
                          no amax call: ``blocks="rowcol"`` (activations,
                          gradients) gives q in 1 x 128 blocks (row_inv
-                         [rows x ceil(cols/128)]) and qc in 128 x 1 blocks
+                         [ceil(cols/128) x rows]) and qc in 128 x 1 blocks
                          (col_inv [ceil(rows/128) x cols]); ``blocks="tile"``
                          (weights) gives q in 128 x 128 blocks (tile_inv)."""
 
@@ -419,7 +419,7 @@ class Float8Tensor:
             self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
             self.qT = None
             if blocks == "rowcol":
-                self.row_inv = torch.zeros((rows, nc), dtype=torch.float32, device=device)
+                self.row_inv = torch.zeros((nc, rows), dtype=torch.float32, device=device)   # block-major
                 self.qc = torch.empty((rows, cols), dtype=torch.uint8, device=device)
                 self.col_inv = torch.zeros((nr, cols), dtype=torch.float32, device=device)
             else:

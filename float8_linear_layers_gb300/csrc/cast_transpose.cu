@@ -335,7 +335,7 @@ fp8lin_status set_carveouts(int device) {
 // block, scale = fmt_max / max(amax, 1e-12), saturating RNE cast).  Every
 // 1 x 128, 128 x 1 and 128 x 128 block lies inside one 128 x 128 tile, so one
 // pass over x makes any of
-//   ROW : 1 x 128 blocks (a scale per row of the tile)     q_row, inv_row [rows x tiles_c]
+//   ROW : 1 x 128 blocks (a scale per row of the tile)     q_row, inv_row [tiles_c x rows]
 //   COL : 128 x 1 blocks (a scale per column of the tile)  q_col, inv_col [tiles_r x cols]
 //   TILE: the 128 x 128 block                              q_tile, inv_tile [tiles_r x tiles_c]
 // (each copy row-major like x), with no separate amax pass: 2 bytes read and
@@ -436,7 +436,7 @@ cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_
         if (ROW) {
             const float s = scale_from_amax(__uint_as_float(rowm[i] << 16), fmt_max);
             if (ok) st_stream8(q_row + off, cast8<FMT>(v[i], s), pol);
-            if (ch == 0 && r < rows) inv_row[(int64_t)r * tiles_c + tc] = __frcp_rn(s);
+            if (ch == 0 && r < rows) inv_row[(int64_t)tc * rows + r] = __frcp_rn(s);
         }
         if (COL && ok) st_stream8(q_col + off, cast8_each<FMT>(v[i], csc), pol);
         if (TILE && ok) st_stream8(q_tile + off, cast8<FMT>(v[i], s_tile), pol);

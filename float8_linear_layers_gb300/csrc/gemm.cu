@@ -1206,19 +1206,19 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 extern "C" fp8lin_status fp8lin_fwd_block(const uint8_t *xq, const float *inv_x, const uint8_t *wq,
                                           const float *inv_w, void *y, int64_t M, int64_t N, int64_t K,
                                           cudaStream_t stream) {
-    // A = Xq (row blocks, inv_x [M x KB]), B = Wq (tiles, inv_w [NB x KB]); contraction K
+    // A = Xq (row blocks, inv_x [KB x M]), B = Wq (tiles, inv_w [NB x KB]); contraction K
     const int64_t kb = ceil_div(K, kBlkTile);
-    return gemm_block<false, false, false>(xq, FP8LIN_E4M3, inv_x, kb, 1, wq, FP8LIN_E4M3, inv_w, kb, 1, y, M, N,
+    return gemm_block<false, false, false>(xq, FP8LIN_E4M3, inv_x, 1, M, wq, FP8LIN_E4M3, inv_w, kb, 1, y, M, N,
                                            K, stream);
 }
 
 extern "C" fp8lin_status fp8lin_dgrad_block(const uint8_t *dyq, const float *inv_dy, const uint8_t *wq,
                                             const float *inv_w, void *dx, int64_t M, int64_t N, int64_t K,
                                             cudaStream_t stream) {
-    // A = dYq (row blocks, inv_dy [M x NB]), B = Wq read MN-major: row k of B,
+    // A = dYq (row blocks, inv_dy [NB x M]), B = Wq read MN-major: row k of B,
     // contraction block j scaled by inv_w[j][k / 128]; contraction N
-    const int64_t nb = ceil_div(N, kBlkTile), kb = ceil_div(K, kBlkTile);
-    return gemm_block<false, true, false>(dyq, FP8LIN_E5M2, inv_dy, nb, 1, wq, FP8LIN_E4M3, inv_w, 1, kb, dx, M, K,
+    const int64_t kb = ceil_div(K, kBlkTile);
+    return gemm_block<false, true, false>(dyq, FP8LIN_E5M2, inv_dy, 1, M, wq, FP8LIN_E4M3, inv_w, 1, kb, dx, M, K,
                                           N, stream);
 }
 

@@ -284,10 +284,13 @@ fp8lin_status fp8lin_wgrad_mn(const uint8_t *dyq, const float *inv_dy, const uin
  * saturating round-to-nearest-even cast -- in one pass over x, with no
  * separate amax call.  Any of three copies, each row-major [rows x cols]
  * like x, with its inverse scales (1 / scale, binary32):
- *   q_row,  inv_row  [rows x ceil(cols/128)]            1 x 128 blocks
+ *   q_row,  inv_row  [ceil(cols/128) x rows]            1 x 128 blocks
  *   q_col,  inv_col  [ceil(rows/128) x cols]            128 x 1 blocks
  *   q_tile, inv_tile [ceil(rows/128) x ceil(cols/128)]  128 x 128 blocks
- * Blocks at the right and bottom edges are cut short.  A linear takes X as
+ * Blocks at the right and bottom edges are cut short.  Scales are stored
+ * block-major (one block column's scales, or one block row's, contiguous),
+ * so that the GEMM reads one contraction block's scales of consecutive rows
+ * in one transaction.  A linear takes X as
  * q_row (forward) and q_col (weight gradient), W as q_tile, dY as q_row
  * (input gradient) and q_col (weight gradient); see fp8lin_fwd_block.
  *
@@ -310,15 +313,15 @@ fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int64_t cols, f
  * tensor cores sum each block in fp32, the partial sum is multiplied by the
  * two operands' inverse scales for that block (fp32) and added to an fp32
  * total, which is rounded to bf16 (round to nearest even) at the end:
- *   fwd  : Y [M x N]  = sum_j (Xq Wq^T)_j  * inv_x[m][j]  * inv_w[n/128][j]   contraction K
- *   dgrad: dX [M x K] = sum_j (dYq Wq)_j   * inv_dy[m][j] * inv_w[j][k/128]   contraction N
+ *   fwd  : Y [M x N]  = sum_j (Xq Wq^T)_j  * inv_x[j][m]  * inv_w[n/128][j]   contraction K
+ *   dgrad: dX [M x K] = sum_j (dYq Wq)_j   * inv_dy[j][m] * inv_w[j][k/128]   contraction N
  *   wgrad: dW [N x K] = sum_j (dYq^T Xq)_j * inv_dy[j][n] * inv_x[j][k]       contraction M
  * (Lecture 9 exercises: FP8 scaling per tensor or per block; TorchTitan
  * analysis page, section 3.3: the Float8 linear's three GEMMs.)
  *
- * fp8lin_fwd_block:   xq = q_row of X [M x K] e4m3, inv_x [M x ceil(K/128)];
+ * fp8lin_fwd_block:   xq = q_row of X [M x K] e4m3, inv_x [ceil(K/128) x M];
  *                     wq = q_tile of W [N x K] e4m3, inv_w [ceil(N/128) x ceil(K/128)].
- * fp8lin_dgrad_block: dyq = q_row of dY [M x N] e5m2, inv_dy [M x ceil(N/128)];
+ * fp8lin_dgrad_block: dyq = q_row of dY [M x N] e5m2, inv_dy [ceil(N/128) x M];
  *                     wq, inv_w as for the forward.
  * fp8lin_wgrad_block: dyq = q_col of dY [M x N] e5m2, inv_dy [ceil(M/128) x N];
  *                     xq = q_col of X [M x K] e4m3, inv_x [ceil(M/128) x K]

@@ -16,7 +16,13 @@ KINDS = {"row": (1, 128), "col": (128, 1), "tile": (128, 128)}
 
 def _blocks(rows, cols, kind):
     br, bc = KINDS[kind]
-    return (rows + br - 1) // br, (cols + bc - 1) // bc
+    n = ((rows + br - 1) // br, (cols + bc - 1) // bc)
+    return n[::-1] if kind == "row" else n   # row-block scales are stored block-major
+
+
+def _layout(kind, inv):
+    """The oracle's [block rows x block columns] scales in the library's layout."""
+    return np.ascontiguousarray(inv.T) if kind == "row" else inv
 
 
 @pytest.mark.parametrize("shape", [(16, 16), (144, 272), (384, 1040), (1040, 384), (2048, 4096)])
@@ -38,7 +44,7 @@ def test_block_cast_bit_exact(fp8lin, shape, fmt, dist, kinds):
     torch.cuda.synchronize()
     for k in kinds:
         ref = oracle.quantize_blocks(x, fmt, *KINDS[k])
-        assert np.array_equal(inv[k].t.cpu().numpy().view(np.uint32), ref["inv_scale"].view(np.uint32)), k
+        assert np.array_equal(inv[k].t.cpu().numpy().view(np.uint32), _layout(k, ref["inv_scale"]).view(np.uint32)), k
         assert np.array_equal(q[k].t.cpu().numpy(), ref["q"]), k
         assert q[k].intact() and inv[k].intact(), k
 
@@ -46,11 +52,11 @@ def test_block_cast_bit_exact(fp8lin, shape, fmt, dist, kinds):
 def test_block_cast_zero_tensor_and_arguments(fp8lin):
     x = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
     q = torch.full((128, 256), 0xFF, dtype=torch.uint8, device="cuda")
-    inv = torch.zeros((128, 2), dtype=torch.float32, device="cuda")
+    inv = torch.zeros((2, 128), dtype=torch.float32, device="cuda")
     fp8lin.fp8lin_cast_blockwise(x, E4M3, q_row=q, inv_row=inv)
     torch.cuda.synchronize()
     ref = oracle.quantize_blocks(np.zeros((128, 256), np.uint16), E4M3, 1, 128)
-    assert (q == 0).all() and np.array_equal(inv.cpu().numpy().view(np.uint32), ref["inv_scale"].view(np.uint32))
+    assert (q == 0).all() and np.array_equal(inv.cpu().numpy().view(np.uint32), ref["inv_scale"].T.copy().view(np.uint32))
     with pytest.raises(fp8lin.Fp8LinError):
         fp8lin.fp8lin_cast_blockwise(x, E4M3, q_row=q)            # a copy without its scales
     with pytest.raises(fp8lin.Fp8LinError):
@@ -79,8 +85,8 @@ def test_block_gemm_matches_oracle(fp8lin, M, N, K, which):
         ref = oracle.wgrad_block_ref(r["dy_m"]["q"], r["dy_m"]["inv_scale"], r["x_m"]["q"], r["x_m"]["inv_scale"])
     out.t.fill_(float("nan"))
     a, b = args
-    getattr(fp8lin, f"fp8lin_{which}_block")(dev(a["q"]), dev(a["inv_scale"]), dev(b["q"]), dev(b["inv_scale"]),
-                                             out.t)
+    ia = a["inv_scale"].T if which in ("fwd", "dgrad") else a["inv_scale"]   # row-block scales block-major
+    getattr(fp8lin, f"fp8lin_{which}_block")(dev(a["q"]), dev(ia), dev(b["q"]), dev(b["inv_scale"]), out.t)
     torch.cuda.synchronize()
     assert fp8lin.fp8lin_device_error() == 0
     assert_gemm_close(bf16_to_f64(out.t), ref, f"{which} block {M}x{N}x{K}")
@@ -88,10 +94,12 @@ def test_block_gemm_matches_oracle(fp8lin, M, N, K, which):
 
 
 def _check_block_copies(name, lin, r):
-    got = {"x_k": (lin.x8.q, lin.x8.row_inv), "x_m": (lin.x8.qc, lin.x8.col_inv), "w": (lin.w8.q, lin.w8.tile_inv),
-           "dy_n": (lin.dy8.q, lin.dy8.row_inv), "dy_m": (lin.dy8.qc, lin.dy8.col_inv)}
+    got = {"x_k": (lin.x8.q, lin.x8.row_inv.t()), "x_m": (lin.x8.qc, lin.x8.col_inv),
+           "w": (lin.w8.q, lin.w8.tile_inv), "dy_n": (lin.dy8.q, lin.dy8.row_inv.t()),
+           "dy_m": (lin.dy8.qc, lin.dy8.col_inv)}
     for key, (q, inv) in got.items():
-        assert np.array_equal(inv.cpu().numpy().view(np.uint32), r[key]["inv_scale"].view(np.uint32)), f"{name} {key}"
+        assert np.array_equal(inv.contiguous().cpu().numpy().view(np.uint32), r[key]["inv_scale"].view(np.uint32)), \
+            f"{name} {key}"
         assert np.array_equal(q.cpu().numpy(), r[key]["q"]), f"{name} {key}"
 
 
