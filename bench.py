@@ -186,20 +186,38 @@ GEMM_SRC = os.path.join(ROOT, "float8_linear_layers_gb300", "csrc", "gemm.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fp8_gemm_tn_kernel__ffn8b_step_traffic.json")
 
 
+# The parts of the GEMM source the per-tensor kernel's traffic depends on:
+# the device code up to the block-scaled kernel (helpers, tile map, kernel)
+# and the host code from the raster to the per-tensor launch.
+GEMM_REGIONS = (("namespace {", "// ------------------------------------------------- block-scaled kernel"),
+                ("// Raster: keep", "std::atomic<bool> g_blk_attr_set"))
+
+
+def gemm_kernel_sha256(path: str = GEMM_SRC) -> str:
+    """SHA-256 over the per-tensor GEMM's device and host code (GEMM_REGIONS)."""
+    import hashlib
+    with open(path) as f:
+        text = f.read()
+    h = hashlib.sha256()
+    for start, end in GEMM_REGIONS:
+        i = text.index(start)
+        h.update(text[i:text.index(end, i)].encode())
+    return h.hexdigest()
+
+
 def gemm_traffic(workload: str, scaling: str):
     """Mean DRAM bytes per GEMM launch of one step of `workload`, from the
-    committed ncu capture of the per-tensor-scale GEMM; None when the GEMM
-    source changed since the counters were taken, no capture covers this
-    workload, or the step runs the row-wise- or block-scaled GEMM instead."""
-    import hashlib
+    committed ncu capture of the per-tensor-scale GEMM; None when that
+    kernel's source changed since the counters were taken, no capture covers
+    this workload, or the step runs the row-wise- or block-scaled GEMM
+    instead."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        with open(GEMM_SRC, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sha = gemm_kernel_sha256()
     except (OSError, ValueError):
         return None
-    if t.get("gemm_cu_sha256") != sha or t.get("workload") != workload or scaling in ("rowwise", "block"):
+    if t.get("gemm_kernel_sha256") != sha or t.get("workload") != workload or scaling in ("rowwise", "block"):
         return None
     return int(t["mean_dram_bytes_per_launch"])
 

@@ -77,3 +77,18 @@ def test_attainable_bound():
     # block scaling: one pass per tensor, two copies for activations and gradients, one for weights
     w_elems = 2 * 14336 * 4096 + 4096 * 14336
     assert bench.cast_bytes(ffn, "block") == 4 * (elems - w_elems) + 3 * w_elems
+
+
+def test_traffic_record_keys_on_the_per_tensor_kernel(tmp_path):
+    """The committed DRAM-traffic record stays valid across edits to the
+    block-scaled kernel and is voided by edits to the per-tensor kernel."""
+    src = open(bench.GEMM_SRC).read()
+    base = bench.gemm_kernel_sha256()
+    block = src.index("// ------------------------------------------------- block-scaled kernel")
+    edited_block = tmp_path / "block.cu"
+    edited_block.write_text(src[:block + 80] + "// edit\n" + src[block + 80:])
+    assert bench.gemm_kernel_sha256(str(edited_block)) == base
+    kern = src.index("fp8_gemm_tn_kernel(")
+    edited_kernel = tmp_path / "kernel.cu"
+    edited_kernel.write_text(src[:kern] + "/* edit */ " + src[kern:])
+    assert bench.gemm_kernel_sha256(str(edited_kernel)) != base
