@@ -298,6 +298,37 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The same wait, tied to the registers the load wrote, so that no use of
+// them can be scheduled above it while another load is in flight.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Asynchronous global -> shared copies (the scale ring of the block-scaled
+// GEMM): 16 bytes, of which the first src_bytes are read and the rest
+// zero-filled; 4 bytes; and an arrival on an mbarrier once every copy this
+// thread issued before it has landed (counted in the barrier's init count).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -598,11 +629,11 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 
 // Block scaling along the contraction: C[p][q] = sum over 128-long
 // contraction blocks j of (sum_{k in j} A[p][k] B[q][k])_fp32 * ia(p, j) * ib(q, j),
-// with ia(p, j) = inv_a[p * sa_p + j * sa_r] and ib(q, j) = inv_b[(q / 128) *
-// sb_q + j * sb_r], or inv_b[q * sb_q + j * sb_r] when B_COLS (one scale per
-// row of B, i.e. per output column).
+// with ia(p, j) = inv_a[j * sa_r + p] and ib(q, j) = inv_b[(q / 128) * sb_q +
+// j * sb_r], or inv_b[j * sb_r + q] when B_COLS (one scale per row of B, i.e.
+// per output column).
 //
-// One CTA per SM, persistent over 128 x 128 output tiles, 320 threads:
+// One CTA per SM, persistent over 128 x 128 output tiles, 352 threads:
 //   warp 0      TMA producer: per contraction block a 128 x 128-byte A slab
 //               and B slab into a 6-stage ring;
 //   warp 1      allocates all 512 TMEM columns: four 128 x 128 fp32 partial
@@ -611,13 +642,17 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 //               block, each block into its own buffer of the pair) and
 //               commits the pair;
 //   warps 2..9  promotion: warp w reads TMEM lanes 32 (w % 4) .. + 31,
-//               columns 64 ((w - 2) / 4) .. + 63 of a buffer (32 rows x 64
-//               columns, two 32-column loads in flight), multiplies by
-//               ia * ib and adds to 64 fp32 accumulators in registers, hands
-//               the pair back after its last block; after the tile's last
-//               block, rounds to bf16 and TMA-stores as the per-tensor
-//               epilogue does.
-// Ten warps leave each thread at most 168 registers (three warps share one
+//               columns 64 ((w - 2) / 4) .. + 63 of a buffer, 32 columns at a
+//               time with the next 32 in flight while the current ones are
+//               scaled by ia * ib and added to 64 fp32 accumulators in
+//               registers; hands the pair back after its last block; after
+//               the tile's last block, rounds to bf16 and TMA-stores as the
+//               per-tensor epilogue does;
+//   warp 10     scale loader: per contraction block the tile's 128 row scales
+//               of A and its B scale (or 128 column scales) into an 8-deep
+//               ring with asynchronous copies, so that no promotion warp ever
+//               waits on a global load.
+// Eleven warps leave each thread at most 168 registers (three warps share one
 // sub-partition's 16K); two buffer pairs let the MMAs of blocks j + 2, j + 3
 // run while blocks j, j + 1 are promoted, and eight MMAs per wait keep the
 // issuer's waits and commits covered.
@@ -625,37 +660,63 @@ constexpr int kBlkTile = 128;                         // output rows and columns
 constexpr int kBlkStages = 6;
 constexpr int kBlkSlab = kBlkTile * kBK;              // 16 KB: one operand slab of one contraction block
 constexpr int kBlkStage = 2 * kBlkSlab;               // A + B
-constexpr int kBlkThreads = 320;
 constexpr int kBlkPromoWarps = 8;
+constexpr int kBlkScaleWarp = 2 + kBlkPromoWarps;
+constexpr int kBlkThreads = 32 * (kBlkScaleWarp + 1);
+constexpr int kBlkMaxRegs = 168;                      // 3 warps x 32 threads x 168 <= 16K per sub-partition
 constexpr int kBlkWarpCols = 64;                      // columns each promotion warp owns
 constexpr int kBlkTmemCols = 4 * kBlkTile;
 constexpr int kBlkEpiBytes = kBlkPromoWarps * kEpiBuf;
-constexpr int kBlkColScaleBytes = kBlkPromoWarps * kBlkWarpCols * 4;  // per-column scales of one block, per warp
+constexpr int kBlkScaleSlots = 8;                     // contraction blocks of scales in flight
+constexpr int kBlkSlotFloats = 2 * kBlkTile;          // row scales of A, then B's scale(s)
+constexpr int kBlkScaleBytes = kBlkScaleSlots * kBlkSlotFloats * 4;
 constexpr int kBlkSmemBytes =
-    kBlkStages * kBlkStage + kBlkEpiBytes + kBlkColScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+    kBlkStages * kBlkStage + kBlkEpiBytes + kBlkScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 static_assert(kBlkSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
 static_assert(kBlkTmemCols <= 512, "TMEM holds 512 columns");
 static_assert(kBlkStages % 2 == 0, "slabs are consumed two at a time");
+static_assert(kBlkThreads / 32 <= 12 && kBlkMaxRegs * 32 * ((kBlkThreads / 32 + 3) / 4) <= 16384,
+              "registers of the warps that share a sub-partition");
+
+// The promotion of 32 partial sums of one row: acc += p * sab, or with
+// per-column scales acc += (p * col[j]) * sab.
+template <bool B_COLS>
+__device__ __forceinline__ void promote32(float *acc, const uint32_t (&p)[32], float sab, const float *col) {
+    if (B_COLS) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const float4 b = reinterpret_cast<const float4 *>(col)[g];
+            acc[4 * g + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 0]), b.x), sab, acc[4 * g + 0]);
+            acc[4 * g + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 1]), b.y), sab, acc[4 * g + 1]);
+            acc[4 * g + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 2]), b.z), sab, acc[4 * g + 2]);
+            acc[4 * g + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 3]), b.w), sab, acc[4 * g + 3]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(__uint_as_float(p[j]), sab, acc[j]);
+    }
+}
 
 template <bool A_MN, bool B_MN, bool B_COLS>
-__global__ void __launch_bounds__(kBlkThreads, 1)
+__global__ void __maxnreg__(kBlkMaxRegs)
 fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_c, int P, int Q, int R,
-                      const float *__restrict__ inv_a, long long sa_p, long long sa_r,
-                      const float *__restrict__ inv_b, long long sb_q, long long sb_r, uint32_t idesc,
-                      TileMap tiles) {
+                      const float *__restrict__ inv_a, long long sa_r, const float *__restrict__ inv_b,
+                      long long sb_q, long long sb_r, uint32_t idesc, TileMap tiles) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *ring = smem;                               // [stages][A slab, B slab]
     uint8_t *sC = ring + kBlkStages * kBlkStage;        // epilogue staging: [8 warps][32 rows x 64 B]
-    float *sCol = reinterpret_cast<float *>(sC + kBlkEpiBytes);  // [8 warps][64] column scales (B_COLS)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sCol + kBlkPromoWarps * kBlkWarpCols);
+    float *sScale = reinterpret_cast<float *>(sC + kBlkEpiBytes);  // [slots][A rows 128, B 128 (or 1)]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kBlkScaleSlots * kBlkSlotFloats);
     uint64_t *full = bars;                              // [stages] slabs landed
     uint64_t *empty = bars + kBlkStages;                // [stages] MMAs done with the slabs
     uint64_t *pfull = bars + 2 * kBlkStages;            // [2] partial sums of a buffer pair ready
     uint64_t *pempty = pfull + 2;                       // [2] the promotion warps have read them
-    uint64_t *mma_done = pempty + 2;
+    uint64_t *sfull = pempty + 2;                       // [slots] a block's scales landed
+    uint64_t *sempty = sfull + kBlkScaleSlots;          // [slots] the promotion warps are done with them
+    uint64_t *mma_done = sempty + kBlkScaleSlots;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -668,6 +729,10 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&pfull[b]), 1);
             mbar_init(smem_u32(&pempty[b]), kBlkPromoWarps);
+        }
+        for (int s = 0; s < kBlkScaleSlots; ++s) {
+            mbar_init(smem_u32(&sfull[s]), 32);         // one asynchronous arrival per loader lane
+            mbar_init(smem_u32(&sempty[s]), kBlkPromoWarps);
         }
         mbar_init(smem_u32(mma_done), 1);
         *abort_flag = 0;
@@ -779,120 +844,78 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
             volatile int no_abort = 0;
             mbar_wait(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
         }
-    } else {
+    } else if (warp < kBlkScaleWarp) {
         // ------------------------------------------------ promotion + epilogue
         const int sub = warp % 4;          // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows
         const int cw = (warp - 2) / 4;     // which 64-column half of the tile
+        const int srow = sub * 32 + lane;  // this thread's row within the tile
         uint8_t *stage_c = sC + (warp - 2) * kEpiBuf;
         uint8_t *dst = stage_c + lane * (kEpiCols * 2);
-        float *col_scale = sCol + (warp - 2) * kBlkWarpCols;
-        int pair = 0;
-        uint32_t pphase = 0;
+        const uint32_t tlane = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(cw * kBlkWarpCols);
+        int pair = 0, slot = 0;
+        uint32_t pphase = 0, sphase = 0;
         bool ok = true;
-        // The scales of block j + 1 are loaded while block j is promoted (the
-        // next tile's first block after a tile's last): sa = this row's A
-        // scale, sb = the B block's scale or, with B_COLS, four column scales
-        // per lane 0..15.
-        auto load_scales = [&](int row_, int col_base_, int kb_, float &sa_o, float &sb_o, float4 &cv_o) {
-            sa_o = row_ < P ? __ldg(inv_a + row_ * sa_p + kb_ * sa_r) : 0.0f;
-            if (B_COLS) {
-                const int c4 = col_base_ + 4 * lane;
-                cv_o = (lane < kBlkWarpCols / 4 && c4 < Q)
-                           ? __ldg(reinterpret_cast<const float4 *>(inv_b + (long long)c4 * sb_q + kb_ * sb_r))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
-                sb_o = col_base_ < Q ? __ldg(inv_b + (long long)(col_base_ / kBlkTile) * sb_q + kb_ * sb_r) : 0.0f;
-            }
-        };
-        auto bases = [&](int t_, int &row_, int &col_base_) {
-            int tm_, tn_;
-            tiles.coords(t_, tm_, tn_);
-            row_ = tm_ * kBlkTile + sub * 32 + lane;
-            col_base_ = tn_ * kBlkTile + cw * kBlkWarpCols;
-        };
-        float sa_c = 0.0f, sb_c = 0.0f;
-        float4 cv_c = make_float4(0.f, 0.f, 0.f, 0.f);
-        if ((int)blockIdx.x < num_tiles) {
-            int r_, c_;
-            bases(blockIdx.x, r_, c_);
-            load_scales(r_, c_, 0, sa_c, sb_c, cv_c);
-        }
+        uint32_t x[32], y[32];             // columns 0..31 and 32..63 of the warp's part of a block
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int tm, tn;
             tiles.coords(t, tm, tn);
             const int row0 = tm * kBlkTile + sub * 32;
-            const int row = row0 + lane;
             const int col_base = tn * kBlkTile + cw * kBlkWarpCols;   // first output column of this warp
-            const int t_next = t + (int)gridDim.x;
-            int row_next = 0, col_next = 0;
-            if (t_next < num_tiles) bases(t_next, row_next, col_next);
             float acc[kBlkWarpCols];
 #pragma unroll
             for (int j = 0; j < kBlkWarpCols; ++j) acc[j] = 0.0f;
-            for (int kb0 = 0; kb0 < num_kb && ok; kb0 += 2) {
-                const int n = min(2, num_kb - kb0);
-                const bool ready = mbar_wait(smem_u32(&pfull[pair]), pphase, abort_flag, kWaitLimitNs);
-                if (!__all_sync(0xFFFFFFFFu, ready)) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&pfull[pair]), pphase, abort_flag, kWaitLimitNs))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_ld_32x32b_x32(tlane + (uint32_t)(pair * 2 * kBlkTile), x);
+            tmem_ld_wait_regs(x);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                // x holds columns 0..31 of block kb; its scales
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait(smem_u32(&sfull[slot]), sphase, abort_flag, kWaitLimitNs))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                for (int i = 0; i < n; ++i) {
-                    const int kb = kb0 + i;
-                    float sa_n = 0.0f, sb_n = 0.0f;
-                    float4 cv_n = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (kb + 1 < num_kb)
-                        load_scales(row, col_base, kb + 1, sa_n, sb_n, cv_n);
-                    else if (t_next < num_tiles)
-                        load_scales(row_next, col_next, 0, sa_n, sb_n, cv_n);
-                    float sab = sa_c;
-                    if (B_COLS) {
-                        __syncwarp();   // the previous block's reads of col_scale are done
-                        if (lane < kBlkWarpCols / 4) reinterpret_cast<float4 *>(col_scale)[lane] = cv_c;
-                        __syncwarp();
-                    } else {
-                        sab = __fmul_rn(sa_c, sb_c);
+                const float *sc = sScale + slot * kBlkSlotFloats;
+                const float sab = B_COLS ? sc[srow] : __fmul_rn(sc[srow], sc[kBlkTile]);
+                const float *col = sc + kBlkTile + cw * kBlkWarpCols;
+                const int i = kb & 1;
+                const bool last_of_pair = i == 1 || kb + 1 == num_kb;
+                tmem_ld_32x32b_x32(tlane + (uint32_t)((pair * 2 + i) * kBlkTile + 32), y);
+                promote32<B_COLS>(acc, x, sab, col);
+                tmem_ld_wait_regs(y);
+                if (last_of_pair) {
+                    // the warp's part of the pair is in registers: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(smem_u32(&pempty[pair]));
+                    if (++pair == 2) {
+                        pair = 0;
+                        pphase ^= 1u;
                     }
-                    const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) +
-                                           (uint32_t)((pair * 2 + i) * kBlkTile + cw * kBlkWarpCols);
-                    uint32_t r0[32], r1[32];
-                    tmem_ld_32x32b_x32(tbase, r0);
-                    tmem_ld_32x32b_x32(tbase + 32u, r1);
-                    tmem_ld_wait();
-                    if (i == n - 1) {
-                        // the warp's part of the pair is in registers: hand it back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_local(smem_u32(&pempty[pair]));
-                    }
-                    if (B_COLS) {
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            const float4 b0 = reinterpret_cast<const float4 *>(col_scale)[g];
-                            const float4 b1 = reinterpret_cast<const float4 *>(col_scale)[8 + g];
-                            r0[4 * g + 0] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 0]), b0.x));
-                            r0[4 * g + 1] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 1]), b0.y));
-                            r0[4 * g + 2] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 2]), b0.z));
-                            r0[4 * g + 3] = __float_as_uint(__fmul_rn(__uint_as_float(r0[4 * g + 3]), b0.w));
-                            r1[4 * g + 0] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 0]), b1.x));
-                            r1[4 * g + 1] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 1]), b1.y));
-                            r1[4 * g + 2] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 2]), b1.z));
-                            r1[4 * g + 3] = __float_as_uint(__fmul_rn(__uint_as_float(r1[4 * g + 3]), b1.w));
+                }
+                const bool more = kb + 1 < num_kb;
+                if (more) {
+                    if (last_of_pair) {
+                        if (!__all_sync(0xFFFFFFFFu,
+                                        mbar_wait(smem_u32(&pfull[pair]), pphase, abort_flag, kWaitLimitNs))) {
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after();
                     }
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        acc[j] = __fmaf_rn(__uint_as_float(r0[j]), sab, acc[j]);
-                        acc[32 + j] = __fmaf_rn(__uint_as_float(r1[j]), sab, acc[32 + j]);
-                    }
-                    sa_c = sa_n;
-                    sb_c = sb_n;
-                    cv_c = cv_n;
+                    tmem_ld_32x32b_x32(tlane + (uint32_t)((pair * 2 + (i ^ 1)) * kBlkTile), x);
                 }
-                if (++pair == 2) {
-                    pair = 0;
-                    pphase ^= 1u;
+                promote32<B_COLS>(acc + 32, y, sab, col + 32);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(smem_u32(&sempty[slot]));
+                if (++slot == kBlkScaleSlots) {
+                    slot = 0;
+                    sphase ^= 1u;
                 }
+                if (more) tmem_ld_wait_regs(x);
             }
             if (!ok) break;
             // epilogue: round to bf16, stage 32 columns at a time, TMA-store
@@ -921,6 +944,40 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+    } else {
+        // ------------------------------------------------ scale loader
+        // Lane l copies rows 4l .. 4l + 3 of the tile (16 bytes; rows past P
+        // zero-filled without a read) and, with B_COLS, columns 4l .. 4l + 3;
+        // otherwise lane 0 copies the B block's one scale.
+        int slot = 0;
+        uint32_t sphase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tiles.coords(t, tm, tn);
+            const int r = tm * kBlkTile + 4 * lane, c = tn * kBlkTile + 4 * lane;
+            const bool r_in = r < P, c_in = c < Q;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait(smem_u32(&sempty[slot]), sphase ^ 1u, abort_flag, kWaitLimitNs))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t s = smem_u32(sScale + slot * kBlkSlotFloats);
+                cp_async_16(s + 16u * lane, r_in ? inv_a + (long long)kb * sa_r + r : inv_a, r_in ? 16u : 0u);
+                if (B_COLS)
+                    cp_async_16(s + 4u * kBlkTile + 16u * lane, c_in ? inv_b + (long long)kb * sb_r + c : inv_b,
+                                c_in ? 16u : 0u);
+                else if (lane == 0)
+                    cp_async_4(s + 4u * kBlkTile, inv_b + (long long)tn * sb_q + (long long)kb * sb_r);
+                cp_async_arrive_noinc(smem_u32(&sfull[slot]));
+                if (++slot == kBlkScaleSlots) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
+            }
+        }
+        cp_async_wait_all();
     }
 
     tc_fence_before();
@@ -1146,16 +1203,19 @@ std::atomic<bool> g_blk_attr_set[8][64];
 std::atomic<int> g_blk_ctas[8][64];
 
 // The block-scaled GEMM (see fp8_gemm_block_kernel): inverse scales of A at
-// inv_a[p * sa_p + j * sa_r], of B at inv_b[(q / 128) * sb_q + j * sb_r] (or
-// [q * sb_q + j * sb_r] when B_COLS); sizes are the caller's to guarantee.
+// inv_a[j * sa_r + p], of B at inv_b[(q / 128) * sb_q + j * sb_r] (or
+// [j * sb_r + q] when B_COLS); sizes are the caller's to guarantee.  The
+// scale loader copies four consecutive rows' (columns') scales at a time, so
+// those vectors are 16-byte aligned with strides that are multiples of 4.
 template <bool A_MN, bool B_MN, bool B_COLS>
-fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, int64_t sa_p, int64_t sa_r,
-                         const uint8_t *B, fp8lin_fmt fb, const float *inv_b, int64_t sb_q, int64_t sb_r, void *C,
-                         int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
+fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, int64_t sa_r, const uint8_t *B,
+                         fp8lin_fmt fb, const float *inv_b, int64_t sb_q, int64_t sb_r, void *C, int64_t P,
+                         int64_t Q, int64_t R, cudaStream_t stream) {
     using namespace fp8lin;
     fp8lin_status st = gemm_checks(A, inv_a, B, inv_b, C, P, Q, R);
     if (st != FP8LIN_OK) return st;
-    if (B_COLS && !aligned(inv_b, 16)) return FP8LIN_ERR_MISALIGNED;
+    if (!aligned(inv_a, 16) || sa_r % 4 || (B_COLS && (!aligned(inv_b, 16) || sb_r % 4)))
+        return FP8LIN_ERR_MISALIGNED;
     DeviceInfo dev;
     st = current_device(&dev);
     if (st != FP8LIN_OK) return st;
@@ -1182,7 +1242,7 @@ fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, in
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlkThreads, kBlkSmemBytes) !=
                 cudaSuccess ||
             per_sm < 1)
-            per_sm = 1;
+            return FP8LIN_ERR_CUDA;   // e.g. a build whose register count does not fit three warps per sub-partition
         g_blk_ctas[inst][dev.device].store(per_sm * dev.sm_count, std::memory_order_relaxed);
         g_blk_attr_set[inst][dev.device].store(true, std::memory_order_release);
     }
@@ -1192,8 +1252,8 @@ fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, in
     const int grid = num_tiles < max_ctas ? num_tiles : max_ctas;
     const uint32_t idesc = make_idesc(fa, fb, A_MN, B_MN, kBlkTile, kBlkTile);
     kernel<<<grid, kBlkThreads, kBlkSmemBytes, stream>>>(map_a, map_b, map_c, (int)P, (int)Q, (int)R, inv_a,
-                                                         (long long)sa_p, (long long)sa_r, inv_b, (long long)sb_q,
-                                                         (long long)sb_r, idesc, tm);
+                                                         (long long)sa_r, inv_b, (long long)sb_q, (long long)sb_r,
+                                                         idesc, tm);
     return check_launch();
 }
 
@@ -1208,7 +1268,7 @@ extern "C" fp8lin_status fp8lin_fwd_block(const uint8_t *xq, const float *inv_x,
                                           cudaStream_t stream) {
     // A = Xq (row blocks, inv_x [KB x M]), B = Wq (tiles, inv_w [NB x KB]); contraction K
     const int64_t kb = ceil_div(K, kBlkTile);
-    return gemm_block<false, false, false>(xq, FP8LIN_E4M3, inv_x, 1, M, wq, FP8LIN_E4M3, inv_w, kb, 1, y, M, N,
+    return gemm_block<false, false, false>(xq, FP8LIN_E4M3, inv_x, M, wq, FP8LIN_E4M3, inv_w, kb, 1, y, M, N,
                                            K, stream);
 }
 
@@ -1218,7 +1278,7 @@ extern "C" fp8lin_status fp8lin_dgrad_block(const uint8_t *dyq, const float *inv
     // A = dYq (row blocks, inv_dy [NB x M]), B = Wq read MN-major: row k of B,
     // contraction block j scaled by inv_w[j][k / 128]; contraction N
     const int64_t kb = ceil_div(K, kBlkTile);
-    return gemm_block<false, true, false>(dyq, FP8LIN_E5M2, inv_dy, 1, M, wq, FP8LIN_E4M3, inv_w, 1, kb, dx, M, K,
+    return gemm_block<false, true, false>(dyq, FP8LIN_E5M2, inv_dy, M, wq, FP8LIN_E4M3, inv_w, 1, kb, dx, M, K,
                                           N, stream);
 }
 
@@ -1227,7 +1287,7 @@ extern "C" fp8lin_status fp8lin_wgrad_block(const uint8_t *dyq, const float *inv
                                             cudaStream_t stream) {
     // A = dYq read MN-major (column blocks: row n of A, block j at inv_dy[j][n]),
     // B = Xq read MN-major (column blocks: row k of B, block j at inv_x[j][k]); contraction M
-    return gemm_block<true, true, true>(dyq, FP8LIN_E5M2, inv_dy, 1, N, xq, FP8LIN_E4M3, inv_x, 1, K, dw, N, K, M,
+    return gemm_block<true, true, true>(dyq, FP8LIN_E5M2, inv_dy, N, xq, FP8LIN_E4M3, inv_x, 1, K, dw, N, K, M,
                                         stream);
 }
 

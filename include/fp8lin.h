@@ -324,10 +324,12 @@ fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int64_t cols, f
  * fp8lin_dgrad_block: dyq = q_row of dY [M x N] e5m2, inv_dy [ceil(N/128) x M];
  *                     wq, inv_w as for the forward.
  * fp8lin_wgrad_block: dyq = q_col of dY [M x N] e5m2, inv_dy [ceil(M/128) x N];
- *                     xq = q_col of X [M x K] e4m3, inv_x [ceil(M/128) x K]
- *                     (16-byte aligned).
- * Outputs bf16 row-major, 16-byte aligned, fully overwritten.  Pointers,
- * shapes and errors otherwise as for fp8lin_fwd.
+ *                     xq = q_col of X [M x K] e4m3, inv_x [ceil(M/128) x K].
+ * The scales of the row and column blocks (inv_x, inv_dy; for the weight
+ * gradient both) are read four rows at a time and must be 16-byte aligned
+ * (FP8LIN_ERR_MISALIGNED otherwise); inv_w needs 4 bytes.  Outputs bf16
+ * row-major, 16-byte aligned, fully overwritten.  Pointers, shapes and
+ * errors otherwise as for fp8lin_fwd.
  */
 fp8lin_status fp8lin_fwd_block(const uint8_t *xq, const float *inv_x, const uint8_t *wq,
                                const float *inv_w, void *y, int64_t M, int64_t N, int64_t K,

@@ -135,7 +135,10 @@ def test_argument_checks_of_mn_and_block_entry_points(lib):
         assert fn(a16, a16, a4, a16, a16, 128, 128, 128, None) == 2, name
         assert fn(a16, a16, a16, a16, a4, 128, 128, 128, None) == 2, name
         assert fn(a16, a16, a16, a16, a16, 136, 128, 128, None) == 3, name
-    # the weight-gradient block GEMM reads its column scales as float4s
+    # the block GEMMs read the row (and column) block scales four at a time
+    for name in ("fp8lin_fwd_block", "fp8lin_dgrad_block", "fp8lin_wgrad_block"):
+        assert getattr(lib, name)(a16, V(4100), a16, a16, a16, 128, 128, 128, None) == 2, name
+    assert lib.fp8lin_fwd_block(a16, a16, a16, V(4100), a16, 128, 128, 128, None) != 2   # inv_w: 4 bytes
     fn = lib.fp8lin_wgrad_block
     assert fn(a16, a16, a16, V(4100), a16, 128, 128, 128, None) == 2
     # block cast: each copy with its scales, at least one copy, formats, alignment, shapes
