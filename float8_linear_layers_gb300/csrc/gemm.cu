@@ -43,9 +43,9 @@
 // raster groups chosen from the operand sizes (see TileMap), so that the
 // smaller operand is read from DRAM once when it fits in L2.
 //
-// The block-scaled GEMM (fp8_gemm_block_kernel, further down) runs one CTA
-// per SM on 128 x 128 tiles and scales every 128-long contraction block's
-// partial sums on the CUDA cores.
+// The block-scaled GEMM (fp8_gemm_block_kernel, further down) runs on the
+// same CTA pairs and 256 x 256 tiles and scales every 128-long contraction
+// block's partial sums on the CUDA cores.
 //
 // Every mbarrier wait is bounded by wall-clock time (globaltimer).  A wait
 // that runs out records FP8LIN_ERR_TIMEOUT in a device word, raises the
@@ -150,6 +150,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, limit);
 }
 
+// The same wait entirely inline, for code after setmaxnreg: a call there
+// would have to follow the caller's changed register budget.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              unsigned long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            *abort_flag = 1;
+            atomicOr(&g_device_error, 1u << FP8LIN_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -208,6 +225,15 @@ __device__ __forceinline__ void cluster_sync() {
 // Arrive on an mbarrier of either CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// The same arrival without release semantics, for a consumer that hands back
+// TMEM it has finished reading (tcgen05.wait::ld has returned and
+// tcgen05.fence::before_thread_sync orders the reads before the arrival):
+// it publishes no memory, and a release at cluster scope costs the arriving
+// warp hundreds of cycles.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is signalled on an
@@ -633,50 +659,63 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 // j * sb_r], or inv_b[j * sb_r + q] when B_COLS (one scale per row of B, i.e.
 // per output column).
 //
-// One CTA per SM, persistent over 128 x 128 output tiles, 352 threads:
-//   warp 0      TMA producer: per contraction block a 128 x 128-byte A slab
-//               and B slab into a 6-stage ring;
-//   warp 1      allocates all 512 TMEM columns: four 128 x 128 fp32 partial
-//               buffers, used as two pairs; one thread issues the MMAs of two
-//               contraction blocks at a time (M 128, N 128, K 32; four per
-//               block, each block into its own buffer of the pair) and
-//               commits the pair;
-//   warps 2..9  promotion: warp w reads TMEM lanes 32 (w % 4) .. + 31,
-//               columns 64 ((w - 2) / 4) .. + 63 of a buffer, 32 columns at a
-//               time with the next 32 in flight while the current ones are
-//               scaled by ia * ib and added to 64 fp32 accumulators in
-//               registers; hands the pair back after its last block; after
-//               the tile's last block, rounds to bf16 and TMA-stores as the
-//               per-tensor epilogue does;
-//   warp 10     scale loader: per contraction block the tile's 128 row scales
-//               of A and its B scale (or 128 column scales) into an 8-deep
-//               ring with asynchronous copies, so that no promotion warp ever
-//               waits on a global load.
-// Eleven warps leave each thread at most 168 registers (three warps share one
-// sub-partition's 16K); two buffer pairs let the MMAs of blocks j + 2, j + 3
-// run while blocks j, j + 1 are promoted, and eight MMAs per wait keep the
-// issuer's waits and commits covered.
-constexpr int kBlkTile = 128;                         // output rows and columns per tile; contraction block
-constexpr int kBlkStages = 6;
-constexpr int kBlkSlab = kBlkTile * kBK;              // 16 KB: one operand slab of one contraction block
-constexpr int kBlkStage = 2 * kBlkSlab;               // A + B
+// The tensor cores cannot accumulate across contraction blocks (every
+// block's partial sum needs its own scales), so each block's MMAs write a
+// fresh fp32 partial into TMEM and the CUDA cores promote it: scale and add
+// into accumulators held in registers.  Clusters of two CTAs, persistent
+// over 256 x 256 output tiles as the per-tensor kernel (cta_group::2 MMAs of
+// M 256, N 256, K 32: half the shared-memory and L2 traffic per flop of a
+// one-SM 128 x 128 tile), 384 threads per CTA:
+//   warpgroup 0 (40 registers after setmaxnreg.dec)
+//     warp 0    TMA producer: this CTA's A and B slabs of each block into a
+//               6-stage ring, completing on the leader's barrier;
+//     warp 1    allocates 512 TMEM columns with the peer: two 128 x 256 fp32
+//               partial buffers; in the leader one thread issues each
+//               block's four MMAs into a free buffer and multicasts the
+//               commits to both CTAs;
+//     warp 2    scale loader: per block this CTA's 128 row scales of A and
+//               the tile's two B scales (or 256 column scales) into an
+//               8-deep ring, with asynchronous copies;
+//     warp 3    idle;
+//   warpgroups 1, 2 (232 registers after setmaxnreg.inc)
+//     warps 4..11 promotion: warp w reads TMEM lanes 32 (w % 4) .. + 31,
+//               columns 128 ((w - 4) / 4) .. + 127 of the buffer, 32 columns
+//               at a time with the next 32 in flight, scales them and adds
+//               them to 128 fp32 accumulators; hands the buffer back to the
+//               leader once its last columns are in registers; after the
+//               tile's last block, rounds to bf16 and TMA-stores as the
+//               per-tensor epilogue does.
+// The register split is 128 x 40 + 256 x 232 = 64512 = 384 x 168, the
+// registers the CTA is launched with (the host checks the compiled count
+// before launching).  The two partial buffers let the MMAs of block j + 1 run
+// while block j is promoted.
+constexpr int kBlk = 128;                             // contraction block and scale block of the recipe
+constexpr int kBlkThreads = 384;
+constexpr int kBlkLaunchRegs = 168;
+constexpr int kBlkLowRegs = 40;
+constexpr int kBlkHighRegs = 232;
+static_assert(128 * kBlkLowRegs + 256 * kBlkHighRegs == kBlkThreads * kBlkLaunchRegs,
+              "the register split must add up to the launch allocation");
 constexpr int kBlkPromoWarps = 8;
-constexpr int kBlkScaleWarp = 2 + kBlkPromoWarps;
-constexpr int kBlkThreads = 32 * (kBlkScaleWarp + 1);
-constexpr int kBlkMaxRegs = 168;                      // 3 warps x 32 threads x 168 <= 16K per sub-partition
-constexpr int kBlkWarpCols = 64;                      // columns each promotion warp owns
-constexpr int kBlkTmemCols = 4 * kBlkTile;
+constexpr int kBlkWarpCols = 128;                     // columns each promotion warp owns
+constexpr int kBlkTmemCols = 2 * kPairN;
 constexpr int kBlkEpiBytes = kBlkPromoWarps * kEpiBuf;
 constexpr int kBlkScaleSlots = 8;                     // contraction blocks of scales in flight
-constexpr int kBlkSlotFloats = 2 * kBlkTile;          // row scales of A, then B's scale(s)
+constexpr int kBlkSlotFloats = kBM + kPairN;          // this CTA's row scales of A, then B's scales
 constexpr int kBlkScaleBytes = kBlkScaleSlots * kBlkSlotFloats * 4;
 constexpr int kBlkSmemBytes =
-    kBlkStages * kBlkStage + kBlkEpiBytes + kBlkScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+    kStages * (kAStage + kBStage) + kBlkEpiBytes + kBlkScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 static_assert(kBlkSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
-static_assert(kBlkTmemCols <= 512, "TMEM holds 512 columns");
-static_assert(kBlkStages % 2 == 0, "slabs are consumed two at a time");
-static_assert(kBlkThreads / 32 <= 12 && kBlkMaxRegs * 32 * ((kBlkThreads / 32 + 3) / 4) <= 16384,
-              "registers of the warps that share a sub-partition");
+static_assert(kBK == kBlk && kBlkWarpCols == kBlk, "a slab is one contraction block; a warp's columns one B block");
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // The promotion of 32 partial sums of one row: acc += p * sab, or with
 // per-column scales acc += (p * col[j]) * sab.
@@ -698,7 +737,7 @@ __device__ __forceinline__ void promote32(float *acc, const uint32_t (&p)[32], f
 }
 
 template <bool A_MN, bool B_MN, bool B_COLS>
-__global__ void __maxnreg__(kBlkMaxRegs)
+__global__ void __launch_bounds__(kBlkThreads, 1)
 fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_c, int P, int Q, int R,
                       const float *__restrict__ inv_a, long long sa_r, const float *__restrict__ inv_b,
@@ -706,14 +745,15 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *ring = smem;                               // [stages][A slab, B slab]
-    uint8_t *sC = ring + kBlkStages * kBlkStage;        // epilogue staging: [8 warps][32 rows x 64 B]
-    float *sScale = reinterpret_cast<float *>(sC + kBlkEpiBytes);  // [slots][A rows 128, B 128 (or 1)]
+    uint8_t *sA = smem;                                 // [stages][128 x 128 B]
+    uint8_t *sB = smem + kStages * kAStage;             // [stages][128 x 128 B]
+    uint8_t *sC = sB + kStages * kBStage;               // epilogue staging: [8 warps][32 rows x 64 B]
+    float *sScale = reinterpret_cast<float *>(sC + kBlkEpiBytes);  // [slots][A rows 128, B 256 (or 2)]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kBlkScaleSlots * kBlkSlotFloats);
-    uint64_t *full = bars;                              // [stages] slabs landed
-    uint64_t *empty = bars + kBlkStages;                // [stages] MMAs done with the slabs
-    uint64_t *pfull = bars + 2 * kBlkStages;            // [2] partial sums of a buffer pair ready
-    uint64_t *pempty = pfull + 2;                       // [2] the promotion warps have read them
+    uint64_t *full = bars;                              // [stages] both CTAs' slabs landed (leader's copy used)
+    uint64_t *empty = bars + kStages;                   // [stages] the pair's MMAs are done with the slabs
+    uint64_t *pfull = bars + 2 * kStages;               // [2] a partial buffer is complete (in both CTAs)
+    uint64_t *pempty = pfull + 2;                       // [2] both CTAs' promotion warps read it (leader's copy)
     uint64_t *sfull = pempty + 2;                       // [slots] a block's scales landed
     uint64_t *sempty = sfull + kBlkScaleSlots;          // [slots] the promotion warps are done with them
     uint64_t *mma_done = sempty + kBlkScaleSlots;
@@ -721,14 +761,17 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kBlkStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&pfull[b]), 1);
-            mbar_init(smem_u32(&pempty[b]), kBlkPromoWarps);
+            mbar_init(smem_u32(&pempty[b]), 2 * kBlkPromoWarps);  // eight warps in each CTA of the pair
         }
         for (int s = 0; s < kBlkScaleSlots; ++s) {
             mbar_init(smem_u32(&sfull[s]), 32);         // one asynchronous arrival per loader lane
@@ -745,176 +788,224 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         prefetch_tensormap(&map_c);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
                      "r"(kBlkTmemCols)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int num_tiles = tiles.tiles_m * tiles.tiles_n;
     const int num_kb = (R + kBK - 1) / kBK;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp < 4) {
+        setmaxnreg_dec<kBlkLowRegs>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
-            for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+            for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
-                const int a_row = tm * kBlkTile, b_row = tn * kBlkTile;
+                const int a_row = tm * kPairM + (int)rank * kBM;
+                const int b_row = tn * kPairN + (int)rank * kBN;
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
-                    const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_arrive_expect_tx(fb, kBlkStage);
-                    const uint32_t dst = smem_u32(ring + stage * kBlkStage);
-                    if (A_MN) tma_load_2d(dst, &map_a, fb, a_row, kb * kBK);
-                    else      tma_load_2d(dst, &map_a, fb, kb * kBK, a_row);
-                    if (B_MN) tma_load_2d(dst + kBlkSlab, &map_b, fb, b_row, kb * kBK);
-                    else      tma_load_2d(dst + kBlkSlab, &map_b, fb, kb * kBK, b_row);
+                    if (!mbar_wait_inl(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
+                    const uint32_t fb_local = smem_u32(&full[stage]);
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
+                    const uint32_t fb = mapa_shared(fb_local, 0);
+                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
+                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
+                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
+                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kBlkStages) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (*abort_flag) {
-                // let every copy land before the CTA exits
-                for (int s = 0; s < kBlkStages; ++s)
+            if (*abort_flag && leader) {
+                // let every copy of the pair land before either CTA exits
+                for (int s = 0; s < kStages; ++s)
                     if (armed & (1u << s))
-                        mbar_wait(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
+                        mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (leader CTA)
             int stage = 0;
             uint32_t phase = 0;
-            int pair = 0;
+            int pb = 0;
             uint32_t pphase = 0;
-            const uint64_t desc0 = sw128_kmajor_desc(smem_u32(ring));
+            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok && !*abort_flag; t += gridDim.x) {
-                for (int kb = 0; kb < num_kb; kb += 2) {
-                    const int n = min(2, num_kb - kb);
-                    if (!mbar_wait(smem_u32(&pempty[pair]), pphase ^ 1u, abort_flag, kWaitLimitNs)) {
+            for (int t = pair; t < num_tiles && ok && !*abort_flag; t += npairs) {
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_inl(smem_u32(&pempty[pb]), pphase ^ 1u, abort_flag, kWaitLimitNs) ||
+                        !mbar_wait_inl(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    int st = stage;
-                    uint32_t ph = phase;
-                    for (int i = 0; i < n && ok; ++i) {
-                        if (!mbar_wait(smem_u32(&full[st]), ph, abort_flag, kWaitLimitNs)) ok = false;
-                        if (++st == kBlkStages) {
-                            st = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
                     tc_fence_after();
-                    for (int i = 0; i < n; ++i) {
-                        const uint64_t a_desc = desc0 + (uint64_t)(stage * (kBlkStage >> 4));
-                        const uint64_t b_desc = a_desc + (uint64_t)(kBlkSlab >> 4);
-                        const uint32_t d_tmem = tmem_base + (uint32_t)((pair * 2 + i) * kBlkTile);
+                    const uint64_t a_desc = a_desc0 + (uint64_t)(stage * (kAStage >> 4));
+                    const uint64_t b_desc = b_desc0 + (uint64_t)(stage * (kBStage >> 4));
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(pb * kPairN);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k)
-                            umma_f8f6f4_single(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc,
-                                               k != 0 ? 1u : 0u);
-                        umma_commit_single(smem_u32(&empty[stage]));
-                        if (++stage == kBlkStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    for (int k = 0; k < kBK / kUmmaK; ++k)
+                        umma_f8f6f4_pair(d_tmem, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k), idesc,
+                                         k != 0 ? 1u : 0u);
+                    umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
+                    umma_commit_multicast(smem_u32(&pfull[pb]), 0x3);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
-                    umma_commit_single(smem_u32(&pfull[pair]));
-                    if (++pair == 2) {
-                        pair = 0;
+                    if (++pb == 2) {
+                        pb = 0;
                         pphase ^= 1u;
                     }
                 }
             }
-            umma_commit_single(smem_u32(mma_done));
+            // every MMA issued above has completed once this arrives
+            umma_commit_multicast(smem_u32(mma_done), 0x1);
             volatile int no_abort = 0;
-            mbar_wait(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
+            mbar_wait_inl(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
+        } else if (warp == 2) {
+            // ------------------------------------------------ scale loader (both CTAs)
+            // Lane l copies this CTA's rows 4l .. 4l + 3 of the tile (16
+            // bytes; rows past P zero-filled without a read) and, with
+            // B_COLS, columns 4l .. 4l + 3 and 128 + 4l .. 128 + 4l + 3;
+            // otherwise lanes 0, 1 copy the scales of the tile's two B blocks
+            // (the last block of B repeated past Q, where every partial sum
+            // is zero).
+            int slot = 0;
+            uint32_t sphase = 0;
+            bool ok = true;
+            const long long last_qb = (long long)(Q - 1) / kBlk;
+            for (int t = pair; t < num_tiles && ok; t += npairs) {
+                int tm, tn;
+                tiles.coords(t, tm, tn);
+                const int r = tm * kPairM + (int)rank * kBM + 4 * lane, c = tn * kPairN + 4 * lane;
+                const bool r_in = r < P, c0_in = c < Q, c1_in = c + kBlk < Q;
+                const long long qb = min((long long)(2 * tn + (lane & 1)), last_qb);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait_inl(smem_u32(&sempty[slot]), sphase ^ 1u, abort_flag,
+                                                               kWaitLimitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t s = smem_u32(sScale + slot * kBlkSlotFloats);
+                    cp_async_16(s + 16u * lane, r_in ? inv_a + (long long)kb * sa_r + r : inv_a, r_in ? 16u : 0u);
+                    if (B_COLS) {
+                        const float *b = inv_b + (long long)kb * sb_r + c;
+                        cp_async_16(s + 4u * kBM + 16u * lane, c0_in ? b : inv_b, c0_in ? 16u : 0u);
+                        cp_async_16(s + 4u * (kBM + kBlk) + 16u * lane, c1_in ? b + kBlk : inv_b, c1_in ? 16u : 0u);
+                    } else if (lane < 2) {
+                        cp_async_4(s + 4u * (kBM + lane), inv_b + qb * sb_q + (long long)kb * sb_r);
+                    }
+                    cp_async_arrive_noinc(smem_u32(&sfull[slot]));
+                    if (++slot == kBlkScaleSlots) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
+                }
+            }
+            cp_async_wait_all();
         }
-    } else if (warp < kBlkScaleWarp) {
-        // ------------------------------------------------ promotion + epilogue
+    } else {
+        setmaxnreg_inc<kBlkHighRegs>();
+        // ------------------------------------------------ promotion + epilogue (warps 4..11, both CTAs)
         const int sub = warp % 4;          // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows
-        const int cw = (warp - 2) / 4;     // which 64-column half of the tile
-        const int srow = sub * 32 + lane;  // this thread's row within the tile
-        uint8_t *stage_c = sC + (warp - 2) * kEpiBuf;
+        const int cw = (warp - 4) / 4;     // which 128-column half of the pair tile
+        const int srow = sub * 32 + lane;  // this thread's row within the CTA's 128
+        uint8_t *stage_c = sC + (warp - 4) * kEpiBuf;
         uint8_t *dst = stage_c + lane * (kEpiCols * 2);
+        const uint32_t pempty_leader0 = mapa_shared(smem_u32(&pempty[0]), 0);
+        const uint32_t pempty_leader1 = mapa_shared(smem_u32(&pempty[1]), 0);
         const uint32_t tlane = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(cw * kBlkWarpCols);
-        int pair = 0, slot = 0;
+        int pb = 0, slot = 0;
         uint32_t pphase = 0, sphase = 0;
         bool ok = true;
-        uint32_t x[32], y[32];             // columns 0..31 and 32..63 of the warp's part of a block
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        uint32_t x[32], y[32];             // alternate 32-column chunks of the warp's 128
+        // A block's scales, read from the ring one block ahead of their use:
+        // sab = row scale (times the B block's scale), col = column scales.
+        auto scales = [&](int slot_, float &sab_, const float *&col_) -> bool {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_inl(smem_u32(&sfull[slot_]), sphase ^ (slot_ < slot ? 1u : 0u),
+                                                       abort_flag, kWaitLimitNs)))
+                return false;
+            const float *sc = sScale + slot_ * kBlkSlotFloats;
+            sab_ = B_COLS ? sc[srow] : __fmul_rn(sc[srow], sc[kBM + cw]);
+            col_ = sc + kBM + cw * kBlkWarpCols;
+            return true;
+        };
+        for (int t = pair; t < num_tiles && ok; t += npairs) {
             int tm, tn;
             tiles.coords(t, tm, tn);
-            const int row0 = tm * kBlkTile + sub * 32;
-            const int col_base = tn * kBlkTile + cw * kBlkWarpCols;   // first output column of this warp
+            const int row0 = tm * kPairM + (int)rank * kBM + sub * 32;
+            const int col_base = tn * kPairN + cw * kBlkWarpCols;   // first output column of this warp
             float acc[kBlkWarpCols];
 #pragma unroll
             for (int j = 0; j < kBlkWarpCols; ++j) acc[j] = 0.0f;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&pfull[pair]), pphase, abort_flag, kWaitLimitNs))) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_inl(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            tmem_ld_32x32b_x32(tlane + (uint32_t)(pair * 2 * kBlkTile), x);
+            tmem_ld_32x32b_x32(tlane + (uint32_t)(pb * kPairN), x);
+            float sab;
+            const float *col;
+            ok = scales(slot, sab, col);
             tmem_ld_wait_regs(x);
+            if (!ok) break;
             for (int kb = 0; kb < num_kb; ++kb) {
-                // x holds columns 0..31 of block kb; its scales
-                if (!__all_sync(0xFFFFFFFFu,
-                                mbar_wait(smem_u32(&sfull[slot]), sphase, abort_flag, kWaitLimitNs))) {
-                    ok = false;
-                    break;
-                }
-                const float *sc = sScale + slot * kBlkSlotFloats;
-                const float sab = B_COLS ? sc[srow] : __fmul_rn(sc[srow], sc[kBlkTile]);
-                const float *col = sc + kBlkTile + cw * kBlkWarpCols;
-                const int i = kb & 1;
-                const bool last_of_pair = i == 1 || kb + 1 == num_kb;
-                tmem_ld_32x32b_x32(tlane + (uint32_t)((pair * 2 + i) * kBlkTile + 32), y);
+                // x holds columns 0..31 of block kb's buffer; sab, col its scales
+                const uint32_t tb = tlane + (uint32_t)(pb * kPairN);
+                tmem_ld_32x32b_x32(tb + 32u, y);
                 promote32<B_COLS>(acc, x, sab, col);
                 tmem_ld_wait_regs(y);
-                if (last_of_pair) {
-                    // the warp's part of the pair is in registers: hand it back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_local(smem_u32(&pempty[pair]));
-                    if (++pair == 2) {
-                        pair = 0;
-                        pphase ^= 1u;
-                    }
+                tmem_ld_32x32b_x32(tb + 64u, x);
+                promote32<B_COLS>(acc + 32, y, sab, col + 32);
+                tmem_ld_wait_regs(x);
+                tmem_ld_32x32b_x32(tb + 96u, y);
+                promote32<B_COLS>(acc + 64, x, sab, col + 64);
+                tmem_ld_wait_regs(y);
+                // the warp's part of the buffer is in registers: hand it back to the leader
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(pb ? pempty_leader1 : pempty_leader0);
+                if (++pb == 2) {
+                    pb = 0;
+                    pphase ^= 1u;
                 }
                 const bool more = kb + 1 < num_kb;
+                const int next_slot = slot + 1 == kBlkScaleSlots ? 0 : slot + 1;
+                float sab_n = 0.0f;
+                const float *col_n = col;
                 if (more) {
-                    if (last_of_pair) {
-                        if (!__all_sync(0xFFFFFFFFu,
-                                        mbar_wait(smem_u32(&pfull[pair]), pphase, abort_flag, kWaitLimitNs))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                    if (!__all_sync(0xFFFFFFFFu,
+                                    mbar_wait_inl(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs)) ||
+                        !scales(next_slot, sab_n, col_n)) {
+                        ok = false;
+                        break;
                     }
-                    tmem_ld_32x32b_x32(tlane + (uint32_t)((pair * 2 + (i ^ 1)) * kBlkTile), x);
+                    tc_fence_after();
+                    tmem_ld_32x32b_x32(tlane + (uint32_t)(pb * kPairN), x);
                 }
-                promote32<B_COLS>(acc + 32, y, sab, col + 32);
+                promote32<B_COLS>(acc + 96, y, sab, col + 96);
                 __syncwarp();
                 if (lane == 0) mbar_arrive_local(smem_u32(&sempty[slot]));
-                if (++slot == kBlkScaleSlots) {
-                    slot = 0;
-                    sphase ^= 1u;
-                }
+                slot = next_slot;
+                if (slot == 0) sphase ^= 1u;
+                sab = sab_n;
+                col = col_n;
                 if (more) tmem_ld_wait_regs(x);
             }
             if (!ok) break;
@@ -944,48 +1035,15 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
-    } else {
-        // ------------------------------------------------ scale loader
-        // Lane l copies rows 4l .. 4l + 3 of the tile (16 bytes; rows past P
-        // zero-filled without a read) and, with B_COLS, columns 4l .. 4l + 3;
-        // otherwise lane 0 copies the B block's one scale.
-        int slot = 0;
-        uint32_t sphase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            int tm, tn;
-            tiles.coords(t, tm, tn);
-            const int r = tm * kBlkTile + 4 * lane, c = tn * kBlkTile + 4 * lane;
-            const bool r_in = r < P, c_in = c < Q;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (!__all_sync(0xFFFFFFFFu,
-                                mbar_wait(smem_u32(&sempty[slot]), sphase ^ 1u, abort_flag, kWaitLimitNs))) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t s = smem_u32(sScale + slot * kBlkSlotFloats);
-                cp_async_16(s + 16u * lane, r_in ? inv_a + (long long)kb * sa_r + r : inv_a, r_in ? 16u : 0u);
-                if (B_COLS)
-                    cp_async_16(s + 4u * kBlkTile + 16u * lane, c_in ? inv_b + (long long)kb * sb_r + c : inv_b,
-                                c_in ? 16u : 0u);
-                else if (lane == 0)
-                    cp_async_4(s + 4u * kBlkTile, inv_b + (long long)tn * sb_q + (long long)kb * sb_r);
-                cp_async_arrive_noinc(smem_u32(&sfull[slot]));
-                if (++slot == kBlkScaleSlots) {
-                    slot = 0;
-                    sphase ^= 1u;
-                }
-            }
-        }
-        cp_async_wait_all();
     }
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // neither CTA frees TMEM or exits while the pair still uses its shared memory
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kBlkTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kBlkTmemCols)
                      : "memory");
     }
 }
@@ -1224,36 +1282,48 @@ fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, in
         return cudaMemsetAsync(C, 0, (size_t)P * (size_t)Q * 2, stream) == cudaSuccess ? FP8LIN_OK
                                                                                        : FP8LIN_ERR_CUDA;
     }
-    const int64_t tiles_m = (P + kBlkTile - 1) / kBlkTile, tiles_n = (Q + kBlkTile - 1) / kBlkTile;
+    const int64_t tiles_m = (P + kPairM - 1) / kPairM, tiles_n = (Q + kPairN - 1) / kPairN;
     if (tiles_m * tiles_n > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
     CUtensorMap map_a, map_b, map_c;
-    const bool ok_a = A_MN ? make_operand_map_mn(&map_a, A, P, R, kBlkTile) : make_operand_map(&map_a, A, P, R, kBlkTile);
-    const bool ok_b = B_MN ? make_operand_map_mn(&map_b, B, Q, R, kBlkTile) : make_operand_map(&map_b, B, Q, R, kBlkTile);
+    const bool ok_a = A_MN ? make_operand_map_mn(&map_a, A, P, R, kBM) : make_operand_map(&map_a, A, P, R, kBM);
+    const bool ok_b = B_MN ? make_operand_map_mn(&map_b, B, Q, R, kBN) : make_operand_map(&map_b, B, Q, R, kBN);
     if (!ok_a || !ok_b || !make_output_map(&map_c, C, P, Q)) return FP8LIN_ERR_CUDA;
     if (dev.device >= 64) return FP8LIN_ERR_CUDA;
     constexpr int inst = A_MN * 4 + B_MN * 2 + B_COLS;
     auto kernel = fp8_gemm_block_kernel<A_MN, B_MN, B_COLS>;
+    cudaLaunchAttribute attr;
+    auto config = [&](int grid, cudaStream_t s) {
+        cudaLaunchConfig_t cfg = launch_config(grid, s, &attr);
+        cfg.blockDim = dim3(kBlkThreads, 1, 1);
+        cfg.dynamicSmemBytes = kBlkSmemBytes;
+        return cfg;
+    };
     if (!g_blk_attr_set[inst][dev.device].load(std::memory_order_acquire)) {
+        // The register split assumes the compiled count; with any other
+        // count setmaxnreg.inc could wait forever, so never launch it then.
+        cudaFuncAttributes fa_attr;
+        if (cudaFuncGetAttributes(&fa_attr, kernel) != cudaSuccess) return FP8LIN_ERR_CUDA;
+        if (fa_attr.numRegs != kBlkLaunchRegs) return FP8LIN_ERR_CUDA;
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBlkSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return FP8LIN_ERR_CUDA;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlkThreads, kBlkSmemBytes) !=
-                cudaSuccess ||
-            per_sm < 1)
-            return FP8LIN_ERR_CUDA;   // e.g. a build whose register count does not fit three warps per sub-partition
-        g_blk_ctas[inst][dev.device].store(per_sm * dev.sm_count, std::memory_order_relaxed);
+        int clusters = 0;
+        cudaLaunchConfig_t cfg = config(2 * (dev.sm_count / 2), nullptr);
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1)
+            return FP8LIN_ERR_CUDA;
+        g_blk_ctas[inst][dev.device].store(clusters, std::memory_order_relaxed);
         g_blk_attr_set[inst][dev.device].store(true, std::memory_order_release);
     }
     const TileMap tm = raster(P, Q, R, tiles_m, tiles_n);
     const int num_tiles = (int)(tiles_m * tiles_n);
-    const int max_ctas = g_blk_ctas[inst][dev.device].load(std::memory_order_relaxed);
-    const int grid = num_tiles < max_ctas ? num_tiles : max_ctas;
-    const uint32_t idesc = make_idesc(fa, fb, A_MN, B_MN, kBlkTile, kBlkTile);
-    kernel<<<grid, kBlkThreads, kBlkSmemBytes, stream>>>(map_a, map_b, map_c, (int)P, (int)Q, (int)R, inv_a,
-                                                         (long long)sa_r, inv_b, (long long)sb_q, (long long)sb_r,
-                                                         idesc, tm);
+    const int max_pairs = g_blk_ctas[inst][dev.device].load(std::memory_order_relaxed);
+    const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
+    cudaLaunchConfig_t cfg = config(2 * pairs, stream);
+    const uint32_t idesc = make_idesc(fa, fb, A_MN, B_MN);
+    if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, map_c, (int)P, (int)Q, (int)R, inv_a, (long long)sa_r, inv_b,
+                           (long long)sb_q, (long long)sb_r, idesc, tm) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
     return check_launch();
 }
 
@@ -1267,7 +1337,7 @@ extern "C" fp8lin_status fp8lin_fwd_block(const uint8_t *xq, const float *inv_x,
                                           const float *inv_w, void *y, int64_t M, int64_t N, int64_t K,
                                           cudaStream_t stream) {
     // A = Xq (row blocks, inv_x [KB x M]), B = Wq (tiles, inv_w [NB x KB]); contraction K
-    const int64_t kb = ceil_div(K, kBlkTile);
+    const int64_t kb = ceil_div(K, kBlk);
     return gemm_block<false, false, false>(xq, FP8LIN_E4M3, inv_x, M, wq, FP8LIN_E4M3, inv_w, kb, 1, y, M, N,
                                            K, stream);
 }
@@ -1277,7 +1347,7 @@ extern "C" fp8lin_status fp8lin_dgrad_block(const uint8_t *dyq, const float *inv
                                             cudaStream_t stream) {
     // A = dYq (row blocks, inv_dy [NB x M]), B = Wq read MN-major: row k of B,
     // contraction block j scaled by inv_w[j][k / 128]; contraction N
-    const int64_t kb = ceil_div(K, kBlkTile);
+    const int64_t kb = ceil_div(K, kBlk);
     return gemm_block<false, true, false>(dyq, FP8LIN_E5M2, inv_dy, M, wq, FP8LIN_E4M3, inv_w, 1, kb, dx, M, K,
                                           N, stream);
 }
