@@ -717,22 +717,46 @@ __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Two lanes of fp32 at once (fma.rn.f32x2 / mul.rn.f32x2: each lane rounded
+// once, as the scalar instructions): acc += p * s, and p * c.
+__device__ __forceinline__ void fma2(float &acc0, float &acc1, float p0, float p1, float s0, float s1) {
+    asm("{\n\t.reg .b64 a, p, s;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 p, {%2, %3};\n\t"
+        "mov.b64 s, {%4, %5};\n\t"
+        "fma.rn.f32x2 a, p, s, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "f"(p0), "f"(p1), "f"(s0), "f"(s1));
+}
+__device__ __forceinline__ void mul2(float &r0, float &r1, float p0, float p1, float c0, float c1) {
+    asm("{\n\t.reg .b64 r, p, c;\n\t"
+        "mov.b64 p, {%2, %3};\n\t"
+        "mov.b64 c, {%4, %5};\n\t"
+        "mul.rn.f32x2 r, p, c;\n\t"
+        "mov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(p0), "f"(p1), "f"(c0), "f"(c1));
+}
+
 // The promotion of 32 partial sums of one row: acc += p * sab, or with
-// per-column scales acc += (p * col[j]) * sab.
+// per-column scales acc += (p * col[j]) * sab; two columns per instruction.
 template <bool B_COLS>
 __device__ __forceinline__ void promote32(float *acc, const uint32_t (&p)[32], float sab, const float *col) {
     if (B_COLS) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
             const float4 b = reinterpret_cast<const float4 *>(col)[g];
-            acc[4 * g + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 0]), b.x), sab, acc[4 * g + 0]);
-            acc[4 * g + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 1]), b.y), sab, acc[4 * g + 1]);
-            acc[4 * g + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 2]), b.z), sab, acc[4 * g + 2]);
-            acc[4 * g + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(p[4 * g + 3]), b.w), sab, acc[4 * g + 3]);
+            float q0, q1, q2, q3;
+            mul2(q0, q1, __uint_as_float(p[4 * g + 0]), __uint_as_float(p[4 * g + 1]), b.x, b.y);
+            mul2(q2, q3, __uint_as_float(p[4 * g + 2]), __uint_as_float(p[4 * g + 3]), b.z, b.w);
+            fma2(acc[4 * g + 0], acc[4 * g + 1], q0, q1, sab, sab);
+            fma2(acc[4 * g + 2], acc[4 * g + 3], q2, q3, sab, sab);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(__uint_as_float(p[j]), sab, acc[j]);
+        for (int j = 0; j < 32; j += 2)
+            fma2(acc[j], acc[j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]), sab, sab);
     }
 }
 
