@@ -337,6 +337,14 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait_regs64(uint32_t (&r)[64]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) :: "memory");
+}
+
+
 // Asynchronous global -> shared copies (the scale ring of the block-scaled
 // GEMM): 16 bytes, of which the first src_bytes are read and the rest
 // zero-filled; 4 bytes; and an arrival on an mbarrier once every copy this
@@ -679,12 +687,15 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 //     warp 3    idle;
 //   warpgroups 1, 2 (232 registers after setmaxnreg.inc)
 //     warps 4..11 promotion: warp w reads TMEM lanes 32 (w % 4) .. + 31,
-//               columns 128 ((w - 4) / 4) .. + 127 of the buffer, 32 columns
-//               at a time with the next 32 in flight, scales them and adds
-//               them to 128 fp32 accumulators; hands the buffer back to the
-//               leader once its last columns are in registers; after the
-//               tile's last block, rounds to bf16 and TMA-stores as the
-//               per-tensor epilogue does.
+//               columns 128 ((w - 4) / 4) .. + 127 of the buffer (64 columns
+//               per load, or with column scales 32 with the next 32 in
+//               flight), scales them and adds them to 128 fp32 accumulators
+//               (two columns per fma.rn.f32x2); hands the buffer back to the
+//               leader once its last columns are in registers, with a
+//               relaxed arrival (a release at cluster scope costs each warp
+//               more than the block's arithmetic); after the tile's last
+//               block, rounds to bf16 and TMA-stores as the per-tensor
+//               epilogue does.
 // The register split is 128 x 40 + 256 x 232 = 64512 = 384 x 168, the
 // registers the CTA is launched with (the host checks the compiled count
 // before launching).  The two partial buffers let the MMAs of block j + 1 run
@@ -758,6 +769,12 @@ __device__ __forceinline__ void promote32(float *acc, const uint32_t (&p)[32], f
         for (int j = 0; j < 32; j += 2)
             fma2(acc[j], acc[j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]), sab, sab);
     }
+}
+
+template <bool B_COLS>
+__device__ __forceinline__ void promote64(float *acc, const uint32_t (&p)[64], float sab, const float *col) {
+    promote32<B_COLS>(acc, reinterpret_cast<const uint32_t (&)[32]>(p[0]), sab, col);
+    promote32<B_COLS>(acc + 32, reinterpret_cast<const uint32_t (&)[32]>(p[32]), sab, col + 32);
 }
 
 template <bool A_MN, bool B_MN, bool B_COLS>
@@ -958,7 +975,11 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         int pb = 0, slot = 0;
         uint32_t pphase = 0, sphase = 0;
         bool ok = true;
-        uint32_t x[32], y[32];             // alternate 32-column chunks of the warp's 128
+        // Partial sums come out of TMEM 64 columns per load, or, with column
+        // scales (whose shared-memory reads need registers of their own), 32
+        // at a time with the next 32 in flight.
+        uint32_t x[32], y[32];
+        uint32_t x64[64];
         // A block's scales, read from the ring one block ahead of their use:
         // sab = row scale (times the B block's scale), col = column scales.
         auto scales = [&](int slot_, float &sab_, const float *&col_) -> bool {
@@ -983,54 +1004,100 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                 break;
             }
             tc_fence_after();
-            tmem_ld_32x32b_x32(tlane + (uint32_t)(pb * kPairN), x);
-            float sab;
-            const float *col;
-            ok = scales(slot, sab, col);
-            tmem_ld_wait_regs(x);
-            if (!ok) break;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                // x holds columns 0..31 of block kb's buffer; sab, col its scales
-                const uint32_t tb = tlane + (uint32_t)(pb * kPairN);
-                tmem_ld_32x32b_x32(tb + 32u, y);
-                promote32<B_COLS>(acc, x, sab, col);
-                tmem_ld_wait_regs(y);
-                tmem_ld_32x32b_x32(tb + 64u, x);
-                promote32<B_COLS>(acc + 32, y, sab, col + 32);
+            if constexpr (B_COLS) {
+                tmem_ld_32x32b_x32(tlane + (uint32_t)(pb * kPairN), x);
+                float sab;
+                const float *col;
+                ok = scales(slot, sab, col);
                 tmem_ld_wait_regs(x);
-                tmem_ld_32x32b_x32(tb + 96u, y);
-                promote32<B_COLS>(acc + 64, x, sab, col + 64);
-                tmem_ld_wait_regs(y);
-                // the warp's part of the buffer is in registers: hand it back to the leader
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_relaxed(pb ? pempty_leader1 : pempty_leader0);
-                if (++pb == 2) {
-                    pb = 0;
-                    pphase ^= 1u;
-                }
-                const bool more = kb + 1 < num_kb;
-                const int next_slot = slot + 1 == kBlkScaleSlots ? 0 : slot + 1;
-                float sab_n = 0.0f;
-                const float *col_n = col;
-                if (more) {
-                    if (!__all_sync(0xFFFFFFFFu,
-                                    mbar_wait_inl(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs)) ||
-                        !scales(next_slot, sab_n, col_n)) {
-                        ok = false;
-                        break;
+                if (!ok) break;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    // x holds columns 0..31 of block kb's buffer; sab, col its scales
+                    const uint32_t tb = tlane + (uint32_t)(pb * kPairN);
+                    tmem_ld_32x32b_x32(tb + 32u, y);
+                    promote32<B_COLS>(acc, x, sab, col);
+                    tmem_ld_wait_regs(y);
+                    tmem_ld_32x32b_x32(tb + 64u, x);
+                    promote32<B_COLS>(acc + 32, y, sab, col + 32);
+                    tmem_ld_wait_regs(x);
+                    tmem_ld_32x32b_x32(tb + 96u, y);
+                    promote32<B_COLS>(acc + 64, x, sab, col + 64);
+                    tmem_ld_wait_regs(y);
+                    // the warp's part of the buffer is in registers: hand it back to the leader
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(pb ? pempty_leader1 : pempty_leader0);
+                    if (++pb == 2) {
+                        pb = 0;
+                        pphase ^= 1u;
                     }
-                    tc_fence_after();
-                    tmem_ld_32x32b_x32(tlane + (uint32_t)(pb * kPairN), x);
+                    const bool more = kb + 1 < num_kb;
+                    const int next_slot = slot + 1 == kBlkScaleSlots ? 0 : slot + 1;
+                    float sab_n = 0.0f;
+                    const float *col_n = col;
+                    if (more) {
+                        if (!__all_sync(0xFFFFFFFFu,
+                                        mbar_wait_inl(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs)) ||
+                            !scales(next_slot, sab_n, col_n)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        tmem_ld_32x32b_x32(tlane + (uint32_t)(pb * kPairN), x);
+                    }
+                    promote32<B_COLS>(acc + 96, y, sab, col + 96);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(smem_u32(&sempty[slot]));
+                    slot = next_slot;
+                    if (slot == 0) sphase ^= 1u;
+                    sab = sab_n;
+                    col = col_n;
+                    if (more) tmem_ld_wait_regs(x);
                 }
-                promote32<B_COLS>(acc + 96, y, sab, col + 96);
-                __syncwarp();
-                if (lane == 0) mbar_arrive_local(smem_u32(&sempty[slot]));
-                slot = next_slot;
-                if (slot == 0) sphase ^= 1u;
-                sab = sab_n;
-                col = col_n;
-                if (more) tmem_ld_wait_regs(x);
+            } else {
+                tmem_ld_32x32b_x64(tlane + (uint32_t)(pb * kPairN), x64);
+                float sab;
+                const float *col;
+                ok = scales(slot, sab, col);
+                tmem_ld_wait_regs64(x64);
+                if (!ok) break;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    // x64 holds columns 0..63 of block kb's buffer; sab, col its scales
+                    const uint32_t tb = tlane + (uint32_t)(pb * kPairN);
+                    promote64<B_COLS>(acc, x64, sab, col);
+                    tmem_ld_32x32b_x64(tb + 64u, x64);
+                    tmem_ld_wait_regs64(x64);
+                    // the warp's part of the buffer is in registers: hand it back to the leader
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(pb ? pempty_leader1 : pempty_leader0);
+                    if (++pb == 2) {
+                        pb = 0;
+                        pphase ^= 1u;
+                    }
+                    const bool more = kb + 1 < num_kb;
+                    const int next_slot = slot + 1 == kBlkScaleSlots ? 0 : slot + 1;
+                    float sab_n = 0.0f;
+                    const float *col_n = col;
+                    promote64<B_COLS>(acc + 64, x64, sab, col + 64);
+                    if (more) {
+                        if (!__all_sync(0xFFFFFFFFu,
+                                        mbar_wait_inl(smem_u32(&pfull[pb]), pphase, abort_flag, kWaitLimitNs)) ||
+                            !scales(next_slot, sab_n, col_n)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        tmem_ld_32x32b_x64(tlane + (uint32_t)(pb * kPairN), x64);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(smem_u32(&sempty[slot]));
+                    slot = next_slot;
+                    if (slot == 0) sphase ^= 1u;
+                    sab = sab_n;
+                    col = col_n;
+                    if (more) tmem_ld_wait_regs64(x64);
+                }
             }
             if (!ok) break;
             // epilogue: round to bf16, stage 32 columns at a time, TMA-store
