@@ -63,7 +63,10 @@ def test_block_cast_zero_tensor_and_arguments(fp8lin):
         fp8lin.fp8lin_cast_blockwise(x, E4M3)                     # nothing asked for
 
 
-GEMM_SHAPES = [(128, 128, 128), (144, 272, 208), (384, 1040, 4112), (1040, 400, 96), (2048, 2048, 2048)]
+# (M, N, K): ragged pair tiles in every direction, a contraction shorter than
+# one block, 16-row and 16-column outputs (one pair tile mostly past the edge)
+GEMM_SHAPES = [(128, 128, 128), (144, 272, 208), (384, 1040, 4112), (1040, 400, 96), (2048, 2048, 2048),
+               (16, 16, 16), (16, 528, 144), (272, 16, 400)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
