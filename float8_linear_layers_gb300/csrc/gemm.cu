@@ -622,6 +622,10 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Wait until at most one of this thread's committed bulk stores still reads
+// shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // tcgen05.wait::ld tied to the registers a load wrote (32 or 64 columns), so
 // that no use of them can be scheduled above it while another load is in
 // flight.
@@ -733,12 +737,13 @@ static_assert(128 * kBlkLowRegs + 256 * kBlkHighRegs == kBlkThreads * kBlkLaunch
 constexpr int kBlkPromoWarps = 8;
 constexpr int kBlkWarpCols = 128;                     // columns each promotion warp owns
 constexpr int kBlkTmemCols = 2 * kPairN;
-constexpr int kBlkEpiBytes = kBlkPromoWarps * kEpiBuf;
+constexpr int kBlkStages = 5;                         // slab ring: about five blocks of lookahead
+constexpr int kBlkEpiBytes = kBlkPromoWarps * 2 * kEpiBuf;  // two staging buffers per promotion warp
 constexpr int kBlkScaleSlots = 8;                     // contraction blocks of scales in flight
 constexpr int kBlkSlotFloats = kBM + kPairN;          // this CTA's row scales of A, then B's scales
 constexpr int kBlkScaleBytes = kBlkScaleSlots * kBlkSlotFloats * 4;
 constexpr int kBlkSmemBytes =
-    kStages * (kAStage + kBStage) + kBlkEpiBytes + kBlkScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+    kBlkStages * (kAStage + kBStage) + kBlkEpiBytes + kBlkScaleBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 static_assert(kBlkSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
 static_assert(kBK == kBlk && kBlkWarpCols == kBlk, "a slab is one contraction block; a warp's columns one B block");
 
@@ -810,13 +815,13 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *sA = smem;                                 // [stages][128 x 128 B]
-    uint8_t *sB = smem + kStages * kAStage;             // [stages][128 x 128 B]
-    uint8_t *sC = sB + kStages * kBStage;               // epilogue staging: [8 warps][32 rows x 64 B]
+    uint8_t *sB = smem + kBlkStages * kAStage;          // [stages][128 x 128 B]
+    uint8_t *sC = sB + kBlkStages * kBStage;            // epilogue staging: [8 warps][2][32 rows x 64 B]
     float *sScale = reinterpret_cast<float *>(sC + kBlkEpiBytes);  // [slots][A rows 128, B 256 (or 2)]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sScale + kBlkScaleSlots * kBlkSlotFloats);
     uint64_t *full = bars;                              // [stages] both CTAs' slabs landed (leader's copy used)
-    uint64_t *empty = bars + kStages;                   // [stages] the pair's MMAs are done with the slabs
-    uint64_t *pfull = bars + 2 * kStages;               // [2] a partial buffer is complete (in both CTAs)
+    uint64_t *empty = bars + kBlkStages;                // [stages] the pair's MMAs are done with the slabs
+    uint64_t *pfull = bars + 2 * kBlkStages;               // [2] a partial buffer is complete (in both CTAs)
     uint64_t *pempty = pfull + 2;                       // [2] both CTAs' promotion warps read it (leader's copy)
     uint64_t *sfull = pempty + 2;                       // [slots] a block's scales landed
     uint64_t *sempty = sfull + kBlkScaleSlots;          // [slots] the promotion warps are done with them
@@ -829,7 +834,7 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kBlkStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -890,7 +895,7 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                     else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
+                    if (++stage == kBlkStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -898,7 +903,7 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
             }
             if (*abort_flag && leader) {
                 // let every copy of the pair land before either CTA exits
-                for (int s = 0; s < kStages; ++s)
+                for (int s = 0; s < kBlkStages; ++s)
                     if (armed & (1u << s))
                         mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
             }
@@ -928,7 +933,7 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                                          k != 0 ? 1u : 0u);
                     umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
                     umma_commit_multicast(smem_u32(&pfull[pb]), 0x3);
-                    if (++stage == kStages) {
+                    if (++stage == kBlkStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -990,8 +995,7 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
         const int sub = warp % 4;          // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows
         const int cw = (warp - 4) / 4;     // which 128-column half of the pair tile
         const int srow = sub * 32 + lane;  // this thread's row within the CTA's 128
-        uint8_t *stage_c = sC + (warp - 4) * kEpiBuf;
-        uint8_t *dst = stage_c + lane * (kEpiCols * 2);
+        uint8_t *stage_c = sC + (warp - 4) * 2 * kEpiBuf;  // two buffers, alternate 32-column blocks
         const uint32_t pempty_leader0 = mapa_shared(smem_u32(&pempty[0]), 0);
         const uint32_t pempty_leader1 = mapa_shared(smem_u32(&pempty[1]), 0);
         const uint32_t tlane = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(cw * kBlkWarpCols);
@@ -1123,12 +1127,18 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                 }
             }
             if (!ok) break;
-            // epilogue: round to bf16, stage 32 columns at a time, TMA-store
+            // epilogue: round to bf16 and TMA-store 32 columns at a time from
+            // two alternating staging buffers; the blocks past the output's
+            // edge (a suffix of the four) are neither staged nor stored
+            if (lane == 0) bulk_wait_read_0();   // the previous tile's stores are done reading
 #pragma unroll
             for (int c = 0; c < kBlkWarpCols / kEpiCols; ++c) {
                 const int col0 = col_base + c * kEpiCols;
-                if (lane == 0) bulk_wait_read_0();
+                if (row0 >= P || col0 >= Q) break;
+                uint8_t *buf = stage_c + (c & 1) * kEpiBuf;
+                if (c >= 2 && lane == 0) bulk_wait_read_1();   // the store of block c - 2 (same buffer) has read it
                 __syncwarp();
+                uint8_t *dst = buf + lane * (kEpiCols * 2);
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const int j = c * kEpiCols + 8 * g;
@@ -1141,8 +1151,8 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0 && row0 < P && col0 < Q) {
-                    tma_store_2d(&map_c, smem_u32(stage_c), col0, row0);
+                if (lane == 0) {
+                    tma_store_2d(&map_c, smem_u32(buf), col0, row0);
                     bulk_commit_group();
                 }
             }
