@@ -543,3 +543,7 @@ class Float8Linear:
 
     # kernels one step launches (amax x3, cast x3, three GEMMs)
     KERNELS_PER_STEP = 9
+
+
+# the autograd / nn.Module front end (imports the names above)
+from .nn import Float8LinearFunction, Float8LinearModule, swap_linear_layers  # noqa: E402

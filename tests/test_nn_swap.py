@@ -1,0 +1,50 @@
+"""The nn.Linear swap of the autograd front end (CPU: construction and module
+surgery only, no kernel runs)."""
+import pytest
+import torch
+
+import float8_linear_layers_gb300 as fl
+
+
+def _lin(i, o, bias=False, dtype=torch.bfloat16):
+    return torch.nn.Linear(i, o, bias=bias, dtype=dtype)
+
+
+def test_swap_replaces_only_eligible_linears_and_shares_weights():
+    eligible, biased, ragged, fp32 = _lin(64, 128), _lin(128, 48, bias=True), _lin(48, 40), _lin(48, 32, dtype=torch.float32)
+    nested = _lin(32, 16)
+    model = torch.nn.Sequential(eligible, torch.nn.ReLU(), biased, ragged, fp32, torch.nn.Sequential(nested))
+    w0, w5 = eligible.weight, nested.weight
+    out = fl.swap_linear_layers(model, scaling="block")
+    assert out is model
+    assert isinstance(model[0], fl.Float8LinearModule) and model[0].weight is w0 and model[0].scaling == "block"
+    assert isinstance(model[5][0], fl.Float8LinearModule) and model[5][0].weight is w5
+    assert model[2] is biased and model[3] is ragged and model[4] is fp32
+    # the swapped weight is still the model's parameter (an optimizer keeps updating it)
+    assert sum(p is w0 for p in model.parameters()) == 1
+
+
+def test_swap_filter_and_a_bare_linear():
+    model = torch.nn.Sequential(_lin(64, 64), _lin(64, 64))
+    fl.swap_linear_layers(model, module_filter=lambda fqn, m: fqn != "1")
+    assert isinstance(model[0], fl.Float8LinearModule) and type(model[1]) is torch.nn.Linear
+    bare = _lin(32, 48)
+    swapped = fl.swap_linear_layers(bare)
+    assert isinstance(swapped, fl.Float8LinearModule) and swapped.weight is bare.weight
+    assert (swapped.in_features, swapped.out_features) == (32, 48)
+
+
+def test_module_and_function_arguments():
+    m = fl.Float8LinearModule(32, 48)
+    assert m.weight.dtype == torch.bfloat16 and tuple(m.weight.shape) == (48, 32)
+    assert m.weight.abs().max() <= 1 / 32 ** 0.5 + 1e-6     # nn.Linear's kaiming-uniform bound
+    with pytest.raises(ValueError):
+        fl.Float8LinearModule(32, 48, bias=True)
+    with pytest.raises(ValueError):
+        fl.Float8LinearModule(32, 48, scaling="delayed")
+    with pytest.raises(ValueError):
+        fl.Float8LinearModule.from_linear(_lin(32, 48, bias=True))
+    with pytest.raises(TypeError):
+        fl.Float8LinearModule.from_linear(_lin(32, 48, dtype=torch.float32))
+    with pytest.raises(TypeError):   # dtype is checked before anything reaches the device
+        fl.Float8LinearFunction.apply(torch.zeros(16, 32), torch.zeros(48, 32, dtype=torch.bfloat16), "dynamic")
