@@ -18,8 +18,11 @@ composable with autograd).  This module is that swap:
   model in place.
 
 Scalings: "dynamic" (default), "rowwise" and "block" are stateless per call.
-Delayed and static scaling keep state across steps (an amax history, a fixed
-scale): use ``Float8Linear`` / ``Float8Tensor`` for those.
+"delayed" and "static" keep per-tensor state across steps (the TorchTitan
+page, section 3.3, names dynamic, delayed and static scaling): a Float8LinearModule
+holds it as buffers, one per tensor role (X, W, dY) -- an amax history ring
+with the slot the next cast records into, or a fixed scale -- and passes
+itself to the function as the owner of that state.
 """
 from __future__ import annotations
 
@@ -31,13 +34,36 @@ from . import (E4M3, E5M2, Float8Tensor, fp8lin_dgrad, fp8lin_dgrad_block, fp8li
                fp8lin_dgrad_rowwise, fp8lin_fwd, fp8lin_fwd_block, fp8lin_fwd_rowwise, fp8lin_wgrad,
                fp8lin_wgrad_block, fp8lin_wgrad_mn, fp8lin_wgrad_rowwise)
 
-SCALINGS = ("dynamic", "rowwise", "block")
+SCALINGS = ("dynamic", "rowwise", "block", "delayed", "static")
+STATEFUL = ("delayed", "static")
+ROLES = ("x", "w", "dy")
 
 
 def _check_scaling(scaling: str) -> None:
     if scaling not in SCALINGS:
-        raise ValueError(f"Float8LinearFunction supports scaling in {SCALINGS}, got {scaling!r} "
-                         "(delayed and static scaling keep state: use Float8Linear)")
+        raise ValueError(f"scaling must be one of {SCALINGS}, got {scaling!r}")
+
+
+def _quantize(src: torch.Tensor, fmt: int, scaling: str, blocks: str, role: str, owner) -> Float8Tensor:
+    """The FP8 copy of one operand for one call: a fresh Float8Tensor, wired
+    to the owner's state for the stateful scalings."""
+    rows, cols = src.shape
+    if scaling in STATEFUL:
+        if owner is None:
+            raise ValueError(f"{scaling} scaling keeps state: call through a Float8LinearModule")
+        t8 = Float8Tensor(rows, cols, fmt, src.device, scaling=scaling, transpose=False,
+                          history_len=getattr(owner, f"amax_history_{role}").numel() if scaling == "delayed" else 1)
+        if scaling == "delayed":
+            t8.history = getattr(owner, f"amax_history_{role}")
+            t8.slot, t8.seeded = owner.history_slot[role], owner.history_seeded[role]
+        else:
+            t8.scale = getattr(owner, f"scale_{role}")
+        t8.quantize(src)
+        if scaling == "delayed":
+            owner.history_slot[role], owner.history_seeded[role] = t8.slot, True
+        return t8
+    t8 = Float8Tensor(rows, cols, fmt, src.device, scaling=scaling, transpose=scaling == "rowwise", blocks=blocks)
+    return t8.quantize(src)
 
 
 def _fwd(x8: Float8Tensor, w8: Float8Tensor, y: torch.Tensor) -> None:
@@ -77,8 +103,10 @@ class Float8LinearFunction(torch.autograd.Function):
     multiples of 16 (the library raises Fp8LinError otherwise)."""
 
     @staticmethod
-    def forward(ctx, x: torch.Tensor, weight: torch.Tensor, scaling: str = "dynamic") -> torch.Tensor:
+    def forward(ctx, x: torch.Tensor, weight: torch.Tensor, scaling: str = "dynamic", owner=None) -> torch.Tensor:
         _check_scaling(scaling)
+        if scaling in STATEFUL and owner is None:
+            raise ValueError(f"{scaling} scaling keeps state: call through a Float8LinearModule")
         for t, name in ((x, "input"), (weight, "weight")):
             if t.dtype != torch.bfloat16:
                 raise TypeError(f"Float8LinearFunction: {name} must be bfloat16, got {t.dtype}")
@@ -87,14 +115,11 @@ class Float8LinearFunction(torch.autograd.Function):
             raise ValueError(f"Float8LinearFunction: input has {x.shape[-1]} features, weight expects {K}")
         x2 = x.reshape(-1, K).contiguous()
         M = x2.shape[0]
-        transpose = scaling == "rowwise"
-        x8 = Float8Tensor(M, K, E4M3, x.device, scaling=scaling, transpose=transpose, blocks="rowcol")
-        w8 = Float8Tensor(N, K, E4M3, x.device, scaling=scaling, transpose=transpose, blocks="tile")
-        x8.quantize(x2)
-        w8.quantize(weight.contiguous())
+        x8 = _quantize(x2, E4M3, scaling, "rowcol", "x", owner)
+        w8 = _quantize(weight.contiguous(), E4M3, scaling, "tile", "w", owner)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
         _fwd(x8, w8, y)
-        ctx.x8, ctx.w8, ctx.scaling, ctx.x_shape = x8, w8, scaling, x.shape
+        ctx.x8, ctx.w8, ctx.scaling, ctx.owner, ctx.x_shape = x8, w8, scaling, owner, x.shape
         return y.view(*x.shape[:-1], N)
 
     @staticmethod
@@ -104,10 +129,7 @@ class Float8LinearFunction(torch.autograd.Function):
         dy2 = dy.reshape(-1, N)
         if dy2.dtype != torch.bfloat16:
             raise TypeError(f"Float8LinearFunction: the output gradient must be bfloat16, got {dy2.dtype}")
-        dy2 = dy2.contiguous()
-        d8 = Float8Tensor(M, N, E5M2, dy.device, scaling=ctx.scaling, transpose=ctx.scaling == "rowwise",
-                          blocks="rowcol")
-        d8.quantize(dy2)
+        d8 = _quantize(dy2.contiguous(), E5M2, ctx.scaling, "rowcol", "dy", ctx.owner)
         dx = dw = None
         if ctx.needs_input_grad[0]:
             dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
@@ -116,8 +138,8 @@ class Float8LinearFunction(torch.autograd.Function):
         if ctx.needs_input_grad[1]:
             dw = torch.empty((N, K), dtype=torch.bfloat16, device=dy.device)
             _wgrad(d8, x8, dw)
-        ctx.x8 = ctx.w8 = None
-        return dx, dw, None
+        ctx.x8 = ctx.w8 = ctx.owner = None
+        return dx, dw, None, None
 
 
 class Float8LinearModule(torch.nn.Module):
@@ -126,7 +148,7 @@ class Float8LinearModule(torch.nn.Module):
     parameter [out_features x in_features]."""
 
     def __init__(self, in_features: int, out_features: int, bias: bool = False, device=None,
-                 scaling: str = "dynamic"):
+                 scaling: str = "dynamic", history_len: int = 16):
         super().__init__()
         if bias:
             raise ValueError("Float8LinearModule has no bias (the Float8 linear path computes x . W^T only)")
@@ -135,9 +157,31 @@ class Float8LinearModule(torch.nn.Module):
         self.weight = torch.nn.Parameter(torch.empty((out_features, in_features), dtype=torch.bfloat16,
                                                      device=device))
         torch.nn.init.kaiming_uniform_(self.weight, a=math.sqrt(5))   # nn.Linear's initialisation
+        self._init_state(history_len)
+
+    def _init_state(self, history_len: int) -> None:
+        """Buffers of the stateful scalings: per role an amax history ring
+        (delayed) or a fixed scale, 1.0 until set_static_scales (static)."""
+        dev = self.weight.device
+        self.history_slot = {r: 0 for r in ROLES}
+        self.history_seeded = {r: False for r in ROLES}
+        for r in ROLES:
+            if self.scaling == "delayed":
+                self.register_buffer(f"amax_history_{r}", torch.zeros(history_len, dtype=torch.float32, device=dev))
+            elif self.scaling == "static":
+                self.register_buffer(f"scale_{r}", torch.ones(1, dtype=torch.float32, device=dev))
+
+    def set_static_scales(self, x: float, w: float, dy: float) -> "Float8LinearModule":
+        """The fixed scales of static scaling (q = sat_RNE(t * scale))."""
+        if self.scaling != "static":
+            raise ValueError("set_static_scales: the module does not use static scaling")
+        for r, v in zip(ROLES, (x, w, dy)):
+            getattr(self, f"scale_{r}").fill_(float(v))
+        return self
 
     @classmethod
-    def from_linear(cls, linear: torch.nn.Linear, scaling: str = "dynamic") -> "Float8LinearModule":
+    def from_linear(cls, linear: torch.nn.Linear, scaling: str = "dynamic",
+                    history_len: int = 16) -> "Float8LinearModule":
         """Wrap an existing bias-free bf16 nn.Linear, sharing its weight parameter."""
         if linear.bias is not None:
             raise ValueError("from_linear: the linear has a bias")
@@ -148,10 +192,11 @@ class Float8LinearModule(torch.nn.Module):
         _check_scaling(scaling)
         mod.in_features, mod.out_features, mod.scaling = linear.in_features, linear.out_features, scaling
         mod.weight = linear.weight
+        mod._init_state(history_len)
         return mod
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
-        return Float8LinearFunction.apply(x, self.weight, self.scaling)
+        return Float8LinearFunction.apply(x, self.weight, self.scaling, self)
 
     def extra_repr(self) -> str:
         return f"in_features={self.in_features}, out_features={self.out_features}, scaling={self.scaling}"
@@ -164,7 +209,8 @@ def eligible(linear: torch.nn.Module) -> bool:
             and linear.in_features % 16 == 0 and linear.out_features % 16 == 0)
 
 
-def swap_linear_layers(model: torch.nn.Module, scaling: str = "dynamic", module_filter=None) -> torch.nn.Module:
+def swap_linear_layers(model: torch.nn.Module, scaling: str = "dynamic", module_filter=None,
+                       history_len: int = 16) -> torch.nn.Module:
     """Replace, in place, every eligible nn.Linear of ``model`` (and ``model``
     itself if it is one) by a Float8LinearModule sharing its weight;
     ``module_filter(fqn, module)`` may exclude more.  Returns the model."""
@@ -174,9 +220,9 @@ def swap_linear_layers(model: torch.nn.Module, scaling: str = "dynamic", module_
         return eligible(mod) and (module_filter is None or module_filter(fqn, mod))
 
     if keep("", model):
-        return Float8LinearModule.from_linear(model, scaling)
+        return Float8LinearModule.from_linear(model, scaling, history_len)
     for fqn, parent in list(model.named_modules()):
         for name, child in list(parent.named_children()):
             if keep(f"{fqn}.{name}" if fqn else name, child):
-                setattr(parent, name, Float8LinearModule.from_linear(child, scaling))
+                setattr(parent, name, Float8LinearModule.from_linear(child, scaling, history_len))
     return model

@@ -75,3 +75,30 @@ def test_weight_gradient_only_and_shape_errors(fp8lin):
         fp8lin.Float8LinearFunction.apply(x[:8], w, "dynamic")
     with pytest.raises(ValueError):
         fp8lin.Float8LinearFunction.apply(x[:, :128], w, "dynamic")
+
+
+@pytest.mark.parametrize("scaling", ["delayed", "static"])
+def test_stateful_module_matches_the_explicit_step_over_steps(fp8lin, scaling):
+    """Three training steps: the module's amax histories (or fixed scales)
+    evolve exactly as Float8Linear's."""
+    M, K, N = 256, 384, 512
+    mod = fp8lin.Float8LinearModule(K, N, device="cuda", scaling=scaling, history_len=4)
+    lin = fp8lin.Float8Linear(M, K, N, scaling=scaling, history_len=4)
+    if scaling == "static":
+        mod.set_static_scales(64.0, 8192.0, 2.0 ** 17)
+        for t8, v in ((lin.x8, 64.0), (lin.w8, 8192.0), (lin.dy8, 2.0 ** 17)):
+            t8.set_scale(v)
+    for step in range(3):
+        X, W, dY = _inputs(M, K, N, 60 + step)
+        with torch.no_grad():
+            mod.weight.copy_(to_dev_bf16(W))
+        mod.weight.grad = None
+        x = to_dev_bf16(X).requires_grad_()
+        y = mod(x)
+        y.backward(to_dev_bf16(dY))
+        y2, dx2, dw2 = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2) and torch.equal(x.grad, dx2) and torch.equal(mod.weight.grad, dw2), step
+        if scaling == "delayed":
+            for r, t8 in (("x", lin.x8), ("w", lin.w8), ("dy", lin.dy8)):
+                assert torch.equal(getattr(mod, f"amax_history_{r}"), t8.history), (step, r)

@@ -41,10 +41,27 @@ def test_module_and_function_arguments():
     with pytest.raises(ValueError):
         fl.Float8LinearModule(32, 48, bias=True)
     with pytest.raises(ValueError):
-        fl.Float8LinearModule(32, 48, scaling="delayed")
+        fl.Float8LinearModule(32, 48, scaling="per-channel")
+    with pytest.raises(ValueError):   # stateful scalings need the module that owns the state
+        fl.Float8LinearFunction.apply(torch.zeros(16, 32, dtype=torch.bfloat16),
+                                      torch.zeros(48, 32, dtype=torch.bfloat16), "delayed")
     with pytest.raises(ValueError):
         fl.Float8LinearModule.from_linear(_lin(32, 48, bias=True))
     with pytest.raises(TypeError):
         fl.Float8LinearModule.from_linear(_lin(32, 48, dtype=torch.float32))
     with pytest.raises(TypeError):   # dtype is checked before anything reaches the device
         fl.Float8LinearFunction.apply(torch.zeros(16, 32), torch.zeros(48, 32, dtype=torch.bfloat16), "dynamic")
+
+
+def test_stateful_scalings_keep_their_state_in_module_buffers():
+    d = fl.Float8LinearModule(32, 48, scaling="delayed", history_len=8)
+    sd = d.state_dict()
+    for r in ("x", "w", "dy"):
+        assert tuple(sd[f"amax_history_{r}"].shape) == (8,) and float(sd[f"amax_history_{r}"].abs().sum()) == 0
+    assert d.history_slot == {"x": 0, "w": 0, "dy": 0}
+    s = fl.Float8LinearModule.from_linear(_lin(32, 48), scaling="static").set_static_scales(2.0, 64.0, 4096.0)
+    assert [float(getattr(s, f"scale_{r}")) for r in ("x", "w", "dy")] == [2.0, 64.0, 4096.0]
+    with pytest.raises(ValueError):
+        d.set_static_scales(1.0, 1.0, 1.0)
+    plain = fl.Float8LinearModule(32, 48)
+    assert not [n for n, _ in plain.named_buffers()]
