@@ -198,6 +198,14 @@ class Float8LinearModule(torch.nn.Module):
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         return Float8LinearFunction.apply(x, self.weight, self.scaling, self)
 
+    # the history slots travel with the history buffers in a state dict
+    def get_extra_state(self):
+        return {"history_slot": dict(self.history_slot), "history_seeded": dict(self.history_seeded)}
+
+    def set_extra_state(self, state) -> None:
+        self.history_slot = dict(state["history_slot"])
+        self.history_seeded = dict(state["history_seeded"])
+
     def extra_repr(self) -> str:
         return f"in_features={self.in_features}, out_features={self.out_features}, scaling={self.scaling}"
 

@@ -65,3 +65,12 @@ def test_stateful_scalings_keep_their_state_in_module_buffers():
         d.set_static_scales(1.0, 1.0, 1.0)
     plain = fl.Float8LinearModule(32, 48)
     assert not [n for n, _ in plain.named_buffers()]
+
+
+def test_history_slots_round_trip_through_a_state_dict():
+    a = fl.Float8LinearModule(32, 48, scaling="delayed", history_len=4)
+    a.history_slot["x"], a.history_seeded["x"] = 3, True
+    a.amax_history_x.fill_(2.5)
+    b = fl.Float8LinearModule(32, 48, scaling="delayed", history_len=4)
+    b.load_state_dict(a.state_dict())
+    assert b.history_slot["x"] == 3 and b.history_seeded["x"] and float(b.amax_history_x[0]) == 2.5
