@@ -72,3 +72,36 @@ def test_rowwise_linear_step(fp8lin, M, K, N):
     assert_gemm_close(bf16_to_f64(y), oracle.gemm_rows_vec(rx["q"], E4M3, rw["q"], E4M3, rx["row_inv"], rw["row_inv"]), "Y")
     assert_gemm_close(bf16_to_f64(dx), oracle.gemm_rows_vec(rd["q"], E5M2, rw["qT"], E4M3, rd["row_inv"], rw["col_inv"]), "dX")
     assert_gemm_close(bf16_to_f64(dw), oracle.gemm_rows_vec(rd["qT"], E5M2, rx["qT"], E4M3, rd["col_inv"], rx["col_inv"]), "dW")
+
+
+def _rows(n, seed, count=40):
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(n, size=min(n, count - 2), replace=False)
+    return np.unique(np.concatenate([[0, n - 1], pick])).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_rowwise_workload_step_matches_oracle(fp8lin, name):
+    """Every configuration at full size: row and column inverse scales and
+    every byte of both FP8 copies of X, W and dY bit-exact; Y, dX, dW on
+    sampled rows."""
+    w = wl.WORKLOADS[name]
+    X, W, dY = w.make_x(), w.make_w(), w.make_dy()
+    lin = fp8lin.Float8Linear(w.M, w.K, w.N, scaling="rowwise")
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    rx, rw, rd = oracle.quantize_rowwise(X, E4M3), oracle.quantize_rowwise(W, E4M3), oracle.quantize_rowwise(dY, E5M2)
+    for key, t8, r in (("X", lin.x8, rx), ("W", lin.w8, rw), ("dY", lin.dy8, rd)):
+        assert np.array_equal(_bits(t8.row_inv), r["row_inv"].view(np.uint32)), f"{name} {key} row scales"
+        assert np.array_equal(_bits(t8.col_inv), r["col_inv"].view(np.uint32)), f"{name} {key} column scales"
+        assert np.array_equal(t8.q.cpu().numpy(), r["q"]), f"{name} {key} q"
+        assert np.array_equal(t8.qT.cpu().numpy(), r["qT"]), f"{name} {key} qT"
+    rm, rn = _rows(w.M, w.seed), _rows(w.N, w.seed + 1)
+    pick = lambda t, rows: bf16_to_f64(t[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(pick(y, rm), oracle.gemm_rows_vec(rx["q"], E4M3, rw["q"], E4M3, rx["row_inv"], rw["row_inv"], rm),
+                      f"{name} Y")
+    assert_gemm_close(pick(dx, rm), oracle.gemm_rows_vec(rd["q"], E5M2, rw["qT"], E4M3, rd["row_inv"], rw["col_inv"],
+                                                         rm), f"{name} dX")
+    assert_gemm_close(pick(dw, rn), oracle.gemm_rows_vec(rd["qT"], E5M2, rx["qT"], E4M3, rd["col_inv"], rx["col_inv"],
+                                                         rn), f"{name} dW")
