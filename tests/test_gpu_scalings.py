@@ -110,3 +110,52 @@ def test_float8_linear_step_with_other_scalings(fp8lin, scaling, transpose):
     assert_gemm_close(bf16_to_f64(y), oracle.fwd_ref(rx["q"], rx["inv_scale"], rw["q"], rw["inv_scale"]), "Y")
     assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_ref(rd["q"], rd["inv_scale"], rw["qT"], rw["inv_scale"]), "dX")
     assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_ref(rd["qT"], rd["inv_scale"], rx["qT"], rx["inv_scale"]), "dW")
+
+
+def _times_two(bits):
+    """x * 2 in bf16, exactly (bf16 -> f32 -> *2 -> the top 16 bits)."""
+    f = wl.bf16_bits_to_f32(bits) * np.float32(2.0)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _rows(n, seed, count=24):
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(n, size=min(n, count - 2), replace=False)
+    return np.unique(np.concatenate([[0, n - 1], pick])).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_delayed_workload_two_steps_match_oracle(fp8lin, name):
+    """Every configuration at full size, two steps of delayed scaling: the
+    second step's tensors are the first's times two, so its scales come from
+    the first step's recorded amax and the upper half of every tensor
+    saturates.  Scales, histories and every FP8 byte bit-exact; Y, dX, dW on
+    sampled rows of the second step."""
+    from gpu_helpers import assert_gemm_close, bf16_to_f64
+    w = wl.WORKLOADS[name]
+    H = 4
+    lin = fp8lin.Float8Linear(w.M, w.K, w.N, scaling="delayed", history_len=H)
+    steps = [(w.make_x(), w.make_w(), w.make_dy())]
+    steps.append(tuple(_times_two(t) for t in steps[0]))
+    hist = {k: np.zeros(H, np.float32) for k in "xwd"}
+    for step, (X, W, dY) in enumerate(steps):
+        y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+        torch.cuda.synchronize()
+        assert fp8lin.fp8lin_device_error() == 0
+        refs = {}
+        for k, bits, fmt in (("x", X, E4M3), ("w", W, E4M3), ("d", dY, E5M2)):
+            if step == 0:
+                hist[k][(0 - 1) % H] = oracle.amax(bits)      # the seed amax pass
+            refs[k] = oracle.quantize_delayed(bits, fmt, hist[k], step)
+            hist[k] = refs[k]["history"]
+        for k, t8 in (("x", lin.x8), ("w", lin.w8), ("d", lin.dy8)):
+            r = refs[k]
+            assert scalar_bits(t8.inv_scale) == f32_bits(r["inv_scale"]), (name, step, k)
+            assert np.array_equal(t8.history.cpu().numpy().view(np.uint32), r["history"].view(np.uint32)), (name, step, k)
+            assert np.array_equal(t8.q.cpu().numpy(), r["q"]), (name, step, k)
+    rx, rw, rd = refs["x"], refs["w"], refs["d"]
+    rm, rn = _rows(w.M, w.seed), _rows(w.N, w.seed + 1)
+    pick = lambda t, rows: bf16_to_f64(t[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(pick(y, rm), oracle.fwd_ref(rx["q"], rx["inv_scale"], rw["q"], rw["inv_scale"], rm), f"{name} Y")
+    assert_gemm_close(pick(dx, rm), oracle.dgrad_ref(rd["q"], rd["inv_scale"], rw["qT"], rw["inv_scale"], rm), f"{name} dX")
+    assert_gemm_close(pick(dw, rn), oracle.wgrad_ref(rd["qT"], rd["inv_scale"], rx["qT"], rx["inv_scale"], rn), f"{name} dW")
