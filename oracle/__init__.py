@@ -106,6 +106,10 @@ def _load():
         lib.orc_gemm_blocks.restype = None
         lib.orc_gemm_blocks.argtypes = [u8p, ctypes.c_int, u8p, ctypes.c_int, i64, i64, i64, i64,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_void_p]
+        lib.orc_pow2_scale_byte.restype = ctypes.c_uint8
+        lib.orc_pow2_scale_byte.argtypes = [f32, f32]
+        lib.orc_pow2_scale_bytes.restype = None
+        lib.orc_pow2_scale_bytes.argtypes = [ctypes.c_void_p, i64, f32, ctypes.c_void_p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -398,6 +402,132 @@ def wgrad_block_ref(dyq_m, idy_m, xq_m, ix_m, rows=None):
     xqT = np.ascontiguousarray(np.asarray(xq_m).T)
     return gemm_blocks(dyqT, E5M2, xqT, E4M3, np.ascontiguousarray(np.asarray(idy_m).T),
                        np.ascontiguousarray(np.asarray(ix_m).T), BLOCK, rows)
+
+
+# ------------------------------------------- power-of-two block scaling
+
+MX_BLOCK = 32    # contraction elements per power-of-two scale (the tensor cores' block-scaled MMA)
+SF_ATOM = 512    # bytes of one scale atom: 128 operand rows x 128 contraction elements
+
+
+def pow2_scale_bytes(amax_values: np.ndarray, fmt_max: float = FMT_MAX) -> np.ndarray:
+    """Power-of-two block scales ([L9]: one factor per block), in C: for each
+    amax the byte 127 - e with 2^e the largest power of two such that
+    max(amax, 1e-12) * 2^e <= fmt_max (clamped to -127 <= e <= 127), i.e. the
+    unsigned-exponent code of the inverse scale 2^-e; 0xFF for a NaN or
+    infinite amax.  Same shape as the input."""
+    a = np.ascontiguousarray(amax_values, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    _load().orc_pow2_scale_bytes(_ptr(a), a.size, float(np.float32(fmt_max)), _ptr(out))
+    return out
+
+
+def pow2_scale(sf: np.ndarray) -> np.ndarray:
+    """The scale 2^e of scale byte 127 - e (float32, exact); NaN for 0xFF."""
+    b = np.asarray(sf, dtype=np.int64)
+    s = np.ldexp(np.float64(1.0), (127 - b).astype(np.int32)).astype(np.float32)
+    return np.where(b == 0xFF, np.float32(np.nan), s).astype(np.float32)
+
+
+def pow2_inverse(sf: np.ndarray) -> np.ndarray:
+    """The inverse scale 2^-e of scale byte 127 - e (float32, exact)."""
+    b = np.asarray(sf, dtype=np.int64)
+    s = np.ldexp(np.float64(1.0), (b - 127).astype(np.int32)).astype(np.float32)
+    return np.where(b == 0xFF, np.float32(np.nan), s).astype(np.float32)
+
+
+def quantize_mx(x_bits: np.ndarray, fmt: int, along: str, fmt_max: float = FMT_MAX) -> dict:
+    """Block scaling with power-of-two scales: x cut into 1 x 32 blocks
+    (along="cols": each row's runs of 32 columns) or 32 x 1 blocks
+    (along="rows": each column's runs of 32 rows), blocks at the edge cut
+    short; each block's amax, its scale 2^e (pow2_scale_bytes) and the
+    saturating round-to-nearest-even cast of fp32(x) * 2^e (the product is
+    exact).  Returns amax and sf ([ceil(rows/32) x cols] or [rows x
+    ceil(cols/32)], like the blocks), scale = 2^e and q (row-major, like x)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    br, bc = (1, MX_BLOCK) if along == "cols" else (MX_BLOCK, 1)
+    a = amax_blocks(x, br, bc)
+    sf = pow2_scale_bytes(a, fmt_max)
+    s = pow2_scale(sf)
+    return {"amax": a, "sf": sf, "scale": s, "q": cast_blocks(x, fmt, br, bc, s)}
+
+
+def sf_by_operand_row(sf: np.ndarray, along: str) -> np.ndarray:
+    """Scale bytes indexed [operand row p][contraction block j] for the GEMM
+    that reads the copy: a row copy (along="cols") is read with its rows as
+    operand rows; a column copy (along="rows") with its columns."""
+    return np.ascontiguousarray(sf if along == "cols" else np.asarray(sf).T)
+
+
+def pack_sf(sf_pj: np.ndarray, P: int, K: int) -> np.ndarray:
+    """Scale bytes [P x ceil(K/32)] (operand row p, 32-long contraction block
+    j) laid out as the tensor cores read them: atoms of 512 bytes, one per
+    128 operand rows x 128 contraction elements, atom (kb, pb) at index
+    kb * ceil(P/128) + pb; inside an atom, row p and block j at byte
+    16 (p % 32) + 4 ((p % 128) // 32) + j % 4.  Entries past P or past the
+    last block hold 127 (scale 1).  Returns uint8 [ceil(K/128) x ceil(P/128) x 512].
+    Pure data layout, no arithmetic."""
+    sf_pj = np.asarray(sf_pj, dtype=np.uint8)
+    nj = (K + MX_BLOCK - 1) // MX_BLOCK
+    assert sf_pj.shape == (P, nj)
+    npb, nkb = (P + 127) // 128, (K + 127) // 128
+    out = np.full((nkb, npb, SF_ATOM), 127, dtype=np.uint8)
+    p = np.arange(P)[:, None]
+    j = np.arange(nj)[None, :]
+    off = 16 * (p % 32) + 4 * ((p % 128) // 32) + j % 4
+    out[(j // 4) + 0 * p, (p // 128) + 0 * j, off] = sf_pj
+    return out
+
+
+def unpack_sf(atoms: np.ndarray, P: int, K: int) -> np.ndarray:
+    """Inverse of pack_sf: the [P x ceil(K/32)] scale bytes held in the atoms."""
+    atoms = np.asarray(atoms, dtype=np.uint8).reshape((K + 127) // 128, (P + 127) // 128, SF_ATOM)
+    nj = (K + MX_BLOCK - 1) // MX_BLOCK
+    p = np.arange(P)[:, None]
+    j = np.arange(nj)[None, :]
+    return atoms[(j // 4) + 0 * p, (p // 128) + 0 * j, 16 * (p % 32) + 4 * ((p % 128) // 32) + j % 4]
+
+
+def quantize_mx_recipe(x_bits, w_bits, dy_bits, fmt_max: float = FMT_MAX) -> dict:
+    """The FP8 copies of one linear under power-of-two block scaling, each
+    with its 32-long blocks along the contraction of the GEMM that reads it:
+    X in 1 x 32 (forward, contraction K) and 32 x 1 (weight gradient,
+    contraction M); W in 1 x 32 (forward) and 32 x 1 (input gradient,
+    contraction N); dY in 1 x 32 (input gradient) and 32 x 1 (weight
+    gradient).  Each entry also carries its scales packed as pack_sf lays
+    them out ("atoms") for the GEMM that reads it."""
+    out = {}
+    for name, bits, fmt, along in (("x_k", x_bits, E4M3, "cols"), ("x_m", x_bits, E4M3, "rows"),
+                                   ("w_k", w_bits, E4M3, "cols"), ("w_n", w_bits, E4M3, "rows"),
+                                   ("dy_n", dy_bits, E5M2, "cols"), ("dy_m", dy_bits, E5M2, "rows")):
+        d = quantize_mx(bits, fmt, along, fmt_max)
+        rows, cols = np.asarray(bits).shape
+        P, K = (rows, cols) if along == "cols" else (cols, rows)
+        d["atoms"] = pack_sf(sf_by_operand_row(d["sf"], along), P, K)
+        out[name] = d
+    return out
+
+
+def fwd_mx_ref(xq_k, sf_x_k, wq_k, sf_w_k, rows=None):
+    """Y = X . W^T with X and W in 1 x 32 power-of-two blocks along K: the
+    block GEMM with 32-long contraction blocks and inverse scales 2^-e."""
+    return gemm_blocks(xq_k, E4M3, wq_k, E4M3, pow2_inverse(sf_x_k), pow2_inverse(sf_w_k), MX_BLOCK, rows)
+
+
+def dgrad_mx_ref(dyq_n, sf_dy_n, wq_n, sf_w_n, rows=None):
+    """dX = dY . W with dY in 1 x 32 blocks along N and W in 32 x 1 blocks
+    along N: B = W^T, whose row k takes W's column-k block scales."""
+    wqT = np.ascontiguousarray(np.asarray(wq_n).T)
+    return gemm_blocks(dyq_n, E5M2, wqT, E4M3, pow2_inverse(sf_dy_n),
+                       pow2_inverse(sf_by_operand_row(sf_w_n, "rows")), MX_BLOCK, rows)
+
+
+def wgrad_mx_ref(dyq_m, sf_dy_m, xq_m, sf_x_m, rows=None):
+    """dW = dY^T . X with dY and X in 32 x 1 blocks along M."""
+    dyqT = np.ascontiguousarray(np.asarray(dyq_m).T)
+    xqT = np.ascontiguousarray(np.asarray(xq_m).T)
+    return gemm_blocks(dyqT, E5M2, xqT, E4M3, pow2_inverse(sf_by_operand_row(sf_dy_m, "rows")),
+                       pow2_inverse(sf_by_operand_row(sf_x_m, "rows")), MX_BLOCK, rows)
 
 
 # ------------------------------------------------------------------ GEMMs

@@ -430,6 +430,35 @@ void orc_gemm_blocks(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t
     }
 }
 
+/* ------------------------------------------------ power-of-two block scales */
+
+/* Block scaling with power-of-two scales (the "per block" factor of the
+ * Lecture 9 exercises, restricted to powers of two so that the tensor cores'
+ * block-scaled MMA can apply it): a block's scale is 2^e, e the largest
+ * integer with max(amax, 1e-12) * 2^e <= fmt_max -- the largest power of two
+ * not above fmt_max / amax, so the block's largest magnitude lands at or
+ * below the format maximum and nothing saturates -- clamped to [-127, 127].
+ * The result is the byte 127 - e, the unsigned-exponent (UE8M0) code of the
+ * inverse scale 2^-e.  A NaN or infinite amax gives 0xFF (the UE8M0 NaN).
+ * Written as a search over e: scaling by a power of two is exact in
+ * binary64 for every value reached here, so each comparison is exact. */
+uint8_t orc_pow2_scale_byte(float amax, float fmt_max) {
+    if (!(amax <= 3.4028234663852886e38f)) return 0xFF;  /* NaN or +Inf */
+    const double a = (amax < 1e-12f) ? (double)1e-12f : (double)amax;
+    const double f = (double)fmt_max;
+    int e = 0;
+    while (e > -400 && ldexp(a, e) > f) --e;
+    while (e < 400 && ldexp(a, e + 1) <= f) ++e;
+    if (e > 127) e = 127;
+    if (e < -127) e = -127;
+    return (uint8_t)(127 - e);
+}
+
+/* orc_pow2_scale_byte applied to n amax values. */
+void orc_pow2_scale_bytes(const float *amax, int64_t n, float fmt_max, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_pow2_scale_byte(amax[i], fmt_max);
+}
+
 /* Number of threads the parallel loops above use. */
 int orc_num_threads(void) {
 #ifdef _OPENMP
