@@ -46,6 +46,7 @@ ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_s
                 "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
                 "fp8lin_cast_blockwise", "fp8lin_fwd_block", "fp8lin_dgrad_block", "fp8lin_wgrad_block",
                 "fp8lin_fwd_rowwise", "fp8lin_dgrad_rowwise", "fp8lin_wgrad_rowwise",
+                "fp8lin_cast_mx", "fp8lin_fwd_mx", "fp8lin_dgrad_mx", "fp8lin_wgrad_mx",
                 "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
 
@@ -96,6 +97,10 @@ SIGNATURES = {
     "fp8lin_wgrad": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_dgrad_mn": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_wgrad_mn": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_cast_mx": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_fwd_mx": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_dgrad_mx": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "fp8lin_wgrad_mx": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_device_error": [_vp, _vp],
     "fp8lin_selftest_bounded_wait": [ctypes.c_uint64, _vp],
 }
@@ -290,6 +295,67 @@ def fp8lin_wgrad_block(dyq, inv_dy, xq, inv_x, dw, stream=None) -> None:
     K = xq.shape[1]
     _block_gemm("fp8lin_wgrad_block", dyq, inv_dy, xq, inv_x, dw, M, N, K, (_blocks(M), N), (_blocks(M), K),
                 (N, K), stream)
+
+
+def sf_atom_bytes(P: int, K: int) -> int:
+    """Bytes of the power-of-two scale atoms of a copy read with P operand rows
+    and a contraction of K: ceil(P/128) * ceil(K/128) * 512."""
+    return _blocks(P) * _blocks(K) * 512
+
+
+def fp8lin_cast_mx(x: torch.Tensor, fmt: int, q_row=None, sf_row=None, q_col=None, sf_col=None,
+                   fmt_max: float = FMT_MAX, stream=None) -> None:
+    """Power-of-two block scaling in one pass: q_row / sf_row (1 x 32 blocks; sf_row holds
+    sf_atom_bytes(rows, cols) bytes), q_col / sf_col (32 x 1 blocks; sf_atom_bytes(cols, rows))."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [rows x cols] matrix")
+    rows, cols = x.shape
+    for q, sf, n, nbytes in ((q_row, sf_row, "row", sf_atom_bytes(rows, cols)),
+                             (q_col, sf_col, "col", sf_atom_bytes(cols, rows))):
+        _dev(q, "q_" + n, torch.uint8)
+        _dev(sf, "sf_" + n, torch.uint8)
+        if q is not None and tuple(q.shape) != (rows, cols):
+            raise ValueError(f"q_{n} must be [{rows} x {cols}]")
+        if sf is not None and sf.numel() != nbytes:
+            raise ValueError(f"sf_{n} must hold {nbytes} bytes, got {sf.numel()}")
+    _check("fp8lin_cast_mx", _lib.fp8lin_cast_mx(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(q_row),
+                                                 _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _stream(stream)))
+
+
+def _mx_gemm(name, a, sa, b, sb, out, M, N, K, sa_bytes, sb_bytes, out_shape, stream):
+    for t, n in ((a, "a"), (b, "b"), (sa, "sf_a"), (sb, "sf_b"), (out, "out")):
+        _dev(t, n)
+    for t, n, nbytes in ((sa, "sf_a", sa_bytes), (sb, "sf_b", sb_bytes)):
+        if t.numel() * t.element_size() != nbytes:
+            raise ValueError(f"{name}: {n} must hold {nbytes} bytes")
+    if tuple(out.shape) != out_shape or out.dtype != torch.bfloat16:
+        raise ValueError(f"{name}: output must be bf16 {out_shape}")
+    _check(name, getattr(_lib, name)(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out), M, N, K, _stream(stream)))
+
+
+def fp8lin_fwd_mx(xq, sf_x, wq, sf_w, y, stream=None) -> None:
+    """Y = X . W^T on the row copies of X [M x K] and W [N x K] (fp8lin_cast_mx)."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _mx_gemm("fp8lin_fwd_mx", xq, sf_x, wq, sf_w, y, M, N, K, sf_atom_bytes(M, K), sf_atom_bytes(N, K), (M, N),
+             stream)
+
+
+def fp8lin_dgrad_mx(dyq, sf_dy, wq, sf_w, dx, stream=None) -> None:
+    """dX = dY . W on the row copy of dY [M x N] and the column copy of W [N x K]."""
+    M, N = dyq.shape
+    K = wq.shape[1]
+    _mx_gemm("fp8lin_dgrad_mx", dyq, sf_dy, wq, sf_w, dx, M, N, K, sf_atom_bytes(M, N), sf_atom_bytes(K, N),
+             (M, K), stream)
+
+
+def fp8lin_wgrad_mx(dyq, sf_dy, xq, sf_x, dw, stream=None) -> None:
+    """dW = dY^T . X on the column copies of dY [M x N] and X [M x K]."""
+    M, N = dyq.shape
+    K = xq.shape[1]
+    _mx_gemm("fp8lin_wgrad_mx", dyq, sf_dy, xq, sf_x, dw, M, N, K, sf_atom_bytes(N, M), sf_atom_bytes(K, M),
+             (N, K), stream)
 
 
 def fp8lin_fwd_rowwise(xq, inv_x_rows, wq, inv_w_rows, y, stream=None) -> None:

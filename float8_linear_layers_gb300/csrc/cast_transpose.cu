@@ -23,6 +23,7 @@
 // Tiles are visited from the last row block to the first, so that the part of
 // the tensor the preceding amax pass read last is re-read from L2.
 #include <cstdint>
+#include <cstring>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -472,6 +473,186 @@ fp8lin_status launch_block_any(int device, int which, int grid, cudaStream_t str
     }
 }
 
+// ------------------------------------------- power-of-two block scaling
+
+// Block scaling with power-of-two scales, in the granularity the tensor
+// cores' block-scaled MMA applies them (one scale per 32 contraction
+// elements): every block's scale is 2^e, e the largest integer with
+// max(amax, 1e-12) * 2^e <= fmt_max (clamped to [-127, 127]); the codes are
+// sat_RNE(fp32(x) * 2^e) (an exact product).  The GEMM reads the inverse
+// scale 2^-e as the unsigned-exponent byte 127 - e; a block with a NaN or
+// infinite amax gets 0xFF (NaN).  Exponent from the bit patterns: with
+// a = ma 2^ea and fmt_max = mf 2^ef (ma, mf in [1, 2)), a 2^e <= fmt_max
+// exactly when e <= ef - ea - (ma > mf).
+__device__ __forceinline__ uint32_t pow2_scale_byte(uint32_t amax_bits, uint32_t fmax_bits) {
+    if (amax_bits >= 0x7F800000u) return 0xFFu;
+    const uint32_t a = amax_bits < 0x2B8CBCCCu ? 0x2B8CBCCCu : amax_bits;  // floor at 1e-12f
+    int e = (int)(fmax_bits >> 23) - (int)(a >> 23) - ((a & 0x7FFFFFu) > (fmax_bits & 0x7FFFFFu) ? 1 : 0);
+    e = e > 127 ? 127 : (e < -127 ? -127 : e);
+    return (uint32_t)(127 - e);
+}
+
+// 2^e from the byte 127 - e (2^-127 is the subnormal 0x00400000; NaN for 0xFF).
+__device__ __forceinline__ float pow2_from_byte(uint32_t b) {
+    if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
+    return b == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - b) << 23);
+}
+
+// One CTA per 128 x 128 tile of x, any of two copies (each row-major like x):
+//   ROW: 1 x 32 blocks (runs of 32 columns), read by a GEMM whose contraction
+//        runs along the columns, scales in atom (tc, tr);
+//   COL: 32 x 1 blocks (runs of 32 rows), read with the contraction along
+//        the rows, scales in atom (tr, tc).
+// A scale atom holds the bytes of 128 operand rows x 4 contraction blocks
+// (128 contraction elements) in the order the tensor cores' scale-factor
+// copy takes them: operand row p and block j at 16 (p % 32) + 4 (p / 32) + j;
+// atom (kb, pb) is 512 bytes at (kb * operand row blocks + pb) * 512.  A tile
+// is exactly one atom of each copy, so each CTA writes whole atoms, with 127
+// (scale 1) for rows or blocks past the matrix's edge.
+// Row blocks: the thread's 8-column maximum, then the 4 lanes of a 32-column
+// run (shuffles).  Column blocks: the thread's rows i = 2b, 2b + 1 of run b,
+// the lane 16 apart, then the 8 warps through shared memory.
+template <int FMT, bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads)
+cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, uint32_t fmax_bits,
+               uint8_t *__restrict__ q_row, uint8_t *__restrict__ sf_row, uint8_t *__restrict__ q_col,
+               uint8_t *__restrict__ sf_col) {
+    __shared__ uint32_t col_part[COL ? kThreads / 32 : 1][4][kTile];  // per-warp maxima of the four row runs
+    __shared__ __align__(16) float col_scale[COL ? 4 : 1][kTile];
+    __shared__ __align__(16) uint32_t atom_row[ROW ? 128 : 4];
+    __shared__ __align__(16) uint32_t atom_col[COL ? 128 : 4];
+
+    const int tr = (int)blockIdx.x / tiles_c, tc = (int)blockIdx.x % tiles_c;
+    const int r0 = tr * kTile, c0 = tc * kTile;
+    const int t = threadIdx.x, lane = t % 32, warp = t / 32;
+    const int ch = t % 16;        // 8-column chunk of the tile row
+    const int row_base = t / 16;  // rows row_base + 16 i
+    const bool col_in = (c0 + ch * 8) < cols;
+    const uint64_t pol = evict_first_policy();
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + row_base + 16 * i;
+        v[i] = (col_in && r < rows) ? ld_stream16(x + (int64_t)r * cols + c0 + ch * 8, pol) : make_uint4(0, 0, 0, 0);
+    }
+    if (t < 128) {
+        if (ROW) atom_row[t] = 0x7F7F7F7Fu;
+        if (COL) atom_col[t] = 0x7F7F7F7Fu;
+    }
+    // magnitudes as bf16 bit patterns without the sign (unsigned order = order of |x|)
+    const uint32_t k = 0x7FFF7FFFu;
+    uint32_t rowm[8];
+    uint32_t colm[4][4];  // [run b][packed column pair j]
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) colm[b][j] = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = v[i].x & k, b = v[i].y & k, c = v[i].z & k, d = v[i].w & k;
+        const uint32_t m = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
+        rowm[i] = max(m & 0xFFFFu, m >> 16);
+        colm[i / 2][0] = __vmaxu2(colm[i / 2][0], a);
+        colm[i / 2][1] = __vmaxu2(colm[i / 2][1], b);
+        colm[i / 2][2] = __vmaxu2(colm[i / 2][2], c);
+        colm[i / 2][3] = __vmaxu2(colm[i / 2][3], d);
+    }
+    uint32_t rbyte[8];
+    if (ROW) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t m = rowm[i];
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            rbyte[i] = pow2_scale_byte(m << 16, fmax_bits);
+        }
+    }
+    if (COL) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t m = __vmaxu2(colm[b][j], __shfl_xor_sync(0xFFFFFFFFu, colm[b][j], 16));
+                if (lane < 16) {
+                    col_part[warp][b][ch * 8 + 2 * j] = m & 0xFFFFu;
+                    col_part[warp][b][ch * 8 + 2 * j + 1] = m >> 16;
+                }
+            }
+    }
+    __syncthreads();
+    if (COL) {
+        // thread t: column t % 128, runs t / 128 and t / 128 + 2
+        const int c = t % kTile;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int b = t / kTile + 2 * h;
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) m = max(m, col_part[w][b][c]);
+            const uint32_t byte = pow2_scale_byte(m << 16, fmax_bits);
+            col_scale[b][c] = pow2_from_byte(byte);
+            if (c0 + c < cols && r0 + 32 * b < rows)
+                reinterpret_cast<uint8_t *>(atom_col)[16 * (c % 32) + 4 * (c / 32) + b] = (uint8_t)byte;
+        }
+    }
+    if (ROW && (ch & 3) == 0 && col_in) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = row_base + 16 * i;
+            if (r0 + rr < rows)
+                reinterpret_cast<uint8_t *>(atom_row)[16 * (rr % 32) + 4 * (rr / 32) + ch / 4] = (uint8_t)rbyte[i];
+        }
+    }
+    __syncthreads();
+    if (ROW && t < 32)
+        reinterpret_cast<uint4 *>(sf_row + ((int64_t)tc * tiles_r + tr) * 512)[t] =
+            reinterpret_cast<const uint4 *>(atom_row)[t];
+    if (COL && t >= 32 && t < 64)
+        reinterpret_cast<uint4 *>(sf_col + ((int64_t)tr * tiles_c + tc) * 512)[t - 32] =
+            reinterpret_cast<const uint4 *>(atom_col)[t - 32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + row_base + 16 * i;
+        const bool ok = col_in && r < rows;
+        const int64_t off = (int64_t)r * cols + c0 + ch * 8;
+        if (ROW && ok) st_stream8(q_row + off, cast8<FMT>(v[i], pow2_from_byte(rbyte[i])), pol);
+        if (COL && ok) {
+            const float4 lo = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8]);
+            const float4 hi = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8 + 4]);
+            const float sc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            st_stream8(q_col + off, cast8_each<FMT>(v[i], sc), pol);
+        }
+    }
+}
+
+template <int FMT, bool ROW, bool COL>
+fp8lin_status launch_mx(int device, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
+                        int tiles_r, int tiles_c, uint32_t fmax_bits, uint8_t *q_row, uint8_t *sf_row,
+                        uint8_t *q_col, uint8_t *sf_col) {
+    // carveout slots 10..12 (e4m3) and 13..15 (e5m2), one per combination of copies
+    const int slot = 10 + (FMT == FP8LIN_E4M3 ? 0 : 3) + (ROW ? 1 : 0) + (COL ? 2 : 0) - 1;
+    fp8lin_status st = fp8lin::prefer_max_shared_carveout(
+        reinterpret_cast<const void *>(&cast_mx_kernel<FMT, ROW, COL>), device, slot);
+    if (st != FP8LIN_OK) return st;
+    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits, q_row,
+                                                                sf_row, q_col, sf_col);
+    return FP8LIN_OK;
+}
+
+template <int FMT>
+fp8lin_status launch_mx_any(int device, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
+                            int tiles_r, int tiles_c, uint32_t fmax_bits, uint8_t *qr, uint8_t *sr, uint8_t *qc,
+                            uint8_t *sc) {
+    if (qr != nullptr && qc != nullptr)
+        return launch_mx<FMT, true, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, qr, sr,
+                                          qc, sc);
+    if (qr != nullptr)
+        return launch_mx<FMT, true, false>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, qr, sr,
+                                           qc, sc);
+    return launch_mx<FMT, false, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, qr, sr, qc,
+                                       sc);
+}
+
 // Checks shared by the three scalings, then the launch.
 fp8lin_status cast_common(int mode, const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
                           const float *src, int hist_len, int slot, float *scale, float *inv_scale, uint8_t *q,
@@ -594,4 +775,41 @@ extern "C" fp8lin_status fp8lin_cast_transpose_rowwise(const void *x, int64_t ro
     if (q == nullptr && qT == nullptr) return FP8LIN_ERR_INVALID_ARG;
     return cast_common(kRowwise, x, rows, cols, fmt, fmt_max, row_amax, 0, 0, nullptr, row_inv_scale, q, qT, nullptr,
                        stream, col_amax, col_inv_scale);
+}
+
+extern "C" fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
+                                        uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col,
+                                        cudaStream_t stream) {
+    using namespace fp8lin;
+    if ((q_row == nullptr) != (sf_row == nullptr) || (q_col == nullptr) != (sf_col == nullptr))
+        return FP8LIN_ERR_INVALID_ARG;
+    if (q_row == nullptr && q_col == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return FP8LIN_ERR_INVALID_ARG;
+    if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
+    // a normal, finite fmt_max: the exponent rule reads its bit pattern
+    if (!(fmt_max >= 1.17549435e-38f) || !(fmt_max <= 3.4e38f)) return FP8LIN_ERR_INVALID_ARG;
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (!empty && (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16) || !aligned(sf_row, 16) ||
+                   !aligned(sf_col, 16)))
+        return FP8LIN_ERR_MISALIGNED;
+    if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    if (empty) return FP8LIN_OK;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    if (tiles_r * tiles_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    const int grid = (int)(tiles_r * tiles_c);
+    uint32_t fmax_bits;
+    memcpy(&fmax_bits, &fmt_max, 4);
+    const uint16_t *xs = static_cast<const uint16_t *>(x);
+    st = fmt == FP8LIN_E4M3 ? launch_mx_any<FP8LIN_E4M3>(dev.device, grid, stream, xs, (int)rows, (int)cols,
+                                                         (int)tiles_r, (int)tiles_c, fmax_bits, q_row, sf_row, q_col,
+                                                         sf_col)
+                            : launch_mx_any<FP8LIN_E5M2>(dev.device, grid, stream, xs, (int)rows, (int)cols,
+                                                         (int)tiles_r, (int)tiles_c, fmax_bits, q_row, sf_row, q_col,
+                                                         sf_col);
+    if (st != FP8LIN_OK) return st;
+    return check_launch();
 }

@@ -1172,6 +1172,310 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
     }
 }
 
+// ------------------------------------- power-of-two block-scaled kernel
+
+// Block scaling with power-of-two scales, applied by the tensor cores:
+// tcgen05.mma kind::mxf8f6f4.block_scale multiplies every 32-long run of the
+// contraction by the scale bytes (unsigned exponents, 2^(byte - 127)) of its
+// A row and B row and accumulates in fp32 across the whole contraction, so
+// the MMAs accumulate in TMEM as in the per-tensor kernel and nothing is
+// promoted on the CUDA cores.  The scales of a 128-long slab (this CTA's
+// 128 A rows and the tile's 256 B rows: 512 + 1024 bytes, stored by the cast
+// as the "atoms" the scale-factor copy takes) ride in the slab's stage and
+// are copied into TMEM by the MMA issuer (tcgen05.cp 32x128b.warpx4: each
+// CTA of the pair from its own shared memory into its own TMEM), just before
+// the slab's MMAs; tcgen05 operations of one thread run in issue order.  In
+// TMEM, row p's scales sit in lane p, column p / 32 of the A region and
+// column n / 32 of the B region for output column n, byte = the 32-run
+// within the slab (the instruction descriptor's scale IDs).
+//
+// TMEM: one 256-column fp32 accumulator (columns 0..255) and a 16-column
+// scale slot per stage from column 256.  With one accumulator the epilogue
+// frees it as soon as it is in registers: eight epilogue warps (two per
+// lane quarter, 128 columns each, 216 registers after setmaxnreg) load
+// their 128 columns, hand the accumulator back to the leader, then round,
+// stage and TMA-store while the next tile's MMAs run.
+//   warpgroup 0 (64 registers)
+//     warp 0    TMA producer: A and B slabs and the slab's scale atoms;
+//     warp 1    TMEM allocation; in the leader one thread copies the scales
+//               and issues the MMAs, two slabs per pair of barrier waits;
+//     warps 2-3 idle;
+//   warpgroups 1, 2 (216 registers): epilogue.
+constexpr int kMxStages = 5;
+constexpr int kMxSfa = 512;                          // this CTA's A scales per slab
+constexpr int kMxSfb = 1024;                         // the tile's B scales per slab (both 128-row blocks)
+constexpr int kMxEpiBytes = kBlkPromoWarps * 2 * kEpiBuf;
+constexpr int kMxSmemBytes = kMxStages * (kAStage + kBStage + kMxSfa + kMxSfb) + kMxEpiBytes + 1024 + 1024;
+constexpr int kMxSfCol = kPairN;                     // first TMEM column of the scale slots
+constexpr int kMxSfSlotCols = 16;
+// The epilogue holds 128 accumulators (no promotion), so the producer /
+// issuer warpgroup keeps more registers than in the block kernel.
+constexpr int kMxLowRegs = 64;
+constexpr int kMxHighRegs = 216;
+static_assert(128 * kMxLowRegs + 256 * kMxHighRegs <= kBlkThreads * kBlkLaunchRegs,
+              "the register split must fit in the launch allocation");
+static_assert(kMxSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
+static_assert(kMxSfCol + kMxStages * kMxSfSlotCols <= 512, "scale slots fit in the allocated TMEM");
+static_assert((kMxStages * (kAStage + kBStage)) % 1024 == 0 && kMxEpiBytes % 1024 == 0,
+              "the epilogue staging (64-byte swizzle) and the scale atoms start on aligned offsets");
+
+// Shared-memory descriptor of one 512-byte scale atom for tcgen05.cp
+// 32x128b: 32 rows of 16 bytes, no swizzle, 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+__device__ __forceinline__ void utccp_pair_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kBlkThreads, 1)
+fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_sfa,
+                   const __grid_constant__ CUtensorMap map_sfb, int P, int Q, int R, int pb_a, int pb_b,
+                   uint32_t idesc, TileMap tiles) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = smem;                                   // [stages][128 x 128 B]
+    uint8_t *sB = sA + kMxStages * kAStage;               // [stages][128 x 128 B]
+    uint8_t *sC = sB + kMxStages * kBStage;               // epilogue staging: [8 warps][2][32 rows x 64 B]
+    uint8_t *sSfa = sC + kMxEpiBytes;                     // [stages][512 B]
+    uint8_t *sSfb = sSfa + kMxStages * kMxSfa;            // [stages][1024 B]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSfb + kMxStages * kMxSfb);
+    uint64_t *full = bars;                                // [stages] both CTAs' slabs and scales landed (leader)
+    uint64_t *empty = bars + kMxStages;                   // [stages] the pair's MMAs are done with the stage
+    uint64_t *acc_full = bars + 2 * kMxStages;            // the tile's accumulator is complete (both CTAs)
+    uint64_t *acc_empty = acc_full + 1;                   // both CTAs' epilogues hold it in registers (leader)
+    uint64_t *mma_done = acc_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMxStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(acc_full), 1);
+        mbar_init(smem_u32(acc_empty), 2 * kBlkPromoWarps);  // eight warps in each CTA of the pair
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
+        prefetch_tensormap(&map_c);
+        prefetch_tensormap(&map_sfa);
+        prefetch_tensormap(&map_sfb);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kBlkTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = tiles.tiles_m * tiles.tiles_n;
+    const int num_kb = (R + kBK - 1) / kBK;
+
+    if (warp < 4) {
+        setmaxnreg_dec<kMxLowRegs>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;
+            for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
+                int tm, tn;
+                tiles.coords(t, tm, tn);
+                const int a_row = tm * kPairM + (int)rank * kBM;
+                const int b_row = tn * kPairN + (int)rank * kBN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_inl(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
+                    const uint32_t fb_local = smem_u32(&full[stage]);
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage + kMxSfa + kMxSfb));
+                    const uint32_t fb = mapa_shared(fb_local, 0);
+                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
+                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
+                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
+                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
+                    // scale atoms: this CTA's 128 A rows; both 128-row blocks of the tile's B rows
+                    tma_load_2d_pair(smem_u32(sSfa + stage * kMxSfa), &map_sfa, fb, 0,
+                                     kb * pb_a + 2 * tm + (int)rank);
+                    tma_load_2d_pair(smem_u32(sSfb + stage * kMxSfb), &map_sfb, fb, 0, kb * pb_b + 2 * tn);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kMxStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag && leader) {
+                // let every copy of the pair land before either CTA exits
+                for (int s = 0; s < kMxStages; ++s)
+                    if (armed & (1u << s))
+                        mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
+            }
+        } else if (warp == 1 && lane == 0 && leader) {
+            // ------------------------------------------------ scale copies + MMA issuer (leader CTA)
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_phase = 0;
+            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
+            const uint64_t sfa_desc0 = sf_atom_desc(smem_u32(sSfa));
+            const uint64_t sfb_desc0 = sf_atom_desc(smem_u32(sSfb));
+            bool ok = true;
+            auto issue_slab = [&](int st, bool first) {
+                const uint32_t sf = tmem_base + (uint32_t)(kMxSfCol + st * kMxSfSlotCols);
+                utccp_pair_32x128b_x4(sf, sfa_desc0 + (uint64_t)((st * kMxSfa) >> 4));
+                utccp_pair_32x128b_x4(sf + 4, sfb_desc0 + (uint64_t)((st * kMxSfb) >> 4));
+                utccp_pair_32x128b_x4(sf + 8, sfb_desc0 + (uint64_t)((st * kMxSfb + 512) >> 4));
+                const uint64_t a_desc = a_desc0 + (uint64_t)(st * (kAStage >> 4));
+                const uint64_t b_desc = b_desc0 + (uint64_t)(st * (kBStage >> 4));
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k)
+                    umma_mx_pair(tmem_base, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k),
+                                 idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf, sf + 4,
+                                 (first && k == 0) ? 0u : 1u);
+                umma_commit_multicast(smem_u32(&empty[st]), 0x3);
+            };
+            for (int t = pair; t < num_tiles && ok && !*abort_flag; t += npairs) {
+                if (!mbar_wait_inl(smem_u32(acc_empty), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < num_kb; kb += 2) {
+                    const bool two = kb + 1 < num_kb;
+                    const bool wrap = stage + 1 == kMxStages;
+                    const int stage2 = wrap ? 0 : stage + 1;
+                    const uint32_t phase2 = wrap ? phase ^ 1u : phase;
+                    if (!mbar_wait_inl(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
+                        (two && !mbar_wait_inl(smem_u32(&full[stage2]), phase2, abort_flag, kWaitLimitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_slab(stage, kb == 0);
+                    stage = stage2;
+                    phase = phase2;
+                    if (two) {
+                        issue_slab(stage, false);
+                        if (++stage == kMxStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) break;
+                umma_commit_multicast(smem_u32(acc_full), 0x3);
+                acc_phase ^= 1u;
+            }
+            // every MMA issued above has completed once this arrives
+            umma_commit_multicast(smem_u32(mma_done), 0x1);
+            volatile int no_abort = 0;
+            mbar_wait_inl(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
+        }
+    } else {
+        setmaxnreg_inc<kMxHighRegs>();
+        // ------------------------------------------------ epilogue (warps 4..11, both CTAs)
+        const int sub = warp % 4;          // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows
+        const int cw = (warp - 4) / 4;     // which 128-column half of the pair tile
+        uint8_t *stage_c = sC + (warp - 4) * 2 * kEpiBuf;  // two buffers, alternate 32-column blocks
+        const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+        const uint32_t tlane = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(cw * kBlkWarpCols);
+        uint32_t acc_phase = 0;
+        uint32_t lo[64], hi[64];
+        for (int t = pair; t < num_tiles; t += npairs) {
+            int tm, tn;
+            tiles.coords(t, tm, tn);
+            const int row0 = tm * kPairM + (int)rank * kBM + sub * 32;
+            const int col_base = tn * kPairN + cw * kBlkWarpCols;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_inl(smem_u32(acc_full), acc_phase, abort_flag, kWaitLimitNs)))
+                break;
+            acc_phase ^= 1u;
+            tc_fence_after();
+            tmem_ld_32x32b_x64(tlane, lo);
+            tmem_ld_32x32b_x64(tlane + 64u, hi);
+            tmem_ld_wait_regs64(lo);
+            tmem_ld_wait_regs64(hi);
+            // the warp's part of the accumulator is in registers: hand it back to the leader
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+            // round to bf16 and TMA-store 32 columns at a time from two alternating
+            // staging buffers; blocks past the output's edge are neither staged nor stored
+            if (lane == 0) bulk_wait_read_0();   // the previous tile's stores are done reading
+#pragma unroll
+            for (int c = 0; c < kBlkWarpCols / kEpiCols; ++c) {
+                const int col0 = col_base + c * kEpiCols;
+                if (row0 >= P || col0 >= Q) break;
+                uint8_t *buf = stage_c + (c & 1) * kEpiBuf;
+                if (c >= 2 && lane == 0) bulk_wait_read_1();   // the store of block c - 2 (same buffer) has read it
+                __syncwarp();
+                uint8_t *dst = buf + lane * (kEpiCols * 2);
+                const uint32_t *src = c < 2 ? lo + 32 * c : hi + 32 * (c - 2);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int j = 8 * g;
+                    uint4 o;
+                    o.x = pack_bf16x2(__uint_as_float(src[j + 0]), __uint_as_float(src[j + 1]));
+                    o.y = pack_bf16x2(__uint_as_float(src[j + 2]), __uint_as_float(src[j + 3]));
+                    o.z = pack_bf16x2(__uint_as_float(src[j + 4]), __uint_as_float(src[j + 5]));
+                    o.w = pack_bf16x2(__uint_as_float(src[j + 6]), __uint_as_float(src[j + 7]));
+                    *reinterpret_cast<uint4 *>(dst + ((g ^ ((lane >> 1) & 3)) << 4)) = o;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&map_c, smem_u32(buf), col0, row0);
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA frees TMEM or exits while the pair still uses its shared memory
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kBlkTmemCols)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1453,6 +1757,112 @@ fp8lin_status gemm_block(const uint8_t *A, fp8lin_fmt fa, const float *inv_a, in
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+std::atomic<bool> g_mx_attr_set[4][64];
+std::atomic<int> g_mx_ctas[4][64];
+
+// 2-D map over scale atoms: [atom_rows x 128] 32-bit words (512 bytes per
+// atom), box = box_rows atoms; atoms past the end read as zero.
+bool make_sf_map(CUtensorMap *map, const void *base, int64_t atom_rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {128, (cuuint64_t)atom_rows};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4.block_scale: A / B
+// formats (bits 7..9 / 10..12), majorness (bits 15 / 16), N >> 3 at bits
+// 17..22, unsigned-exponent scales (bit 23), M >> 4 at bits 24..28; the scale
+// IDs (bits 4..5 for B, 29..30 for A: which byte of the scale words, i.e.
+// which 32-run of the slab) are or-ed in per MMA.
+uint32_t make_idesc_mx(fp8lin_fmt fa, fp8lin_fmt fb, bool a_mn, bool b_mn) {
+    uint32_t d = 0;
+    d |= (uint32_t)fa << 7;
+    d |= (uint32_t)fb << 10;
+    d |= (uint32_t)a_mn << 15;
+    d |= (uint32_t)b_mn << 16;
+    d |= (uint32_t)(kPairN >> 3) << 17;
+    d |= 1u << 23;
+    d |= (uint32_t)(kPairM >> 4) << 24;
+    return d;
+}
+
+// The power-of-two block-scaled GEMM (see fp8_gemm_mx_kernel): C = A . B^T
+// with the scale atoms of A (operand rows P, contraction R) and of B
+// (operand rows Q); sizes are the caller's to guarantee.
+template <bool A_MN, bool B_MN>
+fp8lin_status gemm_mx(const uint8_t *A, fp8lin_fmt fa, const uint8_t *sfa, const uint8_t *B, fp8lin_fmt fb,
+                      const uint8_t *sfb, void *C, int64_t P, int64_t Q, int64_t R, cudaStream_t stream) {
+    using namespace fp8lin;
+    if (P < 0 || Q < 0 || R < 0) return FP8LIN_ERR_INVALID_ARG;
+    const bool empty_out = P == 0 || Q == 0;
+    if (!empty_out && C == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (!empty_out && R > 0 && (A == nullptr || B == nullptr || sfa == nullptr || sfb == nullptr))
+        return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sfa, 16) || !aligned(sfb, 16))
+        return FP8LIN_ERR_MISALIGNED;
+    if (!dim_ok(P) || !dim_ok(Q) || !dim_ok(R) || P % 16 || Q % 16 || R % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    if (empty_out) return FP8LIN_OK;
+    if (R == 0) {
+        return cudaMemsetAsync(C, 0, (size_t)P * (size_t)Q * 2, stream) == cudaSuccess ? FP8LIN_OK
+                                                                                       : FP8LIN_ERR_CUDA;
+    }
+    const int64_t tiles_m = (P + kPairM - 1) / kPairM, tiles_n = (Q + kPairN - 1) / kPairN;
+    const int64_t pb_a = ceil_div(P, 128), pb_b = ceil_div(Q, 128), nkb = ceil_div(R, 128);
+    if (tiles_m * tiles_n > INT32_MAX || nkb * (pb_a + 2) > INT32_MAX || nkb * (pb_b + 2) > INT32_MAX)
+        return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    CUtensorMap map_a, map_b, map_c, map_sfa, map_sfb;
+    const bool ok_a = A_MN ? make_operand_map_mn(&map_a, A, P, R, kBM) : make_operand_map(&map_a, A, P, R, kBM);
+    const bool ok_b = B_MN ? make_operand_map_mn(&map_b, B, Q, R, kBN) : make_operand_map(&map_b, B, Q, R, kBN);
+    if (!ok_a || !ok_b || !make_output_map(&map_c, C, P, Q) || !make_sf_map(&map_sfa, sfa, nkb * pb_a, 1) ||
+        !make_sf_map(&map_sfb, sfb, nkb * pb_b, 2))
+        return FP8LIN_ERR_CUDA;
+    if (dev.device >= 64) return FP8LIN_ERR_CUDA;
+    constexpr int inst = A_MN * 2 + B_MN;
+    auto kernel = fp8_gemm_mx_kernel<A_MN, B_MN>;
+    cudaLaunchAttribute attr;
+    auto config = [&](int grid, cudaStream_t s) {
+        cudaLaunchConfig_t cfg = launch_config(grid, s, &attr);
+        cfg.blockDim = dim3(kBlkThreads, 1, 1);
+        cfg.dynamicSmemBytes = kMxSmemBytes;
+        return cfg;
+    };
+    if (!g_mx_attr_set[inst][dev.device].load(std::memory_order_acquire)) {
+        // the register split assumes the compiled count (see gemm_block)
+        cudaFuncAttributes fa_attr;
+        if (cudaFuncGetAttributes(&fa_attr, kernel) != cudaSuccess) return FP8LIN_ERR_CUDA;
+        if (fa_attr.numRegs != kBlkLaunchRegs) return FP8LIN_ERR_CUDA;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return FP8LIN_ERR_CUDA;
+        int clusters = 0;
+        cudaLaunchConfig_t cfg = config(2 * (dev.sm_count / 2), nullptr);
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1)
+            return FP8LIN_ERR_CUDA;
+        g_mx_ctas[inst][dev.device].store(clusters, std::memory_order_relaxed);
+        g_mx_attr_set[inst][dev.device].store(true, std::memory_order_release);
+    }
+    const TileMap tm = raster(P, Q, R, tiles_m, tiles_n);
+    const int num_tiles = (int)(tiles_m * tiles_n);
+    const int max_pairs = g_mx_ctas[inst][dev.device].load(std::memory_order_relaxed);
+    const int pairs = num_tiles < max_pairs ? num_tiles : max_pairs;
+    cudaLaunchConfig_t cfg = config(2 * pairs, stream);
+    const uint32_t idesc = make_idesc_mx(fa, fb, A_MN, B_MN);
+    if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, map_c, map_sfa, map_sfb, (int)P, (int)Q, (int)R, (int)pb_a,
+                           (int)pb_b, idesc, tm) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
+    return check_launch();
+}
+
+
 }  // namespace
 
 // Block scaling: X and dY in 1 x 128 / 128 x 1 blocks, W in 128 x 128 blocks
@@ -1483,6 +1893,29 @@ extern "C" fp8lin_status fp8lin_wgrad_block(const uint8_t *dyq, const float *inv
     // B = Xq read MN-major (column blocks: row k of B, block j at inv_x[j][k]); contraction M
     return gemm_block<true, true, true>(dyq, FP8LIN_E5M2, inv_dy, N, xq, FP8LIN_E4M3, inv_x, 1, K, dw, N, K, M,
                                         stream);
+}
+
+// Power-of-two block scaling (fp8lin_cast_mx): the tensor cores apply the
+// scales of every 32-long run of the contraction.
+extern "C" fp8lin_status fp8lin_fwd_mx(const uint8_t *xq, const uint8_t *sf_x, const uint8_t *wq,
+                                       const uint8_t *sf_w, void *y, int64_t M, int64_t N, int64_t K,
+                                       cudaStream_t stream) {
+    // A = Xq row copy [M x K], B = Wq row copy [N x K], both K-major; contraction K
+    return gemm_mx<false, false>(xq, FP8LIN_E4M3, sf_x, wq, FP8LIN_E4M3, sf_w, y, M, N, K, stream);
+}
+
+extern "C" fp8lin_status fp8lin_dgrad_mx(const uint8_t *dyq, const uint8_t *sf_dy, const uint8_t *wq,
+                                         const uint8_t *sf_w, void *dx, int64_t M, int64_t N, int64_t K,
+                                         cudaStream_t stream) {
+    // A = dYq row copy [M x N] (K-major), B = Wq column copy [N x K] read MN-major; contraction N
+    return gemm_mx<false, true>(dyq, FP8LIN_E5M2, sf_dy, wq, FP8LIN_E4M3, sf_w, dx, M, K, N, stream);
+}
+
+extern "C" fp8lin_status fp8lin_wgrad_mx(const uint8_t *dyq, const uint8_t *sf_dy, const uint8_t *xq,
+                                         const uint8_t *sf_x, void *dw, int64_t M, int64_t N, int64_t K,
+                                         cudaStream_t stream) {
+    // A = dYq column copy [M x N] read MN-major, B = Xq column copy [M x K] read MN-major; contraction M
+    return gemm_mx<true, true>(dyq, FP8LIN_E5M2, sf_dy, xq, FP8LIN_E4M3, sf_x, dw, N, K, M, stream);
 }
 
 extern "C" fp8lin_status fp8lin_fwd(const uint8_t *xq, const float *inv_x, const uint8_t *wq, const float *inv_w,

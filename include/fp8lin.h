@@ -360,6 +360,79 @@ fp8lin_status fp8lin_wgrad_rowwise(const uint8_t *dyqT, const float *inv_dy_cols
                                    const float *inv_x_cols, void *dw, int64_t M, int64_t N, int64_t K,
                                    cudaStream_t stream);
 
+/*
+ * Block scaling with power-of-two scales, applied by the tensor cores.  The
+ * "per block" factor of the Lecture 9 exercises (the answer on fp16 loss
+ * scaling versus FP8 scaling: one factor per tensor, or even per block),
+ * restricted to powers of two in the granularity the sm_103a block-scaled
+ * MMA (tcgen05.mma kind::mxf8f6f4.block_scale) applies: one scale per 32
+ * contraction elements.  A block's scale is 2^e, e the largest integer with
+ * max(amax, 1e-12) * 2^e <= fmt_max (clamped to -127 .. 127): the largest
+ * power of two not above the per-tensor recipe's fmt_max / amax, so the
+ * block's largest magnitude lands in [fmt_max / 2, fmt_max] and nothing
+ * saturates.  Codes are sat_RNE(fp32(x) * 2^e) (the product is exact).
+ *
+ * Scales are stored as bytes 127 - e (the unsigned-exponent code of the
+ * inverse scale 2^-e; 0xFF for a block whose amax is NaN or infinite), in
+ * the order the tensor cores read them: "atoms" of 512 bytes, one per 128
+ * operand rows x 128 contraction elements.  For a copy read by a GEMM with
+ * operand rows p (P of them) and contraction index k (K of them), atom
+ * (k / 128, p / 128) starts at byte ((k / 128) * ceil(P / 128) + p / 128) * 512,
+ * and holds the scale of row p, block j = k / 32 at byte
+ * 16 (p % 32) + 4 ((p % 128) / 32) + j % 4.  Entries past P or past the
+ * last block hold 127 (scale 1).  Size: ceil(P/128) * ceil(K/128) * 512 bytes.
+ */
+
+/*
+ * One pass over a bf16 [rows x cols] matrix x, writing either or both of
+ *   q_row, sf_row: 1 x 32 blocks (runs of 32 columns); the copy is read with
+ *                  its rows as operand rows and the contraction along the
+ *                  columns (P = rows, K = cols);
+ *   q_col, sf_col: 32 x 1 blocks (runs of 32 rows); read with its columns as
+ *                  operand rows and the contraction along the rows
+ *                  (P = cols, K = rows).
+ * Both copies are row-major [rows x cols] like x.  A linear takes X as q_row
+ * (forward) and q_col (weight gradient), W as q_row (forward) and q_col
+ * (input gradient), dY as q_row (input gradient) and q_col (weight gradient).
+ *
+ *   x        device, bf16 [rows x cols] row-major, 16-byte aligned.
+ *   rows, cols  >= 0, multiples of 16, <= FP8LIN_MAX_DIM.
+ *   fmt      FP8LIN_E4M3 or FP8LIN_E5M2; fmt_max a normal finite float > 0
+ *            (448 by default).
+ *   q_*      device, u8 [rows x cols], 16-byte aligned, or NULL.
+ *   sf_*     device, u8 scale atoms (sizes above), 16-byte aligned, or NULL
+ *            together with their q_*.  Every byte is written.
+ * Errors: a q_* without its sf_* (or the reverse), or no copy at all, is
+ * FP8LIN_ERR_INVALID_ARG; alignment and shapes as for fp8lin_cast_transpose.
+ */
+fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
+                             uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col,
+                             cudaStream_t stream);
+
+/*
+ * The three GEMMs of a linear on power-of-two block-scaled copies
+ * (fp8lin_cast_mx).  The tensor cores apply the scales inside the MMA and
+ * accumulate in fp32 across the whole contraction; the result is rounded to
+ * bf16 (round to nearest even):
+ *   fwd  : Y [M x N]  = sum_k (Xq[m][k] 2^-ex[m][k/32]) (Wq[n][k] 2^-ew[n][k/32])
+ *   dgrad: dX [M x K] = sum_n (dYq[m][n] 2^-edy[m][n/32]) (Wq[n][k] 2^-ew'[n/32][k])
+ *   wgrad: dW [N x K] = sum_m (dYq[m][n] 2^-edy'[m/32][n]) (Xq[m][k] 2^-ex'[m/32][k])
+ * fp8lin_fwd_mx:   xq, sf_x = q_row, sf_row of X [M x K] (e4m3);
+ *                  wq, sf_w = q_row, sf_row of W [N x K] (e4m3).
+ * fp8lin_dgrad_mx: dyq, sf_dy = q_row, sf_row of dY [M x N] (e5m2);
+ *                  wq, sf_w = q_col, sf_col of W [N x K] (e4m3).
+ * fp8lin_wgrad_mx: dyq, sf_dy = q_col, sf_col of dY [M x N] (e5m2);
+ *                  xq, sf_x = q_col, sf_col of X [M x K] (e4m3).
+ * Pointers 16-byte aligned (the scale atoms too); outputs bf16 row-major,
+ * fully overwritten.  M, N, K and the errors as for fp8lin_fwd.
+ */
+fp8lin_status fp8lin_fwd_mx(const uint8_t *xq, const uint8_t *sf_x, const uint8_t *wq, const uint8_t *sf_w,
+                            void *y, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+fp8lin_status fp8lin_dgrad_mx(const uint8_t *dyq, const uint8_t *sf_dy, const uint8_t *wq, const uint8_t *sf_w,
+                              void *dx, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+fp8lin_status fp8lin_wgrad_mx(const uint8_t *dyq, const uint8_t *sf_dy, const uint8_t *xq, const uint8_t *sf_x,
+                              void *dw, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Static English description of a status code (never NULL). */
 const char *fp8lin_status_str(fp8lin_status status);
 

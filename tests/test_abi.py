@@ -153,3 +153,33 @@ def test_argument_checks_of_mn_and_block_entry_points(lib):
     assert cb(a16, 32, 32, 0, 448.0, a4, a16, None, None, None, None, None) == 2     # misaligned copy
     assert cb(a16, 32, 32, 0, 448.0, a16, V(4098), None, None, None, None, None) == 2  # misaligned scales
     assert cb(a16, 32, 40, 0, 448.0, a16, a16, None, None, None, None, None) == 3    # ragged shape
+
+
+def test_argument_checks_of_power_of_two_block_entry_points(lib):
+    a16 = V(4096)      # 16-byte-aligned fake addresses: never dereferenced on these paths
+    a8 = V(4104)
+    for name in ("fp8lin_fwd_mx", "fp8lin_dgrad_mx", "fp8lin_wgrad_mx"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [V, V, V, V, V, I, I, I, V]
+        assert fn(a16, None, a16, a16, a16, 128, 128, 128, None) == 1, name     # no scales for A
+        assert fn(a16, a16, a16, None, a16, 128, 128, 128, None) == 1, name     # no scales for B
+        assert fn(a16, a16, a16, a16, a16, 128, -16, 128, None) == 1, name
+        assert fn(a16, a8, a16, a16, a16, 128, 128, 128, None) == 2, name       # scale atoms: 16 bytes
+        assert fn(a16, a16, a16, a8, a16, 128, 128, 128, None) == 2, name
+        assert fn(a16, a16, a8, a16, a16, 128, 128, 128, None) == 2, name
+        assert fn(a16, a16, a16, a16, a16, 136, 128, 128, None) == 3, name
+        assert fn(a16, a16, a16, a16, a16, 128, 128, 8, None) == 3, name
+    cm = lib.fp8lin_cast_mx
+    cm.restype = ctypes.c_int
+    cm.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V]
+    assert cm(a16, 32, 32, 0, 448.0, a16, None, None, None, None) == 1       # q without scales
+    assert cm(a16, 32, 32, 0, 448.0, None, None, None, a16, None) == 1       # scales without q
+    assert cm(a16, 32, 32, 0, 448.0, None, None, None, None, None) == 1      # nothing asked for
+    assert cm(a16, 32, 32, 2, 448.0, a16, a16, None, None, None) == 1        # format
+    assert cm(a16, 32, 32, 0, 0.0, a16, a16, None, None, None) == 1          # fmt_max
+    assert cm(a16, 32, 32, 0, 1e-40, a16, a16, None, None, None) == 1        # subnormal fmt_max
+    assert cm(a16, 32, 32, 0, float("inf"), a16, a16, None, None, None) == 1
+    assert cm(a16, 32, 32, 0, 448.0, a16, a8, None, None, None) == 2         # misaligned atoms
+    assert cm(V(4098), 32, 32, 0, 448.0, a16, a16, None, None, None) == 2    # misaligned input
+    assert cm(a16, 32, 40, 0, 448.0, None, None, a16, a16, None) == 3        # ragged shape

@@ -1,0 +1,172 @@
+"""Power-of-two block scaling on the GPU against the oracle: the one-pass cast
+(1 x 32 and 32 x 1 blocks) with every FP8 byte and every scale byte of the
+atoms bit-exact, and the three block-scaled GEMMs (scales applied by the
+tensor cores) within the GEMM tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import Guarded, assert_gemm_close, bf16_to_f64, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+E4M3, E5M2 = oracle.E4M3, oracle.E5M2
+
+
+def _atoms(P, K):
+    return ((P + 127) // 128) * ((K + 127) // 128) * 512
+
+
+def _ref_atoms(ref, along, rows, cols):
+    P, K = (rows, cols) if along == "cols" else (cols, rows)
+    return oracle.pack_sf(oracle.sf_by_operand_row(ref["sf"], along), P, K).reshape(-1)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (48, 80), (144, 272), (384, 1040), (1040, 384), (2048, 4096)])
+@pytest.mark.parametrize("fmt,dist", [(E4M3, ("normal", 1.0)), (E5M2, ("laplace", 1e-3))])
+@pytest.mark.parametrize("kinds", [("row", "col"), ("row",), ("col",)])
+def test_mx_cast_bit_exact(fp8lin, shape, fmt, dist, kinds):
+    rows, cols = shape
+    x = wl.generate(shape, *dist, seed=rows * 7 + cols, tensor_id=6, outlier_frac=1e-3)
+    xd = to_dev_bf16(x)
+    bufs = {}
+    for k in kinds:
+        P, K = (rows, cols) if k == "row" else (cols, rows)
+        bufs[k] = (Guarded((rows, cols), torch.uint8), Guarded((_atoms(P, K),), torch.uint8))
+    args = {}
+    for k in ("row", "col"):
+        args["q_" + k] = bufs[k][0].t if k in bufs else None
+        args["sf_" + k] = bufs[k][1].t if k in bufs else None
+    fp8lin.fp8lin_cast_mx(xd, fmt, **args)
+    torch.cuda.synchronize()
+    for k in kinds:
+        along = "cols" if k == "row" else "rows"
+        ref = oracle.quantize_mx(x, fmt, along)
+        q, sf = bufs[k]
+        assert np.array_equal(sf.t.cpu().numpy(), _ref_atoms(ref, along, rows, cols)), k
+        assert np.array_equal(q.t.cpu().numpy(), ref["q"]), k
+        assert q.intact() and sf.intact(), k
+
+
+def test_mx_cast_zero_tensor_and_arguments(fp8lin):
+    x = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
+    q = torch.full((128, 256), 0xFF, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros((_atoms(128, 256),), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_cast_mx(x, E4M3, q_row=q, sf_row=sf)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_mx(np.zeros((128, 256), np.uint16), E4M3, "cols")
+    assert (q == 0).all()
+    assert np.array_equal(sf.cpu().numpy(), _ref_atoms(ref, "cols", 128, 256))
+    assert int(sf[0].item()) == 127 - 48                 # amax floored at 1e-12: scale 2^48
+    with pytest.raises(fp8lin.Fp8LinError):
+        fp8lin.fp8lin_cast_mx(x, E4M3, q_row=q)          # a copy without its scales
+    with pytest.raises(fp8lin.Fp8LinError):
+        fp8lin.fp8lin_cast_mx(x, E4M3)                   # nothing asked for
+
+
+def test_mx_cast_fmt_max_e5m2_range(fp8lin):
+    # the alternative reading of the e5m2 numerator (its own maximum, 57344)
+    x = wl.generate((256, 384), "laplace", 1e-3, 31, 2)
+    q = torch.empty((256, 384), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((_atoms(256, 384),), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_cast_mx(to_dev_bf16(x), E5M2, q_row=q, sf_row=sf, fmt_max=57344.0)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_mx(x, E5M2, "cols", 57344.0)
+    assert np.array_equal(sf.cpu().numpy(), _ref_atoms(ref, "cols", 256, 384))
+    assert np.array_equal(q.cpu().numpy(), ref["q"])
+
+
+# (M, N, K): ragged pair tiles in every direction, a contraction shorter than
+# one slab and not a multiple of 32, 16-row and 16-column outputs, an odd
+# number of 128-row blocks of B
+GEMM_SHAPES = [(128, 128, 128), (144, 272, 208), (384, 1040, 4112), (1040, 400, 96), (2048, 2048, 2048),
+               (16, 16, 16), (16, 528, 144), (272, 16, 400), (256, 384, 48)]
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("which", ["fwd", "dgrad", "wgrad"])
+def test_mx_gemm_matches_oracle(fp8lin, M, N, K, which):
+    X = wl.generate((M, K), "normal", 1.0, M + 1, wl.X, outlier_frac=1e-3)
+    W = wl.generate((N, K), "normal", 0.02, N + 2, wl.W)
+    dY = wl.generate((M, N), "laplace", 1e-3, K + 3, wl.DY)
+    r = oracle.quantize_mx_recipe(X, W, dY)
+    if which == "fwd":
+        out, (a, b) = Guarded((M, N), torch.bfloat16), (r["x_k"], r["w_k"])
+        ref = oracle.fwd_mx_ref(a["q"], a["sf"], b["q"], b["sf"])
+    elif which == "dgrad":
+        out, (a, b) = Guarded((M, K), torch.bfloat16), (r["dy_n"], r["w_n"])
+        ref = oracle.dgrad_mx_ref(a["q"], a["sf"], b["q"], b["sf"])
+    else:
+        out, (a, b) = Guarded((N, K), torch.bfloat16), (r["dy_m"], r["x_m"])
+        ref = oracle.wgrad_mx_ref(a["q"], a["sf"], b["q"], b["sf"])
+    out.t.fill_(float("nan"))
+    getattr(fp8lin, f"fp8lin_{which}_mx")(_dev(a["q"]), _dev(a["atoms"].reshape(-1)), _dev(b["q"]),
+                                         _dev(b["atoms"].reshape(-1)), out.t)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    assert_gemm_close(bf16_to_f64(out.t), ref, f"{which} mx {M}x{N}x{K}")
+    assert out.intact()
+
+
+def test_mx_gemm_scales_per_run_reach_the_output(fp8lin):
+    # Every 32-run of the contraction carries its own power of two: with
+    # codes of 1.0 and scales 2^-(j % 7) per run j of row m, Y[m][n] is a
+    # plain sum of powers of two, which a scale taken from the wrong run or
+    # row changes.
+    M, N, K = 256, 256, 512
+    one = 0x38                                              # e4m3 1.0
+    a = np.full((M, K), one, np.uint8)
+    b = np.full((N, K), one, np.uint8)
+    nj = K // 32
+    sfa = (127 + ((np.arange(M)[:, None] + np.arange(nj)[None, :]) % 7)).astype(np.uint8)   # 2^-0 .. 2^-6
+    sfb = (127 + (np.arange(N)[:, None] % 3) + 0 * np.arange(nj)[None, :]).astype(np.uint8)
+    ref = oracle.gemm_blocks(a, E4M3, b, E4M3, oracle.pow2_inverse(sfa), oracle.pow2_inverse(sfb), 32)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_fwd_mx(_dev(a), _dev(oracle.pack_sf(sfa, M, K).reshape(-1)), _dev(b),
+                         _dev(oracle.pack_sf(sfb, N, K).reshape(-1)), y)
+    torch.cuda.synchronize()
+    got = bf16_to_f64(y)
+    # the fp32 sum is exact (multiples of 2^-3 below 2^10); the kernel rounds it once to bf16
+    want = wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 512, 1024), (144, 208, 272), (640, 384, 1296)])
+def test_mx_cast_then_gemms_match_oracle(fp8lin, M, K, N):
+    """The recipe end to end on the device: cast every copy, then the three GEMMs."""
+    X = wl.generate((M, K), "normal", 1.0, 41, wl.X, outlier_frac=1e-3)
+    W = wl.generate((N, K), "normal", 0.02, 41, wl.W)
+    dY = wl.generate((M, N), "normal", 1e-3, 41, wl.DY)
+    r = oracle.quantize_mx_recipe(X, W, dY)
+    dev = {}
+    for name, bits, fmt in (("x", X, E4M3), ("w", W, E4M3), ("dy", dY, E5M2)):
+        rows, cols = bits.shape
+        qr = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        qc = torch.empty_like(qr)
+        sr = torch.empty((_atoms(rows, cols),), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((_atoms(cols, rows),), dtype=torch.uint8, device="cuda")
+        fp8lin.fp8lin_cast_mx(to_dev_bf16(bits), fmt, q_row=qr, sf_row=sr, q_col=qc, sf_col=sc)
+        dev[name] = (qr, sr, qc, sc)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_fwd_mx(dev["x"][0], dev["x"][1], dev["w"][0], dev["w"][1], y)
+    fp8lin.fp8lin_dgrad_mx(dev["dy"][0], dev["dy"][1], dev["w"][2], dev["w"][3], dx)
+    fp8lin.fp8lin_wgrad_mx(dev["dy"][2], dev["dy"][3], dev["x"][2], dev["x"][3], dw)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    for key, (q, atoms) in (("x_k", dev["x"][0:2]), ("x_m", dev["x"][2:4]), ("w_k", dev["w"][0:2]),
+                            ("w_n", dev["w"][2:4]), ("dy_n", dev["dy"][0:2]), ("dy_m", dev["dy"][2:4])):
+        assert np.array_equal(q.cpu().numpy(), r[key]["q"]), key
+        assert np.array_equal(atoms.cpu().numpy(), r[key]["atoms"].reshape(-1)), key
+    assert_gemm_close(bf16_to_f64(y), oracle.fwd_mx_ref(r["x_k"]["q"], r["x_k"]["sf"], r["w_k"]["q"],
+                                                        r["w_k"]["sf"]), "fwd")
+    assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_mx_ref(r["dy_n"]["q"], r["dy_n"]["sf"], r["w_n"]["q"],
+                                                           r["w_n"]["sf"]), "dgrad")
+    assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
+                                                           r["x_m"]["sf"]), "wgrad")
