@@ -135,9 +135,13 @@ def cast_elem_bytes(scaling: str, transpose: bool, weight: bool = False) -> int:
     row-wise scaling; for block scaling, activations and gradients get a
     row-block and a column-block copy, weights one 128 x 128-block copy);
     dynamic and row-wise scaling read x once more for the amax pass, delayed,
-    static and block scaling do not."""
+    static and block scaling do not.  Power-of-two block scaling ("mx")
+    writes a row-block and a column-block copy of every tensor (plus one
+    scale byte per 32 elements per copy, left out here)."""
     if scaling == "block":
         return 2 + (1 if weight else 2)
+    if scaling == "mx":
+        return 2 + 2
     two_copies = transpose or scaling == "rowwise"
     return 2 + 1 + (1 if two_copies else 0) + (2 if scaling in ("dynamic", "rowwise") else 0)
 
@@ -217,7 +221,7 @@ def gemm_traffic(workload: str, scaling: str):
         sha = gemm_kernel_sha256()
     except (OSError, ValueError):
         return None
-    if t.get("gemm_kernel_sha256") != sha or t.get("workload") != workload or scaling in ("rowwise", "block"):
+    if t.get("gemm_kernel_sha256") != sha or t.get("workload") != workload or scaling in ("rowwise", "block", "mx"):
         return None
     return int(t["mean_dram_bytes_per_launch"])
 
@@ -408,12 +412,14 @@ class StepGraph:
         # one FP8 copy per tensor (backward GEMMs read it MN-major) unless the
         # transposed copies are asked for; row-wise scaling always needs them,
         # block scaling never writes them
-        self.transpose = (transpose or scaling == "rowwise") and scaling != "block"
+        self.transpose = (transpose or scaling == "rowwise") and scaling not in ("block", "mx")
         self.inp = dev_in
         self.lin = {l.name: l for l in spec.linears}
         self.t8 = {}
         for key, (rows, cols, fmt, *_) in cast_inputs(spec).items():
-            if scaling == "block":   # weights in 128 x 128 blocks, activations and gradients in row / column blocks
+            if scaling == "mx":      # every tensor: a 1 x 32 and a 32 x 1 block copy
+                self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=False)
+            elif scaling == "block":   # weights in 128 x 128 blocks, activations and gradients in row / column blocks
                 self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=False,
                                                blocks="tile" if key.startswith("w:") else "rowcol")
             else:
@@ -433,14 +439,17 @@ class StepGraph:
         else:
             self.main = self.side = torch.cuda.current_stream(dev)
         self._plan()
-        per_cast = 2 if scaling in ("dynamic", "rowwise") else 1   # block and delayed: one kernel per cast
+        per_cast = 2 if scaling in ("dynamic", "rowwise") else 1   # block, mx and delayed: one kernel per cast
         self.kernels_per_step = per_cast * len(self.t8) + len(spec.gemms)
 
     def _plan(self):
         self.main_casts, self.side_casts, self.needed_by, self.beside = plan(self.spec, self.overlap)
 
     def describe(self):
-        how = f"{self.scaling} per-tensor scaling" if self.scaling != "rowwise" else "row-wise (per-block) scaling"
+        how = {"rowwise": "row-wise (per-block) scaling",
+               "block": "block scaling (1 x 128 / 128 x 128 blocks, fp32 scales, partial sums promoted per block)",
+               "mx": "power-of-two block scaling (1 x 32 / 32 x 1 blocks, scales applied by the tensor cores)"}.get(
+            self.scaling, f"{self.scaling} per-tensor scaling")
         if not self.overlap:
             return how + "; serial: one stream, shared X cast once"
         return how + ("; two streams: casts that the data dependencies leave hidable run on a low-priority side "
@@ -467,9 +476,9 @@ class StepGraph:
     def _cast(self, rec, key, stream):
         fl, x, t8 = self.fl, self.inp[key], self.t8[key]
         n = x.numel()
-        two_copies = t8.qT is not None or getattr(t8, "blocks", None) == "rowcol"
+        two_copies = t8.qT is not None or getattr(t8, "blocks", None) == "rowcol" or t8.scaling == "mx"
         cast_bytes = (4 if two_copies else 3) * n   # read bf16, write one or two FP8 copies
-        if t8.scaling == "block":
+        if t8.scaling in ("block", "mx"):
             self._mark(stream, rec, "cast", key, cast_bytes, lambda: t8.quantize(x, stream))
         elif t8.scaling == "rowwise":
             self._mark(stream, rec, "amax", key, 2 * n,
@@ -489,7 +498,11 @@ class StepGraph:
         w = wl.WORKLOADS[l.workload]
         x8, w8, d8 = self.t8[l.x], self.t8["w:" + name], self.t8["dy:" + name]
         out = self.out[name][which]
-        if self.scaling == "block":
+        if self.scaling == "mx":
+            fn = {"fwd": lambda: fl.fp8lin_fwd_mx(x8.q, x8.sf_row, w8.q, w8.sf_row, out, m),
+                  "dgrad": lambda: fl.fp8lin_dgrad_mx(d8.q, d8.sf_row, w8.qc, w8.sf_col, out, m),
+                  "wgrad": lambda: fl.fp8lin_wgrad_mx(d8.qc, d8.sf_col, x8.qc, x8.sf_col, out, m)}[which]
+        elif self.scaling == "block":
             fn = {"fwd": lambda: fl.fp8lin_fwd_block(x8.q, x8.row_inv, w8.q, w8.tile_inv, out, m),
                   "dgrad": lambda: fl.fp8lin_dgrad_block(d8.q, d8.row_inv, w8.q, w8.tile_inv, out, m),
                   "wgrad": lambda: fl.fp8lin_wgrad_block(d8.qc, d8.col_inv, x8.qc, x8.col_inv, out, m)}[which]
@@ -761,6 +774,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "config": {"workload": spec.name, "scaling": args.scaling, "linears": spec.description,
                    "fp8_copies": ("row-major and transposed; backward GEMMs read the transposed copies"
                                   if step.transpose else
+                                  "two row-major copies per tensor (blocks along each GEMM's contraction); "
+                                  "GEMMs read them K- or MN-major" if args.scaling in ("block", "mx") else
                                   "one row-major copy per tensor; backward GEMMs read it MN-major"),
                    "l2": "inputs larger than L2: one step streams several GB of distinct operands through a 129 MB L2",
                    "parallelism": f"replicas x{world}"},
@@ -771,7 +786,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sustained,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
                      "traffic": gemm_traffic(args.workload, args.scaling),
-                     "kernel": ("fp8_gemm_block_kernel" if args.scaling == "block" else "fp8_gemm_tn_kernel") +
+                     "kernel": {"block": "fp8_gemm_block_kernel", "mx": "fp8_gemm_mx_kernel"}.get(
+                                   args.scaling, "fp8_gemm_tn_kernel") +
                                ", every launch of the timed region: mean 2*M*N*K flop per "
                                "launch / mean event-timed launch duration (launches run beside the side-stream "
                                "casts); traffic = mean DRAM bytes per GEMM launch of one step (ncu)",
@@ -817,7 +833,7 @@ def run_profile_case(args) -> None:
     need_w = case in ("gemm_fwd", "gemm_dgrad", "gemm_dgrad_mn")
     need_dy = case in ("gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn", "gemm_wgrad_mn", "amax", "cast", "cast_q",
                        "amax_rowcol", "cast_rowwise", "gemm_fwd_block", "gemm_dgrad_block", "gemm_wgrad_block",
-                       "cast_block")  # dY: 235 MB > L2
+                       "cast_block", "gemm_fwd_mx", "gemm_dgrad_mx", "gemm_wgrad_mx", "cast_mx")  # dY: 235 MB > L2
     x8 = w8 = d8 = None
     if need_x:
         x = up(w.make_x())
@@ -861,6 +877,29 @@ def run_profile_case(args) -> None:
             launch = lambda: fl.fp8lin_wgrad_block(db.qc, db.col_inv, xb.qc, xb.col_inv, out)
         if case == "cast_block":
             launch = lambda: db.quantize(dy)
+            work, unit = 4 * w.M * w.N, "byte"
+        else:
+            work, unit = 2 * w.M * w.N * w.K, "flop"
+    elif case in ("gemm_fwd_mx", "gemm_dgrad_mx", "gemm_wgrad_mx", "cast_mx"):
+        xm = fl.Float8Tensor(w.M, w.K, fl.E4M3, dev, scaling="mx")
+        wm = fl.Float8Tensor(w.N, w.K, fl.E4M3, dev, scaling="mx")
+        dm = fl.Float8Tensor(w.M, w.N, fl.E5M2, dev, scaling="mx")
+        if case != "cast_mx":
+            xm.quantize(up(w.make_x()))
+            wm.quantize(up(w.make_w()))
+        dm.quantize(dy)
+        torch.cuda.synchronize()
+        if case == "gemm_fwd_mx":
+            out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+            launch = lambda: fl.fp8lin_fwd_mx(xm.q, xm.sf_row, wm.q, wm.sf_row, out)
+        elif case == "gemm_dgrad_mx":
+            out = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
+            launch = lambda: fl.fp8lin_dgrad_mx(dm.q, dm.sf_row, wm.qc, wm.sf_col, out)
+        elif case == "gemm_wgrad_mx":
+            out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+            launch = lambda: fl.fp8lin_wgrad_mx(dm.qc, dm.sf_col, xm.qc, xm.sf_col, out)
+        if case == "cast_mx":
+            launch = lambda: dm.quantize(dy)
             work, unit = 4 * w.M * w.N, "byte"
         else:
             work, unit = 2 * w.M * w.N * w.K, "flop"
@@ -914,7 +953,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(SPECS), default="ffn8b")
-    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise", "block"], default="dynamic",
+    ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise", "block", "mx"], default="dynamic",
                     help="scaling recipe (the headline metric is dynamic per-tensor)")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
     ap.add_argument("--transpose", action="store_true",
@@ -929,7 +968,8 @@ def main():
     ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn",
                                                "gemm_wgrad_mn", "gemm_fwd_block", "gemm_dgrad_block",
                                                "gemm_wgrad_block", "amax", "cast", "cast_q", "cast_block",
-                                               "amax_rowcol", "cast_rowwise"],
+                                               "amax_rowcol", "cast_rowwise", "gemm_fwd_mx", "gemm_dgrad_mx",
+                                               "gemm_wgrad_mx", "cast_mx"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least three warm-up steps

@@ -470,12 +470,24 @@ class Float8Tensor:
                          gradients) gives q in 1 x 128 blocks (row_inv
                          [ceil(cols/128) x rows]) and qc in 128 x 1 blocks
                          (col_inv [ceil(rows/128) x cols]); ``blocks="tile"``
-                         (weights) gives q in 128 x 128 blocks (tile_inv)."""
+                         (weights) gives q in 128 x 128 blocks (tile_inv);
+              "mx":      power-of-two scales in blocks of 32 along the
+                         contraction, applied by the tensor cores, one pass
+                         with no amax call: q in 1 x 32 blocks (scale atoms
+                         sf_row) and qc in 32 x 1 blocks (sf_col)."""
 
     def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX,
                  scaling: str = "dynamic", history_len: int = 16, transpose: bool = True, blocks: str = "rowcol"):
-        if scaling not in ("dynamic", "delayed", "static", "rowwise", "block"):
+        if scaling not in ("dynamic", "delayed", "static", "rowwise", "block", "mx"):
             raise ValueError(f"unknown scaling {scaling!r}")
+        if scaling == "mx":
+            self.rows, self.cols, self.fmt, self.fmt_max, self.scaling = rows, cols, fmt, fmt_max, scaling
+            self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+            self.qc = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+            self.qT = None
+            self.sf_row = torch.empty(sf_atom_bytes(rows, cols), dtype=torch.uint8, device=device)
+            self.sf_col = torch.empty(sf_atom_bytes(cols, rows), dtype=torch.uint8, device=device)
+            return
         if scaling == "block":
             if blocks not in ("rowcol", "tile"):
                 raise ValueError(f"unknown blocks {blocks!r}")
@@ -516,7 +528,10 @@ class Float8Tensor:
 
     def quantize(self, x: torch.Tensor, stream=None) -> "Float8Tensor":
         """Scale, cast and transpose x according to this tensor's scaling."""
-        if self.scaling == "block":
+        if self.scaling == "mx":
+            fp8lin_cast_mx(x, self.fmt, q_row=self.q, sf_row=self.sf_row, q_col=self.qc, sf_col=self.sf_col,
+                           fmt_max=self.fmt_max, stream=stream)
+        elif self.scaling == "block":
             if self.blocks == "rowcol":
                 fp8lin_cast_blockwise(x, self.fmt, q_row=self.q, inv_row=self.row_inv, q_col=self.qc,
                                       inv_col=self.col_inv, fmt_max=self.fmt_max, stream=stream)
@@ -561,7 +576,7 @@ class Float8Linear:
                  scaling: str = "dynamic", history_len: int = 16, transpose: bool | None = None):
         self.M, self.K, self.N = M, K, N
         self.transpose = (scaling == "rowwise") if transpose is None else bool(transpose)
-        if scaling == "block" and self.transpose:
+        if scaling in ("block", "mx") and self.transpose:
             raise ValueError("block scaling writes no transposed copies")
         args = (device, fmt_max, scaling, history_len, self.transpose)
         self.x8 = Float8Tensor(M, K, E4M3, *args, blocks="rowcol")
@@ -578,7 +593,9 @@ class Float8Linear:
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
         self.x8.quantize(x, stream)
         self.w8.quantize(w, stream)
-        if self.x8.scaling == "block":
+        if self.x8.scaling == "mx":
+            fp8lin_fwd_mx(self.x8.q, self.x8.sf_row, self.w8.q, self.w8.sf_row, self.y, stream)
+        elif self.x8.scaling == "block":
             fp8lin_fwd_block(self.x8.q, self.x8.row_inv, self.w8.q, self.w8.tile_inv, self.y, stream)
         elif self.x8.scaling == "rowwise":
             fp8lin_fwd_rowwise(self.x8.q, self.x8.row_inv, self.w8.q, self.w8.row_inv, self.y, stream)
@@ -588,7 +605,10 @@ class Float8Linear:
 
     def backward(self, dy: torch.Tensor, stream=None):
         self.dy8.quantize(dy, stream)
-        if self.dy8.scaling == "block":
+        if self.dy8.scaling == "mx":
+            fp8lin_dgrad_mx(self.dy8.q, self.dy8.sf_row, self.w8.qc, self.w8.sf_col, self.dx, stream)
+            fp8lin_wgrad_mx(self.dy8.qc, self.dy8.sf_col, self.x8.qc, self.x8.sf_col, self.dw, stream)
+        elif self.dy8.scaling == "block":
             fp8lin_dgrad_block(self.dy8.q, self.dy8.row_inv, self.w8.q, self.w8.tile_inv, self.dx, stream)
             fp8lin_wgrad_block(self.dy8.qc, self.dy8.col_inv, self.x8.qc, self.x8.col_inv, self.dw, stream)
         elif self.dy8.scaling == "rowwise":

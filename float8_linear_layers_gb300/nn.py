@@ -17,7 +17,8 @@ composable with autograd).  This module is that swap:
 * ``swap_linear_layers`` -- replaces the eligible nn.Linear modules of a
   model in place.
 
-Scalings: "dynamic" (default), "rowwise" and "block" are stateless per call.
+Scalings: "dynamic" (default), "rowwise", "block" and "mx" (power-of-two
+block scales applied by the tensor cores) are stateless per call.
 "delayed" and "static" keep per-tensor state across steps (the TorchTitan
 page, section 3.3, names dynamic, delayed and static scaling): a Float8LinearModule
 holds it as buffers, one per tensor role (X, W, dY) -- an amax history ring
@@ -30,11 +31,11 @@ import math
 
 import torch
 
-from . import (E4M3, E5M2, Float8Tensor, fp8lin_dgrad, fp8lin_dgrad_block, fp8lin_dgrad_mn,
-               fp8lin_dgrad_rowwise, fp8lin_fwd, fp8lin_fwd_block, fp8lin_fwd_rowwise, fp8lin_wgrad,
-               fp8lin_wgrad_block, fp8lin_wgrad_mn, fp8lin_wgrad_rowwise)
+from . import (E4M3, E5M2, Float8Tensor, fp8lin_dgrad, fp8lin_dgrad_block, fp8lin_dgrad_mn, fp8lin_dgrad_mx,
+               fp8lin_dgrad_rowwise, fp8lin_fwd, fp8lin_fwd_block, fp8lin_fwd_mx, fp8lin_fwd_rowwise, fp8lin_wgrad,
+               fp8lin_wgrad_block, fp8lin_wgrad_mn, fp8lin_wgrad_mx, fp8lin_wgrad_rowwise)
 
-SCALINGS = ("dynamic", "rowwise", "block", "delayed", "static")
+SCALINGS = ("dynamic", "rowwise", "block", "mx", "delayed", "static")
 STATEFUL = ("delayed", "static")
 ROLES = ("x", "w", "dy")
 
@@ -67,7 +68,9 @@ def _quantize(src: torch.Tensor, fmt: int, scaling: str, blocks: str, role: str,
 
 
 def _fwd(x8: Float8Tensor, w8: Float8Tensor, y: torch.Tensor) -> None:
-    if x8.scaling == "block":
+    if x8.scaling == "mx":
+        fp8lin_fwd_mx(x8.q, x8.sf_row, w8.q, w8.sf_row, y)
+    elif x8.scaling == "block":
         fp8lin_fwd_block(x8.q, x8.row_inv, w8.q, w8.tile_inv, y)
     elif x8.scaling == "rowwise":
         fp8lin_fwd_rowwise(x8.q, x8.row_inv, w8.q, w8.row_inv, y)
@@ -76,7 +79,9 @@ def _fwd(x8: Float8Tensor, w8: Float8Tensor, y: torch.Tensor) -> None:
 
 
 def _dgrad(d8: Float8Tensor, w8: Float8Tensor, dx: torch.Tensor) -> None:
-    if d8.scaling == "block":
+    if d8.scaling == "mx":
+        fp8lin_dgrad_mx(d8.q, d8.sf_row, w8.qc, w8.sf_col, dx)
+    elif d8.scaling == "block":
         fp8lin_dgrad_block(d8.q, d8.row_inv, w8.q, w8.tile_inv, dx)
     elif d8.scaling == "rowwise":
         fp8lin_dgrad_rowwise(d8.q, d8.row_inv, w8.qT, w8.col_inv, dx)
@@ -87,7 +92,9 @@ def _dgrad(d8: Float8Tensor, w8: Float8Tensor, dx: torch.Tensor) -> None:
 
 
 def _wgrad(d8: Float8Tensor, x8: Float8Tensor, dw: torch.Tensor) -> None:
-    if d8.scaling == "block":
+    if d8.scaling == "mx":
+        fp8lin_wgrad_mx(d8.qc, d8.sf_col, x8.qc, x8.sf_col, dw)
+    elif d8.scaling == "block":
         fp8lin_wgrad_block(d8.qc, d8.col_inv, x8.qc, x8.col_inv, dw)
     elif d8.scaling == "rowwise":
         fp8lin_wgrad_rowwise(d8.qT, d8.col_inv, x8.qT, x8.col_inv, dw)

@@ -8,7 +8,7 @@ import workloads as wl
 from gpu_helpers import to_dev_bf16
 
 pytestmark = pytest.mark.gpu
-SCALINGS = ["dynamic", "rowwise", "block"]
+SCALINGS = ["dynamic", "rowwise", "block", "mx"]
 
 
 def _inputs(M, K, N, seed):
