@@ -1179,59 +1179,90 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
 // contraction by the scale bytes (unsigned exponents, 2^(byte - 127)) of its
 // A row and B row and accumulates in fp32 across the whole contraction, so
 // the MMAs accumulate in TMEM as in the per-tensor kernel and nothing is
-// promoted on the CUDA cores.  The scales of a 128-long slab (this CTA's
-// 128 A rows and the tile's 256 B rows: 512 + 1024 bytes, stored by the cast
-// as the "atoms" the scale-factor copy takes) ride in the slab's stage and
-// are copied into TMEM by the MMA issuer (tcgen05.cp 32x128b.warpx4: each
-// CTA of the pair from its own shared memory into its own TMEM), just before
-// the slab's MMAs; tcgen05 operations of one thread run in issue order.  In
-// TMEM, row p's scales sit in lane p, column p / 32 of the A region and
-// column n / 32 of the B region for output column n, byte = the 32-run
-// within the slab (the instruction descriptor's scale IDs).
+// promoted on the CUDA cores.  The scales of a 128-long slab (this CTA's 128
+// A rows and the tile's 256 B rows: 512 + 1024 bytes, stored by the cast as
+// the "atoms" described at fp8lin_cast_mx) ride in the slab's stage.  The
+// MMA reads them from TMEM: row p's four bytes (one per 32-run of the slab,
+// picked by the scale IDs of the instruction descriptor) in lane p, column
+// p / 32 of the A region; column n's in column n / 32 of the B region, in
+// every lane quarter (each quarter's datapath reads its own copy), and in
+// each CTA of the pair its own TMEM for all 256 B rows.
+//
+// The scales go into TMEM with tcgen05.st from a warpgroup of their own
+// (one warp per lane quarter, each writing the same 16 + 32 bytes per lane),
+// not with tcgen05.cp: a copy issued between the MMAs occupies the tensor
+// pipe (about 50 cycles per 512-byte atom, three per 512-cycle slab, where
+// the writes from registers run beside the MMAs).  Once the four writer
+// warps' stores have completed, one thread per CTA hands the slot to the
+// leader's MMA issuer through an mbarrier.
 //
 // TMEM: one 256-column fp32 accumulator (columns 0..255) and a 16-column
 // scale slot per stage from column 256.  With one accumulator the epilogue
 // frees it as soon as it is in registers: eight epilogue warps (two per
-// lane quarter, 128 columns each, 216 registers after setmaxnreg) load
-// their 128 columns, hand the accumulator back to the leader, then round,
-// stage and TMA-store while the next tile's MMAs run.
-//   warpgroup 0 (64 registers)
-//     warp 0    TMA producer: A and B slabs and the slab's scale atoms;
-//     warp 1    TMEM allocation; in the leader one thread copies the scales
-//               and issues the MMAs, two slabs per pair of barrier waits;
+// lane quarter, 128 columns each) load their columns, hand the accumulator
+// back to the leader, then round, stage and TMA-store while the next tile's
+// MMAs run.  512 threads:
+//   warpgroup 0 (56 registers after setmaxnreg)
+//     warp 0    TMA producer: A and B slabs (completing on the leader's
+//               barrier) and the slab's scale atoms (completing on this
+//               CTA's own barrier);
+//     warp 1    TMEM allocation; in the leader one thread issues the MMAs,
+//               two slabs per round of barrier waits;
 //     warps 2-3 idle;
-//   warpgroups 1, 2 (216 registers): epilogue.
+//   warpgroups 1, 2 (200 registers): epilogue;
+//   warpgroup 3 (56 registers): scale writers.
+// 128 x 56 + 256 x 200 + 128 x 56 = 65536 = 512 x 128, the registers the
+// CTA is launched with (the host checks the compiled count).
 constexpr int kMxStages = 5;
+constexpr int kMxThreads = 512;
+constexpr int kMxLaunchRegs = 128;
+constexpr int kMxLowRegs = 56;
+constexpr int kMxHighRegs = 200;
+static_assert(2 * 128 * kMxLowRegs + 256 * kMxHighRegs <= kMxThreads * kMxLaunchRegs,
+              "the register split must fit in the launch allocation");
 constexpr int kMxSfa = 512;                          // this CTA's A scales per slab
 constexpr int kMxSfb = 1024;                         // the tile's B scales per slab (both 128-row blocks)
 constexpr int kMxEpiBytes = kBlkPromoWarps * 2 * kEpiBuf;
 constexpr int kMxSmemBytes = kMxStages * (kAStage + kBStage + kMxSfa + kMxSfb) + kMxEpiBytes + 1024 + 1024;
 constexpr int kMxSfCol = kPairN;                     // first TMEM column of the scale slots
 constexpr int kMxSfSlotCols = 16;
-// The epilogue holds 128 accumulators (no promotion), so the producer /
-// issuer warpgroup keeps more registers than in the block kernel.
-constexpr int kMxLowRegs = 64;
-constexpr int kMxHighRegs = 216;
-static_assert(128 * kMxLowRegs + 256 * kMxHighRegs <= kBlkThreads * kBlkLaunchRegs,
-              "the register split must fit in the launch allocation");
 static_assert(kMxSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
 static_assert(kMxSfCol + kMxStages * kMxSfSlotCols <= 512, "scale slots fit in the allocated TMEM");
 static_assert((kMxStages * (kAStage + kBStage)) % 1024 == 0 && kMxEpiBytes % 1024 == 0,
               "the epilogue staging (64-byte swizzle) and the scale atoms start on aligned offsets");
 
-// Shared-memory descriptor of one 512-byte scale atom for tcgen05.cp
-// 32x128b: 32 rows of 16 bytes, no swizzle, 8-row groups 128 bytes apart.
-__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t smem_addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(128u >> 4) << 16;
-    d |= (uint64_t)(128u >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    return d;
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
-__device__ __forceinline__ void utccp_pair_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, uint4 a, uint4 b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// AND of v over the 128 threads of the scale-writer warpgroup (named barrier 1).
+__device__ __forceinline__ bool writers_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -1246,7 +1277,7 @@ __device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t a_desc, u
 }
 
 template <bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(kBlkThreads, 1)
+__global__ void __launch_bounds__(kMxThreads, 1)
 fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_sfa,
                    const __grid_constant__ CUtensorMap map_sfb, int P, int Q, int R, int pb_a, int pb_b,
@@ -1260,9 +1291,11 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     uint8_t *sSfa = sC + kMxEpiBytes;                     // [stages][512 B]
     uint8_t *sSfb = sSfa + kMxStages * kMxSfa;            // [stages][1024 B]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSfb + kMxStages * kMxSfb);
-    uint64_t *full = bars;                                // [stages] both CTAs' slabs and scales landed (leader)
+    uint64_t *full = bars;                                // [stages] both CTAs' A and B slabs landed (leader)
     uint64_t *empty = bars + kMxStages;                   // [stages] the pair's MMAs are done with the stage
-    uint64_t *acc_full = bars + 2 * kMxStages;            // the tile's accumulator is complete (both CTAs)
+    uint64_t *sf_full = bars + 2 * kMxStages;             // [stages] this CTA's scale atoms landed
+    uint64_t *sf_ready = bars + 3 * kMxStages;            // [stages] both CTAs' scales are in TMEM (leader)
+    uint64_t *acc_full = bars + 4 * kMxStages;            // the tile's accumulator is complete (both CTAs)
     uint64_t *acc_empty = acc_full + 1;                   // both CTAs' epilogues hold it in registers (leader)
     uint64_t *mma_done = acc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
@@ -1276,6 +1309,8 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         for (int s = 0; s < kMxStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&sf_full[s]), 1);
+            mbar_init(smem_u32(&sf_ready[s]), 2);    // one arrival from each CTA of the pair
         }
         mbar_init(smem_u32(acc_full), 1);
         mbar_init(smem_u32(acc_empty), 2 * kBlkPromoWarps);  // eight warps in each CTA of the pair
@@ -1322,16 +1357,17 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_inl(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
                     const uint32_t fb_local = smem_u32(&full[stage]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage + kMxSfa + kMxSfb));
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
+                    const uint32_t sb = smem_u32(&sf_full[stage]);
+                    mbar_arrive_expect_tx(sb, kMxSfa + kMxSfb);
                     const uint32_t fb = mapa_shared(fb_local, 0);
                     if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
                     else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
                     if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
                     else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
                     // scale atoms: this CTA's 128 A rows; both 128-row blocks of the tile's B rows
-                    tma_load_2d_pair(smem_u32(sSfa + stage * kMxSfa), &map_sfa, fb, 0,
-                                     kb * pb_a + 2 * tm + (int)rank);
-                    tma_load_2d_pair(smem_u32(sSfb + stage * kMxSfb), &map_sfb, fb, 0, kb * pb_b + 2 * tn);
+                    tma_load_2d(smem_u32(sSfa + stage * kMxSfa), &map_sfa, sb, 0, kb * pb_a + 2 * tm + (int)rank);
+                    tma_load_2d(smem_u32(sSfb + stage * kMxSfb), &map_sfb, sb, 0, kb * pb_b + 2 * tn);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kMxStages) {
@@ -1340,11 +1376,15 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     }
                 }
             }
-            if (*abort_flag && leader) {
-                // let every copy of the pair land before either CTA exits
+            if (*abort_flag) {
+                // let every copy land before either CTA exits
+                volatile int no_abort = 0;
                 for (int s = 0; s < kMxStages; ++s)
-                    if (armed & (1u << s))
-                        mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
+                    if (armed & (1u << s)) {
+                        if (leader)
+                            mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, &no_abort, kDrainLimitNs);
+                        mbar_wait_inl(smem_u32(&sf_full[s]), (armed_parity >> s) & 1u, &no_abort, kDrainLimitNs);
+                    }
             }
         } else if (warp == 1 && lane == 0 && leader) {
             // ------------------------------------------------ scale copies + MMA issuer (leader CTA)
@@ -1353,14 +1393,9 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             uint32_t acc_phase = 0;
             const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
             const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
-            const uint64_t sfa_desc0 = sf_atom_desc(smem_u32(sSfa));
-            const uint64_t sfb_desc0 = sf_atom_desc(smem_u32(sSfb));
             bool ok = true;
             auto issue_slab = [&](int st, bool first) {
                 const uint32_t sf = tmem_base + (uint32_t)(kMxSfCol + st * kMxSfSlotCols);
-                utccp_pair_32x128b_x4(sf, sfa_desc0 + (uint64_t)((st * kMxSfa) >> 4));
-                utccp_pair_32x128b_x4(sf + 4, sfb_desc0 + (uint64_t)((st * kMxSfb) >> 4));
-                utccp_pair_32x128b_x4(sf + 8, sfb_desc0 + (uint64_t)((st * kMxSfb + 512) >> 4));
                 const uint64_t a_desc = a_desc0 + (uint64_t)(st * (kAStage >> 4));
                 const uint64_t b_desc = b_desc0 + (uint64_t)(st * (kBStage >> 4));
 #pragma unroll
@@ -1379,7 +1414,9 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     const int stage2 = wrap ? 0 : stage + 1;
                     const uint32_t phase2 = wrap ? phase ^ 1u : phase;
                     if (!mbar_wait_inl(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
-                        (two && !mbar_wait_inl(smem_u32(&full[stage2]), phase2, abort_flag, kWaitLimitNs))) {
+                        !mbar_wait_inl(smem_u32(&sf_ready[stage]), phase, abort_flag, kWaitLimitNs) ||
+                        (two && !mbar_wait_inl(smem_u32(&full[stage2]), phase2, abort_flag, kWaitLimitNs)) ||
+                        (two && !mbar_wait_inl(smem_u32(&sf_ready[stage2]), phase2, abort_flag, kWaitLimitNs))) {
                         ok = false;
                         break;
                     }
@@ -1403,6 +1440,51 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             umma_commit_multicast(smem_u32(mma_done), 0x1);
             volatile int no_abort = 0;
             mbar_wait_inl(smem_u32(mma_done), 0, &no_abort, kDrainLimitNs);
+        }
+    } else if (warp >= 12) {
+        setmaxnreg_dec<kMxLowRegs>();
+        // ------------------------------------------------ scale writers (warps 12..15, both CTAs)
+        // Warp 12 + q writes lane quarter q: lane r holds the 16 bytes of atom
+        // row r (rows r, r + 32, r + 64, r + 96, one per column) for A and
+        // for each of B's two 128-row blocks -- the same bytes in every quarter.
+        const int q = warp - 12;
+        const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)kMxSfCol;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = pair; t < num_tiles && ok; t += npairs) {
+            for (int kb = 0; kb < num_kb; ++kb) {
+                // the four writer warps agree on going on (every one of them reaches this
+                // barrier on every slab, so none is left waiting at the one below)
+                if (!writers_all(__all_sync(0xFFFFFFFFu, mbar_wait_inl(smem_u32(&sf_full[stage]), phase,
+                                                                        abort_flag, kWaitLimitNs)))) {
+                    ok = false;
+                    break;
+                }
+                const uint4 a = lds128(smem_u32(sSfa + stage * kMxSfa + 16 * lane));
+                const uint4 b0 = lds128(smem_u32(sSfb + stage * kMxSfb + 16 * lane));
+                const uint4 b1 = lds128(smem_u32(sSfb + stage * kMxSfb + 512 + 16 * lane));
+                const uint32_t slot = tq + (uint32_t)(stage * kMxSfSlotCols);
+                tmem_st_32x32b_x4(slot, a);
+                tmem_st_32x32b_x8(slot + 4, b0, b1);
+                tmem_st_wait();
+                tc_fence_before();
+                // the four writer warps meet; one thread per CTA then tells the
+                // leader's issuer.  The stores have completed (tcgen05.wait::st) and
+                // the fence orders them before the arrival, and nothing in generic
+                // memory is published, so the peer CTA arrives without release
+                // semantics (a release at cluster scope costs hundreds of cycles per
+                // arrival, more than a slab's MMAs leave).
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (q == 0 && lane == 0) {
+                    if (leader) mbar_arrive_local(smem_u32(&sf_ready[stage]));
+                    else        mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&sf_ready[stage]), 0));
+                }
+                if (++stage == kMxStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
     } else {
         setmaxnreg_inc<kMxHighRegs>();
@@ -1830,7 +1912,7 @@ fp8lin_status gemm_mx(const uint8_t *A, fp8lin_fmt fa, const uint8_t *sfa, const
     cudaLaunchAttribute attr;
     auto config = [&](int grid, cudaStream_t s) {
         cudaLaunchConfig_t cfg = launch_config(grid, s, &attr);
-        cfg.blockDim = dim3(kBlkThreads, 1, 1);
+        cfg.blockDim = dim3(kMxThreads, 1, 1);
         cfg.dynamicSmemBytes = kMxSmemBytes;
         return cfg;
     };
@@ -1838,7 +1920,7 @@ fp8lin_status gemm_mx(const uint8_t *A, fp8lin_fmt fa, const uint8_t *sfa, const
         // the register split assumes the compiled count (see gemm_block)
         cudaFuncAttributes fa_attr;
         if (cudaFuncGetAttributes(&fa_attr, kernel) != cudaSuccess) return FP8LIN_ERR_CUDA;
-        if (fa_attr.numRegs != kBlkLaunchRegs) return FP8LIN_ERR_CUDA;
+        if (fa_attr.numRegs != kMxLaunchRegs) return FP8LIN_ERR_CUDA;
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
