@@ -1196,7 +1196,11 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
 // warps' stores have completed, one thread per CTA hands the slot to the
 // leader's MMA issuer through an mbarrier.
 //
-// TMEM: one 256-column fp32 accumulator (columns 0..255) and a 16-column
+// A stage holds two slabs (256 contraction elements): one barrier round,
+// one MMA commit and one scale hand-over per two slabs, since each commit
+// and each copy issued between MMAs costs tensor-pipe time.
+//
+// TMEM: one 256-column fp32 accumulator (columns 0..255) and a 32-column
 // scale slot per stage from column 256.  With one accumulator the epilogue
 // frees it as soon as it is in registers: eight epilogue warps (two per
 // lane quarter, 128 columns each) load their columns, hand the accumulator
@@ -1213,7 +1217,8 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
 //   warpgroup 3 (56 registers): scale writers.
 // 128 x 56 + 256 x 200 + 128 x 56 = 65536 = 512 x 128, the registers the
 // CTA is launched with (the host checks the compiled count).
-constexpr int kMxStages = 5;
+constexpr int kMxSlabs = 2;                          // 128-long slabs per stage
+constexpr int kMxStages = 3;                         // stages: six slabs in flight
 constexpr int kMxThreads = 512;
 constexpr int kMxLaunchRegs = 128;
 constexpr int kMxLowRegs = 56;
@@ -1222,13 +1227,15 @@ static_assert(2 * 128 * kMxLowRegs + 256 * kMxHighRegs <= kMxThreads * kMxLaunch
               "the register split must fit in the launch allocation");
 constexpr int kMxSfa = 512;                          // this CTA's A scales per slab
 constexpr int kMxSfb = 1024;                         // the tile's B scales per slab (both 128-row blocks)
-constexpr int kMxEpiBytes = kBlkPromoWarps * 2 * kEpiBuf;
-constexpr int kMxSmemBytes = kMxStages * (kAStage + kBStage + kMxSfa + kMxSfb) + kMxEpiBytes + 1024 + 1024;
+constexpr int kMxEpiBytes = kBlkPromoWarps * kEpiBuf;  // one staging buffer per epilogue warp
+constexpr int kMxSmemBytes =
+    kMxStages * kMxSlabs * (kAStage + kBStage + kMxSfa + kMxSfb) + kMxEpiBytes + 1024 + 1024;
 constexpr int kMxSfCol = kPairN;                     // first TMEM column of the scale slots
-constexpr int kMxSfSlotCols = 16;
+constexpr int kMxSfSlotCols = 32;                    // per stage: A 2 x 4 columns, B 2 x 8 columns
 static_assert(kMxSmemBytes <= 232448, "shared memory per CTA is at most 227 KB");
 static_assert(kMxSfCol + kMxStages * kMxSfSlotCols <= 512, "scale slots fit in the allocated TMEM");
-static_assert((kMxStages * (kAStage + kBStage)) % 1024 == 0 && kMxEpiBytes % 1024 == 0,
+static_assert(kMxSlabs == 2 && kMxSlabs * (4 + 8) <= kMxSfSlotCols, "a stage's scales fit in its slot");
+static_assert((kMxStages * kMxSlabs * (kAStage + kBStage)) % 1024 == 0 && kMxEpiBytes % 1024 == 0,
               "the epilogue staging (64-byte swizzle) and the scale atoms start on aligned offsets");
 
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
@@ -1285,12 +1292,12 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *sA = smem;                                   // [stages][128 x 128 B]
-    uint8_t *sB = sA + kMxStages * kAStage;               // [stages][128 x 128 B]
-    uint8_t *sC = sB + kMxStages * kBStage;               // epilogue staging: [8 warps][2][32 rows x 64 B]
-    uint8_t *sSfa = sC + kMxEpiBytes;                     // [stages][512 B]
-    uint8_t *sSfb = sSfa + kMxStages * kMxSfa;            // [stages][1024 B]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSfb + kMxStages * kMxSfb);
+    uint8_t *sA = smem;                                   // [stages][2 slabs][128 x 128 B]
+    uint8_t *sB = sA + kMxStages * kMxSlabs * kAStage;    // [stages][2 slabs][128 x 128 B]
+    uint8_t *sC = sB + kMxStages * kMxSlabs * kBStage;    // epilogue staging: [8 warps][32 rows x 64 B]
+    uint8_t *sSfa = sC + kMxEpiBytes;                     // [stages][2 slabs][512 B]
+    uint8_t *sSfb = sSfa + kMxStages * kMxSlabs * kMxSfa; // [stages][2 slabs][1024 B]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSfb + kMxStages * kMxSlabs * kMxSfb);
     uint64_t *full = bars;                                // [stages] both CTAs' A and B slabs landed (leader)
     uint64_t *empty = bars + kMxStages;                   // [stages] the pair's MMAs are done with the stage
     uint64_t *sf_full = bars + 2 * kMxStages;             // [stages] this CTA's scale atoms landed
@@ -1341,6 +1348,7 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 
     const int num_tiles = tiles.tiles_m * tiles.tiles_n;
     const int num_kb = (R + kBK - 1) / kBK;
+    const int num_st = (num_kb + kMxSlabs - 1) / kMxSlabs;   // stages per tile (the last may hold one slab)
 
     if (warp < 4) {
         setmaxnreg_dec<kMxLowRegs>();
@@ -1354,20 +1362,27 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                 tiles.coords(t, tm, tn);
                 const int a_row = tm * kPairM + (int)rank * kBM;
                 const int b_row = tn * kPairN + (int)rank * kBN;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int ks = 0; ks < num_st; ++ks) {
                     if (!mbar_wait_inl(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
                     const uint32_t fb_local = smem_u32(&full[stage]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * kMxSlabs * (kAStage + kBStage));
                     const uint32_t sb = smem_u32(&sf_full[stage]);
-                    mbar_arrive_expect_tx(sb, kMxSfa + kMxSfb);
+                    mbar_arrive_expect_tx(sb, kMxSlabs * (kMxSfa + kMxSfb));
                     const uint32_t fb = mapa_shared(fb_local, 0);
-                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
-                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
-                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
-                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
-                    // scale atoms: this CTA's 128 A rows; both 128-row blocks of the tile's B rows
-                    tma_load_2d(smem_u32(sSfa + stage * kMxSfa), &map_sfa, sb, 0, kb * pb_a + 2 * tm + (int)rank);
-                    tma_load_2d(smem_u32(sSfb + stage * kMxSfb), &map_sfb, sb, 0, kb * pb_b + 2 * tn);
+                    // both slabs are loaded even past the contraction's end (zero-filled,
+                    // scales past the last atom read as zero), so every stage moves the same bytes
+#pragma unroll
+                    for (int h = 0; h < kMxSlabs; ++h) {
+                        const int kb = ks * kMxSlabs + h;
+                        const int sl = stage * kMxSlabs + h;
+                        if (A_MN) tma_load_2d_pair(smem_u32(sA + sl * kAStage), &map_a, fb, a_row, kb * kBK);
+                        else      tma_load_2d_pair(smem_u32(sA + sl * kAStage), &map_a, fb, kb * kBK, a_row);
+                        if (B_MN) tma_load_2d_pair(smem_u32(sB + sl * kBStage), &map_b, fb, b_row, kb * kBK);
+                        else      tma_load_2d_pair(smem_u32(sB + sl * kBStage), &map_b, fb, kb * kBK, b_row);
+                        // scale atoms: this CTA's 128 A rows; both 128-row blocks of the tile's B rows
+                        tma_load_2d(smem_u32(sSfa + sl * kMxSfa), &map_sfa, sb, 0, kb * pb_a + 2 * tm + (int)rank);
+                        tma_load_2d(smem_u32(sSfb + sl * kMxSfb), &map_sfb, sb, 0, kb * pb_b + 2 * tn);
+                    }
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kMxStages) {
@@ -1394,42 +1409,34 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
             const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
             bool ok = true;
-            auto issue_slab = [&](int st, bool first) {
+            // slab h of stage st: its scales at columns 4h (A) and 8 + 8h (B) of the slot
+            auto issue_slab = [&](int st, int h, bool first) {
                 const uint32_t sf = tmem_base + (uint32_t)(kMxSfCol + st * kMxSfSlotCols);
-                const uint64_t a_desc = a_desc0 + (uint64_t)(st * (kAStage >> 4));
-                const uint64_t b_desc = b_desc0 + (uint64_t)(st * (kBStage >> 4));
+                const int sl = st * kMxSlabs + h;
+                const uint64_t a_desc = a_desc0 + (uint64_t)(sl * (kAStage >> 4));
+                const uint64_t b_desc = b_desc0 + (uint64_t)(sl * (kBStage >> 4));
 #pragma unroll
                 for (int k = 0; k < kBK / kUmmaK; ++k)
                     umma_mx_pair(tmem_base, a_desc + kslice<A_MN>(k), b_desc + kslice<B_MN>(k),
-                                 idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf, sf + 4,
+                                 idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sf + 4 * h, sf + 8 + 8 * h,
                                  (first && k == 0) ? 0u : 1u);
-                umma_commit_multicast(smem_u32(&empty[st]), 0x3);
             };
             for (int t = pair; t < num_tiles && ok && !*abort_flag; t += npairs) {
                 if (!mbar_wait_inl(smem_u32(acc_empty), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) break;
                 tc_fence_after();
-                for (int kb = 0; kb < num_kb; kb += 2) {
-                    const bool two = kb + 1 < num_kb;
-                    const bool wrap = stage + 1 == kMxStages;
-                    const int stage2 = wrap ? 0 : stage + 1;
-                    const uint32_t phase2 = wrap ? phase ^ 1u : phase;
+                for (int ks = 0; ks < num_st; ++ks) {
                     if (!mbar_wait_inl(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
-                        !mbar_wait_inl(smem_u32(&sf_ready[stage]), phase, abort_flag, kWaitLimitNs) ||
-                        (two && !mbar_wait_inl(smem_u32(&full[stage2]), phase2, abort_flag, kWaitLimitNs)) ||
-                        (two && !mbar_wait_inl(smem_u32(&sf_ready[stage2]), phase2, abort_flag, kWaitLimitNs))) {
+                        !mbar_wait_inl(smem_u32(&sf_ready[stage]), phase, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_slab(stage, kb == 0);
-                    stage = stage2;
-                    phase = phase2;
-                    if (two) {
-                        issue_slab(stage, false);
-                        if (++stage == kMxStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    issue_slab(stage, 0, ks == 0);
+                    if (ks * kMxSlabs + 1 < num_kb) issue_slab(stage, 1, false);
+                    umma_commit_multicast(smem_u32(&empty[stage]), 0x3);
+                    if (++stage == kMxStages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
                 if (!ok) break;
@@ -1453,7 +1460,7 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         uint32_t phase = 0;
         bool ok = true;
         for (int t = pair; t < num_tiles && ok; t += npairs) {
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int ks = 0; ks < num_st; ++ks) {
                 // the four writer warps agree on going on (every one of them reaches this
                 // barrier on every slab, so none is left waiting at the one below)
                 if (!writers_all(__all_sync(0xFFFFFFFFu, mbar_wait_inl(smem_u32(&sf_full[stage]), phase,
@@ -1461,12 +1468,16 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     ok = false;
                     break;
                 }
-                const uint4 a = lds128(smem_u32(sSfa + stage * kMxSfa + 16 * lane));
-                const uint4 b0 = lds128(smem_u32(sSfb + stage * kMxSfb + 16 * lane));
-                const uint4 b1 = lds128(smem_u32(sSfb + stage * kMxSfb + 512 + 16 * lane));
+                // slot columns: A of slab 0, A of slab 1 (4 each), B of slab 0, B of slab 1 (8 each)
+                const uint32_t a_sm = smem_u32(sSfa + stage * kMxSlabs * kMxSfa + 16 * lane);
+                const uint32_t b_sm = smem_u32(sSfb + stage * kMxSlabs * kMxSfb + 16 * lane);
+                const uint4 a0 = lds128(a_sm), a1 = lds128(a_sm + kMxSfa);
+                const uint4 b00 = lds128(b_sm), b01 = lds128(b_sm + 512);
+                const uint4 b10 = lds128(b_sm + kMxSfb), b11 = lds128(b_sm + kMxSfb + 512);
                 const uint32_t slot = tq + (uint32_t)(stage * kMxSfSlotCols);
-                tmem_st_32x32b_x4(slot, a);
-                tmem_st_32x32b_x8(slot + 4, b0, b1);
+                tmem_st_32x32b_x8(slot, a0, a1);
+                tmem_st_32x32b_x8(slot + 8, b00, b01);
+                tmem_st_32x32b_x8(slot + 16, b10, b11);
                 tmem_st_wait();
                 tc_fence_before();
                 // the four writer warps meet; one thread per CTA then tells the
@@ -1491,7 +1502,7 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         // ------------------------------------------------ epilogue (warps 4..11, both CTAs)
         const int sub = warp % 4;          // TMEM lanes 32 sub .. 32 sub + 31: this warp's 32 rows
         const int cw = (warp - 4) / 4;     // which 128-column half of the pair tile
-        uint8_t *stage_c = sC + (warp - 4) * 2 * kEpiBuf;  // two buffers, alternate 32-column blocks
+        uint8_t *stage_c = sC + (warp - 4) * kEpiBuf;      // this warp's staging buffer
         const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
         const uint32_t tlane = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(cw * kBlkWarpCols);
         uint32_t acc_phase = 0;
@@ -1513,15 +1524,15 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
-            // round to bf16 and TMA-store 32 columns at a time from two alternating
-            // staging buffers; blocks past the output's edge are neither staged nor stored
+            // round to bf16 and TMA-store 32 columns at a time through the staging
+            // buffer; blocks past the output's edge are neither staged nor stored
             if (lane == 0) bulk_wait_read_0();   // the previous tile's stores are done reading
 #pragma unroll
             for (int c = 0; c < kBlkWarpCols / kEpiCols; ++c) {
                 const int col0 = col_base + c * kEpiCols;
                 if (row0 >= P || col0 >= Q) break;
-                uint8_t *buf = stage_c + (c & 1) * kEpiBuf;
-                if (c >= 2 && lane == 0) bulk_wait_read_1();   // the store of block c - 2 (same buffer) has read it
+                uint8_t *buf = stage_c;
+                if (c >= 1 && lane == 0) bulk_wait_read_0();   // the store of block c - 1 has read the buffer
                 __syncwarp();
                 uint8_t *dst = buf + lane * (kEpiCols * 2);
                 const uint32_t *src = c < 2 ? lo + 32 * c : hi + 32 * (c - 2);
