@@ -170,3 +170,37 @@ def test_mx_cast_then_gemms_match_oracle(fp8lin, M, K, N):
                                                            r["w_n"]["sf"]), "dgrad")
     assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
                                                            r["x_m"]["sf"]), "wgrad")
+
+
+def _rows(n, seed, count=40):
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(n, size=min(n, count - 2), replace=False)
+    return np.unique(np.concatenate([[0, n - 1], pick])).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_mx_workload_step_matches_oracle(fp8lin, name):
+    """Every configuration at full size through Float8Linear: every FP8 byte
+    and every scale byte of the six copies bit-exact; Y, dX, dW on sampled
+    rows (the first, the last and 38 seeded others)."""
+    w = wl.WORKLOADS[name]
+    X, W, dY = w.make_x(), w.make_w(), w.make_dy()
+    lin = fp8lin.Float8Linear(w.M, w.K, w.N, scaling="mx")
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    r = oracle.quantize_mx_recipe(X, W, dY)
+    got = {"x_k": (lin.x8.q, lin.x8.sf_row), "x_m": (lin.x8.qc, lin.x8.sf_col),
+           "w_k": (lin.w8.q, lin.w8.sf_row), "w_n": (lin.w8.qc, lin.w8.sf_col),
+           "dy_n": (lin.dy8.q, lin.dy8.sf_row), "dy_m": (lin.dy8.qc, lin.dy8.sf_col)}
+    for key, (q, atoms) in got.items():
+        assert np.array_equal(atoms.cpu().numpy(), r[key]["atoms"].reshape(-1)), f"{name} {key} scales"
+        assert np.array_equal(q.cpu().numpy(), r[key]["q"]), f"{name} {key} codes"
+    rm, rn = _rows(w.M, w.seed), _rows(w.N, w.seed + 1)
+    pick = lambda t, rows: bf16_to_f64(t[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(pick(y, rm), oracle.fwd_mx_ref(r["x_k"]["q"], r["x_k"]["sf"], r["w_k"]["q"], r["w_k"]["sf"],
+                                                     rm), f"{name} Y")
+    assert_gemm_close(pick(dx, rm), oracle.dgrad_mx_ref(r["dy_n"]["q"], r["dy_n"]["sf"], r["w_n"]["q"],
+                                                        r["w_n"]["sf"], rm), f"{name} dX")
+    assert_gemm_close(pick(dw, rn), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
+                                                        r["x_m"]["sf"], rn), f"{name} dW")
