@@ -82,71 +82,99 @@ amax_bf16_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__re
 }
 
 // Row and column amax of a row-major bf16 [rows x cols] matrix (row-wise
-// scaling's statistics).  One CTA per 128 x 128 tile, the same coalesced
-// 16-byte loads as the cast kernel; per-row maxima reduce across the 16
-// threads that share a row (shuffles), per-column maxima across the 16 row
-// groups (shuffle + shared memory); one atomicMax per row and per column of
-// the tile, issued as fire-and-forget reductions (the addresses are spread
-// over all rows and columns, so they do not serialise).
+// scaling's statistics).  A CTA walks a strip of kStrip 128 x 128 tiles
+// along its 128 rows, with the next tile's loads in flight while the current
+// one is reduced (the same coalesced 16-byte loads as the cast kernel: a
+// one-tile-per-CTA version spent most of each CTA's life reducing with no
+// loads in flight and read at half the per-tensor amax's rate).  Row maxima
+// accumulate in registers over the strip and reduce once across the 16
+// threads that share a row (shuffles): one atomicMax per row per strip.
+// Column maxima reduce per tile over the thread's 8 rows, the lane 16 apart
+// and the 8 warps (shared memory): one atomicMax per column per tile.  The
+// atomics are fire-and-forget reductions on the fp32 bit patterns.
 constexpr int kTile = 128;
+constexpr int kStrip = 4;
 
-__global__ void __launch_bounds__(256)
-amax_rowcol_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c,
-                   unsigned int *__restrict__ row_bits, unsigned int *__restrict__ col_bits) {
-    __shared__ uint32_t col_part[8][kTile / 2];  // [warp][packed column pair]
-    const int tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
-    const int r0 = tr * kTile, c0 = tc * kTile;
-    const int t = threadIdx.x, ch = t % 16, row_base = t / 16;
+__device__ __forceinline__ void load_tile(uint4 (&v)[8], const uint16_t *__restrict__ x, int rows, int cols,
+                                          int r0, int c0, int row_base, int ch) {
     const bool col_in = (c0 + ch * 8) < cols;
-    uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = r0 + row_base + 16 * i;
         v[i] = (col_in && r < rows) ? ld_stream16(reinterpret_cast<const uint4 *>(x + (int64_t)r * cols + c0 + ch * 8))
                                     : make_uint4(0, 0, 0, 0);
     }
+}
+
+__global__ void __launch_bounds__(256)
+amax_rowcol_kernel(const uint16_t *__restrict__ x, int rows, int cols, int strips_c, int tiles_c,
+                   unsigned int *__restrict__ row_bits, unsigned int *__restrict__ col_bits) {
+    __shared__ uint32_t col_part[8][kTile / 2];  // [warp][packed column pair]
+    const int tr = blockIdx.x / strips_c, sc = blockIdx.x % strips_c;
+    const int r0 = tr * kTile, tc0 = sc * kStrip;
+    const int ntiles = min(kStrip, tiles_c - tc0);
+    const int t = threadIdx.x, ch = t % 16, row_base = t / 16;
+    const int warp = t / 32, lane = t % 32;
     const uint32_t k = 0x7FFF7FFFu;
-    // columns: packed maxima of this thread's 8 columns over its 8 rows
-    uint4 cm = make_uint4(0, 0, 0, 0);
+    uint32_t rowm[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rowm[i] = 0;
+    uint4 v[8], nx[8];
+    load_tile(v, x, rows, cols, r0, tc0 * kTile, row_base, ch);
+    for (int s = 0; s < ntiles; ++s) {
+        const int c0 = (tc0 + s) * kTile;
+        if (s + 1 < ntiles) load_tile(nx, x, rows, cols, r0, c0 + kTile, row_base, ch);
+        // columns: packed maxima of this thread's 8 columns over its 8 rows; rows: running maxima
+        uint4 cm = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            cm.x = __vmaxu2(cm.x, v[i].x & k);
+            cm.y = __vmaxu2(cm.y, v[i].y & k);
+            cm.z = __vmaxu2(cm.z, v[i].z & k);
+            cm.w = __vmaxu2(cm.w, v[i].w & k);
+            const uint32_t m = absmax4(0u, v[i]);
+            rowm[i] = max(rowm[i], max(m & 0xFFFFu, m >> 16));
+        }
+        if (col_bits != nullptr) {
+            // lanes t and t ^ 16 hold the same columns for two row groups
+            cm.x = __vmaxu2(cm.x, __shfl_xor_sync(0xFFFFFFFFu, cm.x, 16));
+            cm.y = __vmaxu2(cm.y, __shfl_xor_sync(0xFFFFFFFFu, cm.y, 16));
+            cm.z = __vmaxu2(cm.z, __shfl_xor_sync(0xFFFFFFFFu, cm.z, 16));
+            cm.w = __vmaxu2(cm.w, __shfl_xor_sync(0xFFFFFFFFu, cm.w, 16));
+            if (s > 0) __syncthreads();  // the previous tile's column maxima have been read
+            if (lane < 16) {
+                col_part[warp][4 * ch + 0] = cm.x;
+                col_part[warp][4 * ch + 1] = cm.y;
+                col_part[warp][4 * ch + 2] = cm.z;
+                col_part[warp][4 * ch + 3] = cm.w;
+            }
+            __syncthreads();
+            if (t < kTile / 2) {
+                uint32_t m = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) m = __vmaxu2(m, col_part[w][t]);
+                const int c = c0 + 2 * t;
+                if (c < cols) {
+                    const uint32_t lo = (m & 0xFFFFu) << 16, hi = m & 0xFFFF0000u;
+                    if (lo != 0) atomicMax(col_bits + c, lo);
+                    if (hi != 0) atomicMax(col_bits + c + 1, hi);
+                }
+            }
+        }
+        if (s + 1 < ntiles) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = nx[i];
+        }
+    }
+    if (row_bits == nullptr) return;
+    // rows: the 16 lanes sharing a row combine their maxima over the strip
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        cm.x = __vmaxu2(cm.x, v[i].x & k);
-        cm.y = __vmaxu2(cm.y, v[i].y & k);
-        cm.z = __vmaxu2(cm.z, v[i].z & k);
-        cm.w = __vmaxu2(cm.w, v[i].w & k);
-        // rows: the 16 lanes sharing this row combine their 8-column maxima
-        uint32_t m = absmax4(0u, v[i]);
-        m = max(m & 0xFFFFu, m >> 16);
+        uint32_t m = rowm[i];
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         const int r = r0 + row_base + 16 * i;
-        if (row_bits != nullptr && ch == 0 && r < rows && m != 0)
-            atomicMax(row_bits + r, m << 16);  // result unused: a non-blocking reduction
-    }
-    if (col_bits == nullptr) return;
-    // lanes t and t ^ 16 hold the same columns for two row groups
-    cm.x = __vmaxu2(cm.x, __shfl_xor_sync(0xFFFFFFFFu, cm.x, 16));
-    cm.y = __vmaxu2(cm.y, __shfl_xor_sync(0xFFFFFFFFu, cm.y, 16));
-    cm.z = __vmaxu2(cm.z, __shfl_xor_sync(0xFFFFFFFFu, cm.z, 16));
-    cm.w = __vmaxu2(cm.w, __shfl_xor_sync(0xFFFFFFFFu, cm.w, 16));
-    const int warp = t / 32, lane = t % 32;
-    if (lane < 16) {
-        col_part[warp][4 * ch + 0] = cm.x;
-        col_part[warp][4 * ch + 1] = cm.y;
-        col_part[warp][4 * ch + 2] = cm.z;
-        col_part[warp][4 * ch + 3] = cm.w;
-    }
-    __syncthreads();
-    if (t < kTile / 2) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) m = __vmaxu2(m, col_part[w][t]);
-        const int c = c0 + 2 * t;
-        if (c < cols) {
-            const uint32_t lo = (m & 0xFFFFu) << 16, hi = m & 0xFFFF0000u;
-            if (lo != 0) atomicMax(col_bits + c, lo);
-            if (hi != 0) atomicMax(col_bits + c + 1, hi);
-        }
+        if (ch == 0 && r < rows && m != 0) atomicMax(row_bits + r, m << 16);  // result unused: a reduction
     }
 }
 
@@ -174,9 +202,10 @@ extern "C" fp8lin_status fp8lin_amax_rowcol(const void *x, int64_t rows, int64_t
         return FP8LIN_ERR_CUDA;
     if (empty) return FP8LIN_OK;
     const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
-    if (tiles_r * tiles_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
-    amax_rowcol_kernel<<<(int)(tiles_r * tiles_c), 256, 0, stream>>>(
-        static_cast<const uint16_t *>(x), (int)rows, (int)cols, (int)tiles_c,
+    const int64_t strips_c = (tiles_c + kStrip - 1) / kStrip;
+    if (tiles_r * strips_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    amax_rowcol_kernel<<<(int)(tiles_r * strips_c), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(x), (int)rows, (int)cols, (int)strips_c, (int)tiles_c,
         reinterpret_cast<unsigned int *>(row_amax), reinterpret_cast<unsigned int *>(col_amax));
     return check_launch();
 }

@@ -11,7 +11,7 @@ from gpu_helpers import to_dev_bf16
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("scaling", ["dynamic", "block"])
+@pytest.mark.parametrize("scaling", ["dynamic", "block", "mx"])
 def test_linear_step_in_cuda_graph(fp8lin, scaling):
     M, K, N = 640, 384, 1296
     X = to_dev_bf16(wl.generate((M, K), "normal", 1.0, 31, 0))
