@@ -204,3 +204,33 @@ def test_mx_workload_step_matches_oracle(fp8lin, name):
                                                         r["w_n"]["sf"], rm), f"{name} dX")
     assert_gemm_close(pick(dw, rn), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
                                                         r["x_m"]["sf"], rn), f"{name} dW")
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_mx_cast_special_values(fp8lin, fmt):
+    """NaN, +-Inf, signed zeros, bf16 subnormals and the largest bf16 in
+    chosen blocks: a block whose amax is NaN or infinite gets the scale byte
+    0xFF (its codes come out NaN); the other blocks are unaffected."""
+    rows, cols = 128, 256
+    x = wl.generate((rows, cols), "normal", 1.0, 51, 0)
+    x[0, 5] = 0x7FC0            # NaN in row block (0, 0)
+    x[40, 100] = 0xFF80         # -Inf in row block (40, 3)
+    x[70, 200] = 0x7F7F         # largest finite bf16
+    x[3, 33:64] = 0x8000        # -0 across a run
+    x[90, 130:140] = 0x0001     # bf16 subnormals
+    q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    qc = torch.empty_like(q)
+    sr = torch.empty((_atoms(rows, cols),), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((_atoms(cols, rows),), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_cast_mx(to_dev_bf16(x), fmt, q_row=q, sf_row=sr, q_col=qc, sf_col=sc)
+    torch.cuda.synchronize()
+    table = oracle.decode_table(fmt)
+    for along, got_q, got_sf in (("cols", q, sr), ("rows", qc, sc)):
+        ref = oracle.quantize_mx(x, fmt, along)
+        assert np.array_equal(got_sf.cpu().numpy(), _ref_atoms(ref, along, rows, cols)), along
+        assert (ref["sf"] == 0xFF).sum() == 2                 # the NaN and the Inf blocks
+        got = got_q.cpu().numpy()
+        nan_ref = np.isnan(table[ref["q"]])
+        assert nan_ref.sum() == 64                            # every element of those two blocks
+        assert np.isnan(table[got[nan_ref]]).all(), along     # NaN stays NaN (any NaN code)
+        assert np.array_equal(got[~nan_ref], ref["q"][~nan_ref]), along
