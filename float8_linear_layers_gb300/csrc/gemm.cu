@@ -1238,12 +1238,6 @@ static_assert(kMxSlabs == 2 && kMxSlabs * (4 + 8) <= kMxSfSlotCols, "a stage's s
 static_assert((kMxStages * kMxSlabs * (kAStage + kBStage)) % 1024 == 0 && kMxEpiBytes % 1024 == 0,
               "the epilogue staging (64-byte swizzle) and the scale atoms start on aligned offsets");
 
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, uint4 a, uint4 b) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                  "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
