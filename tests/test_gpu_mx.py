@@ -234,3 +234,32 @@ def test_mx_cast_special_values(fp8lin, fmt):
         assert nan_ref.sum() == 64                            # every element of those two blocks
         assert np.isnan(table[got[nan_ref]]).all(), along     # NaN stays NaN (any NaN code)
         assert np.array_equal(got[~nan_ref], ref["q"][~nan_ref]), along
+
+
+def _fuzz_shapes(n=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    return [tuple(int(16 * rng.integers(1, 66)) for _ in range(3)) for _ in range(n)]
+
+
+@pytest.mark.parametrize("M,K,N", _fuzz_shapes())
+def test_mx_fuzz_shapes(fp8lin, M, K, N):
+    """Seeded random shapes (multiples of 16 from 16 to 1040): the device
+    casts of X, W, dY and the three GEMMs on them against the oracle."""
+    X = wl.generate((M, K), "normal", 1.0, M + K, wl.X)
+    W = wl.generate((N, K), "normal", 0.02, N + K, wl.W)
+    dY = wl.generate((M, N), "laplace", 1e-3, M + N, wl.DY)
+    lin = fp8lin.Float8Linear(M, K, N, scaling="mx")
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    r = oracle.quantize_mx_recipe(X, W, dY)
+    for key, (q, atoms) in (("x_k", (lin.x8.q, lin.x8.sf_row)), ("w_n", (lin.w8.qc, lin.w8.sf_col)),
+                            ("dy_m", (lin.dy8.qc, lin.dy8.sf_col))):
+        assert np.array_equal(q.cpu().numpy(), r[key]["q"]), key
+        assert np.array_equal(atoms.cpu().numpy(), r[key]["atoms"].reshape(-1)), key
+    assert_gemm_close(bf16_to_f64(y), oracle.fwd_mx_ref(r["x_k"]["q"], r["x_k"]["sf"], r["w_k"]["q"],
+                                                        r["w_k"]["sf"]), f"Y {M}x{K}x{N}")
+    assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_mx_ref(r["dy_n"]["q"], r["dy_n"]["sf"], r["w_n"]["q"],
+                                                           r["w_n"]["sf"]), f"dX {M}x{K}x{N}")
+    assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
+                                                           r["x_m"]["sf"]), f"dW {M}x{K}x{N}")
