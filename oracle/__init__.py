@@ -110,6 +110,10 @@ def _load():
         lib.orc_pow2_scale_byte.argtypes = [f32, f32]
         lib.orc_pow2_scale_bytes.restype = None
         lib.orc_pow2_scale_bytes.argtypes = [ctypes.c_void_p, i64, f32, ctypes.c_void_p]
+        lib.orc_ocp_scale_byte.restype = ctypes.c_uint8
+        lib.orc_ocp_scale_byte.argtypes = [f32, ctypes.c_int]
+        lib.orc_ocp_scale_bytes.restype = None
+        lib.orc_ocp_scale_bytes.argtypes = [ctypes.c_void_p, i64, ctypes.c_int, ctypes.c_void_p]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -436,18 +440,32 @@ def pow2_inverse(sf: np.ndarray) -> np.ndarray:
     return np.where(b == 0xFF, np.float32(np.nan), s).astype(np.float32)
 
 
-def quantize_mx(x_bits: np.ndarray, fmt: int, along: str, fmt_max: float = FMT_MAX) -> dict:
+def ocp_scale_bytes(amax_values: np.ndarray, fmt: int) -> np.ndarray:
+    """The OCP Microscaling rule, in C: byte 127 + floor(log2 amax) - emax_elem
+    (emax_elem 8 for e4m3, 15 for e5m2), i.e. the code of the shared scale
+    X = 2^(floor(log2 amax) - emax_elem) by which the elements are divided;
+    0 for a zero amax, 0xFF for a NaN or infinite one; clamped to 0 .. 254."""
+    a = np.ascontiguousarray(amax_values, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    _load().orc_ocp_scale_bytes(_ptr(a), a.size, int(fmt), _ptr(out))
+    return out
+
+
+def quantize_mx(x_bits: np.ndarray, fmt: int, along: str, fmt_max: float = FMT_MAX, rule: str = "floor") -> dict:
     """Block scaling with power-of-two scales: x cut into 1 x 32 blocks
     (along="cols": each row's runs of 32 columns) or 32 x 1 blocks
     (along="rows": each column's runs of 32 rows), blocks at the edge cut
-    short; each block's amax, its scale 2^e (pow2_scale_bytes) and the
-    saturating round-to-nearest-even cast of fp32(x) * 2^e (the product is
-    exact).  Returns amax and sf ([ceil(rows/32) x cols] or [rows x
-    ceil(cols/32)], like the blocks), scale = 2^e and q (row-major, like x)."""
+    short; each block's amax, its scale 2^e and the saturating
+    round-to-nearest-even cast of fp32(x) * 2^e (the product is exact).
+    rule="floor": 2^e the largest power of two with amax * 2^e <= fmt_max
+    (pow2_scale_bytes); rule="ocp": the OCP Microscaling rule
+    (ocp_scale_bytes; fmt_max unused).  Returns amax and sf ([ceil(rows/32) x
+    cols] or [rows x ceil(cols/32)], like the blocks), scale = 2^e and q
+    (row-major, like x)."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     br, bc = (1, MX_BLOCK) if along == "cols" else (MX_BLOCK, 1)
     a = amax_blocks(x, br, bc)
-    sf = pow2_scale_bytes(a, fmt_max)
+    sf = pow2_scale_bytes(a, fmt_max) if rule == "floor" else ocp_scale_bytes(a, fmt)
     s = pow2_scale(sf)
     return {"amax": a, "sf": sf, "scale": s, "q": cast_blocks(x, fmt, br, bc, s)}
 

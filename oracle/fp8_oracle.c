@@ -454,6 +454,32 @@ uint8_t orc_pow2_scale_byte(float amax, float fmt_max) {
     return (uint8_t)(127 - e);
 }
 
+/* The OCP Microscaling (MX) rule for the same blocks: the block's shared
+ * scale is X = 2^(floor(log2 amax) - emax_elem), emax_elem the exponent of
+ * the element format's largest normal (8 for e4m3, 15 for e5m2), and the
+ * elements are x / X cast with saturation -- magnitudes in (fmt_max, 2^(emax+1))
+ * saturate.  A zero amax gives the smallest scale (2^-127), a NaN or infinite
+ * amax 0xFF.  Returned as the byte 127 + log2 X (the code of X, which is the
+ * inverse scale here: the cast multiplies by 1 / X), clamped to [0, 254].
+ * floor(log2 amax) is found by search: the largest f with 2^f <= amax. */
+uint8_t orc_ocp_scale_byte(float amax, int fmt) {
+    if (!(amax <= 3.4028234663852886e38f)) return 0xFF;  /* NaN or +Inf */
+    if (amax == 0.0f) return 0;
+    const int emax = fmt == ORC_E4M3 ? 8 : 15;
+    const double a = (double)amax;
+    int f = 0;
+    while (f > -400 && ldexp(1.0, f) > a) --f;
+    while (f < 400 && ldexp(1.0, f + 1) <= a) ++f;
+    int b = 127 + f - emax;
+    if (b < 0) b = 0;
+    if (b > 254) b = 254;
+    return (uint8_t)b;
+}
+
+void orc_ocp_scale_bytes(const float *amax, int64_t n, int fmt, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_ocp_scale_byte(amax[i], fmt);
+}
+
 /* orc_pow2_scale_byte applied to n amax values. */
 void orc_pow2_scale_bytes(const float *amax, int64_t n, float fmt_max, uint8_t *out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_pow2_scale_byte(amax[i], fmt_max);

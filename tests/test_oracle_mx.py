@@ -199,3 +199,65 @@ def test_scale_atom_layout(P, K):
     if P > 130 and nj > 5:
         # row 130 (second row block), block 5 (second contraction block): atom (1, 1), 16 * 2 + 0 + 1
         assert atoms[1, 1, 33] == sf[130, 5]
+
+
+# ---------------------------------------------------------------- OCP rule
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_ocp_rule_against_its_definition(fmt):
+    """byte = 127 + floor(log2 amax) - emax (8 for e4m3, 15 for e5m2), with
+    floor(log2 amax) checked in exact rationals: 2^f <= amax < 2^(f + 1)."""
+    emax = 8 if fmt == E4M3 else 15
+    rng = np.random.default_rng(9)
+    amax = np.concatenate([np.ldexp(rng.uniform(1.0, 2.0, 3000), rng.integers(-140, 128, 3000)),
+                           np.ldexp(1.0, np.arange(-140, 128))]).astype(np.float32)
+    amax = amax[np.isfinite(amax) & (amax > 0)]
+    got = oracle.ocp_scale_bytes(amax, fmt)
+    for a, b in zip(amax, got):
+        fa = Fraction(float(a))
+        f = int(b) - 127 + emax
+        if b == 0:
+            assert fa < Fraction(2) ** (emax - 126), a
+        elif b == 254:
+            assert fa >= Fraction(2) ** (127 + emax), a
+        else:
+            assert Fraction(2) ** f <= fa < Fraction(2) ** (f + 1), (a, b)
+
+
+def test_ocp_rule_hand_cases():
+    cases = [(448.0, E4M3, 127), (500.0, E4M3, 127), (1.0, E4M3, 119), (0.0, E4M3, 0),
+             (57344.0, E4M3, 134), (448.0, E5M2, 120), (57344.0, E5M2, 127), (65000.0, E5M2, 127)]
+    for a, fmt, want in cases:
+        assert int(oracle.ocp_scale_bytes(np.array([a], np.float32), fmt)[0]) == want, (a, fmt)
+    assert oracle.ocp_scale_bytes(np.array([np.inf, np.nan], np.float32), E4M3).tolist() == [255, 255]
+
+
+@pytest.mark.parametrize("fmt,fmt_max", [(E4M3, 448.0), (E5M2, 57344.0)])
+def test_ocp_rule_is_the_floor_rule_or_one_binade_above(fmt, fmt_max):
+    """With fmt_max the format's own maximum (1.75 x 2^emax) the OCP scale is
+    the no-saturation rule's scale, or twice it exactly when the block's
+    amax scaled into [2^emax, 2^(emax+1)) exceeds fmt_max (and then that
+    block's top values saturate)."""
+    rng = np.random.default_rng(10)
+    amax = np.ldexp(rng.uniform(1.0, 2.0, 5000), rng.integers(-20, 20, 5000)).astype(np.float32)
+    fl = oracle.pow2_scale_bytes(amax, fmt_max).astype(int)
+    oc = oracle.ocp_scale_bytes(amax, fmt).astype(int)
+    mant = np.frexp(amax.astype(np.float64))[0] * 2.0          # amax = mant * 2^f, mant in [1, 2)
+    assert np.array_equal(fl - oc, (mant > 1.75).astype(int))
+
+
+@pytest.mark.parametrize("along", ["cols", "rows"])
+def test_ocp_quantize_saturates_only_the_top_of_the_top_binade(along):
+    x = wl.generate((96, 80), "normal", 1.0, 26, 0)
+    m = oracle.quantize_mx(x, E4M3, along, rule="ocp")
+    xf = np.abs(wl.bf16_bits_to_f32(x).astype(np.float64))
+    dec = np.abs(oracle.decode_table(E4M3))
+    br, bc = (1, 32) if along == "cols" else (32, 1)
+    for i in range(m["amax"].shape[0]):
+        for j in range(m["amax"].shape[1]):
+            blk = xf[br * i:br * (i + 1), bc * j:bc * (j + 1)] * float(m["scale"][i, j])
+            assert 256.0 <= blk.max() < 512.0                 # the top magnitude in [2^8, 2^9)
+            qb = dec[m["q"][br * i:br * (i + 1), bc * j:bc * (j + 1)]]
+            sat = blk > 448.0
+            assert np.all(qb[sat] == 448.0)                   # above the format's maximum: saturated
+            assert np.all(np.abs(qb[~sat] - blk[~sat]) <= 2.0 ** -4 * np.maximum(blk[~sat], 2.0 ** -6))
