@@ -46,7 +46,7 @@ ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_s
                 "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
                 "fp8lin_cast_blockwise", "fp8lin_fwd_block", "fp8lin_dgrad_block", "fp8lin_wgrad_block",
                 "fp8lin_fwd_rowwise", "fp8lin_dgrad_rowwise", "fp8lin_wgrad_rowwise",
-                "fp8lin_cast_mx", "fp8lin_fwd_mx", "fp8lin_dgrad_mx", "fp8lin_wgrad_mx",
+                "fp8lin_cast_mx", "fp8lin_cast_mx_ocp", "fp8lin_fwd_mx", "fp8lin_dgrad_mx", "fp8lin_wgrad_mx",
                 "fp8lin_status_str", "fp8lin_device_error", "fp8lin_selftest_bounded_wait")
 
 
@@ -98,6 +98,7 @@ SIGNATURES = {
     "fp8lin_dgrad_mn": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_wgrad_mn": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_cast_mx": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_cast_mx_ocp": [_vp, _i64, _i64, _ci, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_fwd_mx": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_dgrad_mx": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "fp8lin_wgrad_mx": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
@@ -304,9 +305,13 @@ def sf_atom_bytes(P: int, K: int) -> int:
 
 
 def fp8lin_cast_mx(x: torch.Tensor, fmt: int, q_row=None, sf_row=None, q_col=None, sf_col=None,
-                   fmt_max: float = FMT_MAX, stream=None) -> None:
+                   fmt_max: float = FMT_MAX, stream=None, rule: str = "floor") -> None:
     """Power-of-two block scaling in one pass: q_row / sf_row (1 x 32 blocks; sf_row holds
-    sf_atom_bytes(rows, cols) bytes), q_col / sf_col (32 x 1 blocks; sf_atom_bytes(cols, rows))."""
+    sf_atom_bytes(rows, cols) bytes), q_col / sf_col (32 x 1 blocks; sf_atom_bytes(cols, rows)).
+    rule="floor": the largest power of two not above fmt_max / amax (fp8lin_cast_mx);
+    rule="ocp": the OCP Microscaling rule (fp8lin_cast_mx_ocp; fmt_max unused)."""
+    if rule not in ("floor", "ocp"):
+        raise ValueError(f"unknown rule {rule!r}")
     _dev(x, "x", torch.bfloat16)
     if x.dim() != 2:
         raise ValueError("x must be a 2-D [rows x cols] matrix")
@@ -319,6 +324,10 @@ def fp8lin_cast_mx(x: torch.Tensor, fmt: int, q_row=None, sf_row=None, q_col=Non
             raise ValueError(f"q_{n} must be [{rows} x {cols}]")
         if sf is not None and sf.numel() != nbytes:
             raise ValueError(f"sf_{n} must hold {nbytes} bytes, got {sf.numel()}")
+    if rule == "ocp":
+        _check("fp8lin_cast_mx_ocp", _lib.fp8lin_cast_mx_ocp(_ptr(x), rows, cols, int(fmt), _ptr(q_row), _ptr(sf_row),
+                                                             _ptr(q_col), _ptr(sf_col), _stream(stream)))
+        return
     _check("fp8lin_cast_mx", _lib.fp8lin_cast_mx(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(q_row),
                                                  _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _stream(stream)))
 
@@ -474,14 +483,20 @@ class Float8Tensor:
               "mx":      power-of-two scales in blocks of 32 along the
                          contraction, applied by the tensor cores, one pass
                          with no amax call: q in 1 x 32 blocks (scale atoms
-                         sf_row) and qc in 32 x 1 blocks (sf_col)."""
+                         sf_row) and qc in 32 x 1 blocks (sf_col); mx_rule
+                         "floor" (the largest power of two not above
+                         fmt_max / amax) or "ocp" (the OCP Microscaling rule)."""
 
     def __init__(self, rows: int, cols: int, fmt: int, device, fmt_max: float = FMT_MAX,
-                 scaling: str = "dynamic", history_len: int = 16, transpose: bool = True, blocks: str = "rowcol"):
+                 scaling: str = "dynamic", history_len: int = 16, transpose: bool = True, blocks: str = "rowcol",
+                 mx_rule: str = "floor"):
         if scaling not in ("dynamic", "delayed", "static", "rowwise", "block", "mx"):
             raise ValueError(f"unknown scaling {scaling!r}")
         if scaling == "mx":
+            if mx_rule not in ("floor", "ocp"):
+                raise ValueError(f"unknown mx_rule {mx_rule!r}")
             self.rows, self.cols, self.fmt, self.fmt_max, self.scaling = rows, cols, fmt, fmt_max, scaling
+            self.mx_rule = mx_rule
             self.q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
             self.qc = torch.empty((rows, cols), dtype=torch.uint8, device=device)
             self.qT = None
@@ -530,7 +545,7 @@ class Float8Tensor:
         """Scale, cast and transpose x according to this tensor's scaling."""
         if self.scaling == "mx":
             fp8lin_cast_mx(x, self.fmt, q_row=self.q, sf_row=self.sf_row, q_col=self.qc, sf_col=self.sf_col,
-                           fmt_max=self.fmt_max, stream=stream)
+                           fmt_max=self.fmt_max, stream=stream, rule=self.mx_rule)
         elif self.scaling == "block":
             if self.blocks == "rowcol":
                 fp8lin_cast_blockwise(x, self.fmt, q_row=self.q, inv_row=self.row_inv, q_col=self.qc,
@@ -573,15 +588,16 @@ class Float8Linear:
     for row-wise scaling)."""
 
     def __init__(self, M: int, K: int, N: int, device="cuda", fmt_max: float = FMT_MAX,
-                 scaling: str = "dynamic", history_len: int = 16, transpose: bool | None = None):
+                 scaling: str = "dynamic", history_len: int = 16, transpose: bool | None = None,
+                 mx_rule: str = "floor"):
         self.M, self.K, self.N = M, K, N
         self.transpose = (scaling == "rowwise") if transpose is None else bool(transpose)
         if scaling in ("block", "mx") and self.transpose:
             raise ValueError("block scaling writes no transposed copies")
         args = (device, fmt_max, scaling, history_len, self.transpose)
-        self.x8 = Float8Tensor(M, K, E4M3, *args, blocks="rowcol")
-        self.w8 = Float8Tensor(N, K, E4M3, *args, blocks="tile")
-        self.dy8 = Float8Tensor(M, N, E5M2, *args, blocks="rowcol")
+        self.x8 = Float8Tensor(M, K, E4M3, *args, blocks="rowcol", mx_rule=mx_rule)
+        self.w8 = Float8Tensor(N, K, E4M3, *args, blocks="tile", mx_rule=mx_rule)
+        self.dy8 = Float8Tensor(M, N, E5M2, *args, blocks="rowcol", mx_rule=mx_rule)
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=device)

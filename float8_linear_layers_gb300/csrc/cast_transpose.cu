@@ -492,6 +492,23 @@ __device__ __forceinline__ uint32_t pow2_scale_byte(uint32_t amax_bits, uint32_t
     return (uint32_t)(127 - e);
 }
 
+// The OCP Microscaling rule: the byte of the shared scale
+// X = 2^(floor(log2 amax) - emax) (emax 8 for e4m3, 15 for e5m2), by which the
+// elements are divided; floor(log2 amax) is the exponent field minus 127 for
+// a normal amax, so the byte is the exponent field minus emax (0 for a zero
+// or subnormal amax), clamped to 0 .. 254; 0xFF for a NaN or infinite amax.
+__device__ __forceinline__ uint32_t ocp_scale_byte(uint32_t amax_bits, int emax) {
+    if (amax_bits >= 0x7F800000u) return 0xFFu;
+    const int b = (int)(amax_bits >> 23) - emax;
+    return (uint32_t)(b < 0 ? 0 : (b > 254 ? 254 : b));
+}
+
+// The block's scale byte under either rule (ocp_emax 0: the largest power of
+// two not above fmt_max / amax).
+__device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits, uint32_t fmax_bits, int ocp_emax) {
+    return ocp_emax ? ocp_scale_byte(amax_bits, ocp_emax) : pow2_scale_byte(amax_bits, fmax_bits);
+}
+
 // 2^e from the byte 127 - e (2^-127 is the subnormal 0x00400000; NaN for 0xFF).
 __device__ __forceinline__ float pow2_from_byte(uint32_t b) {
     if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
@@ -515,7 +532,7 @@ __device__ __forceinline__ float pow2_from_byte(uint32_t b) {
 template <int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kThreads)
 cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, uint32_t fmax_bits,
-               uint8_t *__restrict__ q_row, uint8_t *__restrict__ sf_row, uint8_t *__restrict__ q_col,
+               int ocp_emax, uint8_t *__restrict__ q_row, uint8_t *__restrict__ sf_row, uint8_t *__restrict__ q_col,
                uint8_t *__restrict__ sf_col) {
     __shared__ uint32_t col_part[COL ? kThreads / 32 : 1][4][kTile];  // per-warp maxima of the four row runs
     __shared__ __align__(16) float col_scale[COL ? 4 : 1][kTile];
@@ -564,7 +581,7 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
             uint32_t m = rowm[i];
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            rbyte[i] = pow2_scale_byte(m << 16, fmax_bits);
+            rbyte[i] = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
         }
     }
     if (COL) {
@@ -589,7 +606,7 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
             uint32_t m = 0;
 #pragma unroll
             for (int w = 0; w < kThreads / 32; ++w) m = max(m, col_part[w][b][c]);
-            const uint32_t byte = pow2_scale_byte(m << 16, fmax_bits);
+            const uint32_t byte = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
             col_scale[b][c] = pow2_from_byte(byte);
             if (c0 + c < cols && r0 + 32 * b < rows)
                 reinterpret_cast<uint8_t *>(atom_col)[16 * (c % 32) + 4 * (c / 32) + b] = (uint8_t)byte;
@@ -627,29 +644,29 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
 
 template <int FMT, bool ROW, bool COL>
 fp8lin_status launch_mx(int device, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
-                        int tiles_r, int tiles_c, uint32_t fmax_bits, uint8_t *q_row, uint8_t *sf_row,
-                        uint8_t *q_col, uint8_t *sf_col) {
+                        int tiles_r, int tiles_c, uint32_t fmax_bits, int ocp_emax, uint8_t *q_row,
+                        uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col) {
     // carveout slots 10..12 (e4m3) and 13..15 (e5m2), one per combination of copies
     const int slot = 10 + (FMT == FP8LIN_E4M3 ? 0 : 3) + (ROW ? 1 : 0) + (COL ? 2 : 0) - 1;
     fp8lin_status st = fp8lin::prefer_max_shared_carveout(
         reinterpret_cast<const void *>(&cast_mx_kernel<FMT, ROW, COL>), device, slot);
     if (st != FP8LIN_OK) return st;
-    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits, q_row,
-                                                                sf_row, q_col, sf_col);
+    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax,
+                                                                q_row, sf_row, q_col, sf_col);
     return FP8LIN_OK;
 }
 
 template <int FMT>
 fp8lin_status launch_mx_any(int device, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
-                            int tiles_r, int tiles_c, uint32_t fmax_bits, uint8_t *qr, uint8_t *sr, uint8_t *qc,
-                            uint8_t *sc) {
+                            int tiles_r, int tiles_c, uint32_t fmax_bits, int ocp_emax, uint8_t *qr, uint8_t *sr,
+                            uint8_t *qc, uint8_t *sc) {
     if (qr != nullptr && qc != nullptr)
-        return launch_mx<FMT, true, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, qr, sr,
+        return launch_mx<FMT, true, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr,
                                           qc, sc);
     if (qr != nullptr)
-        return launch_mx<FMT, true, false>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, qr, sr,
+        return launch_mx<FMT, true, false>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr,
                                            qc, sc);
-    return launch_mx<FMT, false, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, qr, sr, qc,
+    return launch_mx<FMT, false, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr, qc,
                                        sc);
 }
 
@@ -777,9 +794,11 @@ extern "C" fp8lin_status fp8lin_cast_transpose_rowwise(const void *x, int64_t ro
                        stream, col_amax, col_inv_scale);
 }
 
-extern "C" fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
-                                        uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col,
-                                        cudaStream_t stream) {
+namespace {
+
+// Checks and launch shared by the two power-of-two scale rules.
+fp8lin_status cast_mx_common(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max, int ocp_emax,
+                             uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col, cudaStream_t stream) {
     using namespace fp8lin;
     if ((q_row == nullptr) != (sf_row == nullptr) || (q_col == nullptr) != (sf_col == nullptr))
         return FP8LIN_ERR_INVALID_ARG;
@@ -805,11 +824,27 @@ extern "C" fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t col
     memcpy(&fmax_bits, &fmt_max, 4);
     const uint16_t *xs = static_cast<const uint16_t *>(x);
     st = fmt == FP8LIN_E4M3 ? launch_mx_any<FP8LIN_E4M3>(dev.device, grid, stream, xs, (int)rows, (int)cols,
-                                                         (int)tiles_r, (int)tiles_c, fmax_bits, q_row, sf_row, q_col,
-                                                         sf_col)
+                                                         (int)tiles_r, (int)tiles_c, fmax_bits, ocp_emax, q_row,
+                                                         sf_row, q_col, sf_col)
                             : launch_mx_any<FP8LIN_E5M2>(dev.device, grid, stream, xs, (int)rows, (int)cols,
-                                                         (int)tiles_r, (int)tiles_c, fmax_bits, q_row, sf_row, q_col,
-                                                         sf_col);
+                                                         (int)tiles_r, (int)tiles_c, fmax_bits, ocp_emax, q_row,
+                                                         sf_row, q_col, sf_col);
     if (st != FP8LIN_OK) return st;
     return check_launch();
+}
+
+}  // namespace
+
+extern "C" fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
+                                        uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col,
+                                        cudaStream_t stream) {
+    return cast_mx_common(x, rows, cols, fmt, fmt_max, 0, q_row, sf_row, q_col, sf_col, stream);
+}
+
+extern "C" fp8lin_status fp8lin_cast_mx_ocp(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
+                                            uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col,
+                                            cudaStream_t stream) {
+    // the element format's own exponent range fixes the rule (fmt_max only passes the shared checks)
+    const int emax = fmt == FP8LIN_E4M3 ? 8 : 15;
+    return cast_mx_common(x, rows, cols, fmt, 448.0f, emax, q_row, sf_row, q_col, sf_col, stream);
 }

@@ -410,6 +410,21 @@ fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t cols, fp8lin_f
                              cudaStream_t stream);
 
 /*
+ * fp8lin_cast_mx with the OCP Microscaling scale rule instead: the block's
+ * shared scale is X = 2^(floor(log2 amax) - emax), emax the exponent of the
+ * element format's largest normal (8 for e4m3, 15 for e5m2), and the codes
+ * are sat_RNE(fp32(x) / X) -- the top binade's magnitudes above the format's
+ * maximum saturate.  The scale byte is the code of X, 127 + log2 X (0 for an
+ * all-zero block, 0xFF for a NaN or infinite amax, clamped to 0 .. 254), in
+ * the same atoms, so the copies feed the same GEMMs.  For copies exchanged
+ * with other producers of OCP MX data; the pages fix no rule (see
+ * fp8lin_cast_mx for the one that never saturates).  Arguments and errors as
+ * for fp8lin_cast_mx, with no fmt_max.
+ */
+fp8lin_status fp8lin_cast_mx_ocp(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, uint8_t *q_row,
+                                 uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col, cudaStream_t stream);
+
+/*
  * The three GEMMs of a linear on power-of-two block-scaled copies
  * (fp8lin_cast_mx).  The tensor cores apply the scales inside the MMA and
  * accumulate in fp32 across the whole contraction; the result is rounded to

@@ -506,19 +506,19 @@ def unpack_sf(atoms: np.ndarray, P: int, K: int) -> np.ndarray:
     return atoms[(j // 4) + 0 * p, (p // 128) + 0 * j, 16 * (p % 32) + 4 * ((p % 128) // 32) + j % 4]
 
 
-def quantize_mx_recipe(x_bits, w_bits, dy_bits, fmt_max: float = FMT_MAX) -> dict:
+def quantize_mx_recipe(x_bits, w_bits, dy_bits, fmt_max: float = FMT_MAX, rule: str = "floor") -> dict:
     """The FP8 copies of one linear under power-of-two block scaling, each
     with its 32-long blocks along the contraction of the GEMM that reads it:
     X in 1 x 32 (forward, contraction K) and 32 x 1 (weight gradient,
     contraction M); W in 1 x 32 (forward) and 32 x 1 (input gradient,
     contraction N); dY in 1 x 32 (input gradient) and 32 x 1 (weight
     gradient).  Each entry also carries its scales packed as pack_sf lays
-    them out ("atoms") for the GEMM that reads it."""
+    them out ("atoms") for the GEMM that reads it.  rule as for quantize_mx."""
     out = {}
     for name, bits, fmt, along in (("x_k", x_bits, E4M3, "cols"), ("x_m", x_bits, E4M3, "rows"),
                                    ("w_k", w_bits, E4M3, "cols"), ("w_n", w_bits, E4M3, "rows"),
                                    ("dy_n", dy_bits, E5M2, "cols"), ("dy_m", dy_bits, E5M2, "rows")):
-        d = quantize_mx(bits, fmt, along, fmt_max)
+        d = quantize_mx(bits, fmt, along, fmt_max, rule)
         rows, cols = np.asarray(bits).shape
         P, K = (rows, cols) if along == "cols" else (cols, rows)
         d["atoms"] = pack_sf(sf_by_operand_row(d["sf"], along), P, K)

@@ -183,3 +183,15 @@ def test_argument_checks_of_power_of_two_block_entry_points(lib):
     assert cm(a16, 32, 32, 0, 448.0, a16, a8, None, None, None) == 2         # misaligned atoms
     assert cm(V(4098), 32, 32, 0, 448.0, a16, a16, None, None, None) == 2    # misaligned input
     assert cm(a16, 32, 40, 0, 448.0, None, None, a16, a16, None) == 3        # ragged shape
+
+
+def test_argument_checks_of_the_ocp_cast(lib):
+    a16, a8 = V(4096), V(4104)
+    cm = lib.fp8lin_cast_mx_ocp
+    cm.restype = ctypes.c_int
+    cm.argtypes = [V, I, I, ctypes.c_int, V, V, V, V, V]
+    assert cm(a16, 32, 32, 0, a16, None, None, None, None) == 1          # q without scales
+    assert cm(a16, 32, 32, 0, None, None, None, None, None) == 1         # nothing asked for
+    assert cm(a16, 32, 32, 2, a16, a16, None, None, None) == 1           # format
+    assert cm(a16, 32, 32, 0, a16, a8, None, None, None) == 2            # misaligned atoms
+    assert cm(a16, 32, 40, 0, None, None, a16, a16, None) == 3           # ragged shape

@@ -263,3 +263,68 @@ def test_mx_fuzz_shapes(fp8lin, M, K, N):
                                                            r["w_n"]["sf"]), f"dX {M}x{K}x{N}")
     assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
                                                            r["x_m"]["sf"]), f"dW {M}x{K}x{N}")
+
+
+# ------------------------------------------------------- OCP scale rule
+
+@pytest.mark.parametrize("shape", [(16, 16), (48, 80), (384, 1040), (2048, 4096)])
+@pytest.mark.parametrize("fmt,dist", [(E4M3, ("normal", 1.0)), (E5M2, ("laplace", 1e-3))])
+def test_mx_ocp_cast_bit_exact(fp8lin, shape, fmt, dist):
+    """fp8lin_cast_mx_ocp: the OCP Microscaling rule, every code and scale
+    byte bit-exact (the top binade above the format's maximum saturates)."""
+    rows, cols = shape
+    x = wl.generate(shape, *dist, seed=rows * 11 + cols, tensor_id=7, outlier_frac=1e-3)
+    q, qc = Guarded((rows, cols), torch.uint8), Guarded((rows, cols), torch.uint8)
+    sr, sc = Guarded((_atoms(rows, cols),), torch.uint8), Guarded((_atoms(cols, rows),), torch.uint8)
+    fp8lin.fp8lin_cast_mx(to_dev_bf16(x), fmt, q_row=q.t, sf_row=sr.t, q_col=qc.t, sf_col=sc.t, rule="ocp")
+    torch.cuda.synchronize()
+    for along, gq, gs in (("cols", q, sr), ("rows", qc, sc)):
+        ref = oracle.quantize_mx(x, fmt, along, rule="ocp")
+        assert np.array_equal(gs.t.cpu().numpy(), _ref_atoms(ref, along, rows, cols)), along
+        assert np.array_equal(gq.t.cpu().numpy(), ref["q"]), along
+        assert gq.intact() and gs.intact()
+
+
+def test_mx_ocp_cast_zero_and_special_blocks(fp8lin):
+    rows, cols = 64, 128
+    x = wl.generate((rows, cols), "normal", 1.0, 52, 0)
+    x[0:32, 0] = 0                                            # an all-zero 32 x 1 block: scale byte 0
+    x[33, 0:32] = 0                                           # an all-zero 1 x 32 block
+    x[5, 70] = 0x7F80                                         # +Inf
+    x[40, 100] = 0x0003                                       # a bf16 subnormal
+    q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    qc = torch.empty_like(q)
+    sr = torch.empty((_atoms(rows, cols),), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((_atoms(cols, rows),), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_cast_mx(to_dev_bf16(x), E4M3, q_row=q, sf_row=sr, q_col=qc, sf_col=sc, rule="ocp")
+    torch.cuda.synchronize()
+    table = oracle.decode_table(E4M3)
+    for along, gq, gs in (("cols", q, sr), ("rows", qc, sc)):
+        ref = oracle.quantize_mx(x, E4M3, along, rule="ocp")
+        assert np.array_equal(gs.cpu().numpy(), _ref_atoms(ref, along, rows, cols)), along
+        assert (ref["sf"] == 0).sum() >= 1 and (ref["sf"] == 0xFF).sum() == 1
+        got = gq.cpu().numpy()
+        nan_ref = np.isnan(table[ref["q"]])
+        assert np.isnan(table[got[nan_ref]]).all(), along
+        assert np.array_equal(got[~nan_ref], ref["q"][~nan_ref]), along
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 512, 1024), (144, 208, 272)])
+def test_mx_ocp_linear_step_matches_oracle(fp8lin, M, K, N):
+    """Copies cast with the OCP rule feed the same block-scaled GEMMs."""
+    X = wl.generate((M, K), "normal", 1.0, 61, wl.X, outlier_frac=1e-3)
+    W = wl.generate((N, K), "normal", 0.02, 61, wl.W)
+    dY = wl.generate((M, N), "normal", 1e-3, 61, wl.DY)
+    lin = fp8lin.Float8Linear(M, K, N, scaling="mx", mx_rule="ocp")
+    y, dx, dw = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    r = oracle.quantize_mx_recipe(X, W, dY, rule="ocp")
+    assert np.array_equal(lin.x8.q.cpu().numpy(), r["x_k"]["q"])
+    assert np.array_equal(lin.dy8.sf_col.cpu().numpy(), r["dy_m"]["atoms"].reshape(-1))
+    assert_gemm_close(bf16_to_f64(y), oracle.fwd_mx_ref(r["x_k"]["q"], r["x_k"]["sf"], r["w_k"]["q"],
+                                                        r["w_k"]["sf"]), "Y")
+    assert_gemm_close(bf16_to_f64(dx), oracle.dgrad_mx_ref(r["dy_n"]["q"], r["dy_n"]["sf"], r["w_n"]["q"],
+                                                           r["w_n"]["sf"]), "dX")
+    assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
+                                                           r["x_m"]["sf"]), "dW")
