@@ -405,10 +405,10 @@ class StepGraph:
     one has finished (FP8 buffers and outputs are reused)."""
 
     def __init__(self, fl, spec: Spec, dev, dev_in, overlap=True, scaling="dynamic", streams=None,
-                 transpose=False):
+                 transpose=False, mx_rule="floor"):
         import torch
         self.fl, self.t, self.spec = fl, torch, spec
-        self.overlap, self.scaling = overlap, scaling
+        self.overlap, self.scaling, self.mx_rule = overlap, scaling, mx_rule
         # one FP8 copy per tensor (backward GEMMs read it MN-major) unless the
         # transposed copies are asked for; row-wise scaling always needs them,
         # block scaling never writes them
@@ -418,7 +418,8 @@ class StepGraph:
         self.t8 = {}
         for key, (rows, cols, fmt, *_) in cast_inputs(spec).items():
             if scaling == "mx":      # every tensor: a 1 x 32 and a 32 x 1 block copy
-                self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=False)
+                self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=False,
+                                               mx_rule=mx_rule)
             elif scaling == "block":   # weights in 128 x 128 blocks, activations and gradients in row / column blocks
                 self.t8[key] = fl.Float8Tensor(rows, cols, fmt, dev, scaling=scaling, transpose=False,
                                                blocks="tile" if key.startswith("w:") else "rowcol")
@@ -564,7 +565,8 @@ def run_e2e(args, fl, spec, dev, host, step, world, dist, barrier):
     for k in range(2):
         din = {key: torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for key, t in pinned.items()}
         g = step if k == 0 else StepGraph(fl, spec, dev, din, overlap=step.overlap, scaling=step.scaling,
-                                          streams=(step.main, step.side), transpose=step.transpose)
+                                          streams=(step.main, step.side), transpose=step.transpose,
+                                          mx_rule=step.mx_rule)
         g.inp = din
         outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in g.outputs()]
         sets.append((g, din, outs))
@@ -649,7 +651,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     host = host_inputs(spec, rank)
     dev_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in host.items()}
     step = StepGraph(fl, spec, dev, dev_in, overlap=not args.serial, scaling=args.scaling,
-                     transpose=args.transpose)
+                     transpose=args.transpose, mx_rule=args.mx_rule)
     stream = step.main
     torch.cuda.set_stream(stream)
 
@@ -771,7 +773,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": spec.name, "scaling": args.scaling, "linears": spec.description,
+        "config": {"workload": spec.name, "scaling": args.scaling + ("-ocp" if args.scaling == "mx" and
+                                                                       args.mx_rule == "ocp" else ""),
+                   "linears": spec.description,
                    "fp8_copies": ("row-major and transposed; backward GEMMs read the transposed copies"
                                   if step.transpose else
                                   "two row-major copies per tensor (blocks along each GEMM's contraction); "
@@ -955,6 +959,9 @@ def main():
     ap.add_argument("--workload", choices=sorted(SPECS), default="ffn8b")
     ap.add_argument("--scaling", choices=["dynamic", "delayed", "rowwise", "block", "mx"], default="dynamic",
                     help="scaling recipe (the headline metric is dynamic per-tensor)")
+    ap.add_argument("--mx-rule", choices=["floor", "ocp"], default="floor",
+                    help="power-of-two scale rule of --scaling mx: the largest power of two not above "
+                         "fmt_max / amax, or the OCP Microscaling rule")
     ap.add_argument("--serial", action="store_true", help="issue the whole step on one stream")
     ap.add_argument("--transpose", action="store_true",
                     help="casts also write the transposed FP8 copies and the backward GEMMs read those "

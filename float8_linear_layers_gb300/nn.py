@@ -17,8 +17,9 @@ composable with autograd).  This module is that swap:
 * ``swap_linear_layers`` -- replaces the eligible nn.Linear modules of a
   model in place.
 
-Scalings: "dynamic" (default), "rowwise", "block" and "mx" (power-of-two
-block scales applied by the tensor cores) are stateless per call.
+Scalings: "dynamic" (default), "rowwise", "block", "mx" (power-of-two
+block scales applied by the tensor cores) and "mx_ocp" (the same with the OCP
+Microscaling scale rule) are stateless per call.
 "delayed" and "static" keep per-tensor state across steps (the TorchTitan
 page, section 3.3, names dynamic, delayed and static scaling): a Float8LinearModule
 holds it as buffers, one per tensor role (X, W, dY) -- an amax history ring
@@ -35,7 +36,7 @@ from . import (E4M3, E5M2, Float8Tensor, fp8lin_dgrad, fp8lin_dgrad_block, fp8li
                fp8lin_dgrad_rowwise, fp8lin_fwd, fp8lin_fwd_block, fp8lin_fwd_mx, fp8lin_fwd_rowwise, fp8lin_wgrad,
                fp8lin_wgrad_block, fp8lin_wgrad_mn, fp8lin_wgrad_mx, fp8lin_wgrad_rowwise)
 
-SCALINGS = ("dynamic", "rowwise", "block", "mx", "delayed", "static")
+SCALINGS = ("dynamic", "rowwise", "block", "mx", "mx_ocp", "delayed", "static")
 STATEFUL = ("delayed", "static")
 ROLES = ("x", "w", "dy")
 
@@ -63,6 +64,8 @@ def _quantize(src: torch.Tensor, fmt: int, scaling: str, blocks: str, role: str,
         if scaling == "delayed":
             owner.history_slot[role], owner.history_seeded[role] = t8.slot, True
         return t8
+    if scaling == "mx_ocp":   # power-of-two blocks with the OCP Microscaling scale rule
+        return Float8Tensor(rows, cols, fmt, src.device, scaling="mx", mx_rule="ocp").quantize(src)
     t8 = Float8Tensor(rows, cols, fmt, src.device, scaling=scaling, transpose=scaling == "rowwise", blocks=blocks)
     return t8.quantize(src)
 

@@ -8,7 +8,7 @@ import workloads as wl
 from gpu_helpers import to_dev_bf16
 
 pytestmark = pytest.mark.gpu
-SCALINGS = ["dynamic", "rowwise", "block", "mx"]
+SCALINGS = ["dynamic", "rowwise", "block", "mx", "mx_ocp"]
 
 
 def _inputs(M, K, N, seed):
@@ -28,7 +28,8 @@ def test_function_matches_the_explicit_step(fp8lin, scaling, lead):
     y = fp8lin.Float8LinearFunction.apply(x, w, scaling)
     assert y.shape == (*lead, N) and y.dtype == torch.bfloat16
     y.backward(to_dev_bf16(dY).reshape(*lead, N))
-    lin = fp8lin.Float8Linear(M, K, N, scaling=scaling)
+    lin = (fp8lin.Float8Linear(M, K, N, scaling="mx", mx_rule="ocp") if scaling == "mx_ocp"
+           else fp8lin.Float8Linear(M, K, N, scaling=scaling))
     y2, dx2, dw2 = lin.step(to_dev_bf16(X), to_dev_bf16(W), to_dev_bf16(dY))
     torch.cuda.synchronize()
     assert fp8lin.fp8lin_device_error() == 0
