@@ -1,7 +1,10 @@
 /*
  * fp8lin.h -- C ABI of the Float8 linear layer hot path for one GB300 GPU
  * (sm_103a): dynamic per-tensor scaling and the three scaled FP8 GEMMs of a
- * linear layer's forward and backward pass.
+ * linear layer's forward and backward pass, with the other scaling recipes
+ * beside it: static and delayed per-tensor scaling, row-wise scales, fp32
+ * block scales (1 x 128 / 128 x 128) and power-of-two block scales per 32
+ * contraction elements applied by the tensor cores.
  *
  * Source of the method: "TorchTitan: a one-stop PyTorch-native solution for
  * production LLM pre-training" (zenmind.me paper analysis), section 3.3
