@@ -22,6 +22,7 @@
 // no separate launch and no host round trip is needed; CTA 0 publishes it.
 // Tiles are visited from the last row block to the first, so that the part of
 // the tensor the preceding amax pass read last is re-read from L2.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <cuda_bf16.h>
@@ -515,7 +516,8 @@ __device__ __forceinline__ float pow2_from_byte(uint32_t b) {
     return b == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - b) << 23);
 }
 
-// One CTA per 128 x 128 tile of x, any of two copies (each row-major like x):
+// A persistent kernel over 128 x 128 tiles of x, any of two copies (each
+// row-major like x):
 //   ROW: 1 x 32 blocks (runs of 32 columns), read by a GEMM whose contraction
 //        runs along the columns, scales in atom (tc, tr);
 //   COL: 32 x 1 blocks (runs of 32 rows), read with the contraction along
@@ -529,147 +531,222 @@ __device__ __forceinline__ float pow2_from_byte(uint32_t b) {
 // Row blocks: the thread's 8-column maximum, then the 4 lanes of a 32-column
 // run (shuffles).  Column blocks: the thread's rows i = 2b, 2b + 1 of run b,
 // the lane 16 apart, then the 8 warps through shared memory.
-// Three CTAs per SM (at most 80 registers): the two-copy form compiles to
-// 102 registers otherwise, and two CTAs per SM keep too few loads in flight
-// (ncu: DRAM 43% busy; the cap spills 8 bytes and casts dY 16% faster).
+// Loads: every thread copies its own 8 x 16 bytes of a tile into its own
+// slots of a shared-memory ring (cp.async, kMxCastStages tiles deep) and
+// reads back only those, so the ring needs no barrier: the CTA keeps the
+// next two tiles in flight while it reduces and casts the current one, and
+// the registers hold one tile.  (One tile per CTA with the loads held in
+// registers had DRAM 52% busy and the SM issuing on 55% of its cycles.)
+constexpr int kMxCastStages = 3;
+constexpr int kMxCastStage = 8 * kThreads * 16;             // one 128 x 128 bf16 tile
+constexpr int kMxCastSmem = kMxCastStages * kMxCastStage;   // dynamic shared memory
+constexpr int kMxCastCtasPerSm = 2;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+
 template <int FMT, bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kMxCastCtasPerSm)
 cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, uint32_t fmax_bits,
                int ocp_emax, uint8_t *__restrict__ q_row, uint8_t *__restrict__ sf_row, uint8_t *__restrict__ q_col,
                uint8_t *__restrict__ sf_col) {
-    __shared__ uint32_t col_part[COL ? kThreads / 32 : 1][4][kTile];  // per-warp maxima of the four row runs
+    extern __shared__ __align__(16) uint8_t ring[];                       // [stages][8][kThreads][16 B]
+    __shared__ __align__(16) uint32_t col_part[COL ? kThreads / 32 : 1][4][kTile / 2];  // packed column pairs
     __shared__ __align__(16) float col_scale[COL ? 4 : 1][kTile];
     __shared__ __align__(16) uint32_t atom_row[ROW ? 128 : 4];
     __shared__ __align__(16) uint32_t atom_col[COL ? 128 : 4];
 
-    const int tr = (int)blockIdx.x / tiles_c, tc = (int)blockIdx.x % tiles_c;
-    const int r0 = tr * kTile, c0 = tc * kTile;
     const int t = threadIdx.x, lane = t % 32, warp = t / 32;
     const int ch = t % 16;        // 8-column chunk of the tile row
     const int row_base = t / 16;  // rows row_base + 16 i
-    const bool col_in = (c0 + ch * 8) < cols;
+    const int num_tiles = tiles_r * tiles_c;
+    const int step = (int)gridDim.x;
     const uint64_t pol = evict_first_policy();
-    uint4 v[8];
+    // slot i of stage s: + (8 s + i) kThreads 16 bytes
+    const uint32_t my_slots = (uint32_t)__cvta_generic_to_shared(ring) + 16u * (uint32_t)t;
+
+    // copies of tile `tile` into stage `s` (a group even when empty, so
+    // that the group count stays in step with the tiles)
+    auto issue = [&](int tile, int s) {
+        if (tile < num_tiles) {
+            const int r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
+            if (c0 + ch * 8 < cols) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = r0 + row_base + 16 * i;
-        v[i] = (col_in && r < rows) ? ld_stream16(x + (int64_t)r * cols + c0 + ch * 8, pol) : make_uint4(0, 0, 0, 0);
-    }
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + row_base + 16 * i;
+                    if (r < rows)
+                        cp_async16(my_slots + (uint32_t)((8 * s + i) * kThreads * 16),
+                                   x + (int64_t)r * cols + c0 + ch * 8);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
     if (t < 128) {
         if (ROW) atom_row[t] = 0x7F7F7F7Fu;
         if (COL) atom_col[t] = 0x7F7F7F7Fu;
     }
-    // magnitudes as bf16 bit patterns without the sign (unsigned order = order of |x|)
-    const uint32_t k = 0x7FFF7FFFu;
-    uint32_t rowm[8];
-    uint32_t colm[4][4];  // [run b][packed column pair j]
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) colm[b][j] = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = v[i].x & k, b = v[i].y & k, c = v[i].z & k, d = v[i].w & k;
-        const uint32_t m = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
-        rowm[i] = max(m & 0xFFFFu, m >> 16);
-        colm[i / 2][0] = __vmaxu2(colm[i / 2][0], a);
-        colm[i / 2][1] = __vmaxu2(colm[i / 2][1], b);
-        colm[i / 2][2] = __vmaxu2(colm[i / 2][2], c);
-        colm[i / 2][3] = __vmaxu2(colm[i / 2][3], d);
-    }
-    uint32_t rbyte[8];
-    if (ROW) {
+    for (int s = 0; s < kMxCastStages - 1; ++s) issue((int)blockIdx.x + s * step, s);
+
+    int stage = 0;
+    for (int tile = (int)blockIdx.x; tile < num_tiles; tile += step) {
+        {
+            // the stage read in the previous tile takes the tile kMxCastStages - 1 ahead
+            const int ahead = stage == 0 ? kMxCastStages - 1 : stage - 1;
+            issue(tile + (kMxCastStages - 1) * step, ahead);
+        }
+        cp_async_wait<kMxCastStages - 1>();   // this tile's group has landed
+        const int tr = tile / tiles_c, tc = tile % tiles_c;
+        const int r0 = tr * kTile, c0 = tc * kTile;
+        const bool col_in = (c0 + ch * 8) < cols;
+        uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            uint32_t m = rowm[i];
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-            rbyte[i] = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
+            const int r = r0 + row_base + 16 * i;
+            v[i] = (col_in && r < rows) ? lds128(my_slots + (uint32_t)((8 * stage + i) * kThreads * 16))
+                                        : make_uint4(0, 0, 0, 0);
         }
-    }
-    if (COL) {
+        stage = stage + 1 == kMxCastStages ? 0 : stage + 1;
+        // magnitudes as bf16 bit patterns without the sign (unsigned order = order of |x|)
+        const uint32_t k = 0x7FFF7FFFu;
+        uint32_t rowm[8];
+        uint32_t colm[4][4];  // [run b][packed column pair j]
 #pragma unroll
         for (int b = 0; b < 4; ++b)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t m = __vmaxu2(colm[b][j], __shfl_xor_sync(0xFFFFFFFFu, colm[b][j], 16));
-                if (lane < 16) {
-                    col_part[warp][b][ch * 8 + 2 * j] = m & 0xFFFFu;
-                    col_part[warp][b][ch * 8 + 2 * j + 1] = m >> 16;
-                }
-            }
-    }
-    __syncthreads();
-    if (COL) {
-        // thread t: column t % 128, runs t / 128 and t / 128 + 2
-        const int c = t % kTile;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int b = t / kTile + 2 * h;
-            uint32_t m = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) m = max(m, col_part[w][b][c]);
-            const uint32_t byte = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
-            col_scale[b][c] = pow2_from_byte(byte);
-            if (c0 + c < cols && r0 + 32 * b < rows)
-                reinterpret_cast<uint8_t *>(atom_col)[16 * (c % 32) + 4 * (c / 32) + b] = (uint8_t)byte;
-        }
-    }
-    if (ROW && (ch & 3) == 0 && col_in) {
+            for (int j = 0; j < 4; ++j) colm[b][j] = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int rr = row_base + 16 * i;
-            if (r0 + rr < rows)
-                reinterpret_cast<uint8_t *>(atom_row)[16 * (rr % 32) + 4 * (rr / 32) + ch / 4] = (uint8_t)rbyte[i];
+            const uint32_t a = v[i].x & k, b = v[i].y & k, c = v[i].z & k, d = v[i].w & k;
+            const uint32_t m = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
+            rowm[i] = max(m & 0xFFFFu, m >> 16);
+            colm[i / 2][0] = __vmaxu2(colm[i / 2][0], a);
+            colm[i / 2][1] = __vmaxu2(colm[i / 2][1], b);
+            colm[i / 2][2] = __vmaxu2(colm[i / 2][2], c);
+            colm[i / 2][3] = __vmaxu2(colm[i / 2][3], d);
         }
-    }
-    __syncthreads();
-    if (ROW && t < 32)
-        reinterpret_cast<uint4 *>(sf_row + ((int64_t)tc * tiles_r + tr) * 512)[t] =
-            reinterpret_cast<const uint4 *>(atom_row)[t];
-    if (COL && t >= 32 && t < 64)
-        reinterpret_cast<uint4 *>(sf_col + ((int64_t)tr * tiles_c + tc) * 512)[t - 32] =
-            reinterpret_cast<const uint4 *>(atom_col)[t - 32];
+        uint32_t rbyte[8];
+        if (ROW) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = r0 + row_base + 16 * i;
-        const bool ok = col_in && r < rows;
-        const int64_t off = (int64_t)r * cols + c0 + ch * 8;
-        if (ROW && ok) st_stream8(q_row + off, cast8<FMT>(v[i], pow2_from_byte(rbyte[i])), pol);
-        if (COL && ok) {
-            const float4 lo = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8]);
-            const float4 hi = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8 + 4]);
-            const float sc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            st_stream8(q_col + off, cast8_each<FMT>(v[i], sc), pol);
+            for (int i = 0; i < 8; ++i) {
+                uint32_t m = rowm[i];
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                rbyte[i] = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
+            }
+        }
+        if (COL) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t m = __vmaxu2(colm[b][j], __shfl_xor_sync(0xFFFFFFFFu, colm[b][j], 16));
+                    if (lane < 16) col_part[warp][b][ch * 4 + j] = m;   // columns ch 8 + 2 j, + 1
+                }
+        }
+        __syncthreads();
+        if (COL) {
+            // thread t: column t % 128, runs t / 128 and t / 128 + 2
+            const int c = t % kTile;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int b = t / kTile + 2 * h;
+                uint32_t m = 0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) m = max(m, (col_part[w][b][c / 2] >> (16 * (c % 2))) & 0xFFFFu);
+                const uint32_t byte = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
+                col_scale[b][c] = pow2_from_byte(byte);
+                if (c0 + c < cols && r0 + 32 * b < rows)
+                    reinterpret_cast<uint8_t *>(atom_col)[16 * (c % 32) + 4 * (c / 32) + b] = (uint8_t)byte;
+            }
+        }
+        if (ROW && (ch & 3) == 0 && col_in) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rr = row_base + 16 * i;
+                if (r0 + rr < rows)
+                    reinterpret_cast<uint8_t *>(atom_row)[16 * (rr % 32) + 4 * (rr / 32) + ch / 4] = (uint8_t)rbyte[i];
+            }
+        }
+        __syncthreads();
+        // the atoms go out and are reset for the next tile (whose writers
+        // start after the next tile's first barrier)
+        if (ROW && t < 32) {
+            uint4 *a = reinterpret_cast<uint4 *>(atom_row) + t;
+            reinterpret_cast<uint4 *>(sf_row + ((int64_t)tc * tiles_r + tr) * 512)[t] = *a;
+            *a = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        }
+        if (COL && t >= 32 && t < 64) {
+            uint4 *a = reinterpret_cast<uint4 *>(atom_col) + (t - 32);
+            reinterpret_cast<uint4 *>(sf_col + ((int64_t)tr * tiles_c + tc) * 512)[t - 32] = *a;
+            *a = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + row_base + 16 * i;
+            const bool ok = col_in && r < rows;
+            const int64_t off = (int64_t)r * cols + c0 + ch * 8;
+            if (ROW && ok) st_stream8(q_row + off, cast8<FMT>(v[i], pow2_from_byte(rbyte[i])), pol);
+            if (COL && ok) {
+                const float4 lo = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8]);
+                const float4 hi = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8 + 4]);
+                const float sc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                st_stream8(q_col + off, cast8_each<FMT>(v[i], sc), pol);
+            }
         }
     }
+    cp_async_wait<0>();   // no copy outlives the CTA (the tail's groups are empty)
 }
 
 template <int FMT, bool ROW, bool COL>
-fp8lin_status launch_mx(int device, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
-                        int tiles_r, int tiles_c, uint32_t fmax_bits, int ocp_emax, uint8_t *q_row,
+fp8lin_status launch_mx(int device, int sm_count, int num_tiles, cudaStream_t stream, const uint16_t *x, int rows,
+                        int cols, int tiles_r, int tiles_c, uint32_t fmax_bits, int ocp_emax, uint8_t *q_row,
                         uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col) {
-    // carveout slots 10..12 (e4m3) and 13..15 (e5m2), one per combination of copies
-    const int slot = 10 + (FMT == FP8LIN_E4M3 ? 0 : 3) + (ROW ? 1 : 0) + (COL ? 2 : 0) - 1;
-    fp8lin_status st = fp8lin::prefer_max_shared_carveout(
-        reinterpret_cast<const void *>(&cast_mx_kernel<FMT, ROW, COL>), device, slot);
-    if (st != FP8LIN_OK) return st;
-    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax,
-                                                                q_row, sf_row, q_col, sf_col);
+    static std::atomic<int> ctas_per_sm[64];   // per device, 0 until the attributes are set
+    if (device < 0 || device >= 64) return FP8LIN_ERR_CUDA;
+    const void *kernel = reinterpret_cast<const void *>(&cast_mx_kernel<FMT, ROW, COL>);
+    int per_sm = ctas_per_sm[device].load(std::memory_order_acquire);
+    if (per_sm == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxCastSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, kMxCastSmem) != cudaSuccess ||
+            per_sm < 1)
+            return FP8LIN_ERR_CUDA;
+        ctas_per_sm[device].store(per_sm, std::memory_order_release);
+    }
+    const int64_t slots = (int64_t)per_sm * sm_count;
+    const int grid = (int)(num_tiles < slots ? num_tiles : slots);
+    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, kMxCastSmem, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits,
+                                                                          ocp_emax, q_row, sf_row, q_col, sf_col);
     return FP8LIN_OK;
 }
 
 template <int FMT>
-fp8lin_status launch_mx_any(int device, int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols,
+fp8lin_status launch_mx_any(int device, int sm_count, int num_tiles, cudaStream_t stream, const uint16_t *x, int rows, int cols,
                             int tiles_r, int tiles_c, uint32_t fmax_bits, int ocp_emax, uint8_t *qr, uint8_t *sr,
                             uint8_t *qc, uint8_t *sc) {
     if (qr != nullptr && qc != nullptr)
-        return launch_mx<FMT, true, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr,
+        return launch_mx<FMT, true, true>(device, sm_count, num_tiles, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr,
                                           qc, sc);
     if (qr != nullptr)
-        return launch_mx<FMT, true, false>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr,
+        return launch_mx<FMT, true, false>(device, sm_count, num_tiles, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr,
                                            qc, sc);
-    return launch_mx<FMT, false, true>(device, grid, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr, qc,
+    return launch_mx<FMT, false, true>(device, sm_count, num_tiles, stream, x, rows, cols, tiles_r, tiles_c, fmax_bits, ocp_emax, qr, sr, qc,
                                        sc);
 }
 
@@ -821,15 +898,15 @@ fp8lin_status cast_mx_common(const void *x, int64_t rows, int64_t cols, fp8lin_f
     if (st != FP8LIN_OK) return st;
     if (empty) return FP8LIN_OK;
     const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
-    if (tiles_r * tiles_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
-    const int grid = (int)(tiles_r * tiles_c);
+    if (tiles_r * tiles_c > INT32_MAX - (1 << 20)) return FP8LIN_ERR_UNSUPPORTED_SHAPE;  // tile + ring lookahead fits an int
+    const int num_tiles = (int)(tiles_r * tiles_c);
     uint32_t fmax_bits;
     memcpy(&fmax_bits, &fmt_max, 4);
     const uint16_t *xs = static_cast<const uint16_t *>(x);
-    st = fmt == FP8LIN_E4M3 ? launch_mx_any<FP8LIN_E4M3>(dev.device, grid, stream, xs, (int)rows, (int)cols,
+    st = fmt == FP8LIN_E4M3 ? launch_mx_any<FP8LIN_E4M3>(dev.device, dev.sm_count, num_tiles, stream, xs, (int)rows, (int)cols,
                                                          (int)tiles_r, (int)tiles_c, fmax_bits, ocp_emax, q_row,
                                                          sf_row, q_col, sf_col)
-                            : launch_mx_any<FP8LIN_E5M2>(dev.device, grid, stream, xs, (int)rows, (int)cols,
+                            : launch_mx_any<FP8LIN_E5M2>(dev.device, dev.sm_count, num_tiles, stream, xs, (int)rows, (int)cols,
                                                          (int)tiles_r, (int)tiles_c, fmax_bits, ocp_emax, q_row,
                                                          sf_row, q_col, sf_col);
     if (st != FP8LIN_OK) return st;
