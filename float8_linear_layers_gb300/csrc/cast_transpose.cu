@@ -516,6 +516,50 @@ __device__ __forceinline__ float pow2_from_byte(uint32_t b) {
     return b == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - b) << 23);
 }
 
+// The bf16 bit pattern of 2^e from the byte 127 - e (the upper half of
+// pow2_from_byte's fp32 pattern: exact, as the value is a power of two).
+__device__ __forceinline__ uint32_t pow2_bf16_from_byte(uint32_t b) {
+    if (b == 0xFFu) return 0x7FC0u;
+    return b == 254u ? 0x0040u : (254u - b) << 7;
+}
+
+// Four bf16 elements (x01, x23) times their power-of-two scales (bf16 pairs
+// s01, s23, same order) to FP8: each product by one mixed-precision FMA
+// (fp32 result = x * s + (-0), rounded once: exact, and equal to
+// __fmul_rn(fp32(x), fp32(s)) bit for bit, the sign of a zero included),
+// then cvt.rn.satfinite as in cvt4.
+template <int FMT>
+__device__ __forceinline__ uint32_t cast4_pow2(uint32_t x01, uint32_t x23, uint32_t s01, uint32_t s23) {
+    uint32_t r;
+#define FP8LIN_CAST4_POW2(CVT)                                                                        \
+    asm("{\n\t.reg .b16 a0, a1, a2, a3, b0, b1, b2, b3, lo, hi;\n\t.reg .f32 p0, p1, p2, p3;\n\t"     \
+        "mov.b32 {a0, a1}, %1;\n\t"                                                                   \
+        "mov.b32 {a2, a3}, %2;\n\t"                                                                   \
+        "mov.b32 {b0, b1}, %3;\n\t"                                                                   \
+        "mov.b32 {b2, b3}, %4;\n\t"                                                                   \
+        "fma.rn.f32.bf16 p0, a0, b0, 0f80000000;\n\t"                                                 \
+        "fma.rn.f32.bf16 p1, a1, b1, 0f80000000;\n\t"                                                 \
+        "fma.rn.f32.bf16 p2, a2, b2, 0f80000000;\n\t"                                                 \
+        "fma.rn.f32.bf16 p3, a3, b3, 0f80000000;\n\t"                                                 \
+        CVT " lo, p1, p0;\n\t"                                                                        \
+        CVT " hi, p3, p2;\n\t"                                                                        \
+        "mov.b32 %0, {lo, hi};\n\t}"                                                                  \
+        : "=r"(r)                                                                                     \
+        : "r"(x01), "r"(x23), "r"(s01), "r"(s23))
+    if (FMT == FP8LIN_E4M3)
+        FP8LIN_CAST4_POW2("cvt.rn.satfinite.e4m3x2.f32");
+    else
+        FP8LIN_CAST4_POW2("cvt.rn.satfinite.e5m2x2.f32");
+#undef FP8LIN_CAST4_POW2
+    return r;
+}
+
+// Eight elements, the scales of each pair packed as in v.
+template <int FMT>
+__device__ __forceinline__ uint2 cast8_pow2(uint4 v, uint4 s) {
+    return make_uint2(cast4_pow2<FMT>(v.x, v.y, s.x, s.y), cast4_pow2<FMT>(v.z, v.w, s.z, s.w));
+}
+
 // A persistent kernel over 128 x 128 tiles of x, any of two copies (each
 // row-major like x):
 //   ROW: 1 x 32 blocks (runs of 32 columns), read by a GEMM whose contraction
@@ -564,7 +608,7 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
                uint8_t *__restrict__ sf_col) {
     extern __shared__ __align__(16) uint8_t ring[];                       // [stages][8][kThreads][16 B]
     __shared__ __align__(16) uint32_t col_part[COL ? kThreads / 32 : 1][4][kTile / 2];  // packed column pairs
-    __shared__ __align__(16) float col_scale[COL ? 4 : 1][kTile];
+    __shared__ __align__(16) uint16_t col_scale[COL ? 4 : 1][kTile];   // bf16 2^e
     __shared__ __align__(16) uint32_t atom_row[ROW ? 128 : 4];
     __shared__ __align__(16) uint32_t atom_col[COL ? 128 : 4];
 
@@ -669,7 +713,7 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
 #pragma unroll
                 for (int w = 0; w < kThreads / 32; ++w) m = max(m, (col_part[w][b][c / 2] >> (16 * (c % 2))) & 0xFFFFu);
                 const uint32_t byte = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
-                col_scale[b][c] = pow2_from_byte(byte);
+                col_scale[b][c] = (uint16_t)pow2_bf16_from_byte(byte);
                 if (c0 + c < cols && r0 + 32 * b < rows)
                     reinterpret_cast<uint8_t *>(atom_col)[16 * (c % 32) + 4 * (c / 32) + b] = (uint8_t)byte;
             }
@@ -700,13 +744,13 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
             const int r = r0 + row_base + 16 * i;
             const bool ok = col_in && r < rows;
             const int64_t off = (int64_t)r * cols + c0 + ch * 8;
-            if (ROW && ok) st_stream8(q_row + off, cast8<FMT>(v[i], pow2_from_byte(rbyte[i])), pol);
-            if (COL && ok) {
-                const float4 lo = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8]);
-                const float4 hi = *reinterpret_cast<const float4 *>(&col_scale[i / 2][ch * 8 + 4]);
-                const float sc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                st_stream8(q_col + off, cast8_each<FMT>(v[i], sc), pol);
+            if (ROW && ok) {
+                const uint32_t s2 = pow2_bf16_from_byte(rbyte[i]) * 0x10001u;
+                st_stream8(q_row + off, cast8_pow2<FMT>(v[i], make_uint4(s2, s2, s2, s2)), pol);
             }
+            if (COL && ok)
+                st_stream8(q_col + off, cast8_pow2<FMT>(v[i], *reinterpret_cast<const uint4 *>(&col_scale[i / 2][ch * 8])),
+                           pol);
         }
     }
     cp_async_wait<0>();   // no copy outlives the CTA (the tail's groups are empty)

@@ -328,3 +328,28 @@ def test_mx_ocp_linear_step_matches_oracle(fp8lin, M, K, N):
                                                            r["w_n"]["sf"]), "dX")
     assert_gemm_close(bf16_to_f64(dw), oracle.wgrad_mx_ref(r["dy_m"]["q"], r["dy_m"]["sf"], r["x_m"]["q"],
                                                            r["x_m"]["sf"]), "dW")
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_mx_ocp_cast_blocks_of_subnormals(fp8lin, fmt):
+    """A 1 x 32 and a 32 x 1 block of bf16 subnormals (signs mixed) under the
+    OCP rule: scale byte 0, the elements multiplied by 2^127 into normal FP8
+    codes.  The kernel's products take the subnormals as they are (no flush
+    to zero); both copies bit-exact against the oracle."""
+    rows, cols = 128, 128
+    x = wl.generate((rows, cols), "normal", 1.0, 53, 0)
+    sub = np.array([0x0001, 0x0003, 0x8001, 0x007F, 0x0040, 0x8055, 0x0000, 0x8000] * 4, np.uint16)
+    x[10, 32:64] = sub                 # a 1 x 32 block of the row copy
+    x[64:96, 7] = sub                  # a 32 x 1 block of the column copy
+    q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    qc = torch.empty_like(q)
+    sr = torch.empty((_atoms(rows, cols),), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((_atoms(cols, rows),), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_cast_mx(to_dev_bf16(x), fmt, q_row=q, sf_row=sr, q_col=qc, sf_col=sc, rule="ocp")
+    torch.cuda.synchronize()
+    for along, got_q, got_sf in (("cols", q, sr), ("rows", qc, sc)):
+        ref = oracle.quantize_mx(x, fmt, along, rule="ocp")
+        blk = ref["sf"][10, 1] if along == "cols" else ref["sf"][2, 7]
+        assert blk == 0, along
+        assert np.array_equal(got_sf.cpu().numpy(), _ref_atoms(ref, along, rows, cols)), along
+        assert np.array_equal(got_q.cpu().numpy(), ref["q"]), along

@@ -261,3 +261,24 @@ def test_ocp_quantize_saturates_only_the_top_of_the_top_binade(along):
             sat = blk > 448.0
             assert np.all(qb[sat] == 448.0)                   # above the format's maximum: saturated
             assert np.all(np.abs(qb[~sat] - blk[~sat]) <= 2.0 ** -4 * np.maximum(blk[~sat], 2.0 ** -6))
+
+
+def test_ocp_block_of_subnormals_hand_codes():
+    """Under the OCP rule a block whose amax is a bf16 subnormal gets the
+    scale byte 0 (X = 2^-127, the elements multiplied by 2^127), so its codes
+    are not zero: 2^-133 -> 2^-6, 3 * 2^-133 -> 1.5 * 2^-5 and the largest
+    bf16 subnormal 127 * 2^-133 -> 1.984375, which rounds to 2 in e4m3 (the
+    halfway point is 1.9375) and in e5m2 (halfway 1.875).  Codes from the
+    formats' fields: e4m3 = sign | exponent + 7 (4 bits) | 3 mantissa bits,
+    e5m2 = sign | exponent + 15 (5 bits) | 2 mantissa bits."""
+    x = np.zeros((1, 32), np.uint16)
+    x[0, 0], x[0, 1], x[0, 2], x[0, 3] = 0x0001, 0x0003, 0x8001, 0x007F
+    want = {E4M3: [0x08, 0x14, 0x88, 0x40], E5M2: [0x24, 0x2A, 0xA4, 0x40]}
+    for fmt in (E4M3, E5M2):
+        m = oracle.quantize_mx(x, fmt, "cols", rule="ocp")
+        assert int(m["sf"][0, 0]) == 0, fmt
+        assert m["q"][0, :4].tolist() == want[fmt], fmt
+        assert (m["q"][0, 4:] == 0).all()
+    # the floor rule floors amax at 1e-12 instead: these elements cast to zero
+    m = oracle.quantize_mx(x, E4M3, "cols")
+    assert set(m["q"][0].tolist()) <= {0x00, 0x80}
