@@ -331,6 +331,77 @@ fp8lin_status set_carveouts(int device) {
     return st;
 }
 
+// The load ring of the persistent block casts: every thread copies its own
+// 8 x 16 bytes of a 128 x 128 tile into its own slots of a shared-memory
+// ring (cp.async) and reads back only those, so the ring needs no barrier
+// and no spin-wait (cp.async.wait_group covers it): a CTA keeps the next
+// kRingStages - 1 tiles in flight while it reduces and casts the current
+// one, and its registers hold one tile.
+constexpr int kRingStages = 3;
+constexpr int kRingStageBytes = 8 * kThreads * 16;             // one 128 x 128 bf16 tile
+constexpr int kRingSmem = kRingStages * kRingStageBytes;   // dynamic shared memory
+constexpr int kRingCtasPerSm = 2;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+
+
+// This thread's view of the ring over x [rows x cols]: it owns the 16-byte
+// chunk ch of rows row_base + 16 i (i < 8) of every tile, in slot i of a
+// stage at ((8 stage + i) kThreads + t) 16 bytes.
+struct TileRing {
+    const uint16_t *x;
+    int rows, cols, tiles_c, num_tiles;
+    int ch, row_base;
+    uint32_t slots;   // shared address of this thread's slot 0 of stage 0
+
+    __device__ __forceinline__ TileRing(const uint16_t *x_, int rows_, int cols_, int tiles_r, int tiles_c_,
+                                        uint8_t *ring)
+        : x(x_), rows(rows_), cols(cols_), tiles_c(tiles_c_), num_tiles(tiles_r * tiles_c_),
+          ch((int)threadIdx.x % 16), row_base((int)threadIdx.x / 16),
+          slots((uint32_t)__cvta_generic_to_shared(ring) + 16u * threadIdx.x) {}
+
+    __device__ __forceinline__ uint32_t slot(int s, int i) const {
+        return slots + (uint32_t)((8 * s + i) * kThreads * 16);
+    }
+    // Copies of tile `tile` into stage s: one commit group even when the tile
+    // does not exist, so that group n is always tile n of this CTA.
+    __device__ __forceinline__ void issue(int tile, int s) const {
+        if (tile < num_tiles) {
+            const int r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
+            if (c0 + ch * 8 < cols) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + row_base + 16 * i;
+                    if (r < rows) cp_async16(slot(s, i), x + (int64_t)r * cols + c0 + ch * 8);
+                }
+            }
+        }
+        cp_async_commit();
+    }
+    // This thread's 8 x 8 elements of a tile from stage s (zero past the edge).
+    __device__ __forceinline__ void read(int r0, int c0, int s, uint4 (&v)[8]) const {
+        const bool col_in = c0 + ch * 8 < cols;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + row_base + 16 * i;
+            v[i] = (col_in && r < rows) ? lds128(slot(s, i)) : make_uint4(0, 0, 0, 0);
+        }
+    }
+};
+
 // ------------------------------------------------------------ block scaling
 
 // Block scaling: every block is scaled like a tensor of its own (amax of the
@@ -345,133 +416,168 @@ fp8lin_status set_carveouts(int device) {
 // that share a row; column maxima over the thread's 8 rows, the lane pair
 // 16 apart, then the 8 warps through shared memory.
 template <int FMT, bool ROW, bool COL, bool TILE>
-__global__ void __launch_bounds__(kThreads)
-cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c, float fmt_max,
+__global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
+cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, float fmt_max,
                   uint8_t *__restrict__ q_row, float *__restrict__ inv_row, uint8_t *__restrict__ q_col,
                   float *__restrict__ inv_col, uint8_t *__restrict__ q_tile, float *__restrict__ inv_tile) {
-    __shared__ uint32_t col_part[COL ? kThreads / 32 : 1][kTile];  // per-warp column maxima (magnitude bits)
-    __shared__ float col_scale[COL ? kTile : 1];
-    __shared__ uint32_t warp_max[kThreads / 32];
+    extern __shared__ __align__(16) uint8_t ring_smem[];                 // [stages][8][kThreads][16 B]
+    __shared__ uint32_t col_part[COL ? kThreads / 32 : 1][kTile / 2];   // per-warp column maxima, packed pairs
+    __shared__ __align__(16) float col_scale[COL ? kTile : 1];
+    __shared__ uint32_t warp_max[2][kThreads / 32];                      // by tile parity
 
-    const int tr = (int)blockIdx.x / tiles_c, tc = (int)blockIdx.x % tiles_c;
-    const int r0 = tr * kTile, c0 = tc * kTile;
     const int t = threadIdx.x, lane = t % 32, warp = t / 32;
     const int ch = t % 16;        // 8-column chunk of the tile row
     const int row_base = t / 16;  // rows row_base + 16 i
-    const bool col_in = (c0 + ch * 8) < cols;
+    const TileRing ring(x, rows, cols, tiles_r, tiles_c, ring_smem);
+    const int num_tiles = ring.num_tiles;
+    const int step = (int)gridDim.x;
     const uint64_t pol = evict_first_policy();
-    uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = r0 + row_base + 16 * i;
-        v[i] = (col_in && r < rows) ? ld_stream16(x + (int64_t)r * cols + c0 + ch * 8, pol) : make_uint4(0, 0, 0, 0);
-    }
+    for (int s = 0; s < kRingStages - 1; ++s) ring.issue((int)blockIdx.x + s * step, s);
 
-    // magnitudes as bf16 bit patterns without the sign: their unsigned order
-    // is the order of |x| (a NaN above everything); zero padding never wins
-    const uint32_t k = 0x7FFF7FFFu;
-    uint32_t rowm[8];
-    uint32_t colm2[4] = {0, 0, 0, 0};  // packed pairs: columns 2j, 2j + 1 of this thread's chunk
+    int stage = 0, parity = 0;
+    for (int tile = (int)blockIdx.x; tile < num_tiles; tile += step) {
+        ring.issue(tile + (kRingStages - 1) * step, stage == 0 ? kRingStages - 1 : stage - 1);
+        cp_async_wait<kRingStages - 1>();
+        const int tr = tile / tiles_c, tc = tile % tiles_c;
+        const int r0 = tr * kTile, c0 = tc * kTile;
+        const bool col_in = (c0 + ch * 8) < cols;
+        uint4 v[8];
+        ring.read(r0, c0, stage, v);
+        stage = stage + 1 == kRingStages ? 0 : stage + 1;
+
+        // magnitudes as bf16 bit patterns without the sign: their unsigned order
+        // is the order of |x| (a NaN above everything); zero padding never wins
+        const uint32_t k = 0x7FFF7FFFu;
+        uint32_t rowm[8];
+        uint32_t colm2[4] = {0, 0, 0, 0};  // packed pairs: columns 2j, 2j + 1 of this thread's chunk
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = v[i].x & k, b = v[i].y & k, c = v[i].z & k, d = v[i].w & k;
-        const uint32_t m = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
-        rowm[i] = max(m & 0xFFFFu, m >> 16);
-        colm2[0] = __vmaxu2(colm2[0], a);
-        colm2[1] = __vmaxu2(colm2[1], b);
-        colm2[2] = __vmaxu2(colm2[2], c);
-        colm2[3] = __vmaxu2(colm2[3], d);
-    }
-    if (ROW) {
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = v[i].x & k, b = v[i].y & k, c = v[i].z & k, d = v[i].w & k;
+            const uint32_t m = __vmaxu2(__vmaxu2(a, b), __vmaxu2(c, d));
+            rowm[i] = max(m & 0xFFFFu, m >> 16);
+            colm2[0] = __vmaxu2(colm2[0], a);
+            colm2[1] = __vmaxu2(colm2[1], b);
+            colm2[2] = __vmaxu2(colm2[2], c);
+            colm2[3] = __vmaxu2(colm2[3], d);
+        }
+        if (ROW) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) rowm[i] = max(rowm[i], __shfl_xor_sync(0xFFFFFFFFu, rowm[i], o));
-    }
-    if (COL) {
+                for (int o = 8; o >= 1; o >>= 1) rowm[i] = max(rowm[i], __shfl_xor_sync(0xFFFFFFFFu, rowm[i], o));
+        }
+        if (COL) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t m = __vmaxu2(colm2[j], __shfl_xor_sync(0xFFFFFFFFu, colm2[j], 16));
-            if (lane < 16) {
-                col_part[warp][ch * 8 + 2 * j] = m & 0xFFFFu;
-                col_part[warp][ch * 8 + 2 * j + 1] = m >> 16;
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t m = __vmaxu2(colm2[j], __shfl_xor_sync(0xFFFFFFFFu, colm2[j], 16));
+                if (lane < 16) col_part[warp][ch * 4 + j] = m;
             }
         }
-    }
-    if (TILE) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m = max(m, rowm[i]);
-        m = __reduce_max_sync(0xFFFFFFFFu, m);
-        if (lane == 0) warp_max[warp] = m;
-    }
-    if (COL || TILE) __syncthreads();
-    if (COL) {
-        if (t < kTile) {
+        if (TILE) {
             uint32_t m = 0;
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) m = max(m, col_part[w][t]);
-            const float s = scale_from_amax(__uint_as_float(m << 16), fmt_max);
-            col_scale[t] = s;
-            if (c0 + t < cols) inv_col[(int64_t)tr * cols + c0 + t] = __frcp_rn(s);
+            for (int i = 0; i < 8; ++i) m = max(m, rowm[i]);
+            m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (lane == 0) warp_max[parity][warp] = m;
         }
-        __syncthreads();
-    }
-    float s_tile = 0.0f;
-    if (TILE) {
-        uint32_t m = 0;
+        if (COL || TILE) __syncthreads();
+        if (COL) {
+            if (t < kTile) {
+                uint32_t m = 0;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) m = max(m, warp_max[w]);
-        s_tile = scale_from_amax(__uint_as_float(m << 16), fmt_max);
-        if (t == 0) inv_tile[(int64_t)tr * tiles_c + tc] = __frcp_rn(s_tile);
-    }
-    float csc[8];
-    if (COL) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) csc[e] = col_scale[ch * 8 + e];
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = r0 + row_base + 16 * i;
-        const bool ok = col_in && r < rows;
-        const int64_t off = (int64_t)r * cols + c0 + ch * 8;
-        if (ROW) {
-            const float s = scale_from_amax(__uint_as_float(rowm[i] << 16), fmt_max);
-            if (ok) st_stream8(q_row + off, cast8<FMT>(v[i], s), pol);
-            if (ch == 0 && r < rows) inv_row[(int64_t)tc * rows + r] = __frcp_rn(s);
+                for (int w = 0; w < kThreads / 32; ++w) m = max(m, (col_part[w][t / 2] >> (16 * (t % 2))) & 0xFFFFu);
+                const float s = scale_from_amax(__uint_as_float(m << 16), fmt_max);
+                col_scale[t] = s;
+                if (c0 + t < cols) inv_col[(int64_t)tr * cols + c0 + t] = __frcp_rn(s);
+            }
+            __syncthreads();
         }
-        if (COL && ok) st_stream8(q_col + off, cast8_each<FMT>(v[i], csc), pol);
-        if (TILE && ok) st_stream8(q_tile + off, cast8<FMT>(v[i], s_tile), pol);
+        float s_tile = 0.0f;
+        if (TILE) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) m = max(m, warp_max[parity][w]);
+            s_tile = scale_from_amax(__uint_as_float(m << 16), fmt_max);
+            if (t == 0) inv_tile[(int64_t)tr * tiles_c + tc] = __frcp_rn(s_tile);
+        }
+        parity ^= 1;
+        float csc[8];
+        if (COL) {
+            const float4 lo = *reinterpret_cast<const float4 *>(&col_scale[ch * 8]);
+            const float4 hi = *reinterpret_cast<const float4 *>(&col_scale[ch * 8 + 4]);
+            csc[0] = lo.x, csc[1] = lo.y, csc[2] = lo.z, csc[3] = lo.w;
+            csc[4] = hi.x, csc[5] = hi.y, csc[6] = hi.z, csc[7] = hi.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + row_base + 16 * i;
+            const bool ok = col_in && r < rows;
+            const int64_t off = (int64_t)r * cols + c0 + ch * 8;
+            if (ROW) {
+                const float s = scale_from_amax(__uint_as_float(rowm[i] << 16), fmt_max);
+                if (ok) st_stream8(q_row + off, cast8<FMT>(v[i], s), pol);
+                if (ch == 0 && r < rows) inv_row[(int64_t)tc * rows + r] = __frcp_rn(s);
+            }
+            if (COL && ok) st_stream8(q_col + off, cast8_each<FMT>(v[i], csc), pol);
+            if (TILE && ok) st_stream8(q_tile + off, cast8<FMT>(v[i], s_tile), pol);
+        }
     }
+    cp_async_wait<0>();   // no copy outlives the CTA (the tail's groups are empty)
+}
+
+// Persistent grid: min(tiles, CTAs per SM x SMs), the attributes set once
+// per kernel and device.
+template <typename Kernel>
+fp8lin_status ring_grid(Kernel kernel, std::atomic<int> (&ctas_per_sm)[64], int device, int sm_count, int num_tiles,
+                        int *grid) {
+    if (device < 0 || device >= 64) return FP8LIN_ERR_CUDA;
+    int per_sm = ctas_per_sm[device].load(std::memory_order_acquire);
+    if (per_sm == 0) {
+        const void *k = reinterpret_cast<const void *>(kernel);
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, kRingSmem) != cudaSuccess ||
+            per_sm < 1)
+            return FP8LIN_ERR_CUDA;
+        ctas_per_sm[device].store(per_sm, std::memory_order_release);
+    }
+    const int64_t slots = (int64_t)per_sm * sm_count;
+    *grid = (int)(num_tiles < slots ? num_tiles : slots);
+    return FP8LIN_OK;
 }
 
 template <int FMT, bool ROW, bool COL, bool TILE>
-fp8lin_status launch_block(int device, int slot, int grid, cudaStream_t stream, const uint16_t *x, int rows,
-                           int cols, int tiles_c, float fmt_max, uint8_t *q_row, float *inv_row, uint8_t *q_col,
-                           float *inv_col, uint8_t *q_tile, float *inv_tile) {
-    fp8lin_status st = fp8lin::prefer_max_shared_carveout(
-        reinterpret_cast<const void *>(&cast_block_kernel<FMT, ROW, COL, TILE>), device, slot);
+fp8lin_status launch_block(int device, int sm_count, int num_tiles, cudaStream_t stream, const uint16_t *x, int rows,
+                           int cols, int tiles_r, int tiles_c, float fmt_max, uint8_t *q_row, float *inv_row,
+                           uint8_t *q_col, float *inv_col, uint8_t *q_tile, float *inv_tile) {
+    static std::atomic<int> ctas_per_sm[64];
+    int grid = 0;
+    const fp8lin_status st =
+        ring_grid(&cast_block_kernel<FMT, ROW, COL, TILE>, ctas_per_sm, device, sm_count, num_tiles, &grid);
     if (st != FP8LIN_OK) return st;
-    cast_block_kernel<FMT, ROW, COL, TILE><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_c, fmt_max, q_row,
-                                                                         inv_row, q_col, inv_col, q_tile, inv_tile);
+    cast_block_kernel<FMT, ROW, COL, TILE><<<grid, kThreads, kRingSmem, stream>>>(
+        x, rows, cols, tiles_r, tiles_c, fmt_max, q_row, inv_row, q_col, inv_col, q_tile, inv_tile);
     return FP8LIN_OK;
 }
 
 template <int FMT>
-fp8lin_status launch_block_any(int device, int which, int grid, cudaStream_t stream, const uint16_t *x, int rows,
-                               int cols, int tiles_c, float fmt_max, uint8_t *qr, float *ir, uint8_t *qc, float *ic,
-                               uint8_t *qt, float *it) {
-    // carveout slots 32.. (e4m3) and 40.. (e5m2), one per combination of copies
-    const int slot = (FMT == FP8LIN_E4M3 ? 32 : 40) + which;
+fp8lin_status launch_block_any(int device, int sm_count, int which, int num_tiles, cudaStream_t stream,
+                               const uint16_t *x, int rows, int cols, int tiles_r, int tiles_c, float fmt_max,
+                               uint8_t *qr, float *ir, uint8_t *qc, float *ic, uint8_t *qt, float *it) {
+#define FP8LIN_BLOCK_LAUNCH(R, C, T) \
+    launch_block<FMT, R, C, T>(device, sm_count, num_tiles, stream, x, rows, cols, tiles_r, tiles_c, fmt_max, qr, ir, qc, ic, qt, it)
     switch (which) {
-        case 1: return launch_block<FMT, true, false, false>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
-        case 2: return launch_block<FMT, false, true, false>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
-        case 3: return launch_block<FMT, true, true, false>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
-        case 4: return launch_block<FMT, false, false, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
-        case 5: return launch_block<FMT, true, false, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
-        case 6: return launch_block<FMT, false, true, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
-        default: return launch_block<FMT, true, true, true>(device, slot, grid, stream, x, rows, cols, tiles_c, fmt_max, qr, ir, qc, ic, qt, it);
+        case 1: return FP8LIN_BLOCK_LAUNCH(true, false, false);
+        case 2: return FP8LIN_BLOCK_LAUNCH(false, true, false);
+        case 3: return FP8LIN_BLOCK_LAUNCH(true, true, false);
+        case 4: return FP8LIN_BLOCK_LAUNCH(false, false, true);
+        case 5: return FP8LIN_BLOCK_LAUNCH(true, false, true);
+        case 6: return FP8LIN_BLOCK_LAUNCH(false, true, true);
+        default: return FP8LIN_BLOCK_LAUNCH(true, true, true);
     }
+#undef FP8LIN_BLOCK_LAUNCH
 }
 
 // ------------------------------------------- power-of-two block scaling
@@ -510,14 +616,8 @@ __device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits, uint32_t f
     return ocp_emax ? ocp_scale_byte(amax_bits, ocp_emax) : pow2_scale_byte(amax_bits, fmax_bits);
 }
 
-// 2^e from the byte 127 - e (2^-127 is the subnormal 0x00400000; NaN for 0xFF).
-__device__ __forceinline__ float pow2_from_byte(uint32_t b) {
-    if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
-    return b == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - b) << 23);
-}
-
-// The bf16 bit pattern of 2^e from the byte 127 - e (the upper half of
-// pow2_from_byte's fp32 pattern: exact, as the value is a power of two).
+// The bf16 bit pattern of 2^e from the byte 127 - e: exponent field 127 + e,
+// no mantissa; 2^-127 is the subnormal 0x0040; NaN for the byte 0xFF.
 __device__ __forceinline__ uint32_t pow2_bf16_from_byte(uint32_t b) {
     if (b == 0xFFu) return 0x7FC0u;
     return b == 254u ? 0x0040u : (254u - b) << 7;
@@ -576,37 +676,17 @@ __device__ __forceinline__ uint2 cast8_pow2(uint4 v, uint4 s) {
 // run (shuffles).  Column blocks: the thread's rows i = 2b, 2b + 1 of run b,
 // the lane 16 apart, then the 8 warps through shared memory.
 // Loads: every thread copies its own 8 x 16 bytes of a tile into its own
-// slots of a shared-memory ring (cp.async, kMxCastStages tiles deep) and
+// slots of a shared-memory ring (cp.async, kRingStages tiles deep) and
 // reads back only those, so the ring needs no barrier: the CTA keeps the
 // next two tiles in flight while it reduces and casts the current one, and
 // the registers hold one tile.  (One tile per CTA with the loads held in
 // registers had DRAM 52% busy and the SM issuing on 55% of its cycles.)
-constexpr int kMxCastStages = 3;
-constexpr int kMxCastStage = 8 * kThreads * 16;             // one 128 x 128 bf16 tile
-constexpr int kMxCastSmem = kMxCastStages * kMxCastStage;   // dynamic shared memory
-constexpr int kMxCastCtasPerSm = 2;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
-                 : "memory");
-    return v;
-}
-
 template <int FMT, bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads, kMxCastCtasPerSm)
+__global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
 cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, uint32_t fmax_bits,
                int ocp_emax, uint8_t *__restrict__ q_row, uint8_t *__restrict__ sf_row, uint8_t *__restrict__ q_col,
                uint8_t *__restrict__ sf_col) {
-    extern __shared__ __align__(16) uint8_t ring[];                       // [stages][8][kThreads][16 B]
+    extern __shared__ __align__(16) uint8_t ring_smem[];                  // [stages][8][kThreads][16 B]
     __shared__ __align__(16) uint32_t col_part[COL ? kThreads / 32 : 1][4][kTile / 2];  // packed column pairs
     __shared__ __align__(16) uint16_t col_scale[COL ? 4 : 1][kTile];   // bf16 2^e
     __shared__ __align__(16) uint32_t atom_row[ROW ? 128 : 4];
@@ -615,56 +695,29 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
     const int t = threadIdx.x, lane = t % 32, warp = t / 32;
     const int ch = t % 16;        // 8-column chunk of the tile row
     const int row_base = t / 16;  // rows row_base + 16 i
-    const int num_tiles = tiles_r * tiles_c;
+    const TileRing ring(x, rows, cols, tiles_r, tiles_c, ring_smem);
+    const int num_tiles = ring.num_tiles;
     const int step = (int)gridDim.x;
     const uint64_t pol = evict_first_policy();
-    // slot i of stage s: + (8 s + i) kThreads 16 bytes
-    const uint32_t my_slots = (uint32_t)__cvta_generic_to_shared(ring) + 16u * (uint32_t)t;
-
-    // copies of tile `tile` into stage `s` (a group even when empty, so
-    // that the group count stays in step with the tiles)
-    auto issue = [&](int tile, int s) {
-        if (tile < num_tiles) {
-            const int r0 = (tile / tiles_c) * kTile, c0 = (tile % tiles_c) * kTile;
-            if (c0 + ch * 8 < cols) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + row_base + 16 * i;
-                    if (r < rows)
-                        cp_async16(my_slots + (uint32_t)((8 * s + i) * kThreads * 16),
-                                   x + (int64_t)r * cols + c0 + ch * 8);
-                }
-            }
-        }
-        cp_async_commit();
-    };
 
     if (t < 128) {
         if (ROW) atom_row[t] = 0x7F7F7F7Fu;
         if (COL) atom_col[t] = 0x7F7F7F7Fu;
     }
 #pragma unroll
-    for (int s = 0; s < kMxCastStages - 1; ++s) issue((int)blockIdx.x + s * step, s);
+    for (int s = 0; s < kRingStages - 1; ++s) ring.issue((int)blockIdx.x + s * step, s);
 
     int stage = 0;
     for (int tile = (int)blockIdx.x; tile < num_tiles; tile += step) {
-        {
-            // the stage read in the previous tile takes the tile kMxCastStages - 1 ahead
-            const int ahead = stage == 0 ? kMxCastStages - 1 : stage - 1;
-            issue(tile + (kMxCastStages - 1) * step, ahead);
-        }
-        cp_async_wait<kMxCastStages - 1>();   // this tile's group has landed
+        // the stage read in the previous tile takes the tile kRingStages - 1 ahead
+        ring.issue(tile + (kRingStages - 1) * step, stage == 0 ? kRingStages - 1 : stage - 1);
+        cp_async_wait<kRingStages - 1>();   // this tile's group has landed
         const int tr = tile / tiles_c, tc = tile % tiles_c;
         const int r0 = tr * kTile, c0 = tc * kTile;
         const bool col_in = (c0 + ch * 8) < cols;
         uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + row_base + 16 * i;
-            v[i] = (col_in && r < rows) ? lds128(my_slots + (uint32_t)((8 * stage + i) * kThreads * 16))
-                                        : make_uint4(0, 0, 0, 0);
-        }
-        stage = stage + 1 == kMxCastStages ? 0 : stage + 1;
+        ring.read(r0, c0, stage, v);
+        stage = stage + 1 == kRingStages ? 0 : stage + 1;
         // magnitudes as bf16 bit patterns without the sign (unsigned order = order of |x|)
         const uint32_t k = 0x7FFF7FFFu;
         uint32_t rowm[8];
@@ -760,23 +813,12 @@ template <int FMT, bool ROW, bool COL>
 fp8lin_status launch_mx(int device, int sm_count, int num_tiles, cudaStream_t stream, const uint16_t *x, int rows,
                         int cols, int tiles_r, int tiles_c, uint32_t fmax_bits, int ocp_emax, uint8_t *q_row,
                         uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col) {
-    static std::atomic<int> ctas_per_sm[64];   // per device, 0 until the attributes are set
-    if (device < 0 || device >= 64) return FP8LIN_ERR_CUDA;
-    const void *kernel = reinterpret_cast<const void *>(&cast_mx_kernel<FMT, ROW, COL>);
-    int per_sm = ctas_per_sm[device].load(std::memory_order_acquire);
-    if (per_sm == 0) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxCastSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, kMxCastSmem) != cudaSuccess ||
-            per_sm < 1)
-            return FP8LIN_ERR_CUDA;
-        ctas_per_sm[device].store(per_sm, std::memory_order_release);
-    }
-    const int64_t slots = (int64_t)per_sm * sm_count;
-    const int grid = (int)(num_tiles < slots ? num_tiles : slots);
-    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, kMxCastSmem, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits,
-                                                                          ocp_emax, q_row, sf_row, q_col, sf_col);
+    static std::atomic<int> ctas_per_sm[64];
+    int grid = 0;
+    const fp8lin_status st = ring_grid(&cast_mx_kernel<FMT, ROW, COL>, ctas_per_sm, device, sm_count, num_tiles, &grid);
+    if (st != FP8LIN_OK) return st;
+    cast_mx_kernel<FMT, ROW, COL><<<grid, kThreads, kRingSmem, stream>>>(x, rows, cols, tiles_r, tiles_c, fmax_bits,
+                                                                        ocp_emax, q_row, sf_row, q_col, sf_col);
     return FP8LIN_OK;
 }
 
@@ -897,14 +939,16 @@ extern "C" fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int6
     if (st != FP8LIN_OK) return st;
     if (empty) return FP8LIN_OK;
     const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
-    if (tiles_r * tiles_c > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
-    const int grid = (int)(tiles_r * tiles_c);
+    if (tiles_r * tiles_c > INT32_MAX - (1 << 20)) return FP8LIN_ERR_UNSUPPORTED_SHAPE;  // tile + ring lookahead fits an int
+    const int num_tiles = (int)(tiles_r * tiles_c);
     const uint16_t *xs = static_cast<const uint16_t *>(x);
     st = fmt == FP8LIN_E4M3
-             ? launch_block_any<FP8LIN_E4M3>(dev.device, which, grid, stream, xs, (int)rows, (int)cols, (int)tiles_c,
-                                             fmt_max, q_row, inv_row, q_col, inv_col, q_tile, inv_tile)
-             : launch_block_any<FP8LIN_E5M2>(dev.device, which, grid, stream, xs, (int)rows, (int)cols, (int)tiles_c,
-                                             fmt_max, q_row, inv_row, q_col, inv_col, q_tile, inv_tile);
+             ? launch_block_any<FP8LIN_E4M3>(dev.device, dev.sm_count, which, num_tiles, stream, xs, (int)rows,
+                                             (int)cols, (int)tiles_r, (int)tiles_c, fmt_max, q_row, inv_row, q_col,
+                                             inv_col, q_tile, inv_tile)
+             : launch_block_any<FP8LIN_E5M2>(dev.device, dev.sm_count, which, num_tiles, stream, xs, (int)rows,
+                                             (int)cols, (int)tiles_r, (int)tiles_c, fmt_max, q_row, inv_row, q_col,
+                                             inv_col, q_tile, inv_tile);
     if (st != FP8LIN_OK) return st;
     return check_launch();
 }
