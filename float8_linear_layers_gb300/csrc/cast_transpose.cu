@@ -414,7 +414,8 @@ struct TileRing {
 // (each copy row-major like x), with no separate amax pass: 2 bytes read and
 // 1 byte written per element and copy.  Row maxima reduce over the 16 lanes
 // that share a row; column maxima over the thread's 8 rows, the lane pair
-// 16 apart, then the 8 warps through shared memory.
+// 16 apart, then the 8 warps through shared memory.  A persistent kernel
+// whose loads come through the TileRing.
 template <int FMT, bool ROW, bool COL, bool TILE>
 __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
 cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, float fmt_max,
@@ -675,12 +676,9 @@ __device__ __forceinline__ uint2 cast8_pow2(uint4 v, uint4 s) {
 // Row blocks: the thread's 8-column maximum, then the 4 lanes of a 32-column
 // run (shuffles).  Column blocks: the thread's rows i = 2b, 2b + 1 of run b,
 // the lane 16 apart, then the 8 warps through shared memory.
-// Loads: every thread copies its own 8 x 16 bytes of a tile into its own
-// slots of a shared-memory ring (cp.async, kRingStages tiles deep) and
-// reads back only those, so the ring needs no barrier: the CTA keeps the
-// next two tiles in flight while it reduces and casts the current one, and
-// the registers hold one tile.  (One tile per CTA with the loads held in
-// registers had DRAM 52% busy and the SM issuing on 55% of its cycles.)
+// Loads come through the TileRing (the next two tiles in flight).  One tile
+// per CTA with the loads held in registers had DRAM 52% busy and the SM
+// issuing on 55% of its cycles.
 template <int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
 cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, int tiles_c, uint32_t fmax_bits,
