@@ -674,7 +674,8 @@ __device__ __forceinline__ uint2 cast8_pow2(uint4 v, uint4 s) {
 // is exactly one atom of each copy, so each CTA writes whole atoms, with 127
 // (scale 1) for rows or blocks past the matrix's edge.
 // Row blocks: the thread's 8-column maximum, then the 4 lanes of a 32-column
-// run (shuffles).  Column blocks: the thread's rows i = 2b, 2b + 1 of run b,
+// run (shuffles of two rows per word; each lane works out two rows' scale
+// bytes and shares them).  Column blocks: the thread's rows i = 2b, 2b + 1 of run b,
 // the lane 16 apart, then the 8 warps through shared memory.
 // Loads come through the TileRing (the next two tiles in flight).  One tile
 // per CTA with the loads held in registers had DRAM 52% busy and the SM
@@ -736,13 +737,28 @@ cast_mx_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_r, 
         }
         uint32_t rbyte[8];
         if (ROW) {
+            // the run's maxima over its 4 lanes, two rows per word (rows 2j,
+            // 2j + 1 in the low and high halves)
+            uint32_t pm[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t m = rowm[i];
-                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-                rbyte[i] = mx_scale_byte(m << 16, fmax_bits, ocp_emax);
+            for (int j = 0; j < 4; ++j) {
+                pm[j] = rowm[2 * j] | (rowm[2 * j + 1] << 16);
+                pm[j] = __vmaxu2(pm[j], __shfl_xor_sync(0xFFFFFFFFu, pm[j], 1));
+                pm[j] = __vmaxu2(pm[j], __shfl_xor_sync(0xFFFFFFFFu, pm[j], 2));
             }
+            // lane q of the run works out the scale bytes of rows 2q and 2q + 1;
+            // two exchanges hand every lane all eight (row i: byte i % 4 of the
+            // word of rows 0..3 or 4..7)
+            const int q = lane & 3;
+            const uint32_t mine = q == 0 ? pm[0] : (q == 1 ? pm[1] : (q == 2 ? pm[2] : pm[3]));
+            const uint32_t two = mx_scale_byte(mine << 16, fmax_bits, ocp_emax) |
+                                 (mx_scale_byte(mine & 0xFFFF0000u, fmax_bits, ocp_emax) << 8);
+            uint32_t w = two << (16 * (q & 1));                 // rows 2q, 2q + 1 at bytes 2 (q % 2), + 1
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);            // rows 4 (q / 2) .. + 3
+            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+            const uint32_t lo = q < 2 ? w : other, hi = q < 2 ? other : w;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rbyte[i] = ((i < 4 ? lo : hi) >> (8 * (i % 4))) & 0xFFu;
         }
         if (COL) {
 #pragma unroll
