@@ -413,7 +413,8 @@ struct TileRing {
 //   TILE: the 128 x 128 block                              q_tile, inv_tile [tiles_r x tiles_c]
 // (each copy row-major like x), with no separate amax pass: 2 bytes read and
 // 1 byte written per element and copy.  Row maxima reduce over the 16 lanes
-// that share a row; column maxima over the thread's 8 rows, the lane pair
+// that share a row (two rows per shuffle; one lane per row divides for its
+// scale and the others read it); column maxima over the thread's 8 rows, the lane pair
 // 16 apart, then the 8 warps through shared memory.  A persistent kernel
 // whose loads come through the TileRing.
 template <int FMT, bool ROW, bool COL, bool TILE>
@@ -462,11 +463,24 @@ cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_
             colm2[2] = __vmaxu2(colm2[2], c);
             colm2[3] = __vmaxu2(colm2[3], d);
         }
+        float srow[8];  // the rows' scales (ROW)
         if (ROW) {
+            // the row maxima over the 16 lanes sharing the rows, two rows per word
+            uint32_t pm[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 4; ++j) {
+                pm[j] = rowm[2 * j] | (rowm[2 * j + 1] << 16);
 #pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) rowm[i] = max(rowm[i], __shfl_xor_sync(0xFFFFFFFFu, rowm[i], o));
+                for (int o = 8; o >= 1; o >>= 1) pm[j] = __vmaxu2(pm[j], __shfl_xor_sync(0xFFFFFFFFu, pm[j], o));
+                rowm[2 * j] = pm[j] & 0xFFFFu;
+                rowm[2 * j + 1] = pm[j] >> 16;
+            }
+            // lane ch % 8 of the 16 divides for row ch % 8; the others read it
+            const int c = ch & 7;
+            const uint32_t pc = (c >> 1) == 0 ? pm[0] : ((c >> 1) == 1 ? pm[1] : ((c >> 1) == 2 ? pm[2] : pm[3]));
+            const float sc = scale_from_amax(__uint_as_float(((pc >> (16 * (c & 1))) & 0xFFFFu) << 16), fmt_max);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) srow[r] = __shfl_sync(0xFFFFFFFFu, sc, (lane & 16) | r);
         }
         if (COL) {
 #pragma unroll
@@ -516,9 +530,8 @@ cast_block_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_
             const bool ok = col_in && r < rows;
             const int64_t off = (int64_t)r * cols + c0 + ch * 8;
             if (ROW) {
-                const float s = scale_from_amax(__uint_as_float(rowm[i] << 16), fmt_max);
-                if (ok) st_stream8(q_row + off, cast8<FMT>(v[i], s), pol);
-                if (ch == 0 && r < rows) inv_row[(int64_t)tc * rows + r] = __frcp_rn(s);
+                if (ok) st_stream8(q_row + off, cast8<FMT>(v[i], srow[i]), pol);
+                if (ch == 0 && r < rows) inv_row[(int64_t)tc * rows + r] = __frcp_rn(srow[i]);
             }
             if (COL && ok) st_stream8(q_col + off, cast8_each<FMT>(v[i], csc), pol);
             if (TILE && ok) st_stream8(q_tile + off, cast8<FMT>(v[i], s_tile), pol);
