@@ -3,11 +3,13 @@
 // Float8"), writing the row-major copy and, when asked for, the transposed
 // copy in the same pass (the tensor cores read 8-bit operands either way, so
 // per-tensor scaling needs only the row-major copy).  Per-tensor, delayed,
-// static and row-wise scales here; block scales (cast_block_kernel, below)
-// in one pass with no amax call.
+// static and row-wise scales here; block scales with fp32 scales
+// (cast_block_kernel) and with power-of-two scales laid out for the tensor
+// cores (cast_mx_kernel), below, in one pass with no amax call: persistent
+// kernels fed by a per-thread cp.async ring (TileRing).
 //
-// HBM-bound: per element 2 bytes read, 1 (+ 1) bytes written.  One CTA owns a
-// 128 x 128 tile:
+// HBM-bound: per element 2 bytes read, 1 (+ 1) bytes written.  In the
+// per-tensor cast one CTA owns a 128 x 128 tile:
 //  * phase 1: coalesced 16-byte loads (16 threads per 256-byte tile row, all
 //    eight loads of a thread issued before any use), fp32 product with the
 //    scale, cvt.rn.satfinite into packed FP8 pairs; the row-major copy is
