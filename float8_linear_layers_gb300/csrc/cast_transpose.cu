@@ -963,12 +963,12 @@ extern "C" fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int6
     if (!empty && (!aligned(x, 16) || !aligned(q_row, 16) || !aligned(q_col, 16) || !aligned(q_tile, 16)))
         return FP8LIN_ERR_MISALIGNED;
     if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    if (tiles_r * tiles_c > INT32_MAX - (1 << 20)) return FP8LIN_ERR_UNSUPPORTED_SHAPE;  // tile + ring lookahead fits an int
     DeviceInfo dev;
     fp8lin_status st = current_device(&dev);
     if (st != FP8LIN_OK) return st;
     if (empty) return FP8LIN_OK;
-    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
-    if (tiles_r * tiles_c > INT32_MAX - (1 << 20)) return FP8LIN_ERR_UNSUPPORTED_SHAPE;  // tile + ring lookahead fits an int
     const int num_tiles = (int)(tiles_r * tiles_c);
     const uint16_t *xs = static_cast<const uint16_t *>(x);
     st = fmt == FP8LIN_E4M3
@@ -1010,12 +1010,12 @@ fp8lin_status cast_mx_common(const void *x, int64_t rows, int64_t cols, fp8lin_f
                    !aligned(sf_col, 16)))
         return FP8LIN_ERR_MISALIGNED;
     if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
+    if (tiles_r * tiles_c > INT32_MAX - (1 << 20)) return FP8LIN_ERR_UNSUPPORTED_SHAPE;  // tile + ring lookahead fits an int
     DeviceInfo dev;
     fp8lin_status st = current_device(&dev);
     if (st != FP8LIN_OK) return st;
     if (empty) return FP8LIN_OK;
-    const int64_t tiles_r = (rows + kTile - 1) / kTile, tiles_c = (cols + kTile - 1) / kTile;
-    if (tiles_r * tiles_c > INT32_MAX - (1 << 20)) return FP8LIN_ERR_UNSUPPORTED_SHAPE;  // tile + ring lookahead fits an int
     const int num_tiles = (int)(tiles_r * tiles_c);
     uint32_t fmax_bits;
     memcpy(&fmax_bits, &fmt_max, 4);

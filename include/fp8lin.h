@@ -303,7 +303,9 @@ fp8lin_status fp8lin_wgrad_mn(const uint8_t *dyq, const float *inv_dy, const uin
  *   inv_*    device floats (sizes above), or NULL together with their q_*.
  *   rows, cols  >= 0, multiples of 16, <= FP8LIN_MAX_DIM.
  * Errors: a q_* without its inv_* (or the reverse), or no copy at all, is
- * FP8LIN_ERR_INVALID_ARG; alignment and shape as for fp8lin_cast_transpose.
+ * FP8LIN_ERR_INVALID_ARG; alignment and shape as for fp8lin_cast_transpose,
+ * and FP8LIN_ERR_UNSUPPORTED_SHAPE when the 128 x 128 tiles of x number more
+ * than 2^31 - 2^20 - 1 (checked before the device is touched).
  */
 fp8lin_status fp8lin_cast_blockwise(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
                                     float fmt_max, uint8_t *q_row, float *inv_row, uint8_t *q_col,
@@ -406,7 +408,9 @@ fp8lin_status fp8lin_wgrad_rowwise(const uint8_t *dyqT, const float *inv_dy_cols
  *   sf_*     device, u8 scale atoms (sizes above), 16-byte aligned, or NULL
  *            together with their q_*.  Every byte is written.
  * Errors: a q_* without its sf_* (or the reverse), or no copy at all, is
- * FP8LIN_ERR_INVALID_ARG; alignment and shapes as for fp8lin_cast_transpose.
+ * FP8LIN_ERR_INVALID_ARG; alignment and shapes as for fp8lin_cast_transpose,
+ * and FP8LIN_ERR_UNSUPPORTED_SHAPE when the 128 x 128 tiles of x number more
+ * than 2^31 - 2^20 - 1 (checked before the device is touched).
  */
 fp8lin_status fp8lin_cast_mx(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
                              uint8_t *q_row, uint8_t *sf_row, uint8_t *q_col, uint8_t *sf_col,

@@ -195,3 +195,24 @@ def test_argument_checks_of_the_ocp_cast(lib):
     assert cm(a16, 32, 32, 2, a16, a16, None, None, None) == 1           # format
     assert cm(a16, 32, 32, 0, a16, a8, None, None, None) == 2            # misaligned atoms
     assert cm(a16, 32, 40, 0, None, None, a16, a16, None) == 3           # ragged shape
+
+
+def test_tile_count_limit_of_the_block_casts(lib):
+    """The block casts index 128 x 128 tiles (and their ring's lookahead) with
+    32-bit integers: a matrix of more than 2^31 - 2^20 - 1 tiles is refused
+    as an unsupported shape before the device is touched, even though each
+    dimension is within FP8LIN_MAX_DIM."""
+    a16 = V(4096)
+    big = 1 << 30                                    # 2^23 x 2^23 tiles
+    cm = lib.fp8lin_cast_mx
+    cm.restype = ctypes.c_int
+    cm.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V]
+    assert cm(a16, big, big, 0, 448.0, a16, a16, None, None, None) == 3
+    co = lib.fp8lin_cast_mx_ocp
+    co.restype = ctypes.c_int
+    co.argtypes = [V, I, I, ctypes.c_int, V, V, V, V, V]
+    assert co(a16, big, big, 0, None, None, a16, a16, None) == 3
+    cb = lib.fp8lin_cast_blockwise
+    cb.restype = ctypes.c_int
+    cb.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V, V, V]
+    assert cb(a16, big, big, 0, 448.0, a16, a16, None, None, None, None, None) == 3
