@@ -77,6 +77,15 @@ def test_attainable_bound():
     # block scaling: one pass per tensor, two copies for activations and gradients, one for weights
     w_elems = 2 * 14336 * 4096 + 4096 * 14336
     assert bench.cast_bytes(ffn, "block") == 4 * (elems - w_elems) + 3 * w_elems
+    # power-of-two blocks: every tensor, weights included, gets a 1 x 32 and a
+    # 32 x 1 copy (2 B read, 2 x 1 B written; the scale bytes, 1/16 B, are
+    # left out): 2,382,364,672 B for the FFN step, whose serialised bound at
+    # 3423 TFLOP/s and 6775.9 GB/s is 3005 TFLOPS
+    assert bench.cast_bytes(ffn, "mx") == 4 * elems == 2382364672
+    m = bench.attainable(ffn, "mx", 3423.0, 6775.9)
+    gemm_ms = 6 * (2 * 8192 * 4096 * 14336 + 8192 * 14336 * 4096) / 3423e12 * 1e3
+    assert abs(m["frac_of_peak"] - gemm_ms / (gemm_ms + 4 * elems / 6775.9e9 * 1e3)) < 1e-9
+    assert 3004.0 < m["serial_bound_tflops"] < 3006.0
 
 
 def test_traffic_record_keys_on_the_per_tensor_kernel(tmp_path):
