@@ -12,7 +12,7 @@ transformer block.  Nothing is cached across steps (dynamic scaling
 recomputes every statistic every step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload ffn8b|block8b] [--scaling dynamic|delayed|rowwise|block]
+                    [--workload ffn8b|block8b|...] [--scaling dynamic|delayed|rowwise|block|mx]
 
 Prints one JSON line on rank 0.  N > 1 runs under torchrun: each rank runs
 its own replica on its own batch (the path has no exchange step), timing is
@@ -42,6 +42,8 @@ METRIC = "FP8 linear fwd+bwd TFLOPS incl. amax/cast, % of GB300 dense FP8 peak"
 FP8_PER_BF16 = 2.0            # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 E4M3, E5M2 = 0, 1
+L2_FLUSH_BYTES = 512 << 20    # four times GB300's L2
+BURST_REGION_MS = 2000.0      # timed regions shorter than this run at the burst clock
 
 
 # ---------------------------------------------------------- step graphs
@@ -289,20 +291,43 @@ class ClockSampler:
 
 # ---------------------------------------------------------- oracle (CPU)
 
+def sha256_of(bits: np.ndarray) -> str:
+    import hashlib
+    return hashlib.sha256(np.ascontiguousarray(bits).view(np.uint8)).hexdigest()
+
+
 class OracleSample:
     """The CPU oracle on a bounded sample of one step: the per-tensor scaling
     (amax, scale, cast, transpose) of the first `frac` of every cast input's
-    rows and every GEMM on `frac` of its output rows (full FP8 operands
-    prepared once, untimed).  Work scales linearly with rows, so the
-    full-step time is the sample time / frac."""
+    rows and every GEMM on the first `frac` of its output rows (the whole
+    tensors' FP8 copies, which the GEMMs read, prepared once, untimed).
+    Work scales linearly with rows, so the sample does `frac` of the step's
+    work.  The inputs are generated here, independently of the GPU leg, and
+    fingerprinted (SHA-256 of the bf16 bytes) so the two legs can be shown
+    to have seen the same bits."""
 
     def __init__(self, spec: Spec, frac: float):
         import oracle
         self.o, self.spec, self.frac = oracle, spec, frac
-        self.inputs = {}
+        self.inputs, self.sha256 = {}, {}
         for key, (rows, cols, fmt, w, dist, seed, tid, outl) in cast_inputs(spec).items():
             bits = wl.generate((rows, cols), *dist, seed=seed, tensor_id=tid, outlier_frac=outl)
+            self.sha256[key] = sha256_of(bits)
             self.inputs[key] = (bits, fmt, oracle.quantize(bits, fmt))
+        self.rows = {}
+        for l in spec.linears:
+            w = wl.WORKLOADS[l.workload]
+            self.rows[l.name] = (np.arange(max(1, int(round(w.M * frac)))), np.arange(max(1, int(round(w.N * frac)))))
+        self.last = {}
+
+    def flops(self) -> int:
+        """Multiply-adds x 2 of the sample's GEMM rows."""
+        f = 0
+        for l in self.spec.linears:
+            w = wl.WORKLOADS[l.workload]
+            rm, rn = self.rows[l.name]
+            f += 2 * (2 * rm.size * w.N * w.K + rn.size * w.M * w.K)
+        return f
 
     def run(self) -> float:
         o, f = self.o, self.frac
@@ -310,45 +335,85 @@ class OracleSample:
         for key, (bits, fmt, _) in self.inputs.items():
             rows = max(16, int(round(bits.shape[0] * f)))
             o.quantize(bits[:rows], fmt)
+        last = {}
         for l in self.spec.linears:
-            w = wl.WORKLOADS[l.workload]
             qx, qw, qd = (self.inputs[k][2] for k in (l.x, "w:" + l.name, "dy:" + l.name))
-            rm = np.arange(max(1, int(round(w.M * f))))
-            rn = np.arange(max(1, int(round(w.N * f))))
-            o.fwd_ref(qx["q"], qx["inv_scale"], qw["q"], qw["inv_scale"], rm)
-            o.dgrad_ref(qd["q"], qd["inv_scale"], qw["qT"], qw["inv_scale"], rm)
-            o.wgrad_ref(qd["qT"], qd["inv_scale"], qx["qT"], qx["inv_scale"], rn)
-        return time.perf_counter() - t0
+            rm, rn = self.rows[l.name]
+            last[l.name] = {"fwd": o.fwd_ref(qx["q"], qx["inv_scale"], qw["q"], qw["inv_scale"], rm),
+                            "dgrad": o.dgrad_ref(qd["q"], qd["inv_scale"], qw["qT"], qw["inv_scale"], rm),
+                            "wgrad": o.wgrad_ref(qd["qT"], qd["inv_scale"], qx["qT"], qx["inv_scale"], rn)}
+        secs = time.perf_counter() - t0
+        self.last = last
+        return secs
+
+    def check(self, gpu: dict) -> dict:
+        """Compare one GPU step (``StepGraph.parity_state``) with the oracle:
+        amax, scale and inverse scale bits and every FP8 byte of every cast
+        input; the sample's rows of every Y, dX and dW within the GEMM
+        tolerance |y - ref| <= 2^-7 |ref| + 1e-3 rms(ref)."""
+        o = self.o
+        bad = []
+        for key, (bits, fmt, r) in self.inputs.items():
+            g = gpu["casts"][key]
+            for a in ("amax", "scale", "inv_scale"):
+                if g[a] != int(np.float32(r[a]).view(np.uint32)):
+                    bad.append(f"{key} {a}")
+            if not np.array_equal(g["q"], r["q"]):
+                bad.append(f"{key} FP8 bytes")
+        worst = 0.0
+        for l in self.spec.linears:
+            for which, ref in self.last[l.name].items():
+                got = gpu["outputs"][l.name][which][:ref.shape[0]]
+                ok, ratio = o.within_tolerance(got, ref, float(np.sqrt(np.mean(ref ** 2))))
+                worst = max(worst, ratio)
+                if not ok:
+                    bad.append(f"{l.name}.{which}")
+        return {"ok": not bad, "failures": bad, "worst_err_over_bound": worst,
+                "checked": "amax, scale, inverse scale and every FP8 byte of every cast input bit-exact; the "
+                           f"first {self.frac:.5g} of the rows of every Y, dX and dW within the GEMM tolerance"}
+
+    def time_for(self, seconds: float, at_least: int = 1):
+        """Run the sample until `seconds` have passed (at least `at_least` runs); the run times."""
+        times = []
+        while len(times) < at_least or sum(times) < seconds:
+            times.append(self.run())
+        return times
 
     def describe(self) -> str:
         return (f"one step of {self.spec.description}, sampled at {self.frac:.5g} of its rows: "
                 f"amax/scale/cast/transpose of that share of every cast input (shared X once) and that share "
-                f"of the output rows of every fwd/dgrad/wgrad GEMM; full-step time = sample time / share")
+                f"of the output rows of every fwd/dgrad/wgrad GEMM ({self.flops() / 1e9:.4g} GFLOP)")
 
 
 # ------------------------------------------------------------ reference
 
 def run_reference(args, rank: int) -> None:
+    """The oracle as the reference arm: each step is one run of the bounded
+    sample of the workload (OracleSample); value = the sample's flops / its
+    time, so ms_per_step x steps is the wall time spent."""
     if rank != 0:
         return
     import oracle
     spec = SPECS[args.workload]
-    frac = args.ref_frac
+    frac = args.cpu_frac
     s = OracleSample(spec, frac)
     for _ in range(args.warmup):
         s.run()
     times = [s.run() for _ in range(args.steps)]
-    step_s = sum(times) / len(times) / frac
-    value = spec_flops(spec) / step_s / 1e12
+    step_s = sum(times) / len(times)
+    value = s.flops() / step_s / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "extrapolated_ms_per_step": step_s / frac * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": spec.name, "scaling": "dynamic"},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": s.describe()},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "inputs_sha256": s.sha256,
         "gpu_launches": 0,
+        "note": "each step is one run of the sample; extrapolated_ms_per_step = ms_per_step / share",
     }
     print(json.dumps(line), flush=True)
 
@@ -459,6 +524,27 @@ class StepGraph:
 
     def outputs(self):
         return [self.out[l.name][w] for l in self.spec.linears for w in ("fwd", "dgrad", "wgrad")]
+
+    def parity_state(self, frac: float) -> dict:
+        """Host copies of what the last step left on the device, for the
+        oracle comparison (per-tensor scaling): the amax, scale and inverse
+        scale bits and the FP8 copy of every cast input, and the first
+        `frac` of the rows of every Y, dX and dW (as float64)."""
+        t = self.t
+        casts = {}
+        for key, t8 in self.t8.items():
+            bits = lambda v: int(v.cpu().view(t.int32).item()) & 0xFFFFFFFF
+            casts[key] = {"amax": bits(t8.amax), "scale": bits(t8.scale), "inv_scale": bits(t8.inv_scale),
+                          "q": t8.q.cpu().numpy()}
+        outputs = {}
+        for l in self.spec.linears:
+            w = wl.WORKLOADS[l.workload]
+            nm, nn = max(1, int(round(w.M * frac))), max(1, int(round(w.N * frac)))
+            o = self.out[l.name]
+            outputs[l.name] = {"fwd": o["fwd"][:nm].float().cpu().numpy().astype(np.float64),
+                               "dgrad": o["dgrad"][:nm].float().cpu().numpy().astype(np.float64),
+                               "wgrad": o["wgrad"][:nn].float().cpu().numpy().astype(np.float64)}
+        return {"casts": casts, "outputs": outputs}
 
     # -- issue -------------------------------------------------------------
     def _ev(self):
@@ -649,6 +735,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         dist.init_process_group("nccl", device_id=dev)
 
     host = host_inputs(spec, rank)
+    host_sha = {k: sha256_of(v) for k, v in host.items()} if rank == 0 else None
     dev_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in host.items()}
     step = StepGraph(fl, spec, dev, dev_in, overlap=not args.serial, scaling=args.scaling,
                      transpose=args.transpose, mx_rule=args.mx_rule)
@@ -664,7 +751,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         step.run()
     barrier()
 
-    # ---- timed region (device-resident inputs)
+    # ---- timed region (device-resident inputs), L2 flushed before every step:
+    # a buffer four times the L2 is rewritten on the main stream between
+    # steps, outside the step's own events, so no operand is L2-resident when
+    # a step starts; the step time is the sum of the per-step event spans.
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     time.sleep(0.3)
@@ -672,16 +763,31 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         gemm_only = True          # the timed region brackets only the GEMMs (the roofline's launches)
 
     events = _GemmEvents()
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
     t_start.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
+        flush.fill_(i & 0x7F)
+        ev_step[i][0].record(stream)
         step.run(events)
+        ev_step[i][1].record(stream)
     t_end.record(stream)
     barrier()
+    # the same steps back to back, no flush (operands of one step may still
+    # sit in L2 when the next starts)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(args.steps):
+        step.run()
+    u1.record(stream)
+    barrier()
     clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    flushed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_step), dist, dev)
+    region_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    unflushed_ms = max_over_ranks(u0.elapsed_time(u1), dist, dev)
     assert fl.fp8lin_device_error() == 0, "a GEMM kernel reported a timed-out wait"
     # per-kernel breakdown of amax / cast from separate, fully instrumented steps
     detail = []
@@ -712,7 +818,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     gaps = {}
     for k in range(args.steps):
         seq = gemm_evs[k * per_step:(k + 1) * per_step]
-        prev = t_start if k == 0 else gemm_evs[k * per_step - 1][2]
+        prev = ev_step[k][0]
         for label, e0, e1 in seq:
             gaps[label] = gaps.get(label, 0.0) + prev.elapsed_time(e0) / args.steps
             prev = e1
@@ -725,7 +831,12 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     peaks, peak_src = load_peaks()
     fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
     fp8_peak_burst = peaks["bf16_tflops"] * FP8_PER_BF16
-    ms_per_step = elapsed_ms / args.steps
+    # the burst peak for a timed region of under two seconds at full clock,
+    # the sustained one (taken seconds into a loop under the power cap) else
+    burst = region_ms < BURST_REGION_MS
+    fp8_peak = fp8_peak_burst if burst else fp8_peak_sustained
+    peak_kind = "burst" if burst else "sustained"
+    ms_per_step = flushed_ms / args.steps
     value = world * spec_flops(spec) / (ms_per_step * 1e-3) / 1e12
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     w1_fwd_tflops = w1_fwd_flops / (w1_fwd_ms / w1_fwd_n * 1e-3) / 1e12
@@ -754,13 +865,22 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     if args.e2e_steps > 0:
         e2e = run_e2e(args, fl, spec, dev, host, step, world, dist, barrier)
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle on a bounded sample of the same step, timed on the host
+        # cores; the sample's results are then compared with one GPU step
         import oracle
+        gpu_state = step.parity_state(args.cpu_frac) if args.scaling == "dynamic" else None
         s = OracleSample(spec, args.cpu_frac)
-        secs = s.run()
-        cpu = {"value": spec_flops(spec) / (secs / args.cpu_frac) / 1e12, "unit": "TFLOPS",
-               "cores": oracle.num_threads(), "kind": "oracle", "sample": s.describe(), "sample_seconds": secs}
+        times = s.time_for(args.cpu_seconds)
+        secs = sum(times) / len(times)
+        cpu = {"value": s.flops() / secs / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": s.describe(), "sample_seconds": secs, "runs": len(times),
+               "extrapolated_step_seconds": secs / args.cpu_frac}
+        if gpu_state is not None:
+            parity = s.check(gpu_state)
+            parity["inputs_sha256_match"] = s.sha256 == host_sha
+            parity["ok"] = parity["ok"] and parity["inputs_sha256_match"]
 
     if dist is not None:
         dist.barrier()
@@ -781,21 +901,31 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                                   "two row-major copies per tensor (blocks along each GEMM's contraction); "
                                   "GEMMs read them K- or MN-major" if args.scaling in ("block", "mx") else
                                   "one row-major copy per tensor; backward GEMMs read it MN-major"),
-                   "l2": "inputs larger than L2: one step streams several GB of distinct operands through a 129 MB L2",
+                   "l2": f"flushed: a {L2_FLUSH_BYTES >> 20} MiB buffer is rewritten on the main stream before "
+                         "every timed step, outside the step's events (the step's own operands, several GB, "
+                         "exceed the 129 MB L2 as well); the unflushed back-to-back time is reported beside",
                    "parallelism": f"replicas x{world}"},
-        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak_sustained,
-        "attainable": attainable(spec, args.scaling, fp8_peak_sustained, peaks["hbm_gbs"], step.transpose),
-        "fp8_peak_tflops": {"sustained": fp8_peak_sustained, "burst": fp8_peak_burst,
-                            "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sustained,
-                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sustained,
+        "unflushed": {"ms_per_step": unflushed_ms / args.steps,
+                      "value": world * spec_flops(spec) / (unflushed_ms / args.steps * 1e-3) / 1e12,
+                      "unit": "TFLOPS", "steps": args.steps,
+                      "note": "the same steps back to back with no L2 flush, after the flushed ones"},
+        "pct_of_fp8_peak": 100.0 * value / world / fp8_peak,
+        "pct_of_fp8_peak_sustained": 100.0 * value / world / fp8_peak_sustained,
+        "attainable": attainable(spec, args.scaling, fp8_peak, peaks["hbm_gbs"], step.transpose),
+        "fp8_peak_tflops": {"used": peak_kind, "sustained": fp8_peak_sustained, "burst": fp8_peak_burst,
+                            "timed_region_ms": region_ms,
+                            "source": f"{peak_src} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16); burst for a timed "
+                                      f"region under {BURST_REGION_MS / 1e3:g} s, sustained otherwise"},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                     "frac_of_sustained": gemm_tflops / fp8_peak_sustained,
                      "traffic": gemm_traffic(args.workload, args.scaling),
                      "kernel": {"block": "fp8_gemm_block_kernel", "mx": "fp8_gemm_mx_kernel"}.get(
                                    args.scaling, "fp8_gemm_tn_kernel") +
                                ", every launch of the timed region: mean 2*M*N*K flop per "
                                "launch / mean event-timed launch duration (launches run beside the side-stream "
                                "casts); traffic = mean DRAM bytes per GEMM launch of one step (ncu)",
-                     "peak_source": f"{peak_src} sustained bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)",
+                     "peak_source": f"{peak_src} {peak_kind} bf16 x {FP8_PER_BF16:g} (nominal fp8:bf16)",
                      "launches_timed": len(gemm_evs),
                      f"{roof_label}_tflops": w1_fwd_tflops},
         "kernels": {
@@ -815,6 +945,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "e2e": e2e,
         "gpu_launches": step.kernels_per_step * args.steps,
         "cpu_baseline": cpu,
+        "parity": None if parity is None else parity["ok"],
+        "parity_detail": parity if parity is not None else
+        "not checked: the oracle leg runs on rank 0 of a one-GPU run with dynamic scaling",
+        "inputs_sha256": host_sha,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
@@ -969,8 +1103,10 @@ def main():
     ap.add_argument("--graph", action="store_true", help="also time the step replayed from a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=32,
                     help="steps of the end-to-end run; the average includes one pipeline fill and drain")
-    ap.add_argument("--cpu-frac", type=float, default=1.0 / 32)
-    ap.add_argument("--ref-frac", type=float, default=1.0 / 256)
+    ap.add_argument("--cpu-frac", type=float, default=1.0 / 64,
+                    help="share of the step's rows the CPU oracle runs on (cpu_baseline and --impl reference)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="cpu_baseline: repeat the oracle sample until this much CPU time has been timed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["gemm_fwd", "gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn",
                                                "gemm_wgrad_mn", "gemm_fwd_block", "gemm_dgrad_block",

@@ -27,8 +27,15 @@ def _run(args, timeout):
 
 
 def test_reference_arm_json_line():
-    d = _run(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-frac", "0.001"], 900)
+    import time
+    t0 = time.perf_counter()
+    d = _run(["--impl", "reference", "--steps", "2", "--warmup", "3", "--cpu-frac", "0.001"], 900)
+    wall = time.perf_counter() - t0
     assert BASE_KEYS <= set(d) and d["impl"] == "reference"
+    # each step is one run of the sample: the steps' time fits in the run
+    assert d["steps"] * d["ms_per_step"] * 1e-3 < wall
+    assert abs(d["extrapolated_ms_per_step"] - d["ms_per_step"] / 0.001) < 1e-6 * d["extrapolated_ms_per_step"]
+    assert len(d["inputs_sha256"]) == 8 and all(len(h) == 64 for h in d["inputs_sha256"].values())
     assert d["unit"] == "TFLOPS" and d["higher_is_better"] is True and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
@@ -38,7 +45,7 @@ def test_reference_arm_json_line():
 
 @pytest.mark.gpu
 def test_our_arm_json_line(fp8lin):
-    d = _run(["--steps", "3", "--warmup", "3", "--e2e-steps", "2", "--cpu-frac", "0.002"], 900)
+    d = _run(["--steps", "3", "--warmup", "3", "--e2e-steps", "2", "--cpu-frac", "0.002", "--cpu-seconds", "0"], 900)
     assert BASE_KEYS <= set(d) and "impl" not in d
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["value"] > 0
     r = d["roofline"]
@@ -48,3 +55,7 @@ def test_our_arm_json_line(fp8lin):
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    # the oracle leg's check of one GPU step, on inputs with the same fingerprints
+    assert d["parity"] is True and d["parity_detail"]["inputs_sha256_match"] is True
+    assert d["unflushed"]["value"] > 0 and "flushed" in d["config"]["l2"]
+    assert d["fp8_peak_tflops"]["used"] == "burst" and r["peak"] == d["fp8_peak_tflops"]["burst"]
