@@ -121,7 +121,9 @@ static uint64_t shift_rne(uint64_t x, int s) {
 
 /* Saturating round-to-nearest-even of one fp32 value into an FP8 code,
  * by integer manipulation of the binary32 fields:
- *  - NaN stays NaN (sign kept, mantissa all ones);
+ *  - NaN, of either sign and any payload, gives 0x7F: the one NaN code the
+ *    sm_103a conversion emits (positive, mantissa all ones; reading adopted
+ *    from the hardware, the pages being silent on NaN);
  *  - |v| at or above the largest finite value (Inf included) gives the
  *    largest finite code with v's sign (saturation);
  *  - otherwise the significand is rounded to the format's mantissa width at
@@ -133,7 +135,7 @@ uint8_t orc_fp8_encode(int fmt, float v) {
     uint8_t sign = (uint8_t)((u >> 31) << 7);
     uint32_t a = u & 0x7FFFFFFFu;
     if (a > 0x7F800000u) /* NaN */
-        return (uint8_t)(sign | 0x7F);
+        return 0x7F;
     double max_val = orc_fp8_decode(fmt, (uint8_t)f.max_code);
     if ((double)f32_from_bits(a) >= max_val) /* saturate, Inf included */
         return (uint8_t)(sign | f.max_code);
@@ -195,14 +197,24 @@ float orc_amax_bf16(const uint16_t *x, int64_t n) {
 
 /* --------------------------------------------------------------- scale */
 
+/* A binary32 operation whose result is NaN gives, on the GPU, the one NaN
+ * 0x7FFFFFFF (sign clear, every significand bit set), where x86 keeps an
+ * operand's sign and payload.  The scale arithmetic below stores its NaN
+ * results in that form (reading adopted from the hardware; the pages say
+ * nothing of NaN). */
+static float canonical_nan(float v) {
+    return (bits_from_f32(v) & 0x7FFFFFFFu) > 0x7F800000u ? f32_from_bits(0x7FFFFFFFu) : v;
+}
+
 /* scale = fmt_max / max(amax, 1e-12) and inv_scale = 1 / scale, both as
- * binary32 round-to-nearest operations.  A NaN amax propagates. */
+ * binary32 round-to-nearest operations.  A NaN amax gives the canonical NaN
+ * for both. */
 void orc_scale(float amax, float fmt_max, float *scale, float *inv_scale) {
     volatile float a = (amax < 1e-12f) ? 1e-12f : amax;
     volatile float s = fmt_max / a;
     volatile float inv = 1.0f / s;
-    *scale = s;
-    *inv_scale = inv;
+    *scale = canonical_nan(s);
+    *inv_scale = canonical_nan(inv);
 }
 
 /* orc_scale applied to n amax values. */
@@ -214,7 +226,7 @@ void orc_scales(const float *amax, int64_t n, float fmt_max, float *scale, float
  * inverse scale). */
 float orc_reciprocal(float s) {
     volatile float r = 1.0f / s;
-    return r;
+    return canonical_nan(r);
 }
 
 /* Largest entry of an amax history h[0..n), leaving out index `skip` (the

@@ -56,8 +56,13 @@ def test_scale_second_route(amax, fmt_max):
 
 
 def test_scale_nan_propagates():
-    s, inv = oracle.scale(np.float32(np.nan), 448.0)
-    assert np.isnan(s) and np.isnan(inv)
+    # a NaN amax (any sign or payload) gives NaN scales, stored as the GPU's
+    # one binary32 NaN, 0x7FFFFFFF
+    for bits in (0x7FC00000, 0xFFC00000, 0x7F800001, 0x7FFF0000):
+        s, inv = oracle.scale(np.array([bits], np.uint32).view(np.float32)[0], 448.0)
+        assert np.float32(s).view(np.uint32) == 0x7FFFFFFF and np.float32(inv).view(np.uint32) == 0x7FFFFFFF
+    assert np.float32(oracle.quantize_static(np.zeros((1, 16), np.uint16), 0, np.nan)["inv_scale"]).view(
+        np.uint32) == 0x7FFFFFFF
 
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
