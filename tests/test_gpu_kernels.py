@@ -104,11 +104,7 @@ def test_cast_every_bf16_pattern(fp8lin, fmt, fmt_max):
         assert scalar_bits(scale) == f32_bits(s) and scalar_bits(inv) == f32_bits(i)
         ref = oracle.cast(x, fmt, s)
         got = q.cpu().numpy()
-        xf = wl.bf16_bits_to_f32(x)
-        nan_in = np.isnan(xf)
-        table = oracle.decode_table(fmt)
-        assert np.isnan(table[got[nan_in]]).all()          # NaN stays NaN (any NaN code)
-        assert np.array_equal(got[~nan_in], ref[~nan_in])
+        assert np.array_equal(got, ref)                     # NaNs included: every NaN casts to 0x7F
         assert np.array_equal(qT.cpu().numpy(), got.T)
 
 

@@ -232,8 +232,7 @@ def test_mx_cast_special_values(fp8lin, fmt):
         got = got_q.cpu().numpy()
         nan_ref = np.isnan(table[ref["q"]])
         assert nan_ref.sum() == 64                            # every element of those two blocks
-        assert np.isnan(table[got[nan_ref]]).all(), along     # NaN stays NaN (any NaN code)
-        assert np.array_equal(got[~nan_ref], ref["q"][~nan_ref]), along
+        assert np.array_equal(got, ref["q"]), along           # NaN codes included (0x7F)
 
 
 def _fuzz_shapes(n=24, seed=2024):
@@ -298,15 +297,11 @@ def test_mx_ocp_cast_zero_and_special_blocks(fp8lin):
     sc = torch.empty((_atoms(cols, rows),), dtype=torch.uint8, device="cuda")
     fp8lin.fp8lin_cast_mx(to_dev_bf16(x), E4M3, q_row=q, sf_row=sr, q_col=qc, sf_col=sc, rule="ocp")
     torch.cuda.synchronize()
-    table = oracle.decode_table(E4M3)
     for along, gq, gs in (("cols", q, sr), ("rows", qc, sc)):
         ref = oracle.quantize_mx(x, E4M3, along, rule="ocp")
         assert np.array_equal(gs.cpu().numpy(), _ref_atoms(ref, along, rows, cols)), along
         assert (ref["sf"] == 0).sum() >= 1 and (ref["sf"] == 0xFF).sum() == 1
-        got = gq.cpu().numpy()
-        nan_ref = np.isnan(table[ref["q"]])
-        assert np.isnan(table[got[nan_ref]]).all(), along
-        assert np.array_equal(got[~nan_ref], ref["q"][~nan_ref]), along
+        assert np.array_equal(gq.cpu().numpy(), ref["q"]), along   # NaN codes included (0x7F)
 
 
 @pytest.mark.parametrize("M,K,N", [(256, 512, 1024), (144, 208, 272)])
