@@ -17,6 +17,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfp8lin.so")
+# A second library for the tests only: the GEMM built with a fault injector
+# (its producers can withhold one slab's copies) and a 20 ms wait limit, so
+# a test can drive the kernel's abort path.  The product library never has it.
+FAULT_LIB = os.path.join(OUT, "libfp8lin_faultinj.so")
+FAULT_FLAGS = ["-DFP8LIN_FAULT_INJECTION", "-DFP8LIN_WAIT_LIMIT_NS=20000000ull"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -41,9 +46,9 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB) or EXTRA:
+    if EXTRA or not all(os.path.exists(p) for p in (LIB, FAULT_LIB)):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(FAULT_LIB))
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
@@ -54,11 +59,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(os.path.join(OUT, "obj"), exist_ok=True)
     cc = nvcc()
     procs = []
-    objs = []
-    for src in _sources():
-        obj = os.path.join(OUT, "obj", os.path.basename(src)[:-3] + ".o")
-        objs.append(obj)
-        cmd = [cc, *ARCH, *NVCC_FLAGS, *EXTRA, "-c", src, "-o", obj]
+    jobs = [(src, os.path.join(OUT, "obj", os.path.basename(src)[:-3] + ".o"), []) for src in _sources()]
+    objs = [obj for _, obj, _ in jobs]
+    fault_obj = os.path.join(OUT, "obj", "gemm_faultinj.o")
+    jobs.append((os.path.join(CSRC, "gemm.cu"), fault_obj, FAULT_FLAGS))
+    for src, obj, flags in jobs:
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *EXTRA, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd))
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -71,10 +77,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(out.decode(errors="replace"))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"--- {s}\n{o}" for s, o in failed))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    for lib, lib_objs in ((LIB, objs), (FAULT_LIB, [fault_obj, os.path.join(OUT, "obj", "api.o")])):
+        tmp = lib + f".tmp{os.getpid()}"
+        subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *lib_objs], check=True)
+        os.replace(tmp, lib)
     return LIB
 
 

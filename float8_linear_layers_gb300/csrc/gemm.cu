@@ -84,7 +84,10 @@ constexpr int kEpiBytes = 4 * kEpiBuf;       // four epilogue warps, one buffer 
 // The ring plus staging stays small enough that one cast / amax CTA (about
 // 18 KB of shared memory) still fits beside a GEMM CTA on the same SM.
 constexpr int kSmemBytes = kStages * (kAStage + kBStage) + kEpiBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+#ifndef FP8LIN_WAIT_LIMIT_NS
+#define FP8LIN_WAIT_LIMIT_NS 2000000000ull                  // 2 s per wait
+#endif
+constexpr unsigned long long kWaitLimitNs = FP8LIN_WAIT_LIMIT_NS;
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
 
 static_assert(kBK == 128, "one stage is one 128-byte swizzle row of contraction");
@@ -93,6 +96,16 @@ static_assert(kPairN % kEpiCols == 0, "the epilogue stores whole 32-column block
 static_assert(kSmemBytes + 1024 + 18 * 1024 + 1024 <= 233472, "a cast CTA must fit beside a GEMM CTA");
 
 __device__ unsigned int g_device_error = 0;
+
+#ifdef FP8LIN_FAULT_INJECTION
+// Test builds only (a library of its own, never the product one).  When
+// g_withhold_slab >= 0, the producers of every CTA pair of the per-tensor
+// GEMM skip the copies of their g_withhold_slab-th slab (counted over the
+// pair's tiles) and the leader skips its arrival on that stage's full
+// barrier: nothing is ever in flight on it, so the MMA issuer's bounded
+// wait on it runs out and the kernel takes its abort path.
+__device__ int g_withhold_slab = -1;
+#endif
 
 // ------------------------------------------------------------------ PTX
 
@@ -212,13 +225,28 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
 
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier of either CTA of the pair (the leader's, for the pair's MMA).
+// `policy` is an L2 cache policy (createpolicy): the operand the raster
+// holds in L2 is loaded evict_last, the one it streams with the normal policy.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t cluster_bar,
-                                                 int c0, int c1) {
+                                                 int c0, int c1, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "l"(policy)
         : "memory");
+}
+
+// L2 policies of the two operands: the one the tile order holds (A unless
+// the raster swaps the axes) evict_last, so the held panels outlive the
+// streamed ones; the streamed operand keeps the normal policy (each of its
+// panels is read by a whole wave of tiles that do not move through the
+// contraction in lockstep, and evict_first lost slabs between readers).
+__device__ __forceinline__ void operand_policies(int swap, uint64_t &pol_a, uint64_t &pol_b) {
+    uint64_t keep, stream;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(stream));
+    pol_a = swap ? stream : keep;
+    pol_b = swap ? keep : stream;
 }
 
 // TMA store of one box from this CTA's shared memory, tracked in the
@@ -399,6 +427,12 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
+            uint64_t pol_a, pol_b;
+            operand_policies(tiles.swap, pol_a, pol_b);
+#ifdef FP8LIN_FAULT_INJECTION
+            const int withhold = g_withhold_slab;
+            int slab = 0;
+#endif
             for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
@@ -406,26 +440,36 @@ fp8_gemm_tn_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                 const int b_row = tn * kPairN + (int)rank * kBN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
-                    const uint32_t fb_local = smem_u32(&full[stage]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
-                    const uint32_t fb = mapa_shared(fb_local, 0);
-                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
-                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
-                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
-                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    bool issue = true;
+#ifdef FP8LIN_FAULT_INJECTION
+                    issue = slab++ != withhold;
+#endif
+                    if (issue) {
+                        const uint32_t fb_local = smem_u32(&full[stage]);
+                        if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
+                        const uint32_t fb = mapa_shared(fb_local, 0);
+                        if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK, pol_a);
+                        else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row, pol_a);
+                        if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK, pol_b);
+                        else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row, pol_b);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (*abort_flag && leader) {
-                // Let every copy of the pair land before either CTA exits.
+            if (leader) {
+                // Let every copy of the pair land before either CTA exits,
+                // whether or not (or whenever) a wait ran out: both CTAs'
+                // copies complete on the leader's full barriers.  A phase
+                // the MMA issuer consumed has completed already.
+                volatile int no_abort = 0;
                 for (int s = 0; s < kStages; ++s)
                     if (armed & (1u << s))
-                        mbar_wait(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
+                        mbar_wait(smem_u32(&full[s]), (armed_parity >> s) & 1u, &no_abort, kDrainLimitNs);
             }
         }
     } else if (warp == 1) {
@@ -879,6 +923,8 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
+            uint64_t pol_a, pol_b;
+            operand_policies(tiles.swap, pol_a, pol_b);
             for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
@@ -889,10 +935,10 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                     const uint32_t fb_local = smem_u32(&full[stage]);
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
                     const uint32_t fb = mapa_shared(fb_local, 0);
-                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK);
-                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row);
-                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK);
-                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row);
+                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK, pol_a);
+                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row, pol_a);
+                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK, pol_b);
+                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row, pol_b);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kBlkStages) {
@@ -901,11 +947,12 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                     }
                 }
             }
-            if (*abort_flag && leader) {
-                // let every copy of the pair land before either CTA exits
+            if (leader) {
+                // let every copy of the pair land before either CTA exits, abort or not
+                volatile int no_abort = 0;
                 for (int s = 0; s < kBlkStages; ++s)
                     if (armed & (1u << s))
-                        mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, abort_flag, kDrainLimitNs);
+                        mbar_wait_inl(smem_u32(&full[s]), (armed_parity >> s) & 1u, &no_abort, kDrainLimitNs);
             }
         } else if (warp == 1 && lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (leader CTA)
@@ -1351,6 +1398,8 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
+            uint64_t pol_a, pol_b;
+            operand_policies(tiles.swap, pol_a, pol_b);
             for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
@@ -1369,10 +1418,10 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     for (int h = 0; h < kMxSlabs; ++h) {
                         const int kb = ks * kMxSlabs + h;
                         const int sl = stage * kMxSlabs + h;
-                        if (A_MN) tma_load_2d_pair(smem_u32(sA + sl * kAStage), &map_a, fb, a_row, kb * kBK);
-                        else      tma_load_2d_pair(smem_u32(sA + sl * kAStage), &map_a, fb, kb * kBK, a_row);
-                        if (B_MN) tma_load_2d_pair(smem_u32(sB + sl * kBStage), &map_b, fb, b_row, kb * kBK);
-                        else      tma_load_2d_pair(smem_u32(sB + sl * kBStage), &map_b, fb, kb * kBK, b_row);
+                        if (A_MN) tma_load_2d_pair(smem_u32(sA + sl * kAStage), &map_a, fb, a_row, kb * kBK, pol_a);
+                        else      tma_load_2d_pair(smem_u32(sA + sl * kAStage), &map_a, fb, kb * kBK, a_row, pol_a);
+                        if (B_MN) tma_load_2d_pair(smem_u32(sB + sl * kBStage), &map_b, fb, b_row, kb * kBK, pol_b);
+                        else      tma_load_2d_pair(smem_u32(sB + sl * kBStage), &map_b, fb, kb * kBK, b_row, pol_b);
                         // scale atoms: this CTA's 128 A rows; both 128-row blocks of the tile's B rows
                         tma_load_2d(smem_u32(sSfa + sl * kMxSfa), &map_sfa, sb, 0, kb * pb_a + 2 * tm + (int)rank);
                         tma_load_2d(smem_u32(sSfb + sl * kMxSfb), &map_sfb, sb, 0, kb * pb_b + 2 * tn);
@@ -1385,8 +1434,8 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     }
                 }
             }
-            if (*abort_flag) {
-                // let every copy land before either CTA exits
+            {
+                // let every copy land before either CTA exits, abort or not
                 volatile int no_abort = 0;
                 for (int s = 0; s < kMxStages; ++s)
                     if (armed & (1u << s)) {
@@ -1668,12 +1717,14 @@ cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttrib
     return cfg;
 }
 
-// Raster: keep the smaller operand resident in L2 and stream the larger one
-// once.  If neither fits, the tiles running at once move through the
-// contraction together, so L2 only has to hold their current slabs: group
-// kWaveGroup tiles along one axis (a wave covers a compact block of tiles,
-// each panel read once per group), choosing the orientation with the fewest
-// modelled DRAM bytes.
+// Raster: keep the smaller operand resident in L2 (up to kL2Resident: a
+// panel set read by SMs of both dies is cached in each die's half of the L2)
+// and stream the larger one once.  If neither fits, the tiles
+// running at once move through the contraction together, so L2 only has to
+// hold their current slabs: group kWaveGroup tiles along one axis (a wave
+// covers a compact block of tiles, each panel read once per group),
+// choosing the orientation with the fewest modelled DRAM bytes.  Either way
+// the producers load the held operand evict_last (operand_policies).
 TileMap raster(int64_t P, int64_t Q, int64_t R, int64_t tiles_m, int64_t tiles_n) {
     const int64_t bytes_a = P * R, bytes_b = Q * R;
     TileMap tm{(int)tiles_m, (int)tiles_n, 1, 0};
@@ -2089,3 +2140,14 @@ extern "C" fp8lin_status fp8lin_device_error(cudaStream_t stream, uint32_t *word
     if (word != nullptr) *word = v;
     return v == 0 ? FP8LIN_OK : FP8LIN_ERR_TIMEOUT;
 }
+
+#ifdef FP8LIN_FAULT_INJECTION
+// Test builds only: choose the slab whose copies the per-tensor GEMM's
+// producers withhold (-1: none).  Synchronous; takes effect from the next
+// launch on the current device.
+extern "C" fp8lin_status fp8lin_test_withhold_slab(int slab) {
+    if (slab < -1) return FP8LIN_ERR_INVALID_ARG;
+    if (cudaMemcpyToSymbol(g_withhold_slab, &slab, sizeof slab) != cudaSuccess) return FP8LIN_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? FP8LIN_OK : FP8LIN_ERR_CUDA;
+}
+#endif

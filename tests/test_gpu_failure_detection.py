@@ -1,7 +1,15 @@
 """Failure detection without a GPU fault: a bounded wait inside a kernel runs
 out (an mbarrier nothing arrives on), the kernel records FP8LIN_ERR_TIMEOUT
 in the device error word and exits; the host reads the status and the
-context keeps working."""
+context keeps working.
+
+The GEMM's own abort path runs on the test library built with a fault
+injector (libfp8lin_faultinj.so: the same GEMM source with a 20 ms wait
+limit, whose producers can be told to withhold one slab's copies).  Nothing
+is in flight on the withheld stage, so the MMA issuer's wait on it runs out;
+the kernel raises its abort flag, lets every copy it did issue land, meets
+the peer CTA at the cluster barrier, frees its tensor memory and returns."""
+import ctypes
 import time
 
 import numpy as np
@@ -43,3 +51,54 @@ def test_selftest_rejects_out_of_range_limits(fp8lin):
         fp8lin.fp8lin_selftest_bounded_wait(10)
     with pytest.raises(fp8lin.Fp8LinError):
         fp8lin.fp8lin_selftest_bounded_wait(5_000_000_000)
+
+
+def _fault_library(fp8lin):
+    lib = ctypes.CDLL(fp8lin._build.FAULT_LIB)
+    for name in ("fp8lin_fwd", "fp8lin_device_error"):
+        fn = getattr(lib, name)
+        fn.argtypes = fp8lin.SIGNATURES[name]
+        fn.restype = ctypes.c_int
+    lib.fp8lin_test_withhold_slab.argtypes = [ctypes.c_int]
+    lib.fp8lin_test_withhold_slab.restype = ctypes.c_int
+    return lib
+
+
+# (M, N, K, withheld slab): the first slab of every CTA pair's only tile, and
+# the second slab of the second tile of pairs that own two or three tiles
+# (160 pair tiles), so completed tiles were already stored when the wait ran out
+@pytest.mark.parametrize("M,N,K,slab", [(256, 1024, 512, 0), (256, 40960, 512, 5)])
+def test_gemm_abort_path_on_a_withheld_slab(fp8lin, M, N, K, slab):
+    lib = _fault_library(fp8lin)
+    rng = np.random.default_rng(M + N + slab)
+    A = rng.integers(0, 0x70, size=(M, K), dtype=np.uint8)
+    B = rng.integers(0, 0x70, size=(N, K), dtype=np.uint8)
+    a, b = to_dev_u8(A), to_dev_u8(B)
+    one = torch.ones(1, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    word = ctypes.c_uint32(0)
+    fwd = lambda: lib.fp8lin_fwd(a.data_ptr(), one.data_ptr(), b.data_ptr(), one.data_ptr(), y.data_ptr(),
+                                 M, N, K, stream)
+
+    assert lib.fp8lin_test_withhold_slab(slab) == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert fwd() == 0
+    status = lib.fp8lin_device_error(stream, ctypes.byref(word))     # synchronises the stream
+    dt = time.perf_counter() - t0
+    assert status == 5 and word.value == 1 << 5                      # FP8LIN_ERR_TIMEOUT, recorded by the GEMM
+    assert dt < 2.0                                                  # 20 ms waits: the kernel gave up and returned
+    assert lib.fp8lin_device_error(stream, None) == 0                # read-and-clear
+
+    # the next launch of the same kernel runs clean and matches the oracle
+    assert lib.fp8lin_test_withhold_slab(-1) == 0
+    y.fill_(float("nan"))
+    assert fwd() == 0
+    assert lib.fp8lin_device_error(stream, None) == 0
+    rows = np.array([0, 1, M // 2, M - 1])
+    ref = oracle.gemm_rows(A, oracle.E4M3, B, oracle.E4M3, 1.0, 1.0, rows)
+    assert_gemm_close(bf16_to_f64(y[torch.from_numpy(rows).cuda()]), ref, "after the abort")
+    # the product library never saw a timeout
+    assert fp8lin.fp8lin_device_error() == 0
+    _small_gemm(fp8lin)
