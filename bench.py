@@ -256,7 +256,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
@@ -751,10 +751,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         step.run()
     barrier()
 
-    # ---- timed region (device-resident inputs), L2 flushed before every step:
-    # a buffer four times the L2 is rewritten on the main stream between
-    # steps, outside the step's own events, so no operand is L2-resident when
-    # a step starts; the step time is the sum of the per-step event spans.
+    # ---- timed region (device-resident inputs): every step runs after an L2
+    # flush (a buffer four times the L2 rewritten on the main stream, outside
+    # the step's events, so no operand is L2-resident when the step starts);
+    # each step is timed by its own pair of events on the main stream, which
+    # every side-stream cast joins.
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
@@ -763,8 +764,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         gemm_only = True          # the timed region brackets only the GEMMs (the roofline's launches)
 
     events = _GemmEvents()
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+    new_ev = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    ev_step = [new_ev() for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -776,9 +777,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         ev_step[i][1].record(stream)
     t_end.record(stream)
     barrier()
-    # the same steps back to back, no flush (operands of one step may still
-    # sit in L2 when the next starts)
-    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the same number of steps back to back, no flush (run after the flushed
+    # ones, so later in the GPU's clock and power history)
+    u0, u1 = new_ev()
     u0.record(stream)
     for _ in range(args.steps):
         step.run()
@@ -840,6 +841,34 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     value = world * spec_flops(spec) / (ms_per_step * 1e-3) / 1e12
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     w1_fwd_tflops = w1_fwd_flops / (w1_fwd_ms / w1_fwd_n * 1e-3) / 1e12
+
+    # ---- sustained: steps back to back for about --sustain-seconds, the last
+    # --steps of them timed; under this load the GPU reaches its power cap
+    # within tens of milliseconds and settles at a lower SM clock, the state a
+    # training loop runs in.  Compared with the sustained peak.
+    sustained = None
+    if args.sustain_seconds > 0:
+        n_lead = max(0, int(args.sustain_seconds / (ms_per_step * 1e-3)) - args.steps)
+        sampler2 = ClockSampler(dev.index if dev.index is not None else 0)
+        sampler2.start()
+        time.sleep(0.3)
+        barrier()
+        for _ in range(n_lead):
+            step.run()
+        s0, s1 = new_ev()
+        s0.record(stream)
+        for _ in range(args.steps):
+            step.run()
+        s1.record(stream)
+        barrier()
+        clocks2 = sampler2.stop()
+        s_ms = max_over_ranks(s0.elapsed_time(s1) / args.steps, dist, dev)
+        s_value = world * spec_flops(spec) / (s_ms * 1e-3) / 1e12
+        sustained = {"ms_per_step": s_ms, "value": s_value, "unit": "TFLOPS", "steps": args.steps,
+                     "steps_before": n_lead, "pct_of_fp8_peak_sustained": 100.0 * s_value / world / fp8_peak_sustained,
+                     "clocks": clocks2,
+                     "note": "the last steps of about --sustain-seconds of back-to-back steps (no flush), against "
+                             "the sustained peak (cuBLAS bf16 x 2 taken seconds into a loop under the power cap)"}
 
     graph = None
     if args.graph:
@@ -908,7 +937,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "unflushed": {"ms_per_step": unflushed_ms / args.steps,
                       "value": world * spec_flops(spec) / (unflushed_ms / args.steps * 1e-3) / 1e12,
                       "unit": "TFLOPS", "steps": args.steps,
-                      "note": "the same steps back to back with no L2 flush, after the flushed ones"},
+                      "note": "the same number of steps back to back with no flush, right after the flushed "
+                              "ones (later in the clock and power history: see sustained)"},
+        "sustained": sustained,
         "pct_of_fp8_peak": 100.0 * value / world / fp8_peak,
         "pct_of_fp8_peak_sustained": 100.0 * value / world / fp8_peak_sustained,
         "attainable": attainable(spec, args.scaling, fp8_peak, peaks["hbm_gbs"], step.transpose),
@@ -1101,6 +1132,9 @@ def main():
                     help="casts also write the transposed FP8 copies and the backward GEMMs read those "
                          "(default: one copy per tensor, read MN-major by the backward GEMMs)")
     ap.add_argument("--graph", action="store_true", help="also time the step replayed from a CUDA graph")
+    ap.add_argument("--sustain-seconds", type=float, default=1.5,
+                    help="length of the back-to-back run whose last --steps steps give the sustained number "
+                         "(0: skip)")
     ap.add_argument("--e2e-steps", type=int, default=32,
                     help="steps of the end-to-end run; the average includes one pipeline fill and drain")
     ap.add_argument("--cpu-frac", type=float, default=1.0 / 64,

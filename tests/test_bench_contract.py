@@ -59,3 +59,7 @@ def test_our_arm_json_line(fp8lin):
     assert d["parity"] is True and d["parity_detail"]["inputs_sha256_match"] is True
     assert d["unflushed"]["value"] > 0 and "flushed" in d["config"]["l2"]
     assert d["fp8_peak_tflops"]["used"] == "burst" and r["peak"] == d["fp8_peak_tflops"]["burst"]
+    # the steady state under the power cap, against the sustained peak
+    su = d["sustained"]
+    assert su["value"] > 0 and su["steps"] == 3 and "sm_mhz" in su["clocks"]
+    assert abs(su["pct_of_fp8_peak_sustained"] - 100 * su["value"] / d["fp8_peak_tflops"]["sustained"]) < 1e-6
