@@ -41,7 +41,7 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
            6: "FP8LIN_ERR_UNSUPPORTED_DEVICE"}
 
 # Every entry point declared in include/fp8lin.h.
-ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_cast_transpose_static",
+ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_quantize", "fp8lin_cast_transpose_static",
                 "fp8lin_cast_transpose_delayed", "fp8lin_amax_rowcol", "fp8lin_cast_transpose_rowwise",
                 "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
                 "fp8lin_cast_blockwise", "fp8lin_fwd_block", "fp8lin_dgrad_block", "fp8lin_wgrad_block",
@@ -81,6 +81,7 @@ _vp, _i64, _f32, _ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c
 SIGNATURES = {
     "fp8lin_amax": [_vp, _i64, _vp, _vp],
     "fp8lin_cast_transpose": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_quantize": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_cast_transpose_static": [_vp, _i64, _i64, _ci, _vp, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_cast_transpose_delayed": [_vp, _i64, _i64, _ci, _f32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_amax_rowcol": [_vp, _i64, _i64, _vp, _vp, _vp],
@@ -169,6 +170,23 @@ def fp8lin_cast_transpose(x: torch.Tensor, fmt: int, amax: torch.Tensor, scale: 
            _lib.fp8lin_cast_transpose(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(amax),
                                       _ptr(scale), _ptr(inv_scale), _ptr(q), _ptr(qT),
                                       _stream(stream)))
+
+
+def fp8lin_quantize(x: torch.Tensor, fmt: int, amax: torch.Tensor, scale: torch.Tensor, inv_scale: torch.Tensor,
+                    q: torch.Tensor | None, qT: torch.Tensor | None, fmt_max: float = FMT_MAX,
+                    stream=None) -> None:
+    """fp8lin_amax + fp8lin_cast_transpose in one call, for a cast with nothing beside it."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be a 2-D [rows x cols] matrix")
+    for t, n in ((amax, "amax"), (scale, "scale"), (inv_scale, "inv_scale")):
+        _dev(t, n, torch.float32)
+    _dev(q, "q")
+    _dev(qT, "qT")
+    rows, cols = x.shape
+    _check("fp8lin_quantize",
+           _lib.fp8lin_quantize(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(amax), _ptr(scale),
+                                _ptr(inv_scale), _ptr(q), _ptr(qT), _stream(stream)))
 
 
 def fp8lin_cast_transpose_static(x: torch.Tensor, fmt: int, scale: torch.Tensor, inv_scale: torch.Tensor,
@@ -541,8 +559,10 @@ class Float8Tensor:
         self.scale.fill_(float(value))
         return self
 
-    def quantize(self, x: torch.Tensor, stream=None) -> "Float8Tensor":
-        """Scale, cast and transpose x according to this tensor's scaling."""
+    def quantize(self, x: torch.Tensor, stream=None, alone: bool = False) -> "Float8Tensor":
+        """Scale, cast and transpose x according to this tensor's scaling.
+        alone: nothing runs beside this cast (dynamic scaling then takes the
+        one-call fp8lin_quantize, tuned for running alone)."""
         if self.scaling == "mx":
             fp8lin_cast_mx(x, self.fmt, q_row=self.q, sf_row=self.sf_row, q_col=self.qc, sf_col=self.sf_col,
                            fmt_max=self.fmt_max, stream=stream, rule=self.mx_rule)
@@ -553,6 +573,8 @@ class Float8Tensor:
             else:
                 fp8lin_cast_blockwise(x, self.fmt, q_tile=self.q, inv_tile=self.tile_inv, fmt_max=self.fmt_max,
                                       stream=stream)
+        elif self.scaling == "dynamic" and alone:
+            fp8lin_quantize(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT, self.fmt_max, stream)
         elif self.scaling == "dynamic":
             fp8lin_amax(x, self.amax, stream)
             fp8lin_cast_transpose(x, self.fmt, self.amax, self.scale, self.inv_scale, self.q, self.qT,

@@ -10,6 +10,10 @@
 //    patterns order like unsigned integers (NaN above Inf above finite, the
 //    totalOrder of magnitudes), so the reduction runs on packed 16-bit
 //    unsigned maxima (vmaxu2) and never converts to float;
+//  * loads are evict_first in L2 (a GEMM running beside keeps its operands),
+//    except, for a tensor whose cast runs with nothing beside it
+//    (fp8lin_quantize), its last 64 MB: evict_last, so the cast that follows
+//    (last row block first) reads them from L2;
 //  * warp reduction with redux.sync, block reduction through shared memory;
 //    a block issues its atomicMax on the fp32 bit pattern (bf16 << 16) only
 //    when its maximum exceeds the value already there, so the thousands of
@@ -23,12 +27,30 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kVec = 8;                       // 16-byte vectors per thread
 constexpr int kChunk = kThreads * kVec;       // vectors per block (32 KB)
+// Bytes at the end of the tensor the amax pass leaves in L2 for the cast.
+#ifndef FP8LIN_AMAX_KEEP_MB
+#define FP8LIN_AMAX_KEEP_MB 64
+#endif
+constexpr int64_t kKeepBytes = (int64_t)FP8LIN_AMAX_KEEP_MB << 20;
 
 // Streaming 16-byte load: no L1 allocation, and first in line for L2
 // eviction, so a GEMM running beside this kernel keeps its resident operand.
 __device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
+// The same load, kept in L2 (evict_last): the tail of the tensor, which the
+// cast that follows reads first (it visits its tiles last row block first,
+// with evict_first loads that demote the lines once read).
+__device__ __forceinline__ uint4 ld_keep16(const uint4 *p) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -47,13 +69,18 @@ __device__ __forceinline__ uint32_t absmax4(uint32_t m, uint4 v) {
 
 __global__ void __launch_bounds__(kThreads)
 amax_bf16_kernel(const uint4 *__restrict__ x, int64_t nvec, const uint16_t *__restrict__ tail,
-                 int ntail, unsigned int *__restrict__ amax_bits) {
+                 int ntail, unsigned int *__restrict__ amax_bits, int keep_from) {
     const int64_t base = (int64_t)blockIdx.x * kChunk + threadIdx.x;
     uint32_t m = 0;  // two packed 16-bit magnitudes
     if (base + (int64_t)(kVec - 1) * kThreads < nvec) {
         uint4 v[kVec];
+        if ((int)blockIdx.x >= keep_from) {
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) v[u] = ld_stream16(x + base + (int64_t)u * kThreads);
+            for (int u = 0; u < kVec; ++u) v[u] = ld_keep16(x + base + (int64_t)u * kThreads);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) v[u] = ld_stream16(x + base + (int64_t)u * kThreads);
+        }
 #pragma unroll
         for (int u = 0; u < kVec; ++u) m = absmax4(m, v[u]);
     } else {
@@ -210,11 +237,9 @@ extern "C" fp8lin_status fp8lin_amax_rowcol(const void *x, int64_t rows, int64_t
     return check_launch();
 }
 
-extern "C" fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cudaStream_t stream) {
-    using namespace fp8lin;
-    if (amax == nullptr || n < 0 || (n > 0 && x == nullptr)) return FP8LIN_ERR_INVALID_ARG;
-    if (!aligned(amax, 4) || (n > 0 && !aligned(x, 16))) return FP8LIN_ERR_MISALIGNED;
-    if (n > FP8LIN_MAX_DIM * FP8LIN_MAX_DIM) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+namespace fp8lin {
+
+fp8lin_status launch_amax(const void *x, int64_t n, float *amax, cudaStream_t stream, bool alone) {
     DeviceInfo dev;
     fp8lin_status st = current_device(&dev);
     if (st != FP8LIN_OK) return st;
@@ -228,7 +253,21 @@ extern "C" fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cuda
     const int64_t blocks = (nvec + kChunk - 1) / kChunk;
     if (blocks > INT32_MAX) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
     const int grid = blocks < 1 ? 1 : (int)blocks;
+    // Beside a GEMM every load is evict_first (the GEMM's operands keep L2);
+    // alone, the tail is kept for the cast.
+    const int64_t keep_blocks = alone ? kKeepBytes / ((int64_t)kChunk * 16) : 0;
+    const int keep_from = grid > keep_blocks ? (int)(grid - keep_blocks) : 0;
     amax_bf16_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint4 *>(x), nvec, tail, ntail,
-                                                    reinterpret_cast<unsigned int *>(amax));
+                                                    reinterpret_cast<unsigned int *>(amax), keep_from);
     return check_launch();
+}
+
+}  // namespace fp8lin
+
+extern "C" fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cudaStream_t stream) {
+    using namespace fp8lin;
+    if (amax == nullptr || n < 0 || (n > 0 && x == nullptr)) return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(amax, 4) || (n > 0 && !aligned(x, 16))) return FP8LIN_ERR_MISALIGNED;
+    if (n > FP8LIN_MAX_DIM * FP8LIN_MAX_DIM) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    return launch_amax(x, n, amax, stream, false);
 }

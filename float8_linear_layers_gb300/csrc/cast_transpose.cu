@@ -924,6 +924,27 @@ extern "C" fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int6
                        stream);
 }
 
+extern "C" fp8lin_status fp8lin_quantize(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
+                                         float *amax, float *scale, float *inv_scale, uint8_t *q, uint8_t *qT,
+                                         cudaStream_t stream) {
+    using namespace fp8lin;
+    if (amax == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(amax, 4)) return FP8LIN_ERR_MISALIGNED;
+    // the cast's checks first, so that nothing is launched for a bad argument
+    if (rows < 0 || cols < 0 || scale == nullptr || inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
+    if (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f)) return FP8LIN_ERR_INVALID_ARG;
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && x == nullptr) return FP8LIN_ERR_INVALID_ARG;
+    if (!aligned(scale, 4) || !aligned(inv_scale, 4)) return FP8LIN_ERR_MISALIGNED;
+    if (!empty && (!aligned(x, 16) || !aligned(q, 16) || !aligned(qT, 16))) return FP8LIN_ERR_MISALIGNED;
+    if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    fp8lin_status st = launch_amax(x, rows * cols, amax, stream, true);
+    if (st != FP8LIN_OK) return st;
+    return cast_common(kDynamic, x, rows, cols, fmt, fmt_max, amax, 0, 0, scale, inv_scale, q, qT, nullptr,
+                       stream);
+}
+
 extern "C" fp8lin_status fp8lin_cast_transpose_static(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,
                                                       const float *scale, float *inv_scale, uint8_t *q,
                                                       uint8_t *qT, float *amax, cudaStream_t stream) {

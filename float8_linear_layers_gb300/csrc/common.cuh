@@ -34,4 +34,10 @@ fp8lin_status current_device(DeviceInfo *info);
 // cast kernels use the same setting to run beside a GEMM on another stream.
 fp8lin_status prefer_max_shared_carveout(const void *kernel, int device, int slot);
 
+// amax of n bf16 values into *amax (cleared first), on `stream`.  alone:
+// nothing runs beside it, so the tensor's last 64 MB are loaded evict_last
+// and the cast that follows (last rows first) finds them in L2.  Arguments
+// are checked by the caller.
+fp8lin_status launch_amax(const void *x, int64_t n, float *amax, cudaStream_t stream, bool alone);
+
 }  // namespace fp8lin

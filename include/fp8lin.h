@@ -114,13 +114,34 @@ fp8lin_status fp8lin_amax(const void *x, int64_t n, float *amax, cudaStream_t st
  *   qT         device, u8 [cols x rows] or NULL; 16-byte aligned.
  * Every code is sat_RNE(fp32(x) * scale): the binary32 product rounded to
  * nearest even, then rounded to nearest even into the format, saturating at
- * the format's largest finite value (Inf included); NaN stays NaN; the sign
- * of zero is kept.  A NaN amax gives a NaN scale.
+ * the format's largest finite value (Inf included); every NaN (either sign,
+ * any payload) casts to the code 0x7F; the sign of zero is kept.  A NaN amax
+ * gives a NaN scale (0x7FFFFFFF) and every code 0x7F.
  */
 fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols,
                                     fp8lin_fmt fmt, float fmt_max, const float *amax,
                                     float *scale, float *inv_scale,
                                     uint8_t *q, uint8_t *qT, cudaStream_t stream);
+
+/*
+ * Dynamic per-tensor scaling of one tensor in one call: fp8lin_amax followed
+ * by fp8lin_cast_transpose on the same stream, with the same results bit for
+ * bit (TorchTitan analysis page, section 3.3: dynamic scaling takes the
+ * tensor's own statistic every step; Lecture 9 exercises: one factor per
+ * tensor).  For a cast that runs with no GEMM beside it -- the cast a GEMM
+ * waits for: its amax pass loads the tensor's last 64 MB with an L2
+ * evict_last policy, so the cast, which reads the last rows first, finds
+ * them in L2 (fp8lin_amax loads everything evict_first, so that a GEMM
+ * running beside it keeps its own operands in L2).  Beside a running GEMM,
+ * call fp8lin_amax and fp8lin_cast_transpose instead.
+ *
+ *   amax       device, one float: receives max |x| (cleared by the call first).
+ *   x, rows, cols, fmt, fmt_max, scale, inv_scale, q, qT as for
+ *   fp8lin_cast_transpose; arguments are checked before anything is launched.
+ */
+fp8lin_status fp8lin_quantize(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt, float fmt_max,
+                              float *amax, float *scale, float *inv_scale, uint8_t *q, uint8_t *qT,
+                              cudaStream_t stream);
 
 /*
  * Static scaling: cast with a scale the caller fixes (TorchTitan analysis

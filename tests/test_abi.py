@@ -216,3 +216,23 @@ def test_tile_count_limit_of_the_block_casts(lib):
     cb.restype = ctypes.c_int
     cb.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V, V, V]
     assert cb(a16, big, big, 0, 448.0, a16, a16, None, None, None, None, None) == 3
+
+
+def test_argument_checks_of_the_one_call_dynamic_cast(lib):
+    """fp8lin_quantize checks every argument of its amax and its cast before
+    launching either."""
+    a16, a4 = V(4096), V(4100)
+    fq = lib.fp8lin_quantize
+    fq.restype = ctypes.c_int
+    fq.argtypes = [V, I, I, ctypes.c_int, F, V, V, V, V, V, V]
+    assert fq(a16, 32, 32, 0, 448.0, None, a16, a16, a16, None, None) == 1   # no amax slot
+    assert fq(a16, 32, 32, 0, 448.0, a16, None, a16, a16, None, None) == 1   # no scale slot
+    assert fq(a16, 32, 32, 0, 448.0, a16, a16, None, a16, None, None) == 1   # no inverse-scale slot
+    assert fq(a16, 32, 32, 2, 448.0, a16, a16, a16, a16, None, None) == 1    # format
+    assert fq(a16, 32, 32, 0, 0.0, a16, a16, a16, a16, None, None) == 1      # fmt_max
+    assert fq(a16, -16, 32, 0, 448.0, a16, a16, a16, a16, None, None) == 1   # negative rows
+    assert fq(a16, 32, 32, 0, 448.0, V(4098), a16, a16, a16, None, None) == 2  # misaligned amax
+    assert fq(V(4098), 32, 32, 0, 448.0, a16, a16, a16, a16, None, None) == 2  # misaligned input
+    assert fq(a16, 32, 32, 0, 448.0, a16, a16, a16, a4, None, None) == 2     # misaligned copy
+    assert fq(a16, 32, 24, 0, 448.0, a16, a16, a16, a16, None, None) == 3    # ragged shape
+    assert fq(a16, 1 << 31, 32, 0, 448.0, a16, a16, a16, a16, None, None) == 3

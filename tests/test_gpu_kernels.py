@@ -285,3 +285,32 @@ def test_repeated_calls_and_streams(fp8lin):
     torch.cuda.synchronize()
     for u, v in zip(ra, rb):
         assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (144, 272), (1040, 384), (2048, 4096), (8192, 4096)])
+@pytest.mark.parametrize("fmt,dist", [(E4M3, ("normal", 1.0)), (E5M2, ("laplace", 1e-3))])
+@pytest.mark.parametrize("want_qT", [False, True])
+def test_one_call_quantize_matches_amax_then_cast(fp8lin, shape, fmt, dist, want_qT):
+    """fp8lin_quantize (amax + cast in one call, tuned for running alone):
+    amax, scale, inverse scale and every FP8 byte bit-exact against the
+    oracle, and the same bytes as fp8lin_amax followed by
+    fp8lin_cast_transpose.  8192 x 4096 (67 MB) is larger than the part the
+    amax pass keeps in L2, so the cast reads both kept and evicted rows."""
+    rows, cols = shape
+    x = wl.generate(shape, *dist, seed=rows * 3 + cols, tensor_id=9, outlier_frac=1e-3)
+    xd = to_dev_bf16(x)
+    amax = torch.full((1,), -1.0, device="cuda")
+    scale = torch.full((1,), -1.0, device="cuda")
+    inv = torch.full((1,), -1.0, device="cuda")
+    q = Guarded((rows, cols), torch.uint8)
+    qT = Guarded((cols, rows), torch.uint8) if want_qT else None
+    fp8lin.fp8lin_quantize(xd, fmt, amax, scale, inv, q.t, qT.t if qT else None)
+    a2, s2, i2, q2, qT2 = _run_cast(fp8lin, x, fmt, want_qT=want_qT)
+    torch.cuda.synchronize()
+    ref = oracle.quantize(x, fmt)
+    assert scalar_bits(amax) == f32_bits(ref["amax"]) == scalar_bits(a2)
+    assert scalar_bits(scale) == f32_bits(ref["scale"]) == scalar_bits(s2)
+    assert scalar_bits(inv) == f32_bits(ref["inv_scale"]) == scalar_bits(i2)
+    assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and torch.equal(q.t, q2.t) and q.intact()
+    if want_qT:
+        assert np.array_equal(qT.t.cpu().numpy(), ref["qT"]) and torch.equal(qT.t, qT2.t) and qT.intact()
