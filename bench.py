@@ -617,7 +617,12 @@ class StepGraph:
         m, s = self.main, self.side
         ready = {}
         for i, (name, which) in enumerate(self.spec.gemms):
-            if self.beside[i]:
+            if self.beside[i] and self.scaling == "dynamic":
+                # the one-launch dynamic cast occupies every SM: the casts
+                # gating this GEMM run one after another on the main stream
+                for key in self.beside[i]:
+                    self._cast(rec, key, m, alone=True)
+            elif self.beside[i]:
                 marker = self.t.cuda.Event()
                 marker.record(m)                      # the casts gating GEMM i start together
                 s.wait_event(marker)

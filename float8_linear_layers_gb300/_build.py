@@ -77,7 +77,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(out.decode(errors="replace"))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"--- {s}\n{o}" for s, o in failed))
-    for lib, lib_objs in ((LIB, objs), (FAULT_LIB, [fault_obj, os.path.join(OUT, "obj", "api.o")])):
+    fault_objs = [fault_obj] + [os.path.join(OUT, "obj", n) for n in ("api.o", "quantize.o")]
+    for lib, lib_objs in ((LIB, objs), (FAULT_LIB, fault_objs)):
         tmp = lib + f".tmp{os.getpid()}"
         subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *lib_objs], check=True)
         os.replace(tmp, lib)

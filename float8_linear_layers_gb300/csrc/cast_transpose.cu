@@ -939,6 +939,11 @@ extern "C" fp8lin_status fp8lin_quantize(const void *x, int64_t rows, int64_t co
     if (!aligned(scale, 4) || !aligned(inv_scale, 4)) return FP8LIN_ERR_MISALIGNED;
     if (!empty && (!aligned(x, 16) || !aligned(q, 16) || !aligned(qT, 16))) return FP8LIN_ERR_MISALIGNED;
     if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+    if (q != nullptr && qT == nullptr && !empty) {
+        bool launched = false;
+        fp8lin_status st = launch_quantize(x, rows * cols, fmt, fmt_max, amax, scale, inv_scale, q, stream, &launched);
+        if (st != FP8LIN_OK || launched) return st;
+    }
     fp8lin_status st = launch_amax(x, rows * cols, amax, stream, true);
     if (st != FP8LIN_OK) return st;
     return cast_common(kDynamic, x, rows, cols, fmt, fmt_max, amax, 0, 0, scale, inv_scale, q, qT, nullptr,

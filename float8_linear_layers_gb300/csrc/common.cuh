@@ -40,4 +40,16 @@ fp8lin_status prefer_max_shared_carveout(const void *kernel, int device, int slo
 // are checked by the caller.
 fp8lin_status launch_amax(const void *x, int64_t n, float *amax, cudaStream_t stream, bool alone);
 
+// Dynamic per-tensor scaling of n bf16 values into the row-major copy q in
+// one cooperative launch (quantize.cu); *launched says whether it ran (it
+// declines fmt_max above 65504 and devices without cooperative launch, and
+// the caller then takes the two-kernel path).  Arguments are checked by the
+// caller.
+fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fmt_max, float *amax, float *scale,
+                              float *inv_scale, uint8_t *q, cudaStream_t stream, bool *launched);
+
+// Read and clear the device word in which quantize.cu's kernel records a
+// bounded wait that ran out.
+fp8lin_status take_quantize_error(unsigned int *bits);
+
 }  // namespace fp8lin

@@ -2134,9 +2134,11 @@ extern "C" fp8lin_status fp8lin_selftest_bounded_wait(uint64_t limit_ns, cudaStr
 
 extern "C" fp8lin_status fp8lin_device_error(cudaStream_t stream, uint32_t *word) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
-    unsigned int v = 0, zero = 0;
+    unsigned int v = 0, zero = 0, vq = 0;
     if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return FP8LIN_ERR_CUDA;
     if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return FP8LIN_ERR_CUDA;
+    if (fp8lin::take_quantize_error(&vq) != FP8LIN_OK) return FP8LIN_ERR_CUDA;   // the one-launch cast's word
+    v |= vq;
     if (word != nullptr) *word = v;
     return v == 0 ? FP8LIN_OK : FP8LIN_ERR_TIMEOUT;
 }

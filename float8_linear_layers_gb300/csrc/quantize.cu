@@ -1,0 +1,272 @@
+// quantize.cu -- dynamic per-tensor scaling of one bf16 tensor in one launch:
+// amax, scale and the saturating round-to-nearest-even cast to the row-major
+// FP8 copy (TorchTitan analysis page, section 3.3, "Mixed precision and
+// Float8": dynamic scaling takes the tensor's own statistic every step;
+// Lecture 9 exercises: one factor per tensor).  For the cast a GEMM waits
+// for, which runs with nothing beside it.
+//
+// HBM-bound: the two-kernel path (amax, then cast) reads the tensor twice.
+// Here one persistent cooperative grid, one CTA per SM, reads it once for
+// the amax while keeping the last part of each CTA's slice in shared memory,
+// meets at a grid barrier, then casts the staged part from shared memory and
+// the rest of the slice last-read-first (so what L2 still holds is read
+// before it is evicted).  Element i of x becomes byte i of q, so a CTA's
+// slice is a contiguous range of 16-byte vectors (8 elements).
+//
+// The grid barrier uses the call's own output slots, so the kernel needs no
+// memory beyond its inputs and outputs: all three slots are zero when it
+// starts (the host clears them on the stream); every CTA publishes its
+// maximum with atomicMax on the amax slot and then counts itself in on the
+// scale slot (atomicAdd on its bits); the CTA that arrives last reads the
+// amax, overwrites the count with the scale and publishes 1 / scale to the
+// inverse-scale slot with release semantics; the others wait (acquire, at
+// most kWaitLimitNs) until that slot is nonzero.  1 / scale is never zero:
+// scale = fmt_max / max(amax, 1e-12) is finite for fmt_max <= 65504 (the
+// host checks it), and a NaN or infinite amax gives a NaN or infinite
+// inverse.  A wait that runs out records FP8LIN_ERR_TIMEOUT in this file's
+// device error word (read by fp8lin_device_error) and the CTA skips its cast.
+#include <atomic>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kUnroll = 8;                       // 16-byte loads in flight per thread
+#ifndef FP8LIN_QUANTIZE_STAGE_KB
+#define FP8LIN_QUANTIZE_STAGE_KB 192
+#endif
+constexpr int kStageBytes = FP8LIN_QUANTIZE_STAGE_KB * 1024;   // slice tail kept in shared memory
+constexpr int kStageVecs = kStageBytes / 16;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ unsigned int g_quantize_error = 0;
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint4 ld16(const uint4 *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream8(void *p, uint2 v, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, uint4 v) {
+    const uint32_t k = 0x7FFF7FFFu;
+    m = __vmaxu2(m, v.x & k);
+    m = __vmaxu2(m, v.y & k);
+    m = __vmaxu2(m, v.z & k);
+    m = __vmaxu2(m, v.w & k);
+    return m;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d) {
+    // cvt packs its first source operand into the upper byte of each pair
+    uint16_t lo, hi;
+    if (FMT == FP8LIN_E4M3) {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    } else {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    }
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Eight codes sat_RNE(fp32(x) * s): one binary32 multiply, one conversion.
+template <int FMT>
+__device__ __forceinline__ uint2 cast8(uint4 v, float s) {
+    uint2 r;
+    r.x = cvt4<FMT>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s), __fmul_rn(bf16_lo(v.y), s),
+                    __fmul_rn(bf16_hi(v.y), s));
+    r.y = cvt4<FMT>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s), __fmul_rn(bf16_lo(v.w), s),
+                    __fmul_rn(bf16_hi(v.w), s));
+    return r;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+quantize_kernel(const uint4 *__restrict__ x, int64_t nvec, float fmt_max, unsigned int *amax_bits,
+                unsigned int *arrivals, float *scale_out, float *inv_out, uint2 *__restrict__ q) {
+    extern __shared__ uint4 stage[];
+    __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ float s_shared;
+    __shared__ int go;
+
+    const int t = threadIdx.x;
+    const int64_t per = (nvec + gridDim.x - 1) / gridDim.x;
+    const int64_t v0 = min((int64_t)blockIdx.x * per, nvec);
+    const int64_t v1 = min(v0 + per, nvec);
+    const int64_t s0 = max(v0, v1 - (int64_t)kStageVecs);   // [s0, v1) stays in shared memory
+    uint64_t normal, stream;   // phase 1 keeps what phase 2 re-reads; phase 2 and the stores stream
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(normal));
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
+
+    // ---- phase 1: amax of the slice; its tail into shared memory
+    uint32_t m = 0;
+    int64_t i = v0 + t;
+    for (; i + (int64_t)(kUnroll - 1) * kThreads < s0; i += (int64_t)kUnroll * kThreads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld16(x + i + (int64_t)u * kThreads, normal);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) m = absmax8(m, v[u]);
+    }
+    for (; i < s0; i += kThreads) m = absmax8(m, ld16(x + i, normal));
+    for (int64_t j = s0 + t; j < v1; j += (int64_t)kUnroll * kThreads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (j + (int64_t)u * kThreads < v1) v[u] = ld16(x + j + (int64_t)u * kThreads, stream);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (j + (int64_t)u * kThreads < v1) {
+                stage[j + (int64_t)u * kThreads - s0] = v[u];
+                m = absmax8(m, v[u]);
+            }
+    }
+    uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+    if (t % 32 == 0) warp_max[t / 32] = r;
+    __syncthreads();
+
+    // ---- grid barrier on the output slots (see the file comment)
+    if (t < 32) {
+        r = __reduce_max_sync(0xFFFFFFFFu, t < kThreads / 32 ? warp_max[t] : 0u);
+        if (t == 0) {
+            if (r != 0) atomicMax(amax_bits, r << 16);
+            __threadfence();
+            const unsigned int before = atomicAdd(arrivals, 1u);
+            int arrived = 1;
+            float s;
+            if (before == gridDim.x - 1) {
+                __threadfence();
+                float a = __uint_as_float(atomicOr(amax_bits, 0u));
+                a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
+                s = __fdiv_rn(fmt_max, a);
+                *scale_out = s;                 // the count is complete: the slot takes the scale
+                __threadfence();
+                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(inv_out), "r"(__float_as_uint(__frcp_rn(s)))
+                             : "memory");
+            } else {
+                const unsigned long long t0 = globaltimer();
+                uint32_t flag = 0;
+                while (true) {
+                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(flag) : "l"(inv_out) : "memory");
+                    if (flag != 0) break;
+                    if (globaltimer() - t0 > kWaitLimitNs) {
+                        atomicOr(&g_quantize_error, 1u << FP8LIN_ERR_TIMEOUT);
+                        arrived = 0;
+                        break;
+                    }
+                }
+                s = arrived ? *reinterpret_cast<volatile float *>(scale_out) : 0.0f;
+            }
+            s_shared = s;
+            go = arrived;
+        }
+    }
+    __syncthreads();
+    if (!go) return;
+    const float s = s_shared;
+
+    // ---- phase 2: the staged tail from shared memory, then the rest of the
+    // slice last-read-first
+    for (int64_t j = s0 + t; j < v1; j += kThreads) st_stream8(q + j, cast8<FMT>(stage[j - s0], s), stream);
+    const int64_t n_rest = s0 - v0;
+    int64_t k = t;
+    for (; k + (int64_t)(kUnroll - 1) * kThreads < n_rest; k += (int64_t)kUnroll * kThreads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld16(x + (s0 - 1 - k - (int64_t)u * kThreads), stream);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            st_stream8(q + (s0 - 1 - k - (int64_t)u * kThreads), cast8<FMT>(v[u], s), stream);
+    }
+    for (; k < n_rest; k += kThreads) {
+        const int64_t idx = s0 - 1 - k;
+        st_stream8(q + idx, cast8<FMT>(ld16(x + idx, stream), s), stream);
+    }
+}
+
+std::atomic<int> g_grid[2][64];
+
+}  // namespace
+
+namespace fp8lin {
+
+fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fmt_max, float *amax, float *scale,
+                              float *inv_scale, uint8_t *q, cudaStream_t stream, bool *launched) {
+    *launched = false;
+    if (!(fmt_max <= 65504.0f) || n % 8 != 0) return FP8LIN_OK;   // the two-kernel path takes it
+    DeviceInfo dev;
+    fp8lin_status st = current_device(&dev);
+    if (st != FP8LIN_OK) return st;
+    if (dev.device >= 64) return FP8LIN_OK;
+    auto kernel = fmt == FP8LIN_E4M3 ? quantize_kernel<FP8LIN_E4M3> : quantize_kernel<FP8LIN_E5M2>;
+    const int f = fmt == FP8LIN_E4M3 ? 0 : 1;
+    int grid = g_grid[f][dev.device].load(std::memory_order_acquire);
+    if (grid == 0) {
+        int coop = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev.device) != cudaSuccess)
+            return FP8LIN_ERR_CUDA;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, kStageBytes) != cudaSuccess)
+            return FP8LIN_ERR_CUDA;
+        grid = (coop && per_sm >= 1) ? dev.sm_count : -1;   // one CTA per SM, all resident together
+        g_grid[f][dev.device].store(grid, std::memory_order_release);
+    }
+    if (grid < 0) return FP8LIN_OK;
+    const int64_t nvec = n / 8;
+    if (nvec == 0) return FP8LIN_OK;
+    const int g = nvec < grid ? (int)nvec : grid;
+    // the three slots start at zero: the count, the flag and the maximum
+    if (scale == amax + 1 && inv_scale == amax + 2) {
+        if (cudaMemsetAsync(amax, 0, 3 * sizeof(float), stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
+    } else if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess ||
+               cudaMemsetAsync(scale, 0, sizeof(float), stream) != cudaSuccess ||
+               cudaMemsetAsync(inv_scale, 0, sizeof(float), stream) != cudaSuccess) {
+        return FP8LIN_ERR_CUDA;
+    }
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;
+    attr.val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)g);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kStageBytes;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4 *>(x), nvec, fmt_max,
+                           reinterpret_cast<unsigned int *>(amax), reinterpret_cast<unsigned int *>(scale), scale,
+                           inv_scale, reinterpret_cast<uint2 *>(q)) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
+    *launched = true;
+    return check_launch();
+}
+
+fp8lin_status take_quantize_error(unsigned int *bits) {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_quantize_error, sizeof v) != cudaSuccess) return FP8LIN_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_quantize_error, &zero, sizeof zero) != cudaSuccess) return FP8LIN_ERR_CUDA;
+    *bits = v;
+    return FP8LIN_OK;
+}
+
+}  // namespace fp8lin

@@ -314,3 +314,40 @@ def test_one_call_quantize_matches_amax_then_cast(fp8lin, shape, fmt, dist, want
     assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and torch.equal(q.t, q2.t) and q.intact()
     if want_qT:
         assert np.array_equal(qT.t.cpu().numpy(), ref["qT"]) and torch.equal(qT.t, qT2.t) and qT.intact()
+
+
+@pytest.mark.parametrize("fmt_max", [448.0, 57344.0, 1.0e5])
+def test_one_call_quantize_fmt_max_and_separate_slots(fp8lin, fmt_max):
+    """fp8lin_quantize with amax, scale and inverse scale in separate
+    allocations (each slot cleared on its own), and with fmt_max above
+    65504 (taken by the two-kernel path): same bytes as the oracle."""
+    x = wl.generate((1040, 2048), "laplace", 1e-3, seed=77, tensor_id=2)
+    amax, scale, inv = (torch.full((4,), 7.0, device="cuda")[:1] for _ in range(3))
+    q = Guarded((1040, 2048), torch.uint8)
+    fp8lin.fp8lin_quantize(to_dev_bf16(x), E5M2, amax, scale, inv, q.t, None, fmt_max)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    ref = oracle.quantize(x, E5M2, fmt_max)
+    assert scalar_bits(amax) == f32_bits(ref["amax"]) and scalar_bits(scale) == f32_bits(ref["scale"])
+    assert scalar_bits(inv) == f32_bits(ref["inv_scale"])
+    assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and q.intact()
+
+
+def test_one_call_quantize_repeated_and_empty(fp8lin):
+    """Back-to-back calls reuse the same slots (each call clears them before
+    its grid counts itself in); an empty matrix publishes the floor scale."""
+    xs = [wl.generate((2048, 1024), "normal", sd, seed=80 + i, tensor_id=0) for i, sd in enumerate((1.0, 0.02, 3.0))]
+    slots = torch.zeros(3, device="cuda")
+    q = torch.empty((2048, 1024), dtype=torch.uint8, device="cuda")
+    for x in xs:
+        fp8lin.fp8lin_quantize(to_dev_bf16(x), E4M3, slots[0:1], slots[1:2], slots[2:3], q, None)
+        torch.cuda.synchronize()
+        ref = oracle.quantize(x, E4M3)
+        assert scalar_bits(slots[1:2]) == f32_bits(ref["scale"])
+        assert np.array_equal(q.cpu().numpy(), ref["q"])
+    e = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_quantize(e, E4M3, slots[0:1], slots[1:2], slots[2:3], torch.empty((0, 64), dtype=torch.uint8,
+                                                                                     device="cuda"), None)
+    torch.cuda.synchronize()
+    assert slots[0].item() == 0.0 and scalar_bits(slots[1:2]) == f32_bits(oracle.scale(np.float32(0.0))[0])
+    assert fp8lin.fp8lin_device_error() == 0

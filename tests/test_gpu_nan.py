@@ -146,3 +146,21 @@ def test_mx_cast_nan_blocks(fp8lin, fmt, rule):
         ref_atoms = oracle.pack_sf(oracle.sf_by_operand_row(ref["sf"], along), P, K).reshape(-1)
         _same_bytes(gs.cpu().numpy(), ref_atoms, None, f"{along} scale atoms")
         _same_bytes(gq.cpu().numpy(), ref["q"], x, f"{along} q")
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_one_call_quantize_with_nan(fp8lin, fmt):
+    """The one-launch dynamic cast (fp8lin_quantize, no transposed copy) on a
+    tensor holding NaNs: amax, scale and inverse scale NaN exactly as the
+    oracle's, every code 0x7F."""
+    x = _nan_matrix(512, 384, 75)
+    slots = torch.zeros(3, device="cuda")
+    q = torch.empty((512, 384), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_quantize(to_dev_bf16(x), fmt, slots[0:1], slots[1:2], slots[2:3], q, None)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    ref = oracle.quantize(x, fmt)
+    _same_f32(slots[0:1].cpu().numpy(), ref["amax"], "amax")
+    _same_f32(slots[1:2].cpu().numpy(), ref["scale"], "scale")
+    _same_f32(slots[2:3].cpu().numpy(), ref["inv_scale"], "inv_scale")
+    _same_bytes(q.cpu().numpy(), ref["q"], x, "q")
