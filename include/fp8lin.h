@@ -129,11 +129,16 @@ fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols,
  * bit (TorchTitan analysis page, section 3.3: dynamic scaling takes the
  * tensor's own statistic every step; Lecture 9 exercises: one factor per
  * tensor).  For a cast that runs with no GEMM beside it -- the cast a GEMM
- * waits for: its amax pass loads the tensor's last 64 MB with an L2
- * evict_last policy, so the cast, which reads the last rows first, finds
- * them in L2 (fp8lin_amax loads everything evict_first, so that a GEMM
- * running beside it keeps its own operands in L2).  Beside a running GEMM,
- * call fp8lin_amax and fp8lin_cast_transpose instead.
+ * waits for.  With q and no qT (and fmt_max <= 65504) it is one cooperative
+ * launch with one CTA on every SM: the grid reads x once for the amax,
+ * keeping part of it in shared memory, meets at a grid barrier held in the
+ * amax / scale / inverse-scale slots themselves (the call clears them
+ * first; no other device memory is used), and casts.  Otherwise it is
+ * fp8lin_amax (with the tensor's last 64 MB kept in L2 for the cast) and
+ * fp8lin_cast_transpose.  Beside a running GEMM, or for two casts at once on
+ * two streams (each grid wants every SM), call fp8lin_amax and
+ * fp8lin_cast_transpose instead.  A grid barrier that does not complete
+ * within 2 s records FP8LIN_ERR_TIMEOUT for fp8lin_device_error.
  *
  *   amax       device, one float: receives max |x| (cleared by the call first).
  *   x, rows, cols, fmt, fmt_max, scale, inv_scale, q, qT as for
@@ -480,8 +485,8 @@ fp8lin_status fp8lin_wgrad_mx(const uint8_t *dyq, const uint8_t *sf_dy, const ui
 const char *fp8lin_status_str(fp8lin_status status);
 
 /*
- * Read and clear the device word in which a GEMM kernel records a bounded
- * wait that ran out.  Synchronises `stream` first.  Returns FP8LIN_OK when
+ * Read and clear the device words in which a GEMM kernel or the one-launch
+ * cast of fp8lin_quantize records a bounded wait that ran out.  Synchronises `stream` first.  Returns FP8LIN_OK when
  * no kernel timed out since the last call, FP8LIN_ERR_TIMEOUT when one did
  * (and writes the raw word to *word when word is not NULL).
  */
