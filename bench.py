@@ -1015,7 +1015,7 @@ def run_profile_case(args) -> None:
     case = args.profile_case
     need_x = case in ("gemm_fwd", "gemm_wgrad", "gemm_wgrad_mn")
     need_w = case in ("gemm_fwd", "gemm_dgrad", "gemm_dgrad_mn")
-    need_dy = case in ("gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn", "gemm_wgrad_mn", "amax", "cast", "cast_q",
+    need_dy = case in ("gemm_dgrad", "gemm_wgrad", "gemm_dgrad_mn", "gemm_wgrad_mn", "amax", "cast", "cast_q", "quantize",
                        "amax_rowcol", "cast_rowwise", "gemm_fwd_block", "gemm_dgrad_block", "gemm_wgrad_block",
                        "cast_block", "gemm_fwd_mx", "gemm_dgrad_mx", "gemm_wgrad_mx", "cast_mx")  # dY: 235 MB > L2
     x8 = w8 = d8 = None
@@ -1101,6 +1101,10 @@ def run_profile_case(args) -> None:
     elif case == "amax":
         launch = lambda: fl.fp8lin_amax(dy, d8.amax)
         work, unit = 2 * w.M * w.N, "byte"
+    elif case == "quantize":
+        # the one-launch dynamic cast: amax, scale and q (2 B read + 1 B written per element, algorithmic)
+        launch = lambda: fl.fp8lin_quantize(dy, fl.E5M2, d8.amax, d8.scale, d8.inv_scale, d8.q, None)
+        work, unit = 3 * w.M * w.N, "byte"
     elif case == "amax_rowcol":
         ra = torch.zeros(w.M, device=dev)
         ca = torch.zeros(w.N, device=dev)
@@ -1161,7 +1165,7 @@ def main():
                                                "gemm_wgrad_mn", "gemm_fwd_block", "gemm_dgrad_block",
                                                "gemm_wgrad_block", "amax", "cast", "cast_q", "cast_block",
                                                "amax_rowcol", "cast_rowwise", "gemm_fwd_mx", "gemm_dgrad_mx",
-                                               "gemm_wgrad_mx", "cast_mx"],
+                                               "gemm_wgrad_mx", "cast_mx", "quantize"],
                     help="run one kernel of the w1 linear alone (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least three warm-up steps
