@@ -503,7 +503,8 @@ class StepGraph:
             self.main = torch.cuda.Stream(device=dev, priority=-1)
             self.side = torch.cuda.Stream(device=dev, priority=0)
         else:
-            self.main = self.side = torch.cuda.current_stream(dev)
+            # one stream; not the legacy default stream, so the step can be captured in a CUDA graph
+            self.main = self.side = torch.cuda.Stream(device=dev)
         self._plan()
         per_cast = 2 if scaling in ("dynamic", "rowwise") else 1   # block, mx and delayed: one kernel per cast
         self.kernels_per_step = per_cast * len(self.t8) + len(spec.gemms)
