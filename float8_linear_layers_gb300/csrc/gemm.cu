@@ -99,11 +99,12 @@ __device__ unsigned int g_device_error = 0;
 
 #ifdef FP8LIN_FAULT_INJECTION
 // Test builds only (a library of its own, never the product one).  When
-// g_withhold_slab >= 0, the producers of every CTA pair of the per-tensor
-// GEMM skip the copies of their g_withhold_slab-th slab (counted over the
-// pair's tiles) and the leader skips its arrival on that stage's full
-// barrier: nothing is ever in flight on it, so the MMA issuer's bounded
-// wait on it runs out and the kernel takes its abort path.
+// g_withhold_slab >= 0, the producers of every CTA pair skip the copies of
+// their g_withhold_slab-th slab (counted over the pair's tiles; for the
+// power-of-two block-scaled GEMM, its stage of two slabs, scale atoms
+// included) and the arrivals that would have expected them: nothing is ever
+// in flight on that stage, so the MMA issuer's bounded wait on it runs out
+// and the kernel takes its abort path.
 __device__ int g_withhold_slab = -1;
 #endif
 
@@ -925,6 +926,10 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
             uint32_t armed = 0, armed_parity = 0;
             uint64_t pol_a, pol_b;
             operand_policies(tiles.swap, pol_a, pol_b);
+#ifdef FP8LIN_FAULT_INJECTION
+            const int withhold = g_withhold_slab;
+            int slab = 0;
+#endif
             for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
@@ -932,15 +937,21 @@ fp8_gemm_block_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_co
                 const int b_row = tn * kPairN + (int)rank * kBN;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait_inl(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
-                    const uint32_t fb_local = smem_u32(&full[stage]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
-                    const uint32_t fb = mapa_shared(fb_local, 0);
-                    if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK, pol_a);
-                    else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row, pol_a);
-                    if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK, pol_b);
-                    else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row, pol_b);
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    bool issue = true;
+#ifdef FP8LIN_FAULT_INJECTION
+                    issue = slab++ != withhold;
+#endif
+                    if (issue) {
+                        const uint32_t fb_local = smem_u32(&full[stage]);
+                        if (leader) mbar_arrive_expect_tx(fb_local, 2 * (kAStage + kBStage));
+                        const uint32_t fb = mapa_shared(fb_local, 0);
+                        if (A_MN) tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, a_row, kb * kBK, pol_a);
+                        else      tma_load_2d_pair(smem_u32(sA + stage * kAStage), &map_a, fb, kb * kBK, a_row, pol_a);
+                        if (B_MN) tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, b_row, kb * kBK, pol_b);
+                        else      tma_load_2d_pair(smem_u32(sB + stage * kBStage), &map_b, fb, kb * kBK, b_row, pol_b);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    }
                     if (++stage == kBlkStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -1400,6 +1411,10 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             uint32_t armed = 0, armed_parity = 0;
             uint64_t pol_a, pol_b;
             operand_policies(tiles.swap, pol_a, pol_b);
+#ifdef FP8LIN_FAULT_INJECTION
+            const int withhold = g_withhold_slab;   // counted in stages (two slabs each) here
+            int stage_count = 0;
+#endif
             for (int t = pair; t < num_tiles && !*abort_flag; t += npairs) {
                 int tm, tn;
                 tiles.coords(t, tm, tn);
@@ -1407,6 +1422,16 @@ fp8_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                 const int b_row = tn * kPairN + (int)rank * kBN;
                 for (int ks = 0; ks < num_st; ++ks) {
                     if (!mbar_wait_inl(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) break;
+#ifdef FP8LIN_FAULT_INJECTION
+                    if (stage_count++ == withhold) {
+                        // neither this stage's slabs nor its scale atoms are copied
+                        if (++stage == kMxStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+#endif
                     const uint32_t fb_local = smem_u32(&full[stage]);
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * kMxSlabs * (kAStage + kBStage));
                     const uint32_t sb = smem_u32(&sf_full[stage]);
@@ -2144,9 +2169,10 @@ extern "C" fp8lin_status fp8lin_device_error(cudaStream_t stream, uint32_t *word
 }
 
 #ifdef FP8LIN_FAULT_INJECTION
-// Test builds only: choose the slab whose copies the per-tensor GEMM's
-// producers withhold (-1: none).  Synchronous; takes effect from the next
-// launch on the current device.
+// Test builds only: choose the slab (the stage, for the power-of-two
+// block-scaled GEMM) whose copies every GEMM's producers withhold (-1:
+// none).  Synchronous; takes effect from the next launch on the current
+// device.
 extern "C" fp8lin_status fp8lin_test_withhold_slab(int slab) {
     if (slab < -1) return FP8LIN_ERR_INVALID_ARG;
     if (cudaMemcpyToSymbol(g_withhold_slab, &slab, sizeof slab) != cudaSuccess) return FP8LIN_ERR_CUDA;
