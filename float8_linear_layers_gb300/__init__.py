@@ -629,8 +629,9 @@ class Float8Linear:
         return 6 * self.M * self.N * self.K
 
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
-        self.x8.quantize(x, stream)
-        self.w8.quantize(w, stream)
+        # the step runs on one stream: every cast has nothing beside it
+        self.x8.quantize(x, stream, alone=True)
+        self.w8.quantize(w, stream, alone=True)
         if self.x8.scaling == "mx":
             fp8lin_fwd_mx(self.x8.q, self.x8.sf_row, self.w8.q, self.w8.sf_row, self.y, stream)
         elif self.x8.scaling == "block":
@@ -642,7 +643,7 @@ class Float8Linear:
         return self.y
 
     def backward(self, dy: torch.Tensor, stream=None):
-        self.dy8.quantize(dy, stream)
+        self.dy8.quantize(dy, stream, alone=True)
         if self.dy8.scaling == "mx":
             fp8lin_dgrad_mx(self.dy8.q, self.dy8.sf_row, self.w8.qc, self.w8.sf_col, self.dx, stream)
             fp8lin_wgrad_mx(self.dy8.qc, self.dy8.sf_col, self.x8.qc, self.x8.sf_col, self.dw, stream)
@@ -665,7 +666,8 @@ class Float8Linear:
         self.backward(dy, stream)
         return self.y, self.dx, self.dw
 
-    # kernels one step launches (amax x3, cast x3, three GEMMs)
+    # kernels one dynamic step launches at most (amax x3, cast x3, three GEMMs;
+    # fewer where a cast takes the one-launch path of fp8lin_quantize)
     KERNELS_PER_STEP = 9
 
 
