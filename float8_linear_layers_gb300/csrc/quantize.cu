@@ -253,10 +253,18 @@ fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fm
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4 *>(x), nvec, fmt_max,
-                           reinterpret_cast<unsigned int *>(amax), reinterpret_cast<unsigned int *>(scale), scale,
-                           inv_scale, reinterpret_cast<uint2 *>(q)) != cudaSuccess)
-        return FP8LIN_ERR_CUDA;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4 *>(x), nvec, fmt_max,
+                                             reinterpret_cast<unsigned int *>(amax),
+                                             reinterpret_cast<unsigned int *>(scale), scale, inv_scale,
+                                             reinterpret_cast<uint2 *>(q));
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        // fewer SMs than the device reports are available to this context:
+        // the caller takes the two-kernel path, now and from here on
+        (void)cudaGetLastError();
+        g_grid[f][dev.device].store(-1, std::memory_order_release);
+        return FP8LIN_OK;
+    }
+    if (e != cudaSuccess) return FP8LIN_ERR_CUDA;
     *launched = true;
     return check_launch();
 }
