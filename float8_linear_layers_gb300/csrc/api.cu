@@ -36,8 +36,9 @@ fp8lin_status current_device(DeviceInfo *info) {
 }
 
 namespace {
-constexpr int kMaxCarveoutSlots = 48;  // amax 0, amax_rowcol 9, cast e4m3 1..4 and 21, cast e5m2 5..8 and 25,
-                                       // block casts e4m3 33..39, e5m2 41..47
+constexpr int kMaxCarveoutSlots = 80;  // amax 0, amax_rowcol 9, cast e4m3 1..4 and 21, cast e5m2 5..8 and 25,
+                                       // block casts e4m3 33..39, e5m2 41..47, the casts without a
+                                       // transposed copy at 48 more than their transposing form
 std::atomic<bool> g_carveout_set[kMaxDevices][kMaxCarveoutSlots];
 }  // namespace
 

@@ -143,14 +143,17 @@ __device__ __forceinline__ uint32_t absmax8(uint32_t m, uint4 v) {
     return m;
 }
 
-template <int FMT, int MODE, bool RECORD>
+// TRANS = false: no transposed copy (qT is NULL), so no shared tile either:
+// beside a GEMM CTA, whose shared memory leaves room for one 16 KB tile per
+// SM, the registers then fit two CTAs of this kernel instead of one.
+template <int FMT, int MODE, bool RECORD, bool TRANS>
 __global__ void __launch_bounds__(kThreads)
 cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int tiles_c, int num_tiles,
                       float fmt_max, const float *__restrict__ scale_src, int hist_len, int slot,
                       float *__restrict__ scale_out, float *__restrict__ inv_out, uint8_t *__restrict__ q,
                       uint8_t *__restrict__ qT, unsigned int *__restrict__ amax_record,
                       const float *__restrict__ col_src, float *__restrict__ col_inv_out) {
-    __shared__ __align__(16) uint32_t tile[kTile][kTile / 4];
+    __shared__ __align__(16) uint32_t tile[TRANS ? kTile : 1][kTile / 4];
     __shared__ uint32_t warp_max[kThreads / 32];
     __shared__ float srow[MODE == kRowwise ? kTile : 1], scol[MODE == kRowwise ? kTile : 1];
 
@@ -235,8 +238,7 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
             const int r = r0 + lr;
             if (q != nullptr && col_in && r < rows)
                 st_stream8(q + (int64_t)r * cols + c0 + ch * 8, cast8<FMT>(v[i], srow[lr]), pol);
-            if (qT != nullptr)
-                *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = cast8_each<FMT>(v[i], csc);
+            if (TRANS) *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = cast8_each<FMT>(v[i], csc);
         }
     } else {
 #pragma unroll
@@ -246,47 +248,64 @@ cast_transpose_kernel(const uint16_t *__restrict__ x, int rows, int cols, int ti
             const uint2 p = cast8<FMT>(v[i], s);
             if (q != nullptr && col_in && r < rows)
                 st_stream8(q + (int64_t)r * cols + c0 + ch * 8, p, pol);
-            if (qT != nullptr)
-                *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = p;
+            if (TRANS) *reinterpret_cast<uint2 *>(&tile[lr][swz(lr, 2 * ch)]) = p;
         }
     }
-    if (qT == nullptr) return;
-    __syncthreads();
+    if constexpr (!TRANS) {
+        return;
+    } else {
+        __syncthreads();
 
-    // ---- phase 2: warp w owns columns 16w..16w+15; lane (rc, cq) owns rows
-    // 16 rc .. 16 rc + 15 of columns 16 w + 4 cq .. + 3.
-    const int w = t / 32, lane = t % 32;
-    const int rc = lane % 8, cq = lane / 8;
-    const int word = 4 * w + cq;
-    uint32_t rw[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int lr = 16 * rc + i;
-        rw[i] = tile[lr][swz(lr, word)];
-    }
-    // out[j][k]: column j, rows 4k .. 4k+3 (byte b = row 4k+b)
-    uint32_t out[4][4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t a0 = rw[4 * k], a1 = rw[4 * k + 1], a2 = rw[4 * k + 2], a3 = rw[4 * k + 3];
-        const uint32_t t0 = __byte_perm(a0, a1, 0x5140);  // a0.b0 a1.b0 a0.b1 a1.b1
-        const uint32_t t1 = __byte_perm(a2, a3, 0x5140);  // a2.b0 a3.b0 a2.b1 a3.b1
-        const uint32_t t2 = __byte_perm(a0, a1, 0x7362);  // a0.b2 a1.b2 a0.b3 a1.b3
-        const uint32_t t3 = __byte_perm(a2, a3, 0x7362);  // a2.b2 a3.b2 a2.b3 a3.b3
-        out[0][k] = __byte_perm(t0, t1, 0x5410);
-        out[1][k] = __byte_perm(t0, t1, 0x7632);
-        out[2][k] = __byte_perm(t2, t3, 0x5410);
-        out[3][k] = __byte_perm(t2, t3, 0x7632);
-    }
-    const int rr = r0 + 16 * rc;
-    if (rr < rows) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = c0 + 16 * w + 4 * cq + j;
-            if (c < cols)
-                st_stream16(qT + (int64_t)c * rows + rr, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]), pol);
+        // ---- phase 2: warp w owns columns 16w..16w+15; lane (rc, cq) owns rows
+        // 16 rc .. 16 rc + 15 of columns 16 w + 4 cq .. + 3.
+        const int w = t / 32, lane = t % 32;
+        const int rc = lane % 8, cq = lane / 8;
+        const int word = 4 * w + cq;
+        uint32_t rw[16];
+    #pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int lr = 16 * rc + i;
+            rw[i] = tile[lr][swz(lr, word)];
+        }
+        // out[j][k]: column j, rows 4k .. 4k+3 (byte b = row 4k+b)
+        uint32_t out[4][4];
+    #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t a0 = rw[4 * k], a1 = rw[4 * k + 1], a2 = rw[4 * k + 2], a3 = rw[4 * k + 3];
+            const uint32_t t0 = __byte_perm(a0, a1, 0x5140);  // a0.b0 a1.b0 a0.b1 a1.b1
+            const uint32_t t1 = __byte_perm(a2, a3, 0x5140);  // a2.b0 a3.b0 a2.b1 a3.b1
+            const uint32_t t2 = __byte_perm(a0, a1, 0x7362);  // a0.b2 a1.b2 a0.b3 a1.b3
+            const uint32_t t3 = __byte_perm(a2, a3, 0x7362);  // a2.b2 a3.b2 a2.b3 a3.b3
+            out[0][k] = __byte_perm(t0, t1, 0x5410);
+            out[1][k] = __byte_perm(t0, t1, 0x7632);
+            out[2][k] = __byte_perm(t2, t3, 0x5410);
+            out[3][k] = __byte_perm(t2, t3, 0x7632);
+        }
+        const int rr = r0 + 16 * rc;
+        if (rr < rows) {
+    #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + 16 * w + 4 * cq + j;
+                if (c < cols)
+                    st_stream16(qT + (int64_t)c * rows + rr, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]), pol);
+            }
         }
     }
+}
+
+// One launch of the cast, with or without the transposed copy.
+template <int FMT, int MODE, bool REC>
+void launch_cast(int grid, cudaStream_t stream, const uint16_t *x, int rows, int cols, int tiles_c, int num_tiles,
+                 float fmt_max, const float *src, int hist_len, int slot, float *scale, float *inv, uint8_t *q,
+                 uint8_t *qT, unsigned int *rec, const float *col_src, float *col_inv) {
+    if (qT != nullptr)
+        cast_transpose_kernel<FMT, MODE, REC, true><<<grid, kThreads, 0, stream>>>(
+            x, rows, cols, tiles_c, num_tiles, fmt_max, src, hist_len, slot, scale, inv, q, qT, rec, col_src,
+            col_inv);
+    else
+        cast_transpose_kernel<FMT, MODE, REC, false><<<grid, kThreads, 0, stream>>>(
+            x, rows, cols, tiles_c, num_tiles, fmt_max, src, hist_len, slot, scale, inv, q, qT, rec, col_src,
+            col_inv);
 }
 
 template <int FMT>
@@ -294,42 +313,41 @@ void launch_mode(int mode, bool record, int grid, cudaStream_t stream, const uin
                  int tiles_c, int num_tiles, float fmt_max, const float *src, int hist_len, int slot,
                  float *scale, float *inv, uint8_t *q, uint8_t *qT, unsigned int *rec, const float *col_src,
                  float *col_inv) {
-#define FP8LIN_CAST_LAUNCH(MODE, REC)                                                                        \
-    cast_transpose_kernel<FMT, MODE, REC><<<grid, kThreads, 0, stream>>>(x, rows, cols, tiles_c, num_tiles,  \
-                                                                          fmt_max, src, hist_len, slot,      \
-                                                                          scale, inv, q, qT, rec, col_src,   \
-                                                                          col_inv)
+    auto launch = [&](auto fn) {
+        fn(grid, stream, x, rows, cols, tiles_c, num_tiles, fmt_max, src, hist_len, slot, scale, inv, q, qT, rec,
+           col_src, col_inv);
+    };
     if (mode == kRowwise)
-        FP8LIN_CAST_LAUNCH(kRowwise, false);
+        launch(launch_cast<FMT, kRowwise, false>);
     else if (mode == kDynamic)
-        FP8LIN_CAST_LAUNCH(kDynamic, false);
+        launch(launch_cast<FMT, kDynamic, false>);
     else if (mode == kStatic && !record)
-        FP8LIN_CAST_LAUNCH(kStatic, false);
+        launch(launch_cast<FMT, kStatic, false>);
     else if (mode == kStatic)
-        FP8LIN_CAST_LAUNCH(kStatic, true);
+        launch(launch_cast<FMT, kStatic, true>);
     else
-        FP8LIN_CAST_LAUNCH(kDelayed, true);
-#undef FP8LIN_CAST_LAUNCH
+        launch(launch_cast<FMT, kDelayed, true>);
+}
+
+// The max-shared carveout for both forms (with and without the transposed
+// copy) of one mode; carveout slots `slot` and `slot` + 48.
+template <int FMT, int MODE, bool REC>
+fp8lin_status carveout_pair(int device, int slot) {
+    fp8lin_status st = fp8lin::prefer_max_shared_carveout(
+        reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, MODE, REC, true>), device, slot);
+    if (st != FP8LIN_OK) return st;
+    return fp8lin::prefer_max_shared_carveout(
+        reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, MODE, REC, false>), device, slot + 48);
 }
 
 template <int FMT>
 fp8lin_status set_carveouts(int device) {
-    using namespace fp8lin;
     const int base = FMT == FP8LIN_E4M3 ? 1 : 5;
-    fp8lin_status st = prefer_max_shared_carveout(
-        reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kDynamic, false>), device, base);
-    if (st == FP8LIN_OK)
-        st = prefer_max_shared_carveout(
-            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kStatic, false>), device, base + 1);
-    if (st == FP8LIN_OK)
-        st = prefer_max_shared_carveout(
-            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kStatic, true>), device, base + 2);
-    if (st == FP8LIN_OK)
-        st = prefer_max_shared_carveout(
-            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kDelayed, true>), device, base + 3);
-    if (st == FP8LIN_OK)
-        st = prefer_max_shared_carveout(
-            reinterpret_cast<const void *>(&cast_transpose_kernel<FMT, kRowwise, false>), device, base + 20);
+    fp8lin_status st = carveout_pair<FMT, kDynamic, false>(device, base);
+    if (st == FP8LIN_OK) st = carveout_pair<FMT, kStatic, false>(device, base + 1);
+    if (st == FP8LIN_OK) st = carveout_pair<FMT, kStatic, true>(device, base + 2);
+    if (st == FP8LIN_OK) st = carveout_pair<FMT, kDelayed, true>(device, base + 3);
+    if (st == FP8LIN_OK) st = carveout_pair<FMT, kRowwise, false>(device, base + 20);
     return st;
 }
 
