@@ -25,6 +25,9 @@
 // host checks it), and a NaN or infinite amax gives a NaN or infinite
 // inverse.  A wait that runs out records FP8LIN_ERR_TIMEOUT in this file's
 // device error word (read by fp8lin_device_error) and the CTA skips its cast.
+//
+// A tensor of at most 1.5 MB takes quantize_cluster_kernel instead (further
+// down): one cluster of eight CTAs, no grid barrier and no clearing launch.
 #include <atomic>
 #include <cstdint>
 
@@ -204,7 +207,141 @@ quantize_kernel(const uint4 *__restrict__ x, int64_t nvec, float fmt_max, unsign
     }
 }
 
+// Small tensors (up to kSmallMaxVecs vectors, 1.5 MB of bf16): one cluster
+// of kClusterCtas CTAs stages the whole tensor in shared memory, each CTA a
+// contiguous slice.  The CTAs meet at a hardware cluster barrier, read the
+// other CTAs' maxima from their shared memory (distributed shared memory),
+// derive the same scale, and cast their staged slice.  The slots need no
+// clearing and no global memory holds a partial result, so the launch needs
+// no memset, and no wait is a spin: the barrier is the cluster's own, whose
+// CTAs are resident together by construction.  A second barrier keeps every
+// CTA resident until its peers have read its maximum.
+constexpr int kClusterCtas = 8;
+constexpr int kSmallThreads = 512;
+constexpr int kSmallStageBytes = 192 * 1024;
+constexpr int64_t kSmallMaxVecs = (int64_t)kClusterCtas * (kSmallStageBytes / 16);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// A 32-bit word of peer CTA `rank`'s shared memory, at the address `local` has here.
+__device__ __forceinline__ uint32_t ld_peer_u32(const uint32_t *local, uint32_t rank) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+quantize_cluster_kernel(const uint4 *__restrict__ x, int64_t nvec, int64_t per, float fmt_max,
+                        unsigned int *amax_out, float *scale_out, float *inv_out, uint2 *__restrict__ q) {
+    extern __shared__ uint4 stage[];
+    __shared__ uint32_t warp_max[kSmallThreads / 32];
+    __shared__ uint32_t cta_max;
+
+    const int t = threadIdx.x;
+    const uint32_t rank = cluster_rank();
+    const int64_t v0 = min((int64_t)rank * per, nvec);
+    const int64_t v1 = min(v0 + per, nvec);
+    uint64_t stream;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
+
+    // ---- the slice into shared memory, and its maximum |x|
+    uint32_t m = 0;
+    for (int64_t j = v0 + t; j < v1; j += (int64_t)kUnroll * kSmallThreads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (j + (int64_t)u * kSmallThreads < v1) v[u] = ld16(x + j + (int64_t)u * kSmallThreads, stream);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (j + (int64_t)u * kSmallThreads < v1) {
+                stage[j + (int64_t)u * kSmallThreads - v0] = v[u];
+                m = absmax8(m, v[u]);
+            }
+    }
+    uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+    if (t % 32 == 0) warp_max[t / 32] = r;
+    __syncthreads();
+    if (t < 32) {
+        r = __reduce_max_sync(0xFFFFFFFFu, t < kSmallThreads / 32 ? warp_max[t] : 0u);
+        if (t == 0) cta_max = r;
+    }
+    cluster_arrive();
+    cluster_wait();   // every CTA's maximum is in its shared memory
+
+    // ---- the tensor's maximum from every CTA's (each warp reads them), the scale
+    const int lane = t % 32;
+    r = lane < kClusterCtas ? ld_peer_u32(&cta_max, (uint32_t)lane) : 0u;
+    r = __reduce_max_sync(0xFFFFFFFFu, r);
+    cluster_arrive();   // this CTA is done reading its peers' shared memory
+    const uint32_t amax_bits = r << 16;
+    float a = __uint_as_float(amax_bits);
+    a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
+    const float s = __fdiv_rn(fmt_max, a);
+    if (rank == 0 && t == 0) {
+        *amax_out = amax_bits;
+        *scale_out = s;
+        *inv_out = __frcp_rn(s);
+    }
+
+    // ---- the staged slice, cast
+    __syncthreads();
+    for (int64_t j = v0 + t; j < v1; j += kSmallThreads) st_stream8(q + j, cast8<FMT>(stage[j - v0], s), stream);
+    cluster_wait();   // no CTA leaves while a peer may still read its maximum
+}
+
 std::atomic<int> g_grid[2][64];
+std::atomic<int> g_small[2][64];   // 0 = not asked yet, 1 = the cluster path runs, -1 = it does not
+
+// The small-tensor path; *launched says whether it ran.
+fp8lin_status launch_small(const uint4 *x, int64_t nvec, int f, float fmt_max, float *amax, float *scale,
+                           float *inv_scale, uint2 *q, cudaStream_t stream, int device, bool *launched) {
+    auto kernel = f == 0 ? quantize_cluster_kernel<FP8LIN_E4M3> : quantize_cluster_kernel<FP8LIN_E5M2>;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = kClusterCtas;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas);
+    cfg.blockDim = dim3(kSmallThreads);
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int ok = g_small[f][device].load(std::memory_order_acquire);
+    if (ok == 0) {
+        int clusters = 0;
+        cfg.dynamicSmemBytes = kSmallStageBytes;
+        cfg.stream = nullptr;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallStageBytes) != cudaSuccess)
+            return FP8LIN_ERR_CUDA;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            clusters = 0;
+        }
+        ok = clusters >= 1 ? 1 : -1;
+        g_small[f][device].store(ok, std::memory_order_release);
+        cfg.stream = stream;
+    }
+    if (ok < 0) return FP8LIN_OK;
+    const int64_t per = (nvec + kClusterCtas - 1) / kClusterCtas;
+    cfg.dynamicSmemBytes = (size_t)per * 16;
+    if (cudaLaunchKernelEx(&cfg, kernel, x, nvec, per, fmt_max, reinterpret_cast<unsigned int *>(amax), scale,
+                           inv_scale, q) != cudaSuccess)
+        return FP8LIN_ERR_CUDA;
+    *launched = true;
+    return fp8lin::check_launch();
+}
 
 }  // namespace
 
@@ -231,9 +368,14 @@ fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fm
         grid = (coop && per_sm >= 1) ? dev.sm_count : -1;   // one CTA per SM, all resident together
         g_grid[f][dev.device].store(grid, std::memory_order_release);
     }
-    if (grid < 0) return FP8LIN_OK;
     const int64_t nvec = n / 8;
     if (nvec == 0) return FP8LIN_OK;
+    if (nvec <= kSmallMaxVecs) {
+        st = launch_small(static_cast<const uint4 *>(x), nvec, f, fmt_max, amax, scale, inv_scale,
+                          reinterpret_cast<uint2 *>(q), stream, dev.device, launched);
+        if (st != FP8LIN_OK || *launched) return st;
+    }
+    if (grid < 0) return FP8LIN_OK;
     const int g = nvec < grid ? (int)nvec : grid;
     // the three slots start at zero: the count, the flag and the maximum
     if (scale == amax + 1 && inv_scale == amax + 2) {

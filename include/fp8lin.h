@@ -129,18 +129,22 @@ fp8lin_status fp8lin_cast_transpose(const void *x, int64_t rows, int64_t cols,
  * bit (TorchTitan analysis page, section 3.3: dynamic scaling takes the
  * tensor's own statistic every step; Lecture 9 exercises: one factor per
  * tensor).  For a cast that runs with no GEMM beside it -- the cast a GEMM
- * waits for.  With q and no qT (and fmt_max <= 65504) it is one cooperative
- * launch with one CTA on every SM: the grid reads x once for the amax,
- * keeping part of it in shared memory, meets at a grid barrier held in the
- * amax / scale / inverse-scale slots themselves (the call clears them
- * first; no other device memory is used), and casts.  Otherwise it is
+ * waits for.  With q and no qT (and fmt_max <= 65504) it is one launch.  Up
+ * to 786432 elements (1.5 MB of bf16) one cluster of 8 CTAs holds the whole
+ * tensor in shared memory, exchanges the CTAs' maxima through distributed
+ * shared memory at a cluster barrier, writes the three slots and casts;
+ * nothing is cleared first.  Larger tensors take a cooperative launch with
+ * one CTA on every SM: the grid reads x once for the amax, keeping part of
+ * it in shared memory, meets at a grid barrier held in the amax / scale /
+ * inverse-scale slots themselves (the call clears them first; no other
+ * device memory is used), and casts.  Otherwise it is
  * fp8lin_amax (with the tensor's last 64 MB kept in L2 for the cast) and
  * fp8lin_cast_transpose.  Beside a running GEMM, or for two casts at once on
  * two streams (each grid wants every SM), call fp8lin_amax and
  * fp8lin_cast_transpose instead.  A grid barrier that does not complete
  * within 2 s records FP8LIN_ERR_TIMEOUT for fp8lin_device_error.
  *
- *   amax       device, one float: receives max |x| (cleared by the call first).
+ *   amax       device, one float: receives max |x|.
  *   x, rows, cols, fmt, fmt_max, scale, inv_scale, q, qT as for
  *   fp8lin_cast_transpose; arguments are checked before anything is launched.
  */

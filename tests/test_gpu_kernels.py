@@ -333,6 +333,56 @@ def test_one_call_quantize_fmt_max_and_separate_slots(fp8lin, fmt_max):
     assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and q.intact()
 
 
+# 786432 elements (98304 16-byte vectors, 1.5 MB of bf16) is the largest
+# tensor the one-cluster path stages in shared memory; 784 x 1024 is the
+# whole-GPU grid's.
+@pytest.mark.parametrize("shape", [(16, 16), (32, 16), (16, 48), (768, 1024), (784, 1024)])
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_one_call_quantize_small_tensor_edges(fp8lin, shape, fmt):
+    """The one-cluster path of small tensors writes all three slots itself
+    (no clearing first): slots holding NaN or garbage beforehand, slices
+    that do not split evenly over the cluster's CTAs, the largest tensor it
+    takes and the smallest the grid takes, each bit-exact against the oracle
+    and against fp8lin_amax + fp8lin_cast_transpose."""
+    rows, cols = shape
+    x = wl.generate(shape, "laplace", 0.5, seed=rows + 7 * cols + fmt, tensor_id=3, outlier_frac=1e-3)
+    slots = torch.tensor([float("nan"), -1.0, 12345.0], device="cuda")
+    q = Guarded(shape, torch.uint8)
+    fp8lin.fp8lin_quantize(to_dev_bf16(x), fmt, slots[0:1], slots[1:2], slots[2:3], q.t, None)
+    a2, s2, i2, q2, _ = _run_cast(fp8lin, x, fmt, want_qT=False)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    ref = oracle.quantize(x, fmt)
+    assert scalar_bits(slots[0:1]) == f32_bits(ref["amax"]) == scalar_bits(a2)
+    assert scalar_bits(slots[1:2]) == f32_bits(ref["scale"]) == scalar_bits(s2)
+    assert scalar_bits(slots[2:3]) == f32_bits(ref["inv_scale"]) == scalar_bits(i2)
+    assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and torch.equal(q.t, q2.t) and q.intact()
+
+
+def test_one_call_quantize_small_zero_and_alternating_sizes(fp8lin):
+    """An all-zero small tensor publishes amax 0 and the floor scale; small
+    and large tensors alternating on the same slots (the grid path clears
+    them, the cluster path overwrites them) each match the oracle."""
+    slots = torch.full((3,), 9.0, device="cuda")
+    z = np.zeros((64, 128), dtype=np.uint16)
+    q = torch.empty((64, 128), dtype=torch.uint8, device="cuda")
+    fp8lin.fp8lin_quantize(to_dev_bf16(z), E4M3, slots[0:1], slots[1:2], slots[2:3], q, None)
+    torch.cuda.synchronize()
+    assert slots[0].item() == 0.0 and scalar_bits(slots[1:2]) == f32_bits(oracle.scale(np.float32(0.0))[0])
+    assert (q == 0).all()
+    for i, shape in enumerate([(128, 256), (2048, 1024), (256, 128), (1024, 2048), (16, 16)]):
+        x = wl.generate(shape, "normal", (1.0, 0.02, 3.0, 0.5, 7.0)[i], seed=90 + i, tensor_id=1)
+        q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+        fp8lin.fp8lin_quantize(to_dev_bf16(x), E4M3, slots[0:1], slots[1:2], slots[2:3], q, None)
+        torch.cuda.synchronize()
+        ref = oracle.quantize(x, E4M3)
+        assert scalar_bits(slots[0:1]) == f32_bits(ref["amax"])
+        assert scalar_bits(slots[1:2]) == f32_bits(ref["scale"])
+        assert scalar_bits(slots[2:3]) == f32_bits(ref["inv_scale"])
+        assert np.array_equal(q.cpu().numpy(), ref["q"])
+    assert fp8lin.fp8lin_device_error() == 0
+
+
 def test_one_call_quantize_repeated_and_empty(fp8lin):
     """Back-to-back calls reuse the same slots (each call clears them before
     its grid counts itself in); an empty matrix publishes the floor scale."""

@@ -149,13 +149,15 @@ def test_mx_cast_nan_blocks(fp8lin, fmt, rule):
 
 
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
-def test_one_call_quantize_with_nan(fp8lin, fmt):
+@pytest.mark.parametrize("shape", [(512, 384), (1024, 1024)])
+def test_one_call_quantize_with_nan(fp8lin, fmt, shape):
     """The one-launch dynamic cast (fp8lin_quantize, no transposed copy) on a
     tensor holding NaNs: amax, scale and inverse scale NaN exactly as the
-    oracle's, every code 0x7F."""
-    x = _nan_matrix(512, 384, 75)
+    oracle's, every code 0x7F.  512 x 384 takes the one-cluster path of small
+    tensors, 1024 x 1024 the whole-GPU grid."""
+    x = _nan_matrix(*shape, 75)
     slots = torch.zeros(3, device="cuda")
-    q = torch.empty((512, 384), dtype=torch.uint8, device="cuda")
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
     fp8lin.fp8lin_quantize(to_dev_bf16(x), fmt, slots[0:1], slots[1:2], slots[2:3], q, None)
     torch.cuda.synchronize()
     assert fp8lin.fp8lin_device_error() == 0
