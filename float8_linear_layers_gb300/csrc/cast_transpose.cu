@@ -14,8 +14,10 @@
 //    eight loads of a thread issued before any use), fp32 product with the
 //    scale, cvt.rn.satfinite into packed FP8 pairs; the row-major copy is
 //    stored straight from registers (8 bytes per thread, 128-byte rows);
-//    the bytes also go to a 16 KB shared tile whose 4-byte words are XOR
-//    swizzled by row group so that phase 2 reads are bank-conflict free;
+//    with a transposed copy the bytes also go to a 16 KB shared tile whose
+//    4-byte words are XOR swizzled by row group so that phase 2 reads are
+//    bank-conflict free (without one, the kernel is instantiated with no
+//    tile at all, so that two CTAs fit beside a GEMM CTA);
 //  * phase 2: each thread gathers a 16-row x 4-column block as 16 words,
 //    transposes 4 x 4 byte blocks with byte permutes and stores four 16-byte
 //    chunks of the transposed copy; eight lanes cover one 128-byte row of
