@@ -506,11 +506,20 @@ class StepGraph:
             # one stream; not the legacy default stream, so the step can be captured in a CUDA graph
             self.main = self.side = torch.cuda.Stream(device=dev)
         self._plan()
-        per_cast = 2 if scaling in ("dynamic", "rowwise") else 1   # block, mx and delayed: one kernel per cast
-        self.kernels_per_step = per_cast * len(self.t8) + len(spec.gemms)
+        self.kernels_per_step = sum(self._cast_kernels(key) for key in self.t8) + len(spec.gemms)
 
     def _plan(self):
         self.main_casts, self.side_casts, self.needed_by, self.beside = plan(self.spec, self.overlap)
+
+    def _cast_kernels(self, key) -> int:
+        """Kernels one cast of `key` launches: amax + cast for dynamic and
+        row-wise scaling, except a dynamic cast with nothing beside it and no
+        transposed copy, which is one launch (fp8lin_quantize); one for the
+        block, power-of-two block, delayed and static casts."""
+        alone = any(key in v for v in self.main_casts.values()) or any(key in v for v in self.beside.values())
+        if self.scaling == "dynamic":
+            return 1 if alone and self.t8[key].qT is None else 2
+        return 2 if self.scaling == "rowwise" else 1
 
     def describe(self):
         how = {"rowwise": "row-wise (per-block) scaling",
