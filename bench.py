@@ -506,20 +506,44 @@ class StepGraph:
             # one stream; not the legacy default stream, so the step can be captured in a CUDA graph
             self.main = self.side = torch.cuda.Stream(device=dev)
         self._plan()
-        self.kernels_per_step = sum(self._cast_kernels(key) for key in self.t8) + len(spec.gemms)
+        self.kernels_per_step = self._kernels_per_step()
 
     def _plan(self):
         self.main_casts, self.side_casts, self.needed_by, self.beside = plan(self.spec, self.overlap)
 
-    def _cast_kernels(self, key) -> int:
-        """Kernels one cast of `key` launches: amax + cast for dynamic and
-        row-wise scaling, except a dynamic cast with nothing beside it and no
-        transposed copy, which is one launch (fp8lin_quantize); one for the
-        block, power-of-two block, delayed and static casts."""
-        alone = any(key in v for v in self.main_casts.values()) or any(key in v for v in self.beside.values())
-        if self.scaling == "dynamic":
-            return 1 if alone and self.t8[key].qT is None else 2
-        return 2 if self.scaling == "rowwise" else 1
+    def _gate(self, i):
+        """The casts issued on the main stream right before GEMM i, split
+        into the dynamic casts without a transposed copy, which share
+        fp8lin_quantize_batch launches (one per format, at most four tensors
+        each), and the others."""
+        keys = (self.beside[i] if self.scaling == "dynamic" else []) + self.main_casts[i]
+        batch = [k for k in keys if self.scaling == "dynamic" and self.t8[k].qT is None]
+        return batch, [k for k in keys if k not in batch]
+
+    def _kernels_per_step(self) -> int:
+        """Kernels one step launches: the GEMMs; one per batched launch of
+        gating casts; amax + cast for any other dynamic or row-wise cast; one
+        for each block, power-of-two block, delayed and static cast."""
+        per_cast = 2 if self.scaling in ("dynamic", "rowwise") else 1
+        n = len(self.spec.gemms) + per_cast * sum(len(v) for v in self.side_casts.values())
+        if self.scaling != "dynamic":
+            n += per_cast * sum(len(v) for v in self.beside.values())
+        for i in range(len(self.spec.gemms)):
+            batch, rest = self._gate(i)
+            fmts = {}
+            for k in batch:
+                fmts[(self.t8[k].fmt, self.t8[k].fmt_max)] = fmts.get((self.t8[k].fmt, self.t8[k].fmt_max), 0) + 1
+            n += sum(-(-c // self.fl.MAX_QUANTIZE_BATCH) for c in fmts.values()) + per_cast * len(rest)
+        return n
+
+    def _cast_alone(self, rec, keys_batch, keys_rest, stream):
+        for key in keys_rest:
+            self._cast(rec, key, stream, alone=True)
+        if keys_batch:
+            # amax read, cast read and the FP8 copy: 5 B per element
+            work = sum(5 * self.inp[k].numel() for k in keys_batch)
+            self._mark(stream, rec, "quantize", "+".join(keys_batch), work, lambda: self.fl.quantize_alone(
+                [(self.t8[k], self.inp[k]) for k in keys_batch], stream))
 
     def describe(self):
         how = {"rowwise": "row-wise (per-block) scaling",
@@ -627,12 +651,7 @@ class StepGraph:
         m, s = self.main, self.side
         ready = {}
         for i, (name, which) in enumerate(self.spec.gemms):
-            if self.beside[i] and self.scaling == "dynamic":
-                # the one-launch dynamic cast occupies every SM: the casts
-                # gating this GEMM run one after another on the main stream
-                for key in self.beside[i]:
-                    self._cast(rec, key, m, alone=True)
-            elif self.beside[i]:
+            if self.beside[i] and self.scaling != "dynamic":
                 marker = self.t.cuda.Event()
                 marker.record(m)                      # the casts gating GEMM i start together
                 s.wait_event(marker)
@@ -641,8 +660,9 @@ class StepGraph:
                     e = self.t.cuda.Event()
                     e.record(s)
                     ready[key] = e
-            for key in self.main_casts[i]:
-                self._cast(rec, key, m, alone=True)
+            # the one-launch dynamic cast occupies every SM: the casts gating
+            # this GEMM run on the main stream, in one launch where they can
+            self._cast_alone(rec, *self._gate(i), m)
             if self.side_casts[i]:
                 marker = self.t.cuda.Event()
                 marker.record(m)                      # this GEMM is about to launch

@@ -41,7 +41,8 @@ _STATUS = {0: "FP8LIN_OK", 1: "FP8LIN_ERR_INVALID_ARG", 2: "FP8LIN_ERR_MISALIGNE
            6: "FP8LIN_ERR_UNSUPPORTED_DEVICE"}
 
 # Every entry point declared in include/fp8lin.h.
-ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_quantize", "fp8lin_cast_transpose_static",
+ENTRY_POINTS = ("fp8lin_amax", "fp8lin_cast_transpose", "fp8lin_quantize", "fp8lin_quantize_batch",
+                "fp8lin_cast_transpose_static",
                 "fp8lin_cast_transpose_delayed", "fp8lin_amax_rowcol", "fp8lin_cast_transpose_rowwise",
                 "fp8lin_fwd", "fp8lin_dgrad", "fp8lin_wgrad", "fp8lin_dgrad_mn", "fp8lin_wgrad_mn",
                 "fp8lin_cast_blockwise", "fp8lin_fwd_block", "fp8lin_dgrad_block", "fp8lin_wgrad_block",
@@ -82,6 +83,7 @@ SIGNATURES = {
     "fp8lin_amax": [_vp, _i64, _vp, _vp],
     "fp8lin_cast_transpose": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_quantize": [_vp, _i64, _i64, _ci, _f32, _vp, _vp, _vp, _vp, _vp, _vp],
+    "fp8lin_quantize_batch": [_vp, _ci, _ci, _f32, _vp],
     "fp8lin_cast_transpose_static": [_vp, _i64, _i64, _ci, _vp, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_cast_transpose_delayed": [_vp, _i64, _i64, _ci, _f32, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp],
     "fp8lin_amax_rowcol": [_vp, _i64, _i64, _vp, _vp, _vp],
@@ -187,6 +189,38 @@ def fp8lin_quantize(x: torch.Tensor, fmt: int, amax: torch.Tensor, scale: torch.
     _check("fp8lin_quantize",
            _lib.fp8lin_quantize(_ptr(x), rows, cols, int(fmt), float(fmt_max), _ptr(amax), _ptr(scale),
                                 _ptr(inv_scale), _ptr(q), _ptr(qT), _stream(stream)))
+
+
+MAX_QUANTIZE_BATCH = 4   # FP8LIN_MAX_QUANTIZE_BATCH
+
+
+class _QuantizeItem(ctypes.Structure):
+    """fp8lin_quantize_item of include/fp8lin.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("amax", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("inv_scale", ctypes.c_void_p),
+                ("q", ctypes.c_void_p)]
+
+
+def fp8lin_quantize_batch(items, fmt: int, fmt_max: float = FMT_MAX, stream=None) -> None:
+    """fp8lin_quantize for up to MAX_QUANTIZE_BATCH tensors of one format in
+    one launch; items: (x, amax, scale, inv_scale, q) per tensor, each with
+    slots of its own."""
+    items = list(items)
+    if not 1 <= len(items) <= MAX_QUANTIZE_BATCH:
+        raise ValueError(f"1 to {MAX_QUANTIZE_BATCH} tensors per call")
+    arr = (_QuantizeItem * len(items))()
+    for k, (x, amax, scale, inv_scale, q) in enumerate(items):
+        _dev(x, "x", torch.bfloat16)
+        if x.dim() != 2:
+            raise ValueError("x must be a 2-D [rows x cols] matrix")
+        for t, n in ((amax, "amax"), (scale, "scale"), (inv_scale, "inv_scale")):
+            _dev(t, n, torch.float32)
+        _dev(q, "q")
+        if q is not None and tuple(q.shape) != tuple(x.shape):
+            raise ValueError("q must have x's shape")
+        arr[k] = _QuantizeItem(_ptr(x), x.shape[0], x.shape[1], _ptr(amax), _ptr(scale), _ptr(inv_scale), _ptr(q))
+    _check("fp8lin_quantize_batch", _lib.fp8lin_quantize_batch(ctypes.addressof(arr), len(items), int(fmt),
+                                                               float(fmt_max), _stream(stream)))
 
 
 def fp8lin_cast_transpose_static(x: torch.Tensor, fmt: int, scale: torch.Tensor, inv_scale: torch.Tensor,
@@ -597,6 +631,23 @@ class Float8Tensor:
         return self
 
 
+def quantize_alone(pairs, stream=None) -> None:
+    """Cast each (Float8Tensor, x) of `pairs` with nothing running beside the
+    casts.  The dynamic casts without a transposed copy, grouped by format,
+    share one fp8lin_quantize_batch launch; every other cast runs on its own."""
+    groups = {}
+    for t8, x in pairs:
+        if t8.scaling == "dynamic" and t8.qT is None:
+            groups.setdefault((t8.fmt, t8.fmt_max), []).append((t8, x))
+        else:
+            t8.quantize(x, stream, alone=True)
+    for (fmt, fmt_max), members in groups.items():
+        for i in range(0, len(members), MAX_QUANTIZE_BATCH):
+            chunk = members[i:i + MAX_QUANTIZE_BATCH]
+            fp8lin_quantize_batch([(x, t8.amax, t8.scale, t8.inv_scale, t8.q) for t8, x in chunk], fmt, fmt_max,
+                                  stream)
+
+
 class Float8Linear:
     """The nine calls of one Float8 linear's forward and backward pass, on
     caller-owned bf16 X [M x K], W [N x K], dY [M x N].  Buffers for the FP8
@@ -629,9 +680,9 @@ class Float8Linear:
         return 6 * self.M * self.N * self.K
 
     def forward(self, x: torch.Tensor, w: torch.Tensor, stream=None) -> torch.Tensor:
-        # the step runs on one stream: every cast has nothing beside it
-        self.x8.quantize(x, stream, alone=True)
-        self.w8.quantize(w, stream, alone=True)
+        # the step runs on one stream: nothing runs beside the casts, and
+        # X's and W's share one launch where they can
+        quantize_alone([(self.x8, x), (self.w8, w)], stream)
         if self.x8.scaling == "mx":
             fp8lin_fwd_mx(self.x8.q, self.x8.sf_row, self.w8.q, self.w8.sf_row, self.y, stream)
         elif self.x8.scaling == "block":
@@ -667,7 +718,7 @@ class Float8Linear:
         return self.y, self.dx, self.dw
 
     # kernels one dynamic step launches at most (amax x3, cast x3, three GEMMs;
-    # fewer where a cast takes the one-launch path of fp8lin_quantize)
+    # fewer where casts take the one-launch path: X and W together, then dY)
     KERNELS_PER_STEP = 9
 
 

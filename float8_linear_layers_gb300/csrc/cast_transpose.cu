@@ -961,13 +961,58 @@ extern "C" fp8lin_status fp8lin_quantize(const void *x, int64_t rows, int64_t co
     if (!dim_ok(rows) || !dim_ok(cols) || rows % 16 || cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
     if (q != nullptr && qT == nullptr && !empty) {
         bool launched = false;
-        fp8lin_status st = launch_quantize(x, rows * cols, fmt, fmt_max, amax, scale, inv_scale, q, stream, &launched);
+        const QuantizeItem item{x, rows * cols, amax, scale, inv_scale, q};
+        fp8lin_status st = launch_quantize_batch(&item, 1, fmt, fmt_max, stream, &launched);
         if (st != FP8LIN_OK || launched) return st;
     }
     fp8lin_status st = launch_amax(x, rows * cols, amax, stream, true);
     if (st != FP8LIN_OK) return st;
     return cast_common(kDynamic, x, rows, cols, fmt, fmt_max, amax, 0, 0, scale, inv_scale, q, qT, nullptr,
                        stream);
+}
+
+extern "C" fp8lin_status fp8lin_quantize_batch(const fp8lin_quantize_item *items, int count, fp8lin_fmt fmt,
+                                               float fmt_max, cudaStream_t stream) {
+    using namespace fp8lin;
+    if (items == nullptr || count < 1 || count > FP8LIN_MAX_QUANTIZE_BATCH) return FP8LIN_ERR_INVALID_ARG;
+    if (fmt != FP8LIN_E4M3 && fmt != FP8LIN_E5M2) return FP8LIN_ERR_INVALID_ARG;
+    if (!(fmt_max > 0.0f) || !(fmt_max <= 3.4e38f)) return FP8LIN_ERR_INVALID_ARG;
+    // every item's checks first, so that nothing is launched for a bad argument
+    QuantizeItem qi[FP8LIN_MAX_QUANTIZE_BATCH];
+    for (int k = 0; k < count; ++k) {
+        const fp8lin_quantize_item &it = items[k];
+        if (it.amax == nullptr || it.scale == nullptr || it.inv_scale == nullptr) return FP8LIN_ERR_INVALID_ARG;
+        if (it.rows < 0 || it.cols < 0) return FP8LIN_ERR_INVALID_ARG;
+        const bool empty = it.rows == 0 || it.cols == 0;
+        if (!empty && (it.x == nullptr || it.q == nullptr)) return FP8LIN_ERR_INVALID_ARG;
+        if (!aligned(it.amax, 4) || !aligned(it.scale, 4) || !aligned(it.inv_scale, 4)) return FP8LIN_ERR_MISALIGNED;
+        if (!empty && (!aligned(it.x, 16) || !aligned(it.q, 16))) return FP8LIN_ERR_MISALIGNED;
+        if (!dim_ok(it.rows) || !dim_ok(it.cols) || it.rows % 16 || it.cols % 16) return FP8LIN_ERR_UNSUPPORTED_SHAPE;
+        // each tensor needs slots of its own: the launch counts and waits on the first tensor's
+        const float *mine[3] = {it.amax, it.scale, it.inv_scale};
+        for (int a = 0; a < 3; ++a)
+            for (int c = a + 1; c < 3; ++c)
+                if (mine[a] == mine[c]) return FP8LIN_ERR_INVALID_ARG;
+        for (int j = 0; j < k; ++j) {
+            const float *theirs[3] = {items[j].amax, items[j].scale, items[j].inv_scale};
+            for (int a = 0; a < 3; ++a)
+                for (int c = 0; c < 3; ++c)
+                    if (mine[a] == theirs[c]) return FP8LIN_ERR_INVALID_ARG;
+        }
+        qi[k] = QuantizeItem{it.x, it.rows * it.cols, it.amax, it.scale, it.inv_scale, it.q};
+    }
+    bool launched = false;
+    fp8lin_status st = launch_quantize_batch(qi, count, fmt, fmt_max, stream, &launched);
+    if (st != FP8LIN_OK || launched) return st;
+    for (int k = 0; k < count; ++k) {   // one tensor at a time: amax, then cast
+        const fp8lin_quantize_item &it = items[k];
+        st = launch_amax(it.x, it.rows * it.cols, it.amax, stream, true);
+        if (st == FP8LIN_OK)
+            st = cast_common(kDynamic, it.x, it.rows, it.cols, fmt, fmt_max, it.amax, 0, 0, it.scale, it.inv_scale,
+                             it.q, nullptr, nullptr, stream);
+        if (st != FP8LIN_OK) return st;
+    }
+    return FP8LIN_OK;
 }
 
 extern "C" fp8lin_status fp8lin_cast_transpose_static(const void *x, int64_t rows, int64_t cols, fp8lin_fmt fmt,

@@ -40,13 +40,22 @@ fp8lin_status prefer_max_shared_carveout(const void *kernel, int device, int slo
 // are checked by the caller.
 fp8lin_status launch_amax(const void *x, int64_t n, float *amax, cudaStream_t stream, bool alone);
 
-// Dynamic per-tensor scaling of n bf16 values into the row-major copy q in
-// one cooperative launch (quantize.cu); *launched says whether it ran (it
-// declines fmt_max above 65504 and devices without cooperative launch, and
-// the caller then takes the two-kernel path).  Arguments are checked by the
-// caller.
-fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fmt_max, float *amax, float *scale,
-                              float *inv_scale, uint8_t *q, cudaStream_t stream, bool *launched);
+// One tensor of a one-launch dynamic cast: n bf16 values, its own amax,
+// scale and inverse-scale slots and its row-major FP8 copy.
+struct QuantizeItem {
+    const void *x;
+    int64_t n;
+    float *amax, *scale, *inv_scale;
+    uint8_t *q;
+};
+
+// Dynamic per-tensor scaling of `count` tensors (1 .. FP8LIN_MAX_QUANTIZE_BATCH,
+// one format) in one launch (quantize.cu); *launched says whether it ran (it
+// declines fmt_max above 65504, tensors with nothing to read and devices
+// without cooperative launch, and the caller then takes the two-kernel path
+// per tensor).  Arguments are checked by the caller.
+fp8lin_status launch_quantize_batch(const QuantizeItem *items, int count, fp8lin_fmt fmt, float fmt_max,
+                                    cudaStream_t stream, bool *launched);
 
 // Read and clear the device word in which quantize.cu's kernel records a
 // bounded wait that ran out.

@@ -1,33 +1,40 @@
-// quantize.cu -- dynamic per-tensor scaling of one bf16 tensor in one launch:
+// quantize.cu -- dynamic per-tensor scaling of bf16 tensors in one launch:
 // amax, scale and the saturating round-to-nearest-even cast to the row-major
 // FP8 copy (TorchTitan analysis page, section 3.3, "Mixed precision and
 // Float8": dynamic scaling takes the tensor's own statistic every step;
-// Lecture 9 exercises: one factor per tensor).  For the cast a GEMM waits
-// for, which runs with nothing beside it.
+// Lecture 9 exercises: one factor per tensor).  For the casts a GEMM waits
+// for, which run with nothing beside them.  One launch takes up to
+// kMaxBatch tensors of one format (the X and W of a forward pass), each
+// with its own amax, scale and inverse-scale slots and its own scale.
 //
-// HBM-bound: the two-kernel path (amax, then cast) reads the tensor twice.
-// Here one persistent cooperative grid, one CTA per SM, reads it once for
-// the amax while keeping the last part of each CTA's slice in shared memory,
-// meets at a grid barrier, then casts the staged part from shared memory and
-// the rest of the slice last-read-first (so what L2 still holds is read
-// before it is evicted).  Element i of x becomes byte i of q, so a CTA's
-// slice is a contiguous range of 16-byte vectors (8 elements).
+// HBM-bound: the two-kernel path (amax, then cast) reads a tensor twice.
+// Here one persistent cooperative grid, one CTA per SM, reads the tensors
+// once for their amax while keeping the last part of each CTA's slice in
+// shared memory, meets at a grid barrier, then casts the staged part from
+// shared memory and the rest of the slice last-read-first (so what L2 still
+// holds is read before it is evicted).  The tensors are laid end to end as
+// one range of 16-byte vectors (8 elements); element i of a tensor becomes
+// byte i of its copy, and a CTA's slice is a contiguous part of that range,
+// cut where it crosses from one tensor to the next.
 //
 // The grid barrier uses the call's own output slots, so the kernel needs no
-// memory beyond its inputs and outputs: all three slots are zero when it
-// starts (the host clears them on the stream); every CTA publishes its
-// maximum with atomicMax on the amax slot and then counts itself in on the
-// scale slot (atomicAdd on its bits); the CTA that arrives last reads the
-// amax, overwrites the count with the scale and publishes 1 / scale to the
-// inverse-scale slot with release semantics; the others wait (acquire, at
-// most kWaitLimitNs) until that slot is nonzero.  1 / scale is never zero:
-// scale = fmt_max / max(amax, 1e-12) is finite for fmt_max <= 65504 (the
-// host checks it), and a NaN or infinite amax gives a NaN or infinite
-// inverse.  A wait that runs out records FP8LIN_ERR_TIMEOUT in this file's
-// device error word (read by fp8lin_device_error) and the CTA skips its cast.
+// memory beyond its inputs and outputs: every slot is zero when it starts
+// (the host clears them on the stream); every CTA publishes each tensor's
+// maximum over its slice with atomicMax on that tensor's amax slot and then
+// counts itself in on the first tensor's scale slot (atomicAdd on its
+// bits); the CTA that arrives last reads the maxima, writes every other
+// tensor's scale and inverse scale, overwrites the count with the first
+// tensor's scale and publishes the first tensor's 1 / scale with release
+// semantics; the others wait (acquire, at most kWaitLimitNs) until that slot
+// is nonzero, then read the scales.  1 / scale is never zero: scale =
+// fmt_max / max(amax, 1e-12) is finite for fmt_max <= 65504 (the host checks
+// it), and a NaN or infinite amax gives a NaN or infinite inverse.  A wait
+// that runs out records FP8LIN_ERR_TIMEOUT in this file's device error word
+// (read by fp8lin_device_error) and the CTA skips its cast.
 //
-// A tensor of at most 1.5 MB takes quantize_cluster_kernel instead (further
-// down): one cluster of eight CTAs, no grid barrier and no clearing launch.
+// Tensors of at most 1.5 MB in all take quantize_cluster_kernel instead
+// (further down): one cluster of eight CTAs, no grid barrier and no
+// clearing launch.
 #include <atomic>
 #include <cstdint>
 
@@ -43,6 +50,7 @@ constexpr int kUnroll = 8;                       // 16-byte loads in flight per 
 constexpr int kStageBytes = FP8LIN_QUANTIZE_STAGE_KB * 1024;   // slice tail kept in shared memory
 constexpr int kStageVecs = kStageBytes / 16;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr int kMaxBatch = FP8LIN_MAX_QUANTIZE_BATCH;
 
 __device__ unsigned int g_quantize_error = 0;
 
@@ -103,16 +111,72 @@ __device__ __forceinline__ uint2 cast8(uint4 v, float s) {
     return r;
 }
 
+// The tensors of one launch, end to end: tensor k holds vectors
+// [begin(k), end[k]) of the range.
+struct QBatch {
+    const uint4 *x[kMaxBatch];
+    uint2 *q[kMaxBatch];
+    unsigned int *amax[kMaxBatch];
+    float *scale[kMaxBatch];
+    float *inv[kMaxBatch];
+    int64_t end[kMaxBatch];
+    int count;
+    __device__ __forceinline__ int64_t begin(int k) const { return k == 0 ? 0 : end[k - 1]; }
+};
+
+// Maximum |x| (two packed 16-bit magnitudes) of vectors [lo, hi) of x, one
+// thread's share: kUnroll loads in flight.
+__device__ __forceinline__ uint32_t stream_max(const uint4 *__restrict__ x, int64_t lo, int64_t hi, int t,
+                                               int threads, uint64_t policy) {
+    uint32_t m = 0;
+    int64_t i = lo + t;
+    for (; i + (int64_t)(kUnroll - 1) * threads < hi; i += (int64_t)kUnroll * threads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld16(x + i + (int64_t)u * threads, policy);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) m = absmax8(m, v[u]);
+    }
+    for (; i < hi; i += threads) m = absmax8(m, ld16(x + i, policy));
+    return m;
+}
+
+// The same over [lo, hi), each vector also stored to stage[j - stage0].
+__device__ __forceinline__ uint32_t stage_max(const uint4 *__restrict__ x, int64_t lo, int64_t hi, int t,
+                                              int threads, uint64_t policy, uint4 *stage, int64_t stage0) {
+    uint32_t m = 0;
+    for (int64_t j = lo + t; j < hi; j += (int64_t)kUnroll * threads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (j + (int64_t)u * threads < hi) v[u] = ld16(x + j + (int64_t)u * threads, policy);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (j + (int64_t)u * threads < hi) {
+                stage[j + (int64_t)u * threads - stage0] = v[u];
+                m = absmax8(m, v[u]);
+            }
+    }
+    return m;
+}
+
+// fmt_max / max(amax, 1e-12) in binary32, from the amax slot's bits.
+__device__ __forceinline__ float scale_of(unsigned int amax_bits, float fmt_max) {
+    float a = __uint_as_float(amax_bits);
+    a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
+    return __fdiv_rn(fmt_max, a);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
-quantize_kernel(const uint4 *__restrict__ x, int64_t nvec, float fmt_max, unsigned int *amax_bits,
-                unsigned int *arrivals, float *scale_out, float *inv_out, uint2 *__restrict__ q) {
+quantize_kernel(const QBatch b, float fmt_max) {
     extern __shared__ uint4 stage[];
-    __shared__ uint32_t warp_max[kThreads / 32];
-    __shared__ float s_shared;
+    __shared__ uint32_t warp_max[kMaxBatch][kThreads / 32];
+    __shared__ float s_shared[kMaxBatch];
     __shared__ int go;
 
     const int t = threadIdx.x;
+    const int64_t nvec = b.end[b.count - 1];
     const int64_t per = (nvec + gridDim.x - 1) / gridDim.x;
     const int64_t v0 = min((int64_t)blockIdx.x * per, nvec);
     const int64_t v1 = min(v0 + per, nvec);
@@ -121,56 +185,57 @@ quantize_kernel(const uint4 *__restrict__ x, int64_t nvec, float fmt_max, unsign
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(normal));
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
 
-    // ---- phase 1: amax of the slice; its tail into shared memory
-    uint32_t m = 0;
-    int64_t i = v0 + t;
-    for (; i + (int64_t)(kUnroll - 1) * kThreads < s0; i += (int64_t)kUnroll * kThreads) {
-        uint4 v[kUnroll];
+    // ---- phase 1: each tensor's amax over the slice; the slice's tail into shared memory
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld16(x + i + (int64_t)u * kThreads, normal);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) m = absmax8(m, v[u]);
+    for (int k = 0; k < kMaxBatch; ++k) {
+        if (k >= b.count) break;
+        const int64_t beg = b.begin(k), end = b.end[k];
+        const uint4 *x = b.x[k] - beg;   // indexed by position in the whole range
+        uint32_t m = 0;
+        if (max(v0, beg) < min(s0, end)) m = stream_max(x, max(v0, beg), min(s0, end), t, kThreads, normal);
+        if (max(s0, beg) < min(v1, end))   // packed maxima: combined lane by lane
+            m = __vmaxu2(m, stage_max(x, max(s0, beg), min(v1, end), t, kThreads, stream, stage, s0));
+        // packed maxima compare lane-wise; fold the two halves, then the warp
+        const uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+        if (t % 32 == 0) warp_max[k][t / 32] = r;
     }
-    for (; i < s0; i += kThreads) m = absmax8(m, ld16(x + i, normal));
-    for (int64_t j = s0 + t; j < v1; j += (int64_t)kUnroll * kThreads) {
-        uint4 v[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (j + (int64_t)u * kThreads < v1) v[u] = ld16(x + j + (int64_t)u * kThreads, stream);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (j + (int64_t)u * kThreads < v1) {
-                stage[j + (int64_t)u * kThreads - s0] = v[u];
-                m = absmax8(m, v[u]);
-            }
-    }
-    uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
-    if (t % 32 == 0) warp_max[t / 32] = r;
     __syncthreads();
 
     // ---- grid barrier on the output slots (see the file comment)
     if (t < 32) {
-        r = __reduce_max_sync(0xFFFFFFFFu, t < kThreads / 32 ? warp_max[t] : 0u);
+        uint32_t r[kMaxBatch];
+#pragma unroll
+        for (int k = 0; k < kMaxBatch; ++k)
+            r[k] = __reduce_max_sync(0xFFFFFFFFu, (k < b.count && t < kThreads / 32) ? warp_max[k][t] : 0u);
         if (t == 0) {
-            if (r != 0) atomicMax(amax_bits, r << 16);
+#pragma unroll
+            for (int k = 0; k < kMaxBatch; ++k)
+                if (k < b.count && r[k] != 0) atomicMax(b.amax[k], r[k] << 16);
             __threadfence();
+            unsigned int *arrivals = reinterpret_cast<unsigned int *>(b.scale[0]);
             const unsigned int before = atomicAdd(arrivals, 1u);
             int arrived = 1;
-            float s;
             if (before == gridDim.x - 1) {
                 __threadfence();
-                float a = __uint_as_float(atomicOr(amax_bits, 0u));
-                a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
-                s = __fdiv_rn(fmt_max, a);
-                *scale_out = s;                 // the count is complete: the slot takes the scale
+#pragma unroll
+                for (int k = kMaxBatch - 1; k >= 1; --k) {
+                    if (k >= b.count) continue;
+                    const float s = scale_of(atomicOr(b.amax[k], 0u), fmt_max);
+                    *b.scale[k] = s;
+                    *b.inv[k] = __frcp_rn(s);
+                    s_shared[k] = s;
+                }
+                const float s = scale_of(atomicOr(b.amax[0], 0u), fmt_max);
+                *b.scale[0] = s;                // the count is complete: the slot takes the scale
+                s_shared[0] = s;
                 __threadfence();
-                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(inv_out), "r"(__float_as_uint(__frcp_rn(s)))
+                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(b.inv[0]), "r"(__float_as_uint(__frcp_rn(s)))
                              : "memory");
             } else {
                 const unsigned long long t0 = globaltimer();
                 uint32_t flag = 0;
                 while (true) {
-                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(flag) : "l"(inv_out) : "memory");
+                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(flag) : "l"(b.inv[0]) : "memory");
                     if (flag != 0) break;
                     if (globaltimer() - t0 > kWaitLimitNs) {
                         atomicOr(&g_quantize_error, 1u << FP8LIN_ERR_TIMEOUT);
@@ -178,44 +243,62 @@ quantize_kernel(const uint4 *__restrict__ x, int64_t nvec, float fmt_max, unsign
                         break;
                     }
                 }
-                s = arrived ? *reinterpret_cast<volatile float *>(scale_out) : 0.0f;
+#pragma unroll
+                for (int k = 0; k < kMaxBatch; ++k)
+                    if (k < b.count) s_shared[k] = arrived ? *reinterpret_cast<volatile float *>(b.scale[k]) : 0.0f;
             }
-            s_shared = s;
             go = arrived;
         }
     }
     __syncthreads();
     if (!go) return;
-    const float s = s_shared;
 
     // ---- phase 2: the staged tail from shared memory, then the rest of the
     // slice last-read-first
-    for (int64_t j = s0 + t; j < v1; j += kThreads) st_stream8(q + j, cast8<FMT>(stage[j - s0], s), stream);
-    const int64_t n_rest = s0 - v0;
-    int64_t k = t;
-    for (; k + (int64_t)(kUnroll - 1) * kThreads < n_rest; k += (int64_t)kUnroll * kThreads) {
-        uint4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld16(x + (s0 - 1 - k - (int64_t)u * kThreads), stream);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            st_stream8(q + (s0 - 1 - k - (int64_t)u * kThreads), cast8<FMT>(v[u], s), stream);
+    for (int k = 0; k < kMaxBatch; ++k) {
+        if (k >= b.count) break;
+        const int64_t beg = b.begin(k), lo = max(s0, beg), hi = min(v1, b.end[k]);
+        const float s = s_shared[k];
+        uint2 *q = b.q[k] - beg;
+        for (int64_t j = lo + t; j < hi; j += kThreads) st_stream8(q + j, cast8<FMT>(stage[j - s0], s), stream);
     }
-    for (; k < n_rest; k += kThreads) {
-        const int64_t idx = s0 - 1 - k;
-        st_stream8(q + idx, cast8<FMT>(ld16(x + idx, stream), s), stream);
+#pragma unroll
+    for (int kk = 0; kk < kMaxBatch; ++kk) {
+        const int k = kMaxBatch - 1 - kk;
+        if (k >= b.count) continue;
+        const int64_t beg = b.begin(k), lo = max(v0, beg), hi = min(s0, b.end[k]);
+        if (lo >= hi) continue;
+        const float s = s_shared[k];
+        const uint4 *x = b.x[k] - beg;
+        uint2 *q = b.q[k] - beg;
+        const int64_t n_rest = hi - lo;
+        int64_t i = t;
+        for (; i + (int64_t)(kUnroll - 1) * kThreads < n_rest; i += (int64_t)kUnroll * kThreads) {
+            uint4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) v[u] = ld16(x + (hi - 1 - i - (int64_t)u * kThreads), stream);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                st_stream8(q + (hi - 1 - i - (int64_t)u * kThreads), cast8<FMT>(v[u], s), stream);
+        }
+        for (; i < n_rest; i += kThreads) {
+            const int64_t idx = hi - 1 - i;
+            st_stream8(q + idx, cast8<FMT>(ld16(x + idx, stream), s), stream);
+        }
     }
 }
 
-// Small tensors (up to kSmallMaxVecs vectors, 1.5 MB of bf16): one cluster
-// of kClusterCtas CTAs stages the whole tensor in shared memory, each CTA a
-// contiguous slice.  The CTAs meet at a hardware cluster barrier, read the
-// other CTAs' maxima from their shared memory (distributed shared memory),
-// derive the same scale, and cast their staged slice.  The slots need no
-// clearing and no global memory holds a partial result, so the launch needs
-// no memset, and no wait is a spin: the barrier is the cluster's own, whose
-// CTAs are resident together by construction.  A second barrier keeps every
-// CTA resident until its peers have read its maximum.
+// Small batches (up to kSmallMaxVecs vectors in all, 1.5 MB of bf16): one
+// cluster of kClusterCtas CTAs stages the whole range in shared memory, each
+// CTA a contiguous slice.  The CTAs meet at a hardware cluster barrier, read
+// the other CTAs' maxima from their shared memory (distributed shared
+// memory), derive the same scales, and cast their staged slice.  The slots
+// need no clearing and no global memory holds a partial result, so the
+// launch needs no memset, and no wait is a spin: the barrier is the
+// cluster's own, whose CTAs are resident together by construction.  A
+// second barrier keeps every CTA resident until its peers have read its
+// maxima.
 constexpr int kClusterCtas = 8;
 constexpr int kSmallThreads = 512;
 constexpr int kSmallStageBytes = 192 * 1024;
@@ -242,70 +325,73 @@ __device__ __forceinline__ uint32_t ld_peer_u32(const uint32_t *local, uint32_t 
 
 template <int FMT>
 __global__ void __launch_bounds__(kSmallThreads, 1)
-quantize_cluster_kernel(const uint4 *__restrict__ x, int64_t nvec, int64_t per, float fmt_max,
-                        unsigned int *amax_out, float *scale_out, float *inv_out, uint2 *__restrict__ q) {
+quantize_cluster_kernel(const QBatch b, int64_t per, float fmt_max) {
     extern __shared__ uint4 stage[];
-    __shared__ uint32_t warp_max[kSmallThreads / 32];
-    __shared__ uint32_t cta_max;
+    __shared__ uint32_t warp_max[kMaxBatch][kSmallThreads / 32];
+    __shared__ uint32_t cta_max[kMaxBatch];
 
     const int t = threadIdx.x;
     const uint32_t rank = cluster_rank();
+    const int64_t nvec = b.end[b.count - 1];
     const int64_t v0 = min((int64_t)rank * per, nvec);
     const int64_t v1 = min(v0 + per, nvec);
     uint64_t stream;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
 
-    // ---- the slice into shared memory, and its maximum |x|
-    uint32_t m = 0;
-    for (int64_t j = v0 + t; j < v1; j += (int64_t)kUnroll * kSmallThreads) {
-        uint4 v[kUnroll];
+    // ---- the slice into shared memory, and each tensor's maximum |x| over it
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (j + (int64_t)u * kSmallThreads < v1) v[u] = ld16(x + j + (int64_t)u * kSmallThreads, stream);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (j + (int64_t)u * kSmallThreads < v1) {
-                stage[j + (int64_t)u * kSmallThreads - v0] = v[u];
-                m = absmax8(m, v[u]);
-            }
+    for (int k = 0; k < kMaxBatch; ++k) {
+        if (k >= b.count) break;
+        const int64_t beg = b.begin(k), lo = max(v0, beg), hi = min(v1, b.end[k]);
+        const uint32_t m = lo < hi ? stage_max(b.x[k] - beg, lo, hi, t, kSmallThreads, stream, stage, v0) : 0u;
+        const uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+        if (t % 32 == 0) warp_max[k][t / 32] = r;
     }
-    uint32_t r = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
-    if (t % 32 == 0) warp_max[t / 32] = r;
     __syncthreads();
     if (t < 32) {
-        r = __reduce_max_sync(0xFFFFFFFFu, t < kSmallThreads / 32 ? warp_max[t] : 0u);
-        if (t == 0) cta_max = r;
+#pragma unroll
+        for (int k = 0; k < kMaxBatch; ++k) {
+            const uint32_t r =
+                __reduce_max_sync(0xFFFFFFFFu, (k < b.count && t < kSmallThreads / 32) ? warp_max[k][t] : 0u);
+            if (t == 0) cta_max[k] = r;
+        }
     }
     cluster_arrive();
-    cluster_wait();   // every CTA's maximum is in its shared memory
+    cluster_wait();   // every CTA's maxima are in its shared memory
 
-    // ---- the tensor's maximum from every CTA's (each warp reads them), the scale
+    // ---- each tensor's maximum from every CTA's (each warp reads them), its scale
     const int lane = t % 32;
-    r = lane < kClusterCtas ? ld_peer_u32(&cta_max, (uint32_t)lane) : 0u;
-    r = __reduce_max_sync(0xFFFFFFFFu, r);
-    cluster_arrive();   // this CTA is done reading its peers' shared memory
-    const uint32_t amax_bits = r << 16;
-    float a = __uint_as_float(amax_bits);
-    a = (a < 1e-12f) ? 1e-12f : a;  // a NaN amax stays NaN
-    const float s = __fdiv_rn(fmt_max, a);
-    if (rank == 0 && t == 0) {
-        *amax_out = amax_bits;
-        *scale_out = s;
-        *inv_out = __frcp_rn(s);
+    float s[kMaxBatch];
+#pragma unroll
+    for (int k = 0; k < kMaxBatch; ++k) {
+        uint32_t r = (k < b.count && lane < kClusterCtas) ? ld_peer_u32(&cta_max[k], (uint32_t)lane) : 0u;
+        r = __reduce_max_sync(0xFFFFFFFFu, r);
+        s[k] = scale_of(r << 16, fmt_max);
+        if (k < b.count && rank == 0 && t == 0) {
+            *b.amax[k] = r << 16;
+            *b.scale[k] = s[k];
+            *b.inv[k] = __frcp_rn(s[k]);
+        }
     }
+    cluster_arrive();   // this CTA is done reading its peers' shared memory
 
     // ---- the staged slice, cast
-    __syncthreads();
-    for (int64_t j = v0 + t; j < v1; j += kSmallThreads) st_stream8(q + j, cast8<FMT>(stage[j - v0], s), stream);
-    cluster_wait();   // no CTA leaves while a peer may still read its maximum
+#pragma unroll
+    for (int k = 0; k < kMaxBatch; ++k) {
+        if (k >= b.count) break;
+        const int64_t beg = b.begin(k), lo = max(v0, beg), hi = min(v1, b.end[k]);
+        uint2 *q = b.q[k] - beg;
+        for (int64_t j = lo + t; j < hi; j += kSmallThreads) st_stream8(q + j, cast8<FMT>(stage[j - v0], s[k]), stream);
+    }
+    cluster_wait();   // no CTA leaves while a peer may still read its maxima
 }
 
 std::atomic<int> g_grid[2][64];
 std::atomic<int> g_small[2][64];   // 0 = not asked yet, 1 = the cluster path runs, -1 = it does not
 
-// The small-tensor path; *launched says whether it ran.
-fp8lin_status launch_small(const uint4 *x, int64_t nvec, int f, float fmt_max, float *amax, float *scale,
-                           float *inv_scale, uint2 *q, cudaStream_t stream, int device, bool *launched) {
+// The small-batch path; *launched says whether it ran.
+fp8lin_status launch_small(const QBatch &b, int64_t nvec, int f, float fmt_max, cudaStream_t stream, int device,
+                           bool *launched) {
     auto kernel = f == 0 ? quantize_cluster_kernel<FP8LIN_E4M3> : quantize_cluster_kernel<FP8LIN_E5M2>;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -315,14 +401,12 @@ fp8lin_status launch_small(const uint4 *x, int64_t nvec, int f, float fmt_max, f
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterCtas);
     cfg.blockDim = dim3(kSmallThreads);
-    cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int ok = g_small[f][device].load(std::memory_order_acquire);
     if (ok == 0) {
         int clusters = 0;
         cfg.dynamicSmemBytes = kSmallStageBytes;
-        cfg.stream = nullptr;
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallStageBytes) != cudaSuccess)
             return FP8LIN_ERR_CUDA;
         if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
@@ -331,14 +415,12 @@ fp8lin_status launch_small(const uint4 *x, int64_t nvec, int f, float fmt_max, f
         }
         ok = clusters >= 1 ? 1 : -1;
         g_small[f][device].store(ok, std::memory_order_release);
-        cfg.stream = stream;
     }
     if (ok < 0) return FP8LIN_OK;
     const int64_t per = (nvec + kClusterCtas - 1) / kClusterCtas;
     cfg.dynamicSmemBytes = (size_t)per * 16;
-    if (cudaLaunchKernelEx(&cfg, kernel, x, nvec, per, fmt_max, reinterpret_cast<unsigned int *>(amax), scale,
-                           inv_scale, q) != cudaSuccess)
-        return FP8LIN_ERR_CUDA;
+    cfg.stream = stream;
+    if (cudaLaunchKernelEx(&cfg, kernel, b, per, fmt_max) != cudaSuccess) return FP8LIN_ERR_CUDA;
     *launched = true;
     return fp8lin::check_launch();
 }
@@ -347,16 +429,34 @@ fp8lin_status launch_small(const uint4 *x, int64_t nvec, int f, float fmt_max, f
 
 namespace fp8lin {
 
-fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fmt_max, float *amax, float *scale,
-                              float *inv_scale, uint8_t *q, cudaStream_t stream, bool *launched) {
+fp8lin_status launch_quantize_batch(const QuantizeItem *items, int count, fp8lin_fmt fmt, float fmt_max,
+                                    cudaStream_t stream, bool *launched) {
     *launched = false;
-    if (!(fmt_max <= 65504.0f) || n % 8 != 0) return FP8LIN_OK;   // the two-kernel path takes it
+    if (count < 1 || count > kMaxBatch || !(fmt_max <= 65504.0f)) return FP8LIN_OK;   // the two-kernel path
+    QBatch b = {};
+    int64_t nvec = 0;
+    for (int k = 0; k < count; ++k) {
+        if (items[k].n % 8 != 0) return FP8LIN_OK;
+        nvec += items[k].n / 8;
+        b.x[k] = static_cast<const uint4 *>(items[k].x);
+        b.q[k] = reinterpret_cast<uint2 *>(items[k].q);
+        b.amax[k] = reinterpret_cast<unsigned int *>(items[k].amax);
+        b.scale[k] = items[k].scale;
+        b.inv[k] = items[k].inv_scale;
+        b.end[k] = nvec;
+    }
+    b.count = count;
+    if (nvec == 0) return FP8LIN_OK;   // nothing to read: the two-kernel path publishes the floor scales
     DeviceInfo dev;
     fp8lin_status st = current_device(&dev);
     if (st != FP8LIN_OK) return st;
     if (dev.device >= 64) return FP8LIN_OK;
-    auto kernel = fmt == FP8LIN_E4M3 ? quantize_kernel<FP8LIN_E4M3> : quantize_kernel<FP8LIN_E5M2>;
     const int f = fmt == FP8LIN_E4M3 ? 0 : 1;
+    if (nvec <= kSmallMaxVecs) {
+        st = launch_small(b, nvec, f, fmt_max, stream, dev.device, launched);
+        if (st != FP8LIN_OK || *launched) return st;
+    }
+    auto kernel = f == 0 ? quantize_kernel<FP8LIN_E4M3> : quantize_kernel<FP8LIN_E5M2>;
     int grid = g_grid[f][dev.device].load(std::memory_order_acquire);
     if (grid == 0) {
         int coop = 0, per_sm = 0;
@@ -368,22 +468,18 @@ fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fm
         grid = (coop && per_sm >= 1) ? dev.sm_count : -1;   // one CTA per SM, all resident together
         g_grid[f][dev.device].store(grid, std::memory_order_release);
     }
-    const int64_t nvec = n / 8;
-    if (nvec == 0) return FP8LIN_OK;
-    if (nvec <= kSmallMaxVecs) {
-        st = launch_small(static_cast<const uint4 *>(x), nvec, f, fmt_max, amax, scale, inv_scale,
-                          reinterpret_cast<uint2 *>(q), stream, dev.device, launched);
-        if (st != FP8LIN_OK || *launched) return st;
-    }
     if (grid < 0) return FP8LIN_OK;
     const int g = nvec < grid ? (int)nvec : grid;
-    // the three slots start at zero: the count, the flag and the maximum
-    if (scale == amax + 1 && inv_scale == amax + 2) {
-        if (cudaMemsetAsync(amax, 0, 3 * sizeof(float), stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
-    } else if (cudaMemsetAsync(amax, 0, sizeof(float), stream) != cudaSuccess ||
-               cudaMemsetAsync(scale, 0, sizeof(float), stream) != cudaSuccess ||
-               cudaMemsetAsync(inv_scale, 0, sizeof(float), stream) != cudaSuccess) {
-        return FP8LIN_ERR_CUDA;
+    // every slot starts at zero: the first tensor's count and flag, each tensor's maximum
+    for (int k = 0; k < count; ++k) {
+        const QuantizeItem &it = items[k];
+        if (it.scale == it.amax + 1 && it.inv_scale == it.amax + 2) {
+            if (cudaMemsetAsync(it.amax, 0, 3 * sizeof(float), stream) != cudaSuccess) return FP8LIN_ERR_CUDA;
+        } else if (cudaMemsetAsync(it.amax, 0, sizeof(float), stream) != cudaSuccess ||
+                   cudaMemsetAsync(it.scale, 0, sizeof(float), stream) != cudaSuccess ||
+                   cudaMemsetAsync(it.inv_scale, 0, sizeof(float), stream) != cudaSuccess) {
+            return FP8LIN_ERR_CUDA;
+        }
     }
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeCooperative;
@@ -395,10 +491,7 @@ fp8lin_status launch_quantize(const void *x, int64_t n, fp8lin_fmt fmt, float fm
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4 *>(x), nvec, fmt_max,
-                                             reinterpret_cast<unsigned int *>(amax),
-                                             reinterpret_cast<unsigned int *>(scale), scale, inv_scale,
-                                             reinterpret_cast<uint2 *>(q));
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, b, fmt_max);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         // fewer SMs than the device reports are available to this context:
         // the caller takes the two-kernel path, now and from here on

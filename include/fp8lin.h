@@ -152,6 +152,43 @@ fp8lin_status fp8lin_quantize(const void *x, int64_t rows, int64_t cols, fp8lin_
                               float *amax, float *scale, float *inv_scale, uint8_t *q, uint8_t *qT,
                               cudaStream_t stream);
 
+/* Most tensors one fp8lin_quantize_batch call takes. */
+#define FP8LIN_MAX_QUANTIZE_BATCH 4
+
+/* One tensor of fp8lin_quantize_batch: the arguments of fp8lin_quantize
+ * without the transposed copy. */
+typedef struct fp8lin_quantize_item {
+    const void *x;        /* device, bf16 [rows x cols] row-major, 16-byte aligned           */
+    int64_t rows, cols;   /* >= 0, multiples of 16, <= FP8LIN_MAX_DIM                        */
+    float *amax;          /* device, one float each, 4-byte aligned: receives max |x|,       */
+    float *scale;         /*   fmt_max / max(amax, 1e-12) and 1 / scale; no two slots of a   */
+    float *inv_scale;     /*   call (of this tensor or another) may coincide                 */
+    uint8_t *q;           /* device, u8 [rows x cols], 16-byte aligned (NULL if empty)      */
+} fp8lin_quantize_item;
+
+/*
+ * fp8lin_quantize for several tensors of one format, each with its own amax
+ * and scale (TorchTitan analysis page, section 3.3: dynamic scaling takes
+ * each tensor's own statistic every step; Lecture 9 exercises: one factor
+ * per tensor), in one launch: the casts that gate the same GEMM, such as the
+ * X and W of a forward pass, share one grid, one barrier and one clearing
+ * memset instead of one each.  Every tensor's amax, scale, inverse scale and
+ * FP8 bytes are bit for bit those of fp8lin_quantize on that tensor alone.
+ * Up to 786432 elements in all the tensors take one cluster of 8 CTAs (no
+ * memset); larger batches the whole-GPU cooperative grid.  With fmt_max
+ * above 65504, or no cooperative launch on the device, the tensors are cast
+ * one after another through fp8lin_amax and fp8lin_cast_transpose.  The same
+ * conditions as fp8lin_quantize hold: nothing beside it, a grid barrier
+ * bounded at 2 s (FP8LIN_ERR_TIMEOUT for fp8lin_device_error).
+ *
+ *   items   host array of `count` items, read during the call only.
+ *   count   1 .. FP8LIN_MAX_QUANTIZE_BATCH.
+ *   fmt, fmt_max  as for fp8lin_cast_transpose, shared by every item.
+ * Every item is checked before anything is launched.
+ */
+fp8lin_status fp8lin_quantize_batch(const fp8lin_quantize_item *items, int count, fp8lin_fmt fmt,
+                                    float fmt_max, cudaStream_t stream);
+
 /*
  * Static scaling: cast with a scale the caller fixes (TorchTitan analysis
  * page, section 3.3: torchao offers dynamic, delayed and static per-tensor

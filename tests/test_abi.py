@@ -236,3 +236,42 @@ def test_argument_checks_of_the_one_call_dynamic_cast(lib):
     assert fq(a16, 32, 32, 0, 448.0, a16, a16, a16, a4, None, None) == 2     # misaligned copy
     assert fq(a16, 32, 24, 0, 448.0, a16, a16, a16, a16, None, None) == 3    # ragged shape
     assert fq(a16, 1 << 31, 32, 0, 448.0, a16, a16, a16, a16, None, None) == 3
+
+
+class QItem(ctypes.Structure):
+    _fields_ = [("x", V), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("amax", V), ("scale", V),
+                ("inv_scale", V), ("q", V)]
+
+
+def test_argument_checks_of_the_batched_dynamic_cast(lib):
+    """fp8lin_quantize_batch checks every item, and that no two slots of a
+    call coincide, before launching anything."""
+    fb = lib.fp8lin_quantize_batch
+    fb.restype = ctypes.c_int
+    fb.argtypes = [V, ctypes.c_int, ctypes.c_int, F, V]
+    a16 = 4096
+
+    def items(*specs):
+        arr = (QItem * len(specs))()
+        for k, sp in enumerate(specs):
+            arr[k] = QItem(*sp)
+        return arr
+
+    def ok_item(base):  # x, 32 x 32, three slots, q
+        return (a16, 32, 32, base, base + 4, base + 8, a16)
+
+    two = items(ok_item(8192), ok_item(8448))
+    assert fb(None, 1, 0, 448.0, None) == 1                        # no items
+    assert fb(two, 0, 0, 448.0, None) == 1                         # empty batch
+    five = items(*[ok_item(8192 + 256 * k) for k in range(5)])
+    assert fb(five, 5, 0, 448.0, None) == 1                        # beyond the limit
+    assert fb(two, 2, 2, 448.0, None) == 1                         # format
+    assert fb(two, 2, 0, 0.0, None) == 1                           # fmt_max
+    assert fb(items(ok_item(8192), (a16, 32, 32, 0, 8708, 8712, a16)), 2, 0, 448.0, None) == 1  # no amax slot
+    assert fb(items(ok_item(8192), (a16, 32, 32, 8705, 8708, 8712, a16)), 2, 0, 448.0, None) == 2  # misaligned slot
+    assert fb(items(ok_item(8192), (a16 + 4, 32, 32, 8704, 8708, 8712, a16)), 2, 0, 448.0, None) == 2  # input
+    assert fb(items(ok_item(8192), (a16, 32, 24, 8704, 8708, 8712, a16)), 2, 0, 448.0, None) == 3  # ragged
+    assert fb(items(ok_item(8192), (a16, 32, 32, 8704, 8708, 8712, 0)), 2, 0, 448.0, None) == 1   # no copy
+    assert fb(items(ok_item(8192), ok_item(8192)), 2, 0, 448.0, None) == 1   # slots shared by two tensors
+    assert fb(items(ok_item(8192), (a16, 32, 32, 8704, 8704, 8712, a16)), 2, 0, 448.0, None) == 1  # within one
+    assert fb(items(ok_item(8192), (a16, 32, 32, 8704, 8708, 8200, a16)), 2, 0, 448.0, None) == 1  # across

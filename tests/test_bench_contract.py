@@ -51,9 +51,9 @@ def test_our_arm_json_line(fp8lin):
     r = d["roofline"]
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and 0 < r["frac"] < 2
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
-    # the FFN step: 9 GEMMs, 3 one-launch casts (X, W1 before w1's forward;
-    # H before w2's) and 5 amax + cast pairs under the GEMMs
-    assert d["gpu_launches"] == (9 + 3 + 2 * 5) * 3
+    # the FFN step: 9 GEMMs, 2 one-launch casts (X and W1 together before
+    # w1's forward, H before w2's) and 5 amax + cast pairs under the GEMMs
+    assert d["gpu_launches"] == (9 + 2 + 2 * 5) * 3
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]

@@ -383,6 +383,111 @@ def test_one_call_quantize_small_zero_and_alternating_sizes(fp8lin):
     assert fp8lin.fp8lin_device_error() == 0
 
 
+# batches on both one-launch paths: up to 786432 elements in all one cluster
+# of eight CTAs, beyond that the whole-GPU grid; empty members inside
+BATCHES = [
+    [(16, 16)],
+    [(256, 512), (1024, 512)],          # the 1024 x 512 linear's X and W: one cluster
+    [(256, 1024), (32, 16), (16, 48)],  # slices cut across three tensors
+    [(768, 1024), (16, 16)],            # just past the cluster's 1.5 MB: the grid
+    [(1040, 384), (2048, 4096), (0, 64), (16, 48)],
+    [(8192, 4096), (14336, 4096)],      # the 8B FFN's X and W1
+]
+
+
+@pytest.mark.parametrize("shapes", BATCHES, ids=lambda b: "+".join(f"{r}x{c}" for r, c in b))
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_batched_quantize_matches_each_tensor_alone(fp8lin, shapes, fmt):
+    """fp8lin_quantize_batch: every tensor's amax, scale, inverse scale and
+    FP8 bytes bit-exact against the oracle and against fp8lin_quantize on
+    that tensor alone, with every slot holding garbage beforehand."""
+    xs = [wl.generate(sh, "laplace" if fmt == E5M2 else "normal", 1e-3 if fmt == E5M2 else 1.0,
+                      seed=31 * k + sh[0] + sh[1], tensor_id=k, outlier_frac=1e-3) if sh[0] * sh[1] else
+          np.zeros(sh, dtype=np.uint16) for k, sh in enumerate(shapes)]
+    slots = [torch.tensor([float("nan"), -3.0, 7.5], device="cuda") for _ in shapes]
+    qs = [Guarded(sh, torch.uint8) for sh in shapes]
+    fp8lin.fp8lin_quantize_batch([(to_dev_bf16(x), sl[0:1], sl[1:2], sl[2:3], q.t) for x, sl, q in zip(xs, slots, qs)],
+                                 fmt)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    for x, sl, q in zip(xs, slots, qs):
+        ref = oracle.quantize(x, fmt)
+        alone = torch.zeros(3, device="cuda")
+        q1 = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+        fp8lin.fp8lin_quantize(to_dev_bf16(x), fmt, alone[0:1], alone[1:2], alone[2:3], q1, None)
+        torch.cuda.synchronize()
+        assert scalar_bits(sl[0:1]) == f32_bits(ref["amax"]) == scalar_bits(alone[0:1])
+        assert scalar_bits(sl[1:2]) == f32_bits(ref["scale"]) == scalar_bits(alone[1:2])
+        assert scalar_bits(sl[2:3]) == f32_bits(ref["inv_scale"]) == scalar_bits(alone[2:3])
+        assert np.array_equal(q.t.cpu().numpy(), ref["q"]) and torch.equal(q.t, q1) and q.intact()
+
+
+@pytest.mark.parametrize("shapes", [[(8192, 4096)], [(2048, 4096), (8192, 4096)], [(256, 512), (1024, 512)]],
+                         ids=["grid", "grid-batch", "cluster-batch"])
+def test_quantize_max_in_either_half_of_a_packed_pair(fp8lin, shapes):
+    """Each CTA folds the magnitudes of element pairs (an even and an odd
+    element share one 32-bit word): the largest |x| sits in the first
+    element of the tensor, an even one, in the part of a slice read before
+    the staged tail, while larger values than the rest sit in odd elements
+    of every slice's tail.  A fold that compared whole words instead of
+    each half would report the odd elements' 0.5."""
+    xs = []
+    for rows, cols in shapes:
+        x = np.zeros((rows, cols), dtype=np.uint16)
+        flat = x.reshape(-1)
+        flat[1::16] = 0x3F00            # 0.5 in odd elements everywhere, tails included
+        flat[0] = 0x4080                # 4.0: the first (even) element
+        flat[-7] = 0xBF80               # -1.0 near the end, odd element
+        xs.append(x)
+    slots = [torch.zeros(3, device="cuda") for _ in xs]
+    qs = [torch.empty(x.shape, dtype=torch.uint8, device="cuda") for x in xs]
+    fp8lin.fp8lin_quantize_batch([(to_dev_bf16(x), sl[0:1], sl[1:2], sl[2:3], q) for x, sl, q in zip(xs, slots, qs)],
+                                 E4M3)
+    torch.cuda.synchronize()
+    for x, sl, q in zip(xs, slots, qs):
+        ref = oracle.quantize(x, E4M3)
+        assert sl[0].item() == 4.0 and scalar_bits(sl[0:1]) == f32_bits(ref["amax"])
+        assert np.array_equal(q.cpu().numpy(), ref["q"])
+
+
+def test_batched_quantize_nan_empty_and_fallback(fp8lin):
+    """A NaN in one tensor of a batch leaves the others' scales alone; a
+    batch of empty tensors publishes the floor scales; fmt_max above 65504
+    casts each tensor through amax + cast, with the same results as the
+    oracle."""
+    x_nan = wl.generate((256, 256), "normal", 1.0, seed=5, tensor_id=0)
+    x_nan[17, 33] = 0x7FC1
+    x_ok = wl.generate((512, 256), "normal", 0.02, seed=6, tensor_id=1)
+    for shapes_x in ([x_nan, x_ok], [x_nan, wl.generate((2048, 1024), "normal", 0.02, seed=7, tensor_id=2)]):
+        slots = [torch.zeros(3, device="cuda") for _ in shapes_x]
+        qs = [torch.empty(x.shape, dtype=torch.uint8, device="cuda") for x in shapes_x]
+        fp8lin.fp8lin_quantize_batch([(to_dev_bf16(x), sl[0:1], sl[1:2], sl[2:3], q)
+                                      for x, sl, q in zip(shapes_x, slots, qs)], E4M3)
+        torch.cuda.synchronize()
+        for x, sl, q in zip(shapes_x, slots, qs):
+            ref = oracle.quantize(x, E4M3)
+            assert scalar_bits(sl[0:1]) == f32_bits(ref["amax"])
+            assert scalar_bits(sl[1:2]) == f32_bits(ref["scale"])
+            assert np.array_equal(q.cpu().numpy(), ref["q"])
+    empties = [torch.full((3,), 5.0, device="cuda") for _ in range(2)]
+    e = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    fp8lin.fp8lin_quantize_batch([(e, sl[0:1], sl[1:2], sl[2:3], torch.empty((0, 64), dtype=torch.uint8,
+                                                                             device="cuda")) for sl in empties], E4M3)
+    torch.cuda.synchronize()
+    for sl in empties:
+        assert sl[0].item() == 0.0 and scalar_bits(sl[1:2]) == f32_bits(oracle.scale(np.float32(0.0))[0])
+    xs = [wl.generate((1040, 2048), "laplace", 1e-3, seed=77 + k, tensor_id=k) for k in range(2)]
+    slots = [torch.zeros(3, device="cuda") for _ in xs]
+    qs = [torch.empty(x.shape, dtype=torch.uint8, device="cuda") for x in xs]
+    fp8lin.fp8lin_quantize_batch([(to_dev_bf16(x), sl[0:1], sl[1:2], sl[2:3], q) for x, sl, q in zip(xs, slots, qs)],
+                                 E5M2, 1.0e5)
+    torch.cuda.synchronize()
+    assert fp8lin.fp8lin_device_error() == 0
+    for x, sl, q in zip(xs, slots, qs):
+        ref = oracle.quantize(x, E5M2, 1.0e5)
+        assert scalar_bits(sl[1:2]) == f32_bits(ref["scale"]) and np.array_equal(q.cpu().numpy(), ref["q"])
+
+
 def test_one_call_quantize_repeated_and_empty(fp8lin):
     """Back-to-back calls reuse the same slots (each call clears them before
     its grid counts itself in); an empty matrix publishes the floor scale."""
