@@ -101,3 +101,50 @@ def test_traffic_record_keys_on_the_per_tensor_kernel(tmp_path):
     edited_kernel = tmp_path / "kernel.cu"
     edited_kernel.write_text(src[:kern] + "/* edit */ " + src[kern:])
     assert bench.gemm_kernel_sha256(str(edited_kernel)) != base
+
+
+class _T8:
+    """A cast target's host-side attributes (no device memory)."""
+
+    def __init__(self, fmt, qT=None):
+        self.fmt, self.fmt_max, self.qT = fmt, 448.0, qT
+
+
+class _Fl:
+    MAX_QUANTIZE_BATCH = 4
+
+
+def _step(name, overlap, scaling, transpose=False):
+    g = bench.StepGraph.__new__(bench.StepGraph)
+    g.spec, g.overlap, g.scaling, g.fl = bench.SPECS[name], overlap, scaling, _Fl()
+    g.t8 = {k: _T8(v[2], object() if transpose else None) for k, v in bench.cast_inputs(g.spec).items()}
+    g._plan()
+    return g
+
+
+def test_gating_casts_share_launches_and_the_launch_count():
+    """The casts issued right before a GEMM: with dynamic scaling and one FP8
+    copy per tensor they share one fp8lin_quantize_batch launch; the bench's
+    gpu_launches claim counts one kernel for that launch, two (amax + cast)
+    for every dynamic or row-wise cast beside the GEMMs, one for any other
+    recipe's cast, and one per GEMM."""
+    g = _step("ffn8b", True, "dynamic")
+    assert g._gate(0) == (["w:w1", "xf"], []) and g._gate(2) == (["h"], [])
+    assert not any(g._gate(i)[0] or g._gate(i)[1] for i in (1, 3, 4, 5, 6, 7, 8))
+    assert g._kernels_per_step() == 9 + 2 + 2 * 5
+    # one stream: every cast gates its first GEMM; same-format casts share a launch
+    g = _step("ffn8b", False, "dynamic")
+    assert g._gate(2) == (["h", "w:w2"], [])
+    assert g._kernels_per_step() == 9 + 6
+    # both FP8 copies asked for: the gating casts go amax + cast, one tensor at a time
+    g = _step("ffn8b", True, "dynamic", transpose=True)
+    assert g._gate(0) == ([], ["w:w1", "xf"])
+    assert g._kernels_per_step() == 9 + 2 * 3 + 2 * 5
+    for scaling, per_cast in (("rowwise", 2), ("delayed", 1), ("block", 1), ("mx", 1)):
+        g = _step("ffn8b", True, scaling)
+        assert g._gate(0) == ([], ["xf"])                 # W1 runs beside X on the side stream
+        assert g._kernels_per_step() == 9 + per_cast * 8
+    g = _step("tiny", True, "dynamic")
+    assert g._kernels_per_step() == 3 + 2              # X and W in one launch, then dY
+    g = _step("block8b", True, "dynamic")
+    assert g._kernels_per_step() == 15 + 4 + 2 * 9     # 15 GEMMs, four gates, nine casts beside the GEMMs
